@@ -1,0 +1,173 @@
+/*
+ * unified_attention.h -- C ABI of the GB300 (sm_103a) unified paged varlen
+ * attention library (libua_gb300.so).
+ *
+ * The operation.  One call computes attention for a flattened batch that
+ * mixes prefill, chunked-prefill and decode sequences.  This is the unified
+ * kernel's statement of the problem: it "works like flash_attn_varlen_func"
+ * for an arbitrary number of new query tokens per sequence, packs the query
+ * heads that share a KV head together along the query dimension, and reads
+ * the key cache in the FlashAttention layout ("[Kernel] Unified Triton kernel
+ * that doesn't distinguish between prefill + decode", vLLM PR #16828, PR
+ * description, first and third bullets).  The batch is described by the
+ * usual varlen metadata (cu_seqlens_q, seqused_k, block_table), unchanged
+ * from what the serving engine already keeps ("[Kernel] [V1] Improved
+ * performance for V1 Triton (ROCm) backend", vLLM PR #14152, section "How is
+ * this performance improvement achieved?").
+ *
+ * For sequence s with Lq = cu_seqlens_q[s+1] - cu_seqlens_q[s] new tokens
+ * and Lk = seqused_k[s] context tokens (the new ones included, their K/V
+ * already written to the cache), query head h of new token i (i < Lq, flat
+ * row t = cu_seqlens_q[s] + i) attends to keys j < limit, where
+ *     limit = causal ? Lk - Lq + i + 1 : Lk
+ * (bottom-right alignment: the new tokens are the last Lq of the context),
+ * using KV head h / (Hq / Hkv).  Key j lives in physical page
+ * block_table[s][j / block_size], slot j % block_size:
+ *     out[t][h] = softmax_j(scale * <q[t][h], k_j>) . v_j
+ *
+ * Layouts (all row-major, contiguous, bf16 = IEEE bfloat16):
+ *   q        bf16  [total_q, num_q_heads, head_size]            device
+ *   k_cache  bf16  [num_blocks, block_size, num_kv_heads, head_size]  device
+ *   v_cache  bf16  same as k_cache                               device
+ *   out      bf16  [total_q, num_q_heads, head_size]             device
+ *   cu_seqlens_q int32 [num_seqs + 1], cu[0] = 0, non-decreasing  device
+ *   seqused_k    int32 [num_seqs]                                 device
+ *   block_table  int32 [num_seqs, block_table_stride]             device
+ *   *_host       host copies of cu_seqlens_q / seqused_k, used to plan the
+ *                launch without a device-to-host read; they must hold the
+ *                same values as the device arrays.
+ *
+ * Supported set: head_size 64 or 128, block_size 16, num_q_heads a multiple
+ * of num_kv_heads.  Anything else returns UA_ERR_UNSUPPORTED before any
+ * launch.
+ *
+ * Ownership: the caller owns every buffer.  The library never allocates
+ * device memory on a call; split-KV partials and the launch plan live in the
+ * caller's workspace (size from ua_workspace_size).  Calls are asynchronous on
+ * the given stream.  Two calls that share a workspace must be ordered (same
+ * stream, or synchronised by the caller).
+ *
+ * Errors are returned, never aborted on.  Invalid metadata is rejected on
+ * the host before any launch.  Device-side problems (a block id outside
+ * [0, num_blocks), a pipeline wait that ran out of time) never fault: the
+ * kernels skip the bad access, record a code in a device status word, and
+ * finish; ua_device_status() reads and clears it.
+ */
+#ifndef UNIFIED_ATTENTION_H
+#define UNIFIED_ATTENTION_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ua_status {
+    UA_OK = 0,
+    UA_ERR_INVALID_ARG = 1,   /* null pointer, bad metadata, misaligned buffer */
+    UA_ERR_UNSUPPORTED = 2,   /* head_size / block_size / head ratio outside the supported set */
+    UA_ERR_WORKSPACE = 3,     /* workspace missing, misaligned or too small */
+    UA_ERR_CUDA = 4,          /* a CUDA runtime call failed (launch, copy, device query) */
+    UA_ERR_DEVICE_CHECK = 5   /* ua_device_status found a code recorded by a kernel */
+} ua_status;
+
+/* Device status word bits (ua_device_status). */
+#define UA_DEVICE_BAD_BLOCK_ID 0x1   /* a block_table entry outside [0, num_blocks) was skipped */
+#define UA_DEVICE_WAIT_TIMEOUT 0x2   /* a pipeline wait gave up; the output is incomplete */
+
+/*
+ * unified_attention -- attention over a paged varlen batch (definition above,
+ * from the unified kernel's PR description).
+ *
+ *   softmax_scale  multiplies every score; finite.
+ *   causal         non-zero: bottom-right causal mask; zero: every one of the
+ *                  Lk keys is visible (the non-causal mode requested in the
+ *                  review thread of the same page, for cascade attention).
+ *   num_blocks     pages in k_cache / v_cache; num_blocks * block_size < 2^31.
+ *   workspace      device scratch of at least ua_workspace_size() bytes,
+ *                  256-byte aligned; may be NULL only when that size is 0.
+ *   stream         a cudaStream_t (NULL = legacy default stream).
+ *
+ * Host-side checks (UA_ERR_INVALID_ARG): cu_seqlens_q_host[0] == 0 and
+ * non-decreasing; seqused_k_host[s] >= 0; Lk > 0 whenever Lq > 0; Lk >= Lq
+ * when causal; ceil(Lk / block_size) <= block_table_stride; q, k_cache,
+ * v_cache, out 16-byte aligned.  Sequences with Lq = 0 are allowed and write
+ * nothing.  Block-table entries at or beyond ceil(Lk / block_size) are never
+ * read; entries may alias (one physical page in several sequences).
+ * Every out row of every sequence is fully overwritten.
+ */
+ua_status unified_attention(const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *cu_seqlens_q, const int32_t *seqused_k,
+                            const int32_t *block_table, float softmax_scale, int32_t causal,
+                            void *out, const int32_t *cu_seqlens_q_host,
+                            const int32_t *seqused_k_host, int32_t num_seqs,
+                            int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                            int32_t block_size, int32_t num_blocks, int32_t block_table_stride,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * ua_workspace_size -- bytes of device workspace unified_attention needs for
+ * this batch on the current CUDA device: the launch plan (per-(sequence,
+ * kv-head, query-tile) work items and their page ranges) plus the split-KV
+ * partial outputs.  Host-only apart from a cached device-property query.
+ * Same metadata checks as unified_attention; *bytes is written on UA_OK.
+ */
+ua_status ua_workspace_size(const int32_t *cu_seqlens_q_host, const int32_t *seqused_k_host,
+                            int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                            int32_t head_size, int32_t block_size, int32_t block_table_stride,
+                            int32_t causal, size_t *bytes);
+
+/* ua_status_string -- static, human-readable name of a status code. */
+const char *ua_status_string(ua_status status);
+
+/*
+ * ua_device_status -- synchronises the current device, then reads and clears
+ * the device status word the kernels write (UA_DEVICE_* bits).  *code gets
+ * the bits; returns UA_ERR_DEVICE_CHECK if any bit was set, UA_OK if none.
+ */
+ua_status ua_device_status(int32_t *code);
+
+/*
+ * ua_plan_inspect -- host-only view of the work partition unified_attention
+ * would launch for this batch on a GPU with num_sms multiprocessors (no CUDA
+ * call is made).  This is the partition pass of the hot path: the pages
+ * motivate one plan per batch because a single fixed grid fits prefill and
+ * decode badly (vLLM PR #14152, section "How is this performance improvement
+ * achieved?").
+ *
+ * counts[0..7] receives: decode CTAs, decode pieces, split units (combined),
+ * partial slots, prefill tiles, prefill CTAs, decode pages in total,
+ * workspace bytes (saturated to INT32_MAX).
+ * If items != NULL, up to items_cap rows of 8 int32 are written:
+ *   decode pieces   {0, cta, seq, kv_head, row0, nrows, page_begin, page_end}
+ *                   followed by one row {1, slot or -1, unit, 0, 0, 0, 0, 0}
+ *   prefill tiles   {2, order, seq, kv_head, row0, nrows, kv_tiles, 0}
+ *   split units     {3, seq, kv_head, row0, nrows, slot_begin, nslots, 0}
+ * Rows are packed (token, head-in-group) pairs: row r is token r / G, query
+ * head kv_head * G + r % G, with G = num_q_heads / num_kv_heads.
+ * *n_items gets the number of rows the full listing needs.
+ */
+ua_status ua_plan_inspect(const int32_t *cu_seqlens_q_host, const int32_t *seqused_k_host,
+                          int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t head_size, int32_t block_size, int32_t block_table_stride,
+                          int32_t causal, int32_t num_sms, int32_t *counts, int32_t *items,
+                          int64_t items_cap, int64_t *n_items);
+
+/*
+ * Per-kernel timing of the last call, for roofline figures.  When enabled,
+ * unified_attention records CUDA events around each kernel it launches on the
+ * caller's stream (events are created once per device and reused).
+ * ua_profile_last synchronises on the last call's events and fills:
+ *   ms[0..3]       decode, prefill, combine kernel time and the plan copy
+ *                  (-1 when that step did not run);
+ *   launches[0..3] kernel launches of each kind (the copy counts as 0).
+ */
+ua_status ua_profile_enable(int32_t enable);
+ua_status ua_profile_last(float *ms, int32_t *launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UNIFIED_ATTENTION_H */

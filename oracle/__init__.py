@@ -1,0 +1,140 @@
+"""fp64 CPU oracle for unified paged varlen attention.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` are the only callers.  The product path never
+imports this package.
+
+The arithmetic lives in ``ua_oracle.c`` (plain C, fp64, see its header for the
+definition it writes out); this module compiles it with gcc on first use and
+wraps it with ctypes.
+
+Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
+against a library routine (torch fp64 scaled_dot_product_attention on dense
+per-sequence K/V with an explicit bottom-right mask), closed forms (a single
+visible key, identical keys, zero scale, a hand-derived two-key example under
+``tests/golden/``), exact mask-boundary counts, and invariances (physical
+placement, aliasing, decode vs prefill, chunking, split-KV merge).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ua_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libua_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ERRORS = {1: "bad shape", 2: "bad sequence lengths", 3: "block id out of range", 4: "out of memory"}
+
+
+class OracleError(ValueError):
+    pass
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP, fp64, no fast-math)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_BUILD_DIR)
+    os.close(fd)
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-fno-fast-math",
+           "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i = ctypes.c_int
+            lib.ua_oracle_attention.argtypes = [P, P, P, P, P, P, i, i, i, i, i, i, i,
+                                                ctypes.c_double, i, i, i, P, P, i]
+            lib.ua_oracle_attention.restype = i
+            lib.ua_oracle_merge.argtypes = [i, P, P, ctypes.c_int64, i, P, P]
+            lib.ua_oracle_merge.restype = i
+            lib.ua_oracle_max_threads.restype = i
+            _lib = lib
+    return _lib
+
+
+def max_threads() -> int:
+    return int(_load().ua_oracle_max_threads())
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def attention(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table, softmax_scale,
+              causal, num_kv_heads=None, key_window=None, nthreads=0):
+    """fp64 attention over a paged varlen batch.
+
+    q: uint16 (bf16 bits) [total_q, Hq, D]; k_cache / v_cache: uint16
+    [num_blocks, block_size, Hkv, D]; cu_seqlens_q int32 [N+1]; seqused_k int32
+    [N]; block_table int32 [N, stride].  Returns (out fp64 [total_q, Hq, D],
+    lse fp64 [total_q, Hq]) with lse the natural-log normaliser.
+    """
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k_cache = np.ascontiguousarray(k_cache, dtype=np.uint16)
+    v_cache = np.ascontiguousarray(v_cache, dtype=np.uint16)
+    cu = np.ascontiguousarray(cu_seqlens_q, dtype=np.int32)
+    sk = np.ascontiguousarray(seqused_k, dtype=np.int32)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    if bt.ndim == 1:
+        bt = bt.reshape(len(sk), -1)
+    total_q, hq, d = q.shape
+    nb, bs, hk, d2 = k_cache.shape
+    if num_kv_heads is not None and num_kv_heads != hk:
+        raise OracleError("num_kv_heads disagrees with the cache shape")
+    if d2 != d or v_cache.shape != k_cache.shape:
+        raise OracleError("q / cache shapes disagree")
+    if len(cu) != len(sk) + 1 or (len(sk) and cu[-1] != total_q):
+        raise OracleError("cu_seqlens_q does not match q")
+    lo, hi = (0, 2**31 - 1) if key_window is None else key_window
+    out = np.zeros((total_q, hq, d), dtype=np.float64)
+    lse = np.full((total_q, hq), -np.inf, dtype=np.float64)
+    rc = _load().ua_oracle_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu), _ptr(sk),
+                                     _ptr(bt), len(sk), hq, hk, d, bs, nb, bt.shape[1],
+                                     float(softmax_scale), int(bool(causal)), int(lo), int(hi),
+                                     _ptr(out), _ptr(lse), int(nthreads))
+    if rc != 0:
+        raise OracleError(ERRORS.get(rc, f"oracle error {rc}"))
+    return out, lse
+
+
+def attention_batch(batch, key_window=None, nthreads=0):
+    """``attention`` on a ``workloads.Batch``."""
+    s = batch.spec
+    return attention(batch.q, batch.k_cache, batch.v_cache, batch.cu_seqlens_q, batch.seqused_k,
+                     batch.block_table, s.softmax_scale, s.causal, key_window=key_window,
+                     nthreads=nthreads)
+
+
+def merge(outs, lses):
+    """Log-sum-exp merge of partials over disjoint key sets (same shapes as ``attention``)."""
+    outs = [np.ascontiguousarray(o, dtype=np.float64) for o in outs]
+    lses = [np.ascontiguousarray(l, dtype=np.float64) for l in lses]
+    shape = outs[0].shape
+    d = shape[-1]
+    rows = int(np.prod(shape[:-1]))
+    out = np.zeros(shape, dtype=np.float64)
+    lse = np.zeros(shape[:-1], dtype=np.float64)
+    op = (ctypes.c_void_p * len(outs))(*[o.ctypes.data for o in outs])
+    lp = (ctypes.c_void_p * len(lses))(*[l.ctypes.data for l in lses])
+    _load().ua_oracle_merge(len(outs), ctypes.cast(op, ctypes.c_void_p),
+                            ctypes.cast(lp, ctypes.c_void_p), rows, d, _ptr(out), _ptr(lse))
+    return out, lse
