@@ -1,0 +1,489 @@
+"""Benchmark of unified paged varlen attention on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one unified_attention call over one synthetic batch (the whole hot
+path: the partition pass, the plan copy, the decode / split-KV kernel, the
+prefill kernel when the batch has prefill rows, and the combine kernel).  The
+default workload is the Llama-3.1-8B-shaped pure-decode batch (64 sequences,
+one new token each, contexts uniform in [2048, 4096], Hq 32, Hkv 8, head size
+128, bf16, 16-token pages).  Inputs are resident in HBM when timing starts;
+the KV working set (~0.8 GB) is far larger than L2, and L2 is also flushed
+(a 256 MB write) between timed steps, outside the timed interval.
+
+The JSON line carries the metric (query tokens/s), the roofline of the
+dominant kernel (CUDA-event time per launch against the measured HBM
+bandwidth), the fp64 oracle timed on the host cores (cpu_baseline), an
+end-to-end number through the public API with host buffers, clocks sampled
+during the timed region, and the number of kernels launched.
+
+--impl reference times the fp64 CPU oracle (the reference arm of this build)
+on the same workload, a bounded sample of sequences per step.
+
+Multi-GPU: one process per GPU under torchrun; each rank runs its own replica
+of the workload (no data-path collective, weak scaling); the time is the max
+over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from paged_varlen_attention_gb300 import workloads as W  # noqa: E402
+
+METRIC = "attention tokens/s on 1 GB300; HBM GB/s (decode) / TFLOP/s (prefill) vs roofline"
+WORKLOADS = {
+    "llama3_8b_decode_64x2k-4k": 2,
+    "tiny_mixed_d64": 1,
+    "mistral_24b_prefill_16x1000": 3,
+    "llama3_8b_mixed_256dec_4x512chunk": 4,
+    "llama3_70b_long_mixed_32x8k-32k_2x2048chunk": 5,
+}
+DEFAULT_WORKLOAD = "llama3_8b_decode_64x2k-4k"
+KERNEL_SOURCES = {
+    "decode": "paged_varlen_attention_gb300/csrc/ua_decode.cu",
+    "prefill": "paged_varlen_attention_gb300/csrc/ua_prefill.cu",
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def algorithmic_work(spec) -> dict:
+    """Minimum bytes and flops of one call (roofline numerators).
+
+    bytes: each visible context token's K and V rows read once per KV head
+    (GQA packing shares them across the group), Q read and O written once,
+    the used block-table entries and the metadata.  flops: 4 * Hq * D per
+    visible (query, key) pair; causally hidden pairs are not counted.
+    """
+    ql = spec.q_lens.astype(np.int64)
+    kl = spec.k_lens.astype(np.int64)
+    hq, hk, d = spec.num_q_heads, spec.num_kv_heads, spec.head_size
+    pairs = int((ql * (kl - ql) + ql * (ql + 1) // 2).sum()) if spec.causal else int((ql * kl).sum())
+    kv_bytes = int(kl.sum()) * 2 * hk * d * 2
+    qo_bytes = 2 * spec.total_q * hq * d * 2
+    meta = 4 * (2 * spec.num_seqs + 1) + 4 * int(spec.pages_per_seq().sum())
+    decode = ql * hq // hk <= 16
+    dec_kv = int(kl[decode].sum()) * 2 * hk * d * 2
+    dec_qo = 2 * int(ql[decode].sum()) * hq * d * 2
+    dec_meta = 4 * int(spec.pages_per_seq()[decode].sum())
+    return {"bytes": kv_bytes + qo_bytes + meta, "kv_bytes": kv_bytes, "flops": 4 * hq * d * pairs,
+            "decode_bytes": dec_kv + dec_qo + dec_meta, "q_tokens": spec.total_q,
+            "kv_tokens": int(kl.sum()), "pairs": pairs}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def source_hash(rel):
+    with open(os.path.join(ROOT, rel), "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        entries = json.load(fh)
+    e = entries.get(f"{kernel}:{workload}")
+    if not e or e.get("source_sha256_16") != source_hash(KERNEL_SOURCES[kernel]):
+        return None
+    return float(e["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        self.out = tempfile.TemporaryFile(mode="w+")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.out.seek(0)
+        rows = [[c.strip() for c in ln.split(",")] for ln in self.out.read().splitlines() if ln.strip()]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- distributed
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+        return rank, world, local, dist
+    return rank, world, local, None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value, device=None):
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- our arm
+def device_batch(batch, torch, device):
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+
+    return dict(q=bf16(batch.q), k_cache=bf16(batch.k_cache), v_cache=bf16(batch.v_cache),
+                cu_seqlens_q=i32(batch.cu_seqlens_q), seqused_k=i32(batch.seqused_k),
+                block_table=i32(batch.block_table))
+
+
+def cpu_baseline(spec_idx, budget_s=12.0):
+    """The fp64 oracle on the host cores over a bounded sample of the workload."""
+    import oracle
+
+    b = W.config_batch(spec_idx, poison=False)
+    s = b.spec
+    n = s.num_seqs
+    # sample: whole sequences in batch order until the token budget of ~the first call
+    t0 = time.perf_counter()
+    oracle.attention_batch(b)
+    one = time.perf_counter() - t0
+    reps = max(1, min(10, int(budget_s / max(one, 1e-3))))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.attention_batch(b)
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": s.total_q / dt, "unit": "tokens/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"the whole workload ({n} sequences, {s.total_q} query tokens), "
+                      f"{reps} repetitions after one untimed call, fp64 C oracle with OpenMP",
+            "seconds_per_call": dt}
+
+
+def run_ours(args, rank, world, local, dist):
+    import torch
+
+    import paged_varlen_attention_gb300 as ua
+    from paged_varlen_attention_gb300 import build_lib
+
+    build_lib.build()
+    ua.load_library()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    idx = WORKLOADS[args.workload]
+    batch = W.config_batch(idx, poison=False)
+    spec = batch.spec
+    dev = device_batch(batch, torch, device)
+    out = torch.empty_like(dev["q"])
+    cu_h, sk_h = batch.cu_seqlens_q.copy(), batch.seqused_k.copy()
+    ws_bytes = ua.workspace_size(cu_h, sk_h, spec.num_q_heads, spec.num_kv_heads,
+                                 spec.head_size, batch.block_table_stride, spec.causal)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        ua.unified_attention(dev["q"], dev["k_cache"], dev["v_cache"], dev["cu_seqlens_q"],
+                             dev["seqused_k"], dev["block_table"], spec.softmax_scale, spec.causal,
+                             out=out, cu_seqlens_q_host=cu_h, seqused_k_host=sk_h, workspace=ws,
+                             stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    ua.device_status()
+    ua.profile_enable(True)
+    kern = {"decode": [], "prefill": [], "combine": [], "plan_copy": []}
+    launches = 0
+    times = []
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id_for_smi(torch, local)) as clocks:
+        for _ in range(args.steps):
+            flush.fill_(1)                      # L2 flush, outside the timed interval
+            ev0.record(stream)
+            step()
+            ev1.record(stream)
+            ev1.synchronize()
+            times.append(ev0.elapsed_time(ev1))
+            ms, ln = ua.profile_last()
+            for key, v in zip(("decode", "prefill", "combine", "plan_copy"), ms):
+                if v >= 0:
+                    kern[key].append(v)
+            launches += sum(ln[:3])
+        torch.cuda.synchronize()
+    barrier(dist)
+    ua.profile_enable(False)
+    status = ua.device_status()
+    if status:
+        raise RuntimeError(f"device status {status:#x} after the timed steps")
+    total_ms = sum(times)
+    total_ms = max_over_ranks(dist, total_ms, device)
+    work = algorithmic_work(spec)
+    peaks = measured_peaks()
+    res = {"spec": spec, "work": work, "total_ms": total_ms, "times": times, "kern": kern,
+           "launches": launches, "clocks": clocks.summary(), "peaks": peaks}
+
+    # end to end through the public API: pinned host q + metadata in, output back out
+    if not args.no_e2e:
+        pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+        host = {k: pin(dev[k]) for k in ("q", "cu_seqlens_q", "seqused_k", "block_table")}
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        dq = {k: torch.empty_like(dev[k]) for k in host}
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = out_h.numel() * out_h.element_size()
+
+        def e2e_step():
+            for k in host:
+                dq[k].copy_(host[k], non_blocking=True)
+            ua.unified_attention(dq["q"], dev["k_cache"], dev["v_cache"], dq["cu_seqlens_q"],
+                                 dq["seqused_k"], dq["block_table"], spec.softmax_scale,
+                                 spec.causal, out=out, cu_seqlens_q_host=cu_h,
+                                 seqused_k_host=sk_h, workspace=ws, stream=stream)
+            out_h.copy_(out, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        et = []
+        for _ in range(args.steps):
+            flush.fill_(1)
+            ev0.record(stream)
+            e2e_step()
+            ev1.record(stream)
+            ev1.synchronize()
+            et.append(ev0.elapsed_time(ev1))
+        e2e_ms = max_over_ranks(dist, sum(et), device)
+        res["e2e"] = {"value": world * spec.total_q * args.steps / (e2e_ms / 1e3),
+                      "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+                      "d2h_bytes_per_step": int(d2h),
+                      "ms_per_step": e2e_ms / args.steps,
+                      "note": "pinned host q + varlen metadata copied in and the output copied "
+                              "back every step; the paged KV cache stays resident in HBM"}
+    return res
+
+
+def gpu_id_for_smi(torch, local):
+    """nvidia-smi --id value of the device torch calls cuda:local (UUID when available)."""
+    try:
+        u = str(torch.cuda.get_device_properties(local).uuid)
+        return u if u.startswith("GPU-") else f"GPU-{u}"
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            return vis.split(",")[local].strip()
+        return str(local)
+
+
+def run_reference(args, rank, world):
+    """The fp64 CPU oracle as the reference arm: a bounded sample of sequences per step."""
+    import oracle
+
+    if rank != 0:
+        return None
+    idx = WORKLOADS[args.workload]
+    b = W.config_batch(idx, poison=False)
+    s = b.spec
+    # per step: a rotating window of sequences sized to a few tenths of a second
+    per_step = max(1, min(s.num_seqs, 8 if idx in (1, 2) else 2))
+    if idx == 1:
+        per_step = s.num_seqs
+
+    def sub_batch(start):
+        sel = [(start + j) % s.num_seqs for j in range(per_step)]
+        ql = s.q_lens[sel]
+        cu = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+        rows = np.concatenate([np.arange(b.cu_seqlens_q[j], b.cu_seqlens_q[j + 1]) for j in sel])
+        return (b.q[rows], cu, b.seqused_k[sel], b.block_table[sel], int(ql.sum()))
+
+    for w in range(args.warmup):
+        q, cu, sk, bt, _ = sub_batch(w * per_step)
+        oracle.attention(q, b.k_cache, b.v_cache, cu, sk, bt, s.softmax_scale, s.causal)
+    tokens = 0
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        q, cu, sk, bt, nt = sub_batch(k * per_step)
+        oracle.attention(q, b.k_cache, b.v_cache, cu, sk, bt, s.softmax_scale, s.causal)
+        tokens += nt
+    dt = time.perf_counter() - t0
+    value = tokens / dt
+    sample = (f"{per_step} of {s.num_seqs} sequences per step (a rotating window), "
+              f"{tokens} query tokens over {args.steps} steps, fp64 C oracle with OpenMP")
+    return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": args.workload, "num_seqs": s.num_seqs,
+                       "q_tokens": s.total_q, "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.max_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def assemble(args, res, world, cpu):
+    spec, work, peaks = res["spec"], res["work"], res["peaks"]
+    k = args.steps
+    total_s = res["total_ms"] / 1e3
+    value = world * spec.total_q * k / total_s
+    kern = res["kern"]
+    dec = statistics.mean(kern["decode"]) if kern["decode"] else None
+    pre = statistics.mean(kern["prefill"]) if kern["prefill"] else None
+    # dominant kernel: the one with the larger share of the step
+    if pre is not None and (dec is None or pre > dec):
+        achieved = work["flops"] / (pre / 1e3) / 1e12
+        roof = {"kernel": "ua_prefill_kernel", "bound": "tensor", "achieved": achieved,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"],
+                "traffic": ncu_traffic("prefill", args.workload),
+                "per_launch": f"{work['flops']} algorithmic flops (4 Hq D per visible pair)",
+                "launch_ms": pre}
+    else:
+        achieved = work["decode_bytes"] / (dec / 1e3) / 1e9
+        roof = {"kernel": "ua_decode_kernel", "bound": "hbm", "achieved": achieved,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "traffic": ncu_traffic("decode", args.workload),
+                "per_launch": f"{work['decode_bytes']} algorithmic bytes (K+V rows once per kv "
+                              "head, Q, O, block-table entries)",
+                "launch_ms": dec}
+    roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json)" if peaks["source"] == "measured" \
+        else "fallback"
+    call_gbs = work["bytes"] / (total_s / k) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": k,
+        "warmup": args.warmup, "ms_per_step": res["total_ms"] / k, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, shuffled pages)",
+        "config": {"workload": args.workload, "num_seqs": spec.num_seqs,
+                   "q_tokens": spec.total_q, "kv_tokens": work["kv_tokens"],
+                   "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads,
+                   "head_size": spec.head_size, "block_size": spec.block_size,
+                   "causal": bool(spec.causal),
+                   "l2": "inputs larger than L2, and L2 flushed (256 MB write) between steps",
+                   "parallelism": f"{world} independent replica(s), no collective"},
+        "roofline": roof,
+        "call": {"kv_tokens_per_s": world * work["kv_tokens"] * k / total_s,
+                 "algorithmic_gbs": call_gbs, "algorithmic_tflops": work["flops"] / (total_s / k) / 1e12,
+                 "kernel_ms": {kk: (statistics.mean(v) if v else None) for kk, v in kern.items()}},
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = {kk: cpu[kk] for kk in ("value", "unit", "cores", "kind", "sample")}
+    if "e2e" in res:
+        line["e2e"] = res["e2e"]
+    return line
+
+
+def main():
+    args = parse_args()
+    rank, world, local, dist = dist_setup(args.gpus)
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    import torch
+
+    res = run_ours(args, rank, world, local, dist)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(WORKLOADS[args.workload])
+    if rank == 0:
+        line = assemble(args, res, world, cpu)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,206 @@
+"""ctypes binding of ``libua_gb300.so`` (argument marshalling only).
+
+Every step of the computation runs in the library's CUDA kernels.  This
+module checks tensor types, reads the host copies of the varlen metadata the
+planner needs, keeps a per-device workspace (PyTorch is used for device
+memory and streams only), and calls the C ABI declared in
+``include/unified_attention.h``.  There is no fallback: if the library is not
+built, every call raises ``UAError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "_build", "libua_gb300.so")
+
+STATUS = {0: "UA_OK", 1: "UA_ERR_INVALID_ARG", 2: "UA_ERR_UNSUPPORTED", 3: "UA_ERR_WORKSPACE",
+          4: "UA_ERR_CUDA", 5: "UA_ERR_DEVICE_CHECK"}
+DEVICE_BAD_BLOCK_ID = 0x1
+DEVICE_WAIT_TIMEOUT = 0x2
+
+SYMBOLS = ("unified_attention", "ua_workspace_size", "ua_status_string", "ua_device_status",
+           "ua_plan_inspect", "ua_profile_enable", "ua_profile_last")
+
+
+class UAError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)}" if what else STATUS.get(status, str(status)))
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load the CUDA library; raise if it has not been built (no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise UAError(4, f"CUDA library missing at {_LIB_PATH}; build it with "
+                             "`python -m paged_varlen_attention_gb300.build_lib`")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        lib.unified_attention.argtypes = [P, P, P, P, P, P, ctypes.c_float, I32, P, P, P,
+                                          I32, I32, I32, I32, I32, I32, I32, P, ctypes.c_size_t, P]
+        lib.unified_attention.restype = ctypes.c_int
+        lib.ua_workspace_size.argtypes = [P, P, I32, I32, I32, I32, I32, I32, I32,
+                                          ctypes.POINTER(ctypes.c_size_t)]
+        lib.ua_workspace_size.restype = ctypes.c_int
+        lib.ua_status_string.argtypes = [ctypes.c_int]
+        lib.ua_status_string.restype = ctypes.c_char_p
+        lib.ua_device_status.argtypes = [ctypes.POINTER(I32)]
+        lib.ua_device_status.restype = ctypes.c_int
+        lib.ua_plan_inspect.argtypes = [P, P, I32, I32, I32, I32, I32, I32, I32, I32, P, P, I64,
+                                        ctypes.POINTER(I64)]
+        lib.ua_plan_inspect.restype = ctypes.c_int
+        lib.ua_profile_enable.argtypes = [I32]
+        lib.ua_profile_enable.restype = ctypes.c_int
+        lib.ua_profile_last.argtypes = [P, P]
+        lib.ua_profile_last.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _host_i32(x) -> np.ndarray:
+    """Host int32 copy of metadata (numpy array, list or tensor; a CUDA tensor is read back)."""
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int32))
+
+
+def _np_ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise UAError(rc, what)
+
+
+def workspace_size(cu_seqlens_q_host, seqused_k_host, num_q_heads, num_kv_heads, head_size,
+                   block_table_stride, causal=True, block_size=16) -> int:
+    lib = load_library()
+    cu = _host_i32(cu_seqlens_q_host)
+    sk = _host_i32(seqused_k_host)
+    out = ctypes.c_size_t(0)
+    _check(lib.ua_workspace_size(_np_ptr(cu), _np_ptr(sk), len(sk), num_q_heads, num_kv_heads,
+                                 head_size, block_size, block_table_stride, int(bool(causal)),
+                                 ctypes.byref(out)), "ua_workspace_size")
+    return int(out.value)
+
+
+_workspaces = {}
+
+
+def _workspace(torch, device, nbytes):
+    """Grow-only per-device workspace (allocated through PyTorch)."""
+    key = device.index if device.index is not None else torch.cuda.current_device()
+    buf = _workspaces.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _workspaces[key] = buf
+    return buf
+
+
+def unified_attention(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table, softmax_scale,
+                      causal=True, out=None, *, cu_seqlens_q_host=None, seqused_k_host=None,
+                      workspace=None, stream=None):
+    """Attention over a paged varlen batch (see ``include/unified_attention.h``).
+
+    q: bf16 [total_q, Hq, D]; k_cache / v_cache: bf16 [num_blocks, 16, Hkv, D];
+    cu_seqlens_q int32 [N+1], seqused_k int32 [N], block_table int32 [N, stride],
+    all CUDA tensors.  Host copies of cu_seqlens_q / seqused_k may be passed to
+    avoid a device-to-host read.  Returns ``out`` (bf16 [total_q, Hq, D]).
+    """
+    import torch
+
+    lib = load_library()
+    for name, t, dt in (("q", q, torch.bfloat16), ("k_cache", k_cache, torch.bfloat16),
+                        ("v_cache", v_cache, torch.bfloat16),
+                        ("cu_seqlens_q", cu_seqlens_q, torch.int32),
+                        ("seqused_k", seqused_k, torch.int32),
+                        ("block_table", block_table, torch.int32)):
+        if not t.is_cuda or t.dtype != dt or not t.is_contiguous():
+            raise UAError(1, f"{name} must be a contiguous CUDA {dt} tensor")
+    total_q, hq, d = q.shape
+    nb, bs, hk, d2 = k_cache.shape
+    if v_cache.shape != k_cache.shape or d2 != d:
+        raise UAError(1, "q / k_cache / v_cache shapes disagree")
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous() \
+            or not out.is_cuda:
+        raise UAError(1, "out must be a contiguous CUDA bf16 tensor shaped like q")
+    cu_h = _host_i32(cu_seqlens_q if cu_seqlens_q_host is None else cu_seqlens_q_host)
+    sk_h = _host_i32(seqused_k if seqused_k_host is None else seqused_k_host)
+    num_seqs = int(sk_h.shape[0])
+    stride = int(block_table.shape[1]) if block_table.dim() == 2 else 0
+    if workspace is None:
+        need = workspace_size(cu_h, sk_h, hq, hk, d, stride, causal, bs)
+        workspace = _workspace(torch, q.device, need)
+    ws_ptr = workspace.data_ptr() if workspace.numel() else None
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    rc = lib.unified_attention(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                               cu_seqlens_q.data_ptr(), seqused_k.data_ptr(),
+                               block_table.data_ptr(), float(softmax_scale), int(bool(causal)),
+                               out.data_ptr(), _np_ptr(cu_h), _np_ptr(sk_h), num_seqs, hq, hk, d,
+                               bs, nb, stride, ws_ptr, workspace.numel(), stream)
+    _check(rc, "unified_attention")
+    return out
+
+
+def device_status() -> int:
+    """Synchronise, then read and clear the kernels' device status word."""
+    lib = load_library()
+    code = ctypes.c_int32(0)
+    rc = lib.ua_device_status(ctypes.byref(code))
+    if rc not in (0, 5):
+        _check(rc, "ua_device_status")
+    return int(code.value)
+
+
+def plan_inspect(cu_seqlens_q_host, seqused_k_host, num_q_heads, num_kv_heads, head_size,
+                 block_table_stride, causal=True, num_sms=152, block_size=16):
+    """Host-only view of the work partition (no CUDA call).  Returns (counts, items)."""
+    lib = load_library()
+    cu = _host_i32(cu_seqlens_q_host)
+    sk = _host_i32(seqused_k_host)
+    counts = np.zeros(8, dtype=np.int32)
+    n = ctypes.c_int64(0)
+    args = (_np_ptr(cu), _np_ptr(sk), len(sk), num_q_heads, num_kv_heads, head_size, block_size,
+            block_table_stride, int(bool(causal)), num_sms)
+    _check(lib.ua_plan_inspect(*args, _np_ptr(counts), None, 0, ctypes.byref(n)),
+           "ua_plan_inspect")
+    items = np.zeros((max(int(n.value), 1), 8), dtype=np.int32)
+    _check(lib.ua_plan_inspect(*args, _np_ptr(counts), _np_ptr(items), int(n.value),
+                               ctypes.byref(n)), "ua_plan_inspect")
+    keys = ("dec_ctas", "pieces", "split_units", "slots", "prefill_tiles", "prefill_ctas",
+            "dec_pages", "workspace_bytes")
+    return dict(zip(keys, (int(c) for c in counts))), items[:int(n.value)]
+
+
+def profile_enable(on: bool = True):
+    _check(load_library().ua_profile_enable(int(bool(on))), "ua_profile_enable")
+
+
+def profile_last():
+    """(ms[decode, prefill, combine, plan_copy], launches[...]) of the last call; -1 = not run."""
+    ms = np.zeros(4, dtype=np.float32)
+    ln = np.zeros(4, dtype=np.int32)
+    _check(load_library().ua_profile_last(_np_ptr(ms), _np_ptr(ln)), "ua_profile_last")
+    return ms.tolist(), ln.tolist()

@@ -1,0 +1,95 @@
+"""Build the C-ABI library ``_build/libua_gb300.so`` in-tree for sm_103a.
+
+Each translation unit compiles in parallel (nvcc for ``.cu``, g++ for the
+host-only planner), then nvcc links a shared library with the CUDA runtime
+linked statically, so the library needs no ``libcudart`` at load time and
+loads (without running anything) on machines that have no GPU.
+
+    python -m paged_varlen_attention_gb300.build_lib [--force]
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import os
+import shutil
+import subprocess
+import sys
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+BUILD = os.path.join(PKG, "_build")
+LIB = os.path.join(BUILD, "libua_gb300.so")
+
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+DEFINES = ["-DUA_PREFILL_ENABLED=0"]
+NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
+              "--expt-relaxed-constexpr"]
+CXX_FLAGS = ["-O2", "-fPIC", "-std=c++17", "-Wall"]
+
+
+def _nvcc() -> str:
+    for cand in (shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found")
+
+
+def _sources():
+    cu = sorted(f for f in os.listdir(CSRC) if f.endswith(".cu"))
+    cpp = sorted(f for f in os.listdir(CSRC) if f.endswith(".cpp"))
+    return cu, cpp
+
+
+def _deps_mtime() -> float:
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
+    files.append(os.path.abspath(__file__))
+    return max(os.path.getmtime(f) for f in files)
+
+
+def _compile(cmd, log_path):
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    with open(log_path, "w") as fh:
+        fh.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
+    if r.returncode != 0:
+        raise RuntimeError(f"compile failed: {' '.join(cmd)}\n{r.stdout}{r.stderr}")
+    return log_path
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile every CUDA / C++ source of the library; return the .so path."""
+    os.makedirs(BUILD, exist_ok=True)
+    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
+        return LIB
+    nvcc = _nvcc()
+    cu, cpp = _sources()
+    jobs = []
+    objs = []
+    for f in cu:
+        obj = os.path.join(BUILD, f + ".o")
+        objs.append(obj)
+        jobs.append(([nvcc, *ARCH, *NVCC_FLAGS, *DEFINES, "-I", INCLUDE, "-I", CSRC, "-c",
+                      os.path.join(CSRC, f), "-o", obj], obj + ".log"))
+    cxx = os.environ.get("CXX", "g++")
+    cuda_inc = os.path.join(os.path.dirname(os.path.dirname(nvcc)), "include")
+    for f in cpp:
+        obj = os.path.join(BUILD, f + ".o")
+        objs.append(obj)
+        jobs.append(([cxx, *CXX_FLAGS, *DEFINES, "-I", INCLUDE, "-I", CSRC, "-I", cuda_inc, "-c",
+                      os.path.join(CSRC, f), "-o", obj], obj + ".log"))
+    with cf.ThreadPoolExecutor(max_workers=min(8, len(jobs))) as ex:
+        logs = list(ex.map(lambda j: _compile(*j), jobs))
+    if verbose:
+        for lg in logs:
+            sys.stdout.write(open(lg).read())
+    tmp = LIB + ".tmp"
+    link = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lpthread", "-ldl", "-lrt"]
+    _compile(link, os.path.join(BUILD, "link.log"))
+    os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

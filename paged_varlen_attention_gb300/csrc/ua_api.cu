@@ -1,0 +1,423 @@
+// ua_api.cu -- the C ABI of the library: validation, the partition pass, the
+// host-to-device copy of the plan, tensor-map set-up, and the kernel launches.
+//
+// The operation is the unified kernel's ("[Kernel] Unified Triton kernel that
+// doesn't distinguish between prefill + decode", vLLM PR #16828, PR
+// description): one call for a batch that mixes prefill, chunked prefill and
+// decode, over the FlashAttention-layout paged cache.  Inside the call the
+// batch is split into decode units (memory-bound, split-KV, warp MMA) and
+// prefill tiles (tensor-core tcgen05 tiles), as the planner decides.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "unified_attention.h"
+#include "ua_kernels.h"
+#include "ua_planner.h"
+
+namespace ua {
+
+// The device status word the kernels write (bounded waits, bad block ids).
+__device__ int g_ua_device_status = 0;
+
+// Prefill rows go to the tcgen05 kernel when this is set; otherwise every
+// row tile runs in the decode kernel (correct for any shape, slower for long
+// query runs).
+constexpr bool kPrefillEnabled = UA_PREFILL_ENABLED;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int sms = 0;
+    int *status = nullptr;             // device address of g_ua_device_status
+    bool events = false;
+    cudaEvent_t ev[5] = {};            // plan copy | decode | prefill | combine
+    // what the last profiled call ran
+    bool ran[4] = {false, false, false, false};
+    int launches[4] = {0, 0, 0, 0};
+    bool profiled = false;
+};
+
+static std::mutex g_mutex;
+static DeviceState g_devices[kMaxDevices];
+static bool g_profile = false;
+
+static ua_status device_state(DeviceState **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return UA_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState &s = g_devices[dev];
+    if (!s.ready) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return UA_ERR_CUDA;
+        }
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_ua_device_status) != cudaSuccess) {
+            cudaGetLastError();
+            return UA_ERR_CUDA;
+        }
+        s.sms = sms;
+        s.status = static_cast<int *>(addr);
+        s.ready = true;
+    }
+    *out = &s;
+    return UA_OK;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// 3-D bf16 map over a [outer, mid, inner] tensor with 128-byte swizzled boxes
+// of {64, box_mid, box_outer} elements.  Out-of-range boxes read zeros.
+static bool encode_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t mid,
+                       uint64_t outer, uint32_t box_mid, uint32_t box_outer) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {inner, mid, outer};
+    cuuint64_t strides[2] = {inner * 2, inner * mid * 2};
+    cuuint32_t box[3] = {64, box_mid, box_outer};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+static bool aligned(const void *p, size_t a) {
+    return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+}  // namespace ua
+
+using namespace ua;
+
+extern "C" const char *ua_status_string(ua_status s) {
+    switch (s) {
+        case UA_OK: return "UA_OK";
+        case UA_ERR_INVALID_ARG: return "UA_ERR_INVALID_ARG";
+        case UA_ERR_UNSUPPORTED: return "UA_ERR_UNSUPPORTED";
+        case UA_ERR_WORKSPACE: return "UA_ERR_WORKSPACE";
+        case UA_ERR_CUDA: return "UA_ERR_CUDA";
+        case UA_ERR_DEVICE_CHECK: return "UA_ERR_DEVICE_CHECK";
+    }
+    return "UA_ERR_UNKNOWN";
+}
+
+static Problem make_problem(const int32_t *cu, const int32_t *lk, int32_t num_seqs, int32_t hq,
+                            int32_t hkv, int32_t d, int32_t bs, int32_t bt_stride,
+                            int32_t causal) {
+    Problem p;
+    p.cu = cu;
+    p.lk = lk;
+    p.num_seqs = num_seqs;
+    p.hq = hq;
+    p.hkv = hkv;
+    p.d = d;
+    p.bs = bs;
+    p.bt_stride = bt_stride;
+    p.causal = causal != 0;
+    return p;
+}
+
+extern "C" ua_status ua_workspace_size(const int32_t *cu_seqlens_q_host,
+                                       const int32_t *seqused_k_host, int32_t num_seqs,
+                                       int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_size, int32_t block_size,
+                                       int32_t block_table_stride, int32_t causal,
+                                       size_t *bytes) {
+    if (!bytes) return UA_ERR_INVALID_ARG;
+    Problem pr = make_problem(cu_seqlens_q_host, seqused_k_host, num_seqs, num_q_heads,
+                              num_kv_heads, head_size, block_size, block_table_stride, causal);
+    int v = validate_problem(pr);
+    if (v) return static_cast<ua_status>(v);
+    DeviceState *ds = nullptr;
+    ua_status st = device_state(&ds);
+    if (st != UA_OK) return st;
+    thread_local Plan plan;
+    build_plan(pr, ds->sms, kPrefillEnabled, plan);
+    *bytes = plan.layout.total_bytes;
+    return UA_OK;
+}
+
+extern "C" ua_status ua_plan_inspect(const int32_t *cu_seqlens_q_host,
+                                     const int32_t *seqused_k_host, int32_t num_seqs,
+                                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                                     int32_t block_size, int32_t block_table_stride,
+                                     int32_t causal, int32_t num_sms, int32_t *counts,
+                                     int32_t *items, int64_t items_cap, int64_t *n_items) {
+    if (!counts || num_sms <= 0) return UA_ERR_INVALID_ARG;
+    Problem pr = make_problem(cu_seqlens_q_host, seqused_k_host, num_seqs, num_q_heads,
+                              num_kv_heads, head_size, block_size, block_table_stride, causal);
+    int v = validate_problem(pr);
+    if (v) return static_cast<ua_status>(v);
+    Plan plan;
+    build_plan(pr, num_sms, kPrefillEnabled, plan);
+    counts[0] = plan.dec_ctas;
+    counts[1] = (int32_t)plan.pieces.size();
+    counts[2] = (int32_t)plan.comb.size();
+    counts[3] = plan.n_slots;
+    counts[4] = (int32_t)plan.tiles.size();
+    counts[5] = plan.pre_ctas;
+    counts[6] = (int32_t)std::min<int64_t>(plan.dec_pages, INT32_MAX);
+    counts[7] = (int32_t)std::min<size_t>(plan.layout.total_bytes, (size_t)INT32_MAX);
+    const int64_t need = 2 * (int64_t)plan.pieces.size() + (int64_t)plan.tiles.size() +
+                         (int64_t)plan.comb.size();
+    if (n_items) *n_items = need;
+    if (!items) return UA_OK;
+    int64_t row = 0;
+    auto put = [&](int32_t a, int32_t b, int32_t c, int32_t d, int32_t e, int32_t f, int32_t g,
+                   int32_t h) {
+        if (row >= items_cap) return;
+        int32_t *r = items + 8 * row;
+        r[0] = a; r[1] = b; r[2] = c; r[3] = d; r[4] = e; r[5] = f; r[6] = g; r[7] = h;
+        ++row;
+    };
+    for (int c = 0; c < plan.dec_ctas; ++c)
+        for (int i = plan.cta_begin[c]; i < plan.cta_begin[c + 1]; ++i) {
+            const DecPiece &pc = plan.pieces[i];
+            put(0, c, pc.seq, pc.kvh, pc.row0, pc.nrows, pc.page_begin, pc.page_end);
+            put(1, pc.slot, pc.unit, 0, 0, 0, 0, 0);
+        }
+    for (size_t i = 0; i < plan.tiles.size(); ++i) {
+        const PreTile &t = plan.tiles[i];
+        put(2, (int32_t)i, t.seq, t.kvh, t.row0, t.nrows, t.kv_tiles, 0);
+    }
+    for (const CombUnit &u : plan.comb)
+        put(3, u.seq, u.kvh, u.row0, u.nrows, u.slot_begin, u.nslots, 0);
+    return UA_OK;
+}
+
+extern "C" ua_status ua_device_status(int32_t *code) {
+    if (!code) return UA_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return UA_ERR_CUDA;
+    }
+    int value = 0;
+    if (cudaMemcpyFromSymbol(&value, g_ua_device_status, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return UA_ERR_CUDA;
+    }
+    *code = value;
+    if (value != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_ua_device_status, &zero, sizeof(int)) != cudaSuccess) {
+            cudaGetLastError();
+            return UA_ERR_CUDA;
+        }
+        return UA_ERR_DEVICE_CHECK;
+    }
+    return UA_OK;
+}
+
+extern "C" ua_status ua_profile_enable(int32_t enable) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    g_profile = enable != 0;
+    return UA_OK;
+}
+
+extern "C" ua_status ua_profile_last(float *ms, int32_t *launches) {
+    if (!ms || !launches) return UA_ERR_INVALID_ARG;
+    DeviceState *ds = nullptr;
+    ua_status st = device_state(&ds);
+    if (st != UA_OK) return st;
+    for (int i = 0; i < 4; ++i) {
+        ms[i] = -1.f;
+        launches[i] = 0;
+    }
+    if (!ds->profiled) return UA_OK;
+    if (cudaEventSynchronize(ds->ev[4]) != cudaSuccess) {
+        cudaGetLastError();
+        return UA_ERR_CUDA;
+    }
+    // ev[0] before the plan copy, ev[1] after it, ev[2] after decode,
+    // ev[3] after prefill, ev[4] after combine.
+    const int from[4] = {1, 2, 3, 0};
+    const int to[4] = {2, 3, 4, 1};
+    for (int i = 0; i < 4; ++i) {
+        if (!ds->ran[i]) continue;
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, ds->ev[from[i]], ds->ev[to[i]]) != cudaSuccess) {
+            cudaGetLastError();
+            return UA_ERR_CUDA;
+        }
+        ms[i] = t;
+        launches[i] = ds->launches[i];
+    }
+    return UA_OK;
+}
+
+extern "C" ua_status unified_attention(const void *q, const void *k_cache, const void *v_cache,
+                                       const int32_t *cu_seqlens_q, const int32_t *seqused_k,
+                                       const int32_t *block_table, float softmax_scale,
+                                       int32_t causal, void *out,
+                                       const int32_t *cu_seqlens_q_host,
+                                       const int32_t *seqused_k_host, int32_t num_seqs,
+                                       int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_size, int32_t block_size, int32_t num_blocks,
+                                       int32_t block_table_stride, void *workspace,
+                                       size_t workspace_bytes, void *stream_ptr) {
+    // ---- host-side checks, before any CUDA call
+    Problem pr = make_problem(cu_seqlens_q_host, seqused_k_host, num_seqs, num_q_heads,
+                              num_kv_heads, head_size, block_size, block_table_stride, causal);
+    int v = validate_problem(pr);
+    if (v) return static_cast<ua_status>(v);
+    if (!std::isfinite(softmax_scale)) return UA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return UA_OK;
+    const int64_t total_q = cu_seqlens_q_host[num_seqs];
+    if (total_q == 0) return UA_OK;
+    if (!q || !k_cache || !v_cache || !out || !cu_seqlens_q || !seqused_k || !block_table)
+        return UA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+        return UA_ERR_INVALID_ARG;
+    if (num_blocks <= 0 || (int64_t)num_blocks * block_size >= ((int64_t)1 << 31))
+        return UA_ERR_INVALID_ARG;
+    if (total_q >= ((int64_t)1 << 31)) return UA_ERR_INVALID_ARG;
+
+    DeviceState *ds = nullptr;
+    ua_status st = device_state(&ds);
+    if (st != UA_OK) return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+
+    // ---- partition pass
+    thread_local Plan plan;
+    thread_local std::vector<uint8_t> blob;
+    build_plan(pr, ds->sms, kPrefillEnabled, plan);
+    const Layout &L = plan.layout;
+    if (L.total_bytes > 0) {
+        if (!workspace || workspace_bytes < L.total_bytes || !aligned(workspace, kAlign))
+            return UA_ERR_WORKSPACE;
+    }
+    serialize_plan(plan, blob);
+
+    // ---- tensor maps: K/V as [num_blocks * block_size, Hkv, D], Q as [total_q, Hq, D]
+    const int g = num_q_heads / num_kv_heads;
+    const uint64_t tokens = (uint64_t)num_blocks * block_size;
+    CUtensorMap tm_k, tm_v, tm_q;
+    if (!encode_map(&tm_k, k_cache, head_size, num_kv_heads, tokens, 1, kBlockSize) ||
+        !encode_map(&tm_v, v_cache, head_size, num_kv_heads, tokens, 1, kBlockSize))
+        return UA_ERR_CUDA;
+    if (!plan.tiles.empty() &&
+        !encode_map(&tm_q, q, head_size, num_q_heads, (uint64_t)total_q, g, kPreRows / g))
+        return UA_ERR_CUDA;
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const bool prof = g_profile;
+    if (prof && !ds->events) {
+        for (int i = 0; i < 5; ++i)
+            if (cudaEventCreate(&ds->ev[i]) != cudaSuccess) {
+                cudaGetLastError();
+                return UA_ERR_CUDA;
+            }
+        ds->events = true;
+    }
+    auto mark = [&](int i) {
+        if (prof) cudaEventRecord(ds->ev[i], stream);
+    };
+    const float scale_log2 = softmax_scale * 1.4426950408889634f;
+
+    mark(0);
+    if (L.blob_bytes > 0 &&
+        cudaMemcpyAsync(ws, blob.data(), L.blob_bytes, cudaMemcpyHostToDevice, stream) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return UA_ERR_CUDA;
+    }
+    mark(1);
+    cudaError_t e = cudaSuccess;
+    if (plan.dec_ctas > 0) {
+        DecodeParams dp{};
+        dp.q = static_cast<const __nv_bfloat16 *>(q);
+        dp.out = static_cast<__nv_bfloat16 *>(out);
+        dp.cu = cu_seqlens_q;
+        dp.seqused_k = seqused_k;
+        dp.block_table = block_table;
+        dp.bt_stride = block_table_stride;
+        dp.num_blocks = num_blocks;
+        dp.hq = num_q_heads;
+        dp.hkv = num_kv_heads;
+        dp.g = g;
+        dp.causal = causal != 0;
+        dp.scale_log2 = scale_log2;
+        dp.cta_begin = reinterpret_cast<const int32_t *>(ws + L.off_cta);
+        dp.pieces = reinterpret_cast<const DecPiece *>(ws + L.off_pieces);
+        dp.part_o = reinterpret_cast<float *>(ws + L.off_part_o);
+        dp.part_ml = reinterpret_cast<float *>(ws + L.off_part_ml);
+        dp.status = ds->status;
+        e = launch_decode(head_size, dp, tm_k, tm_v, plan.dec_ctas, stream);
+        if (e != cudaSuccess) return UA_ERR_CUDA;
+    }
+    mark(2);
+    if (!plan.tiles.empty()) {
+        PrefillParams pp{};
+        pp.out = static_cast<__nv_bfloat16 *>(out);
+        pp.cu = cu_seqlens_q;
+        pp.seqused_k = seqused_k;
+        pp.block_table = block_table;
+        pp.bt_stride = block_table_stride;
+        pp.num_blocks = num_blocks;
+        pp.hq = num_q_heads;
+        pp.hkv = num_kv_heads;
+        pp.g = g;
+        pp.causal = causal != 0;
+        pp.scale_log2 = scale_log2;
+        pp.tiles = reinterpret_cast<const PreTile *>(ws + L.off_tiles);
+        pp.n_tiles = (int32_t)plan.tiles.size();
+        pp.status = ds->status;
+        e = launch_prefill(head_size, pp, tm_q, tm_k, tm_v, plan.pre_ctas, stream);
+        if (e != cudaSuccess) return UA_ERR_CUDA;
+    }
+    mark(3);
+    if (!plan.comb.empty()) {
+        CombineParams cp{};
+        cp.out = static_cast<__nv_bfloat16 *>(out);
+        cp.cu = cu_seqlens_q;
+        cp.hq = num_q_heads;
+        cp.g = g;
+        cp.units = reinterpret_cast<const CombUnit *>(ws + L.off_comb);
+        cp.part_o = reinterpret_cast<const float *>(ws + L.off_part_o);
+        cp.part_ml = reinterpret_cast<const float *>(ws + L.off_part_ml);
+        e = launch_combine(head_size, cp, (int)plan.comb.size(), stream);
+        if (e != cudaSuccess) return UA_ERR_CUDA;
+    }
+    mark(4);
+    if (prof) {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        ds->ran[0] = plan.dec_ctas > 0;
+        ds->ran[1] = !plan.tiles.empty();
+        ds->ran[2] = !plan.comb.empty();
+        ds->ran[3] = L.blob_bytes > 0;
+        ds->launches[0] = plan.dec_ctas > 0 ? 1 : 0;
+        ds->launches[1] = plan.tiles.empty() ? 0 : 1;
+        ds->launches[2] = plan.comb.empty() ? 0 : 1;
+        ds->launches[3] = 0;
+        ds->profiled = true;
+    }
+    return UA_OK;
+}

@@ -1,0 +1,412 @@
+// ua_decode.cu -- memory-bound decode / split-KV kernel and the LSE-merge combine.
+//
+// The decode rows of a unified batch (a handful of new tokens per sequence)
+// are HBM-bound: every KV page of every sequence is read once per KV head and
+// used by the G query heads that share it.  Packing those G heads (times the
+// few new tokens) into the M dimension of one 16-row warp MMA tile is the GQA
+// packing of the unified kernel ("[Kernel] Unified Triton kernel that doesn't
+// distinguish between prefill + decode", vLLM PR #16828, PR description):
+// each page is fetched once and feeds all heads of its group.
+//
+// Structure (one persistent CTA = 4 consumer warps + 1 producer warp):
+//   * the producer walks the CTA's pieces (contiguous page ranges of
+//     (sequence, kv head, row tile) units), reads 32 block-table entries at a
+//     time, and issues one TMA load per 64-column chunk of each K and V page
+//     into a ring of shared-memory stages (128-byte swizzle);
+//   * consumer warp w takes pages w, w+4, ... of each piece: S = Q K^T with
+//     mma.sync m16n8k16 (bf16 in, fp32 accumulate), bottom-right causal mask,
+//     online softmax in the exp2 domain, O += P V;
+//   * at the end of each piece the four warps merge their (m, l, O) through
+//     shared memory and write the bf16 output, or an fp32 partial plus its
+//     running (max, sum) when the unit was split across CTAs (split-KV).
+// Offsets into the cache are 64-bit; TMA coordinates stay 32-bit
+// (num_blocks * block_size < 2^31 is checked on the host).
+#include "ua_device.cuh"
+#include "ua_kernels.h"
+
+namespace ua {
+
+template <int D>
+struct DecCfg {
+    static constexpr int kChunks = D / 64;                        // 64-column TMA boxes per row
+    static constexpr int kPageBytes = kBlockSize * D * 2;        // one page, one kv head, K or V
+    static constexpr int kStageBytes = 2 * kPageBytes;           // K + V
+    static constexpr int kStages = (D == 128) ? 8 : 16;
+    static constexpr int kConsumerWarps = 4;
+    static constexpr int kThreads = (kConsumerWarps + 1) * 32;
+    static constexpr int kMergeFloats = kDecRows * D + 2 * kDecRows;   // per warp
+    static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes +
+                                         (size_t)kConsumerWarps * kMergeFloats * 4 +
+                                         2 * kStages * 8;
+};
+
+template <int D>
+__global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
+    ua_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v) {
+    using C = DecCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *stages = smem;
+    float *merge = reinterpret_cast<float *>(smem + (size_t)C::kStages * C::kStageBytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(merge + C::kConsumerWarps * C::kMergeFloats);
+    const uint32_t stage0 = smem_u32(stages);
+    const uint32_t full0 = smem_u32(bars);
+    const uint32_t empty0 = smem_u32(bars + C::kStages);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kStages; ++i) {
+            mbar_init(full0 + 8 * i, 1);
+            mbar_init(empty0 + 8 * i, 1);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    const int pbeg = p.cta_begin[blockIdx.x];
+    const int pend = p.cta_begin[blockIdx.x + 1];
+    uint32_t issued = 0;   // producer: pages issued (kept for the final drain)
+
+    if (warp == C::kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+        }
+        const uint64_t policy = l2_policy_evict_first();
+        bool ok = true;
+        for (int pi = pbeg; pi < pend && ok; ++pi) {
+            const DecPiece pc = p.pieces[pi];
+            const int32_t *bt_row = p.block_table + (int64_t)pc.seq * p.bt_stride;
+            for (int base = pc.page_begin; base < pc.page_end && ok; base += 32) {
+                const int n = min(32, pc.page_end - base);
+                int bid = 0;
+                if (lane < n) {
+                    bid = __ldg(bt_row + base + lane);
+                    if (bid < 0 || bid >= p.num_blocks) {
+                        record_status(p.status, UA_DEVICE_BAD_BLOCK_ID_BIT);
+                        bid = p.num_blocks;   // outside the tensor map: TMA fills zeros
+                    }
+                }
+                for (int k = 0; k < n; ++k) {
+                    const int b = __shfl_sync(0xffffffffu, bid, k);
+                    int good = 1;
+                    if (lane == 0) {
+                        const uint32_t st = issued % C::kStages;
+                        const uint32_t ph = (issued / C::kStages) & 1;
+                        if (!mbar_wait(empty0 + 8 * st, ph ^ 1, p.status)) {
+                            good = 0;
+                        } else {
+                            const uint32_t fb = full0 + 8 * st;
+                            const uint32_t kdst = stage0 + st * C::kStageBytes;
+                            const uint32_t vdst = kdst + C::kPageBytes;
+                            mbar_arrive_expect_tx(fb, C::kStageBytes);
+#pragma unroll
+                            for (int c = 0; c < C::kChunks; ++c) {
+                                tma_load_3d_hint(kdst + c * 2048, &tm_k, c * 64, pc.kvh,
+                                                 b * kBlockSize, fb, policy);
+                                tma_load_3d_hint(vdst + c * 2048, &tm_v, c * 64, pc.kvh,
+                                                 b * kBlockSize, fb, policy);
+                            }
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+                    if (!ok) break;
+                    ++issued;
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ consumers
+        const int w = warp;
+        const int qr = lane >> 2;          // fragment row (and row + 8)
+        const int qc = (lane & 3) * 2;     // fragment column pair
+        float *mrg_o = merge + w * C::kMergeFloats;
+        float *mrg_m = mrg_o + kDecRows * D;
+        float *mrg_l = mrg_m + kDecRows;
+        uint32_t gbase = 0;
+        bool ok = true;
+        for (int pi = pbeg; pi < pend; ++pi) {
+            const DecPiece pc = p.pieces[pi];
+            const int q0 = p.cu[pc.seq];
+            const int lq = p.cu[pc.seq + 1] - q0;
+            const int lk = p.seqused_k[pc.seq];
+            const int npages = pc.page_end - pc.page_begin;
+
+            // visible-key limit of this thread's two rows (bottom-right causal)
+            int kend[2];
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int r = qr + 8 * rr;
+                const int i = (pc.row0 + r) / p.g;
+                kend[rr] = (p.causal && r < pc.nrows) ? min(lk, lk - lq + i + 1) : lk;
+            }
+            // Q fragments (A operand), zero for rows past the unit
+            uint32_t qa[D / 16][4];
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+#pragma unroll
+                for (int ri = 0; ri < 4; ++ri) {
+                    const int r = qr + (ri & 1) * 8;
+                    const int col = ks * 16 + qc + (ri >> 1) * 8;
+                    uint32_t v = 0;
+                    if (r < pc.nrows) {
+                        const int pr = pc.row0 + r;
+                        const int64_t t = (int64_t)q0 + pr / p.g;
+                        const int h = pc.kvh * p.g + pr % p.g;
+                        v = __ldg(reinterpret_cast<const uint32_t *>(p.q + (t * p.hq + h) * D + col));
+                    }
+                    qa[ks][ri] = v;
+                }
+
+            float o[D / 8][4];
+#pragma unroll
+            for (int nt = 0; nt < D / 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
+            float m[2] = {-INFINITY, -INFINITY};
+            float l[2] = {0.f, 0.f};
+
+            for (int k = w; k < npages && ok; k += C::kConsumerWarps) {
+                const uint32_t gidx = gbase + k;
+                const uint32_t st = gidx % C::kStages;
+                const uint32_t ph = (gidx / C::kStages) & 1;
+                if (!mbar_wait(full0 + 8 * st, ph, p.status)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t kb = stage0 + st * C::kStageBytes;
+                const uint32_t vb = kb + C::kPageBytes;
+                const int key0 = (pc.page_begin + k) * kBlockSize;
+
+                // S = Q K^T for 16 rows x 16 keys
+                float s[2][4];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const int c = ks >> 2;
+                    const int ch = (ks & 3) * 2 + ((lane >> 3) & 1);
+                    const int r = ((lane >> 4) << 3) + (lane & 7);
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4(kb + c * 2048 + r * 128 + ((ch ^ (r & 7)) << 4), b0, b1, b2, b3);
+                    mma_bf16_16816(s[0], qa[ks], b0, b1);
+                    mma_bf16_16816(s[1], qa[ks], b2, b3);
+                }
+                // scale into the log2 domain and mask
+                float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int rr = e >> 1;
+                        const int key = key0 + nt * 8 + qc + (e & 1);
+                        const float x = key < kend[rr] ? s[nt][e] * p.scale_log2 : -INFINITY;
+                        s[nt][e] = x;
+                        mx[rr] = fmaxf(mx[rr], x);
+                    }
+                float mu[2];
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
+                    mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
+                    const float mn = fmaxf(m[rr], mx[rr]);
+                    mu[rr] = (mn == -INFINITY) ? 0.f : mn;
+                    const float alpha = fast_exp2(m[rr] - mu[rr]);
+                    m[rr] = mn;
+                    l[rr] *= alpha;
+#pragma unroll
+                    for (int nt = 0; nt < D / 8; ++nt) {
+                        o[nt][2 * rr] *= alpha;
+                        o[nt][2 * rr + 1] *= alpha;
+                    }
+                }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float pv = fast_exp2(s[nt][e] - mu[e >> 1]);
+                        s[nt][e] = pv;
+                        l[e >> 1] += pv;
+                    }
+                uint32_t pa[4];
+                pa[0] = pack_bf16x2(s[0][0], s[0][1]);
+                pa[1] = pack_bf16x2(s[0][2], s[0][3]);
+                pa[2] = pack_bf16x2(s[1][0], s[1][1]);
+                pa[3] = pack_bf16x2(s[1][2], s[1][3]);
+                // V rows past the context (last page) may hold anything, NaN
+                // included: zero them so 0 * NaN never reaches O.
+                uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+                if (key0 + kBlockSize > lk) {
+                    vm0 = (key0 + qc < lk ? 0x0000ffffu : 0u) | (key0 + qc + 1 < lk ? 0xffff0000u : 0u);
+                    vm1 = (key0 + 8 + qc < lk ? 0x0000ffffu : 0u) |
+                          (key0 + 9 + qc < lk ? 0xffff0000u : 0u);
+                }
+#pragma unroll
+                for (int np = 0; np < D / 16; ++np) {
+                    const int c = np >> 2;
+                    const int ch = (np & 3) * 2 + (lane >> 4);
+                    const int r = ((lane >> 3) & 1) * 8 + (lane & 7);
+                    uint32_t v0, v1, v2, v3;
+                    ldmatrix_x4_trans(vb + c * 2048 + r * 128 + ((ch ^ (r & 7)) << 4), v0, v1, v2, v3);
+                    mma_bf16_16816(o[2 * np], pa, v0 & vm0, v1 & vm1);
+                    mma_bf16_16816(o[2 * np + 1], pa, v2 & vm0, v3 & vm1);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty0 + 8 * st);
+            }
+            gbase += npages;
+
+            // ---- merge the four warps' states and write the result
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 1);
+                l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 2);
+            }
+#pragma unroll
+            for (int nt = 0; nt < D / 8; ++nt) {
+                const int col = nt * 8 + qc;
+                *reinterpret_cast<float2 *>(mrg_o + qr * D + col) = make_float2(o[nt][0], o[nt][1]);
+                *reinterpret_cast<float2 *>(mrg_o + (qr + 8) * D + col) = make_float2(o[nt][2], o[nt][3]);
+            }
+            if ((lane & 3) == 0) {
+                mrg_m[qr] = m[0];
+                mrg_m[qr + 8] = m[1];
+                mrg_l[qr] = l[0];
+                mrg_l[qr + 8] = l[1];
+            }
+            named_barrier_sync(1, C::kConsumerWarps * 32);
+            const int tid = threadIdx.x;
+            for (int gi = tid; gi < kDecRows * (D / 4); gi += C::kConsumerWarps * 32) {
+                const int row = gi / (D / 4);
+                const int col = (gi % (D / 4)) * 4;
+                if (row >= pc.nrows) continue;
+                float mw[C::kConsumerWarps];
+                float M = -INFINITY;
+#pragma unroll
+                for (int ww = 0; ww < C::kConsumerWarps; ++ww) {
+                    mw[ww] = merge[ww * C::kMergeFloats + kDecRows * D + row];
+                    M = fmaxf(M, mw[ww]);
+                }
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                float L = 0.f;
+                if (M != -INFINITY) {
+#pragma unroll
+                    for (int ww = 0; ww < C::kConsumerWarps; ++ww) {
+                        const float f = fast_exp2(mw[ww] - M);
+                        L += f * merge[ww * C::kMergeFloats + kDecRows * D + kDecRows + row];
+                        const float4 ov =
+                            *reinterpret_cast<const float4 *>(merge + ww * C::kMergeFloats + row * D + col);
+                        acc.x += f * ov.x;
+                        acc.y += f * ov.y;
+                        acc.z += f * ov.z;
+                        acc.w += f * ov.w;
+                    }
+                }
+                if (pc.slot < 0) {
+                    const float inv = L > 0.f ? 1.f / L : 0.f;
+                    const int pr = pc.row0 + row;
+                    const int64_t t = (int64_t)q0 + pr / p.g;
+                    const int h = pc.kvh * p.g + pr % p.g;
+                    uint2 packed;
+                    packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+                    packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+                    *reinterpret_cast<uint2 *>(p.out + (t * p.hq + h) * D + col) = packed;
+                } else {
+                    // partial: unnormalised sum relative to M, plus (M, L)
+                    const int64_t base = ((int64_t)pc.slot * kDecRows + row);
+                    *reinterpret_cast<float4 *>(p.part_o + base * D + col) = acc;
+                    if (col == 0) *reinterpret_cast<float2 *>(p.part_ml + 2 * base) = make_float2(M, L);
+                }
+            }
+            named_barrier_sync(1, C::kConsumerWarps * 32);
+        }
+    }
+
+    // Drain: every TMA load this CTA issued must have landed before the CTA
+    // exits (on the normal path they all have; this matters after a timeout).
+    __syncthreads();
+    if (warp == C::kConsumerWarps && lane == 0) {
+        const uint32_t first = issued > (uint32_t)C::kStages ? issued - C::kStages : 0;
+        for (uint32_t gidx = first; gidx < issued; ++gidx)
+            mbar_wait(full0 + 8 * (gidx % C::kStages), (gidx / C::kStages) & 1, p.status);
+    }
+}
+
+// Merge of the partials of split units (log2 domain).  Partial s holds
+// O_s = sum_j 2^(x_j - m_s) v_j, its max m_s and l_s = sum_j 2^(x_j - m_s):
+//   M = max_s m_s,  out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+template <int D>
+__global__ void __launch_bounds__(128) ua_combine_kernel(const CombineParams p) {
+    const CombUnit u = p.units[blockIdx.x];
+    const int q0 = p.cu[u.seq];
+    for (int gi = threadIdx.x; gi < u.nrows * (D / 4); gi += blockDim.x) {
+        const int row = gi / (D / 4);
+        const int col = (gi % (D / 4)) * 4;
+        float M = -INFINITY;
+        for (int s = 0; s < u.nslots; ++s)
+            M = fmaxf(M, p.part_ml[2 * ((int64_t)(u.slot_begin + s) * kDecRows + row)]);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float W = 0.f;
+        if (M != -INFINITY) {
+            for (int s = 0; s < u.nslots; ++s) {
+                const int64_t base = (int64_t)(u.slot_begin + s) * kDecRows + row;
+                const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + 2 * base);
+                const float w = fast_exp2(ml.x - M);     // 0 for an empty partial (m = -inf)
+                W += w * ml.y;
+                const float4 ov = *reinterpret_cast<const float4 *>(p.part_o + base * D + col);
+                acc.x += w * ov.x;
+                acc.y += w * ov.y;
+                acc.z += w * ov.z;
+                acc.w += w * ov.w;
+            }
+        }
+        const float inv = W > 0.f ? 1.f / W : 0.f;
+        const int pr = u.row0 + row;
+        const int64_t t = (int64_t)q0 + pr / p.g;
+        const int h = u.kvh * p.g + pr % p.g;
+        uint2 packed;
+        packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+        packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2 *>(p.out + (t * p.hq + h) * D + col) = packed;
+    }
+}
+
+template <int D>
+static cudaError_t launch_decode_t(const DecodeParams &p, const CUtensorMap &tm_k,
+                                   const CUtensorMap &tm_v, int ctas, cudaStream_t stream) {
+    using C = DecCfg<D>;
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(ua_decode_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    ua_decode_kernel<D><<<ctas, C::kThreads, C::kSmemBytes, stream>>>(p, tm_k, tm_v);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode(int d, const DecodeParams &p, const CUtensorMap &tm_k,
+                          const CUtensorMap &tm_v, int ctas, cudaStream_t stream) {
+    return d == 64 ? launch_decode_t<64>(p, tm_k, tm_v, ctas, stream)
+                   : launch_decode_t<128>(p, tm_k, tm_v, ctas, stream);
+}
+
+cudaError_t launch_combine(int d, const CombineParams &p, int n_units, cudaStream_t stream) {
+    if (d == 64)
+        ua_combine_kernel<64><<<n_units, 128, 0, stream>>>(p);
+    else
+        ua_combine_kernel<128><<<n_units, 128, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace ua

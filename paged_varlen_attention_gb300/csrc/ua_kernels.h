@@ -1,0 +1,67 @@
+// ua_kernels.h -- launch interface between the C ABI (ua_api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ua_plan.h"
+
+namespace ua {
+
+struct DecodeParams {
+    const __nv_bfloat16 *q;
+    __nv_bfloat16 *out;
+    const int32_t *cu;           // device cu_seqlens_q
+    const int32_t *seqused_k;    // device seqused_k
+    const int32_t *block_table;
+    int32_t bt_stride;
+    int32_t num_blocks;
+    int32_t hq;
+    int32_t hkv;
+    int32_t g;                   // hq / hkv
+    int32_t causal;
+    float scale_log2;            // softmax_scale * log2(e)
+    const int32_t *cta_begin;    // plan: [ctas + 1]
+    const DecPiece *pieces;      // plan
+    float *part_o;               // [slots][kDecRows][d]
+    float *part_ml;              // [slots][kDecRows][2]: running max (log2 domain), sum
+    int *status;                 // device status word
+};
+
+struct CombineParams {
+    __nv_bfloat16 *out;
+    const int32_t *cu;
+    int32_t hq;
+    int32_t g;
+    const CombUnit *units;
+    const float *part_o;
+    const float *part_ml;
+};
+
+struct PrefillParams {
+    __nv_bfloat16 *out;
+    const int32_t *cu;
+    const int32_t *seqused_k;
+    const int32_t *block_table;
+    int32_t bt_stride;
+    int32_t num_blocks;
+    int32_t hq;
+    int32_t hkv;
+    int32_t g;
+    int32_t causal;
+    float scale_log2;
+    const PreTile *tiles;
+    int32_t n_tiles;
+    int *status;
+};
+
+// Each returns the launch error (cudaSuccess when the launch was queued).
+cudaError_t launch_decode(int d, const DecodeParams &p, const CUtensorMap &tm_k,
+                          const CUtensorMap &tm_v, int ctas, cudaStream_t stream);
+cudaError_t launch_combine(int d, const CombineParams &p, int n_units, cudaStream_t stream);
+cudaError_t launch_prefill(int d, const PrefillParams &p, const CUtensorMap &tm_q,
+                           const CUtensorMap &tm_k, const CUtensorMap &tm_v, int ctas,
+                           cudaStream_t stream);
+
+}  // namespace ua

@@ -1,0 +1,101 @@
+// ua_plan.h -- the work partition of unified paged varlen attention.
+//
+// The pages behind this library explain why one call needs a per-batch plan:
+// a single fixed grid fits prefill, chunked prefill and decode badly, and
+// tile sizes good for one are poor for the other ("[Kernel] [V1] Improved
+// performance for V1 Triton (ROCm) backend", vLLM PR #14152, section "How is
+// this performance improvement achieved?").  The unified kernel instead packs
+// the query heads of one KV head along the query dimension ("[Kernel] Unified
+// Triton kernel that doesn't distinguish between prefill + decode", vLLM PR
+// #16828, PR description).  This plan keeps the single call and the GQA
+// packing, and splits the batch into:
+//
+//   * decode units -- (sequence, kv head, 16-row tile) for sequences whose
+//     packed rows (Lq * G) fit one 16-row warp-MMA tile.  Their KV pages are
+//     concatenated and cut into equal page ranges, one per persistent CTA, so
+//     every SM streams the same number of pages (split-KV).  A unit cut into
+//     several pieces writes fp32 partials that the combine kernel merges with
+//     a log-sum-exp rule.
+//   * prefill tiles -- (sequence, kv head, 128-row tile) for the rest, one
+//     tensor-core tile of 128 packed rows each, longest first.
+//
+// Rows are packed (token, head-in-group) pairs: packed row r of a (sequence,
+// kv head) is token r / G and query head kv_head * G + r % G.
+//
+// This header is shared by host and device code; it holds plain structs only.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#define UA_DEVICE_BAD_BLOCK_ID_BIT 0x1
+#define UA_DEVICE_WAIT_TIMEOUT_BIT 0x2
+
+namespace ua {
+
+constexpr int kBlockSize = 16;      // tokens per KV page (the supported page size)
+constexpr int kDecRows = 16;        // packed rows per decode tile (warp MMA M)
+constexpr int kPreRows = 128;       // packed rows per prefill tile (tcgen05 M)
+constexpr int kKvTile = 128;        // keys per prefill KV tile (8 pages)
+constexpr int kDecCtasPerSm = 2;    // resident decode CTAs per SM
+constexpr size_t kAlign = 256;
+
+struct alignas(16) DecPiece {   // one contiguous page range of one decode unit
+    int32_t seq;
+    int32_t kvh;
+    int32_t row0;        // first packed row of the unit
+    int32_t nrows;       // packed rows in the unit (<= kDecRows)
+    int32_t page_begin;  // first logical page of the range
+    int32_t page_end;    // one past the last logical page
+    int32_t slot;        // -1: the piece is the whole unit, write bf16 output; else partial slot
+    int32_t unit;
+};
+
+struct alignas(16) CombUnit {   // a decode unit split over several pieces
+    int32_t seq;
+    int32_t kvh;
+    int32_t row0;
+    int32_t nrows;
+    int32_t slot_begin;
+    int32_t nslots;
+    int32_t pad0;
+    int32_t pad1;
+};
+
+struct alignas(16) PreTile {    // one 128-row prefill tile
+    int32_t seq;
+    int32_t kvh;
+    int32_t row0;
+    int32_t nrows;
+    int32_t kv_tiles;    // 128-key tiles it visits
+    int32_t pad0;
+    int32_t pad1;
+    int32_t pad2;
+};
+
+// Problem description as seen by the planner (host metadata).
+struct Problem {
+    const int32_t *cu;     // [num_seqs + 1]
+    const int32_t *lk;     // [num_seqs]
+    int32_t num_seqs;
+    int32_t hq;
+    int32_t hkv;
+    int32_t d;
+    int32_t bs;
+    int32_t bt_stride;
+    bool causal;
+};
+
+// Offsets of the plan sections inside the device workspace.
+struct Layout {
+    size_t off_cta;        // int32 [dec_ctas + 1]
+    size_t off_pieces;     // DecPiece [n_pieces]
+    size_t off_comb;       // CombUnit [n_comb]
+    size_t off_tiles;      // PreTile [n_tiles]
+    size_t blob_bytes;     // bytes copied host -> device per call
+    size_t off_part_o;     // float [n_slots][kDecRows][d]
+    size_t off_part_ml;    // float [n_slots][kDecRows][2]
+    size_t total_bytes;    // workspace bytes
+};
+
+}  // namespace ua

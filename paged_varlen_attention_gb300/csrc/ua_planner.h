@@ -1,0 +1,35 @@
+// ua_planner.h -- host-side validation and work partition (no CUDA calls).
+#pragma once
+
+#include <vector>
+
+#include "ua_plan.h"
+
+namespace ua {
+
+struct Plan {
+    int32_t dec_ctas = 0;
+    int64_t dec_pages = 0;
+    std::vector<int32_t> cta_begin;     // dec_ctas + 1
+    std::vector<DecPiece> pieces;
+    std::vector<CombUnit> comb;
+    int32_t n_slots = 0;
+    std::vector<PreTile> tiles;
+    int32_t pre_ctas = 0;
+    Layout layout{};
+};
+
+// Status codes follow ua_status (0 ok, 1 invalid arg, 2 unsupported).
+int validate_problem(const Problem &p);
+
+// Builds the partition for a GPU with num_sms multiprocessors.
+// prefill_enabled = false routes every row tile to the decode kernel.
+void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan);
+
+// Packs the plan sections into one host blob laid out as plan.layout says.
+void serialize_plan(const Plan &plan, std::vector<uint8_t> &blob);
+
+// True when the prefill (tcgen05) kernel can take this head grouping.
+bool prefill_supports(const Problem &p);
+
+}  // namespace ua

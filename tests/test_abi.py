@@ -1,0 +1,94 @@
+"""The C-ABI library loads, exports every declared entry point, and rejects bad
+arguments on the host before any CUDA call (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from paged_varlen_attention_gb300 import _binding as B
+from paged_varlen_attention_gb300 import build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return B.load_library()
+
+
+def declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if not f.endswith(".h"):
+            continue
+        text = open(os.path.join(inc, f)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*([a-z_][a-z0-9_]*)\s*\(",
+                            text, flags=re.M)
+    return names
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("unified_attention", "ua_workspace_size", "ua_status_string", "ua_device_status",
+              "ua_plan_inspect", "ua_profile_enable", "ua_profile_last"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_status_strings(lib):
+    for code, name in B.STATUS.items():
+        assert lib.ua_status_string(code).decode() == name
+
+
+def _call(lib, cu, sk, hq=4, hk=2, d=64, bs=16, nb=8, stride=4, causal=1, scale=0.125,
+          ptr=16, out=16, ws=None, ws_bytes=0):
+    cu = np.asarray(cu, np.int32)
+    sk = np.asarray(sk, np.int32)
+    p = ctypes.c_void_p(ptr) if ptr else None
+    o = ctypes.c_void_p(out) if out else None
+    return lib.unified_attention(p, p, p, p, p, p, scale, causal, o,
+                                 cu.ctypes.data_as(ctypes.c_void_p),
+                                 sk.ctypes.data_as(ctypes.c_void_p), len(sk), hq, hk, d, bs, nb,
+                                 stride, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cu=[0, 1, 6], sk=[17, 4]), 1),          # Lk < Lq with causal
+    (dict(cu=[0, 1, 6], sk=[0, 40]), 1),          # Lq > 0, Lk = 0
+    (dict(cu=[1, 1, 6], sk=[17, 40]), 1),         # cu[0] != 0
+    (dict(cu=[0, 3, 2], sk=[17, 40]), 1),         # decreasing cu
+    (dict(cu=[0, 1, 6], sk=[17, 90]), 1),         # needs more pages than the table holds
+    (dict(cu=[0, 1, 6], sk=[17, 40], hq=6, hk=4), 2),   # Hq not a multiple of Hkv
+    (dict(cu=[0, 1, 6], sk=[17, 40], d=96), 2),   # unsupported head size
+    (dict(cu=[0, 1, 6], sk=[17, 40], bs=32), 2),  # unsupported block size
+    (dict(cu=[0, 1, 6], sk=[17, 40], ptr=0), 1),  # null device pointers
+    (dict(cu=[0, 1, 6], sk=[17, 40], ptr=8), 1),  # misaligned buffers
+    (dict(cu=[0, 1, 6], sk=[17, 40], scale=float("nan")), 1),
+    (dict(cu=[0, 1, 6], sk=[17, 40], nb=0), 1),
+])
+def test_invalid_arguments_rejected_before_any_launch(lib, kw, code):
+    assert _call(lib, **kw) == code
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert _call(lib, cu=[0], sk=[]) == 0
+    assert _call(lib, cu=[0, 0, 0], sk=[5, 9]) == 0      # two sequences, no new tokens
+
+
+def test_noncausal_allows_more_queries_than_keys(lib):
+    # passes validation; stops only when it needs the device (no GPU here)
+    cu = np.asarray([0, 5], np.int32)
+    sk = np.asarray([3], np.int32)
+    counts, _ = B.plan_inspect(cu, sk, 4, 2, 64, 1, causal=False)
+    assert counts["dec_pages"] > 0 or counts["prefill_tiles"] > 0
+    with pytest.raises(B.UAError):
+        B.plan_inspect(cu, sk, 4, 2, 64, 1, causal=True)

@@ -1,0 +1,138 @@
+"""The work-partition pass (host C++, through ua_plan_inspect; no GPU needed).
+
+Properties: every (sequence, kv head, packed query row) is in exactly one
+decode unit or prefill tile; each decode unit's pages [0, n) are covered by
+its pieces exactly once, in order; pieces of split units own distinct partial
+slots that the combine list names; decode CTAs get equal page counts (within
+one page); prefill tiles come longest first.
+"""
+import numpy as np
+import pytest
+
+from paged_varlen_attention_gb300 import _binding as B
+from paged_varlen_attention_gb300 import build_lib
+from paged_varlen_attention_gb300 import workloads as W
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build_lib.build()
+    B.load_library()
+
+
+def visible_pages(lq, lk, last_token, causal, bs=16):
+    kend = min(lk, lk - lq + last_token + 1) if causal else lk
+    return -(-kend // bs)
+
+
+def check_plan(q_lens, k_lens, hq, hk, d=128, causal=True, num_sms=152):
+    q_lens = np.asarray(q_lens, np.int64)
+    k_lens = np.asarray(k_lens, np.int64)
+    cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    stride = max(1, int(-(-k_lens.max() // 16)))
+    counts, items = B.plan_inspect(cu, k_lens.astype(np.int32), hq, hk, d, stride, causal,
+                                   num_sms=num_sms)
+    g = hq // hk
+    pieces = [(items[i], items[i + 1]) for i in range(len(items) - 1)
+              if items[i][0] == 0 and items[i + 1][0] == 1]
+    tiles = [r for r in items if r[0] == 2]
+    comb = [r for r in items if r[0] == 3]
+    assert len(pieces) == counts["pieces"]
+    assert len(tiles) == counts["prefill_tiles"]
+    assert len(comb) == counts["split_units"]
+
+    # rows covered exactly once
+    covered = {}
+    units = {}
+    for pc, ex in pieces:
+        _, cta, seq, kvh, row0, nrows, pb, pe = pc
+        units.setdefault((seq, kvh, row0, nrows), []).append((cta, pb, pe, ex[1]))
+    for key in units:
+        seq, kvh, row0, nrows = key
+        assert 1 <= nrows <= 16
+        for r in range(row0, row0 + nrows):
+            covered[(seq, kvh, r)] = covered.get((seq, kvh, r), 0) + 1
+    for t in tiles:
+        _, _, seq, kvh, row0, nrows, kvt, _ = t
+        assert 1 <= nrows <= 128
+        for r in range(row0, row0 + nrows):
+            covered[(seq, kvh, r)] = covered.get((seq, kvh, r), 0) + 1
+        last_token = (row0 + nrows - 1) // g
+        kend = min(k_lens[seq], k_lens[seq] - q_lens[seq] + last_token + 1) if causal else k_lens[seq]
+        assert kvt == -(-kend // 128)
+    expect = {(s, h, r) for s in range(len(q_lens)) for h in range(hk)
+              for r in range(int(q_lens[s]) * g)}
+    assert set(covered) == expect
+    assert all(v == 1 for v in covered.values())
+
+    # page coverage of each decode unit, slot bookkeeping
+    slots = []
+    comb_by_unit = {(c[1], c[2], c[3], c[4]): (c[5], c[6]) for c in comb}
+    total_pages = 0
+    for key, ps in units.items():
+        seq, kvh, row0, nrows = key
+        n = visible_pages(int(q_lens[seq]), int(k_lens[seq]), (row0 + nrows - 1) // g, causal)
+        total_pages += n
+        ranges = sorted((pb, pe) for _, pb, pe, _ in ps)
+        assert ranges[0][0] == 0 and ranges[-1][1] == n
+        for (a0, a1), (b0, b1) in zip(ranges, ranges[1:]):
+            assert a1 == b0
+        assert all(pe > pb for pb, pe in ranges)
+        if len(ps) == 1:
+            assert ps[0][3] == -1 and key not in comb_by_unit
+        else:
+            s0, ns = comb_by_unit[key]
+            assert ns == len(ps)
+            assert sorted(p[3] for p in ps) == list(range(s0, s0 + ns))
+            slots += [p[3] for p in ps]
+    assert len(slots) == len(set(slots)) == counts["slots"]
+    assert total_pages == counts["dec_pages"]
+
+    # balance across decode CTAs
+    if counts["dec_ctas"]:
+        per_cta = np.zeros(counts["dec_ctas"], np.int64)
+        for pc, _ in pieces:
+            per_cta[pc[1]] += pc[7] - pc[6]
+        assert per_cta.max() - per_cta.min() <= 1
+        assert counts["dec_ctas"] <= 2 * num_sms
+    # longest prefill tiles first
+    kv = [t[6] for t in tiles]
+    assert kv == sorted(kv, reverse=True)
+    return counts
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4])
+def test_standard_batches(idx):
+    s = W.config_spec(idx)
+    check_plan(s.q_lens, s.k_lens, s.num_q_heads, s.num_kv_heads, s.head_size, s.causal)
+
+
+def test_long_mixed_batch():
+    s = W.config_spec(5)
+    c = check_plan(s.q_lens, s.k_lens, s.num_q_heads, s.num_kv_heads, s.head_size, s.causal)
+    assert c["dec_ctas"] == 2 * 152
+
+
+@pytest.mark.parametrize("case", [
+    ([1], [1], 4, 4), ([1, 1], [16, 17], 8, 1), ([3, 0, 20], [3, 9, 40], 4, 2),
+    ([5], [100], 64, 2), ([7, 1], [7, 2], 6, 1), ([2, 2], [1, 2], 2, 1),
+])
+@pytest.mark.parametrize("num_sms", [1, 3, 152])
+@pytest.mark.parametrize("causal", [True, False])
+def test_small_shapes(case, num_sms, causal):
+    q, k, hq, hk = case
+    if causal and any(a > b for a, b in zip(q, k)):
+        pytest.skip("causal needs Lk >= Lq")
+    check_plan(q, k, hq, hk, 64, causal, num_sms)
+
+
+def test_random_batches():
+    rng = np.random.default_rng(7)
+    for _ in range(30):
+        n = int(rng.integers(1, 12))
+        q = rng.integers(0, 40, n)
+        k = q + rng.integers(0, 300, n)
+        k[(q == 0) & (k == 0)] = 1
+        hk = int(rng.choice([1, 2, 4, 8]))
+        hq = hk * int(rng.choice([1, 2, 3, 4, 8, 16]))
+        check_plan(q, k, hq, hk, 128, True, int(rng.integers(1, 200)))
