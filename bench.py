@@ -53,10 +53,6 @@ WORKLOADS = {
     "llama3_70b_long_mixed_32x8k-32k_2x2048chunk": 5,
 }
 DEFAULT_WORKLOAD = "llama3_8b_decode_64x2k-4k"
-KERNEL_SOURCES = {
-    "decode": "paged_varlen_attention_gb300/csrc/ua_decode.cu",
-    "prefill": "paged_varlen_attention_gb300/csrc/ua_prefill.cu",
-}
 
 
 def parse_args():
@@ -107,20 +103,24 @@ def measured_peaks():
             "source": "fallback"}
 
 
-def source_hash(rel):
-    with open(os.path.join(ROOT, rel), "rb") as fh:
-        return hashlib.sha256(fh.read()).hexdigest()[:16]
+def source_hash(paths):
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel, workload):
-    """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
+    """DRAM bytes per launch from the committed ncu record (profiles/ncu_traffic.json),
+    or None when the kernel's sources have changed since that capture."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as fh:
         entries = json.load(fh)
     e = entries.get(f"{kernel}:{workload}")
-    if not e or e.get("source_sha256_16") != source_hash(KERNEL_SOURCES[kernel]):
+    if not e or e.get("source_sha256_16") != source_hash(e.get("sources", [])):
         return None
     return float(e["dram_bytes_per_launch"])
 

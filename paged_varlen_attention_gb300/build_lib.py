@@ -23,7 +23,6 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libua_gb300.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-DEFINES = ["-DUA_PREFILL_ENABLED=0"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
               "--expt-relaxed-constexpr"]
 CXX_FLAGS = ["-O2", "-fPIC", "-std=c++17", "-Wall"]
@@ -58,10 +57,21 @@ def _compile(cmd, log_path):
     return log_path
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every CUDA / C++ source of the library; return the .so path."""
+def build(force: bool = False, verbose: bool = False, prefill=None) -> str:
+    """Compile every CUDA / C++ source of the library; return the .so path.
+
+    prefill=False builds a library whose planner sends every row tile to the
+    decode kernel (used to cross-check the two kernels against each other);
+    prefill=None keeps the setting of the existing build (on by default).
+    """
+    stamp = os.path.join(BUILD, "prefill_flag")
     os.makedirs(BUILD, exist_ok=True)
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
+    old_flag = open(stamp).read() if os.path.exists(stamp) else ""
+    if prefill is None:
+        prefill = old_flag != "-DUA_PREFILL_ENABLED=0"
+    defines = [f"-DUA_PREFILL_ENABLED={int(bool(prefill))}"]
+    if (not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime()
+            and old_flag == defines[0]):
         return LIB
     nvcc = _nvcc()
     cu, cpp = _sources()
@@ -70,14 +80,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
     for f in cu:
         obj = os.path.join(BUILD, f + ".o")
         objs.append(obj)
-        jobs.append(([nvcc, *ARCH, *NVCC_FLAGS, *DEFINES, "-I", INCLUDE, "-I", CSRC, "-c",
+        jobs.append(([nvcc, *ARCH, *NVCC_FLAGS, *defines, "-I", INCLUDE, "-I", CSRC, "-c",
                       os.path.join(CSRC, f), "-o", obj], obj + ".log"))
     cxx = os.environ.get("CXX", "g++")
     cuda_inc = os.path.join(os.path.dirname(os.path.dirname(nvcc)), "include")
     for f in cpp:
         obj = os.path.join(BUILD, f + ".o")
         objs.append(obj)
-        jobs.append(([cxx, *CXX_FLAGS, *DEFINES, "-I", INCLUDE, "-I", CSRC, "-I", cuda_inc, "-c",
+        jobs.append(([cxx, *CXX_FLAGS, *defines, "-I", INCLUDE, "-I", CSRC, "-I", cuda_inc, "-c",
                       os.path.join(CSRC, f), "-o", obj], obj + ".log"))
     with cf.ThreadPoolExecutor(max_workers=min(8, len(jobs))) as ex:
         logs = list(ex.map(lambda j: _compile(*j), jobs))
@@ -88,8 +98,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
     link = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lpthread", "-ldl", "-lrt"]
     _compile(link, os.path.join(BUILD, "link.log"))
     os.replace(tmp, LIB)
+    with open(stamp, "w") as fh:
+        fh.write(defines[0])
     return LIB
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    pf = False if "--no-prefill" in sys.argv else (True if "--prefill" in sys.argv else None)
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, prefill=pf))
