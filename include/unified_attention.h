@@ -166,6 +166,42 @@ ua_status ua_plan_inspect(const int32_t *cu_seqlens_q_host, const int32_t *sequs
 ua_status ua_profile_enable(int32_t enable);
 ua_status ua_profile_last(float *ms, int32_t *launches);
 
+/*
+ * unified_attention_no_alloc -- the same operation and arguments as
+ * unified_attention, minus the workspace: the launch plan and the split-KV
+ * partials go into a device array the library owns, so the caller never
+ * allocates device memory.  The pages have no counterpart to this entry
+ * point; it exists for callers that cannot call cudaMalloc or any other
+ * device allocator -- e.g. a plugin running inside a framework whose caching
+ * allocator owns all device memory and offers the plugin no way to borrow
+ * it, or a latency-critical path where an allocation could synchronise the
+ * device.  The caller still owns q, the caches, the metadata and out.
+ *
+ *   - The array holds UA_STATIC_WORKSPACE_BYTES (16 MiB).  Every GPU that
+ *     loads the library's module keeps that memory until the process exits.
+ *   - A batch whose workspace (as ua_workspace_size reports it) is larger
+ *     returns UA_ERR_WORKSPACE before anything is launched.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind.  Nothing in it needs to start at zero: each call writes the
+ *     plan and every partial before reading them.  Calls that overlap on the
+ *     GPU (different streams, not ordered by the caller) race on the array.
+ *   - No cudaMalloc, cudaFree or other allocating routine is called.
+ */
+#define UA_STATIC_WORKSPACE_BYTES ((size_t)16 << 20)
+
+ua_status unified_attention_no_alloc(const void *q, const void *k_cache, const void *v_cache,
+                                     const int32_t *cu_seqlens_q, const int32_t *seqused_k,
+                                     const int32_t *block_table, float softmax_scale,
+                                     int32_t causal, void *out,
+                                     const int32_t *cu_seqlens_q_host,
+                                     const int32_t *seqused_k_host, int32_t num_seqs,
+                                     int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t head_size, int32_t block_size, int32_t num_blocks,
+                                     int32_t block_table_stride, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
