@@ -155,16 +155,21 @@ ua_status ua_plan_inspect(const int32_t *cu_seqlens_q_host, const int32_t *sequs
                           int64_t items_cap, int64_t *n_items);
 
 /*
- * Per-kernel timing of the last call, for roofline figures.  When enabled,
- * unified_attention records CUDA events around each kernel it launches on the
- * caller's stream (events are created once per device and reused).
- * ua_profile_last synchronises on the last call's events and fills:
+ * Per-kernel timing, for roofline figures.  When enabled, unified_attention
+ * records CUDA events around each kernel it launches on the caller's stream,
+ * into a ring of UA_PROFILE_RING call slots per device (events are created
+ * once and reused), so a caller can time many calls without synchronising
+ * between them and read them afterwards.
+ * ua_profile_read(calls_back, ...) synchronises on that call's last event and
+ * fills, for the call calls_back calls before the latest (0 = latest):
  *   ms[0..3]       decode, prefill, combine kernel time and the plan copy
  *                  (-1 when that step did not run);
  *   launches[0..3] kernel launches of each kind (the copy counts as 0).
+ * calls_back must be below min(profiled calls, UA_PROFILE_RING).
  */
+#define UA_PROFILE_RING 64
 ua_status ua_profile_enable(int32_t enable);
-ua_status ua_profile_last(float *ms, int32_t *launches);
+ua_status ua_profile_read(int32_t calls_back, float *ms, int32_t *launches);
 
 /*
  * unified_attention_no_alloc -- the same operation and arguments as

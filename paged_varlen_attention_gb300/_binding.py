@@ -24,7 +24,7 @@ DEVICE_BAD_BLOCK_ID = 0x1
 DEVICE_WAIT_TIMEOUT = 0x2
 
 SYMBOLS = ("unified_attention", "ua_workspace_size", "ua_status_string", "ua_device_status",
-           "ua_plan_inspect", "ua_profile_enable", "ua_profile_last")
+           "ua_plan_inspect", "ua_profile_enable", "ua_profile_read")
 
 
 class UAError(RuntimeError):
@@ -67,8 +67,8 @@ def load_library():
         lib.ua_plan_inspect.restype = ctypes.c_int
         lib.ua_profile_enable.argtypes = [I32]
         lib.ua_profile_enable.restype = ctypes.c_int
-        lib.ua_profile_last.argtypes = [P, P]
-        lib.ua_profile_last.restype = ctypes.c_int
+        lib.ua_profile_read.argtypes = [I32, P, P]
+        lib.ua_profile_read.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -198,9 +198,11 @@ def profile_enable(on: bool = True):
     _check(load_library().ua_profile_enable(int(bool(on))), "ua_profile_enable")
 
 
-def profile_last():
-    """(ms[decode, prefill, combine, plan_copy], launches[...]) of the last call; -1 = not run."""
+def profile_read(calls_back: int = 0):
+    """(ms[decode, prefill, combine, plan_copy], launches[...]) of a profiled call
+    (0 = the latest, up to 63 back); -1 = that step did not run."""
     ms = np.zeros(4, dtype=np.float32)
     ln = np.zeros(4, dtype=np.int32)
-    _check(load_library().ua_profile_last(_np_ptr(ms), _np_ptr(ln)), "ua_profile_last")
+    _check(load_library().ua_profile_read(int(calls_back), _np_ptr(ms), _np_ptr(ln)),
+           "ua_profile_read")
     return ms.tolist(), ln.tolist()

@@ -11,6 +11,7 @@ from __future__ import annotations
 
 import concurrent.futures as cf
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -57,6 +58,33 @@ def _compile(cmd, log_path):
     return log_path
 
 
+# Register counts the kernels are written for (their warp roles and tiles
+# assume them); a build where ptxas picks another count is refused.
+LAUNCH_REGS = {"ua_prefill_kernel": 168}
+
+
+def _registers_by_kernel(log_text: str) -> dict:
+    out, current = {}, None
+    for line in log_text.splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            current = m.group(1)
+            continue
+        m = re.search(r"Used (\d+) registers", line)
+        if m and current:
+            out[current] = int(m.group(1))
+    return out
+
+
+def _check_launch_registers(log_path: str):
+    regs = _registers_by_kernel(open(log_path).read())
+    for mangled, n in regs.items():
+        for name, want in LAUNCH_REGS.items():
+            if name in mangled and n != want:
+                raise RuntimeError(f"{name}: ptxas chose {n} registers per thread, the "
+                                   f"kernel is laid out for {want}; refusing to build")
+
+
 def build(force: bool = False, verbose: bool = False, prefill=None) -> str:
     """Compile every CUDA / C++ source of the library; return the .so path.
 
@@ -94,6 +122,8 @@ def build(force: bool = False, verbose: bool = False, prefill=None) -> str:
     if verbose:
         for lg in logs:
             sys.stdout.write(open(lg).read())
+    for lg in logs:
+        _check_launch_registers(lg)
     tmp = LIB + ".tmp"
     link = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lpthread", "-ldl", "-lrt"]
     _compile(link, os.path.join(BUILD, "link.log"))

@@ -37,11 +37,12 @@ struct DeviceState {
     int sms = 0;
     int *status = nullptr;             // device address of g_ua_device_status
     bool events = false;
-    cudaEvent_t ev[5] = {};            // plan copy | decode | prefill | combine
-    // what the last profiled call ran
-    bool ran[4] = {false, false, false, false};
-    int launches[4] = {0, 0, 0, 0};
-    bool profiled = false;
+    // profiling ring: per call, events before the plan copy, after it, after
+    // decode, after prefill, after combine; what ran and how many launches
+    cudaEvent_t ev[UA_PROFILE_RING][5] = {};
+    bool ran[UA_PROFILE_RING][4] = {};
+    int launches[UA_PROFILE_RING][4] = {};
+    int64_t calls = 0;                 // profiled calls so far
 };
 
 static std::mutex g_mutex;
@@ -103,6 +104,27 @@ static bool encode_map(CUtensorMap *map, const void *base, uint64_t inner, uint6
     cuuint32_t box[3] = {64, box_mid, box_outer};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// 5-D bf16 map over the paged cache [num_blocks][16][Hkv][D] viewed as
+// (64 columns, 16 slots, D/64 chunks, Hkv, blocks): one box {64, 16, D/64, 1, 1}
+// is one 16-token page of one KV head, laid out [chunk][slot][64] in shared
+// memory with the 128-byte swizzle.  Out-of-range blocks read zeros.
+static bool encode_page_map(CUtensorMap *map, const void *base, int d, int hkv,
+                            uint64_t num_blocks) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const uint64_t row = (uint64_t)hkv * d * 2;   // bytes between slots
+    cuuint64_t dims[5] = {64, (cuuint64_t)kBlockSize, (cuuint64_t)(d / 64), (cuuint64_t)hkv,
+                          num_blocks};
+    cuuint64_t strides[4] = {row, 128, (cuuint64_t)d * 2, row * kBlockSize};
+    cuuint32_t box[5] = {64, (cuuint32_t)kBlockSize, (cuuint32_t)(d / 64), 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -176,7 +198,7 @@ extern "C" ua_status ua_plan_inspect(const int32_t *cu_seqlens_q_host,
                               num_kv_heads, head_size, block_size, block_table_stride, causal);
     int v = validate_problem(pr);
     if (v) return static_cast<ua_status>(v);
-    Plan plan;
+    thread_local Plan plan;
     build_plan(pr, num_sms, kPrefillEnabled, plan);
     counts[0] = plan.dec_ctas;
     counts[1] = (int32_t)plan.pieces.size();
@@ -242,33 +264,32 @@ extern "C" ua_status ua_profile_enable(int32_t enable) {
     return UA_OK;
 }
 
-extern "C" ua_status ua_profile_last(float *ms, int32_t *launches) {
+extern "C" ua_status ua_profile_read(int32_t calls_back, float *ms, int32_t *launches) {
     if (!ms || !launches) return UA_ERR_INVALID_ARG;
     DeviceState *ds = nullptr;
     ua_status st = device_state(&ds);
     if (st != UA_OK) return st;
-    for (int i = 0; i < 4; ++i) {
-        ms[i] = -1.f;
-        launches[i] = 0;
-    }
-    if (!ds->profiled) return UA_OK;
-    if (cudaEventSynchronize(ds->ev[4]) != cudaSuccess) {
+    if (calls_back < 0 || calls_back >= std::min<int64_t>(ds->calls, UA_PROFILE_RING))
+        return UA_ERR_INVALID_ARG;
+    const int slot = (int)((ds->calls - 1 - calls_back) % UA_PROFILE_RING);
+    if (cudaEventSynchronize(ds->ev[slot][4]) != cudaSuccess) {
         cudaGetLastError();
         return UA_ERR_CUDA;
     }
-    // ev[0] before the plan copy, ev[1] after it, ev[2] after decode,
-    // ev[3] after prefill, ev[4] after combine.
+    // ev 0 before the plan copy, 1 after it, 2 after decode, 3 after prefill, 4 after combine
     const int from[4] = {1, 2, 3, 0};
     const int to[4] = {2, 3, 4, 1};
     for (int i = 0; i < 4; ++i) {
-        if (!ds->ran[i]) continue;
+        ms[i] = -1.f;
+        launches[i] = 0;
+        if (!ds->ran[slot][i]) continue;
         float t = 0.f;
-        if (cudaEventElapsedTime(&t, ds->ev[from[i]], ds->ev[to[i]]) != cudaSuccess) {
+        if (cudaEventElapsedTime(&t, ds->ev[slot][from[i]], ds->ev[slot][to[i]]) != cudaSuccess) {
             cudaGetLastError();
             return UA_ERR_CUDA;
         }
         ms[i] = t;
-        launches[i] = ds->launches[i];
+        launches[i] = ds->launches[slot][i];
     }
     return UA_OK;
 }
@@ -316,29 +337,33 @@ extern "C" ua_status unified_attention(const void *q, const void *k_cache, const
     }
     serialize_plan(plan, blob);
 
-    // ---- tensor maps: K/V as [num_blocks * block_size, Hkv, D], Q as [total_q, Hq, D]
+    // ---- tensor maps: K/V page views (5-D), Q as [total_q, Hq, D]
     const int g = num_q_heads / num_kv_heads;
-    const uint64_t tokens = (uint64_t)num_blocks * block_size;
-    CUtensorMap tm_k, tm_v, tm_q;
-    if (!encode_map(&tm_k, k_cache, head_size, num_kv_heads, tokens, 1, kBlockSize) ||
-        !encode_map(&tm_v, v_cache, head_size, num_kv_heads, tokens, 1, kBlockSize))
+    CUtensorMap tm_kp, tm_vp, tm_q, tm_k3;
+    if (!encode_page_map(&tm_kp, k_cache, head_size, num_kv_heads, (uint64_t)num_blocks) ||
+        !encode_page_map(&tm_vp, v_cache, head_size, num_kv_heads, (uint64_t)num_blocks))
         return UA_ERR_CUDA;
+    // prefill: Q tiles, and K as [num_blocks * 16, Hkv, D] with one box per 64 columns
     if (!plan.tiles.empty() &&
-        !encode_map(&tm_q, q, head_size, num_q_heads, (uint64_t)total_q, g, kPreRows / g))
+        (!encode_map(&tm_q, q, head_size, num_q_heads, (uint64_t)total_q, g, kPreRows / g) ||
+         !encode_map(&tm_k3, k_cache, head_size, num_kv_heads,
+                     (uint64_t)num_blocks * block_size, 1, kBlockSize)))
         return UA_ERR_CUDA;
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const bool prof = g_profile;
     if (prof && !ds->events) {
-        for (int i = 0; i < 5; ++i)
-            if (cudaEventCreate(&ds->ev[i]) != cudaSuccess) {
-                cudaGetLastError();
-                return UA_ERR_CUDA;
-            }
+        for (int c = 0; c < UA_PROFILE_RING; ++c)
+            for (int i = 0; i < 5; ++i)
+                if (cudaEventCreate(&ds->ev[c][i]) != cudaSuccess) {
+                    cudaGetLastError();
+                    return UA_ERR_CUDA;
+                }
         ds->events = true;
     }
+    const int pslot = (int)(ds->calls % UA_PROFILE_RING);
     auto mark = [&](int i) {
-        if (prof) cudaEventRecord(ds->ev[i], stream);
+        if (prof) cudaEventRecord(ds->ev[pslot][i], stream);
     };
     const float scale_log2 = softmax_scale * 1.4426950408889634f;
 
@@ -370,12 +395,13 @@ extern "C" ua_status unified_attention(const void *q, const void *k_cache, const
         dp.part_o = reinterpret_cast<float *>(ws + L.off_part_o);
         dp.part_ml = reinterpret_cast<float *>(ws + L.off_part_ml);
         dp.status = ds->status;
-        e = launch_decode(head_size, dp, tm_k, tm_v, plan.dec_ctas, stream);
+        e = launch_decode(head_size, dp, tm_kp, tm_vp, plan.dec_ctas, stream);
         if (e != cudaSuccess) return UA_ERR_CUDA;
     }
     mark(2);
     if (!plan.tiles.empty()) {
         PrefillParams pp{};
+        pp.k_cache = static_cast<const __nv_bfloat16 *>(k_cache);
         pp.out = static_cast<__nv_bfloat16 *>(out);
         pp.cu = cu_seqlens_q;
         pp.seqused_k = seqused_k;
@@ -390,7 +416,7 @@ extern "C" ua_status unified_attention(const void *q, const void *k_cache, const
         pp.tiles = reinterpret_cast<const PreTile *>(ws + L.off_tiles);
         pp.n_tiles = (int32_t)plan.tiles.size();
         pp.status = ds->status;
-        e = launch_prefill(head_size, pp, tm_q, tm_k, tm_v, plan.pre_ctas, stream);
+        e = launch_prefill(head_size, pp, tm_q, tm_k3, tm_vp, plan.pre_ctas, stream);
         if (e != cudaSuccess) return UA_ERR_CUDA;
     }
     mark(3);
@@ -409,15 +435,15 @@ extern "C" ua_status unified_attention(const void *q, const void *k_cache, const
     mark(4);
     if (prof) {
         std::lock_guard<std::mutex> lock(g_mutex);
-        ds->ran[0] = plan.dec_ctas > 0;
-        ds->ran[1] = !plan.tiles.empty();
-        ds->ran[2] = !plan.comb.empty();
-        ds->ran[3] = L.blob_bytes > 0;
-        ds->launches[0] = plan.dec_ctas > 0 ? 1 : 0;
-        ds->launches[1] = plan.tiles.empty() ? 0 : 1;
-        ds->launches[2] = plan.comb.empty() ? 0 : 1;
-        ds->launches[3] = 0;
-        ds->profiled = true;
+        ds->ran[pslot][0] = plan.dec_ctas > 0;
+        ds->ran[pslot][1] = !plan.tiles.empty();
+        ds->ran[pslot][2] = !plan.comb.empty();
+        ds->ran[pslot][3] = L.blob_bytes > 0;
+        ds->launches[pslot][0] = plan.dec_ctas > 0 ? 1 : 0;
+        ds->launches[pslot][1] = plan.tiles.empty() ? 0 : 1;
+        ds->launches[pslot][2] = plan.comb.empty() ? 0 : 1;
+        ds->launches[pslot][3] = 0;
+        ++ds->calls;
     }
     return UA_OK;
 }

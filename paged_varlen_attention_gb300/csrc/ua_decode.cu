@@ -11,7 +11,8 @@
 // Structure (one persistent CTA = 4 consumer warps + 1 producer warp):
 //   * the producer walks the CTA's pieces (contiguous page ranges of
 //     (sequence, kv head, row tile) units), reads 32 block-table entries at a
-//     time, and issues one TMA load per 64-column chunk of each K and V page
+//     time, and issues one TMA box per K page and one per V page (a 5-D view
+//     of the cache, so one box holds all D columns of the page's 16 tokens)
 //     into a ring of shared-memory stages (128-byte swizzle);
 //   * consumer warp w takes pages w, w+4, ... of each piece: S = Q K^T with
 //     mma.sync m16n8k16 (bf16 in, fp32 accumulate), bottom-right causal mask,
@@ -104,13 +105,10 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
                             const uint32_t kdst = stage0 + st * C::kStageBytes;
                             const uint32_t vdst = kdst + C::kPageBytes;
                             mbar_arrive_expect_tx(fb, C::kStageBytes);
-#pragma unroll
-                            for (int c = 0; c < C::kChunks; ++c) {
-                                tma_load_3d_hint(kdst + c * 2048, &tm_k, c * 64, pc.kvh,
-                                                 b * kBlockSize, fb, policy);
-                                tma_load_3d_hint(vdst + c * 2048, &tm_v, c * 64, pc.kvh,
-                                                 b * kBlockSize, fb, policy);
-                            }
+                            // one box per page and tensor: all D columns of 16 tokens,
+                            // laid out [chunk][slot][64] with the 128-byte swizzle
+                            tma_load_5d_hint(kdst, &tm_k, 0, 0, 0, pc.kvh, b, fb, policy);
+                            tma_load_5d_hint(vdst, &tm_v, 0, 0, 0, pc.kvh, b, fb, policy);
                         }
                     }
                     ok = __shfl_sync(0xffffffffu, good, 0) != 0;

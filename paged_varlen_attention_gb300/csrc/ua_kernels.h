@@ -40,6 +40,7 @@ struct CombineParams {
 };
 
 struct PrefillParams {
+    const __nv_bfloat16 *k_cache;   // read directly by the K loaders (cp.async)
     __nv_bfloat16 *out;
     const int32_t *cu;
     const int32_t *seqused_k;

@@ -16,8 +16,9 @@
 //     every SM streams the same number of pages (split-KV).  A unit cut into
 //     several pieces writes fp32 partials that the combine kernel merges with
 //     a log-sum-exp rule.
-//   * prefill tiles -- (sequence, kv head, 128-row tile) for the rest, one
-//     tensor-core tile of 128 packed rows each, longest first.
+//   * prefill tiles -- (sequence, kv head, 256-row tile) for the rest: two
+//     128-row tensor-core tiles that share every K/V tile they load, longest
+//     first.
 //
 // Rows are packed (token, head-in-group) pairs: packed row r of a (sequence,
 // kv head) is token r / G and query head kv_head * G + r % G.
@@ -35,7 +36,8 @@ namespace ua {
 
 constexpr int kBlockSize = 16;      // tokens per KV page (the supported page size)
 constexpr int kDecRows = 16;        // packed rows per decode tile (warp MMA M)
-constexpr int kPreRows = 128;       // packed rows per prefill tile (tcgen05 M)
+constexpr int kPreRows = 128;       // packed rows per tcgen05 tile (MMA M)
+constexpr int kPreTileRows = 256;   // packed rows per prefill work item (two MMA tiles)
 constexpr int kKvTile = 128;        // keys per prefill KV tile (8 pages)
 constexpr int kDecCtasPerSm = 2;    // resident decode CTAs per SM
 constexpr size_t kAlign = 256;
@@ -62,12 +64,12 @@ struct alignas(16) CombUnit {   // a decode unit split over several pieces
     int32_t pad1;
 };
 
-struct alignas(16) PreTile {    // one 128-row prefill tile
+struct alignas(16) PreTile {    // one prefill work item: up to two 128-row MMA tiles
     int32_t seq;
     int32_t kvh;
     int32_t row0;
     int32_t nrows;
-    int32_t kv_tiles;    // 128-key tiles it visits
+    int32_t kv_tiles;    // 128-key tiles its last row visits
     int32_t pad0;
     int32_t pad1;
     int32_t pad2;

@@ -68,40 +68,54 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
     struct Unit {
         int32_t seq, kvh, row0, nrows, pages;
     };
-    std::vector<Unit> units;
+    // scratch kept per thread; bound to plain references once (each access to a
+    // thread_local object with a constructor goes through an init check)
+    thread_local std::vector<Unit> tl_units;
+    thread_local std::vector<PreTile> tl_unsorted;
+    thread_local std::vector<int32_t> tl_counts;
+    std::vector<Unit> &units = tl_units;
+    std::vector<PreTile> &unsorted = tl_unsorted;
+    std::vector<int32_t> &counts = tl_counts;
+    units.clear();
+    unsorted.clear();
+    int32_t max_kv = 0;
+    // 32-bit arithmetic below: validate_problem bounds Lq * G and Lk well inside int32
     for (int s = 0; s < p.num_seqs; ++s) {
-        const int64_t lq = (int64_t)p.cu[s + 1] - p.cu[s];
-        const int64_t lk = p.lk[s];
+        const int32_t lq = p.cu[s + 1] - p.cu[s];
+        const int32_t lk = p.lk[s];
         if (lq == 0) continue;
-        const int64_t rows = lq * g;
+        const int32_t rows = lq * g;
         const bool decode = rows <= kDecRows || !pre_ok;
-        if (decode) {
-            for (int h = 0; h < p.hkv; ++h)
-                for (int64_t r0 = 0; r0 < rows; r0 += kDecRows) {
-                    const int64_t nr = std::min<int64_t>(kDecRows, rows - r0);
-                    const int64_t kend = tile_key_end(p, lq, lk, r0 + nr - 1, g);
-                    units.push_back({s, h, (int32_t)r0, (int32_t)nr,
-                                     (int32_t)((kend + p.bs - 1) / p.bs)});
-                }
-        } else {
-            for (int h = 0; h < p.hkv; ++h)
-                for (int64_t r0 = 0; r0 < rows; r0 += kPreRows) {
-                    const int64_t nr = std::min<int64_t>(kPreRows, rows - r0);
-                    const int64_t kend = tile_key_end(p, lq, lk, r0 + nr - 1, g);
-                    PreTile t{};
-                    t.seq = s;
+        const int32_t step = decode ? kDecRows : kPreTileRows;
+        // visible keys of the last row of each row tile; the same for every kv head
+        for (int32_t r0 = 0; r0 < rows; r0 += step) {
+            const int32_t nr = std::min<int32_t>(step, rows - r0);
+            const int32_t kend = p.causal ? std::min<int32_t>(lk, lk - lq + (r0 + nr - 1) / g + 1) : lk;
+            if (decode) {
+                const int32_t pages = (kend + kBlockSize - 1) / kBlockSize;
+                for (int h = 0; h < p.hkv; ++h) units.push_back({s, h, r0, nr, pages});
+            } else {
+                PreTile t{};
+                t.seq = s;
+                t.row0 = r0;
+                t.nrows = nr;
+                t.kv_tiles = (kend + kKvTile - 1) / kKvTile;
+                max_kv = std::max(max_kv, t.kv_tiles);
+                for (int h = 0; h < p.hkv; ++h) {
                     t.kvh = h;
-                    t.row0 = (int32_t)r0;
-                    t.nrows = (int32_t)nr;
-                    t.kv_tiles = (int32_t)((kend + kKvTile - 1) / kKvTile);
-                    plan.tiles.push_back(t);
+                    unsorted.push_back(t);
                 }
+            }
         }
     }
-
-    // ---- prefill: longest first (stable, so equal lengths keep batch order)
-    std::stable_sort(plan.tiles.begin(), plan.tiles.end(),
-                     [](const PreTile &a, const PreTile &b) { return a.kv_tiles > b.kv_tiles; });
+    // ---- prefill: longest first; equal lengths keep batch order (counting sort)
+    if (!unsorted.empty()) {
+        counts.assign((size_t)max_kv + 2, 0);
+        for (const PreTile &t : unsorted) ++counts[(size_t)(max_kv - t.kv_tiles) + 1];
+        for (size_t b = 1; b < counts.size(); ++b) counts[b] += counts[b - 1];
+        plan.tiles.resize(unsorted.size());
+        for (const PreTile &t : unsorted) plan.tiles[(size_t)counts[(size_t)(max_kv - t.kv_tiles)]++] = t;
+    }
     plan.pre_ctas = (int32_t)std::min<size_t>(plan.tiles.size(), (size_t)std::max(num_sms, 1));
 
     // ---- decode: equal page ranges over the concatenated units
@@ -113,56 +127,9 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
         const int64_t ctas = std::min<int64_t>(want, total);
         plan.dec_ctas = (int32_t)ctas;
         plan.cta_begin.assign(ctas + 1, 0);
-        // pieces per unit, gathered first so slots can be assigned per unit
-        std::vector<std::vector<DecPiece>> per_unit(units.size());
+        counts.assign(units.size(), 0);              // pieces per unit
         size_t ui = 0;
-        int64_t unit_start = 0;   // global page index of units[ui]'s first page
-        for (int64_t c = 0; c < ctas; ++c) {
-            const int64_t lo = total * c / ctas;
-            const int64_t hi = total * (c + 1) / ctas;
-            int64_t pos = lo;
-            while (pos < hi) {
-                while (unit_start + units[ui].pages <= pos) {
-                    unit_start += units[ui].pages;
-                    ++ui;
-                }
-                const Unit &u = units[ui];
-                const int64_t b = pos - unit_start;
-                const int64_t e = std::min<int64_t>(u.pages, hi - unit_start);
-                DecPiece pc{};
-                pc.seq = u.seq;
-                pc.kvh = u.kvh;
-                pc.row0 = u.row0;
-                pc.nrows = u.nrows;
-                pc.page_begin = (int32_t)b;
-                pc.page_end = (int32_t)e;
-                pc.slot = -1;
-                pc.unit = (int32_t)ui;
-                // remember which CTA owns it through the order of emission
-                per_unit[ui].push_back(pc);
-                pos = unit_start + e;
-            }
-        }
-        // slots for split units
-        int32_t slot = 0;
-        for (size_t u = 0; u < units.size(); ++u) {
-            if (per_unit[u].size() > 1) {
-                CombUnit cu{};
-                cu.seq = units[u].seq;
-                cu.kvh = units[u].kvh;
-                cu.row0 = units[u].row0;
-                cu.nrows = units[u].nrows;
-                cu.slot_begin = slot;
-                cu.nslots = (int32_t)per_unit[u].size();
-                plan.comb.push_back(cu);
-                for (DecPiece &pc : per_unit[u]) pc.slot = slot++;
-            }
-        }
-        plan.n_slots = slot;
-        // emit pieces in CTA order (re-walk the same partition)
-        std::vector<size_t> next(units.size(), 0);
-        ui = 0;
-        unit_start = 0;
+        int64_t unit_start = 0;                      // global page index of units[ui]'s first page
         for (int64_t c = 0; c < ctas; ++c) {
             plan.cta_begin[c] = (int32_t)plan.pieces.size();
             const int64_t lo = total * c / ctas;
@@ -173,12 +140,43 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
                     unit_start += units[ui].pages;
                     ++ui;
                 }
-                const int64_t e = std::min<int64_t>(units[ui].pages, hi - unit_start);
-                plan.pieces.push_back(per_unit[ui][next[ui]++]);
+                const Unit &u = units[ui];
+                const int64_t e = std::min<int64_t>(u.pages, hi - unit_start);
+                DecPiece pc{};
+                pc.seq = u.seq;
+                pc.kvh = u.kvh;
+                pc.row0 = u.row0;
+                pc.nrows = u.nrows;
+                pc.page_begin = (int32_t)(pos - unit_start);
+                pc.page_end = (int32_t)e;
+                pc.slot = counts[ui]++;              // index among the unit's pieces for now
+                pc.unit = (int32_t)ui;
+                plan.pieces.push_back(pc);
                 pos = unit_start + e;
             }
         }
         plan.cta_begin[ctas] = (int32_t)plan.pieces.size();
+        // split units get consecutive partial slots, in unit order
+        int32_t slot = 0;
+        for (size_t u = 0; u < units.size(); ++u) {
+            if (counts[u] > 1) {
+                CombUnit cu{};
+                cu.seq = units[u].seq;
+                cu.kvh = units[u].kvh;
+                cu.row0 = units[u].row0;
+                cu.nrows = units[u].nrows;
+                cu.slot_begin = slot;
+                cu.nslots = counts[u];
+                plan.comb.push_back(cu);
+                counts[u] = slot;                    // now: first slot of the unit
+                slot += cu.nslots;
+            } else {
+                counts[u] = -1;                      // whole unit in one piece
+            }
+        }
+        plan.n_slots = slot;
+        for (DecPiece &pc : plan.pieces)
+            pc.slot = counts[pc.unit] < 0 ? -1 : counts[pc.unit] + pc.slot;
     }
 
     // ---- workspace layout

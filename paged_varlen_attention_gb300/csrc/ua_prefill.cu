@@ -1,29 +1,35 @@
 // ua_prefill.cu -- tensor-core prefill / chunked-prefill kernel (tcgen05 + TMEM + TMA).
 //
 // Query runs longer than one 16-row tile go here.  The query heads that share
-// a KV head are stacked along M, so one 128-row tile holds 128/G tokens x G
-// heads and every K/V tile loaded from the paged cache feeds all of them
+// a KV head are stacked along M, so one 128-row MMA tile holds 128/G tokens x
+// G heads and every K/V tile loaded from the paged cache feeds all of them
 // (the GQA packing of "[Kernel] Unified Triton kernel that doesn't
 // distinguish between prefill + decode", vLLM PR #16828, PR description,
 // there done "to ensure the Tensor cores are well used").
 //
-// One persistent CTA per SM walks its 128-row tiles (longest first).  Roles:
-//   warp 0    TMA producer: the Q tile (box {64, G, 128/G} of [T, Hq, D]) and,
-//             per 128-key tile, eight 16-token pages of K and of V
-//             (box {64, 1, 16} of [pages*16, Hkv, D]), 128-byte swizzled;
-//             pages past the tile's last visible key are read out of bounds,
-//             which fills zeros.
-//   warp 1    allocates TMEM and issues the MMAs from one thread:
-//               S[e%2] = Q K_e^T      (M 128, N 128, K D; both operands K-major)
-//               O     += P_e V_e      (A = P in TMEM as bf16, B = V MN-major)
-//             in the order S0, S1, PV0, S2, PV1, ... so that the scores of
-//             tile e+1 are computed while the softmax of tile e runs.
-//   warps 2-5 softmax, one thread per row (TMEM lane): scale into the log2
-//             domain, bottom-right causal mask, row max, exp2, row sum, P as
-//             bf16 written over S in TMEM.  O is rescaled only when a row max
-//             grows by more than 2^8 (the stale max cancels in O / l); the
-//             epilogue divides by l and writes bf16 rows.
-// Every wait is bounded (see ua_device.cuh); TMEM is always freed.
+// One persistent CTA per SM walks its work items (longest first).  A work item
+// is a pair of 128-row MMA tiles, A and B, of the same (sequence, KV head):
+// both use every K/V tile the CTA loads, and their softmax steps run at the
+// same time on two warpgroups, which hides each other's latency.  Roles:
+//   warps 0-3 softmax of tile A, one thread per row (TMEM lane)
+//   warps 4-7 softmax of tile B
+//             scale into the log2 domain, bottom-right causal mask, row max,
+//             exp2, row sum, P as bf16 written over S in TMEM; O is rescaled
+//             only when a row max grows by more than 2^8 (the stale max
+//             cancels in O / l); the epilogue divides by l and writes bf16.
+//   warp 8    allocates TMEM (S_A, O_A, S_B, O_B: 4 x 128 columns) and issues
+//             the MMAs from one thread, per 128-key tile j:
+//               S_X = Q_X K_j^T   (M 128, N 128, K D; both operands K-major)
+//               O_X += P_X V_j    (A = P in TMEM as bf16, B = V MN-major)
+//   warp 9    TMA producer of the Q tiles (box {64, G, 128/G} of [T, Hq, D])
+//             and of V: one box per 16-token page (a 5-D view of the cache,
+//             so one box holds all D columns of the page), page-major.
+//   warp 10   TMA producer of K: two boxes per page ({64, 1, 16} of
+//             [pages*16, Hkv, D]), into [chunk][key][64] so that each 64-wide
+//             column chunk of the 128-key tile is one K-major operand.
+// Pages past a tile's last visible key are read out of bounds (zero fill)
+// instead of from the block table.  Every wait is bounded (see
+// ua_device.cuh); TMEM is always freed.
 #include "ua_device.cuh"
 #include "ua_kernels.h"
 
@@ -34,77 +40,108 @@ struct PreCfg {
     static constexpr int kChunks = D / 64;
     static constexpr int kQBytes = kPreRows * D * 2;          // one 128-row Q tile
     static constexpr int kKvBytes = kKvTile * D * 2;          // one 128-key K (or V) tile
-    static constexpr int kChunkBytes = kKvTile * 128;         // 128 rows x 64 columns
-    static constexpr int kThreads = 192;
+    static constexpr int kChunkBytes = kKvTile * 128;         // K: 128 rows x 64 columns
+    static constexpr int kPageBytes = kBlockSize * D * 2;     // V: one 16-token page
+    static constexpr int kThreads = 352;                      // 11 warps: 3 per SMSP, 168 regs
+    static constexpr int kKStages = 3;
+    static constexpr int kVStages = 2;
     static constexpr int kTmemCols = 512;
-    static constexpr uint32_t kColS0 = 0;
-    static constexpr uint32_t kColS1 = 128;
-    static constexpr uint32_t kColO = 256;
-    // Q x2, K x2, V x2, barriers; padded so one CTA owns the SM (and its TMEM)
-    static constexpr size_t kUsed = 1024 + 2 * (size_t)kQBytes + 4 * (size_t)kKvBytes + 256;
+    static constexpr uint32_t kColS = 0;                      // + 256 * sub-tile
+    static constexpr uint32_t kColO = 128;
+    // Q x2 (A, B), K x3, V x2, barriers; one CTA owns the SM (and its TMEM)
+    static constexpr size_t kUsed = 1024 + 2 * (size_t)kQBytes +
+                                    (size_t)(kKStages + kVStages) * kKvBytes + 512;
     static constexpr size_t kSmemBytes = kUsed < 120 * 1024 ? 120 * 1024 : kUsed;
     static constexpr float kRescaleThreshold = 8.0f;          // log2 units
 };
 
-// mbarrier slots
+// mbarrier slots ([2] = one per sub-tile A/B unless noted)
 enum : int {
     kBarQFull = 0,      // [2]
     kBarQEmpty = 2,     // [2]
-    kBarKFull = 4,      // [2]
-    kBarKEmpty = 6,     // [2]
-    kBarVFull = 8,      // [2]
-    kBarVEmpty = 10,    // [2]
-    kBarSFull = 12,     // [2]
-    kBarPFull = 14,     // [2]
-    kBarSFree = 16,     // [2]
-    kBarPvDone = 18,
-    kBarOFull = 19,
+    kBarKFull = 4,      // [3] K stages
+    kBarKEmpty = 7,     // [3]
+    kBarVFull = 10,     // [2] V stages
+    kBarVEmpty = 12,    // [2]
+    kBarSFull = 14,     // [2]
+    kBarPFull = 16,     // [2] (128 arrivals)
+    kBarPvDone = 18,    // [2]
     kBarDrain = 20,
     kNumBars = 21
 };
 
-struct TileInfo {
-    int q0, lq, lk, kvh, row0, nrows, n;
-    int kend_max;   // keys visible to the last row of the tile
-    int kend_lo;    // keys visible to the first row of the tile
+struct SubInfo {
+    int row0, nrows, n;      // packed rows of this 128-row sub-tile; its KV tiles
+    int kend_max, kend_lo;   // keys visible to its last / first row
 };
 
-__device__ __forceinline__ TileInfo load_tile(const PrefillParams &p, int t) {
+struct PairInfo {
+    int seq, q0, lq, lk, kvh, n;   // n: KV tiles of the pair (= max over sub-tiles)
+    SubInfo sub[2];
+};
+
+__device__ __forceinline__ int visible_keys(const PrefillParams &p, int lq, int lk, int row) {
+    if (!p.causal) return lk;
+    return min(lk, lk - lq + row / p.g + 1);
+}
+
+__device__ __forceinline__ PairInfo load_pair(const PrefillParams &p, int t) {
     const PreTile pt = p.tiles[t];
-    TileInfo ti;
-    ti.q0 = p.cu[pt.seq];
-    ti.lq = p.cu[pt.seq + 1] - ti.q0;
-    ti.lk = p.seqused_k[pt.seq];
-    ti.kvh = pt.kvh;
-    ti.row0 = pt.row0;
-    ti.nrows = pt.nrows;
-    ti.n = pt.kv_tiles;
-    if (p.causal) {
-        const int i_last = (pt.row0 + pt.nrows - 1) / p.g;
-        const int i_first = pt.row0 / p.g;
-        ti.kend_max = min(ti.lk, ti.lk - ti.lq + i_last + 1);
-        ti.kend_lo = min(ti.lk, ti.lk - ti.lq + i_first + 1);
-    } else {
-        ti.kend_max = ti.lk;
-        ti.kend_lo = ti.lk;
+    PairInfo pi;
+    pi.seq = pt.seq;
+    pi.q0 = p.cu[pt.seq];
+    pi.lq = p.cu[pt.seq + 1] - pi.q0;
+    pi.lk = p.seqused_k[pt.seq];
+    pi.kvh = pt.kvh;
+    pi.n = 0;
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+        SubInfo &s = pi.sub[x];
+        s.row0 = pt.row0 + x * kPreRows;
+        s.nrows = max(0, min(kPreRows, pt.nrows - x * kPreRows));
+        if (s.nrows > 0) {
+            s.kend_max = visible_keys(p, pi.lq, pi.lk, s.row0 + s.nrows - 1);
+            s.kend_lo = visible_keys(p, pi.lq, pi.lk, s.row0);
+            s.n = (s.kend_max + kKvTile - 1) / kKvTile;
+        } else {
+            s.kend_max = s.kend_lo = 0;
+            s.n = 0;
+        }
+        pi.n = max(pi.n, s.n);
     }
-    return ti;
+    return pi;
+}
+
+// Block ids of the 8 pages of KV tile j (lanes 0-7 load; out-of-range or
+// not-needed pages give num_blocks, which TMA reads as zeros).
+__device__ __forceinline__ int tile_block_id(const PrefillParams &p, const int32_t *bt_row, int j,
+                                             int kend, int lane) {
+    int bid = p.num_blocks;
+    const int page = j * (kKvTile / kBlockSize) + lane;
+    if (lane < kKvTile / kBlockSize && page * kBlockSize < kend) {
+        bid = __ldg(bt_row + page);
+        if (bid < 0 || bid >= p.num_blocks) {
+            record_status(p.status, UA_DEVICE_BAD_BLOCK_ID_BIT);
+            bid = p.num_blocks;
+        }
+    }
+    return bid;
 }
 
 template <int D>
 __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
     ua_prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v) {
+                      const __grid_constant__ CUtensorMap tm_vp) {
     using C = PreCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t sq = smem_u32(smem);                         // Q[2]
-    const uint32_t sk = sq + 2 * C::kQBytes;                    // K[2]
-    const uint32_t sv = sk + 2 * C::kKvBytes;                   // V[2]
-    uint8_t *sv_ptr = smem + 2 * C::kQBytes + 2 * C::kKvBytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + 2 * C::kQBytes + 4 * C::kKvBytes);
+    const uint32_t sq = smem_u32(smem);                         // Q[2]: A, B
+    const uint32_t sk = sq + 2 * C::kQBytes;                    // K[3]: [chunk][128 keys][64]
+    const uint32_t sv = sk + C::kKStages * C::kKvBytes;         // V[2]: [page][chunk][16][64]
+    uint8_t *sv_ptr = smem + 2 * C::kQBytes + C::kKStages * C::kKvBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sv_ptr + C::kVStages * C::kKvBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
     const uint32_t bar0 = smem_u32(bars);
     auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
@@ -116,20 +153,20 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(kBarQFull + i), 1);
             mbar_init(bar(kBarQEmpty + i), 1);
-            mbar_init(bar(kBarKFull + i), 1);
-            mbar_init(bar(kBarKEmpty + i), 1);
             mbar_init(bar(kBarVFull + i), 1);
             mbar_init(bar(kBarVEmpty + i), 1);
             mbar_init(bar(kBarSFull + i), 1);
             mbar_init(bar(kBarPFull + i), 128);
-            mbar_init(bar(kBarSFree + i), 1);
+            mbar_init(bar(kBarPvDone + i), 1);
         }
-        mbar_init(bar(kBarPvDone), 1);
-        mbar_init(bar(kBarOFull), 1);
+        for (int i = 0; i < C::kKStages; ++i) {
+            mbar_init(bar(kBarKFull + i), 1);
+            mbar_init(bar(kBarKEmpty + i), 1);
+        }
         mbar_init(bar(kBarDrain), 1);
         fence_barrier_init();
     }
-    if (warp == 1) {
+    if (warp == 8) {
         tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
         tmem_relinquish();
     }
@@ -137,75 +174,57 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-
-    if (warp == 0) {
-        // ================================================================ producer
+    if (warp == 9) {
+        // ================================================================ Q + V producer
         if (lane == 0) {
             prefetch_tensormap(&tm_q);
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
+            prefetch_tensormap(&tm_vp);
         }
         const uint64_t pol_kv = l2_policy_evict_last();   // K/V tiles are re-read by sibling tiles
         bool ok = true;
-        uint32_t e = 0, tc = 0;
-        for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x, ++tc) {
-            const TileInfo ti = load_tile(p, t);
-            const uint32_t qb = tc & 1;
+        uint32_t e = 0, v_issued = 0;
+        uint32_t q_issued[2] = {0, 0};
+        for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+            const PairInfo pi = load_pair(p, t);
             int good = 1;
             if (lane == 0) {
-                if (!mbar_wait(bar(kBarQEmpty + qb), ((tc >> 1) & 1) ^ 1, p.status)) {
-                    good = 0;
-                } else {
-                    mbar_arrive_expect_tx(bar(kBarQFull + qb), C::kQBytes);
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    if (!good || pi.sub[x].nrows == 0) continue;
+                    // Q buffer x is free once the last S of its previous sub-tile is done
+                    if (q_issued[x] > 0 &&
+                        !mbar_wait(bar(kBarQEmpty + x), (q_issued[x] - 1) & 1, p.status)) {
+                        good = 0;
+                        continue;
+                    }
+                    mbar_arrive_expect_tx(bar(kBarQFull + x), C::kQBytes);
 #pragma unroll
                     for (int c = 0; c < C::kChunks; ++c)
-                        tma_load_3d(sq + qb * C::kQBytes + c * (kPreRows * 128), &tm_q, c * 64,
-                                    ti.kvh * p.g, ti.q0 + ti.row0 / p.g, bar(kBarQFull + qb));
+                        tma_load_3d(sq + x * C::kQBytes + c * (kPreRows * 128), &tm_q, c * 64,
+                                    pi.kvh * p.g, pi.q0 + pi.sub[x].row0 / p.g, bar(kBarQFull + x));
+                    ++q_issued[x];
                 }
             }
             ok = __shfl_sync(0xffffffffu, good, 0) != 0;
-            const int32_t *bt_row = p.block_table + (int64_t)(p.tiles[t].seq) * p.bt_stride;
-            for (int j = 0; j < ti.n && ok; ++j, ++e) {
-                // block ids of the tile's 8 pages; pages past the last visible key
-                // are never read from the table and load as zeros
-                int bid = p.num_blocks;
-                const int page = j * (kKvTile / kBlockSize) + lane;
-                if (lane < kKvTile / kBlockSize && page * kBlockSize < ti.kend_max) {
-                    bid = __ldg(bt_row + page);
-                    if (bid < 0 || bid >= p.num_blocks) {
-                        record_status(p.status, UA_DEVICE_BAD_BLOCK_ID_BIT);
-                        bid = p.num_blocks;
-                    }
-                }
+            const int kend = max(pi.sub[0].kend_max, pi.sub[1].kend_max);
+            const int32_t *bt_row = p.block_table + (int64_t)pi.seq * p.bt_stride;
+            for (int j = 0; j < pi.n && ok; ++j, ++e) {
+                const int bid = tile_block_id(p, bt_row, j, kend, lane);
                 int b[kKvTile / kBlockSize];
 #pragma unroll
                 for (int i = 0; i < kKvTile / kBlockSize; ++i) b[i] = __shfl_sync(0xffffffffu, bid, i);
-                const uint32_t st = e & 1, ph = (e >> 1) & 1;
+                const uint32_t vs = e % C::kVStages, vph = (e / C::kVStages) & 1;
                 good = 1;
                 if (lane == 0) {
-                    if (!mbar_wait(bar(kBarKEmpty + st), ph ^ 1, p.status)) {
+                    if (!mbar_wait(bar(kBarVEmpty + vs), vph ^ 1, p.status)) {
                         good = 0;
                     } else {
-                        mbar_arrive_expect_tx(bar(kBarKFull + st), C::kKvBytes);
+                        mbar_arrive_expect_tx(bar(kBarVFull + vs), C::kKvBytes);
 #pragma unroll
                         for (int i = 0; i < kKvTile / kBlockSize; ++i)
-#pragma unroll
-                            for (int c = 0; c < C::kChunks; ++c)
-                                tma_load_3d_hint(sk + st * C::kKvBytes + c * C::kChunkBytes + i * 2048,
-                                                 &tm_k, c * 64, ti.kvh, b[i] * kBlockSize,
-                                                 bar(kBarKFull + st), pol_kv);
-                    }
-                    if (good && !mbar_wait(bar(kBarVEmpty + st), ph ^ 1, p.status)) {
-                        good = 0;
-                    } else if (good) {
-                        mbar_arrive_expect_tx(bar(kBarVFull + st), C::kKvBytes);
-#pragma unroll
-                        for (int i = 0; i < kKvTile / kBlockSize; ++i)
-#pragma unroll
-                            for (int c = 0; c < C::kChunks; ++c)
-                                tma_load_3d_hint(sv + st * C::kKvBytes + c * C::kChunkBytes + i * 2048,
-                                                 &tm_v, c * 64, ti.kvh, b[i] * kBlockSize,
-                                                 bar(kBarVFull + st), pol_kv);
+                            tma_load_5d_hint(sv + vs * C::kKvBytes + i * C::kPageBytes, &tm_vp, 0, 0, 0,
+                                             pi.kvh, b[i], bar(kBarVFull + vs), pol_kv);
+                        ++v_issued;
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, good, 0) != 0;
@@ -213,77 +232,127 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
         }
         // drain: the last loads issued must land before the CTA can exit
         if (lane == 0) {
-            for (uint32_t x = (e > 2 ? e - 2 : 0); x < e; ++x) {
-                mbar_wait(bar(kBarKFull + (x & 1)), (x >> 1) & 1, p.status);
-                mbar_wait(bar(kBarVFull + (x & 1)), (x >> 1) & 1, p.status);
-            }
-            for (uint32_t x = (tc > 2 ? tc - 2 : 0); x < tc; ++x)
-                mbar_wait(bar(kBarQFull + (x & 1)), (x >> 1) & 1, p.status);
+            for (uint32_t x = (v_issued > (uint32_t)C::kVStages ? v_issued - C::kVStages : 0); x < v_issued; ++x)
+                mbar_wait(bar(kBarVFull + x % C::kVStages), (x / C::kVStages) & 1, p.status);
+            for (int x = 0; x < 2; ++x)
+                if (q_issued[x] > 0) mbar_wait(bar(kBarQFull + x), (q_issued[x] - 1) & 1, p.status);
         }
-    } else if (warp == 1) {
+    } else if (warp == 10) {
+        // ================================================================ K producer
+        if (lane == 0) prefetch_tensormap(&tm_k);
+        const uint64_t pol_kv = l2_policy_evict_last();
+        bool ok = true;
+        uint32_t e = 0, k_issued = 0;
+        for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+            const PairInfo pi = load_pair(p, t);
+            const int kend = max(pi.sub[0].kend_max, pi.sub[1].kend_max);
+            const int32_t *bt_row = p.block_table + (int64_t)pi.seq * p.bt_stride;
+            for (int j = 0; j < pi.n && ok; ++j, ++e) {
+                const int bid = tile_block_id(p, bt_row, j, kend, lane);
+                int b[kKvTile / kBlockSize];
+#pragma unroll
+                for (int i = 0; i < kKvTile / kBlockSize; ++i) b[i] = __shfl_sync(0xffffffffu, bid, i);
+                const uint32_t ks = e % C::kKStages, kph = (e / C::kKStages) & 1;
+                int good = 1;
+                if (lane == 0) {
+                    if (!mbar_wait(bar(kBarKEmpty + ks), kph ^ 1, p.status)) {
+                        good = 0;
+                    } else {
+                        mbar_arrive_expect_tx(bar(kBarKFull + ks), C::kKvBytes);
+#pragma unroll
+                        for (int i = 0; i < kKvTile / kBlockSize; ++i)
+#pragma unroll
+                            for (int c = 0; c < C::kChunks; ++c)
+                                tma_load_3d_hint(sk + ks * C::kKvBytes + c * C::kChunkBytes + i * 2048,
+                                                 &tm_k, c * 64, pi.kvh, b[i] * kBlockSize,
+                                                 bar(kBarKFull + ks), pol_kv);
+                        ++k_issued;
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+            }
+        }
+        if (lane == 0) {
+            for (uint32_t x = (k_issued > (uint32_t)C::kKStages ? k_issued - C::kKStages : 0); x < k_issued; ++x)
+                mbar_wait(bar(kBarKFull + x % C::kKStages), (x / C::kKStages) & 1, p.status);
+        }
+    } else if (warp == 8) {
         // ================================================================ MMA issuer
         constexpr uint32_t idesc_s = umma_idesc_bf16(kPreRows, kKvTile, 0, 0);
         constexpr uint32_t idesc_pv = umma_idesc_bf16(kPreRows, D, 0, 1);
         bool ok = true;
-        uint32_t e = 0, tc = 0, issued_any = 0;
-        // O += P_e V_e for KV tile event ev; `first` starts a fresh accumulator.
-        auto issue_pv = [&](uint32_t ev, bool first) -> bool {
-            const uint32_t sb = ev & 1, ph = (ev >> 1) & 1;
-            if (!mbar_wait(bar(kBarPFull + sb), ph, p.status)) return false;
-            if (!mbar_wait(bar(kBarVFull + sb), ph, p.status)) return false;
-            tc_fence_after();
-            const uint32_t p_col = tmem + (sb ? C::kColS1 : C::kColS0);
-#pragma unroll
-            for (int kk = 0; kk < kKvTile / 16; ++kk) {
-                // 16 keys per step: P columns kk*8 .. +8 (bf16 pairs), V rows kk*16 .. +16
-                const uint64_t bdesc = umma_desc_sw128(sv + sb * C::kKvBytes + kk * 2048,
-                                                       C::kChunkBytes, 1024);
-                umma_ts(tmem + C::kColO, p_col + kk * 8, bdesc, idesc_pv, (first && kk == 0) ? 0u : 1u);
-            }
-            umma_commit(bar(kBarVEmpty + sb));
-            umma_commit(bar(kBarSFree + sb));
-            umma_commit(bar(kBarPvDone));
-            return true;
-        };
+        uint32_t e = 0, issued_any = 0;
+        uint32_t qcnt[2] = {0, 0};   // Q tiles consumed per sub-tile slot
+        uint32_t ecnt[2] = {0, 0};   // S / P V events per sub-tile slot
         if (lane == 0) {
-            for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x, ++tc) {
-                const int n = p.tiles[t].kv_tiles;
-                const uint32_t qb = tc & 1;
-                if (!mbar_wait(bar(kBarQFull + qb), (tc >> 1) & 1, p.status)) {
-                    ok = false;
-                    break;
-                }
-                for (int j = 0; j < n && ok; ++j, ++e) {
-                    const uint32_t sb = e & 1, ph = (e >> 1) & 1;
-                    if (!mbar_wait(bar(kBarKFull + sb), ph, p.status) ||
-                        (e >= 2 && !mbar_wait(bar(kBarSFree + sb), ph ^ 1, p.status))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t s_col = tmem + (sb ? C::kColS1 : C::kColS0);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-                        const uint64_t adesc = umma_desc_sw128(sq + qb * C::kQBytes + off, 16, 1024);
-                        const uint64_t bdesc = umma_desc_sw128(sk + sb * C::kKvBytes + off, 16, 1024);
-                        umma_ss(s_col, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
-                    }
-                    issued_any = 1;
-                    umma_commit(bar(kBarSFull + sb));
-                    umma_commit(bar(kBarKEmpty + sb));
-                    if (j == n - 1) umma_commit(bar(kBarQEmpty + qb));
-                    if (j >= 1 && !issue_pv(e - 1, j == 1)) {
-                        ok = false;
-                        break;
-                    }
-                }
+            for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+                const PairInfo pi = load_pair(p, t);
+                const int nx[2] = {pi.sub[0].n, pi.sub[1].n};
+                for (int x = 0; x < 2 && ok; ++x)
+                    if (nx[x] > 0 && !mbar_wait(bar(kBarQFull + x), qcnt[x] & 1, p.status)) ok = false;
                 if (!ok) break;
-                if (!issue_pv(e - 1, n == 1)) {
-                    ok = false;
-                    break;
+                for (int j = 0; j < pi.n && ok; ++j, ++e) {
+                    const uint32_t ks = e % C::kKStages, kph = (e / C::kKStages) & 1;
+                    if (!mbar_wait(bar(kBarKFull + ks), kph, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    // ---- S_X = Q_X K_j^T
+                    for (int x = 0; x < 2; ++x) {
+                        if (j >= nx[x]) continue;
+                        // S_X is overwritten: its P from the previous event must be consumed
+                        if (ecnt[x] > 0 &&
+                            !mbar_wait(bar(kBarPvDone + x), (ecnt[x] - 1) & 1, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t s_col = tmem + x * 256 + C::kColS;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+                            const uint64_t adesc = umma_desc_sw128(sq + x * C::kQBytes + off, 16, 1024);
+                            const uint64_t bdesc = umma_desc_sw128(sk + ks * C::kKvBytes + off, 16, 1024);
+                            umma_ss(s_col, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
+                        }
+                        issued_any = 1;
+                        umma_commit(bar(kBarSFull + x));
+                        if (j == nx[x] - 1) umma_commit(bar(kBarQEmpty + x));
+                    }
+                    if (!ok) break;
+                    umma_commit(bar(kBarKEmpty + ks));
+                    // ---- O_X += P_X V_j
+                    const uint32_t vs = e % C::kVStages, vph = (e / C::kVStages) & 1;
+                    if (!mbar_wait(bar(kBarVFull + vs), vph, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    for (int x = 0; x < 2; ++x) {
+                        if (j >= nx[x]) continue;
+                        if (!mbar_wait(bar(kBarPFull + x), ecnt[x] & 1, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t p_col = tmem + x * 256 + C::kColS;
+#pragma unroll
+                        for (int kk = 0; kk < kKvTile / 16; ++kk) {
+                            // 16 keys per step = one page of V: P columns kk*8 .. +8 (bf16
+                            // pairs); V page kk is [chunk][16 keys][64], MN-major: 64-wide
+                            // d chunks 2 KB apart (LBO), 8-key groups 1 KB apart (SBO)
+                            const uint64_t bdesc = umma_desc_sw128(sv + vs * C::kKvBytes + kk * C::kPageBytes,
+                                                                   kBlockSize * 128, 1024);
+                            umma_ts(tmem + x * 256 + C::kColO, p_col + kk * 8, bdesc, idesc_pv,
+                                    (j == 0 && kk == 0) ? 0u : 1u);
+                        }
+                        umma_commit(bar(kBarPvDone + x));
+                        ++ecnt[x];
+                    }
+                    if (!ok) break;
+                    umma_commit(bar(kBarVEmpty + vs));
                 }
-                umma_commit(bar(kBarOFull));
+                for (int x = 0; x < 2; ++x)
+                    if (nx[x] > 0) ++qcnt[x];
             }
             // every MMA issued has completed before TMEM is released
             if (issued_any) {
@@ -292,46 +361,61 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp < 8) {
         // ================================================================ softmax + epilogue
+        const int x = warp >> 2;                        // sub-tile A (0) or B (1)
         const int quarter = warp & 3;                   // TMEM lanes this warp may touch
-        const int r = quarter * 32 + lane;              // row of the tile = TMEM lane
+        const int r = quarter * 32 + lane;              // row of the sub-tile = TMEM lane
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t s_addr = tmem + lane_off + x * 256 + C::kColS;
+        const uint32_t o_addr = tmem + lane_off + x * 256 + C::kColO;
         bool ok = true;
-        uint32_t e = 0, tc = 0;
-        for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x, ++tc) {
-            const TileInfo ti = load_tile(p, t);
-            const int pr = ti.row0 + r;
-            const bool valid = r < ti.nrows;
+        uint32_t e = 0, ex = 0;    // KV tile events of the CTA; S / P V events of this slot
+        for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+            const PairInfo pi = load_pair(p, t);
+            const SubInfo si = x ? pi.sub[1] : pi.sub[0];
+            const int n_a = pi.sub[0].n;
+            if (si.nrows == 0) {
+                e += pi.n;
+                continue;
+            }
+            const int pr = si.row0 + r;
+            const bool valid = r < si.nrows;
             const int i = pr / p.g;
-            const int kend = (p.causal && valid) ? min(ti.lk, ti.lk - ti.lq + i + 1) : ti.lk;
+            const int kend = (p.causal && valid) ? min(pi.lk, pi.lk - pi.lq + i + 1) : pi.lk;
+            const int kend_pair = max(pi.sub[0].kend_max, pi.sub[1].kend_max);
             float m_run = -INFINITY;
             float l = 0.f;
-            for (int j = 0; j < ti.n; ++j, ++e) {
-                const uint32_t sb = e & 1, ph = (e >> 1) & 1;
-                if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + sb), ph, p.status))) {
+            for (int j = 0; j < si.n; ++j, ++ex) {
+                if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + x), ex & 1, p.status))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t s_addr = tmem + lane_off + (sb ? C::kColS1 : C::kColS0);
-                float x[kKvTile];
+                // The scores of this row, masked.  With a positive scale (the usual
+                // case) the max is taken on the raw scores and the scale is folded
+                // into the exponent's FFMA.
+                const bool pos_scale = p.scale_log2 > 0.f;
+                const float c_exp = pos_scale ? p.scale_log2 : 1.f;
+                const float c_pre = pos_scale ? 1.f : p.scale_log2;
+                const bool masked = (j + 1) * kKvTile > si.kend_lo;   // diagonal / tail tile
+                const int lim = kend - j * kKvTile;                    // visible keys of this tile
+                // pass 1: the masked row max (the scores stay in TMEM)
+                float mx;
+                {
+                    uint32_t xs[kKvTile];
+                    tmem_ld128(s_addr, xs);
+                    float m8[8];
 #pragma unroll
-                for (int c = 0; c < kKvTile / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(s_addr + 32 * c, v);
+                    for (int a = 0; a < 8; ++a) m8[a] = -INFINITY;
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) x[32 * c + k] = __uint_as_float(v[k]) * p.scale_log2;
+                    for (int k = 0; k < kKvTile; ++k) {
+                        const float xv = __uint_as_float(xs[k]) * c_pre;
+                        m8[k & 7] = fmaxf(m8[k & 7], (masked && k >= lim) ? -INFINITY : xv);
+                    }
+                    mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * c_exp;
                 }
-                if ((j + 1) * kKvTile > ti.kend_lo) {       // diagonal / tail tile: mask
-                    const int lim = kend - j * kKvTile;
-#pragma unroll
-                    for (int k = 0; k < kKvTile; ++k)
-                        if (k >= lim) x[k] = -INFINITY;
-                }
-                float mx = x[0];
-#pragma unroll
-                for (int k = 1; k < kKvTile; ++k) mx = fmaxf(mx, x[k]);
                 if (j == 0) {
                     m_run = mx;
                 } else if (__any_sync(0xffffffffu, mx > m_run + C::kRescaleThreshold)) {
@@ -340,7 +424,7 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
                     // TMEM loads / stores are warp-wide, so the whole warp takes this path.
                     const float m_new = fmaxf(m_run, mx);
                     const float alpha = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run - m_new);
-                    const bool waited = mbar_wait(bar(kBarPvDone), (e - 1) & 1, p.status);
+                    const bool waited = mbar_wait(bar(kBarPvDone + x), (ex - 1) & 1, p.status);
                     if (!__all_sync(0xffffffffu, waited)) {
                         ok = false;
                         break;
@@ -349,46 +433,67 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t v[32];
-                        tmem_ld32(tmem + lane_off + C::kColO + 32 * c, v);
+                        tmem_ld32(o_addr + 32 * c, v);
 #pragma unroll
                         for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-                        tmem_st32(tmem + lane_off + C::kColO + 32 * c, v);
+                        tmem_st32(o_addr + 32 * c, v);
                     }
                     l *= alpha;
                     m_run = m_new;
                 }
                 const float mu = (m_run == -INFINITY) ? 0.f : m_run;
-                float lsum = 0.f;
+                // p = 2^(s * c - mu), summed in 8 independent chains, packed to bf16
+                // pairs and written over the first 64 columns of S
+                float l8[8];
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int a = 0; a < 8; ++a) l8[a] = 0.f;
+                // pass 2, 64 keys at a time: p = 2^(s * c - mu), summed in 8 chains,
+                // packed to bf16 pairs; keys 64h..64h+63 go to columns 32h..32h+31,
+                // which this pass has already read
+#pragma unroll
+                for (int h = 0; h < kKvTile / 64; ++h) {
+                    uint32_t xs[64];
+                    tmem_ld32(s_addr + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&xs[0]));
+                    tmem_ld32(s_addr + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&xs[32]));
                     uint32_t pk[32];
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
-                        const float p0 = fast_exp2(x[64 * c + 2 * k] - mu);
-                        const float p1 = fast_exp2(x[64 * c + 2 * k + 1] - mu);
-                        lsum += p0 + p1;
+                        const int k0 = 64 * h + 2 * k;
+                        float x0 = __uint_as_float(xs[2 * k]) * c_pre;
+                        float x1 = __uint_as_float(xs[2 * k + 1]) * c_pre;
+                        if (masked && k0 >= lim) x0 = -INFINITY;
+                        if (masked && k0 + 1 >= lim) x1 = -INFINITY;
+                        const float p0 = fast_exp2(fmaf(x0, c_exp, -mu));
+                        const float p1 = fast_exp2(fmaf(x1, c_exp, -mu));
+                        l8[(2 * k) & 7] += p0;
+                        l8[(2 * k + 1) & 7] += p1;
                         pk[k] = pack_bf16x2(p0, p1);
                     }
-                    tmem_st32(s_addr + 32 * c, pk);      // P (bf16 pairs) over the first 64 columns of S
+                    tmem_st32(s_addr + 32 * h, pk);
                 }
-                l += lsum;
+                l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
                 // V rows past the context in the sequence's last page may hold
-                // anything (NaN included): zero them before P V reads them.
-                const int last_page_start = (ti.lk - 1) & ~(kBlockSize - 1);
-                if (warp == 2 && (ti.lk & (kBlockSize - 1)) != 0 && ((ti.lk - 1) / kKvTile) == j &&
-                    last_page_start < ti.kend_max) {
-                    if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarVFull + sb), ph, p.status))) {
+                // anything (NaN included): zero them before P V reads them.  The
+                // first sub-tile that uses this KV tile does it (its P V goes first).
+                const int last_page_start = (pi.lk - 1) & ~(kBlockSize - 1);
+                const bool zero_here = (x == 0) ? (warp == 0) : (warp == 4 && j >= n_a);
+                if (zero_here && (pi.lk & (kBlockSize - 1)) != 0 && ((pi.lk - 1) / kKvTile) == j &&
+                    last_page_start < kend_pair) {
+                    const uint32_t vs = (e + j) % C::kVStages, vph = ((e + j) / C::kVStages) & 1;
+                    if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarVFull + vs), vph, p.status))) {
                         ok = false;
                     } else {
-                        const int k0 = ti.lk - j * kKvTile;
+                        const int k0 = pi.lk - j * kKvTile;
                         const int k1 = last_page_start + kBlockSize - j * kKvTile;
                         const int per_row = C::kChunks * 8;     // 16-byte pieces per key row
                         for (int u = lane; u < (k1 - k0) * per_row; u += 32) {
                             const int key = k0 + u / per_row;
                             const int c = (u % per_row) / 8;
                             const int piece = u % 8;
-                            *reinterpret_cast<uint4 *>(sv_ptr + sb * C::kKvBytes + c * C::kChunkBytes +
-                                                       key * 128 + piece * 16) = make_uint4(0, 0, 0, 0);
+                            *reinterpret_cast<uint4 *>(sv_ptr + vs * C::kKvBytes +
+                                                       (key / kBlockSize) * C::kPageBytes + c * 2048 +
+                                                       (key % kBlockSize) * 128 + piece * 16) =
+                                make_uint4(0, 0, 0, 0);
                         }
                         fence_proxy_async_smem();
                     }
@@ -396,31 +501,32 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(kBarPFull + sb));
+                mbar_arrive(bar(kBarPFull + x));
                 if (!ok) break;
             }
             if (!ok) break;
-            // ---- epilogue: O / l -> bf16 rows of out
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarOFull), tc & 1, p.status))) {
+            e += pi.n;
+            // ---- epilogue: O / l -> bf16 rows of out (after the last P V of this slot)
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarPvDone + x), (ex - 1) & 1, p.status))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            __nv_bfloat16 *orow = p.out + ((int64_t)(ti.q0 + i) * p.hq + ti.kvh * p.g + pr % p.g) * D;
+            __nv_bfloat16 *orow = p.out + ((int64_t)(pi.q0 + i) * p.hq + pi.kvh * p.g + pr % p.g) * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
-                tmem_ld32(tmem + lane_off + C::kColO + 32 * c, v);
-                uint32_t pk[16];
-#pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    pk[k] = pack_bf16x2(__uint_as_float(v[2 * k]) * inv, __uint_as_float(v[2 * k + 1]) * inv);
+                tmem_ld32(o_addr + 32 * c, v);
                 if (valid) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                        dst[k] = make_uint4(
+                            pack_bf16x2(__uint_as_float(v[8 * k]) * inv, __uint_as_float(v[8 * k + 1]) * inv),
+                            pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv),
+                            pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv),
+                            pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv));
                 }
             }
         }
@@ -429,7 +535,7 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
     // ---- teardown: every role is done with TMEM before it is freed
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 8) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
@@ -437,7 +543,7 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
 
 template <int D>
 static cudaError_t launch_prefill_t(const PrefillParams &p, const CUtensorMap &tm_q,
-                                    const CUtensorMap &tm_k, const CUtensorMap &tm_v, int ctas,
+                                    const CUtensorMap &tm_k, const CUtensorMap &tm_vp, int ctas,
                                     cudaStream_t stream) {
     using C = PreCfg<D>;
     static thread_local int configured_device = -1;
@@ -450,15 +556,15 @@ static cudaError_t launch_prefill_t(const PrefillParams &p, const CUtensorMap &t
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    ua_prefill_kernel<D><<<ctas, C::kThreads, C::kSmemBytes, stream>>>(p, tm_q, tm_k, tm_v);
+    ua_prefill_kernel<D><<<ctas, C::kThreads, C::kSmemBytes, stream>>>(p, tm_q, tm_k, tm_vp);
     return cudaGetLastError();
 }
 
 cudaError_t launch_prefill(int d, const PrefillParams &p, const CUtensorMap &tm_q,
-                           const CUtensorMap &tm_k, const CUtensorMap &tm_v, int ctas,
+                           const CUtensorMap &tm_k, const CUtensorMap &tm_vp, int ctas,
                            cudaStream_t stream) {
-    return d == 64 ? launch_prefill_t<64>(p, tm_q, tm_k, tm_v, ctas, stream)
-                   : launch_prefill_t<128>(p, tm_q, tm_k, tm_v, ctas, stream);
+    return d == 64 ? launch_prefill_t<64>(p, tm_q, tm_k, tm_vp, ctas, stream)
+                   : launch_prefill_t<128>(p, tm_q, tm_k, tm_vp, ctas, stream);
 }
 
 }  // namespace ua

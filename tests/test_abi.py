@@ -35,7 +35,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("unified_attention", "ua_workspace_size", "ua_status_string", "ua_device_status",
-              "ua_plan_inspect", "ua_profile_enable", "ua_profile_last"):
+              "ua_plan_inspect", "ua_profile_enable", "ua_profile_read"):
         assert n in names
 
 

@@ -54,7 +54,7 @@ def check_plan(q_lens, k_lens, hq, hk, d=128, causal=True, num_sms=152):
             covered[(seq, kvh, r)] = covered.get((seq, kvh, r), 0) + 1
     for t in tiles:
         _, _, seq, kvh, row0, nrows, kvt, _ = t
-        assert 1 <= nrows <= 128
+        assert 1 <= nrows <= 256 and row0 % 256 == 0
         for r in range(row0, row0 + nrows):
             covered[(seq, kvh, r)] = covered.get((seq, kvh, r), 0) + 1
         last_token = (row0 + nrows - 1) // g
