@@ -128,7 +128,7 @@ __device__ __forceinline__ int tile_block_id(const PrefillParams &p, const int32
     return bid;
 }
 
-template <int D>
+template <int D, bool kPos>
 __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
     ua_prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -392,29 +392,37 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                // The scores of this row, masked.  With a positive scale (the usual
-                // case) the max is taken on the raw scores and the scale is folded
-                // into the exponent's FFMA.
-                const bool pos_scale = p.scale_log2 > 0.f;
-                const float c_exp = pos_scale ? p.scale_log2 : 1.f;
-                const float c_pre = pos_scale ? 1.f : p.scale_log2;
+                // The scores of this row.  With a positive scale (kPos, the usual case)
+                // the max is taken on the raw scores and the scale is folded into the
+                // exponent's FMA; otherwise the scores are scaled first.  Keys at or
+                // past the row's limit (diagonal and tail tiles only) become -inf.
                 const bool masked = (j + 1) * kKvTile > si.kend_lo;   // diagonal / tail tile
                 const int lim = kend - j * kKvTile;                    // visible keys of this tile
+                constexpr uint32_t kNegInf = 0xff800000u;
                 // pass 1: the masked row max (the scores stay in TMEM)
                 float mx;
                 {
                     uint32_t xs[kKvTile];
                     tmem_ld128(s_addr, xs);
+                    if (!kPos) {
+#pragma unroll
+                        for (int k = 0; k < kKvTile; ++k)
+                            xs[k] = __float_as_uint(__uint_as_float(xs[k]) * p.scale_log2);
+                    }
+                    if (masked) {
+#pragma unroll
+                        for (int k = 0; k < kKvTile; ++k) xs[k] = k < lim ? xs[k] : kNegInf;
+                    }
                     float m8[8];
 #pragma unroll
-                    for (int a = 0; a < 8; ++a) m8[a] = -INFINITY;
+                    for (int a = 0; a < 8; ++a) m8[a] = __uint_as_float(xs[a]);
 #pragma unroll
-                    for (int k = 0; k < kKvTile; ++k) {
-                        const float xv = __uint_as_float(xs[k]) * c_pre;
-                        m8[k & 7] = fmaxf(m8[k & 7], (masked && k >= lim) ? -INFINITY : xv);
-                    }
-                    mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * c_exp;
+                    for (int k = 8; k < kKvTile; k += 2)
+                        m8[(k >> 1) & 7] = fmax3(m8[(k >> 1) & 7], __uint_as_float(xs[k]),
+                                                 __uint_as_float(xs[k + 1]));
+                    mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
+                               fmaxf(m8[6], m8[7]));
+                    if (kPos) mx *= p.scale_log2;
                 }
                 if (j == 0) {
                     m_run = mx;
@@ -442,36 +450,40 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
                     m_run = m_new;
                 }
                 const float mu = (m_run == -INFINITY) ? 0.f : m_run;
-                // p = 2^(s * c - mu), summed in 8 independent chains, packed to bf16
-                // pairs and written over the first 64 columns of S
-                float l8[8];
+                // pass 2, 64 keys at a time: p = 2^(s * c - mu) (two lanes of work per
+                // FMA), summed in 8 chains, packed to bf16 pairs; keys 64h..64h+63 go
+                // to columns 32h..32h+31, which this pass has already read
+                const float2 c2 = kPos ? make_float2(p.scale_log2, p.scale_log2) : make_float2(1.f, 1.f);
+                const float2 nmu2 = make_float2(-mu, -mu);
+                float2 l4[4];
 #pragma unroll
-                for (int a = 0; a < 8; ++a) l8[a] = 0.f;
-                // pass 2, 64 keys at a time: p = 2^(s * c - mu), summed in 8 chains,
-                // packed to bf16 pairs; keys 64h..64h+63 go to columns 32h..32h+31,
-                // which this pass has already read
+                for (int a = 0; a < 4; ++a) l4[a] = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int h = 0; h < kKvTile / 64; ++h) {
                     uint32_t xs[64];
                     tmem_ld32(s_addr + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&xs[0]));
                     tmem_ld32(s_addr + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&xs[32]));
+                    if (!kPos) {
+#pragma unroll
+                        for (int k = 0; k < 64; ++k)
+                            xs[k] = __float_as_uint(__uint_as_float(xs[k]) * p.scale_log2);
+                    }
+                    if (masked) {
+#pragma unroll
+                        for (int k = 0; k < 64; ++k) xs[k] = 64 * h + k < lim ? xs[k] : kNegInf;
+                    }
                     uint32_t pk[32];
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
-                        const int k0 = 64 * h + 2 * k;
-                        float x0 = __uint_as_float(xs[2 * k]) * c_pre;
-                        float x1 = __uint_as_float(xs[2 * k + 1]) * c_pre;
-                        if (masked && k0 >= lim) x0 = -INFINITY;
-                        if (masked && k0 + 1 >= lim) x1 = -INFINITY;
-                        const float p0 = fast_exp2(fmaf(x0, c_exp, -mu));
-                        const float p1 = fast_exp2(fmaf(x1, c_exp, -mu));
-                        l8[(2 * k) & 7] += p0;
-                        l8[(2 * k + 1) & 7] += p1;
-                        pk[k] = pack_bf16x2(p0, p1);
+                        const float2 y = ffma2(make_float2(__uint_as_float(xs[2 * k]),
+                                                           __uint_as_float(xs[2 * k + 1])), c2, nmu2);
+                        const float2 pv = make_float2(fast_exp2(y.x), fast_exp2(y.y));
+                        l4[k & 3] = fadd2(l4[k & 3], pv);
+                        pk[k] = pack_bf16x2(pv.x, pv.y);
                     }
                     tmem_st32(s_addr + 32 * h, pk);
                 }
-                l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+                l += ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) + ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y));
                 // V rows past the context in the sequence's last page may hold
                 // anything (NaN included): zero them before P V reads them.  The
                 // first sub-tile that uses this KV tile does it (its P V goes first).
@@ -541,7 +553,7 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
     }
 }
 
-template <int D>
+template <int D, bool kPos>
 static cudaError_t launch_prefill_t(const PrefillParams &p, const CUtensorMap &tm_q,
                                     const CUtensorMap &tm_k, const CUtensorMap &tm_vp, int ctas,
                                     cudaStream_t stream) {
@@ -550,21 +562,25 @@ static cudaError_t launch_prefill_t(const PrefillParams &p, const CUtensorMap &t
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(ua_prefill_kernel<D>,
+        cudaError_t e = cudaFuncSetAttribute(ua_prefill_kernel<D, kPos>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    ua_prefill_kernel<D><<<ctas, C::kThreads, C::kSmemBytes, stream>>>(p, tm_q, tm_k, tm_vp);
+    ua_prefill_kernel<D, kPos><<<ctas, C::kThreads, C::kSmemBytes, stream>>>(p, tm_q, tm_k, tm_vp);
     return cudaGetLastError();
 }
 
 cudaError_t launch_prefill(int d, const PrefillParams &p, const CUtensorMap &tm_q,
                            const CUtensorMap &tm_k, const CUtensorMap &tm_vp, int ctas,
                            cudaStream_t stream) {
-    return d == 64 ? launch_prefill_t<64>(p, tm_q, tm_k, tm_vp, ctas, stream)
-                   : launch_prefill_t<128>(p, tm_q, tm_k, tm_vp, ctas, stream);
+    const bool pos = p.scale_log2 > 0.f;
+    if (d == 64)
+        return pos ? launch_prefill_t<64, true>(p, tm_q, tm_k, tm_vp, ctas, stream)
+                   : launch_prefill_t<64, false>(p, tm_q, tm_k, tm_vp, ctas, stream);
+    return pos ? launch_prefill_t<128, true>(p, tm_q, tm_k, tm_vp, ctas, stream)
+               : launch_prefill_t<128, false>(p, tm_q, tm_k, tm_vp, ctas, stream);
 }
 
 }  // namespace ua
