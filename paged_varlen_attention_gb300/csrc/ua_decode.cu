@@ -36,9 +36,19 @@ struct DecCfg {
     static constexpr int kConsumerWarps = 4;
     static constexpr int kThreads = (kConsumerWarps + 1) * 32;
     static constexpr int kMergeFloats = kDecRows * D + 2 * kDecRows;   // per warp
-    static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes +
-                                         (size_t)kConsumerWarps * kMergeFloats * 4 +
-                                         2 * kStages * 8;
+    // ring of piece descriptors + Q tiles, filled by the producer ahead of use
+    static constexpr int kRing = 3;
+    static constexpr int kQTileBytes = kDecRows * D * 2;
+    static constexpr int kDescInts = 16;
+    static constexpr size_t kMergeBytes = (size_t)kConsumerWarps * kMergeFloats * 4;
+    static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kMergeBytes +
+                                         (size_t)kRing * (kQTileBytes + kDescInts * 4) +
+                                         (2 * kStages + 2 * kRing) * 8;
+};
+
+// Fields of a piece descriptor in the shared-memory ring.
+enum : int {
+    kDq0 = 0, kDlq, kDlk, kDkvh, kDrow0, kDnrows, kDpb, kDpe, kDslot
 };
 
 template <int D>
@@ -51,10 +61,15 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *stages = smem;
     float *merge = reinterpret_cast<float *>(smem + (size_t)C::kStages * C::kStageBytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(merge + C::kConsumerWarps * C::kMergeFloats);
+    uint8_t *qring = reinterpret_cast<uint8_t *>(merge) + C::kMergeBytes;       // [kRing][16][D] bf16
+    int *dring = reinterpret_cast<int *>(qring + C::kRing * C::kQTileBytes);   // [kRing][kDescInts]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(dring + C::kRing * C::kDescInts);
     const uint32_t stage0 = smem_u32(stages);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + C::kStages);
+    const uint32_t pfull0 = smem_u32(bars + 2 * C::kStages);
+    const uint32_t pempty0 = smem_u32(bars + 2 * C::kStages + C::kRing);
+    const uint32_t qring0 = smem_u32(qring);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -62,6 +77,10 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
         for (int i = 0; i < C::kStages; ++i) {
             mbar_init(full0 + 8 * i, 1);
             mbar_init(empty0 + 8 * i, 1);
+        }
+        for (int i = 0; i < C::kRing; ++i) {
+            mbar_init(pfull0 + 8 * i, 1);
+            mbar_init(pempty0 + 8 * i, 1);
         }
         fence_barrier_init();
     }
@@ -79,9 +98,52 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
         }
         const uint64_t policy = l2_policy_evict_first();
         bool ok = true;
+        uint32_t filled = 0;   // ring entries filled
+        DecPiece nxt{};
+        if (pbeg < pend) nxt = p.pieces[pbeg];
         for (int pi = pbeg; pi < pend && ok; ++pi) {
-            const DecPiece pc = p.pieces[pi];
+            // this piece (loaded one piece ahead) and the next one's struct
+            const DecPiece pc = nxt;
+            if (pi + 1 < pend) nxt = p.pieces[pi + 1];
             const int32_t *bt_row = p.block_table + (int64_t)pc.seq * p.bt_stride;
+            const int q0 = p.cu[pc.seq];
+            const int lq = p.cu[pc.seq + 1] - q0;
+            const int lk = p.seqused_k[pc.seq];
+            // ---- ring entry: descriptor + the piece's Q rows (bulk copies, one per token)
+            int good = 1;
+            if (lane == 0) {
+                const uint32_t slot = filled % C::kRing, ph = (filled / C::kRing) & 1;
+                if (!mbar_wait(pempty0 + 8 * slot, ph ^ 1, p.status)) {
+                    good = 0;
+                } else {
+                    int *d = dring + slot * C::kDescInts;
+                    d[kDq0] = q0;
+                    d[kDlq] = lq;
+                    d[kDlk] = lk;
+                    d[kDkvh] = pc.kvh;
+                    d[kDrow0] = pc.row0;
+                    d[kDnrows] = pc.nrows;
+                    d[kDpb] = pc.page_begin;
+                    d[kDpe] = pc.page_end;
+                    d[kDslot] = pc.slot;
+                    const uint32_t pb = pfull0 + 8 * slot;
+                    mbar_arrive_expect_tx(pb, (uint32_t)pc.nrows * D * 2);
+                    for (int r = 0; r < pc.nrows;) {
+                        const int pr = pc.row0 + r;
+                        const int h0 = pr % p.g;
+                        const int cnt = min(p.g - h0, pc.nrows - r);
+                        const __nv_bfloat16 *src =
+                            p.q + ((int64_t)(q0 + pr / p.g) * p.hq + pc.kvh * p.g + h0) * D;
+                        bulk_load(qring0 + slot * C::kQTileBytes + r * D * 2, src,
+                                  (uint32_t)cnt * D * 2, pb);
+                        r += cnt;
+                    }
+                    ++filled;
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+            if (!ok) break;
+            // ---- the piece's pages, 32 block-table entries at a time
             for (int base = pc.page_begin; base < pc.page_end && ok; base += 32) {
                 const int n = min(32, pc.page_end - base);
                 int bid = 0;
@@ -94,7 +156,7 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
                 }
                 for (int k = 0; k < n; ++k) {
                     const int b = __shfl_sync(0xffffffffu, bid, k);
-                    int good = 1;
+                    good = 1;
                     if (lane == 0) {
                         const uint32_t st = issued % C::kStages;
                         const uint32_t ph = (issued / C::kStages) & 1;
@@ -117,6 +179,10 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
                 }
             }
         }
+        // the ring's last bulk copies must land before the CTA can exit
+        if (lane == 0)
+            for (uint32_t x = (filled > (uint32_t)C::kRing ? filled - C::kRing : 0); x < filled; ++x)
+                mbar_wait(pfull0 + 8 * (x % C::kRing), (x / C::kRing) & 1, p.status);
     } else {
         // ------------------------------------------------------------ consumers
         const int w = warp;
@@ -127,11 +193,29 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
         float *mrg_l = mrg_m + kDecRows;
         uint32_t gbase = 0;
         bool ok = true;
+        // Every consumer warp walks every piece (the merges use a named barrier),
+        // even after a failed wait: a piece it could not get counts as empty.
         for (int pi = pbeg; pi < pend; ++pi) {
-            const DecPiece pc = p.pieces[pi];
-            const int q0 = p.cu[pc.seq];
-            const int lq = p.cu[pc.seq + 1] - q0;
-            const int lk = p.seqused_k[pc.seq];
+            // the piece's descriptor and Q rows, prepared by the producer
+            const uint32_t ring = (uint32_t)(pi - pbeg);
+            const uint32_t slot = ring % C::kRing;
+            if (ok && !__all_sync(0xffffffffu,
+                                  mbar_wait(pfull0 + 8 * slot, (ring / C::kRing) & 1, p.status)))
+                ok = false;
+            const int *d = dring + slot * C::kDescInts;
+            struct {
+                int kvh, row0, nrows, page_begin, page_end, slot;
+            } pc;
+            const int q0 = ok ? d[kDq0] : 0;
+            const int lq = ok ? d[kDlq] : 0;
+            const int lk = ok ? d[kDlk] : 0;
+            pc.kvh = ok ? d[kDkvh] : 0;
+            pc.row0 = ok ? d[kDrow0] : 0;
+            pc.nrows = ok ? d[kDnrows] : 0;
+            pc.page_begin = ok ? d[kDpb] : 0;
+            pc.page_end = ok ? d[kDpe] : 0;
+            pc.slot = ok ? d[kDslot] : -1;
+            const uint8_t *qtile = qring + slot * C::kQTileBytes;
             const int npages = pc.page_end - pc.page_begin;
 
             // visible-key limit of this thread's two rows (bottom-right causal)
@@ -150,14 +234,9 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
                 for (int ri = 0; ri < 4; ++ri) {
                     const int r = qr + (ri & 1) * 8;
                     const int col = ks * 16 + qc + (ri >> 1) * 8;
-                    uint32_t v = 0;
-                    if (r < pc.nrows) {
-                        const int pr = pc.row0 + r;
-                        const int64_t t = (int64_t)q0 + pr / p.g;
-                        const int h = pc.kvh * p.g + pr % p.g;
-                        v = __ldg(reinterpret_cast<const uint32_t *>(p.q + (t * p.hq + h) * D + col));
-                    }
-                    qa[ks][ri] = v;
+                    qa[ks][ri] = r < pc.nrows
+                                     ? *reinterpret_cast<const uint32_t *>(qtile + (r * D + col) * 2)
+                                     : 0u;
                 }
 
             float o[D / 8][4];
@@ -279,6 +358,8 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
                 mrg_l[qr + 8] = l[1];
             }
             named_barrier_sync(1, C::kConsumerWarps * 32);
+            // every consumer has its copy of the descriptor and Q: free the ring slot
+            if (threadIdx.x == 0) mbar_arrive(pempty0 + 8 * slot);
             const int tid = threadIdx.x;
             for (int gi = tid; gi < kDecRows * (D / 4); gi += C::kConsumerWarps * 32) {
                 const int row = gi / (D / 4);
