@@ -58,8 +58,9 @@ def _compile(cmd, log_path):
     return log_path
 
 
-# Register counts the kernels are written for (their warp roles and tiles
-# assume them); a build where ptxas picks another count is refused.
+# Register ceilings of the kernels: the prefill kernel runs 384 threads on one
+# SM, so a thread may hold at most 65536 / 384 -> 168 registers; a build where
+# ptxas goes past that is refused.
 LAUNCH_REGS = {"ua_prefill_kernel": 168}
 
 
@@ -80,9 +81,9 @@ def _check_launch_registers(log_path: str):
     regs = _registers_by_kernel(open(log_path).read())
     for mangled, n in regs.items():
         for name, want in LAUNCH_REGS.items():
-            if name in mangled and n != want:
-                raise RuntimeError(f"{name}: ptxas chose {n} registers per thread, the "
-                                   f"kernel is laid out for {want}; refusing to build")
+            if name in mangled and n > want:
+                raise RuntimeError(f"{name}: ptxas chose {n} registers per thread, more than "
+                                   f"the {want} its launch allows; refusing to build")
 
 
 def build(force: bool = False, verbose: bool = False, prefill=None) -> str:

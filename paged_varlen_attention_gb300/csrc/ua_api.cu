@@ -34,6 +34,7 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceState {
     bool ready = false;
+    int dev = 0;
     int sms = 0;
     int *status = nullptr;             // device address of g_ua_device_status
     bool events = false;
@@ -48,6 +49,64 @@ struct DeviceState {
 static std::mutex g_mutex;
 static DeviceState g_devices[kMaxDevices];
 static bool g_profile = false;
+
+// Page-locked staging for the plan, per device: a ring of buffers that grow
+// on demand, each reused only after the copy that last read it has finished
+// (an event recorded behind that copy).  From page-locked memory the copy is
+// one DMA that does not hold up the host thread; from pageable memory the
+// driver stages it through its own buffers first.
+struct PlanStaging {
+    static constexpr int kSlots = 8;
+    uint8_t *buf[kSlots] = {};
+    size_t cap[kSlots] = {};
+    cudaEvent_t done[kSlots] = {};
+    bool busy[kSlots] = {};
+    int next = 0;
+};
+static std::mutex g_stage_mutex;
+static PlanStaging g_staging[kMaxDevices];
+
+// Copies the plan into dst on the stream through the staging ring.
+static ua_status copy_plan_pinned(int dev, const Plan &plan, void *dst, cudaStream_t stream) {
+    const size_t bytes = plan.layout.blob_bytes;
+    std::lock_guard<std::mutex> lock(g_stage_mutex);
+    PlanStaging &st = g_staging[dev];
+    const int i = st.next;
+    st.next = (st.next + 1) % PlanStaging::kSlots;
+    if (st.busy[i]) {
+        if (cudaEventSynchronize(st.done[i]) != cudaSuccess) {
+            cudaGetLastError();
+            return UA_ERR_CUDA;
+        }
+        st.busy[i] = false;
+    }
+    if (!st.done[i] && cudaEventCreateWithFlags(&st.done[i], cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        st.done[i] = nullptr;
+        return UA_ERR_CUDA;
+    }
+    if (st.cap[i] < bytes) {
+        if (st.buf[i]) cudaFreeHost(st.buf[i]);
+        st.buf[i] = nullptr;
+        st.cap[i] = 0;
+        const size_t want = bytes + bytes / 2 + 4096;
+        void *h = nullptr;
+        if (cudaHostAlloc(&h, want, cudaHostAllocDefault) != cudaSuccess) {
+            cudaGetLastError();
+            return UA_ERR_CUDA;
+        }
+        st.buf[i] = static_cast<uint8_t *>(h);
+        st.cap[i] = want;
+    }
+    serialize_plan_to(plan, st.buf[i]);
+    if (cudaMemcpyAsync(dst, st.buf[i], bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaEventRecord(st.done[i], stream) != cudaSuccess) {
+        cudaGetLastError();
+        return UA_ERR_CUDA;
+    }
+    st.busy[i] = true;
+    return UA_OK;
+}
 
 static ua_status device_state(DeviceState **out) {
     int dev = 0;
@@ -68,6 +127,7 @@ static ua_status device_state(DeviceState **out) {
             cudaGetLastError();
             return UA_ERR_CUDA;
         }
+        s.dev = dev;
         s.sms = sms;
         s.status = static_cast<int *>(addr);
         s.ready = true;
@@ -294,16 +354,16 @@ extern "C" ua_status ua_profile_read(int32_t calls_back, float *ms, int32_t *lau
     return UA_OK;
 }
 
-extern "C" ua_status unified_attention(const void *q, const void *k_cache, const void *v_cache,
-                                       const int32_t *cu_seqlens_q, const int32_t *seqused_k,
-                                       const int32_t *block_table, float softmax_scale,
-                                       int32_t causal, void *out,
-                                       const int32_t *cu_seqlens_q_host,
-                                       const int32_t *seqused_k_host, int32_t num_seqs,
-                                       int32_t num_q_heads, int32_t num_kv_heads,
-                                       int32_t head_size, int32_t block_size, int32_t num_blocks,
-                                       int32_t block_table_stride, void *workspace,
-                                       size_t workspace_bytes, void *stream_ptr) {
+namespace ua {
+
+ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
+                        const int32_t *cu_seqlens_q, const int32_t *seqused_k,
+                        const int32_t *block_table, float softmax_scale, int32_t causal, void *out,
+                        const int32_t *cu_seqlens_q_host, const int32_t *seqused_k_host,
+                        int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                        int32_t head_size, int32_t block_size, int32_t num_blocks,
+                        int32_t block_table_stride, void *workspace, size_t workspace_bytes,
+                        void *stream_ptr, bool pinned_plan) {
     // ---- host-side checks, before any CUDA call
     Problem pr = make_problem(cu_seqlens_q_host, seqused_k_host, num_seqs, num_q_heads,
                               num_kv_heads, head_size, block_size, block_table_stride, causal);
@@ -335,7 +395,7 @@ extern "C" ua_status unified_attention(const void *q, const void *k_cache, const
         if (!workspace || workspace_bytes < L.total_bytes || !aligned(workspace, kAlign))
             return UA_ERR_WORKSPACE;
     }
-    serialize_plan(plan, blob);
+    if (!pinned_plan) serialize_plan(plan, blob);
 
     // ---- tensor maps: K/V page views (5-D), Q as [total_q, Hq, D]
     const int g = num_q_heads / num_kv_heads;
@@ -368,11 +428,15 @@ extern "C" ua_status unified_attention(const void *q, const void *k_cache, const
     const float scale_log2 = softmax_scale * 1.4426950408889634f;
 
     mark(0);
-    if (L.blob_bytes > 0 &&
-        cudaMemcpyAsync(ws, blob.data(), L.blob_bytes, cudaMemcpyHostToDevice, stream) !=
-            cudaSuccess) {
-        cudaGetLastError();
-        return UA_ERR_CUDA;
+    if (L.blob_bytes > 0) {
+        if (pinned_plan) {
+            st = copy_plan_pinned(ds->dev, plan, ws, stream);
+            if (st != UA_OK) return st;
+        } else if (cudaMemcpyAsync(ws, blob.data(), L.blob_bytes, cudaMemcpyHostToDevice,
+                                   stream) != cudaSuccess) {
+            cudaGetLastError();
+            return UA_ERR_CUDA;
+        }
     }
     mark(1);
     cudaError_t e = cudaSuccess;
@@ -446,4 +510,23 @@ extern "C" ua_status unified_attention(const void *q, const void *k_cache, const
         ++ds->calls;
     }
     return UA_OK;
+}
+
+}  // namespace ua
+
+extern "C" ua_status unified_attention(const void *q, const void *k_cache, const void *v_cache,
+                                       const int32_t *cu_seqlens_q, const int32_t *seqused_k,
+                                       const int32_t *block_table, float softmax_scale,
+                                       int32_t causal, void *out,
+                                       const int32_t *cu_seqlens_q_host,
+                                       const int32_t *seqused_k_host, int32_t num_seqs,
+                                       int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_size, int32_t block_size, int32_t num_blocks,
+                                       int32_t block_table_stride, void *workspace,
+                                       size_t workspace_bytes, void *stream) {
+    return ua::run_attention(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table,
+                             softmax_scale, causal, out, cu_seqlens_q_host, seqused_k_host,
+                             num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                             num_blocks, block_table_stride, workspace, workspace_bytes, stream,
+                             /*pinned_plan=*/true);
 }

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "ua_plan.h"
+#include "unified_attention.h"
 
 namespace ua {
 
@@ -64,5 +65,18 @@ cudaError_t launch_combine(int d, const CombineParams &p, int n_units, cudaStrea
 cudaError_t launch_prefill(int d, const PrefillParams &p, const CUtensorMap &tm_q,
                            const CUtensorMap &tm_k, const CUtensorMap &tm_v, int ctas,
                            cudaStream_t stream);
+
+// The whole call behind unified_attention (arguments as declared in
+// unified_attention.h).  pinned_plan: stage the plan through the library's
+// page-locked ring (allocated on first use) rather than copy it from pageable
+// memory; the entry point that must allocate nothing passes false.
+ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
+                        const int32_t *cu_seqlens_q, const int32_t *seqused_k,
+                        const int32_t *block_table, float softmax_scale, int32_t causal, void *out,
+                        const int32_t *cu_seqlens_q_host, const int32_t *seqused_k_host,
+                        int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                        int32_t head_size, int32_t block_size, int32_t num_blocks,
+                        int32_t block_table_stride, void *workspace, size_t workspace_bytes,
+                        void *stream, bool pinned_plan);
 
 }  // namespace ua

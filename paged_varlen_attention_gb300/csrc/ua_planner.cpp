@@ -198,20 +198,22 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
     L.total_bytes = (plan.pieces.empty() && plan.tiles.empty()) ? 0 : off;
 }
 
-void serialize_plan(const Plan &plan, std::vector<uint8_t> &blob) {
+void serialize_plan_to(const Plan &plan, uint8_t *dst) {
     const Layout &L = plan.layout;
-    blob.assign(L.blob_bytes, 0);
+    std::memset(dst, 0, L.blob_bytes);
     if (!plan.cta_begin.empty())
-        std::memcpy(blob.data() + L.off_cta, plan.cta_begin.data(),
-                    sizeof(int32_t) * plan.cta_begin.size());
+        std::memcpy(dst + L.off_cta, plan.cta_begin.data(), sizeof(int32_t) * plan.cta_begin.size());
     if (!plan.pieces.empty())
-        std::memcpy(blob.data() + L.off_pieces, plan.pieces.data(),
-                    sizeof(DecPiece) * plan.pieces.size());
+        std::memcpy(dst + L.off_pieces, plan.pieces.data(), sizeof(DecPiece) * plan.pieces.size());
     if (!plan.comb.empty())
-        std::memcpy(blob.data() + L.off_comb, plan.comb.data(), sizeof(CombUnit) * plan.comb.size());
+        std::memcpy(dst + L.off_comb, plan.comb.data(), sizeof(CombUnit) * plan.comb.size());
     if (!plan.tiles.empty())
-        std::memcpy(blob.data() + L.off_tiles, plan.tiles.data(),
-                    sizeof(PreTile) * plan.tiles.size());
+        std::memcpy(dst + L.off_tiles, plan.tiles.data(), sizeof(PreTile) * plan.tiles.size());
+}
+
+void serialize_plan(const Plan &plan, std::vector<uint8_t> &blob) {
+    blob.resize(plan.layout.blob_bytes);
+    if (!blob.empty()) serialize_plan_to(plan, blob.data());
 }
 
 }  // namespace ua

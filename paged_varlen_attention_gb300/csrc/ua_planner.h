@@ -28,6 +28,8 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
 
 // Packs the plan sections into one host blob laid out as plan.layout says.
 void serialize_plan(const Plan &plan, std::vector<uint8_t> &blob);
+// The same into dst, which holds at least plan.layout.blob_bytes bytes.
+void serialize_plan_to(const Plan &plan, uint8_t *dst);
 
 // True when the prefill (tcgen05) kernel can take this head grouping.
 bool prefill_supports(const Problem &p);

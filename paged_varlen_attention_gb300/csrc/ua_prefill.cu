@@ -8,26 +8,42 @@
 // there done "to ensure the Tensor cores are well used").
 //
 // One persistent CTA per SM walks its work items (longest first).  A work item
-// is a pair of 128-row MMA tiles, A and B, of the same (sequence, KV head):
-// both use every K/V tile the CTA loads, and their softmax steps run at the
-// same time on two warpgroups, which hides each other's latency.  Roles:
-//   warps 0-3 softmax of tile A, one thread per row (TMEM lane)
-//   warps 4-7 softmax of tile B
-//             scale into the log2 domain, bottom-right causal mask, row max,
-//             exp2, row sum, P as bf16 written over S in TMEM; O is rescaled
-//             only when a row max grows by more than 2^8 (the stale max
-//             cancels in O / l); the epilogue divides by l and writes bf16.
-//   warp 8    allocates TMEM (S_A, O_A, S_B, O_B: 4 x 128 columns) and issues
-//             the MMAs from one thread, per 128-key tile j:
-//               S_X = Q_X K_j^T   (M 128, N 128, K D; both operands K-major)
-//               O_X += P_X V_j    (A = P in TMEM as bf16, B = V MN-major)
-//   warp 9    TMA producer of the Q tiles (box {64, G, 128/G} of [T, Hq, D])
-//             and of V: one box per 16-token page (a 5-D view of the cache,
-//             so one box holds all D columns of the page), page-major.
-//   warp 10   TMA producer of K: two boxes per page ({64, 1, 16} of
-//             [pages*16, Hkv, D]), into [chunk][key][64] so that each 64-wide
-//             column chunk of the 128-key tile is one K-major operand.
-// Pages past a tile's last visible key are read out of bounds (zero fill)
+// is a pair of 128-row MMA tiles, A and B, of the same (sequence, KV head);
+// both use every K/V step the CTA loads.  A step is 64 keys (4 pages).
+//
+// TMEM (512 columns) holds, per tile X: two S buffers of 64 fp32 columns
+// (steps alternate between them; P is written as bf16 pairs over the first 32
+// columns of its S) and O (D fp32 columns).  With two S buffers the scores of
+// step j+1 are computed while the softmax of step j runs and while P V of
+// step j-1 is still reading its P, so each tile keeps up to three MMA groups
+// (S, S, P V) in flight and the tensor core overlaps them across A and B: a
+// chain of MMAs into one accumulator is latency-bound, independent chains are
+// not.
+//
+// Roles (12 warps):
+//   warps 0-3   softmax of tile A, one thread per row (TMEM lane): scale into
+//               the log2 domain, bottom-right causal mask, row max, exp2, row
+//               sum, P as bf16 into TMEM.  O is rescaled only when a row max
+//               grows by more than 2^8 (the stale max cancels in O / l).  The
+//               epilogue divides by l and writes bf16 rows of out.
+//   warps 4-7   the same for tile B
+//   warp 8      allocates TMEM; issues tile A's MMAs (whole warp, one elected
+//               lane):  S_A = Q_A K_j^T  (M 128, N 64, K D; K-major operands)
+//                       O_A += P_A V_j   (A = P in TMEM, B = V MN-major)
+//               in the order S(0), S(1), then P V(j) and S(j+2) as each buffer
+//               frees up.
+//   warp 11     the same for tile B
+//   warp 9      TMA producer of the Q tiles (box {64, G, 128/G} of [T, Hq, D])
+//               and of V (one box per 16-token page: a 5-D view of the cache,
+//               so one box holds all D columns of the page).  The step that
+//               holds a sequence's last, partial page lands on a barrier of its
+//               own: this warp zeroes the rows past the context (they may hold
+//               anything, NaN included, and 0 x NaN is NaN in P V) before it
+//               releases the step.
+//   warp 10     TMA producer of K: per page one {64, 1, 16} box per 64 columns
+//               of [pages*16, Hkv, D], into [chunk][key][64] so that each
+//               64-wide column chunk of the step is one K-major operand.
+// Pages past a step's last visible key are read out of bounds (zero fill)
 // instead of from the block table.  Every wait is bounded (see
 // ua_device.cuh); TMEM is always freed.
 #include "ua_device.cuh"
@@ -35,48 +51,52 @@
 
 namespace ua {
 
+constexpr int kStep = 64;                            // keys per KV step
+constexpr int kStepPages = kStep / kBlockSize;       // 4 pages
+
 template <int D>
 struct PreCfg {
     static constexpr int kChunks = D / 64;
     static constexpr int kQBytes = kPreRows * D * 2;          // one 128-row Q tile
-    static constexpr int kKvBytes = kKvTile * D * 2;          // one 128-key K (or V) tile
-    static constexpr int kChunkBytes = kKvTile * 128;         // K: 128 rows x 64 columns
+    static constexpr int kKvBytes = kStep * D * 2;            // one step of K (or V)
+    static constexpr int kKChunkBytes = kStep * 128;          // K: 64 keys x 64 columns
     static constexpr int kPageBytes = kBlockSize * D * 2;     // V: one 16-token page
-    static constexpr int kThreads = 352;                      // 11 warps: 3 per SMSP, 168 regs
-    static constexpr int kKStages = 3;
-    static constexpr int kVStages = 2;
+    static constexpr int kThreads = 384;                      // 12 warps: 3 per SMSP, 168 regs
+    static constexpr int kKStages = 4;
+    static constexpr int kVStages = 4;
     static constexpr int kTmemCols = 512;
-    static constexpr uint32_t kColS = 0;                      // + 256 * sub-tile
-    static constexpr uint32_t kColO = 128;
-    // Q x2 (A, B), K x3, V x2, barriers; one CTA owns the SM (and its TMEM)
+    static constexpr uint32_t kColO = 128;                    // + 256 * tile; S buffers at 0, 64
+    // Q x2 (A, B), K x4, V x4, barriers; one CTA owns the SM (and its TMEM)
     static constexpr size_t kUsed = 1024 + 2 * (size_t)kQBytes +
                                     (size_t)(kKStages + kVStages) * kKvBytes + 512;
     static constexpr size_t kSmemBytes = kUsed < 120 * 1024 ? 120 * 1024 : kUsed;
     static constexpr float kRescaleThreshold = 8.0f;          // log2 units
 };
 
-// mbarrier slots ([2] = one per sub-tile A/B unless noted)
+// mbarrier slots.  [2]: one per tile X; [4] of S / P / P V: index 2 * X + b,
+// b the S buffer.
 enum : int {
     kBarQFull = 0,      // [2]
     kBarQEmpty = 2,     // [2]
-    kBarKFull = 4,      // [3] K stages
-    kBarKEmpty = 7,     // [3]
-    kBarVFull = 10,     // [2] V stages
-    kBarVEmpty = 12,    // [2]
-    kBarSFull = 14,     // [2]
-    kBarPFull = 16,     // [2] (128 arrivals)
-    kBarPvDone = 18,    // [2]
-    kBarDrain = 20,
-    kNumBars = 21
+    kBarKFull = 4,      // [4] K stages
+    kBarKEmpty = 8,     // [4] 2 arrivals: both MMA warps
+    kBarVFull = 12,     // [4] V stages
+    kBarVEmpty = 16,    // [4] 2 arrivals: both MMA warps
+    kBarVTail = 20,     // TMA of a step that holds a sequence's partial last page
+    kBarSFull = 21,     // [4]
+    kBarPFull = 25,     // [4] 128 arrivals
+    kBarPvDone = 29,    // [4]
+    kBarDrain = 33,     // [2]
+    kNumBars = 35
 };
 
 struct SubInfo {
-    int row0, nrows, n;      // packed rows of this 128-row sub-tile; its KV tiles
+    int row0, nrows, n;      // packed rows of this 128-row tile; its KV steps
     int kend_max, kend_lo;   // keys visible to its last / first row
 };
 
 struct PairInfo {
-    int seq, q0, lq, lk, kvh, n;   // n: KV tiles of the pair (= max over sub-tiles)
+    int seq, q0, lq, lk, kvh, n;   // n: KV steps of the pair (= max over tiles)
     SubInfo sub[2];
 };
 
@@ -102,7 +122,7 @@ __device__ __forceinline__ PairInfo load_pair(const PrefillParams &p, int t) {
         if (s.nrows > 0) {
             s.kend_max = visible_keys(p, pi.lq, pi.lk, s.row0 + s.nrows - 1);
             s.kend_lo = visible_keys(p, pi.lq, pi.lk, s.row0);
-            s.n = (s.kend_max + kKvTile - 1) / kKvTile;
+            s.n = (s.kend_max + kStep - 1) / kStep;
         } else {
             s.kend_max = s.kend_lo = 0;
             s.n = 0;
@@ -112,13 +132,13 @@ __device__ __forceinline__ PairInfo load_pair(const PrefillParams &p, int t) {
     return pi;
 }
 
-// Block ids of the 8 pages of KV tile j (lanes 0-7 load; out-of-range or
+// Block ids of the 4 pages of KV step j (lanes 0-3 load; out-of-range or
 // not-needed pages give num_blocks, which TMA reads as zeros).
-__device__ __forceinline__ int tile_block_id(const PrefillParams &p, const int32_t *bt_row, int j,
+__device__ __forceinline__ int step_block_id(const PrefillParams &p, const int32_t *bt_row, int j,
                                              int kend, int lane) {
     int bid = p.num_blocks;
-    const int page = j * (kKvTile / kBlockSize) + lane;
-    if (lane < kKvTile / kBlockSize && page * kBlockSize < kend) {
+    const int page = j * kStepPages + lane;
+    if (lane < kStepPages && page * kBlockSize < kend) {
         bid = __ldg(bt_row + page);
         if (bid < 0 || bid >= p.num_blocks) {
             record_status(p.status, UA_DEVICE_BAD_BLOCK_ID_BIT);
@@ -126,6 +146,45 @@ __device__ __forceinline__ int tile_block_id(const PrefillParams &p, const int32
         }
     }
     return bid;
+}
+
+// tcgen05.mma / commit issued by one elected lane of a converged warp.
+__device__ __forceinline__ void umma_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_warp(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar)
+        : "memory");
 }
 
 template <int D, bool kPos>
@@ -138,8 +197,8 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sq = smem_u32(smem);                         // Q[2]: A, B
-    const uint32_t sk = sq + 2 * C::kQBytes;                    // K[3]: [chunk][128 keys][64]
-    const uint32_t sv = sk + C::kKStages * C::kKvBytes;         // V[2]: [page][chunk][16][64]
+    const uint32_t sk = sq + 2 * C::kQBytes;                    // K[4]: [chunk][64 keys][64]
+    const uint32_t sv = sk + C::kKStages * C::kKvBytes;         // V[4]: [page][chunk][16][64]
     uint8_t *sv_ptr = smem + 2 * C::kQBytes + C::kKStages * C::kKvBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sv_ptr + C::kVStages * C::kKvBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
@@ -153,17 +212,18 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(kBarQFull + i), 1);
             mbar_init(bar(kBarQEmpty + i), 1);
+            mbar_init(bar(kBarDrain + i), 1);
+        }
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(bar(kBarKFull + i), 1);
+            mbar_init(bar(kBarKEmpty + i), 2);
             mbar_init(bar(kBarVFull + i), 1);
-            mbar_init(bar(kBarVEmpty + i), 1);
+            mbar_init(bar(kBarVEmpty + i), 2);
             mbar_init(bar(kBarSFull + i), 1);
             mbar_init(bar(kBarPFull + i), 128);
             mbar_init(bar(kBarPvDone + i), 1);
         }
-        for (int i = 0; i < C::kKStages; ++i) {
-            mbar_init(bar(kBarKFull + i), 1);
-            mbar_init(bar(kBarKEmpty + i), 1);
-        }
-        mbar_init(bar(kBarDrain), 1);
+        mbar_init(bar(kBarVTail), 1);
         fence_barrier_init();
     }
     if (warp == 8) {
@@ -180,9 +240,9 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
             prefetch_tensormap(&tm_q);
             prefetch_tensormap(&tm_vp);
         }
-        const uint64_t pol_kv = l2_policy_evict_last();   // K/V tiles are re-read by sibling tiles
+        const uint64_t pol_kv = l2_policy_evict_last();   // K/V steps are re-read by sibling items
         bool ok = true;
-        uint32_t e = 0, v_issued = 0;
+        uint32_t e = 0, v_issued = 0, tails = 0;
         uint32_t q_issued[2] = {0, 0};
         for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
             const PairInfo pi = load_pair(p, t);
@@ -191,7 +251,7 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
 #pragma unroll
                 for (int x = 0; x < 2; ++x) {
                     if (!good || pi.sub[x].nrows == 0) continue;
-                    // Q buffer x is free once the last S of its previous sub-tile is done
+                    // Q buffer x is free once the last S of its previous tile is done
                     if (q_issued[x] > 0 &&
                         !mbar_wait(bar(kBarQEmpty + x), (q_issued[x] - 1) & 1, p.status)) {
                         good = 0;
@@ -208,26 +268,57 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
             ok = __shfl_sync(0xffffffffu, good, 0) != 0;
             const int kend = max(pi.sub[0].kend_max, pi.sub[1].kend_max);
             const int32_t *bt_row = p.block_table + (int64_t)pi.seq * p.bt_stride;
+            // the step holding the sequence's partial last page, if a row sees it
+            const int last_page_start = (pi.lk - 1) & ~(kBlockSize - 1);
+            const int tail_step = ((pi.lk & (kBlockSize - 1)) != 0 && last_page_start < kend)
+                                      ? last_page_start / kStep : -1;
             for (int j = 0; j < pi.n && ok; ++j, ++e) {
-                const int bid = tile_block_id(p, bt_row, j, kend, lane);
-                int b[kKvTile / kBlockSize];
+                const int bid = step_block_id(p, bt_row, j, kend, lane);
+                int b[kStepPages];
 #pragma unroll
-                for (int i = 0; i < kKvTile / kBlockSize; ++i) b[i] = __shfl_sync(0xffffffffu, bid, i);
+                for (int i = 0; i < kStepPages; ++i) b[i] = __shfl_sync(0xffffffffu, bid, i);
                 const uint32_t vs = e % C::kVStages, vph = (e / C::kVStages) & 1;
+                const bool tail = (j == tail_step);
+                const uint32_t land = tail ? bar(kBarVTail) : bar(kBarVFull + vs);
                 good = 1;
                 if (lane == 0) {
                     if (!mbar_wait(bar(kBarVEmpty + vs), vph ^ 1, p.status)) {
                         good = 0;
                     } else {
-                        mbar_arrive_expect_tx(bar(kBarVFull + vs), C::kKvBytes);
+                        mbar_arrive_expect_tx(land, C::kKvBytes);
 #pragma unroll
-                        for (int i = 0; i < kKvTile / kBlockSize; ++i)
+                        for (int i = 0; i < kStepPages; ++i)
                             tma_load_5d_hint(sv + vs * C::kKvBytes + i * C::kPageBytes, &tm_vp, 0, 0, 0,
-                                             pi.kvh, b[i], bar(kBarVFull + vs), pol_kv);
+                                             pi.kvh, b[i], land, pol_kv);
                         ++v_issued;
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+                if (ok && tail) {
+                    // wait for this step's data, zero the key rows past the context in the
+                    // last page, then release the step to the MMA warps
+                    const bool landed = mbar_wait(bar(kBarVTail), tails & 1, p.status);
+                    ++tails;
+                    if (!__all_sync(0xffffffffu, landed)) {
+                        ok = false;
+                    } else {
+                        const int k0 = pi.lk - j * kStep;                       // first row to clear
+                        const int k1 = last_page_start + kBlockSize - j * kStep;  // end of the page
+                        constexpr int per_row = C::kChunks * 8;                 // 16-byte pieces per key row
+                        for (int u = lane; u < (k1 - k0) * per_row; u += 32) {
+                            const int key = k0 + u / per_row;
+                            const int c = (u % per_row) / 8;
+                            const int piece = u % 8;
+                            *reinterpret_cast<uint4 *>(sv_ptr + vs * C::kKvBytes +
+                                                       (key / kBlockSize) * C::kPageBytes + c * 2048 +
+                                                       (key % kBlockSize) * 128 + piece * 16) =
+                                make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(kBarVFull + vs));
+                    }
+                }
             }
         }
         // drain: the last loads issued must land before the CTA can exit
@@ -248,10 +339,10 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
             const int kend = max(pi.sub[0].kend_max, pi.sub[1].kend_max);
             const int32_t *bt_row = p.block_table + (int64_t)pi.seq * p.bt_stride;
             for (int j = 0; j < pi.n && ok; ++j, ++e) {
-                const int bid = tile_block_id(p, bt_row, j, kend, lane);
-                int b[kKvTile / kBlockSize];
+                const int bid = step_block_id(p, bt_row, j, kend, lane);
+                int b[kStepPages];
 #pragma unroll
-                for (int i = 0; i < kKvTile / kBlockSize; ++i) b[i] = __shfl_sync(0xffffffffu, bid, i);
+                for (int i = 0; i < kStepPages; ++i) b[i] = __shfl_sync(0xffffffffu, bid, i);
                 const uint32_t ks = e % C::kKStages, kph = (e / C::kKStages) & 1;
                 int good = 1;
                 if (lane == 0) {
@@ -260,10 +351,10 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
                     } else {
                         mbar_arrive_expect_tx(bar(kBarKFull + ks), C::kKvBytes);
 #pragma unroll
-                        for (int i = 0; i < kKvTile / kBlockSize; ++i)
+                        for (int i = 0; i < kStepPages; ++i)
 #pragma unroll
                             for (int c = 0; c < C::kChunks; ++c)
-                                tma_load_3d_hint(sk + ks * C::kKvBytes + c * C::kChunkBytes + i * 2048,
+                                tma_load_3d_hint(sk + ks * C::kKvBytes + c * C::kKChunkBytes + i * 2048,
                                                  &tm_k, c * 64, pi.kvh, b[i] * kBlockSize,
                                                  bar(kBarKFull + ks), pol_kv);
                         ++k_issued;
@@ -276,163 +367,168 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
             for (uint32_t x = (k_issued > (uint32_t)C::kKStages ? k_issued - C::kKStages : 0); x < k_issued; ++x)
                 mbar_wait(bar(kBarKFull + x % C::kKStages), (x / C::kKStages) & 1, p.status);
         }
-    } else if (warp == 8) {
-        // ================================================================ MMA issuer
-        constexpr uint32_t idesc_s = umma_idesc_bf16(kPreRows, kKvTile, 0, 0);
+    } else if (warp == 8 || warp == 11) {
+        // ================================================================ MMA issuers (A: warp 8, B: warp 11)
+        const int x = warp == 8 ? 0 : 1;
+        constexpr uint32_t idesc_s = umma_idesc_bf16(kPreRows, kStep, 0, 0);
         constexpr uint32_t idesc_pv = umma_idesc_bf16(kPreRows, D, 0, 1);
+        const uint32_t tbase = tmem + (uint32_t)x * 256;
+        const uint32_t qbase = sq + (uint32_t)x * C::kQBytes;
         bool ok = true;
-        uint32_t e = 0, issued_any = 0;
-        uint32_t qcnt[2] = {0, 0};   // Q tiles consumed per sub-tile slot
-        uint32_t ecnt[2] = {0, 0};   // S / P V events per sub-tile slot
-        if (lane == 0) {
-            for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
-                const PairInfo pi = load_pair(p, t);
-                const int nx[2] = {pi.sub[0].n, pi.sub[1].n};
-                for (int x = 0; x < 2 && ok; ++x)
-                    if (nx[x] > 0 && !mbar_wait(bar(kBarQFull + x), qcnt[x] & 1, p.status)) ok = false;
-                if (!ok) break;
-                for (int j = 0; j < pi.n && ok; ++j, ++e) {
-                    const uint32_t ks = e % C::kKStages, kph = (e / C::kKStages) & 1;
-                    if (!mbar_wait(bar(kBarKFull + ks), kph, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    // ---- S_X = Q_X K_j^T
-                    for (int x = 0; x < 2; ++x) {
-                        if (j >= nx[x]) continue;
-                        // S_X is overwritten: its P from the previous event must be consumed
-                        if (ecnt[x] > 0 &&
-                            !mbar_wait(bar(kBarPvDone + x), (ecnt[x] - 1) & 1, p.status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t s_col = tmem + x * 256 + C::kColS;
+        bool issued_any = false;
+        uint32_t e = 0, qcnt = 0;
+        uint32_t scnt = 0, pcnt = 0;   // S and P V issued by this warp over all items; P V k reads S k
+        // S of KV event ev into buffer scnt % 2, which is free once P V scnt-2 has read its P
+        auto issue_s = [&](uint32_t ev) -> bool {
+            const uint32_t b = scnt & 1;
+            if (scnt >= 2 &&
+                !mbar_wait(bar(kBarPvDone + 2 * x + b), ((scnt - 2) >> 1) & 1, p.status))
+                return false;
+            const uint32_t ks = ev % C::kKStages, kph = (ev / C::kKStages) & 1;
+            if (!mbar_wait(bar(kBarKFull + ks), kph, p.status)) return false;
+            tc_fence_after();
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-                            const uint64_t adesc = umma_desc_sw128(sq + x * C::kQBytes + off, 16, 1024);
-                            const uint64_t bdesc = umma_desc_sw128(sk + ks * C::kKvBytes + off, 16, 1024);
-                            umma_ss(s_col, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
-                        }
-                        issued_any = 1;
-                        umma_commit(bar(kBarSFull + x));
-                        if (j == nx[x] - 1) umma_commit(bar(kBarQEmpty + x));
-                    }
-                    if (!ok) break;
-                    umma_commit(bar(kBarKEmpty + ks));
-                    // ---- O_X += P_X V_j
-                    const uint32_t vs = e % C::kVStages, vph = (e / C::kVStages) & 1;
-                    if (!mbar_wait(bar(kBarVFull + vs), vph, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    for (int x = 0; x < 2; ++x) {
-                        if (j >= nx[x]) continue;
-                        if (!mbar_wait(bar(kBarPFull + x), ecnt[x] & 1, p.status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t p_col = tmem + x * 256 + C::kColS;
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t qoff = (kk >> 2) * (kPreRows * 128) + (kk & 3) * 32;
+                const uint32_t koff = (kk >> 2) * C::kKChunkBytes + (kk & 3) * 32;
+                umma_ss_warp(tbase + b * kStep, umma_desc_sw128(qbase + qoff, 16, 1024),
+                             umma_desc_sw128(sk + ks * C::kKvBytes + koff, 16, 1024), idesc_s,
+                             kk > 0 ? 1u : 0u);
+            }
+            umma_commit_warp(bar(kBarSFull + 2 * x + b));
+            umma_commit_warp(bar(kBarKEmpty + ks));
+            ++scnt;
+            issued_any = true;
+            return true;
+        };
+        // O += P V for S pcnt, V of KV event ev; first: O starts from zero
+        auto issue_pv = [&](uint32_t ev, bool first) -> bool {
+            const uint32_t b = pcnt & 1;
+            if (!mbar_wait(bar(kBarPFull + 2 * x + b), (pcnt >> 1) & 1, p.status)) return false;
+            const uint32_t vs = ev % C::kVStages, vph = (ev / C::kVStages) & 1;
+            if (!mbar_wait(bar(kBarVFull + vs), vph, p.status)) return false;
+            tc_fence_after();
 #pragma unroll
-                        for (int kk = 0; kk < kKvTile / 16; ++kk) {
-                            // 16 keys per step = one page of V: P columns kk*8 .. +8 (bf16
-                            // pairs); V page kk is [chunk][16 keys][64], MN-major: 64-wide
-                            // d chunks 2 KB apart (LBO), 8-key groups 1 KB apart (SBO)
-                            const uint64_t bdesc = umma_desc_sw128(sv + vs * C::kKvBytes + kk * C::kPageBytes,
-                                                                   kBlockSize * 128, 1024);
-                            umma_ts(tmem + x * 256 + C::kColO, p_col + kk * 8, bdesc, idesc_pv,
-                                    (j == 0 && kk == 0) ? 0u : 1u);
-                        }
-                        umma_commit(bar(kBarPvDone + x));
-                        ++ecnt[x];
-                    }
-                    if (!ok) break;
-                    umma_commit(bar(kBarVEmpty + vs));
+            for (int kk = 0; kk < kStepPages; ++kk) {
+                // 16 keys per MMA = one page of V: P columns b*64 + kk*8 .. +8 (bf16
+                // pairs); V page kk is [chunk][16 keys][64], MN-major: 64-wide d
+                // chunks 2 KB apart (LBO), 8-key groups 1 KB apart (SBO)
+                const uint64_t bdesc =
+                    umma_desc_sw128(sv + vs * C::kKvBytes + kk * C::kPageBytes, kBlockSize * 128, 1024);
+                umma_ts_warp(tbase + C::kColO, tbase + b * kStep + kk * 8, bdesc, idesc_pv,
+                             (first && kk == 0) ? 0u : 1u);
+            }
+            umma_commit_warp(bar(kBarPvDone + 2 * x + b));
+            umma_commit_warp(bar(kBarVEmpty + vs));
+            ++pcnt;
+            return true;
+        };
+        for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+            const PairInfo pi = load_pair(p, t);
+            const int nx = x ? pi.sub[1].n : pi.sub[0].n;
+            if (nx > 0) {
+                if (!mbar_wait(bar(kBarQFull + x), qcnt & 1, p.status)) {
+                    ok = false;
+                    break;
                 }
-                for (int x = 0; x < 2; ++x)
-                    if (nx[x] > 0) ++qcnt[x];
+                ++qcnt;
+                ok = issue_s(e);
+                if (ok && nx > 1) ok = issue_s(e + 1);
+                if (ok && nx <= 2) umma_commit_warp(bar(kBarQEmpty + x));   // after the last S
+                for (int j = 0; j < nx && ok; ++j) {
+                    ok = issue_pv(e + j, j == 0);
+                    if (ok && j + 2 < nx) {
+                        ok = issue_s(e + j + 2);
+                        if (ok && j + 2 == nx - 1) umma_commit_warp(bar(kBarQEmpty + x));
+                    }
+                }
             }
-            // every MMA issued has completed before TMEM is released
-            if (issued_any) {
-                umma_commit(bar(kBarDrain));
-                mbar_wait(bar(kBarDrain), 0, p.status);
+            // KV steps of the pair this tile does not see: release them, in order
+            for (int j = nx; j < pi.n && ok; ++j) {
+                const uint32_t ev = e + j;
+                if (!mbar_wait(bar(kBarKFull + ev % C::kKStages), (ev / C::kKStages) & 1, p.status) ||
+                    !mbar_wait(bar(kBarVFull + ev % C::kVStages), (ev / C::kVStages) & 1, p.status)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_warp(bar(kBarKEmpty + ev % C::kKStages));
+                mbar_arrive_warp(bar(kBarVEmpty + ev % C::kVStages));
             }
+            e += pi.n;
+        }
+        // every MMA issued has completed before TMEM is released
+        if (issued_any) {
+            umma_commit_warp(bar(kBarDrain + x));
+            mbar_wait(bar(kBarDrain + x), 0, p.status);
         }
         __syncwarp();
     } else if (warp < 8) {
         // ================================================================ softmax + epilogue
-        const int x = warp >> 2;                        // sub-tile A (0) or B (1)
+        const int x = warp >> 2;                        // tile A (0) or B (1)
         const int quarter = warp & 3;                   // TMEM lanes this warp may touch
-        const int r = quarter * 32 + lane;              // row of the sub-tile = TMEM lane
+        const int r = quarter * 32 + lane;              // row of the tile = TMEM lane
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t s_addr = tmem + lane_off + x * 256 + C::kColS;
-        const uint32_t o_addr = tmem + lane_off + x * 256 + C::kColO;
+        const uint32_t s_addr = tmem + lane_off + (uint32_t)x * 256;
+        const uint32_t o_addr = s_addr + C::kColO;
         bool ok = true;
-        uint32_t e = 0, ex = 0;    // KV tile events of the CTA; S / P V events of this slot
+        uint32_t ex = 0;    // steps of this tile slot over all items (S k lives in buffer k % 2)
         for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
             const PairInfo pi = load_pair(p, t);
             const SubInfo si = x ? pi.sub[1] : pi.sub[0];
-            const int n_a = pi.sub[0].n;
-            if (si.nrows == 0) {
-                e += pi.n;
-                continue;
-            }
+            if (si.nrows == 0) continue;
             const int pr = si.row0 + r;
             const bool valid = r < si.nrows;
             const int i = pr / p.g;
             const int kend = (p.causal && valid) ? min(pi.lk, pi.lk - pi.lq + i + 1) : pi.lk;
-            const int kend_pair = max(pi.sub[0].kend_max, pi.sub[1].kend_max);
             float m_run = -INFINITY;
             float l = 0.f;
             for (int j = 0; j < si.n; ++j, ++ex) {
-                if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + x), ex & 1, p.status))) {
+                const uint32_t b = ex & 1;
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(bar(kBarSFull + 2 * x + b), (ex >> 1) & 1, p.status))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                // The scores of this row.  With a positive scale (kPos, the usual case)
+                // The 64 scores of this row.  With a positive scale (kPos, the usual case)
                 // the max is taken on the raw scores and the scale is folded into the
                 // exponent's FMA; otherwise the scores are scaled first.  Keys at or
-                // past the row's limit (diagonal and tail tiles only) become -inf.
-                const bool masked = (j + 1) * kKvTile > si.kend_lo;   // diagonal / tail tile
-                const int lim = kend - j * kKvTile;                    // visible keys of this tile
-                constexpr uint32_t kNegInf = 0xff800000u;
-                // pass 1: the masked row max (the scores stay in TMEM)
-                float mx;
-                {
-                    uint32_t xs[kKvTile];
-                    tmem_ld128(s_addr, xs);
-                    if (!kPos) {
+                // past the row's limit (diagonal and tail steps only) become -inf.
+                uint32_t xs[kStep];
+                tmem_ld32(s_addr + b * kStep, *reinterpret_cast<uint32_t(*)[32]>(&xs[0]));
+                tmem_ld32(s_addr + b * kStep + 32, *reinterpret_cast<uint32_t(*)[32]>(&xs[32]));
+                if (!kPos) {
 #pragma unroll
-                        for (int k = 0; k < kKvTile; ++k)
-                            xs[k] = __float_as_uint(__uint_as_float(xs[k]) * p.scale_log2);
-                    }
-                    if (masked) {
-#pragma unroll
-                        for (int k = 0; k < kKvTile; ++k) xs[k] = k < lim ? xs[k] : kNegInf;
-                    }
-                    float m8[8];
-#pragma unroll
-                    for (int a = 0; a < 8; ++a) m8[a] = __uint_as_float(xs[a]);
-#pragma unroll
-                    for (int k = 8; k < kKvTile; k += 2)
-                        m8[(k >> 1) & 7] = fmax3(m8[(k >> 1) & 7], __uint_as_float(xs[k]),
-                                                 __uint_as_float(xs[k + 1]));
-                    mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
-                               fmaxf(m8[6], m8[7]));
-                    if (kPos) mx *= p.scale_log2;
+                    for (int k = 0; k < kStep; ++k)
+                        xs[k] = __float_as_uint(__uint_as_float(xs[k]) * p.scale_log2);
                 }
+                constexpr uint32_t kNegInf = 0xff800000u;
+                if ((j + 1) * kStep > si.kend_lo) {
+                    const int lim = kend - j * kStep;               // visible keys of this step
+#pragma unroll
+                    for (int k = 0; k < kStep; ++k) xs[k] = k < lim ? xs[k] : kNegInf;
+                }
+                float m8[8];
+#pragma unroll
+                for (int a = 0; a < 8; ++a) m8[a] = __uint_as_float(xs[a]);
+#pragma unroll
+                for (int k = 8; k < kStep; k += 2)
+                    m8[(k >> 1) & 7] = fmax3(m8[(k >> 1) & 7], __uint_as_float(xs[k]),
+                                             __uint_as_float(xs[k + 1]));
+                float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
+                                 fmaxf(m8[6], m8[7]));
+                if (kPos) mx *= p.scale_log2;
                 if (j == 0) {
                     m_run = mx;
                 } else if (__any_sync(0xffffffffu, mx > m_run + C::kRescaleThreshold)) {
                     // a row max of this warp grew a lot: move the warp's rows to their
-                    // new max and rescale O (after P V of the previous tile) and l.
+                    // new max and rescale O (after the P V of the previous step) and l.
                     // TMEM loads / stores are warp-wide, so the whole warp takes this path.
                     const float m_new = fmaxf(m_run, mx);
                     const float alpha = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run - m_new);
-                    const bool waited = mbar_wait(bar(kBarPvDone + x), (ex - 1) & 1, p.status);
+                    const uint32_t pb = (ex - 1) & 1;
+                    const bool waited =
+                        mbar_wait(bar(kBarPvDone + 2 * x + pb), ((ex - 1) >> 1) & 1, p.status);
                     if (!__all_sync(0xffffffffu, waited)) {
                         ok = false;
                         break;
@@ -450,76 +546,33 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
                     m_run = m_new;
                 }
                 const float mu = (m_run == -INFINITY) ? 0.f : m_run;
-                // pass 2, 64 keys at a time: p = 2^(s * c - mu) (two lanes of work per
-                // FMA), summed in 8 chains, packed to bf16 pairs; keys 64h..64h+63 go
-                // to columns 32h..32h+31, which this pass has already read
+                // p = 2^(s * c - mu), two lanes of work per FMA, summed in 4 chains,
+                // packed to bf16 pairs over the first 32 columns of this S buffer
                 const float2 c2 = kPos ? make_float2(p.scale_log2, p.scale_log2) : make_float2(1.f, 1.f);
                 const float2 nmu2 = make_float2(-mu, -mu);
                 float2 l4[4];
 #pragma unroll
                 for (int a = 0; a < 4; ++a) l4[a] = make_float2(0.f, 0.f);
+                uint32_t pk[32];
 #pragma unroll
-                for (int h = 0; h < kKvTile / 64; ++h) {
-                    uint32_t xs[64];
-                    tmem_ld32(s_addr + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&xs[0]));
-                    tmem_ld32(s_addr + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&xs[32]));
-                    if (!kPos) {
-#pragma unroll
-                        for (int k = 0; k < 64; ++k)
-                            xs[k] = __float_as_uint(__uint_as_float(xs[k]) * p.scale_log2);
-                    }
-                    if (masked) {
-#pragma unroll
-                        for (int k = 0; k < 64; ++k) xs[k] = 64 * h + k < lim ? xs[k] : kNegInf;
-                    }
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const float2 y = ffma2(make_float2(__uint_as_float(xs[2 * k]),
-                                                           __uint_as_float(xs[2 * k + 1])), c2, nmu2);
-                        const float2 pv = make_float2(fast_exp2(y.x), fast_exp2(y.y));
-                        l4[k & 3] = fadd2(l4[k & 3], pv);
-                        pk[k] = pack_bf16x2(pv.x, pv.y);
-                    }
-                    tmem_st32(s_addr + 32 * h, pk);
+                for (int k = 0; k < 32; ++k) {
+                    const float2 y = ffma2(make_float2(__uint_as_float(xs[2 * k]), __uint_as_float(xs[2 * k + 1])),
+                                           c2, nmu2);
+                    const float2 pv = make_float2(fast_exp2(y.x), fast_exp2(y.y));
+                    l4[k & 3] = fadd2(l4[k & 3], pv);
+                    pk[k] = pack_bf16x2(pv.x, pv.y);
                 }
+                tmem_st32(s_addr + b * kStep, pk);
                 l += ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) + ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y));
-                // V rows past the context in the sequence's last page may hold
-                // anything (NaN included): zero them before P V reads them.  The
-                // first sub-tile that uses this KV tile does it (its P V goes first).
-                const int last_page_start = (pi.lk - 1) & ~(kBlockSize - 1);
-                const bool zero_here = (x == 0) ? (warp == 0) : (warp == 4 && j >= n_a);
-                if (zero_here && (pi.lk & (kBlockSize - 1)) != 0 && ((pi.lk - 1) / kKvTile) == j &&
-                    last_page_start < kend_pair) {
-                    const uint32_t vs = (e + j) % C::kVStages, vph = ((e + j) / C::kVStages) & 1;
-                    if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarVFull + vs), vph, p.status))) {
-                        ok = false;
-                    } else {
-                        const int k0 = pi.lk - j * kKvTile;
-                        const int k1 = last_page_start + kBlockSize - j * kKvTile;
-                        const int per_row = C::kChunks * 8;     // 16-byte pieces per key row
-                        for (int u = lane; u < (k1 - k0) * per_row; u += 32) {
-                            const int key = k0 + u / per_row;
-                            const int c = (u % per_row) / 8;
-                            const int piece = u % 8;
-                            *reinterpret_cast<uint4 *>(sv_ptr + vs * C::kKvBytes +
-                                                       (key / kBlockSize) * C::kPageBytes + c * 2048 +
-                                                       (key % kBlockSize) * 128 + piece * 16) =
-                                make_uint4(0, 0, 0, 0);
-                        }
-                        fence_proxy_async_smem();
-                    }
-                    __syncwarp();
-                }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(kBarPFull + x));
-                if (!ok) break;
+                mbar_arrive(bar(kBarPFull + 2 * x + b));
             }
             if (!ok) break;
-            e += pi.n;
-            // ---- epilogue: O / l -> bf16 rows of out (after the last P V of this slot)
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarPvDone + x), (ex - 1) & 1, p.status))) {
+            // ---- epilogue: O / l -> bf16 rows of out (after the last P V of this tile)
+            const uint32_t lb = (ex - 1) & 1;
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(bar(kBarPvDone + 2 * x + lb), ((ex - 1) >> 1) & 1, p.status))) {
                 ok = false;
                 break;
             }
@@ -541,6 +594,8 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
                             pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv));
                 }
             }
+            // O is read: the next item's first P V (which overwrites O) waits for this
+            // warpgroup's P of that item, which comes after these loads
         }
     }
 

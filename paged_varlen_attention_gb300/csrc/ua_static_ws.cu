@@ -19,6 +19,7 @@
 #include <mutex>
 
 #include "unified_attention.h"
+#include "ua_kernels.h"
 
 namespace {
 
@@ -69,8 +70,10 @@ extern "C" ua_status unified_attention_no_alloc(
     void *ws = nullptr;
     st = static_workspace(&ws);
     if (st != UA_OK) return st;
-    return unified_attention(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table,
+    // the plan goes up from pageable memory: no page-locked buffer is allocated
+    return ua::run_attention(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table,
                              softmax_scale, causal, out, cu_seqlens_q_host, seqused_k_host,
                              num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
-                             num_blocks, block_table_stride, ws, kStaticBytes, stream);
+                             num_blocks, block_table_stride, ws, kStaticBytes, stream,
+                             /*pinned_plan=*/false);
 }
