@@ -69,10 +69,10 @@ struct alignas(16) PreTile {    // one prefill work item: up to two 128-row MMA 
     int32_t kvh;
     int32_t row0;
     int32_t nrows;
-    int32_t kv_tiles;    // 128-key tiles its last row visits
-    int32_t pad0;
-    int32_t pad1;
-    int32_t pad2;
+    int32_t kv_tiles;    // 128-key tiles its last row visits (the ordering key)
+    int32_t q0;          // cu_seqlens_q[seq]: first token of the sequence
+    int32_t lq;          // query tokens of the sequence
+    int32_t lk;          // seqused_k[seq]
 };
 
 // Problem description as seen by the planner (host metadata).

@@ -97,6 +97,9 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
             } else {
                 PreTile t{};
                 t.seq = s;
+                t.q0 = p.cu[s];
+                t.lq = lq;
+                t.lk = lk;
                 t.row0 = r0;
                 t.nrows = nr;
                 t.kv_tiles = (kend + kKvTile - 1) / kKvTile;

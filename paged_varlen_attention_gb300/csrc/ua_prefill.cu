@@ -66,9 +66,12 @@ struct PreCfg {
     static constexpr int kVStages = 4;
     static constexpr int kTmemCols = 512;
     static constexpr uint32_t kColO = 128;                    // + 256 * tile; S buffers at 0, 64
-    // Q x2 (A, B), K x4, V x4, barriers; one CTA owns the SM (and its TMEM)
+    // epilogue transpose scratch per softmax warp: 32 rows x (64 + 16 pad) bytes
+    static constexpr int kRowPitch = 80;
+    static constexpr int kScratchBytes = 8 * 32 * kRowPitch;
+    // Q x2 (A, B), K x4, V x4, scratch, barriers; one CTA owns the SM (and its TMEM)
     static constexpr size_t kUsed = 1024 + 2 * (size_t)kQBytes +
-                                    (size_t)(kKStages + kVStages) * kKvBytes + 512;
+                                    (size_t)(kKStages + kVStages) * kKvBytes + kScratchBytes + 512;
     static constexpr size_t kSmemBytes = kUsed < 120 * 1024 ? 120 * 1024 : kUsed;
     static constexpr float kRescaleThreshold = 8.0f;          // log2 units
 };
@@ -105,13 +108,14 @@ __device__ __forceinline__ int visible_keys(const PrefillParams &p, int lq, int 
     return min(lk, lk - lq + row / p.g + 1);
 }
 
-__device__ __forceinline__ PairInfo load_pair(const PrefillParams &p, int t) {
-    const PreTile pt = p.tiles[t];
+// The work item's geometry from its plan record (sequence offsets and lengths
+// are in the record, so no dependent loads of the metadata arrays).
+__device__ __forceinline__ PairInfo make_pair(const PrefillParams &p, const PreTile &pt) {
     PairInfo pi;
     pi.seq = pt.seq;
-    pi.q0 = p.cu[pt.seq];
-    pi.lq = p.cu[pt.seq + 1] - pi.q0;
-    pi.lk = p.seqused_k[pt.seq];
+    pi.q0 = pt.q0;
+    pi.lq = pt.lq;
+    pi.lk = pt.lk;
     pi.kvh = pt.kvh;
     pi.n = 0;
 #pragma unroll
@@ -131,6 +135,26 @@ __device__ __forceinline__ PairInfo load_pair(const PrefillParams &p, int t) {
     }
     return pi;
 }
+
+// Walks this CTA's work items; the record of the next item is loaded one item
+// ahead so that its latency hides behind the current one.
+struct ItemCursor {
+    int t;
+    PreTile cur;
+    __device__ __forceinline__ ItemCursor(const PrefillParams &p) : t(blockIdx.x) {
+        if (t < p.n_tiles) cur = p.tiles[t];
+    }
+    __device__ __forceinline__ bool valid(const PrefillParams &p) const { return t < p.n_tiles; }
+    // returns the current record and starts the load of the next one
+    __device__ __forceinline__ PreTile take(const PrefillParams &p, PreTile &next) const {
+        next = (t + (int)gridDim.x < p.n_tiles) ? p.tiles[t + gridDim.x] : cur;
+        return cur;
+    }
+    __device__ __forceinline__ void advance(const PreTile &next) {
+        cur = next;
+        t += gridDim.x;
+    }
+};
 
 // Block ids of the 4 pages of KV step j (lanes 0-3 load; out-of-range or
 // not-needed pages give num_blocks, which TMA reads as zeros).
@@ -200,7 +224,8 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
     const uint32_t sk = sq + 2 * C::kQBytes;                    // K[4]: [chunk][64 keys][64]
     const uint32_t sv = sk + C::kKStages * C::kKvBytes;         // V[4]: [page][chunk][16][64]
     uint8_t *sv_ptr = smem + 2 * C::kQBytes + C::kKStages * C::kKvBytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sv_ptr + C::kVStages * C::kKvBytes);
+    uint8_t *scratch = sv_ptr + C::kVStages * C::kKvBytes;       // [8 warps][32 rows][80 B]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(scratch + C::kScratchBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
     const uint32_t bar0 = smem_u32(bars);
     auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
@@ -244,8 +269,9 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
         bool ok = true;
         uint32_t e = 0, v_issued = 0, tails = 0;
         uint32_t q_issued[2] = {0, 0};
-        for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
-            const PairInfo pi = load_pair(p, t);
+        PreTile nxt_tile;
+        for (ItemCursor it(p); it.valid(p) && ok; it.advance(nxt_tile)) {
+            const PairInfo pi = make_pair(p, it.take(p, nxt_tile));
             int good = 1;
             if (lane == 0) {
 #pragma unroll
@@ -334,8 +360,9 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
         const uint64_t pol_kv = l2_policy_evict_last();
         bool ok = true;
         uint32_t e = 0, k_issued = 0;
-        for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
-            const PairInfo pi = load_pair(p, t);
+        PreTile nxt_tile;
+        for (ItemCursor it(p); it.valid(p) && ok; it.advance(nxt_tile)) {
+            const PairInfo pi = make_pair(p, it.take(p, nxt_tile));
             const int kend = max(pi.sub[0].kend_max, pi.sub[1].kend_max);
             const int32_t *bt_row = p.block_table + (int64_t)pi.seq * p.bt_stride;
             for (int j = 0; j < pi.n && ok; ++j, ++e) {
@@ -423,8 +450,9 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
             ++pcnt;
             return true;
         };
-        for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
-            const PairInfo pi = load_pair(p, t);
+        PreTile nxt_tile;
+        for (ItemCursor it(p); it.valid(p) && ok; it.advance(nxt_tile)) {
+            const PairInfo pi = make_pair(p, it.take(p, nxt_tile));
             const int nx = x ? pi.sub[1].n : pi.sub[0].n;
             if (nx > 0) {
                 if (!mbar_wait(bar(kBarQFull + x), qcnt & 1, p.status)) {
@@ -472,8 +500,9 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
         const uint32_t o_addr = s_addr + C::kColO;
         bool ok = true;
         uint32_t ex = 0;    // steps of this tile slot over all items (S k lives in buffer k % 2)
-        for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
-            const PairInfo pi = load_pair(p, t);
+        PreTile nxt_tile;
+        for (ItemCursor it(p); it.valid(p) && ok; it.advance(nxt_tile)) {
+            const PairInfo pi = make_pair(p, it.take(p, nxt_tile));
             const SubInfo si = x ? pi.sub[1] : pi.sub[0];
             if (si.nrows == 0) continue;
             const int pr = si.row0 + r;
@@ -577,22 +606,40 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
                 break;
             }
             tc_fence_after();
+            // O / l as bf16, 32 columns at a time: each thread puts its row into the
+            // warp's scratch, then each store instruction writes 8 rows x 64
+            // contiguous bytes (4 lanes per row) instead of 32 rows x 16 bytes.
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            __nv_bfloat16 *orow = p.out + ((int64_t)(pi.q0 + i) * p.hq + pi.kvh * p.g + pr % p.g) * D;
+            uint8_t *wscr = scratch + warp * 32 * C::kRowPitch;
+            __nv_bfloat16 *dst_row[4];
+            bool dst_ok[4];
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4) {
+                const int rr = quarter * 32 + 8 * s4 + (lane >> 2);    // tile row this lane stores
+                const int prr = si.row0 + rr;
+                dst_ok[s4] = rr < si.nrows;
+                dst_row[s4] = p.out + ((int64_t)(pi.q0 + prr / p.g) * p.hq + pi.kvh * p.g + prr % p.g) * D +
+                              (lane & 3) * 8;
+            }
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld32(o_addr + 32 * c, v);
-                if (valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        dst[k] = make_uint4(
-                            pack_bf16x2(__uint_as_float(v[8 * k]) * inv, __uint_as_float(v[8 * k + 1]) * inv),
-                            pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv),
-                            pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv),
-                            pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv));
+                for (int k = 0; k < 4; ++k)
+                    *reinterpret_cast<uint4 *>(wscr + lane * C::kRowPitch + 16 * k) = make_uint4(
+                        pack_bf16x2(__uint_as_float(v[8 * k]) * inv, __uint_as_float(v[8 * k + 1]) * inv),
+                        pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv),
+                        pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv),
+                        pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv));
+                __syncwarp();
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4) {
+                    const uint4 val = *reinterpret_cast<const uint4 *>(
+                        wscr + (8 * s4 + (lane >> 2)) * C::kRowPitch + 16 * (lane & 3));
+                    if (dst_ok[s4]) *reinterpret_cast<uint4 *>(dst_row[s4] + 32 * c) = val;
                 }
+                __syncwarp();
             }
             // O is read: the next item's first P V (which overwrites O) waits for this
             // warpgroup's P of that item, which comes after these loads
