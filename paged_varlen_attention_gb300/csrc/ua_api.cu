@@ -11,6 +11,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -288,7 +289,9 @@ extern "C" ua_status ua_plan_inspect(const int32_t *cu_seqlens_q_host,
         }
     for (size_t i = 0; i < plan.tiles.size(); ++i) {
         const PreTile &t = plan.tiles[i];
-        put(2, (int32_t)i, t.seq, t.kvh, t.row0, t.nrows, t.kv_tiles, 0);
+        const int32_t cta = (int32_t)(std::upper_bound(plan.pre_begin.begin(), plan.pre_begin.end(),
+                                                       (int32_t)i) - plan.pre_begin.begin()) - 1;
+        put(2, cta, t.seq, t.kvh, t.row0, t.nrows, t.kv_tiles, (int32_t)i);
     }
     for (const CombUnit &u : plan.comb)
         put(3, u.seq, u.kvh, u.row0, u.nrows, u.slot_begin, u.nslots, 0);
@@ -478,6 +481,7 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
         pp.causal = causal != 0;
         pp.scale_log2 = scale_log2;
         pp.tiles = reinterpret_cast<const PreTile *>(ws + L.off_tiles);
+        pp.tile_begin = reinterpret_cast<const int32_t *>(ws + L.off_pre_begin);
         pp.n_tiles = (int32_t)plan.tiles.size();
         pp.status = ds->status;
         e = launch_prefill(head_size, pp, tm_q, tm_k3, tm_vp, plan.pre_ctas, stream);

@@ -53,7 +53,8 @@ struct PrefillParams {
     int32_t g;
     int32_t causal;
     float scale_log2;
-    const PreTile *tiles;
+    const PreTile *tiles;        // grouped by CTA
+    const int32_t *tile_begin;   // [ctas + 1]: CTA c runs tiles [tile_begin[c], tile_begin[c+1])
     int32_t n_tiles;
     int *status;
 };

@@ -94,6 +94,7 @@ struct Layout {
     size_t off_pieces;     // DecPiece [n_pieces]
     size_t off_comb;       // CombUnit [n_comb]
     size_t off_tiles;      // PreTile [n_tiles]
+    size_t off_pre_begin;  // int32 [pre_ctas + 1]
     size_t blob_bytes;     // bytes copied host -> device per call
     size_t off_part_o;     // float [n_slots][kDecRows][d]
     size_t off_part_ml;    // float [n_slots][kDecRows][2]

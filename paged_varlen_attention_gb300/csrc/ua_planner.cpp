@@ -4,11 +4,15 @@
 // for V1 Triton (ROCm) backend" (vLLM PR #14152, section "How is this
 // performance improvement achieved?"): decode rows and prefill rows want
 // different grids, so each call plans its own.  Decode units are balanced by
-// pages across persistent CTAs; prefill tiles are ordered longest first.
+// pages across persistent CTAs; prefill work items go to CTAs longest first,
+// each to the CTA with the least work so far (greedy longest-processing-time
+// scheduling), so that the persistent CTAs finish together.
 #include "ua_planner.h"
 
 #include <algorithm>
 #include <cstring>
+#include <functional>
+#include <queue>
 
 namespace ua {
 
@@ -51,6 +55,19 @@ static int64_t tile_key_end(const Problem &p, int64_t lq, int64_t lk, int64_t la
     return std::min<int64_t>(lk, lk - lq + i_last + 1);
 }
 
+// Work of a prefill item in 64-key steps of its two 128-row tiles, plus a
+// fixed charge for its start and epilogue (the same order of cost as a few
+// steps).
+static int64_t prefill_item_cost(const Problem &p, const PreTile &t, int g) {
+    constexpr int64_t kStepKeys = 64, kItemCharge = 3;
+    int64_t cost = kItemCharge;
+    for (int32_t r0 = t.row0; r0 < t.row0 + t.nrows; r0 += kPreRows) {
+        const int64_t last = std::min<int64_t>(r0 + kPreRows, t.row0 + t.nrows) - 1;
+        cost += (tile_key_end(p, t.lq, t.lk, last, g) + kStepKeys - 1) / kStepKeys;
+    }
+    return cost;
+}
+
 void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan) {
     // reuse the vectors' capacity across calls (the plan is thread-local in the API)
     plan.dec_ctas = 0;
@@ -60,6 +77,7 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
     plan.comb.clear();
     plan.n_slots = 0;
     plan.tiles.clear();
+    plan.pre_begin.clear();
     plan.pre_ctas = 0;
     plan.layout = Layout{};
     const int g = p.hq / p.hkv;
@@ -111,15 +129,41 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
             }
         }
     }
-    // ---- prefill: longest first; equal lengths keep batch order (counting sort)
+    // ---- prefill: longest first (counting sort, equal lengths keep batch order),
+    // then each item to the CTA with the least work so far (ties: lowest CTA)
     if (!unsorted.empty()) {
+        thread_local std::vector<PreTile> tl_sorted;
+        thread_local std::vector<int32_t> tl_owner;
+        std::vector<PreTile> &sorted = tl_sorted;
+        std::vector<int32_t> &owner = tl_owner;
         counts.assign((size_t)max_kv + 2, 0);
         for (const PreTile &t : unsorted) ++counts[(size_t)(max_kv - t.kv_tiles) + 1];
         for (size_t b = 1; b < counts.size(); ++b) counts[b] += counts[b - 1];
-        plan.tiles.resize(unsorted.size());
-        for (const PreTile &t : unsorted) plan.tiles[(size_t)counts[(size_t)(max_kv - t.kv_tiles)]++] = t;
+        sorted.resize(unsorted.size());
+        for (const PreTile &t : unsorted) sorted[(size_t)counts[(size_t)(max_kv - t.kv_tiles)]++] = t;
+
+        const int32_t ctas = (int32_t)std::min<size_t>(sorted.size(), (size_t)std::max(num_sms, 1));
+        plan.pre_ctas = ctas;
+        using Load = std::pair<int64_t, int32_t>;   // (work so far, CTA)
+        std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+        for (int32_t c = 0; c < ctas; ++c) heap.push({0, c});
+        owner.resize(sorted.size());
+        plan.pre_begin.assign((size_t)ctas + 1, 0);
+        for (size_t i = 0; i < sorted.size(); ++i) {
+            Load l = heap.top();
+            heap.pop();
+            owner[i] = l.second;
+            ++plan.pre_begin[(size_t)l.second + 1];
+            l.first += prefill_item_cost(p, sorted[i], g);
+            heap.push(l);
+        }
+        for (int32_t c = 0; c < ctas; ++c) plan.pre_begin[(size_t)c + 1] += plan.pre_begin[(size_t)c];
+        // group by CTA, keeping each CTA's items in assignment (longest-first) order
+        counts.assign((size_t)ctas, 0);
+        for (int32_t c = 0; c < ctas; ++c) counts[(size_t)c] = plan.pre_begin[(size_t)c];
+        plan.tiles.resize(sorted.size());
+        for (size_t i = 0; i < sorted.size(); ++i) plan.tiles[(size_t)counts[(size_t)owner[i]]++] = sorted[i];
     }
-    plan.pre_ctas = (int32_t)std::min<size_t>(plan.tiles.size(), (size_t)std::max(num_sms, 1));
 
     // ---- decode: equal page ranges over the concatenated units
     int64_t total = 0;
@@ -193,6 +237,8 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
     off = align_up(off + sizeof(CombUnit) * plan.comb.size(), kAlign);
     L.off_tiles = off;
     off = align_up(off + sizeof(PreTile) * plan.tiles.size(), kAlign);
+    L.off_pre_begin = off;
+    off = align_up(off + sizeof(int32_t) * plan.pre_begin.size(), kAlign);
     L.blob_bytes = off;
     L.off_part_o = off;
     off = align_up(off + sizeof(float) * (size_t)plan.n_slots * kDecRows * p.d, kAlign);
@@ -212,6 +258,8 @@ void serialize_plan_to(const Plan &plan, uint8_t *dst) {
         std::memcpy(dst + L.off_comb, plan.comb.data(), sizeof(CombUnit) * plan.comb.size());
     if (!plan.tiles.empty())
         std::memcpy(dst + L.off_tiles, plan.tiles.data(), sizeof(PreTile) * plan.tiles.size());
+    if (!plan.pre_begin.empty())
+        std::memcpy(dst + L.off_pre_begin, plan.pre_begin.data(), sizeof(int32_t) * plan.pre_begin.size());
 }
 
 void serialize_plan(const Plan &plan, std::vector<uint8_t> &blob) {

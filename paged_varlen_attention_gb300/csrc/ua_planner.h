@@ -14,7 +14,8 @@ struct Plan {
     std::vector<DecPiece> pieces;
     std::vector<CombUnit> comb;
     int32_t n_slots = 0;
-    std::vector<PreTile> tiles;
+    std::vector<PreTile> tiles;         // grouped by prefill CTA
+    std::vector<int32_t> pre_begin;     // pre_ctas + 1: CTA c runs tiles [pre_begin[c], pre_begin[c+1])
     int32_t pre_ctas = 0;
     Layout layout{};
 };

@@ -136,23 +136,24 @@ __device__ __forceinline__ PairInfo make_pair(const PrefillParams &p, const PreT
     return pi;
 }
 
-// Walks this CTA's work items; the record of the next item is loaded one item
-// ahead so that its latency hides behind the current one.
+// Walks this CTA's work items (its range of the plan); the record of the next
+// item is loaded one item ahead so that its latency hides behind the current one.
 struct ItemCursor {
-    int t;
+    int t, end;
     PreTile cur;
-    __device__ __forceinline__ ItemCursor(const PrefillParams &p) : t(blockIdx.x) {
-        if (t < p.n_tiles) cur = p.tiles[t];
+    __device__ __forceinline__ ItemCursor(const PrefillParams &p)
+        : t(p.tile_begin[blockIdx.x]), end(p.tile_begin[blockIdx.x + 1]) {
+        if (t < end) cur = p.tiles[t];
     }
-    __device__ __forceinline__ bool valid(const PrefillParams &p) const { return t < p.n_tiles; }
+    __device__ __forceinline__ bool valid(const PrefillParams &) const { return t < end; }
     // returns the current record and starts the load of the next one
     __device__ __forceinline__ PreTile take(const PrefillParams &p, PreTile &next) const {
-        next = (t + (int)gridDim.x < p.n_tiles) ? p.tiles[t + gridDim.x] : cur;
+        next = (t + 1 < end) ? p.tiles[t + 1] : cur;
         return cur;
     }
     __device__ __forceinline__ void advance(const PreTile &next) {
         cur = next;
-        t += gridDim.x;
+        ++t;
     }
 };
 

@@ -25,6 +25,10 @@ def visible_pages(lq, lk, last_token, causal, bs=16):
     return -(-kend // bs)
 
 
+def prefill_kend(lq, lk, last_token, causal):
+    return min(lk, lk - lq + last_token + 1) if causal else lk
+
+
 def check_plan(q_lens, k_lens, hq, hk, d=128, causal=True, num_sms=152):
     q_lens = np.asarray(q_lens, np.int64)
     k_lens = np.asarray(k_lens, np.int64)
@@ -95,9 +99,27 @@ def check_plan(q_lens, k_lens, hq, hk, d=128, causal=True, num_sms=152):
             per_cta[pc[1]] += pc[7] - pc[6]
         assert per_cta.max() - per_cta.min() <= 1
         assert counts["dec_ctas"] <= 2 * num_sms
-    # longest prefill tiles first
-    kv = [t[6] for t in tiles]
-    assert kv == sorted(kv, reverse=True)
+    # prefill items: the CTAs' ranges cover the tile list in order, each CTA's
+    # items come longest first, and the greedy assignment keeps the CTAs' work
+    # within one item of each other
+    ctas = [t[1] for t in tiles]
+    assert ctas == sorted(ctas)
+    assert [t[7] for t in tiles] == list(range(len(tiles)))
+    if tiles:
+        assert counts["prefill_ctas"] == len(set(ctas)) <= num_sms
+        load, biggest = {}, 0
+        for t in tiles:
+            _, cta, seq, kvh, row0, nrows, kvt, _ = t
+            cost = 3
+            for r0 in range(row0, row0 + nrows, 128):
+                last = min(r0 + 128, row0 + nrows) - 1
+                cost += -(-prefill_kend(int(q_lens[seq]), int(k_lens[seq]), last // g, causal) // 64)
+            load[cta] = load.get(cta, 0) + cost
+            biggest = max(biggest, cost)
+        assert max(load.values()) - min(load.values()) <= biggest
+        for c in set(ctas):
+            kv = [t[6] for t in tiles if t[1] == c]
+            assert kv == sorted(kv, reverse=True)
     return counts
 
 
