@@ -402,13 +402,15 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
 
     // ---- tensor maps: K/V page views (5-D), Q as [total_q, Hq, D]
     const int g = num_q_heads / num_kv_heads;
-    CUtensorMap tm_kp, tm_vp, tm_q, tm_k3;
+    CUtensorMap tm_kp, tm_vp, tm_q, tm_o, tm_k3;
     if (!encode_page_map(&tm_kp, k_cache, head_size, num_kv_heads, (uint64_t)num_blocks) ||
         !encode_page_map(&tm_vp, v_cache, head_size, num_kv_heads, (uint64_t)num_blocks))
         return UA_ERR_CUDA;
-    // prefill: Q tiles, and K as [num_blocks * 16, Hkv, D] with one box per 64 columns
+    // prefill: Q tiles (loads) and out tiles (stores) as [total_q, Hq, D], and K as
+    // [num_blocks * 16, Hkv, D] with one box per 64 columns
     if (!plan.tiles.empty() &&
         (!encode_map(&tm_q, q, head_size, num_q_heads, (uint64_t)total_q, g, kPreRows / g) ||
+         !encode_map(&tm_o, out, head_size, num_q_heads, (uint64_t)total_q, g, kPreRows / g) ||
          !encode_map(&tm_k3, k_cache, head_size, num_kv_heads,
                      (uint64_t)num_blocks * block_size, 1, kBlockSize)))
         return UA_ERR_CUDA;
@@ -484,7 +486,7 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
         pp.tile_begin = reinterpret_cast<const int32_t *>(ws + L.off_pre_begin);
         pp.n_tiles = (int32_t)plan.tiles.size();
         pp.status = ds->status;
-        e = launch_prefill(head_size, pp, tm_q, tm_k3, tm_vp, plan.pre_ctas, stream);
+        e = launch_prefill(head_size, pp, tm_q, tm_o, tm_k3, tm_vp, plan.pre_ctas, stream);
         if (e != cudaSuccess) return UA_ERR_CUDA;
     }
     mark(3);

@@ -63,7 +63,7 @@ struct PrefillParams {
 cudaError_t launch_decode(int d, const DecodeParams &p, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, int ctas, cudaStream_t stream);
 cudaError_t launch_combine(int d, const CombineParams &p, int n_units, cudaStream_t stream);
-cudaError_t launch_prefill(int d, const PrefillParams &p, const CUtensorMap &tm_q,
+cudaError_t launch_prefill(int d, const PrefillParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_o,
                            const CUtensorMap &tm_k, const CUtensorMap &tm_v, int ctas,
                            cudaStream_t stream);
 

@@ -66,12 +66,11 @@ struct PreCfg {
     static constexpr int kVStages = 4;
     static constexpr int kTmemCols = 512;
     static constexpr uint32_t kColO = 128;                    // + 256 * tile; S buffers at 0, 64
-    // epilogue transpose scratch per softmax warp: 32 rows x (64 + 16 pad) bytes
-    static constexpr int kRowPitch = 80;
-    static constexpr int kScratchBytes = 8 * 32 * kRowPitch;
-    // Q x2 (A, B), K x4, V x4, scratch, barriers; one CTA owns the SM (and its TMEM)
+    // output staging per tile: 128 rows x 64 columns of bf16 (one TMA store box)
+    static constexpr int kStageBytes = kPreRows * 128;
+    // Q x2 (A, B), K x4, V x4, staging x2, barriers; one CTA owns the SM (and its TMEM)
     static constexpr size_t kUsed = 1024 + 2 * (size_t)kQBytes +
-                                    (size_t)(kKStages + kVStages) * kKvBytes + kScratchBytes + 512;
+                                    (size_t)(kKStages + kVStages) * kKvBytes + 2 * kStageBytes + 512;
     static constexpr size_t kSmemBytes = kUsed < 120 * 1024 ? 120 * 1024 : kUsed;
     static constexpr float kRescaleThreshold = 8.0f;          // log2 units
 };
@@ -212,10 +211,25 @@ __device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
         : "memory");
 }
 
+// Rows [0, nrows) of a staged 64-column slice of O (layout of a Q tile: row r
+// at r * 128 bytes, 16-byte pieces XOR-ed with r % 8) to out, by the tile's
+// 128 threads.  Used for a tile that ends before 128 rows; kept out of line.
+template <int D>
+__device__ __noinline__ void copy_partial_rows(__nv_bfloat16 *out, const uint8_t *stg, int tid, int nrows,
+                                               int row0, int q0, int kvh, int g, int hq, int col0) {
+    for (int u = tid; u < nrows * 8; u += 128) {
+        const int row = u >> 3, piece = u & 7;
+        const uint4 val = *reinterpret_cast<const uint4 *>(stg + row * 128 + ((piece ^ (row & 7)) << 4));
+        const int prr = row0 + row;
+        *reinterpret_cast<uint4 *>(out + ((int64_t)(q0 + prr / g) * hq + kvh * g + prr % g) * D + col0 + 8 * piece) =
+            val;
+    }
+}
+
 template <int D, bool kPos>
 __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
     ua_prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tm_q,
-                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_vp) {
     using C = PreCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -225,8 +239,9 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
     const uint32_t sk = sq + 2 * C::kQBytes;                    // K[4]: [chunk][64 keys][64]
     const uint32_t sv = sk + C::kKStages * C::kKvBytes;         // V[4]: [page][chunk][16][64]
     uint8_t *sv_ptr = smem + 2 * C::kQBytes + C::kKStages * C::kKvBytes;
-    uint8_t *scratch = sv_ptr + C::kVStages * C::kKvBytes;       // [8 warps][32 rows][80 B]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(scratch + C::kScratchBytes);
+    uint8_t *stage_ptr = sv_ptr + C::kVStages * C::kKvBytes;     // [tile][128 rows][64] bf16, 128B swizzle
+    const uint32_t sstage = smem_u32(stage_ptr);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(stage_ptr + 2 * C::kStageBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
     const uint32_t bar0 = smem_u32(bars);
     auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
@@ -607,46 +622,52 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
                 break;
             }
             tc_fence_after();
-            // O / l as bf16, 32 columns at a time: each thread puts its row into the
-            // warp's scratch, then each store instruction writes 8 rows x 64
-            // contiguous bytes (4 lanes per row) instead of 32 rows x 16 bytes.
+            // O / l as bf16, 64 columns per pass, into the tile's staging buffer in
+            // the layout of a Q tile (row r at r * 128 bytes, 16-byte pieces XOR-ed
+            // with r % 8); then one TMA store per pass writes the 128 rows into
+            // out.  A tile that ends before 128 rows (the last of its sequence)
+            // copies its rows out by hand instead, as the box would run into the
+            // next sequence's rows.
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            uint8_t *wscr = scratch + warp * 32 * C::kRowPitch;
-            __nv_bfloat16 *dst_row[4];
-            bool dst_ok[4];
+            const bool leader = quarter == 0 && lane == 0;
+            const int tid = quarter * 32 + lane;        // thread of the tile = row r
+            uint8_t *stg = stage_ptr + x * C::kStageBytes;
+#pragma unroll 1
+            for (int h = 0; h < D / 64; ++h) {
+                if (leader) bulk_wait_read_all();       // the last store has read the buffer
+                named_barrier_sync(1 + x, 128);
 #pragma unroll
-            for (int s4 = 0; s4 < 4; ++s4) {
-                const int rr = quarter * 32 + 8 * s4 + (lane >> 2);    // tile row this lane stores
-                const int prr = si.row0 + rr;
-                dst_ok[s4] = rr < si.nrows;
-                dst_row[s4] = p.out + ((int64_t)(pi.q0 + prr / p.g) * p.hq + pi.kvh * p.g + prr % p.g) * D +
-                              (lane & 3) * 8;
-            }
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(o_addr + 64 * h + 32 * c, v);
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(o_addr + 32 * c, v);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    *reinterpret_cast<uint4 *>(wscr + lane * C::kRowPitch + 16 * k) = make_uint4(
-                        pack_bf16x2(__uint_as_float(v[8 * k]) * inv, __uint_as_float(v[8 * k + 1]) * inv),
-                        pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv),
-                        pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv),
-                        pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv));
-                __syncwarp();
-#pragma unroll
-                for (int s4 = 0; s4 < 4; ++s4) {
-                    const uint4 val = *reinterpret_cast<const uint4 *>(
-                        wscr + (8 * s4 + (lane >> 2)) * C::kRowPitch + 16 * (lane & 3));
-                    if (dst_ok[s4]) *reinterpret_cast<uint4 *>(dst_row[s4] + 32 * c) = val;
+                    for (int k = 0; k < 4; ++k)
+                        *reinterpret_cast<uint4 *>(stg + r * 128 + (((4 * c + k) ^ (r & 7)) << 4)) = make_uint4(
+                            pack_bf16x2(__uint_as_float(v[8 * k]) * inv, __uint_as_float(v[8 * k + 1]) * inv),
+                            pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv),
+                            pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv),
+                            pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv));
                 }
-                __syncwarp();
+                fence_proxy_async_smem();
+                named_barrier_sync(1 + x, 128);
+                if (si.nrows == kPreRows) {
+                    if (leader) {
+                        tma_store_3d(&tm_o, sstage + x * C::kStageBytes, 64 * h, pi.kvh * p.g,
+                                     pi.q0 + si.row0 / p.g);
+                        bulk_commit_group();
+                    }
+                } else {
+                    copy_partial_rows<D>(p.out, stg, tid, si.nrows, si.row0, pi.q0, pi.kvh, p.g, p.hq, 64 * h);
+                    named_barrier_sync(1 + x, 128);     // the buffer is free for the next pass
+                }
             }
             // O is read: the next item's first P V (which overwrites O) waits for this
             // warpgroup's P of that item, which comes after these loads
         }
     }
 
+    // the output stores have completed before the CTA's shared memory goes away
+    if (warp < 8 && (warp & 3) == 0 && lane == 0) bulk_wait_all();
     // ---- teardown: every role is done with TMEM before it is freed
     tc_fence_before();
     __syncthreads();
@@ -658,7 +679,7 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
 
 template <int D, bool kPos>
 static cudaError_t launch_prefill_t(const PrefillParams &p, const CUtensorMap &tm_q,
-                                    const CUtensorMap &tm_k, const CUtensorMap &tm_vp, int ctas,
+                                    const CUtensorMap &tm_o, const CUtensorMap &tm_k, const CUtensorMap &tm_vp, int ctas,
                                     cudaStream_t stream) {
     using C = PreCfg<D>;
     static thread_local int configured_device = -1;
@@ -671,19 +692,19 @@ static cudaError_t launch_prefill_t(const PrefillParams &p, const CUtensorMap &t
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    ua_prefill_kernel<D, kPos><<<ctas, C::kThreads, C::kSmemBytes, stream>>>(p, tm_q, tm_k, tm_vp);
+    ua_prefill_kernel<D, kPos><<<ctas, C::kThreads, C::kSmemBytes, stream>>>(p, tm_q, tm_o, tm_k, tm_vp);
     return cudaGetLastError();
 }
 
-cudaError_t launch_prefill(int d, const PrefillParams &p, const CUtensorMap &tm_q,
+cudaError_t launch_prefill(int d, const PrefillParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_o,
                            const CUtensorMap &tm_k, const CUtensorMap &tm_vp, int ctas,
                            cudaStream_t stream) {
     const bool pos = p.scale_log2 > 0.f;
     if (d == 64)
-        return pos ? launch_prefill_t<64, true>(p, tm_q, tm_k, tm_vp, ctas, stream)
-                   : launch_prefill_t<64, false>(p, tm_q, tm_k, tm_vp, ctas, stream);
-    return pos ? launch_prefill_t<128, true>(p, tm_q, tm_k, tm_vp, ctas, stream)
-               : launch_prefill_t<128, false>(p, tm_q, tm_k, tm_vp, ctas, stream);
+        return pos ? launch_prefill_t<64, true>(p, tm_q, tm_o, tm_k, tm_vp, ctas, stream)
+                   : launch_prefill_t<64, false>(p, tm_q, tm_o, tm_k, tm_vp, ctas, stream);
+    return pos ? launch_prefill_t<128, true>(p, tm_q, tm_o, tm_k, tm_vp, ctas, stream)
+               : launch_prefill_t<128, false>(p, tm_q, tm_o, tm_k, tm_vp, ctas, stream);
 }
 
 }  // namespace ua
