@@ -540,8 +540,7 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
                 // exponent's FMA; otherwise the scores are scaled first.  Keys at or
                 // past the row's limit (diagonal and tail steps only) become -inf.
                 uint32_t xs[kStep];
-                tmem_ld32(s_addr + b * kStep, *reinterpret_cast<uint32_t(*)[32]>(&xs[0]));
-                tmem_ld32(s_addr + b * kStep + 32, *reinterpret_cast<uint32_t(*)[32]>(&xs[32]));
+                tmem_ld64(s_addr + b * kStep, xs);
                 if (!kPos) {
 #pragma unroll
                     for (int k = 0; k < kStep; ++k)
