@@ -163,7 +163,9 @@ ua_status ua_plan_inspect(const int32_t *cu_seqlens_q_host, const int32_t *sequs
  * ua_profile_read(calls_back, ...) synchronises on that call's last event and
  * fills, for the call calls_back calls before the latest (0 = latest):
  *   ms[0..3]       decode, prefill, combine kernel time and the plan copy
- *                  (-1 when that step did not run);
+ *                  (-1 when that step did not run; the combine is always -1
+ *                  now: split units are merged inside the decode kernel by
+ *                  the CTA that writes a unit's last partial);
  *   launches[0..3] kernel launches of each kind (the copy counts as 0).
  * calls_back must be below min(profiled calls, UA_PROFILE_RING).
  */

@@ -56,6 +56,12 @@ static bool g_profile = false;
 // (an event recorded behind that copy).  From page-locked memory the copy is
 // one DMA that does not hold up the host thread; from pageable memory the
 // driver stages it through its own buffers first.
+//
+// The copy runs on a library-owned stream and lands in one of two plan slots
+// of the workspace, alternating per call: it waits only for the kernels of the
+// call two back (the slot's last reader), so it overlaps the previous call's
+// kernels, and the caller's stream waits for the copy before this call's
+// kernels.
 struct PlanStaging {
     static constexpr int kSlots = 8;
     uint8_t *buf[kSlots] = {};
@@ -63,28 +69,51 @@ struct PlanStaging {
     cudaEvent_t done[kSlots] = {};
     bool busy[kSlots] = {};
     int next = 0;
+    cudaStream_t side = nullptr;           // copy stream
+    cudaEvent_t copied = nullptr;          // behind the latest copy
+    cudaEvent_t slot_free[2] = {};         // behind the kernels of the slot's last call
+    bool slot_used[2] = {};
+    int next_slot = 0;
 };
 static std::mutex g_stage_mutex;
 static PlanStaging g_staging[kMaxDevices];
 
-// Copies the plan into dst on the stream through the staging ring.
-static ua_status copy_plan_pinned(int dev, const Plan &plan, void *dst, cudaStream_t stream) {
+static ua_status cuda_failed() {
+    cudaGetLastError();
+    return UA_ERR_CUDA;
+}
+
+// Copies the plan into plan slot *slot_out of ws (see above); the caller's
+// stream is made to wait for it.
+static ua_status stage_plan(int dev, const Plan &plan, uint8_t *ws, cudaStream_t stream, int *slot_out) {
     const size_t bytes = plan.layout.blob_bytes;
     std::lock_guard<std::mutex> lock(g_stage_mutex);
     PlanStaging &st = g_staging[dev];
+    if (!st.side) {
+        cudaStream_t sd = nullptr;
+        if (cudaStreamCreateWithFlags(&sd, cudaStreamNonBlocking) != cudaSuccess) return cuda_failed();
+        if (cudaEventCreateWithFlags(&st.copied, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&st.slot_free[0], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&st.slot_free[1], cudaEventDisableTiming) != cudaSuccess) {
+            cudaStreamDestroy(sd);
+            return cuda_failed();
+        }
+        st.side = sd;
+    }
+    const int s = st.next_slot;
+    st.next_slot ^= 1;
+    if (st.slot_used[s] && cudaStreamWaitEvent(st.side, st.slot_free[s], 0) != cudaSuccess)
+        return cuda_failed();
+    // a staging buffer that no copy in flight still reads
     const int i = st.next;
     st.next = (st.next + 1) % PlanStaging::kSlots;
     if (st.busy[i]) {
-        if (cudaEventSynchronize(st.done[i]) != cudaSuccess) {
-            cudaGetLastError();
-            return UA_ERR_CUDA;
-        }
+        if (cudaEventSynchronize(st.done[i]) != cudaSuccess) return cuda_failed();
         st.busy[i] = false;
     }
     if (!st.done[i] && cudaEventCreateWithFlags(&st.done[i], cudaEventDisableTiming) != cudaSuccess) {
-        cudaGetLastError();
         st.done[i] = nullptr;
-        return UA_ERR_CUDA;
+        return cuda_failed();
     }
     if (st.cap[i] < bytes) {
         if (st.buf[i]) cudaFreeHost(st.buf[i]);
@@ -92,20 +121,26 @@ static ua_status copy_plan_pinned(int dev, const Plan &plan, void *dst, cudaStre
         st.cap[i] = 0;
         const size_t want = bytes + bytes / 2 + 4096;
         void *h = nullptr;
-        if (cudaHostAlloc(&h, want, cudaHostAllocDefault) != cudaSuccess) {
-            cudaGetLastError();
-            return UA_ERR_CUDA;
-        }
+        if (cudaHostAlloc(&h, want, cudaHostAllocDefault) != cudaSuccess) return cuda_failed();
         st.buf[i] = static_cast<uint8_t *>(h);
         st.cap[i] = want;
     }
     serialize_plan_to(plan, st.buf[i]);
-    if (cudaMemcpyAsync(dst, st.buf[i], bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-        cudaEventRecord(st.done[i], stream) != cudaSuccess) {
-        cudaGetLastError();
-        return UA_ERR_CUDA;
-    }
+    if (cudaMemcpyAsync(ws + (size_t)s * bytes, st.buf[i], bytes, cudaMemcpyHostToDevice, st.side) != cudaSuccess ||
+        cudaEventRecord(st.done[i], st.side) != cudaSuccess || cudaEventRecord(st.copied, st.side) != cudaSuccess ||
+        cudaStreamWaitEvent(stream, st.copied, 0) != cudaSuccess)
+        return cuda_failed();
     st.busy[i] = true;
+    *slot_out = s;
+    return UA_OK;
+}
+
+// After this call's kernels: plan slot s is free once they have finished.
+static ua_status release_plan_slot(int dev, int s, cudaStream_t stream) {
+    std::lock_guard<std::mutex> lock(g_stage_mutex);
+    PlanStaging &st = g_staging[dev];
+    if (cudaEventRecord(st.slot_free[s], stream) != cudaSuccess) return cuda_failed();
+    st.slot_used[s] = true;
     return UA_OK;
 }
 
@@ -433,9 +468,10 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
     const float scale_log2 = softmax_scale * 1.4426950408889634f;
 
     mark(0);
+    int plan_slot = 0;
     if (L.blob_bytes > 0) {
         if (pinned_plan) {
-            st = copy_plan_pinned(ds->dev, plan, ws, stream);
+            st = stage_plan(ds->dev, plan, ws, stream, &plan_slot);
             if (st != UA_OK) return st;
         } else if (cudaMemcpyAsync(ws, blob.data(), L.blob_bytes, cudaMemcpyHostToDevice,
                                    stream) != cudaSuccess) {
@@ -443,6 +479,7 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
             return UA_ERR_CUDA;
         }
     }
+    uint8_t *pl = ws + (size_t)plan_slot * L.blob_bytes;   // this call's plan
     mark(1);
     cudaError_t e = cudaSuccess;
     if (plan.dec_ctas > 0) {
@@ -459,10 +496,12 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
         dp.g = g;
         dp.causal = causal != 0;
         dp.scale_log2 = scale_log2;
-        dp.cta_begin = reinterpret_cast<const int32_t *>(ws + L.off_cta);
-        dp.pieces = reinterpret_cast<const DecPiece *>(ws + L.off_pieces);
+        dp.cta_begin = reinterpret_cast<const int32_t *>(pl + L.off_cta);
+        dp.pieces = reinterpret_cast<const DecPiece *>(pl + L.off_pieces);
         dp.part_o = reinterpret_cast<float *>(ws + L.off_part_o);
         dp.part_ml = reinterpret_cast<float *>(ws + L.off_part_ml);
+        dp.comb = reinterpret_cast<const CombUnit *>(pl + L.off_comb);
+        dp.comb_count = reinterpret_cast<int32_t *>(pl + L.off_comb_count);
         dp.status = ds->status;
         e = launch_decode(head_size, dp, tm_kp, tm_vp, plan.dec_ctas, stream);
         if (e != cudaSuccess) return UA_ERR_CUDA;
@@ -482,36 +521,29 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
         pp.g = g;
         pp.causal = causal != 0;
         pp.scale_log2 = scale_log2;
-        pp.tiles = reinterpret_cast<const PreTile *>(ws + L.off_tiles);
-        pp.tile_begin = reinterpret_cast<const int32_t *>(ws + L.off_pre_begin);
+        pp.tiles = reinterpret_cast<const PreTile *>(pl + L.off_tiles);
+        pp.tile_begin = reinterpret_cast<const int32_t *>(pl + L.off_pre_begin);
         pp.n_tiles = (int32_t)plan.tiles.size();
         pp.status = ds->status;
         e = launch_prefill(head_size, pp, tm_q, tm_o, tm_k3, tm_vp, plan.pre_ctas, stream);
         if (e != cudaSuccess) return UA_ERR_CUDA;
     }
     mark(3);
-    if (!plan.comb.empty()) {
-        CombineParams cp{};
-        cp.out = static_cast<__nv_bfloat16 *>(out);
-        cp.cu = cu_seqlens_q;
-        cp.hq = num_q_heads;
-        cp.g = g;
-        cp.units = reinterpret_cast<const CombUnit *>(ws + L.off_comb);
-        cp.part_o = reinterpret_cast<const float *>(ws + L.off_part_o);
-        cp.part_ml = reinterpret_cast<const float *>(ws + L.off_part_ml);
-        e = launch_combine(head_size, cp, (int)plan.comb.size(), stream);
-        if (e != cudaSuccess) return UA_ERR_CUDA;
-    }
+    // (split units are merged inside the decode kernel: no separate combine step)
     mark(4);
+    if (pinned_plan && L.blob_bytes > 0) {
+        st = release_plan_slot(ds->dev, plan_slot, stream);
+        if (st != UA_OK) return st;
+    }
     if (prof) {
         std::lock_guard<std::mutex> lock(g_mutex);
         ds->ran[pslot][0] = plan.dec_ctas > 0;
         ds->ran[pslot][1] = !plan.tiles.empty();
-        ds->ran[pslot][2] = !plan.comb.empty();
+        ds->ran[pslot][2] = false;
         ds->ran[pslot][3] = L.blob_bytes > 0;
         ds->launches[pslot][0] = plan.dec_ctas > 0 ? 1 : 0;
         ds->launches[pslot][1] = plan.tiles.empty() ? 0 : 1;
-        ds->launches[pslot][2] = plan.comb.empty() ? 0 : 1;
+        ds->launches[pslot][2] = 0;
         ds->launches[pslot][3] = 0;
         ++ds->calls;
     }

@@ -1,4 +1,5 @@
-// ua_decode.cu -- memory-bound decode / split-KV kernel and the LSE-merge combine.
+// ua_decode.cu -- memory-bound decode / split-KV kernel with the LSE merge of
+// split units done by the CTA that finishes a unit's last partial.
 //
 // The decode rows of a unified batch (a handful of new tokens per sequence)
 // are HBM-bound: every KV page of every sequence is read once per KV head and
@@ -19,7 +20,13 @@
 //     online softmax in the exp2 domain, O += P V;
 //   * at the end of each piece the four warps merge their (m, l, O) through
 //     shared memory and write the bf16 output, or an fp32 partial plus its
-//     running (max, sum) when the unit was split across CTAs (split-KV).
+//     running (max, sum) when the unit was split across CTAs (split-KV);
+//   * a split unit is merged by the CTA whose partial completes it: each CTA
+//     counts its partial in (device-scope fence, then an atomic add on the
+//     unit's counter, zeroed by the plan copy of every call), and the one that
+//     brings the count to the unit's number of pieces reads all partials back
+//     from L2 and writes the bf16 output, in slot order (so the result does
+//     not depend on which CTA finished last).
 // Offsets into the cache are 64-bit; TMA coordinates stay 32-bit
 // (num_blocks * block_size < 2^31 is checked on the host).
 #include "ua_device.cuh"
@@ -48,8 +55,48 @@ struct DecCfg {
 
 // Fields of a piece descriptor in the shared-memory ring.
 enum : int {
-    kDq0 = 0, kDlq, kDlk, kDkvh, kDrow0, kDnrows, kDpb, kDpe, kDslot
+    kDq0 = 0, kDlq, kDlk, kDkvh, kDrow0, kDnrows, kDpb, kDpe, kDslot, kDcomb, kDslot0, kDnslots
 };
+
+// Merge of the partials of split unit u (log2 domain) by the 128 consumer
+// threads of the CTA that wrote the unit's last partial.  Partial s holds
+// O_s = sum_j 2^(x_j - m_s) v_j, its max m_s and l_s = sum_j 2^(x_j - m_s):
+//   M = max_s m_s,  out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+// The partials of other CTAs are read through L2 (ld.global.cg).
+template <int D>
+__device__ __forceinline__ void merge_unit(const DecodeParams &p, int q0, int kvh, int row0, int nrows,
+                                           int slot0, int nslots, int tid, int nthreads) {
+    for (int gi = tid; gi < nrows * (D / 4); gi += nthreads) {
+        const int row = gi / (D / 4);
+        const int col = (gi % (D / 4)) * 4;
+        float M = -INFINITY;
+        for (int s = 0; s < nslots; ++s)
+            M = fmaxf(M, __ldcg(p.part_ml + 2 * ((int64_t)(slot0 + s) * kDecRows + row)));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float W = 0.f;
+        if (M != -INFINITY) {
+            for (int s = 0; s < nslots; ++s) {
+                const int64_t base = (int64_t)(slot0 + s) * kDecRows + row;
+                const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + 2 * base));
+                const float w = fast_exp2(ml.x - M);     // 0 for an empty partial (m = -inf)
+                W += w * ml.y;
+                const float4 ov = __ldcg(reinterpret_cast<const float4 *>(p.part_o + base * D + col));
+                acc.x += w * ov.x;
+                acc.y += w * ov.y;
+                acc.z += w * ov.z;
+                acc.w += w * ov.w;
+            }
+        }
+        const float inv = W > 0.f ? 1.f / W : 0.f;
+        const int pr = row0 + row;
+        const int64_t t = (int64_t)q0 + pr / p.g;
+        const int h = kvh * p.g + pr % p.g;
+        uint2 packed;
+        packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+        packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2 *>(p.out + (t * p.hq + h) * D + col) = packed;
+    }
+}
 
 template <int D>
 __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
@@ -73,6 +120,7 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    __shared__ int s_merge;   // this CTA completed the split unit of its current piece
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kStages; ++i) {
             mbar_init(full0 + 8 * i, 1);
@@ -126,6 +174,12 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
                     d[kDpb] = pc.page_begin;
                     d[kDpe] = pc.page_end;
                     d[kDslot] = pc.slot;
+                    if (pc.unit >= 0) {
+                        const CombUnit cu = p.comb[pc.unit];
+                        d[kDcomb] = pc.unit;
+                        d[kDslot0] = cu.slot_begin;
+                        d[kDnslots] = cu.nslots;
+                    }
                     const uint32_t pb = pfull0 + 8 * slot;
                     mbar_arrive_expect_tx(pb, (uint32_t)pc.nrows * D * 2);
                     for (int r = 0; r < pc.nrows;) {
@@ -204,7 +258,7 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
                 ok = false;
             const int *d = dring + slot * C::kDescInts;
             struct {
-                int kvh, row0, nrows, page_begin, page_end, slot;
+                int kvh, row0, nrows, page_begin, page_end, slot, comb, slot0, nslots;
             } pc;
             const int q0 = ok ? d[kDq0] : 0;
             const int lq = ok ? d[kDlq] : 0;
@@ -215,6 +269,11 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
             pc.page_begin = ok ? d[kDpb] : 0;
             pc.page_end = ok ? d[kDpe] : 0;
             pc.slot = ok ? d[kDslot] : -1;
+            if (pc.slot >= 0) {
+                pc.comb = d[kDcomb];
+                pc.slot0 = d[kDslot0];
+                pc.nslots = d[kDnslots];
+            }
             const uint8_t *qtile = qring + slot * C::kQTileBytes;
             const int npages = pc.page_end - pc.page_begin;
 
@@ -403,6 +462,18 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
                     if (col == 0) *reinterpret_cast<float2 *>(p.part_ml + 2 * base) = make_float2(M, L);
                 }
             }
+            if (pc.slot >= 0) {
+                // count this partial in; the CTA that completes the unit merges it
+                __threadfence();
+                named_barrier_sync(1, C::kConsumerWarps * 32);
+                if (tid == 0) s_merge = atomicAdd(p.comb_count + pc.comb, 1) == pc.nslots - 1;
+                named_barrier_sync(1, C::kConsumerWarps * 32);
+                if (s_merge) {
+                    __threadfence();
+                    merge_unit<D>(p, q0, pc.kvh, pc.row0, pc.nrows, pc.slot0, pc.nslots, tid,
+                                  C::kConsumerWarps * 32);
+                }
+            }
             named_barrier_sync(1, C::kConsumerWarps * 32);
         }
     }
@@ -414,45 +485,6 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
         const uint32_t first = issued > (uint32_t)C::kStages ? issued - C::kStages : 0;
         for (uint32_t gidx = first; gidx < issued; ++gidx)
             mbar_wait(full0 + 8 * (gidx % C::kStages), (gidx / C::kStages) & 1, p.status);
-    }
-}
-
-// Merge of the partials of split units (log2 domain).  Partial s holds
-// O_s = sum_j 2^(x_j - m_s) v_j, its max m_s and l_s = sum_j 2^(x_j - m_s):
-//   M = max_s m_s,  out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
-template <int D>
-__global__ void __launch_bounds__(128) ua_combine_kernel(const CombineParams p) {
-    const CombUnit u = p.units[blockIdx.x];
-    const int q0 = p.cu[u.seq];
-    for (int gi = threadIdx.x; gi < u.nrows * (D / 4); gi += blockDim.x) {
-        const int row = gi / (D / 4);
-        const int col = (gi % (D / 4)) * 4;
-        float M = -INFINITY;
-        for (int s = 0; s < u.nslots; ++s)
-            M = fmaxf(M, p.part_ml[2 * ((int64_t)(u.slot_begin + s) * kDecRows + row)]);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float W = 0.f;
-        if (M != -INFINITY) {
-            for (int s = 0; s < u.nslots; ++s) {
-                const int64_t base = (int64_t)(u.slot_begin + s) * kDecRows + row;
-                const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + 2 * base);
-                const float w = fast_exp2(ml.x - M);     // 0 for an empty partial (m = -inf)
-                W += w * ml.y;
-                const float4 ov = *reinterpret_cast<const float4 *>(p.part_o + base * D + col);
-                acc.x += w * ov.x;
-                acc.y += w * ov.y;
-                acc.z += w * ov.z;
-                acc.w += w * ov.w;
-            }
-        }
-        const float inv = W > 0.f ? 1.f / W : 0.f;
-        const int pr = u.row0 + row;
-        const int64_t t = (int64_t)q0 + pr / p.g;
-        const int h = u.kvh * p.g + pr % p.g;
-        uint2 packed;
-        packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-        packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2 *>(p.out + (t * p.hq + h) * D + col) = packed;
     }
 }
 
@@ -478,14 +510,6 @@ cudaError_t launch_decode(int d, const DecodeParams &p, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, int ctas, cudaStream_t stream) {
     return d == 64 ? launch_decode_t<64>(p, tm_k, tm_v, ctas, stream)
                    : launch_decode_t<128>(p, tm_k, tm_v, ctas, stream);
-}
-
-cudaError_t launch_combine(int d, const CombineParams &p, int n_units, cudaStream_t stream) {
-    if (d == 64)
-        ua_combine_kernel<64><<<n_units, 128, 0, stream>>>(p);
-    else
-        ua_combine_kernel<128><<<n_units, 128, 0, stream>>>(p);
-    return cudaGetLastError();
 }
 
 }  // namespace ua

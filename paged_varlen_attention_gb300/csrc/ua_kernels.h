@@ -27,17 +27,9 @@ struct DecodeParams {
     const DecPiece *pieces;      // plan
     float *part_o;               // [slots][kDecRows][d]
     float *part_ml;              // [slots][kDecRows][2]: running max (log2 domain), sum
+    const CombUnit *comb;        // plan: split units
+    int32_t *comb_count;         // plan: partials written per split unit (zero at launch)
     int *status;                 // device status word
-};
-
-struct CombineParams {
-    __nv_bfloat16 *out;
-    const int32_t *cu;
-    int32_t hq;
-    int32_t g;
-    const CombUnit *units;
-    const float *part_o;
-    const float *part_ml;
 };
 
 struct PrefillParams {
@@ -62,7 +54,6 @@ struct PrefillParams {
 // Each returns the launch error (cudaSuccess when the launch was queued).
 cudaError_t launch_decode(int d, const DecodeParams &p, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, int ctas, cudaStream_t stream);
-cudaError_t launch_combine(int d, const CombineParams &p, int n_units, cudaStream_t stream);
 cudaError_t launch_prefill(int d, const PrefillParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_o,
                            const CUtensorMap &tm_k, const CUtensorMap &tm_v, int ctas,
                            cudaStream_t stream);

@@ -50,7 +50,7 @@ struct alignas(16) DecPiece {   // one contiguous page range of one decode unit
     int32_t page_begin;  // first logical page of the range
     int32_t page_end;    // one past the last logical page
     int32_t slot;        // -1: the piece is the whole unit, write bf16 output; else partial slot
-    int32_t unit;
+    int32_t unit;        // split piece: index of its unit in the combine list; else -1
 };
 
 struct alignas(16) CombUnit {   // a decode unit split over several pieces
@@ -93,9 +93,12 @@ struct Layout {
     size_t off_cta;        // int32 [dec_ctas + 1]
     size_t off_pieces;     // DecPiece [n_pieces]
     size_t off_comb;       // CombUnit [n_comb]
+    size_t off_comb_count; // int32 [n_comb]: partials written so far (zero in the blob)
     size_t off_tiles;      // PreTile [n_tiles]
     size_t off_pre_begin;  // int32 [pre_ctas + 1]
-    size_t blob_bytes;     // bytes copied host -> device per call
+    size_t blob_bytes;     // bytes copied host -> device per call (one plan slot; the
+                           // workspace holds two, at 0 and blob_bytes; offsets above
+                           // are relative to the slot)
     size_t off_part_o;     // float [n_slots][kDecRows][d]
     size_t off_part_ml;    // float [n_slots][kDecRows][2]
     size_t total_bytes;    // workspace bytes

@@ -203,10 +203,15 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
             }
         }
         plan.cta_begin[ctas] = (int32_t)plan.pieces.size();
-        // split units get consecutive partial slots, in unit order
+        // split units get consecutive partial slots, in unit order; comb_of: a
+        // unit's index in the combine list
+        thread_local std::vector<int32_t> tl_comb_of;
+        std::vector<int32_t> &comb_of = tl_comb_of;
+        comb_of.assign(units.size(), -1);
         int32_t slot = 0;
         for (size_t u = 0; u < units.size(); ++u) {
             if (counts[u] > 1) {
+                comb_of[u] = (int32_t)plan.comb.size();
                 CombUnit cu{};
                 cu.seq = units[u].seq;
                 cu.kvh = units[u].kvh;
@@ -222,8 +227,21 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
             }
         }
         plan.n_slots = slot;
-        for (DecPiece &pc : plan.pieces)
-            pc.slot = counts[pc.unit] < 0 ? -1 : counts[pc.unit] + pc.slot;
+        // split pieces get their partial slot and the index of their combine entry
+        for (DecPiece &pc : plan.pieces) {
+            const int32_t first = counts[pc.unit];
+            pc.slot = first < 0 ? -1 : first + pc.slot;
+            pc.unit = comb_of[pc.unit];
+        }
+        // A CTA's last piece is the head of a unit that the next CTA finishes
+        // first thing; run it first, so that both halves of the unit are done
+        // early and its merge (by whichever CTA completes it) overlaps the rest
+        // of the work instead of landing at the end of the kernel.
+        for (int64_t c = 0; c < ctas; ++c) {
+            const int32_t b0 = plan.cta_begin[c], b1 = plan.cta_begin[c + 1];
+            if (b1 - b0 > 1 && plan.pieces[b1 - 1].slot >= 0)
+                std::rotate(plan.pieces.begin() + b0, plan.pieces.begin() + (b1 - 1), plan.pieces.begin() + b1);
+        }
     }
 
     // ---- workspace layout
@@ -235,11 +253,16 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
     off = align_up(off + sizeof(DecPiece) * plan.pieces.size(), kAlign);
     L.off_comb = off;
     off = align_up(off + sizeof(CombUnit) * plan.comb.size(), kAlign);
+    L.off_comb_count = off;
+    off = align_up(off + sizeof(int32_t) * plan.comb.size(), kAlign);
     L.off_tiles = off;
     off = align_up(off + sizeof(PreTile) * plan.tiles.size(), kAlign);
     L.off_pre_begin = off;
     off = align_up(off + sizeof(int32_t) * plan.pre_begin.size(), kAlign);
     L.blob_bytes = off;
+    // two plan slots: a call's plan copy can run while the previous call's
+    // kernels still read the other slot
+    off = 2 * off;
     L.off_part_o = off;
     off = align_up(off + sizeof(float) * (size_t)plan.n_slots * kDecRows * p.d, kAlign);
     L.off_part_ml = off;
