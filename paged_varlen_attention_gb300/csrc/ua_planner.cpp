@@ -5,14 +5,12 @@
 // performance improvement achieved?"): decode rows and prefill rows want
 // different grids, so each call plans its own.  Decode units are balanced by
 // pages across persistent CTAs; prefill work items go to CTAs longest first,
-// each to the CTA with the least work so far (greedy longest-processing-time
-// scheduling), so that the persistent CTAs finish together.
+// dealt in rounds of alternating direction, so that the persistent CTAs
+// finish together.
 #include "ua_planner.h"
 
 #include <algorithm>
 #include <cstring>
-#include <functional>
-#include <queue>
 
 namespace ua {
 
@@ -53,19 +51,6 @@ static int64_t tile_key_end(const Problem &p, int64_t lq, int64_t lk, int64_t la
     if (!p.causal) return lk;
     const int64_t i_last = last_row / g;
     return std::min<int64_t>(lk, lk - lq + i_last + 1);
-}
-
-// Work of a prefill item in 64-key steps of its two 128-row tiles, plus a
-// fixed charge for its start and epilogue (the same order of cost as a few
-// steps).
-static int64_t prefill_item_cost(const Problem &p, const PreTile &t, int g) {
-    constexpr int64_t kStepKeys = 64, kItemCharge = 3;
-    int64_t cost = kItemCharge;
-    for (int32_t r0 = t.row0; r0 < t.row0 + t.nrows; r0 += kPreRows) {
-        const int64_t last = std::min<int64_t>(r0 + kPreRows, t.row0 + t.nrows) - 1;
-        cost += (tile_key_end(p, t.lq, t.lk, last, g) + kStepKeys - 1) / kStepKeys;
-    }
-    return cost;
 }
 
 void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan) {
@@ -130,7 +115,10 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
         }
     }
     // ---- prefill: longest first (counting sort, equal lengths keep batch order),
-    // then each item to the CTA with the least work so far (ties: lowest CTA)
+    // then dealt to the CTAs in rounds whose direction alternates (CTA 0..n-1,
+    // then n-1..0, ...): the CTA that got the longest item of a round gets the
+    // shortest of the next, which keeps the CTAs' totals within about one
+    // item of each other at O(items) host cost
     if (!unsorted.empty()) {
         thread_local std::vector<PreTile> tl_sorted;
         thread_local std::vector<int32_t> tl_owner;
@@ -144,18 +132,12 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
 
         const int32_t ctas = (int32_t)std::min<size_t>(sorted.size(), (size_t)std::max(num_sms, 1));
         plan.pre_ctas = ctas;
-        using Load = std::pair<int64_t, int32_t>;   // (work so far, CTA)
-        std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
-        for (int32_t c = 0; c < ctas; ++c) heap.push({0, c});
         owner.resize(sorted.size());
         plan.pre_begin.assign((size_t)ctas + 1, 0);
         for (size_t i = 0; i < sorted.size(); ++i) {
-            Load l = heap.top();
-            heap.pop();
-            owner[i] = l.second;
-            ++plan.pre_begin[(size_t)l.second + 1];
-            l.first += prefill_item_cost(p, sorted[i], g);
-            heap.push(l);
+            const size_t round = i / (size_t)ctas, k = i % (size_t)ctas;
+            owner[i] = (int32_t)((round & 1) ? (size_t)ctas - 1 - k : k);
+            ++plan.pre_begin[(size_t)owner[i] + 1];
         }
         for (int32_t c = 0; c < ctas; ++c) plan.pre_begin[(size_t)c + 1] += plan.pre_begin[(size_t)c];
         // group by CTA, keeping each CTA's items in assignment (longest-first) order

@@ -62,12 +62,14 @@ struct PreCfg {
     static constexpr int kKChunkBytes = kStep * 128;          // K: 64 keys x 64 columns
     static constexpr int kPageBytes = kBlockSize * D * 2;     // V: one 16-token page
     static constexpr int kThreads = 384;                      // 12 warps: 3 per SMSP, 168 regs
-    static constexpr int kKStages = 4;
-    static constexpr int kVStages = 4;
+    static constexpr int kKStages = 3;
+    static constexpr int kVStages = 3;
     static constexpr int kTmemCols = 512;
     static constexpr uint32_t kColO = 128;                    // + 256 * tile; S buffers at 0, 64
-    // output staging per tile: 128 rows x 64 columns of bf16 (one TMA store box)
-    static constexpr int kStageBytes = kPreRows * 128;
+    // output staging per tile: D/64 buffers of 128 rows x 64 columns of bf16
+    // (one TMA store box each), so the passes of an epilogue never wait for
+    // each other's stores
+    static constexpr int kStageBytes = kPreRows * 128 * kChunks;
     // Q x2 (A, B), K x4, V x4, staging x2, barriers; one CTA owns the SM (and its TMEM)
     static constexpr size_t kUsed = 1024 + 2 * (size_t)kQBytes +
                                     (size_t)(kKStages + kVStages) * kKvBytes + 2 * kStageBytes + 512;
@@ -630,11 +632,12 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const bool leader = quarter == 0 && lane == 0;
             const int tid = quarter * 32 + lane;        // thread of the tile = row r
-            uint8_t *stg = stage_ptr + x * C::kStageBytes;
+            // the previous item's stores have read the staging buffers
+            if (leader) bulk_wait_read_all();
+            named_barrier_sync(1 + x, 128);
 #pragma unroll 1
             for (int h = 0; h < D / 64; ++h) {
-                if (leader) bulk_wait_read_all();       // the last store has read the buffer
-                named_barrier_sync(1 + x, 128);
+                uint8_t *stg = stage_ptr + x * C::kStageBytes + h * (kPreRows * 128);
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t v[32];
@@ -651,8 +654,8 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
                 named_barrier_sync(1 + x, 128);
                 if (si.nrows == kPreRows) {
                     if (leader) {
-                        tma_store_3d(&tm_o, sstage + x * C::kStageBytes, 64 * h, pi.kvh * p.g,
-                                     pi.q0 + si.row0 / p.g);
+                        tma_store_3d(&tm_o, sstage + x * C::kStageBytes + h * (kPreRows * 128), 64 * h,
+                                     pi.kvh * p.g, pi.q0 + si.row0 / p.g);
                         bulk_commit_group();
                     }
                 } else {

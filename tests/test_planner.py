@@ -100,8 +100,8 @@ def check_plan(q_lens, k_lens, hq, hk, d=128, causal=True, num_sms=152):
         assert per_cta.max() - per_cta.min() <= 1
         assert counts["dec_ctas"] <= 2 * num_sms
     # prefill items: the CTAs' ranges cover the tile list in order, each CTA's
-    # items come longest first, and the greedy assignment keeps the CTAs' work
-    # within one item of each other
+    # items come longest first, and dealing the longest-first list in rounds of
+    # alternating direction keeps the CTAs' work within one item of each other
     ctas = [t[1] for t in tiles]
     assert ctas == sorted(ctas)
     assert [t[7] for t in tiles] == list(range(len(tiles)))
