@@ -174,6 +174,47 @@ ua_status ua_profile_enable(int32_t enable);
 ua_status ua_profile_read(int32_t calls_back, float *ms, int32_t *launches);
 
 /*
+ * unified_attention_lse -- unified_attention that also writes, for every
+ * query row, the natural-log normaliser of its softmax,
+ *     lse[t][h] = ln( sum over visible keys j of e^(softmax_scale * <q_t,h, k_j>) ),
+ * into lse (device, fp32 [total_q, Hq], row-major, caller-owned; must not be
+ * NULL, 4-byte aligned).  Rows of sequences with Lq = 0 are not written.  The
+ * other arguments, the output and the errors are those of unified_attention.
+ * Together with ua_merge_attn_states it gives cascade (shared-prefix)
+ * attention: one call over the shared prefix with causal = 0 (every new token
+ * sees the whole prefix), one over each sequence's own keys with causal = 1,
+ * then the merge.  Non-causal attention for cascade attention is the review
+ * request on "[Kernel] Unified Triton kernel that doesn't distinguish between
+ * prefill + decode" (vLLM PR #16828, review thread).
+ */
+ua_status unified_attention_lse(const void *q, const void *k_cache, const void *v_cache,
+                                const int32_t *cu_seqlens_q, const int32_t *seqused_k,
+                                const int32_t *block_table, float softmax_scale, int32_t causal,
+                                void *out, float *lse, const int32_t *cu_seqlens_q_host,
+                                const int32_t *seqused_k_host, int32_t num_seqs,
+                                int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                                int32_t block_size, int32_t num_blocks,
+                                int32_t block_table_stride, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
+/*
+ * ua_merge_attn_states -- combine two attention results of the same query
+ * rows over disjoint key sets, A and B, by their normalisers:
+ *     m = max(lse_a, lse_b),  w_x = e^(lse_x - m),
+ *     out = (w_a out_a + w_b out_b) / (w_a + w_b),  lse_out = m + ln(w_a + w_b).
+ * A side with lse = -inf (no key) gets weight 0; both -inf gives out = 0 and
+ * lse_out = -inf.  out_a, out_b, out: device bf16 [rows][head_size], 16-byte
+ * aligned (out may alias out_a or out_b); lse_a, lse_b: device fp32 [rows];
+ * lse_out: device fp32 [rows] or NULL.  rows = total_q * Hq for the outputs
+ * of two unified_attention_lse calls.  head_size: a multiple of 8.  Async on
+ * stream; returns UA_ERR_INVALID_ARG for bad arguments (nothing launched),
+ * UA_ERR_CUDA if the launch fails.
+ */
+ua_status ua_merge_attn_states(const void *out_a, const float *lse_a, const void *out_b,
+                               const float *lse_b, void *out, float *lse_out, int64_t rows,
+                               int32_t head_size, void *stream);
+
+/*
  * unified_attention_no_alloc -- the same operation and arguments as
  * unified_attention, minus the workspace: the launch plan and the split-KV
  * partials go into a device array the library owns, so the caller never

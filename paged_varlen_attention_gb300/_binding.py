@@ -23,8 +23,9 @@ STATUS = {0: "UA_OK", 1: "UA_ERR_INVALID_ARG", 2: "UA_ERR_UNSUPPORTED", 3: "UA_E
 DEVICE_BAD_BLOCK_ID = 0x1
 DEVICE_WAIT_TIMEOUT = 0x2
 
-SYMBOLS = ("unified_attention", "ua_workspace_size", "ua_status_string", "ua_device_status",
-           "ua_plan_inspect", "ua_profile_enable", "ua_profile_read")
+SYMBOLS = ("unified_attention", "unified_attention_lse", "ua_merge_attn_states",
+           "ua_workspace_size", "ua_status_string", "ua_device_status", "ua_plan_inspect",
+           "ua_profile_enable", "ua_profile_read")
 
 
 class UAError(RuntimeError):
@@ -55,6 +56,12 @@ def load_library():
         lib.unified_attention.argtypes = [P, P, P, P, P, P, ctypes.c_float, I32, P, P, P,
                                           I32, I32, I32, I32, I32, I32, I32, P, ctypes.c_size_t, P]
         lib.unified_attention.restype = ctypes.c_int
+        lib.unified_attention_lse.argtypes = [P, P, P, P, P, P, ctypes.c_float, I32, P, P, P, P,
+                                              I32, I32, I32, I32, I32, I32, I32, P,
+                                              ctypes.c_size_t, P]
+        lib.unified_attention_lse.restype = ctypes.c_int
+        lib.ua_merge_attn_states.argtypes = [P, P, P, P, P, P, I64, I32, P]
+        lib.ua_merge_attn_states.restype = ctypes.c_int
         lib.ua_workspace_size.argtypes = [P, P, I32, I32, I32, I32, I32, I32, I32,
                                           ctypes.POINTER(ctypes.c_size_t)]
         lib.ua_workspace_size.restype = ctypes.c_int
@@ -116,13 +123,15 @@ def _workspace(torch, device, nbytes):
 
 def unified_attention(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table, softmax_scale,
                       causal=True, out=None, *, cu_seqlens_q_host=None, seqused_k_host=None,
-                      workspace=None, stream=None):
+                      workspace=None, stream=None, lse=None):
     """Attention over a paged varlen batch (see ``include/unified_attention.h``).
 
     q: bf16 [total_q, Hq, D]; k_cache / v_cache: bf16 [num_blocks, 16, Hkv, D];
     cu_seqlens_q int32 [N+1], seqused_k int32 [N], block_table int32 [N, stride],
     all CUDA tensors.  Host copies of cu_seqlens_q / seqused_k may be passed to
     avoid a device-to-host read.  Returns ``out`` (bf16 [total_q, Hq, D]).
+    lse: an fp32 CUDA tensor [total_q, Hq] to also receive each row's natural-log
+    softmax normaliser (calls ``unified_attention_lse``).
     """
     import torch
 
@@ -155,13 +164,55 @@ def unified_attention(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table,
         stream = torch.cuda.current_stream(q.device).cuda_stream
     elif hasattr(stream, "cuda_stream"):
         stream = stream.cuda_stream
-    rc = lib.unified_attention(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-                               cu_seqlens_q.data_ptr(), seqused_k.data_ptr(),
-                               block_table.data_ptr(), float(softmax_scale), int(bool(causal)),
-                               out.data_ptr(), _np_ptr(cu_h), _np_ptr(sk_h), num_seqs, hq, hk, d,
-                               bs, nb, stride, ws_ptr, workspace.numel(), stream)
-    _check(rc, "unified_attention")
+    if lse is None:
+        rc = lib.unified_attention(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                   cu_seqlens_q.data_ptr(), seqused_k.data_ptr(),
+                                   block_table.data_ptr(), float(softmax_scale), int(bool(causal)),
+                                   out.data_ptr(), _np_ptr(cu_h), _np_ptr(sk_h), num_seqs, hq, hk,
+                                   d, bs, nb, stride, ws_ptr, workspace.numel(), stream)
+        _check(rc, "unified_attention")
+        return out
+    if (not lse.is_cuda or lse.dtype != torch.float32 or not lse.is_contiguous()
+            or tuple(lse.shape) != (total_q, hq)):
+        raise UAError(1, "lse must be a contiguous CUDA float32 tensor [total_q, Hq]")
+    rc = lib.unified_attention_lse(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                   cu_seqlens_q.data_ptr(), seqused_k.data_ptr(),
+                                   block_table.data_ptr(), float(softmax_scale), int(bool(causal)),
+                                   out.data_ptr(), lse.data_ptr(), _np_ptr(cu_h), _np_ptr(sk_h),
+                                   num_seqs, hq, hk, d, bs, nb, stride, ws_ptr, workspace.numel(),
+                                   stream)
+    _check(rc, "unified_attention_lse")
     return out
+
+
+def merge_attn_states(out_a, lse_a, out_b, lse_b, out=None, lse_out=None, stream=None):
+    """Combine two results of the same rows over disjoint key sets (``ua_merge_attn_states``).
+
+    out_a / out_b: bf16 CUDA [..., D]; lse_a / lse_b: fp32 CUDA [...] (one per row).
+    Returns ``(out, lse_out)``; lse_out is None unless given.
+    """
+    import torch
+
+    lib = load_library()
+    for name, t, dt in (("out_a", out_a, torch.bfloat16), ("out_b", out_b, torch.bfloat16),
+                        ("lse_a", lse_a, torch.float32), ("lse_b", lse_b, torch.float32)):
+        if not t.is_cuda or t.dtype != dt or not t.is_contiguous():
+            raise UAError(1, f"{name} must be a contiguous CUDA {dt} tensor")
+    if out_b.shape != out_a.shape or lse_a.shape != out_a.shape[:-1] or lse_b.shape != lse_a.shape:
+        raise UAError(1, "merge inputs disagree in shape")
+    if out is None:
+        out = torch.empty_like(out_a)
+    d = int(out_a.shape[-1])
+    rows = int(lse_a.numel())
+    if stream is None:
+        stream = torch.cuda.current_stream(out_a.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    rc = lib.ua_merge_attn_states(out_a.data_ptr(), lse_a.data_ptr(), out_b.data_ptr(),
+                                  lse_b.data_ptr(), out.data_ptr(),
+                                  None if lse_out is None else lse_out.data_ptr(), rows, d, stream)
+    _check(rc, "ua_merge_attn_states")
+    return out, lse_out
 
 
 def device_status() -> int:

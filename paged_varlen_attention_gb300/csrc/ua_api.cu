@@ -401,7 +401,7 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
                         int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                         int32_t head_size, int32_t block_size, int32_t num_blocks,
                         int32_t block_table_stride, void *workspace, size_t workspace_bytes,
-                        void *stream_ptr, bool pinned_plan) {
+                        void *stream_ptr, bool pinned_plan, float *lse) {
     // ---- host-side checks, before any CUDA call
     Problem pr = make_problem(cu_seqlens_q_host, seqused_k_host, num_seqs, num_q_heads,
                               num_kv_heads, head_size, block_size, block_table_stride, causal);
@@ -413,7 +413,8 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
     if (total_q == 0) return UA_OK;
     if (!q || !k_cache || !v_cache || !out || !cu_seqlens_q || !seqused_k || !block_table)
         return UA_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(lse, 4))
         return UA_ERR_INVALID_ARG;
     if (num_blocks <= 0 || (int64_t)num_blocks * block_size >= ((int64_t)1 << 31))
         return UA_ERR_INVALID_ARG;
@@ -502,6 +503,7 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
         dp.part_ml = reinterpret_cast<float *>(ws + L.off_part_ml);
         dp.comb = reinterpret_cast<const CombUnit *>(pl + L.off_comb);
         dp.comb_count = reinterpret_cast<int32_t *>(pl + L.off_comb_count);
+        dp.lse = lse;
         dp.status = ds->status;
         e = launch_decode(head_size, dp, tm_kp, tm_vp, plan.dec_ctas, stream);
         if (e != cudaSuccess) return UA_ERR_CUDA;
@@ -511,6 +513,7 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
         PrefillParams pp{};
         pp.k_cache = static_cast<const __nv_bfloat16 *>(k_cache);
         pp.out = static_cast<__nv_bfloat16 *>(out);
+        pp.lse = lse;
         pp.cu = cu_seqlens_q;
         pp.seqused_k = seqused_k;
         pp.block_table = block_table;
@@ -566,5 +569,23 @@ extern "C" ua_status unified_attention(const void *q, const void *k_cache, const
                              softmax_scale, causal, out, cu_seqlens_q_host, seqused_k_host,
                              num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
                              num_blocks, block_table_stride, workspace, workspace_bytes, stream,
-                             /*pinned_plan=*/true);
+                             /*pinned_plan=*/true, /*lse=*/nullptr);
+}
+
+extern "C" ua_status unified_attention_lse(const void *q, const void *k_cache, const void *v_cache,
+                                           const int32_t *cu_seqlens_q, const int32_t *seqused_k,
+                                           const int32_t *block_table, float softmax_scale,
+                                           int32_t causal, void *out, float *lse,
+                                           const int32_t *cu_seqlens_q_host,
+                                           const int32_t *seqused_k_host, int32_t num_seqs,
+                                           int32_t num_q_heads, int32_t num_kv_heads,
+                                           int32_t head_size, int32_t block_size, int32_t num_blocks,
+                                           int32_t block_table_stride, void *workspace,
+                                           size_t workspace_bytes, void *stream) {
+    if (lse == nullptr) return UA_ERR_INVALID_ARG;
+    return ua::run_attention(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table,
+                             softmax_scale, causal, out, cu_seqlens_q_host, seqused_k_host,
+                             num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                             num_blocks, block_table_stride, workspace, workspace_bytes, stream,
+                             /*pinned_plan=*/true, lse);
 }

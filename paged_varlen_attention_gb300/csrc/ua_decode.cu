@@ -91,6 +91,7 @@ __device__ __forceinline__ void merge_unit(const DecodeParams &p, int q0, int kv
         const int pr = row0 + row;
         const int64_t t = (int64_t)q0 + pr / p.g;
         const int h = kvh * p.g + pr % p.g;
+        if (p.lse != nullptr && col == 0) p.lse[t * p.hq + h] = row_lse(M, W);
         uint2 packed;
         packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
         packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
@@ -451,6 +452,7 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
                     const int pr = pc.row0 + row;
                     const int64_t t = (int64_t)q0 + pr / p.g;
                     const int h = pc.kvh * p.g + pr % p.g;
+                    if (p.lse != nullptr && col == 0) p.lse[t * p.hq + h] = row_lse(M, L);
                     uint2 packed;
                     packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
                     packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);

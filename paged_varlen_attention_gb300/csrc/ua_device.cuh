@@ -273,6 +273,13 @@ __device__ __forceinline__ float fast_log2(float x) {
     return y;
 }
 
+// Natural-log normaliser of a row from its running max m (log2 domain, scale
+// folded in) and sum l = sum_j 2^(x_j - m): ln(sum_j e^(scale s_j)) =
+// ln 2 * (m + log2 l); -inf for a row without keys.
+__device__ __forceinline__ float row_lse(float m, float l) {
+    return l > 0.f ? 0.69314718055994531f * (m + fast_log2(l)) : -INFINITY;
+}
+
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

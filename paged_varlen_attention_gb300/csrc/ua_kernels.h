@@ -29,12 +29,14 @@ struct DecodeParams {
     float *part_ml;              // [slots][kDecRows][2]: running max (log2 domain), sum
     const CombUnit *comb;        // plan: split units
     int32_t *comb_count;         // plan: partials written per split unit (zero at launch)
+    float *lse;                  // optional [total_q, Hq]: natural-log normaliser per row
     int *status;                 // device status word
 };
 
 struct PrefillParams {
-    const __nv_bfloat16 *k_cache;   // read directly by the K loaders (cp.async)
+    const __nv_bfloat16 *k_cache;
     __nv_bfloat16 *out;
+    float *lse;                  // optional [total_q, Hq]: natural-log normaliser per row
     const int32_t *cu;
     const int32_t *seqused_k;
     const int32_t *block_table;
@@ -61,7 +63,8 @@ cudaError_t launch_prefill(int d, const PrefillParams &p, const CUtensorMap &tm_
 // The whole call behind unified_attention (arguments as declared in
 // unified_attention.h).  pinned_plan: stage the plan through the library's
 // page-locked ring (allocated on first use) rather than copy it from pageable
-// memory; the entry point that must allocate nothing passes false.
+// memory; the entry point that must allocate nothing passes false.  lse:
+// optional fp32 [total_q, Hq] output of the natural-log normaliser per row.
 ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
                         const int32_t *cu_seqlens_q, const int32_t *seqused_k,
                         const int32_t *block_table, float softmax_scale, int32_t causal, void *out,
@@ -69,6 +72,6 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
                         int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                         int32_t head_size, int32_t block_size, int32_t num_blocks,
                         int32_t block_table_stride, void *workspace, size_t workspace_bytes,
-                        void *stream, bool pinned_plan);
+                        void *stream, bool pinned_plan, float *lse);
 
 }  // namespace ua

@@ -45,14 +45,6 @@ int validate_problem(const Problem &p) {
     return 0;
 }
 
-// Visible keys of the last packed row of a tile (all rows of the tile see a
-// prefix of the context; the last row sees the longest one).
-static int64_t tile_key_end(const Problem &p, int64_t lq, int64_t lk, int64_t last_row, int g) {
-    if (!p.causal) return lk;
-    const int64_t i_last = last_row / g;
-    return std::min<int64_t>(lk, lk - lq + i_last + 1);
-}
-
 void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan) {
     // reuse the vectors' capacity across calls (the plan is thread-local in the API)
     plan.dec_ctas = 0;

@@ -75,5 +75,5 @@ extern "C" ua_status unified_attention_no_alloc(
                              softmax_scale, causal, out, cu_seqlens_q_host, seqused_k_host,
                              num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
                              num_blocks, block_table_stride, ws, kStaticBytes, stream,
-                             /*pinned_plan=*/false);
+                             /*pinned_plan=*/false, /*lse=*/nullptr);
 }

@@ -300,3 +300,35 @@ def test_invalid_metadata_is_rejected(bad):
         sk[1] = 16 * bt.shape[1] + 1
     with pytest.raises(oracle.OracleError):
         oracle.attention(b.q, b.k_cache, b.v_cache, cu, sk, bt, 0.25, True)
+
+
+@pytest.mark.parametrize("causal_suffix", [True, False])
+def test_shared_prefix_cascade_equals_full_attention(causal_suffix):
+    """Cascade attention: P shared prefix keys attended without the causal mask
+    (every new token sees the whole prefix), each sequence's own keys with its
+    mask, merged by log-sum-exp == attention over prefix ++ own keys (the use
+    of non-causal mode named in the review thread of vLLM PR #16828).  The full
+    result is also checked against torch fp64 SDPA on dense keys."""
+    P, hq, hk, d = 48, 4, 2, 32
+    q_lens, own = [3, 1, 5], [7, 20, 5]
+    rng = np.random.Generator(np.random.PCG64(46))
+    q = W.f32_to_bf16_bits(rng.standard_normal((sum(q_lens), hq, d), dtype=np.float32))
+    pk = W.f32_to_bf16_bits(rng.standard_normal((P, hk, d), dtype=np.float32))
+    pv = W.f32_to_bf16_bits(rng.standard_normal((P, hk, d), dtype=np.float32))
+    oks = [W.f32_to_bf16_bits(rng.standard_normal((n, hk, d), dtype=np.float32)) for n in own]
+    ovs = [W.f32_to_bf16_bits(rng.standard_normal((n, hk, d), dtype=np.float32)) for n in own]
+    scale = 1.0 / math.sqrt(d)
+    pre, pre_lse = oracle.attention_batch(batch_from_dense(q, [pk] * 3, [pv] * 3, q_lens, hq,
+                                                           causal=False, softmax_scale=scale))
+    suf, suf_lse = oracle.attention_batch(batch_from_dense(q, oks, ovs, q_lens, hq,
+                                                           causal=causal_suffix, softmax_scale=scale))
+    merged, mlse = oracle.merge([pre, suf], [pre_lse, suf_lse])
+    fks = [np.concatenate([pk, k]) for k in oks]
+    fvs = [np.concatenate([pv, v]) for v in ovs]
+    full_b = batch_from_dense(q, fks, fvs, q_lens, hq, causal=causal_suffix, softmax_scale=scale)
+    full, full_lse = oracle.attention_batch(full_b)
+    np.testing.assert_allclose(merged, full, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(mlse, full_lse, rtol=1e-13, atol=1e-12)
+    if causal_suffix:
+        ref = sdpa_reference(q, fks, fvs, q_lens, hq, True, scale)
+        np.testing.assert_allclose(merged, ref, rtol=0, atol=1e-12)
