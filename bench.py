@@ -3,8 +3,9 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 A step is one unified_attention call over one synthetic batch (the whole hot
-path: the partition pass, the plan copy, the decode / split-KV kernel, the
-prefill kernel when the batch has prefill rows, and the combine kernel).  The
+path: the partition pass, the plan copy, the decode / split-KV kernel with its
+in-kernel merge of split units, and the prefill kernel when the batch has
+prefill rows).  The
 default workload is the Llama-3.1-8B-shaped pure-decode batch (64 sequences,
 one new token each, contexts uniform in [2048, 4096], Hq 32, Hkv 8, head size
 128, bf16, 16-token pages).  Inputs are resident in HBM when timing starts;
@@ -20,6 +21,10 @@ during the timed region, and the number of kernels launched.
 --impl reference times the fp64 CPU oracle (the reference arm of this build)
 on the same workload, a bounded sample of sequences per step.
 
+--workload llama3_8b_cascade_64dec_shared4k times a cascade step instead
+(shared-prefix pass + own-keys pass + LSE merge) next to the same attention
+as one direct call.
+
 Multi-GPU: one process per GPU under torchrun; each rank runs its own replica
 of the workload (no data-path collective, weak scaling); the time is the max
 over ranks.
@@ -29,6 +34,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -53,6 +59,10 @@ WORKLOADS = {
     "llama3_70b_long_mixed_32x8k-32k_2x2048chunk": 5,
 }
 DEFAULT_WORKLOAD = "llama3_8b_decode_64x2k-4k"
+# Cascade (shared-prefix) step: 64 decode sequences (Llama-3.1-8B heads) that
+# share a 4096-token prefix, own contexts U[256, 1024] tokens; prefix pass over
+# the whole group as one non-causal sequence + own-keys pass + LSE merge.
+CASCADE_WORKLOAD = "llama3_8b_cascade_64dec_shared4k"
 
 
 def parse_args():
@@ -60,7 +70,8 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(WORKLOADS) + [CASCADE_WORKLOAD])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -473,6 +484,126 @@ def assemble(args, res, world, cpu):
     return line
 
 
+def run_cascade(args):
+    """The cascade workload (one GPU): time the three calls of a cascade step and,
+    for comparison, the same attention as one direct call over prefix ++ own keys."""
+    import torch
+    import paged_varlen_attention_gb300 as ua
+
+    ua.load_library()
+    dev = torch.device("cuda:0")
+    n, P, hq, hk, d = 64, 4096, 32, 8, 128
+    rng = np.random.Generator(np.random.PCG64(3000))
+    own = rng.integers(256, 1025, n)
+    bf = lambda *shape: W.f32_to_bf16_bits(rng.standard_normal(shape, dtype=np.float32))  # noqa: E731
+    pre_pages, own_pages = P // 16, [-(-int(k) // 16) for k in own]
+    pool = pre_pages + sum(own_pages)
+    perm = rng.permutation(pool).astype(np.int32)
+    kc, vc = bf(pool, 16, hk, d), bf(pool, 16, hk, d)
+    q = bf(n, hq, d)
+    stride = pre_pages + max(own_pages)
+    bt_group = np.zeros((1, stride), np.int32)
+    bt_group[0, :pre_pages] = perm[:pre_pages]
+    bt_own = np.zeros((n, stride), np.int32)
+    bt_full = np.zeros((n, stride), np.int32)
+    off = pre_pages
+    for s_ in range(n):
+        ids = perm[off:off + own_pages[s_]]
+        off += own_pages[s_]
+        bt_own[s_, :len(ids)] = ids
+        bt_full[s_, :pre_pages] = perm[:pre_pages]
+        bt_full[s_, pre_pages:pre_pages + len(ids)] = ids
+    t16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
+    t32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)  # noqa: E731
+    qd, kd, vd = t16(q), t16(kc), t16(vc)
+    cu_g, sk_g = np.array([0, n], np.int32), np.array([P], np.int32)
+    cu_o, sk_o = np.arange(n + 1, dtype=np.int32), own.astype(np.int32)
+    sk_f = (own + P).astype(np.int32)
+    dv = {k: t32(v) for k, v in dict(cu_g=cu_g, sk_g=sk_g, bt_g=bt_group, cu_o=cu_o, sk_o=sk_o,
+                                     bt_o=bt_own, sk_f=sk_f, bt_f=bt_full).items()}
+    scale = 1.0 / math.sqrt(d)
+    out_p, out_o, out = (torch.empty_like(qd) for _ in range(3))
+    out_f = torch.empty_like(qd)
+    lse_p = torch.empty((n, hq), dtype=torch.float32, device=dev)
+    lse_o = torch.empty_like(lse_p)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def cascade():
+        ua.unified_attention(qd, kd, vd, dv["cu_g"], dv["sk_g"], dv["bt_g"], scale, False, out=out_p,
+                             cu_seqlens_q_host=cu_g, seqused_k_host=sk_g, lse=lse_p)
+        ua.unified_attention(qd, kd, vd, dv["cu_o"], dv["sk_o"], dv["bt_o"], scale, True, out=out_o,
+                             cu_seqlens_q_host=cu_o, seqused_k_host=sk_o, lse=lse_o)
+        ua.merge_attn_states(out_p, lse_p, out_o, lse_o, out=out)
+
+    def direct():
+        ua.unified_attention(qd, kd, vd, dv["cu_o"], dv["sk_f"], dv["bt_f"], scale, True, out=out_f,
+                             cu_seqlens_q_host=cu_o, seqused_k_host=sk_f)
+
+    for _ in range(max(args.warmup, 3)):
+        cascade()
+        direct()
+    torch.cuda.synchronize()
+    diff = (out.float() - out_f.float()).abs()
+    if not bool(torch.isfinite(out).all()) or float(diff.max()) > 2e-2:
+        raise RuntimeError(f"cascade and direct results differ (max {float(diff.max()):.3e})")
+    steps = args.steps
+
+    def timed(fn):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        torch.cuda.synchronize()
+        for a, b in evs:
+            flush.fill_(1)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    with ClockSampler(gpu_id_for_smi(torch, 0)) as clocks:
+        t_cas = timed(cascade)
+        t_dir = timed(direct)
+        ua.profile_enable(True)
+        timed(cascade)
+    # per-call kernel times of the profiled pass: calls alternate prefix, own
+    pre_ms, own_ms = [], []
+    for back in range(2 * steps):
+        ms, _ = ua.profile_read(back)
+        (pre_ms if back % 2 else own_ms).append(max(ms[0], 0.0) + max(ms[1], 0.0))
+    ua.profile_enable(False)
+    if ua.device_status():
+        raise RuntimeError("device status set after the cascade steps")
+    own_spec = W.Spec("own", np.ones(n), own, hq, hk, d, softmax_scale=scale)
+    work_own = algorithmic_work(own_spec)
+    dec_ms = statistics.mean(own_ms)
+    achieved = work_own["decode_bytes"] / (dec_ms / 1e3) / 1e9
+    peaks = measured_peaks()
+    total_s = sum(t_cas) / 1e3
+    return {
+        "metric": METRIC, "value": n * steps / total_s, "unit": "tokens/s", "n_gpus": 1,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": sum(t_cas) / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, shuffled pages)",
+        "config": {"workload": CASCADE_WORKLOAD, "num_seqs": n, "q_tokens": n,
+                   "shared_prefix_tokens": P, "own_kv_tokens": int(own.sum()),
+                   "num_q_heads": hq, "num_kv_heads": hk, "head_size": d, "block_size": 16,
+                   "l2": "L2 flushed (256 MB write) between steps",
+                   "parallelism": "1 GPU, no collective"},
+        "roofline": {"kernel": "ua_decode_kernel (own-keys pass)", "bound": "hbm",
+                     "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "per_launch": f"{work_own['decode_bytes']} algorithmic bytes", "launch_ms": dec_ms,
+                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"},
+        "cascade": {"prefix_pass_ms": statistics.mean(pre_ms), "own_pass_ms": dec_ms,
+                    "direct_ms_per_step": sum(t_dir) / steps,
+                    "speedup_vs_direct": sum(t_dir) / sum(t_cas),
+                    "max_abs_diff_vs_direct": float(diff.max())},
+        "gpu_launches": 3 * steps,
+        "clocks": clocks.summary(),
+    }
+
+
 def main():
     args = parse_args()
     rank, world, local, dist = dist_setup(args.gpus)
@@ -485,6 +616,11 @@ def main():
         return
     import torch
 
+    if args.workload == CASCADE_WORKLOAD:
+        if world != 1:
+            raise SystemExit("the cascade workload runs on one GPU")
+        print(json.dumps(run_cascade(args)), flush=True)
+        return
     res = run_ours(args, rank, world, local, dist)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

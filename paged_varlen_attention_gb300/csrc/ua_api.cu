@@ -57,11 +57,14 @@ static bool g_profile = false;
 // one DMA that does not hold up the host thread; from pageable memory the
 // driver stages it through its own buffers first.
 //
-// The copy runs on a library-owned stream and lands in one of two plan slots
-// of the workspace, alternating per call: it waits only for the kernels of the
-// call two back (the slot's last reader), so it overlaps the previous call's
-// kernels, and the caller's stream waits for the copy before this call's
-// kernels.
+// The copy runs on a library-owned stream.  It waits for the kernels of the
+// previous call (whatever its stream or workspace: a call's workspace layout
+// depends on its batch, so the previous call may still be reading the bytes
+// this plan goes to), and the caller's stream waits for the copy before this
+// call's kernels.  So the copy overlaps whatever the caller's stream runs
+// between two calls (other layers' kernels), though not the previous call's
+// own kernels.  One workspace must not serve calls that may run at the same
+// time (their plans and partials would collide anyway).
 struct PlanStaging {
     static constexpr int kSlots = 8;
     uint8_t *buf[kSlots] = {};
@@ -71,9 +74,8 @@ struct PlanStaging {
     int next = 0;
     cudaStream_t side = nullptr;           // copy stream
     cudaEvent_t copied = nullptr;          // behind the latest copy
-    cudaEvent_t slot_free[2] = {};         // behind the kernels of the slot's last call
-    bool slot_used[2] = {};
-    int next_slot = 0;
+    cudaEvent_t call_done = nullptr;       // behind the kernels of the latest call
+    bool called = false;
 };
 static std::mutex g_stage_mutex;
 static PlanStaging g_staging[kMaxDevices];
@@ -83,9 +85,9 @@ static ua_status cuda_failed() {
     return UA_ERR_CUDA;
 }
 
-// Copies the plan into plan slot *slot_out of ws (see above); the caller's
-// stream is made to wait for it.
-static ua_status stage_plan(int dev, const Plan &plan, uint8_t *ws, cudaStream_t stream, int *slot_out) {
+// Copies the plan to the start of ws (see above); the caller's stream is made
+// to wait for it.
+static ua_status stage_plan(int dev, const Plan &plan, uint8_t *ws, cudaStream_t stream) {
     const size_t bytes = plan.layout.blob_bytes;
     std::lock_guard<std::mutex> lock(g_stage_mutex);
     PlanStaging &st = g_staging[dev];
@@ -93,16 +95,13 @@ static ua_status stage_plan(int dev, const Plan &plan, uint8_t *ws, cudaStream_t
         cudaStream_t sd = nullptr;
         if (cudaStreamCreateWithFlags(&sd, cudaStreamNonBlocking) != cudaSuccess) return cuda_failed();
         if (cudaEventCreateWithFlags(&st.copied, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&st.slot_free[0], cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&st.slot_free[1], cudaEventDisableTiming) != cudaSuccess) {
+            cudaEventCreateWithFlags(&st.call_done, cudaEventDisableTiming) != cudaSuccess) {
             cudaStreamDestroy(sd);
             return cuda_failed();
         }
         st.side = sd;
     }
-    const int s = st.next_slot;
-    st.next_slot ^= 1;
-    if (st.slot_used[s] && cudaStreamWaitEvent(st.side, st.slot_free[s], 0) != cudaSuccess)
+    if (st.called && cudaStreamWaitEvent(st.side, st.call_done, 0) != cudaSuccess)
         return cuda_failed();
     // a staging buffer that no copy in flight still reads
     const int i = st.next;
@@ -126,21 +125,20 @@ static ua_status stage_plan(int dev, const Plan &plan, uint8_t *ws, cudaStream_t
         st.cap[i] = want;
     }
     serialize_plan_to(plan, st.buf[i]);
-    if (cudaMemcpyAsync(ws + (size_t)s * bytes, st.buf[i], bytes, cudaMemcpyHostToDevice, st.side) != cudaSuccess ||
+    if (cudaMemcpyAsync(ws, st.buf[i], bytes, cudaMemcpyHostToDevice, st.side) != cudaSuccess ||
         cudaEventRecord(st.done[i], st.side) != cudaSuccess || cudaEventRecord(st.copied, st.side) != cudaSuccess ||
         cudaStreamWaitEvent(stream, st.copied, 0) != cudaSuccess)
         return cuda_failed();
     st.busy[i] = true;
-    *slot_out = s;
     return UA_OK;
 }
 
-// After this call's kernels: plan slot s is free once they have finished.
-static ua_status release_plan_slot(int dev, int s, cudaStream_t stream) {
+// After this call's kernels are enqueued: the next call's plan copy waits for them.
+static ua_status mark_call_done(int dev, cudaStream_t stream) {
     std::lock_guard<std::mutex> lock(g_stage_mutex);
     PlanStaging &st = g_staging[dev];
-    if (cudaEventRecord(st.slot_free[s], stream) != cudaSuccess) return cuda_failed();
-    st.slot_used[s] = true;
+    if (cudaEventRecord(st.call_done, stream) != cudaSuccess) return cuda_failed();
+    st.called = true;
     return UA_OK;
 }
 
@@ -469,18 +467,29 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
     const float scale_log2 = softmax_scale * 1.4426950408889634f;
 
     mark(0);
-    int plan_slot = 0;
+    // Once the plan copy is issued, every way out of this call records the
+    // call-done event behind whatever kernels it launched, so that the next
+    // call's copy cannot overwrite a plan that is still being read.
+    struct CallDone {
+        int dev = -1;
+        cudaStream_t stream = nullptr;
+        ~CallDone() {
+            if (dev >= 0) mark_call_done(dev, stream);
+        }
+    } call_done;
     if (L.blob_bytes > 0) {
         if (pinned_plan) {
-            st = stage_plan(ds->dev, plan, ws, stream, &plan_slot);
+            st = stage_plan(ds->dev, plan, ws, stream);
             if (st != UA_OK) return st;
+            call_done.dev = ds->dev;
+            call_done.stream = stream;
         } else if (cudaMemcpyAsync(ws, blob.data(), L.blob_bytes, cudaMemcpyHostToDevice,
                                    stream) != cudaSuccess) {
             cudaGetLastError();
             return UA_ERR_CUDA;
         }
     }
-    uint8_t *pl = ws + (size_t)plan_slot * L.blob_bytes;   // this call's plan
+    uint8_t *pl = ws;   // this call's plan
     mark(1);
     cudaError_t e = cudaSuccess;
     if (plan.dec_ctas > 0) {
@@ -534,8 +543,9 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
     mark(3);
     // (split units are merged inside the decode kernel: no separate combine step)
     mark(4);
-    if (pinned_plan && L.blob_bytes > 0) {
-        st = release_plan_slot(ds->dev, plan_slot, stream);
+    if (call_done.dev >= 0) {
+        call_done.dev = -1;
+        st = mark_call_done(ds->dev, stream);
         if (st != UA_OK) return st;
     }
     if (prof) {

@@ -96,9 +96,8 @@ struct Layout {
     size_t off_comb_count; // int32 [n_comb]: partials written so far (zero in the blob)
     size_t off_tiles;      // PreTile [n_tiles]
     size_t off_pre_begin;  // int32 [pre_ctas + 1]
-    size_t blob_bytes;     // bytes copied host -> device per call (one plan slot; the
-                           // workspace holds two, at 0 and blob_bytes; offsets above
-                           // are relative to the slot)
+    size_t blob_bytes;     // bytes copied host -> device per call (offsets above are
+                           // from the start of the workspace)
     size_t off_part_o;     // float [n_slots][kDecRows][d]
     size_t off_part_ml;    // float [n_slots][kDecRows][2]
     size_t total_bytes;    // workspace bytes

@@ -234,9 +234,6 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
     L.off_pre_begin = off;
     off = align_up(off + sizeof(int32_t) * plan.pre_begin.size(), kAlign);
     L.blob_bytes = off;
-    // two plan slots: a call's plan copy can run while the previous call's
-    // kernels still read the other slot
-    off = 2 * off;
     L.off_part_o = off;
     off = align_up(off + sizeof(float) * (size_t)plan.n_slots * kDecRows * p.d, kAlign);
     L.off_part_ml = off;

@@ -187,3 +187,56 @@ def test_cascade_shared_prefix_matches_full_attention(hq, hk, d):
     assert np.abs(mlse.cpu().numpy() - ref_lse).max() <= LSE_TOL
     single = res["full"][0].float().cpu().numpy().astype(np.float64)
     assert_close(got, single, "cascade vs one GPU pass")
+
+    # the prefix pass over the whole group as ONE non-causal sequence (every
+    # token of the group against the prefix, which is then read once per KV
+    # head): the rows come out in the same order, so the merge is unchanged
+    tot = int(cu[-1])
+    spec_g = W.Spec("group", [tot], [P], hq, hk, d, causal=False, softmax_scale=scale)
+    b_g = W.Batch(spec_g, q, kc, vc, np.array([0, tot], np.int32), np.array([P], np.int32),
+                  bt_pre[:1].copy(), np.zeros(0, np.int32))
+    dev = to_device(b_g)
+    lse_g = torch.empty((tot, hq), dtype=torch.float32, device="cuda")
+    out_g = ua.unified_attention(dev["q"], dev["k_cache"], dev["v_cache"], dev["cu_seqlens_q"],
+                                 dev["seqused_k"], dev["block_table"], scale, False,
+                                 cu_seqlens_q_host=b_g.cu_seqlens_q, seqused_k_host=b_g.seqused_k,
+                                 lse=lse_g)
+    merged_g, _ = ua.merge_attn_states(out_g, lse_g, res["own"][0], res["own"][1])
+    torch.cuda.synchronize()
+    assert_close(merged_g.float().cpu().numpy().astype(np.float64), ref,
+                 "grouped cascade vs oracle full attention")
+
+
+def test_back_to_back_calls_with_different_layouts():
+    """Calls whose workspace layouts differ (decode-only, prefill-only, mixed),
+    issued back to back on one stream with no synchronisation in between, give
+    the same results as the same calls run one at a time.  (The plan of each
+    call is copied on a library stream; the copy must not overwrite what the
+    previous call's kernels still read.)"""
+    import torch
+    import paged_varlen_attention_gb300 as ua
+
+    specs = [W.custom_spec([1] * 40, [700 + 37 * i for i in range(40)], 32, 8, 128, seed=1),
+             W.custom_spec([300], [300], 32, 8, 128, seed=2),
+             W.custom_spec([1, 1, 90, 1], [3000, 20, 400, 5000], 32, 8, 128, seed=3)]
+    batches = [W.materialize(s_) for s_ in specs]
+    devs = [to_device(b) for b in batches]
+
+    def call(b, dev, out):
+        s_ = b.spec
+        return ua.unified_attention(dev["q"], dev["k_cache"], dev["v_cache"], dev["cu_seqlens_q"],
+                                    dev["seqused_k"], dev["block_table"], s_.softmax_scale, s_.causal,
+                                    out=out, cu_seqlens_q_host=b.cu_seqlens_q,
+                                    seqused_k_host=b.seqused_k)
+
+    want = []
+    for b, dev in zip(batches, devs):
+        want.append(call(b, dev, None).clone())
+        torch.cuda.synchronize()
+    outs = [torch.empty_like(w) for w in want]
+    for _ in range(5):
+        for b, dev, o in zip(batches, devs, outs):
+            call(b, dev, o)
+    torch.cuda.synchronize()
+    for w, o in zip(want, outs):
+        assert torch.equal(w, o)
