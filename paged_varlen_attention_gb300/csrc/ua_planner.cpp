@@ -74,13 +74,29 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
     units.clear();
     unsorted.clear();
     int32_t max_kv = 0;
+    // Prefill rows that would make only a few long work items (say a group's
+    // new tokens against a long shared prefix) leave most SMs idle in the
+    // prefill kernel, one CTA per item; they go to the decode kernel instead,
+    // whose split-KV spreads the same keys over every CTA.
+    bool prefill_rows_to_decode = false;
+    if (pre_ok) {
+        int64_t items = 0;
+        int64_t max_steps = 0;
+        for (int s = 0; s < p.num_seqs; ++s) {
+            const int64_t lq = (int64_t)p.cu[s + 1] - p.cu[s];
+            if (lq * g <= kDecRows) continue;
+            items += (lq * g + kPreTileRows - 1) / kPreTileRows * p.hkv;
+            max_steps = std::max<int64_t>(max_steps, ((int64_t)p.lk[s] + 63) / 64);
+        }
+        prefill_rows_to_decode = items > 0 && items * 4 < std::max(num_sms, 1) && max_steps >= 32;
+    }
     // 32-bit arithmetic below: validate_problem bounds Lq * G and Lk well inside int32
     for (int s = 0; s < p.num_seqs; ++s) {
         const int32_t lq = p.cu[s + 1] - p.cu[s];
         const int32_t lk = p.lk[s];
         if (lq == 0) continue;
         const int32_t rows = lq * g;
-        const bool decode = rows <= kDecRows || !pre_ok;
+        const bool decode = rows <= kDecRows || !pre_ok || prefill_rows_to_decode;
         const int32_t step = decode ? kDecRows : kPreTileRows;
         // visible keys of the last row of each row tile; the same for every kv head
         for (int32_t r0 = 0; r0 < rows; r0 += step) {

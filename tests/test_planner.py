@@ -158,3 +158,17 @@ def test_random_batches():
         hk = int(rng.choice([1, 2, 4, 8]))
         hq = hk * int(rng.choice([1, 2, 3, 4, 8, 16]))
         check_plan(q, k, hq, hk, 128, True, int(rng.integers(1, 200)))
+
+
+def test_few_long_prefill_items_go_to_the_decode_kernel():
+    """A group's 64 new tokens against a 4096-token shared prefix (non-causal):
+    one work item per KV head would leave most SMs idle, so the rows become
+    split decode units; the standard prefill batches keep their prefill items."""
+    c = check_plan([64], [4096], 32, 8, 128, causal=False)
+    assert c["prefill_tiles"] == 0 and c["dec_ctas"] == 2 * 152
+    s = W.config_spec(3)
+    c = check_plan(s.q_lens, s.k_lens, s.num_q_heads, s.num_kv_heads, s.head_size, s.causal)
+    assert c["prefill_tiles"] == 2048
+    # short contexts stay on the prefill kernel even with few items
+    c = check_plan([200], [200], 8, 2, 128)
+    assert c["prefill_tiles"] > 0
