@@ -10,7 +10,9 @@ default workload is the Llama-3.1-8B-shaped pure-decode batch (64 sequences,
 one new token each, contexts uniform in [2048, 4096], Hq 32, Hkv 8, head size
 128, bf16, 16-token pages).  Inputs are resident in HBM when timing starts;
 the KV working set (~0.8 GB) is far larger than L2, and L2 is also flushed
-(a 256 MB write) between timed steps, outside the timed interval.
+between timed steps, outside the timed interval: a 256 MB write, then a 256 MB
+read, so that the write's dirty lines are not written back inside the next
+timed step.
 
 The JSON line carries the metric (query tokens/s), the roofline of the
 dominant kernel (CUDA-event time per launch against the measured HBM
@@ -63,6 +65,8 @@ DEFAULT_WORKLOAD = "llama3_8b_decode_64x2k-4k"
 # share a 4096-token prefix, own contexts U[256, 1024] tokens; prefix pass over
 # the whole group as one non-causal sequence + own-keys pass + LSE merge.
 CASCADE_WORKLOAD = "llama3_8b_cascade_64dec_shared4k"
+# KV-cache append of the 16 x 1000-token prefill batch's new tokens (Hkv 8, D 128).
+APPEND_WORKLOAD = "kv_append_mistral_24b_16x1000"
 
 
 def parse_args():
@@ -71,7 +75,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=sorted(WORKLOADS) + [CASCADE_WORKLOAD])
+                    choices=sorted(WORKLOADS) + [CASCADE_WORKLOAD, APPEND_WORKLOAD])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -134,6 +138,21 @@ def ncu_traffic(kernel, workload):
     if not e or e.get("source_sha256_16") != source_hash(e.get("sources", [])):
         return None
     return float(e["dram_bytes_per_launch"])
+
+
+class L2Flush:
+    """Between timed steps: write a 256 MB buffer (evicts everything useful from
+    the 126 MB L2), then read another 256 MB buffer, so that the write's dirty
+    lines are written back here and not inside the next timed interval."""
+
+    def __init__(self, torch, device):
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+        self.r = torch.ones(64 << 20, dtype=torch.int32, device=device)
+        self.sink = torch.empty((), dtype=torch.int64, device=device)
+
+    def __call__(self):
+        self.w.fill_(1)
+        self.sink.copy_(self.r.sum())
 
 
 class ClockSampler:
@@ -275,7 +294,7 @@ def run_ours(args, rank, world, local, dist):
     ws_bytes = ua.workspace_size(cu_h, sk_h, spec.num_q_heads, spec.num_kv_heads,
                                  spec.head_size, batch.block_table_stride, spec.causal)
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    flush = L2Flush(torch, device)
     stream = torch.cuda.current_stream(device)
 
     def step():
@@ -297,12 +316,12 @@ def run_ours(args, rank, world, local, dist):
 
     def timed_pass():
         # steps back to back (no host sync in between, so the host-side planning of
-        # one step overlaps the GPU work of the previous one); L2 is flushed by a
+        # one step overlaps the GPU work of the previous one); L2 is flushed (a
         # 256 MB write before every step, outside the timed interval
         barrier(dist)
         torch.cuda.synchronize()
         for k in range(steps):
-            flush.fill_(1)
+            flush()
             ev0[k].record(stream)
             step()
             ev1[k].record(stream)
@@ -356,7 +375,7 @@ def run_ours(args, rank, world, local, dist):
             e2e_step()
         torch.cuda.synchronize()
         for k in range(steps):
-            flush.fill_(1)
+            flush()
             ev0[k].record(stream)
             e2e_step()
             ev1[k].record(stream)
@@ -468,7 +487,7 @@ def assemble(args, res, world, cpu):
                    "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads,
                    "head_size": spec.head_size, "block_size": spec.block_size,
                    "causal": bool(spec.causal),
-                   "l2": "inputs larger than L2, and L2 flushed (256 MB write) between steps",
+                   "l2": "inputs larger than L2, and L2 flushed between steps (256 MB write, then 256 MB read so the write-back is outside the timed interval)",
                    "parallelism": f"{world} independent replica(s), no collective"},
         "roofline": roof,
         "call": {"kv_tokens_per_s": world * work["kv_tokens"] * k / total_s,
@@ -527,7 +546,7 @@ def run_cascade(args):
     lse_p = torch.empty((n, hq), dtype=torch.float32, device=dev)
     lse_o = torch.empty_like(lse_p)
     stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
 
     def cascade():
         ua.unified_attention(qd, kd, vd, dv["cu_g"], dv["sk_g"], dv["bt_g"], scale, False, out=out_p,
@@ -554,7 +573,7 @@ def run_cascade(args):
                for _ in range(steps)]
         torch.cuda.synchronize()
         for a, b in evs:
-            flush.fill_(1)
+            flush()
             a.record(stream)
             fn()
             b.record(stream)
@@ -588,7 +607,7 @@ def run_cascade(args):
         "config": {"workload": CASCADE_WORKLOAD, "num_seqs": n, "q_tokens": n,
                    "shared_prefix_tokens": P, "own_kv_tokens": int(own.sum()),
                    "num_q_heads": hq, "num_kv_heads": hk, "head_size": d, "block_size": 16,
-                   "l2": "L2 flushed (256 MB write) between steps",
+                   "l2": "L2 flushed between steps (256 MB write, then 256 MB read so the write-back is outside the timed interval)",
                    "parallelism": "1 GPU, no collective"},
         "roofline": {"kernel": "ua_decode_kernel (own-keys pass)", "bound": "hbm",
                      "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -600,6 +619,70 @@ def run_cascade(args):
                     "speedup_vs_direct": sum(t_dir) / sum(t_cas),
                     "max_abs_diff_vs_direct": float(diff.max())},
         "gpu_launches": 3 * steps,
+        "clocks": clocks.summary(),
+    }
+
+
+def run_kv_append(args):
+    """Time ua_kv_append alone on one GPU (HBM-bound: each new token's K and V rows
+    read once and written once into their pages)."""
+    import torch
+    import paged_varlen_attention_gb300 as ua
+
+    ua.load_library()
+    dev = torch.device("cuda:0")
+    b = W.config_batch(WORKLOADS["mistral_24b_prefill_16x1000"], poison=False)
+    s_ = b.spec
+    total = int(b.cu_seqlens_q[-1])
+    rng = np.random.Generator(np.random.PCG64(3100))
+    hk, d = s_.num_kv_heads, s_.head_size
+    t16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
+    k_new = t16(W.f32_to_bf16_bits(rng.standard_normal((total, hk, d), dtype=np.float32)))
+    v_new = t16(W.f32_to_bf16_bits(rng.standard_normal((total, hk, d), dtype=np.float32)))
+    kc, vc = t16(b.k_cache), t16(b.v_cache)
+    cu = torch.from_numpy(b.cu_seqlens_q).to(dev)
+    sk = torch.from_numpy(b.seqused_k).to(dev)
+    bt = torch.from_numpy(b.block_table).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = L2Flush(torch, dev)
+
+    def step():
+        ua.kv_append(k_new, v_new, kc, vc, cu, sk, bt, cu_seqlens_q_host=b.cu_seqlens_q,
+                     seqused_k_host=b.seqused_k)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    with ClockSampler(gpu_id_for_smi(torch, 0)) as clocks:
+        torch.cuda.synchronize()
+        for a, e in evs:
+            flush()
+            a.record(stream)
+            step()
+            e.record(stream)
+        torch.cuda.synchronize()
+    times = [a.elapsed_time(e) for a, e in evs]
+    if ua.device_status():
+        raise RuntimeError("device status set after the append steps")
+    nbytes = 2 * 2 * total * hk * d * 2            # K and V: read once, written once
+    ms = statistics.mean(times)
+    achieved = nbytes / (ms / 1e3) / 1e9
+    peaks = measured_peaks()
+    return {
+        "metric": "KV-cache append tokens/s on 1 GB300 vs HBM roofline", "value": total / (ms / 1e3),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, shuffled pages)",
+        "config": {"workload": APPEND_WORKLOAD, "new_tokens": total, "num_kv_heads": hk,
+                   "head_size": d, "block_size": 16, "l2": "L2 flushed between steps (256 MB write, then 256 MB read so the write-back is outside the timed interval)",
+                   "parallelism": "1 GPU, no collective"},
+        "roofline": {"kernel": "ua_kv_append_kernel", "bound": "hbm", "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": None, "per_launch": f"{nbytes} bytes (K and V rows read + written)",
+                     "launch_ms": ms, "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"},
+        "gpu_launches": args.steps,
         "clocks": clocks.summary(),
     }
 
@@ -616,10 +699,11 @@ def main():
         return
     import torch
 
-    if args.workload == CASCADE_WORKLOAD:
+    if args.workload in (CASCADE_WORKLOAD, APPEND_WORKLOAD):
         if world != 1:
-            raise SystemExit("the cascade workload runs on one GPU")
-        print(json.dumps(run_cascade(args)), flush=True)
+            raise SystemExit("this workload runs on one GPU")
+        fn = run_cascade if args.workload == CASCADE_WORKLOAD else run_kv_append
+        print(json.dumps(fn(args)), flush=True)
         return
     res = run_ours(args, rank, world, local, dist)
     cpu = None

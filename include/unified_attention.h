@@ -215,6 +215,48 @@ ua_status ua_merge_attn_states(const void *out_a, const float *lse_a, const void
                                int32_t head_size, void *stream);
 
 /*
+ * ua_kv_append -- the step just before attention: write the new tokens' K
+ * and V rows into their pages.  Token i of sequence s (0 <= i < Lq) goes to
+ * context position p = seqused_k[s] - Lq + i (the new tokens are the last Lq
+ * positions of the context that seqused_k counts, as in the bottom-right
+ * causal mask), i.e. k_cache[block_table[s][p / 16]][p % 16][:][:] = k_new[t]
+ * with t = cu_seqlens_q[s] + i, and the same for V.  Nothing else in the
+ * caches is written.  The metadata and cache arguments are those of
+ * unified_attention; k_new, v_new: device bf16 [total_q, Hkv, D], 16-byte
+ * aligned.  Every sequence needs Lq <= Lk; Hkv * D up to 2048 (else
+ * UA_ERR_UNSUPPORTED).  Host checks as for
+ * unified_attention (nothing launched on failure); a block id outside
+ * [0, num_blocks) is skipped and reported through ua_device_status.  Async on
+ * stream.  The pages describe the cache layout and that seqused_k counts the
+ * whole context; the append itself is the step the attention call assumes
+ * has happened.
+ */
+ua_status ua_kv_append(const void *k_new, const void *v_new, const int32_t *cu_seqlens_q,
+                       const int32_t *seqused_k, const int32_t *block_table, void *k_cache,
+                       void *v_cache, const int32_t *cu_seqlens_q_host,
+                       const int32_t *seqused_k_host, int32_t num_seqs, int32_t num_kv_heads,
+                       int32_t head_size, int32_t block_size, int32_t num_blocks,
+                       int32_t block_table_stride, void *stream);
+
+/*
+ * unified_attention_append -- ua_kv_append of k_new / v_new, then
+ * unified_attention over the updated caches, in one call on one stream (the
+ * new tokens' keys are in the cache before any attention kernel reads it).
+ * Arguments as for the two calls; every check of both runs before anything is
+ * launched.
+ */
+ua_status unified_attention_append(const void *q, const void *k_new, const void *v_new,
+                                   void *k_cache, void *v_cache, const int32_t *cu_seqlens_q,
+                                   const int32_t *seqused_k, const int32_t *block_table,
+                                   float softmax_scale, int32_t causal, void *out,
+                                   const int32_t *cu_seqlens_q_host,
+                                   const int32_t *seqused_k_host, int32_t num_seqs,
+                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                                   int32_t block_size, int32_t num_blocks,
+                                   int32_t block_table_stride, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+
+/*
  * unified_attention_no_alloc -- the same operation and arguments as
  * unified_attention, minus the workspace: the launch plan and the split-KV
  * partials go into a device array the library owns, so the caller never

@@ -138,3 +138,36 @@ def merge(outs, lses):
     _load().ua_oracle_merge(len(outs), ctypes.cast(op, ctypes.c_void_p),
                             ctypes.cast(lp, ctypes.c_void_p), rows, d, _ptr(out), _ptr(lse))
     return out, lse
+
+
+def kv_append(k_cache, v_cache, k_new, v_new, cu_seqlens_q, seqused_k, block_table):
+    """Write each new token's K and V rows into its page slot; returns new caches.
+
+    The reading (the pages say only that seqused_k counts the whole context and
+    that the cache is paged): the Lq new tokens of sequence s are the LAST Lq
+    positions of its context of Lk = seqused_k[s] tokens, so token i of the
+    sequence goes to position p = Lk - Lq + i, page block_table[s][p // bs],
+    slot p % bs.  Every other cache entry is left as it was.  Plain loops; the
+    caches are copied, not modified.  k_new / v_new: uint16 (bf16 bits)
+    [total_q, Hkv, D]; caches [num_blocks, bs, Hkv, D].
+    """
+    k_out = np.array(k_cache, dtype=np.uint16, copy=True)
+    v_out = np.array(v_cache, dtype=np.uint16, copy=True)
+    cu = np.asarray(cu_seqlens_q, dtype=np.int64)
+    sk = np.asarray(seqused_k, dtype=np.int64)
+    bt = np.asarray(block_table, dtype=np.int64)
+    bs = k_out.shape[1]
+    for s in range(len(sk)):
+        lq = int(cu[s + 1] - cu[s])
+        lk = int(sk[s])
+        if lq > lk:
+            raise OracleError("a sequence has more new tokens than context")
+        for i in range(lq):
+            t = int(cu[s]) + i
+            pos = lk - lq + i
+            page = int(bt[s, pos // bs])
+            if not 0 <= page < k_out.shape[0]:
+                raise OracleError("block id out of range")
+            k_out[page, pos % bs] = k_new[t]
+            v_out[page, pos % bs] = v_new[t]
+    return k_out, v_out

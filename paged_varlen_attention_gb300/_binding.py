@@ -23,7 +23,8 @@ STATUS = {0: "UA_OK", 1: "UA_ERR_INVALID_ARG", 2: "UA_ERR_UNSUPPORTED", 3: "UA_E
 DEVICE_BAD_BLOCK_ID = 0x1
 DEVICE_WAIT_TIMEOUT = 0x2
 
-SYMBOLS = ("unified_attention", "unified_attention_lse", "ua_merge_attn_states",
+SYMBOLS = ("unified_attention", "unified_attention_lse", "ua_merge_attn_states", "ua_kv_append",
+           "unified_attention_append",
            "ua_workspace_size", "ua_status_string", "ua_device_status", "ua_plan_inspect",
            "ua_profile_enable", "ua_profile_read")
 
@@ -62,6 +63,12 @@ def load_library():
         lib.unified_attention_lse.restype = ctypes.c_int
         lib.ua_merge_attn_states.argtypes = [P, P, P, P, P, P, I64, I32, P]
         lib.ua_merge_attn_states.restype = ctypes.c_int
+        lib.ua_kv_append.argtypes = [P, P, P, P, P, P, P, P, P, I32, I32, I32, I32, I32, I32, P]
+        lib.ua_kv_append.restype = ctypes.c_int
+        lib.unified_attention_append.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_float, I32, P, P,
+                                                 P, I32, I32, I32, I32, I32, I32, I32, P,
+                                                 ctypes.c_size_t, P]
+        lib.unified_attention_append.restype = ctypes.c_int
         lib.ua_workspace_size.argtypes = [P, P, I32, I32, I32, I32, I32, I32, I32,
                                           ctypes.POINTER(ctypes.c_size_t)]
         lib.ua_workspace_size.restype = ctypes.c_int
@@ -123,7 +130,7 @@ def _workspace(torch, device, nbytes):
 
 def unified_attention(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table, softmax_scale,
                       causal=True, out=None, *, cu_seqlens_q_host=None, seqused_k_host=None,
-                      workspace=None, stream=None, lse=None):
+                      workspace=None, stream=None, lse=None, k_new=None, v_new=None):
     """Attention over a paged varlen batch (see ``include/unified_attention.h``).
 
     q: bf16 [total_q, Hq, D]; k_cache / v_cache: bf16 [num_blocks, 16, Hkv, D];
@@ -132,6 +139,8 @@ def unified_attention(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table,
     avoid a device-to-host read.  Returns ``out`` (bf16 [total_q, Hq, D]).
     lse: an fp32 CUDA tensor [total_q, Hq] to also receive each row's natural-log
     softmax normaliser (calls ``unified_attention_lse``).
+    k_new, v_new: the new tokens' K / V rows (bf16 [total_q, Hkv, D]) to write into
+    their pages first (calls ``unified_attention_append``; see ``kv_append``).
     """
     import torch
 
@@ -164,6 +173,25 @@ def unified_attention(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table,
         stream = torch.cuda.current_stream(q.device).cuda_stream
     elif hasattr(stream, "cuda_stream"):
         stream = stream.cuda_stream
+    if k_new is not None:
+        if v_new is None:
+            raise UAError(1, "k_new and v_new go together")
+        if lse is not None:
+            kv_append(k_new, v_new, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table,
+                      cu_seqlens_q_host=cu_h, seqused_k_host=sk_h, stream=stream)
+        else:
+            for name, t in (("k_new", k_new), ("v_new", v_new)):
+                if (not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous()
+                        or tuple(t.shape) != (total_q, hk, d)):
+                    raise UAError(1, f"{name} must be a contiguous CUDA bf16 tensor [total_q, Hkv, D]")
+            rc = lib.unified_attention_append(
+                q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(),
+                v_cache.data_ptr(), cu_seqlens_q.data_ptr(), seqused_k.data_ptr(),
+                block_table.data_ptr(), float(softmax_scale), int(bool(causal)), out.data_ptr(),
+                _np_ptr(cu_h), _np_ptr(sk_h), num_seqs, hq, hk, d, bs, nb, stride, ws_ptr,
+                workspace.numel(), stream)
+            _check(rc, "unified_attention_append")
+            return out
     if lse is None:
         rc = lib.unified_attention(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                                    cu_seqlens_q.data_ptr(), seqused_k.data_ptr(),
@@ -257,3 +285,37 @@ def profile_read(calls_back: int = 0):
     _check(load_library().ua_profile_read(int(calls_back), _np_ptr(ms), _np_ptr(ln)),
            "ua_profile_read")
     return ms.tolist(), ln.tolist()
+
+
+def kv_append(k_new, v_new, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table, *,
+              cu_seqlens_q_host=None, seqused_k_host=None, stream=None):
+    """Write the new tokens' K / V rows ([total_q, Hkv, D] bf16 CUDA tensors) into
+    their pages of k_cache / v_cache (``ua_kv_append``): token i of sequence s goes to
+    context position seqused_k[s] - Lq + i."""
+    import torch
+
+    lib = load_library()
+    for name, t, dt in (("k_new", k_new, torch.bfloat16), ("v_new", v_new, torch.bfloat16),
+                        ("k_cache", k_cache, torch.bfloat16), ("v_cache", v_cache, torch.bfloat16),
+                        ("cu_seqlens_q", cu_seqlens_q, torch.int32),
+                        ("seqused_k", seqused_k, torch.int32),
+                        ("block_table", block_table, torch.int32)):
+        if not t.is_cuda or t.dtype != dt or not t.is_contiguous():
+            raise UAError(1, f"{name} must be a contiguous CUDA {dt} tensor")
+    nb, bs, hk, d = k_cache.shape
+    if v_cache.shape != k_cache.shape or k_new.shape[1:] != (hk, d) or v_new.shape != k_new.shape:
+        raise UAError(1, "k_new / v_new / cache shapes disagree")
+    cu_h = _host_i32(cu_seqlens_q if cu_seqlens_q_host is None else cu_seqlens_q_host)
+    sk_h = _host_i32(seqused_k if seqused_k_host is None else seqused_k_host)
+    if len(cu_h) and int(cu_h[-1]) != k_new.shape[0]:
+        raise UAError(1, "cu_seqlens_q does not match k_new")
+    stride = int(block_table.shape[1]) if block_table.dim() == 2 else 0
+    if stream is None:
+        stream = torch.cuda.current_stream(k_new.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    rc = lib.ua_kv_append(k_new.data_ptr(), v_new.data_ptr(), cu_seqlens_q.data_ptr(),
+                          seqused_k.data_ptr(), block_table.data_ptr(), k_cache.data_ptr(),
+                          v_cache.data_ptr(), _np_ptr(cu_h), _np_ptr(sk_h), int(sk_h.shape[0]), hk,
+                          d, bs, nb, stride, stream)
+    _check(rc, "ua_kv_append")

@@ -599,3 +599,65 @@ extern "C" ua_status unified_attention_lse(const void *q, const void *k_cache, c
                              num_blocks, block_table_stride, workspace, workspace_bytes, stream,
                              /*pinned_plan=*/true, lse);
 }
+
+extern "C" ua_status ua_kv_append(const void *k_new, const void *v_new, const int32_t *cu_seqlens_q,
+                                  const int32_t *seqused_k, const int32_t *block_table,
+                                  void *k_cache, void *v_cache, const int32_t *cu_seqlens_q_host,
+                                  const int32_t *seqused_k_host, int32_t num_seqs,
+                                  int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                  int32_t num_blocks, int32_t block_table_stride, void *stream) {
+    // the attention call's checks with causal = 1 (every sequence has Lq <= Lk:
+    // its new tokens fit in its context)
+    Problem pr = make_problem(cu_seqlens_q_host, seqused_k_host, num_seqs, num_kv_heads,
+                              num_kv_heads, head_size, block_size, block_table_stride, 1);
+    const int v = validate_problem(pr);
+    if (v) return static_cast<ua_status>(v);
+    if (num_seqs == 0 || cu_seqlens_q_host[num_seqs] == 0) return UA_OK;
+    if (!k_new || !v_new || !cu_seqlens_q || !seqused_k || !block_table || !k_cache || !v_cache)
+        return UA_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return UA_ERR_INVALID_ARG;
+    if (num_blocks <= 0 || (int64_t)num_blocks * block_size >= ((int64_t)1 << 31)) return UA_ERR_INVALID_ARG;
+    if ((int64_t)num_kv_heads * head_size > 2048) return UA_ERR_UNSUPPORTED;
+    DeviceState *ds = nullptr;
+    ua_status st = device_state(&ds);
+    if (st != UA_OK) return st;
+    if (launch_kv_append(k_new, v_new, cu_seqlens_q, seqused_k, block_table, k_cache, v_cache,
+                         num_seqs, cu_seqlens_q_host[num_seqs], num_kv_heads, head_size, num_blocks,
+                         block_table_stride, ds->status, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return UA_ERR_CUDA;
+    }
+    return UA_OK;
+}
+
+extern "C" ua_status unified_attention_append(
+    const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+    const int32_t *cu_seqlens_q, const int32_t *seqused_k, const int32_t *block_table,
+    float softmax_scale, int32_t causal, void *out, const int32_t *cu_seqlens_q_host,
+    const int32_t *seqused_k_host, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_size, int32_t block_size, int32_t num_blocks, int32_t block_table_stride,
+    void *workspace, size_t workspace_bytes, void *stream) {
+    // everything the attention call checks, first, so that a rejected call writes nothing
+    Problem pr = make_problem(cu_seqlens_q_host, seqused_k_host, num_seqs, num_q_heads,
+                              num_kv_heads, head_size, block_size, block_table_stride, causal);
+    const int v = validate_problem(pr);
+    if (v) return static_cast<ua_status>(v);
+    size_t need = 0;
+    ua_status st = ua_workspace_size(cu_seqlens_q_host, seqused_k_host, num_seqs, num_q_heads,
+                                     num_kv_heads, head_size, block_size, block_table_stride,
+                                     causal, &need);
+    if (st != UA_OK) return st;
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, kAlign)))
+        return UA_ERR_WORKSPACE;
+    if (!std::isfinite(softmax_scale) || !q || !out || !aligned(q, 16) || !aligned(out, 16))
+        return UA_ERR_INVALID_ARG;
+    st = ua_kv_append(k_new, v_new, cu_seqlens_q, seqused_k, block_table, k_cache, v_cache,
+                      cu_seqlens_q_host, seqused_k_host, num_seqs, num_kv_heads, head_size,
+                      block_size, num_blocks, block_table_stride, stream);
+    if (st != UA_OK) return st;
+    return unified_attention(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table, softmax_scale,
+                             causal, out, cu_seqlens_q_host, seqused_k_host, num_seqs, num_q_heads,
+                             num_kv_heads, head_size, block_size, num_blocks, block_table_stride,
+                             workspace, workspace_bytes, stream);
+}

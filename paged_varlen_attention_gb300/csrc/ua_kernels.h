@@ -74,4 +74,12 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
                         int32_t block_table_stride, void *workspace, size_t workspace_bytes,
                         void *stream, bool pinned_plan, float *lse);
 
+// Writes the new tokens' K / V rows ([total_q, Hkv, D] bf16) into their
+// pages: token i of sequence s to position seqused_k[s] - Lq + i.
+cudaError_t launch_kv_append(const void *k_new, const void *v_new, const int32_t *cu,
+                             const int32_t *seqused_k, const int32_t *block_table, void *k_cache,
+                             void *v_cache, int32_t num_seqs, int32_t total_q, int32_t num_kv_heads,
+                             int32_t head_size, int32_t num_blocks, int32_t bt_stride, int *status,
+                             cudaStream_t stream);
+
 }  // namespace ua

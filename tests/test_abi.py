@@ -92,3 +92,13 @@ def test_noncausal_allows_more_queries_than_keys(lib):
     assert counts["dec_pages"] > 0 or counts["prefill_tiles"] > 0
     with pytest.raises(B.UAError):
         B.plan_inspect(cu, sk, 4, 2, 64, 1, causal=True)
+
+
+def test_kv_append_rejects_more_new_tokens_than_context(lib):
+    import ctypes
+    cu = np.array([0, 5], np.int32)
+    sk = np.array([3], np.int32)          # Lq = 5 > Lk = 3
+    p = ctypes.c_void_p(16)
+    rc = lib.ua_kv_append(p, p, p, p, p, p, p, cu.ctypes.data_as(ctypes.c_void_p),
+                          sk.ctypes.data_as(ctypes.c_void_p), 1, 2, 64, 16, 8, 1, None)
+    assert rc == 1                        # UA_ERR_INVALID_ARG, nothing launched

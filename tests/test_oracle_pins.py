@@ -332,3 +332,32 @@ def test_shared_prefix_cascade_equals_full_attention(causal_suffix):
     if causal_suffix:
         ref = sdpa_reference(q, fks, fvs, q_lens, hq, True, scale)
         np.testing.assert_allclose(merged, ref, rtol=0, atol=1e-12)
+
+
+def test_kv_append_then_attention_equals_dense_attention():
+    """New tokens appended into the pages at positions Lk - Lq .. Lk - 1 (the
+    reading that seqused_k counts them, bottom-right): attention over the cache
+    afterwards equals attention over the dense concatenation old ++ new; the
+    entries the append does not own are unchanged bit for bit."""
+    q_lens, old = [1, 4, 0, 9], [30, 16, 5, 7]
+    hq, hk, d = 4, 2, 32
+    k_lens = [o + n for o, n in zip(old, q_lens)]
+    q, ks, vs, rng = random_dense(q_lens, k_lens, hq, hk, d, seed=47)
+    full = batch_from_dense(q, ks, vs, q_lens, hq, poison=False)
+    # the same pages, with the new tokens' rows holding garbage before the append
+    before_k, before_v = full.k_cache.copy(), full.v_cache.copy()
+    k_new = np.concatenate([k[o:] for k, o in zip(ks, old)])
+    v_new = np.concatenate([v[o:] for v, o in zip(vs, old)])
+    for s, (o, n) in enumerate(zip(old, q_lens)):
+        for pos in range(o, o + n):
+            page = full.block_table[s, pos // 16]
+            before_k[page, pos % 16] = W.BF16_NAN
+            before_v[page, pos % 16] = W.BF16_NAN
+    after_k, after_v = oracle.kv_append(before_k, before_v, k_new, v_new, full.cu_seqlens_q,
+                                        full.seqused_k, full.block_table)
+    assert np.array_equal(after_k, full.k_cache) and np.array_equal(after_v, full.v_cache)
+    appended = W.Batch(full.spec, q, after_k, after_v, full.cu_seqlens_q, full.seqused_k,
+                       full.block_table, full.poison_blocks)
+    got, _ = oracle.attention_batch(appended)
+    ref = sdpa_reference(q, ks, vs, q_lens, hq, True, full.spec.softmax_scale)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
