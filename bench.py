@@ -67,6 +67,8 @@ DEFAULT_WORKLOAD = "llama3_8b_decode_64x2k-4k"
 CASCADE_WORKLOAD = "llama3_8b_cascade_64dec_shared4k"
 # KV-cache append of the 16 x 1000-token prefill batch's new tokens (Hkv 8, D 128).
 APPEND_WORKLOAD = "kv_append_mistral_24b_16x1000"
+# The headline decode batch over an FP8 E4M3 KV cache (per-tensor scales).
+FP8_WORKLOAD = "llama3_8b_decode_64x2k-4k_fp8kv"
 
 
 def parse_args():
@@ -75,7 +77,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=sorted(WORKLOADS) + [CASCADE_WORKLOAD, APPEND_WORKLOAD])
+                    choices=sorted(WORKLOADS) + [CASCADE_WORKLOAD, APPEND_WORKLOAD, FP8_WORKLOAD])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -687,6 +689,83 @@ def run_kv_append(args):
     }
 
 
+def run_fp8kv(args):
+    """The headline decode batch over an E4M3 cache: the same call as the default
+    workload, with K / V read as one byte per element (half the bytes)."""
+    import torch
+    import paged_varlen_attention_gb300 as ua
+
+    ua.load_library()
+    dev = torch.device("cuda:0")
+    b = W.config_batch(WORKLOADS[DEFAULT_WORKLOAD], poison=False)
+    s_ = b.spec
+    ks, vs = 0.05, 0.05
+    k8, v8 = W.fp8_caches(b, ks, vs)
+    t16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
+    qd = t16(b.q)
+    kd, vd = torch.from_numpy(k8).to(dev), torch.from_numpy(v8).to(dev)
+    cu = torch.from_numpy(b.cu_seqlens_q).to(dev)
+    sk = torch.from_numpy(b.seqused_k).to(dev)
+    bt = torch.from_numpy(b.block_table).to(dev)
+    out = torch.empty_like(qd)
+    stream = torch.cuda.current_stream(dev)
+    flush = L2Flush(torch, dev)
+
+    def step():
+        ua.unified_attention_fp8kv(qd, kd, vd, ks, vs, cu, sk, bt, s_.softmax_scale, True, out=out,
+                                   cu_seqlens_q_host=b.cu_seqlens_q, seqused_k_host=b.seqused_k)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    steps = args.steps
+
+    def timed():
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        torch.cuda.synchronize()
+        for a, e in evs:
+            flush()
+            a.record(stream)
+            step()
+            e.record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(e) for a, e in evs]
+
+    with ClockSampler(gpu_id_for_smi(torch, 0)) as clocks:
+        times = timed()
+        ua.profile_enable(True)
+        timed()
+    dec = [ua.profile_read(k)[0][0] for k in range(steps)]
+    ua.profile_enable(False)
+    if ua.device_status():
+        raise RuntimeError("device status set after the fp8 steps")
+    work = algorithmic_work(s_)
+    # K and V one byte per element: the bf16 figure's K+V bytes halved
+    dec_bytes = work["decode_bytes"] - work["kv_bytes"] // 2
+    dec_ms = statistics.mean(dec)
+    achieved = dec_bytes / (dec_ms / 1e3) / 1e9
+    peaks = measured_peaks()
+    total_s = sum(times) / 1e3
+    return {
+        "metric": METRIC, "value": s_.total_q * steps / total_s, "unit": "tokens/s", "n_gpus": 1,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": sum(times) / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 q/o, e4m3 kv",
+        "data": "synthetic (seeded N(0,1) bf16 quantised to e4m3 with scale 0.05, shuffled pages)",
+        "config": {"workload": FP8_WORKLOAD, "num_seqs": s_.num_seqs, "q_tokens": s_.total_q,
+                   "kv_tokens": work["kv_tokens"], "num_q_heads": s_.num_q_heads,
+                   "num_kv_heads": s_.num_kv_heads, "head_size": s_.head_size, "block_size": 16,
+                   "l2": "L2 flushed between steps (256 MB write, then 256 MB read so the write-back is outside the timed interval)",
+                   "parallelism": "1 GPU, no collective"},
+        "roofline": {"kernel": "ua_decode_kernel<128, fp8 kv>", "bound": "hbm", "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": None, "per_launch": f"{dec_bytes} algorithmic bytes (1-byte K/V)",
+                     "launch_ms": dec_ms, "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"},
+        "gpu_launches": steps,
+        "clocks": clocks.summary(),
+    }
+
+
 def main():
     args = parse_args()
     rank, world, local, dist = dist_setup(args.gpus)
@@ -699,10 +778,11 @@ def main():
         return
     import torch
 
-    if args.workload in (CASCADE_WORKLOAD, APPEND_WORKLOAD):
+    if args.workload in (CASCADE_WORKLOAD, APPEND_WORKLOAD, FP8_WORKLOAD):
         if world != 1:
             raise SystemExit("this workload runs on one GPU")
-        fn = run_cascade if args.workload == CASCADE_WORKLOAD else run_kv_append
+        fn = {CASCADE_WORKLOAD: run_cascade, APPEND_WORKLOAD: run_kv_append,
+              FP8_WORKLOAD: run_fp8kv}[args.workload]
         print(json.dumps(fn(args)), flush=True)
         return
     res = run_ours(args, rank, world, local, dist)

@@ -257,6 +257,39 @@ ua_status unified_attention_append(const void *q, const void *k_new, const void 
                                    size_t workspace_bytes, void *stream);
 
 /*
+ * unified_attention_fp8kv -- unified_attention over a KV cache stored as
+ * FP8 e4m3 bytes with one scale per tensor: the keys are k_scale * e4m3(byte)
+ * and the values v_scale * e4m3(byte) (the OCP "E4M3" format: 1 sign, 4
+ * exponent bits with bias 7, 3 mantissa bits; no infinities; 0x7f / 0xff are
+ * NaN).  k_cache, v_cache: device uint8 [num_blocks, block_size, Hkv, D], 16-
+ * byte aligned; q and out bf16 as for unified_attention; lse: optional fp32
+ * [total_q, Hq] (as unified_attention_lse) or NULL.  Every row runs in the
+ * decode kernel, whose warps turn each page into f16 (exact: e4m3 values are
+ * f16 values) and multiply with f16 Q (q is rounded to f16, so |q| must stay
+ * below 65504) and f16 P; k_scale is folded into the softmax scale and
+ * v_scale into the output.  head_size 128 only (else UA_ERR_UNSUPPORTED).
+ * Workspace size from ua_workspace_size_fp8kv.  The FP8 cache is the "KV cache
+ * compression" discussed on "[Kernel] [V1] Improved performance for V1 Triton
+ * (ROCm) backend" (vLLM PR #14152, review thread); the pages fix neither the
+ * format nor the scaling, and this reading takes e4m3 with per-tensor scales.
+ */
+ua_status unified_attention_fp8kv(const void *q, const void *k_cache, const void *v_cache,
+                                  float k_scale, float v_scale, const int32_t *cu_seqlens_q,
+                                  const int32_t *seqused_k, const int32_t *block_table,
+                                  float softmax_scale, int32_t causal, void *out, float *lse,
+                                  const int32_t *cu_seqlens_q_host,
+                                  const int32_t *seqused_k_host, int32_t num_seqs,
+                                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                                  int32_t block_size, int32_t num_blocks,
+                                  int32_t block_table_stride, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+ua_status ua_workspace_size_fp8kv(const int32_t *cu_seqlens_q_host,
+                                  const int32_t *seqused_k_host, int32_t num_seqs,
+                                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                                  int32_t block_size, int32_t block_table_stride, int32_t causal,
+                                  size_t *bytes);
+
+/*
  * unified_attention_no_alloc -- the same operation and arguments as
  * unified_attention, minus the workspace: the launch plan and the split-KV
  * partials go into a device array the library owns, so the caller never

@@ -64,6 +64,12 @@ def _load():
             lib.ua_oracle_attention.argtypes = [P, P, P, P, P, P, i, i, i, i, i, i, i,
                                                 ctypes.c_double, i, i, i, P, P, i]
             lib.ua_oracle_attention.restype = i
+            lib.ua_oracle_attention_fp8kv.argtypes = [P, P, P, ctypes.c_double, ctypes.c_double,
+                                                      P, P, P, i, i, i, i, i, i, i,
+                                                      ctypes.c_double, i, P, P, i]
+            lib.ua_oracle_attention_fp8kv.restype = i
+            lib.ua_oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+            lib.ua_oracle_e4m3_to_f64.restype = ctypes.c_double
             lib.ua_oracle_merge.argtypes = [i, P, P, ctypes.c_int64, i, P, P]
             lib.ua_oracle_merge.restype = i
             lib.ua_oracle_max_threads.restype = i
@@ -171,3 +177,40 @@ def kv_append(k_cache, v_cache, k_new, v_new, cu_seqlens_q, seqused_k, block_tab
             k_out[page, pos % bs] = k_new[t]
             v_out[page, pos % bs] = v_new[t]
     return k_out, v_out
+
+
+def e4m3_to_f64(code: int) -> float:
+    """Value of one FP8 E4M3 byte (see ua_oracle_e4m3_to_f64)."""
+    return float(_load().ua_oracle_e4m3_to_f64(int(code) & 0xff))
+
+
+def attention_fp8kv(q, k_cache, v_cache, k_scale, v_scale, cu_seqlens_q, seqused_k, block_table,
+                    softmax_scale, causal, nthreads=0):
+    """fp64 attention over a paged cache of E4M3 bytes (k = k_scale * e4m3(byte), v likewise).
+
+    q: uint16 (bf16 bits) [total_q, Hq, D]; k_cache / v_cache: uint8
+    [num_blocks, block_size, Hkv, D].  Returns (out fp64, lse fp64) as ``attention``.
+    """
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k_cache = np.ascontiguousarray(k_cache, dtype=np.uint8)
+    v_cache = np.ascontiguousarray(v_cache, dtype=np.uint8)
+    cu = np.ascontiguousarray(cu_seqlens_q, dtype=np.int32)
+    sk = np.ascontiguousarray(seqused_k, dtype=np.int32)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    if bt.ndim == 1:
+        bt = bt.reshape(len(sk), -1)
+    total_q, hq, d = q.shape
+    nb, bs, hk, d2 = k_cache.shape
+    if d2 != d or v_cache.shape != k_cache.shape:
+        raise OracleError("q / cache shapes disagree")
+    if len(cu) != len(sk) + 1 or (len(sk) and cu[-1] != total_q):
+        raise OracleError("cu_seqlens_q does not match q")
+    out = np.zeros((total_q, hq, d), dtype=np.float64)
+    lse = np.full((total_q, hq), -np.inf, dtype=np.float64)
+    rc = _load().ua_oracle_attention_fp8kv(_ptr(q), _ptr(k_cache), _ptr(v_cache), float(k_scale),
+                                           float(v_scale), _ptr(cu), _ptr(sk), _ptr(bt), len(sk),
+                                           hq, hk, d, bs, nb, bt.shape[1], float(softmax_scale),
+                                           int(bool(causal)), _ptr(out), _ptr(lse), int(nthreads))
+    if rc != 0:
+        raise OracleError(ERRORS.get(rc, f"oracle error {rc}"))
+    return out, lse

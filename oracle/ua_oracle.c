@@ -57,6 +57,28 @@ static double bf16_to_f64(uint16_t b)
     return (double)f;
 }
 
+/*
+ * FP8 E4M3 (the OCP 8-bit format with 4 exponent bits, bias 7, and 3
+ * mantissa bits, "fn": no infinities) to double, from the format's
+ * definition: exponent field e = 0 is subnormal, m/8 * 2^-6; otherwise
+ * (1 + m/8) * 2^(e-7); the code with e = 15 and m = 7 is NaN.  The FP8 cache
+ * is the "KV cache compression" of the review thread on "[Kernel] [V1]
+ * Improved performance for V1 Triton (ROCm) backend" (vLLM PR #14152), which
+ * names the fp8_e4m3fn type.
+ */
+double ua_oracle_e4m3_to_f64(uint8_t b)
+{
+    const int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
 /* Check the batch description before touching any data. */
 static int check_batch(const int32_t *cu, const int32_t *seqused_k, const int32_t *block_table,
                        int num_seqs, int num_q_heads, int num_kv_heads, int head_size,
@@ -97,12 +119,22 @@ static int check_batch(const int32_t *cu, const int32_t *seqused_k, const int32_
  * pass 0 and INT32_MAX for the plain operation.  Rows with no visible key get
  * out = 0 and lse = -inf (only possible with a window).
  */
-int ua_oracle_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
-                        const int32_t *cu_seqlens_q, const int32_t *seqused_k,
-                        const int32_t *block_table, int num_seqs, int num_q_heads,
-                        int num_kv_heads, int head_size, int block_size, int num_blocks,
-                        int block_table_stride, double softmax_scale, int causal,
-                        int key_lo, int key_hi, double *out, double *lse, int nthreads)
+/* One element of a K or V cache row: bf16 bits (kv8 = 0) or an e4m3 byte
+ * times the cache's scale (kv8 = 1). */
+static double cache_elem(const void *cache, int64_t idx, int kv8, double scale)
+{
+    if (kv8)
+        return scale * ua_oracle_e4m3_to_f64(((const uint8_t *)cache)[idx]);
+    return bf16_to_f64(((const uint16_t *)cache)[idx]);
+}
+
+static int attention_impl(const uint16_t *q, const void *k_cache, const void *v_cache, int kv8,
+                          double k_scale, double v_scale, const int32_t *cu_seqlens_q,
+                          const int32_t *seqused_k, const int32_t *block_table, int num_seqs,
+                          int num_q_heads, int num_kv_heads, int head_size, int block_size,
+                          int num_blocks, int block_table_stride, double softmax_scale,
+                          int causal, int key_lo, int key_hi, double *out, double *lse,
+                          int nthreads)
 {
     int rc = check_batch(cu_seqlens_q, seqused_k, block_table, num_seqs, num_q_heads,
                          num_kv_heads, head_size, block_size, num_blocks, block_table_stride,
@@ -149,11 +181,10 @@ int ua_oracle_attention(const uint16_t *q, const uint16_t *k_cache, const uint16
             for (int j = j0; j < j1; ++j) {
                 int64_t page = block_table[(int64_t)s * block_table_stride + j / block_size];
                 int64_t slot = j % block_size;
-                const uint16_t *krow =
-                    k_cache + ((page * block_size + slot) * num_kv_heads + g) * (int64_t)head_size;
+                const int64_t krow = ((page * block_size + slot) * num_kv_heads + g) * (int64_t)head_size;
                 double dot = 0.0;
                 for (int d = 0; d < head_size; ++d)
-                    dot += bf16_to_f64(qrow[d]) * bf16_to_f64(krow[d]);
+                    dot += bf16_to_f64(qrow[d]) * cache_elem(k_cache, krow + d, kv8, k_scale);
                 x[j - j0] = softmax_scale * dot;
                 if (x[j - j0] > m)
                     m = x[j - j0];
@@ -165,10 +196,9 @@ int ua_oracle_attention(const uint16_t *q, const uint16_t *k_cache, const uint16
                 denom += w;
                 int64_t page = block_table[(int64_t)s * block_table_stride + j / block_size];
                 int64_t slot = j % block_size;
-                const uint16_t *vrow =
-                    v_cache + ((page * block_size + slot) * num_kv_heads + g) * (int64_t)head_size;
+                const int64_t vrow = ((page * block_size + slot) * num_kv_heads + g) * (int64_t)head_size;
                 for (int d = 0; d < head_size; ++d)
-                    orow[d] += w * bf16_to_f64(vrow[d]);
+                    orow[d] += w * cache_elem(v_cache, vrow + d, kv8, v_scale);
             }
             for (int d = 0; d < head_size; ++d)
                 orow[d] /= denom;
@@ -178,6 +208,33 @@ int ua_oracle_attention(const uint16_t *q, const uint16_t *k_cache, const uint16
         free(x);
     }
     return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
+}
+
+int ua_oracle_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                        const int32_t *cu_seqlens_q, const int32_t *seqused_k,
+                        const int32_t *block_table, int num_seqs, int num_q_heads,
+                        int num_kv_heads, int head_size, int block_size, int num_blocks,
+                        int block_table_stride, double softmax_scale, int causal,
+                        int key_lo, int key_hi, double *out, double *lse, int nthreads)
+{
+    return attention_impl(q, k_cache, v_cache, 0, 1.0, 1.0, cu_seqlens_q, seqused_k, block_table,
+                          num_seqs, num_q_heads, num_kv_heads, head_size, block_size, num_blocks,
+                          block_table_stride, softmax_scale, causal, key_lo, key_hi, out, lse,
+                          nthreads);
+}
+
+/* The same over an e4m3 cache: k = k_scale * e4m3(byte), v = v_scale * e4m3(byte). */
+int ua_oracle_attention_fp8kv(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                              double k_scale, double v_scale, const int32_t *cu_seqlens_q,
+                              const int32_t *seqused_k, const int32_t *block_table, int num_seqs,
+                              int num_q_heads, int num_kv_heads, int head_size, int block_size,
+                              int num_blocks, int block_table_stride, double softmax_scale,
+                              int causal, double *out, double *lse, int nthreads)
+{
+    return attention_impl(q, k_cache, v_cache, 1, k_scale, v_scale, cu_seqlens_q, seqused_k,
+                          block_table, num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                          num_blocks, block_table_stride, softmax_scale, causal, 0, 2147483647,
+                          out, lse, nthreads);
 }
 
 /*

@@ -11,7 +11,8 @@ generator) can be used on machines without the built library.
 """
 
 _EXPORTS = ("UAError", "device_status", "library_path", "load_library", "plan_inspect",
-            "unified_attention", "merge_attn_states", "kv_append", "workspace_size",
+            "unified_attention", "unified_attention_fp8kv", "merge_attn_states", "kv_append",
+            "workspace_size",
             "profile_enable",
             "profile_read")
 

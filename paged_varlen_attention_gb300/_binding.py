@@ -24,7 +24,7 @@ DEVICE_BAD_BLOCK_ID = 0x1
 DEVICE_WAIT_TIMEOUT = 0x2
 
 SYMBOLS = ("unified_attention", "unified_attention_lse", "ua_merge_attn_states", "ua_kv_append",
-           "unified_attention_append",
+           "unified_attention_append", "unified_attention_fp8kv", "ua_workspace_size_fp8kv",
            "ua_workspace_size", "ua_status_string", "ua_device_status", "ua_plan_inspect",
            "ua_profile_enable", "ua_profile_read")
 
@@ -63,6 +63,13 @@ def load_library():
         lib.unified_attention_lse.restype = ctypes.c_int
         lib.ua_merge_attn_states.argtypes = [P, P, P, P, P, P, I64, I32, P]
         lib.ua_merge_attn_states.restype = ctypes.c_int
+        lib.unified_attention_fp8kv.argtypes = [P, P, P, ctypes.c_float, ctypes.c_float, P, P, P,
+                                                ctypes.c_float, I32, P, P, P, P, I32, I32, I32,
+                                                I32, I32, I32, I32, P, ctypes.c_size_t, P]
+        lib.unified_attention_fp8kv.restype = ctypes.c_int
+        lib.ua_workspace_size_fp8kv.argtypes = [P, P, I32, I32, I32, I32, I32, I32, I32,
+                                                ctypes.POINTER(ctypes.c_size_t)]
+        lib.ua_workspace_size_fp8kv.restype = ctypes.c_int
         lib.ua_kv_append.argtypes = [P, P, P, P, P, P, P, P, P, I32, I32, I32, I32, I32, I32, P]
         lib.ua_kv_append.restype = ctypes.c_int
         lib.unified_attention_append.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_float, I32, P, P,
@@ -319,3 +326,58 @@ def kv_append(k_new, v_new, k_cache, v_cache, cu_seqlens_q, seqused_k, block_tab
                           v_cache.data_ptr(), _np_ptr(cu_h), _np_ptr(sk_h), int(sk_h.shape[0]), hk,
                           d, bs, nb, stride, stream)
     _check(rc, "ua_kv_append")
+
+
+def unified_attention_fp8kv(q, k_cache, v_cache, k_scale, v_scale, cu_seqlens_q, seqused_k,
+                            block_table, softmax_scale, causal=True, out=None, *,
+                            cu_seqlens_q_host=None, seqused_k_host=None, workspace=None,
+                            stream=None, lse=None):
+    """Attention over a paged cache of FP8 E4M3 bytes (``unified_attention_fp8kv``).
+
+    k_cache / v_cache: uint8 CUDA tensors [num_blocks, 16, Hkv, 128] of E4M3 codes
+    with k = k_scale * e4m3(byte), v = v_scale * e4m3(byte); the rest as
+    ``unified_attention``.  Returns ``out``.
+    """
+    import torch
+
+    lib = load_library()
+    for name, t, dt in (("q", q, torch.bfloat16), ("k_cache", k_cache, torch.uint8),
+                        ("v_cache", v_cache, torch.uint8),
+                        ("cu_seqlens_q", cu_seqlens_q, torch.int32),
+                        ("seqused_k", seqused_k, torch.int32),
+                        ("block_table", block_table, torch.int32)):
+        if not t.is_cuda or t.dtype != dt or not t.is_contiguous():
+            raise UAError(1, f"{name} must be a contiguous CUDA {dt} tensor")
+    total_q, hq, d = q.shape
+    nb, bs, hk, d2 = k_cache.shape
+    if v_cache.shape != k_cache.shape or d2 != d:
+        raise UAError(1, "q / k_cache / v_cache shapes disagree")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is not None and (not lse.is_cuda or lse.dtype != torch.float32
+                            or tuple(lse.shape) != (total_q, hq) or not lse.is_contiguous()):
+        raise UAError(1, "lse must be a contiguous CUDA float32 tensor [total_q, Hq]")
+    cu_h = _host_i32(cu_seqlens_q if cu_seqlens_q_host is None else cu_seqlens_q_host)
+    sk_h = _host_i32(seqused_k if seqused_k_host is None else seqused_k_host)
+    num_seqs = int(sk_h.shape[0])
+    stride = int(block_table.shape[1]) if block_table.dim() == 2 else 0
+    if workspace is None:
+        need = ctypes.c_size_t(0)
+        _check(lib.ua_workspace_size_fp8kv(_np_ptr(cu_h), _np_ptr(sk_h), num_seqs, hq, hk, d, bs,
+                                           stride, int(bool(causal)), ctypes.byref(need)),
+               "ua_workspace_size_fp8kv")
+        workspace = _workspace(torch, q.device, int(need.value))
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    rc = lib.unified_attention_fp8kv(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                     float(k_scale), float(v_scale), cu_seqlens_q.data_ptr(),
+                                     seqused_k.data_ptr(), block_table.data_ptr(),
+                                     float(softmax_scale), int(bool(causal)), out.data_ptr(),
+                                     None if lse is None else lse.data_ptr(), _np_ptr(cu_h),
+                                     _np_ptr(sk_h), num_seqs, hq, hk, d, bs, nb, stride,
+                                     workspace.data_ptr() if workspace.numel() else None,
+                                     workspace.numel(), stream)
+    _check(rc, "unified_attention_fp8kv")
+    return out

@@ -208,17 +208,20 @@ static bool encode_map(CUtensorMap *map, const void *base, uint64_t inner, uint6
 // (64 columns, 16 slots, D/64 chunks, Hkv, blocks): one box {64, 16, D/64, 1, 1}
 // is one 16-token page of one KV head, laid out [chunk][slot][64] in shared
 // memory with the 128-byte swizzle.  Out-of-range blocks read zeros.
+// eb: bytes per element, 2 (bf16) or 1 (e4m3): a 128-byte chunk is 64 or 128
+// elements, and a page row D * eb bytes.
 static bool encode_page_map(CUtensorMap *map, const void *base, int d, int hkv,
-                            uint64_t num_blocks) {
+                            uint64_t num_blocks, int eb = 2) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
-    const uint64_t row = (uint64_t)hkv * d * 2;   // bytes between slots
-    cuuint64_t dims[5] = {64, (cuuint64_t)kBlockSize, (cuuint64_t)(d / 64), (cuuint64_t)hkv,
-                          num_blocks};
-    cuuint64_t strides[4] = {row, 128, (cuuint64_t)d * 2, row * kBlockSize};
-    cuuint32_t box[5] = {64, (cuuint32_t)kBlockSize, (cuuint32_t)(d / 64), 1, 1};
+    const uint64_t row = (uint64_t)hkv * d * eb;   // bytes between slots
+    const cuuint32_t inner = 128 / eb, chunks = (cuuint32_t)(d * eb / 128);
+    cuuint64_t dims[5] = {inner, (cuuint64_t)kBlockSize, chunks, (cuuint64_t)hkv, num_blocks};
+    cuuint64_t strides[4] = {row, 128, (cuuint64_t)d * eb, row * kBlockSize};
+    cuuint32_t box[5] = {inner, (cuuint32_t)kBlockSize, chunks, 1, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims,
+    CUresult r = enc(map, eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 5,
+                     const_cast<void *>(base), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -277,6 +280,27 @@ extern "C" ua_status ua_workspace_size(const int32_t *cu_seqlens_q_host,
     if (st != UA_OK) return st;
     thread_local Plan plan;
     build_plan(pr, ds->sms, kPrefillEnabled, plan);
+    *bytes = plan.layout.total_bytes;
+    return UA_OK;
+}
+
+extern "C" ua_status ua_workspace_size_fp8kv(const int32_t *cu_seqlens_q_host,
+                                             const int32_t *seqused_k_host, int32_t num_seqs,
+                                             int32_t num_q_heads, int32_t num_kv_heads,
+                                             int32_t head_size, int32_t block_size,
+                                             int32_t block_table_stride, int32_t causal,
+                                             size_t *bytes) {
+    if (!bytes) return UA_ERR_INVALID_ARG;
+    Problem pr = make_problem(cu_seqlens_q_host, seqused_k_host, num_seqs, num_q_heads,
+                              num_kv_heads, head_size, block_size, block_table_stride, causal);
+    int v = validate_problem(pr);
+    if (v) return static_cast<ua_status>(v);
+    if (head_size != 128) return UA_ERR_UNSUPPORTED;
+    DeviceState *ds = nullptr;
+    ua_status st = device_state(&ds);
+    if (st != UA_OK) return st;
+    thread_local Plan plan;
+    build_plan(pr, ds->sms, false, plan);     // every row in the decode kernel
     *bytes = plan.layout.total_bytes;
     return UA_OK;
 }
@@ -399,13 +423,16 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
                         int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                         int32_t head_size, int32_t block_size, int32_t num_blocks,
                         int32_t block_table_stride, void *workspace, size_t workspace_bytes,
-                        void *stream_ptr, bool pinned_plan, float *lse) {
+                        void *stream_ptr, bool pinned_plan, float *lse, int kv_fp8, float k_scale,
+                        float v_scale) {
     // ---- host-side checks, before any CUDA call
     Problem pr = make_problem(cu_seqlens_q_host, seqused_k_host, num_seqs, num_q_heads,
                               num_kv_heads, head_size, block_size, block_table_stride, causal);
     int v = validate_problem(pr);
     if (v) return static_cast<ua_status>(v);
-    if (!std::isfinite(softmax_scale)) return UA_ERR_INVALID_ARG;
+    if (!std::isfinite(softmax_scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+        return UA_ERR_INVALID_ARG;
+    if (kv_fp8 && head_size != 128) return UA_ERR_UNSUPPORTED;
     if (num_seqs == 0) return UA_OK;
     const int64_t total_q = cu_seqlens_q_host[num_seqs];
     if (total_q == 0) return UA_OK;
@@ -426,7 +453,8 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
     // ---- partition pass
     thread_local Plan plan;
     thread_local std::vector<uint8_t> blob;
-    build_plan(pr, ds->sms, kPrefillEnabled, plan);
+    // an fp8 cache is read by the decode kernel only
+    build_plan(pr, ds->sms, kPrefillEnabled && !kv_fp8, plan);
     const Layout &L = plan.layout;
     if (L.total_bytes > 0) {
         if (!workspace || workspace_bytes < L.total_bytes || !aligned(workspace, kAlign))
@@ -437,8 +465,9 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
     // ---- tensor maps: K/V page views (5-D), Q as [total_q, Hq, D]
     const int g = num_q_heads / num_kv_heads;
     CUtensorMap tm_kp, tm_vp, tm_q, tm_o, tm_k3;
-    if (!encode_page_map(&tm_kp, k_cache, head_size, num_kv_heads, (uint64_t)num_blocks) ||
-        !encode_page_map(&tm_vp, v_cache, head_size, num_kv_heads, (uint64_t)num_blocks))
+    const int eb = kv_fp8 ? 1 : 2;
+    if (!encode_page_map(&tm_kp, k_cache, head_size, num_kv_heads, (uint64_t)num_blocks, eb) ||
+        !encode_page_map(&tm_vp, v_cache, head_size, num_kv_heads, (uint64_t)num_blocks, eb))
         return UA_ERR_CUDA;
     // prefill: Q tiles (loads) and out tiles (stores) as [total_q, Hq, D], and K as
     // [num_blocks * 16, Hkv, D] with one box per 64 columns
@@ -464,7 +493,7 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
     auto mark = [&](int i) {
         if (prof) cudaEventRecord(ds->ev[pslot][i], stream);
     };
-    const float scale_log2 = softmax_scale * 1.4426950408889634f;
+    const float scale_log2 = softmax_scale * k_scale * 1.4426950408889634f;
 
     mark(0);
     // Once the plan copy is issued, every way out of this call records the
@@ -513,8 +542,9 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
         dp.comb = reinterpret_cast<const CombUnit *>(pl + L.off_comb);
         dp.comb_count = reinterpret_cast<int32_t *>(pl + L.off_comb_count);
         dp.lse = lse;
+        dp.v_scale = v_scale;
         dp.status = ds->status;
-        e = launch_decode(head_size, dp, tm_kp, tm_vp, plan.dec_ctas, stream);
+        e = launch_decode(head_size, kv_fp8 != 0, dp, tm_kp, tm_vp, plan.dec_ctas, stream);
         if (e != cudaSuccess) return UA_ERR_CUDA;
     }
     mark(2);
@@ -660,4 +690,18 @@ extern "C" ua_status unified_attention_append(
                              causal, out, cu_seqlens_q_host, seqused_k_host, num_seqs, num_q_heads,
                              num_kv_heads, head_size, block_size, num_blocks, block_table_stride,
                              workspace, workspace_bytes, stream);
+}
+
+extern "C" ua_status unified_attention_fp8kv(
+    const void *q, const void *k_cache, const void *v_cache, float k_scale, float v_scale,
+    const int32_t *cu_seqlens_q, const int32_t *seqused_k, const int32_t *block_table,
+    float softmax_scale, int32_t causal, void *out, float *lse, const int32_t *cu_seqlens_q_host,
+    const int32_t *seqused_k_host, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_size, int32_t block_size, int32_t num_blocks, int32_t block_table_stride,
+    void *workspace, size_t workspace_bytes, void *stream) {
+    return ua::run_attention(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table,
+                             softmax_scale, causal, out, cu_seqlens_q_host, seqused_k_host,
+                             num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                             num_blocks, block_table_stride, workspace, workspace_bytes, stream,
+                             /*pinned_plan=*/true, lse, /*kv_fp8=*/1, k_scale, v_scale);
 }

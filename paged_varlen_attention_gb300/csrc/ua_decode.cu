@@ -34,13 +34,18 @@
 
 namespace ua {
 
-template <int D>
+// KV8: the cache holds e4m3 bytes (per-tensor scales); each consumer warp
+// converts its page to f16 in a scratch laid out like a bf16 page (so the
+// fragment loads are the same) and the MMAs run on f16 operands.
+template <int D, bool KV8>
 struct DecCfg {
     static constexpr int kChunks = D / 64;                        // 64-column TMA boxes per row
-    static constexpr int kPageBytes = kBlockSize * D * 2;        // one page, one kv head, K or V
+    static constexpr int kPageBytes = kBlockSize * D * (KV8 ? 1 : 2);   // one page, one kv head, K or V
     static constexpr int kStageBytes = 2 * kPageBytes;           // K + V
     static constexpr int kStages = (D == 128) ? 8 : 16;
     static constexpr int kConsumerWarps = 4;
+    static constexpr int kF16PageBytes = kBlockSize * D * 2;     // a converted page
+    static constexpr int kScratchBytes = KV8 ? kConsumerWarps * 2 * kF16PageBytes : 0;
     static constexpr int kThreads = (kConsumerWarps + 1) * 32;
     static constexpr int kMergeFloats = kDecRows * D + 2 * kDecRows;   // per warp
     // ring of piece descriptors + Q tiles, filled by the producer ahead of use
@@ -48,8 +53,8 @@ struct DecCfg {
     static constexpr int kQTileBytes = kDecRows * D * 2;
     static constexpr int kDescInts = 16;
     static constexpr size_t kMergeBytes = (size_t)kConsumerWarps * kMergeFloats * 4;
-    static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kMergeBytes +
-                                         (size_t)kRing * (kQTileBytes + kDescInts * 4) +
+    static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kScratchBytes +
+                                         kMergeBytes + (size_t)kRing * (kQTileBytes + kDescInts * 4) +
                                          (2 * kStages + 2 * kRing) * 8;
 };
 
@@ -87,7 +92,7 @@ __device__ __forceinline__ void merge_unit(const DecodeParams &p, int q0, int kv
                 acc.w += w * ov.w;
             }
         }
-        const float inv = W > 0.f ? 1.f / W : 0.f;
+        const float inv = W > 0.f ? p.v_scale / W : 0.f;
         const int pr = row0 + row;
         const int64_t t = (int64_t)q0 + pr / p.g;
         const int h = kvh * p.g + pr % p.g;
@@ -99,16 +104,17 @@ __device__ __forceinline__ void merge_unit(const DecodeParams &p, int q0, int kv
     }
 }
 
-template <int D>
-__global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
+template <int D, bool KV8>
+__global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, 2)
     ua_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v) {
-    using C = DecCfg<D>;
+    using C = DecCfg<D, KV8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *stages = smem;
-    float *merge = reinterpret_cast<float *>(smem + (size_t)C::kStages * C::kStageBytes);
+    uint8_t *scratch = smem + (size_t)C::kStages * C::kStageBytes;   // KV8: [warp][K, V] f16 pages
+    float *merge = reinterpret_cast<float *>(scratch + C::kScratchBytes);
     uint8_t *qring = reinterpret_cast<uint8_t *>(merge) + C::kMergeBytes;       // [kRing][16][D] bf16
     int *dring = reinterpret_cast<int *>(qring + C::kRing * C::kQTileBytes);   // [kRing][kDescInts]
     uint64_t *bars = reinterpret_cast<uint64_t *>(dring + C::kRing * C::kDescInts);
@@ -297,6 +303,7 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
                     qa[ks][ri] = r < pc.nrows
                                      ? *reinterpret_cast<const uint32_t *>(qtile + (r * D + col) * 2)
                                      : 0u;
+                    if (KV8) qa[ks][ri] = bf16x2_to_f16x2(qa[ks][ri]);
                 }
 
             float o[D / 8][4];
@@ -315,8 +322,42 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
                     ok = false;
                     break;
                 }
-                const uint32_t kb = stage0 + st * C::kStageBytes;
-                const uint32_t vb = kb + C::kPageBytes;
+                uint32_t kb = stage0 + st * C::kStageBytes;
+                uint32_t vb = kb + C::kPageBytes;
+                if (KV8) {
+                    // e4m3 page (16 rows x D bytes, 128-byte swizzle) -> f16 page in this
+                    // warp's scratch ([chunk][row][64], 128-byte swizzle), K then V; the
+                    // stage is free once both are converted
+                    uint8_t *wk = scratch + w * 2 * C::kF16PageBytes;
+                    __syncwarp();   // the previous page's fragment loads are done
+#pragma unroll 1
+                    for (int kv = 0; kv < 2; ++kv) {
+                        const uint8_t *src = stages + (size_t)st * C::kStageBytes + kv * C::kPageBytes;
+                        uint8_t *dst = wk + kv * C::kF16PageBytes;
+#pragma unroll 1
+                        for (int u = 0; u < (kBlockSize * D / 16) / 32; ++u) {
+                            const int idx = lane + 32 * u;
+                            const int r = idx / (D / 16), j = idx % (D / 16);
+                            const uint4 raw = *reinterpret_cast<const uint4 *>(src + r * D + ((j ^ (r & 7)) << 4));
+                            const int c = j >> 2, p0 = (j & 3) * 2;
+                            uint8_t *row = dst + c * 2048 + r * 128;
+                            *reinterpret_cast<uint4 *>(row + ((p0 ^ (r & 7)) << 4)) =
+                                make_uint4(e4m3x2_to_f16x2((uint16_t)(raw.x & 0xffffu)),
+                                           e4m3x2_to_f16x2((uint16_t)(raw.x >> 16)),
+                                           e4m3x2_to_f16x2((uint16_t)(raw.y & 0xffffu)),
+                                           e4m3x2_to_f16x2((uint16_t)(raw.y >> 16)));
+                            *reinterpret_cast<uint4 *>(row + (((p0 + 1) ^ (r & 7)) << 4)) =
+                                make_uint4(e4m3x2_to_f16x2((uint16_t)(raw.z & 0xffffu)),
+                                           e4m3x2_to_f16x2((uint16_t)(raw.z >> 16)),
+                                           e4m3x2_to_f16x2((uint16_t)(raw.w & 0xffffu)),
+                                           e4m3x2_to_f16x2((uint16_t)(raw.w >> 16)));
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(empty0 + 8 * st);
+                    kb = smem_u32(wk);
+                    vb = kb + C::kF16PageBytes;
+                }
                 const int key0 = (pc.page_begin + k) * kBlockSize;
 
                 // S = Q K^T for 16 rows x 16 keys
@@ -332,8 +373,13 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
                     const int r = ((lane >> 4) << 3) + (lane & 7);
                     uint32_t b0, b1, b2, b3;
                     ldmatrix_x4(kb + c * 2048 + r * 128 + ((ch ^ (r & 7)) << 4), b0, b1, b2, b3);
-                    mma_bf16_16816(s[0], qa[ks], b0, b1);
-                    mma_bf16_16816(s[1], qa[ks], b2, b3);
+                    if (KV8) {
+                        mma_f16_16816(s[0], qa[ks], b0, b1);
+                        mma_f16_16816(s[1], qa[ks], b2, b3);
+                    } else {
+                        mma_bf16_16816(s[0], qa[ks], b0, b1);
+                        mma_bf16_16816(s[1], qa[ks], b2, b3);
+                    }
                 }
                 // scale into the log2 domain and mask
                 float mx[2] = {-INFINITY, -INFINITY};
@@ -372,10 +418,17 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
                         l[e >> 1] += pv;
                     }
                 uint32_t pa[4];
-                pa[0] = pack_bf16x2(s[0][0], s[0][1]);
-                pa[1] = pack_bf16x2(s[0][2], s[0][3]);
-                pa[2] = pack_bf16x2(s[1][0], s[1][1]);
-                pa[3] = pack_bf16x2(s[1][2], s[1][3]);
+                if (KV8) {
+                    pa[0] = pack_f16x2(s[0][0], s[0][1]);
+                    pa[1] = pack_f16x2(s[0][2], s[0][3]);
+                    pa[2] = pack_f16x2(s[1][0], s[1][1]);
+                    pa[3] = pack_f16x2(s[1][2], s[1][3]);
+                } else {
+                    pa[0] = pack_bf16x2(s[0][0], s[0][1]);
+                    pa[1] = pack_bf16x2(s[0][2], s[0][3]);
+                    pa[2] = pack_bf16x2(s[1][0], s[1][1]);
+                    pa[3] = pack_bf16x2(s[1][2], s[1][3]);
+                }
                 // V rows past the context (last page) may hold anything, NaN
                 // included: zero them so 0 * NaN never reaches O.
                 uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
@@ -391,11 +444,16 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
                     const int r = ((lane >> 3) & 1) * 8 + (lane & 7);
                     uint32_t v0, v1, v2, v3;
                     ldmatrix_x4_trans(vb + c * 2048 + r * 128 + ((ch ^ (r & 7)) << 4), v0, v1, v2, v3);
-                    mma_bf16_16816(o[2 * np], pa, v0 & vm0, v1 & vm1);
-                    mma_bf16_16816(o[2 * np + 1], pa, v2 & vm0, v3 & vm1);
+                    if (KV8) {
+                        mma_f16_16816(o[2 * np], pa, v0 & vm0, v1 & vm1);
+                        mma_f16_16816(o[2 * np + 1], pa, v2 & vm0, v3 & vm1);
+                    } else {
+                        mma_bf16_16816(o[2 * np], pa, v0 & vm0, v1 & vm1);
+                        mma_bf16_16816(o[2 * np + 1], pa, v2 & vm0, v3 & vm1);
+                    }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(empty0 + 8 * st);
+                if (!KV8 && lane == 0) mbar_arrive(empty0 + 8 * st);
             }
             gbase += npages;
 
@@ -448,7 +506,7 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
                     }
                 }
                 if (pc.slot < 0) {
-                    const float inv = L > 0.f ? 1.f / L : 0.f;
+                    const float inv = L > 0.f ? p.v_scale / L : 0.f;
                     const int pr = pc.row0 + row;
                     const int64_t t = (int64_t)q0 + pr / p.g;
                     const int h = pc.kvh * p.g + pr % p.g;
@@ -490,28 +548,32 @@ __global__ void __launch_bounds__(DecCfg<D>::kThreads, 2)
     }
 }
 
-template <int D>
+template <int D, bool KV8>
 static cudaError_t launch_decode_t(const DecodeParams &p, const CUtensorMap &tm_k,
                                    const CUtensorMap &tm_v, int ctas, cudaStream_t stream) {
-    using C = DecCfg<D>;
+    using C = DecCfg<D, KV8>;
     static thread_local int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(ua_decode_kernel<D>,
+        cudaError_t e = cudaFuncSetAttribute(ua_decode_kernel<D, KV8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    ua_decode_kernel<D><<<ctas, C::kThreads, C::kSmemBytes, stream>>>(p, tm_k, tm_v);
+    ua_decode_kernel<D, KV8><<<ctas, C::kThreads, C::kSmemBytes, stream>>>(p, tm_k, tm_v);
     return cudaGetLastError();
 }
 
-cudaError_t launch_decode(int d, const DecodeParams &p, const CUtensorMap &tm_k,
+cudaError_t launch_decode(int d, bool kv8, const DecodeParams &p, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, int ctas, cudaStream_t stream) {
-    return d == 64 ? launch_decode_t<64>(p, tm_k, tm_v, ctas, stream)
-                   : launch_decode_t<128>(p, tm_k, tm_v, ctas, stream);
+    if (kv8) {
+        if (d != 128) return cudaErrorInvalidValue;
+        return launch_decode_t<128, true>(p, tm_k, tm_v, ctas, stream);
+    }
+    return d == 64 ? launch_decode_t<64, false>(p, tm_k, tm_v, ctas, stream)
+                   : launch_decode_t<128, false>(p, tm_k, tm_v, ctas, stream);
 }
 
 }  // namespace ua

@@ -30,6 +30,7 @@ struct DecodeParams {
     const CombUnit *comb;        // plan: split units
     int32_t *comb_count;         // plan: partials written per split unit (zero at launch)
     float *lse;                  // optional [total_q, Hq]: natural-log normaliser per row
+    float v_scale;               // scale of the V values (fp8 cache; 1 otherwise)
     int *status;                 // device status word
 };
 
@@ -54,7 +55,7 @@ struct PrefillParams {
 };
 
 // Each returns the launch error (cudaSuccess when the launch was queued).
-cudaError_t launch_decode(int d, const DecodeParams &p, const CUtensorMap &tm_k,
+cudaError_t launch_decode(int d, bool kv8, const DecodeParams &p, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, int ctas, cudaStream_t stream);
 cudaError_t launch_prefill(int d, const PrefillParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_o,
                            const CUtensorMap &tm_k, const CUtensorMap &tm_v, int ctas,
@@ -65,6 +66,8 @@ cudaError_t launch_prefill(int d, const PrefillParams &p, const CUtensorMap &tm_
 // page-locked ring (allocated on first use) rather than copy it from pageable
 // memory; the entry point that must allocate nothing passes false.  lse:
 // optional fp32 [total_q, Hq] output of the natural-log normaliser per row.
+// kv_fp8: the caches hold e4m3 bytes, k = k_scale * code and v = v_scale *
+// code (every row then runs in the decode kernel; D = 128 only).
 ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
                         const int32_t *cu_seqlens_q, const int32_t *seqused_k,
                         const int32_t *block_table, float softmax_scale, int32_t causal, void *out,
@@ -72,7 +75,8 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
                         int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                         int32_t head_size, int32_t block_size, int32_t num_blocks,
                         int32_t block_table_stride, void *workspace, size_t workspace_bytes,
-                        void *stream, bool pinned_plan, float *lse);
+                        void *stream, bool pinned_plan, float *lse, int kv_fp8 = 0,
+                        float k_scale = 1.f, float v_scale = 1.f);
 
 // Writes the new tokens' K / V rows ([total_q, Hkv, D] bf16) into their
 // pages: token i of sequence s to position seqused_k[s] - Lq + i.

@@ -230,3 +230,17 @@ def custom_spec(q_lens: Sequence[int], k_lens: Sequence[int], num_q_heads: int, 
     return Spec(name, q_lens, k_lens, num_q_heads, num_kv_heads, head_size, block_size=block_size,
                 causal=causal, softmax_scale=softmax_scale, pool_blocks=pool_blocks,
                 data_seed=10_000 + seed, layout_seed=20_000 + seed)
+
+
+def fp8_caches(batch, k_scale=0.05, v_scale=0.05):
+    """E4M3 byte copies of a batch's caches: byte = e4m3(value / scale), rounded to
+    nearest by torch's float8_e4m3fn conversion (input generation only; the
+    attention paths decode the bytes themselves).  NaN-poisoned slots stay NaN."""
+    import torch
+
+    def q8(bits, scale):
+        f = (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+        t = torch.from_numpy(np.ascontiguousarray(f / np.float32(scale)))
+        return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+    return q8(batch.k_cache, k_scale), q8(batch.v_cache, v_scale)

@@ -361,3 +361,39 @@ def test_kv_append_then_attention_equals_dense_attention():
     got, _ = oracle.attention_batch(appended)
     ref = sdpa_reference(q, ks, vs, q_lens, hq, True, full.spec.softmax_scale)
     np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_e4m3_decoding_matches_torch_for_every_code():
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_to_f64(c) for c in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_fp8_kv_attention_matches_sdpa_on_dequantized_keys(causal):
+    """Attention over an E4M3 cache with per-tensor scales equals torch fp64 SDPA
+    over the dense dequantized keys / values (k = k_scale * e4m3(byte))."""
+    q_lens, k_lens, hq, hk, d = [1, 4, 2], [37, 20, 2], 4, 2, 32
+    q, ks, vs, _ = random_dense(q_lens, k_lens, hq, hk, d, seed=48)
+    b = batch_from_dense(q, ks, vs, q_lens, hq, causal=causal, poison=True)
+    k8, v8 = W.fp8_caches(b, 0.07, 0.11)
+    out, lse = oracle.attention_fp8kv(b.q, k8, v8, 0.07, 0.11, b.cu_seqlens_q, b.seqused_k,
+                                      b.block_table, b.spec.softmax_scale, causal)
+    deq = lambda c, sc: sc * torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.float64).numpy()  # noqa: E731
+    kd, vd = deq(k8, 0.07), deq(v8, 0.11)
+    t0 = 0
+    for s, (lq, lk) in enumerate(zip(q_lens, k_lens)):
+        rows = [b.block_table[s, j // 16] * 16 + j % 16 for j in range(lk)]
+        kk = torch.from_numpy(kd.reshape(-1, hk, d)[rows]).permute(1, 0, 2)[None]
+        vv = torch.from_numpy(vd.reshape(-1, hk, d)[rows]).permute(1, 0, 2)[None]
+        qq = torch.from_numpy(widen(q[t0:t0 + lq])).permute(1, 0, 2)[None]
+        mask = torch.ones(lq, lk, dtype=torch.bool)
+        if causal:
+            mask = torch.tril(mask, diagonal=lk - lq)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qq, kk, vv, attn_mask=mask, scale=b.spec.softmax_scale, enable_gqa=True)
+        np.testing.assert_allclose(out[t0:t0 + lq], ref[0].permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+        t0 += lq
