@@ -187,6 +187,13 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
+// L2 fill width for boxes whose rows hold `run` contiguous useful bytes: a
+// 256-byte fill over a 128-byte run drags in bytes that another CTA reads much
+// later (the next KV head's row), which costs DRAM bandwidth, not hits.
+static CUtensorMapL2promotion l2_fill(uint64_t run) {
+    return run >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
+}
+
 // 3-D bf16 map over a [outer, mid, inner] tensor with 128-byte swizzled boxes
 // of {64, box_mid, box_outer} elements.  Out-of-range boxes read zeros.
 static bool encode_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t mid,
@@ -197,10 +204,12 @@ static bool encode_map(CUtensorMap *map, const void *base, uint64_t inner, uint6
     cuuint64_t strides[2] = {inner * 2, inner * mid * 2};
     cuuint32_t box[3] = {64, box_mid, box_outer};
     cuuint32_t estr[3] = {1, 1, 1};
+    // a box row's useful run: all of `inner` (the other 64-column boxes of a
+    // row follow), times box_mid when that spans the whole middle extent
+    const uint64_t run = inner * 2 * (box_mid == mid ? mid : box_mid);
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     CU_TENSOR_MAP_SWIZZLE_128B, l2_fill(run), CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -209,22 +218,27 @@ static bool encode_map(CUtensorMap *map, const void *base, uint64_t inner, uint6
 // is one 16-token page of one KV head, laid out [chunk][slot][64] in shared
 // memory with the 128-byte swizzle.  Out-of-range blocks read zeros.
 // eb: bytes per element, 2 (bf16) or 1 (e4m3): a 128-byte chunk is 64 or 128
-// elements, and a page row D * eb bytes.
+// elements, and a page row D * eb bytes.  box_heads: KV heads per box (1, or
+// 2 adjacent heads laid out [head][chunk][slot][128 B]).
 static bool encode_page_map(CUtensorMap *map, const void *base, int d, int hkv,
-                            uint64_t num_blocks, int eb = 2) {
+                            uint64_t num_blocks, int eb = 2, int box_heads = 1) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
     const uint64_t row = (uint64_t)hkv * d * eb;   // bytes between slots
     const cuuint32_t inner = 128 / eb, chunks = (cuuint32_t)(d * eb / 128);
     cuuint64_t dims[5] = {inner, (cuuint64_t)kBlockSize, chunks, (cuuint64_t)hkv, num_blocks};
     cuuint64_t strides[4] = {row, 128, (cuuint64_t)d * eb, row * kBlockSize};
-    cuuint32_t box[5] = {inner, (cuuint32_t)kBlockSize, chunks, 1, 1};
+    cuuint32_t box[5] = {inner, (cuuint32_t)kBlockSize, chunks, (cuuint32_t)box_heads, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    // the box's heads of one slot are the useful run (the whole slot when
+    // they are all Hkv heads); with 128-byte runs (one e4m3 head at D = 128)
+    // a 256-byte fill read 1.38x the algorithmic DRAM bytes
+    const CUtensorMapL2promotion promo =
+        l2_fill(hkv == box_heads ? row * kBlockSize : (uint64_t)d * eb * box_heads);
     CUresult r = enc(map, eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 5,
                      const_cast<void *>(base), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     CU_TENSOR_MAP_SWIZZLE_128B, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -293,6 +307,7 @@ extern "C" ua_status ua_workspace_size_fp8kv(const int32_t *cu_seqlens_q_host,
     if (!bytes) return UA_ERR_INVALID_ARG;
     Problem pr = make_problem(cu_seqlens_q_host, seqused_k_host, num_seqs, num_q_heads,
                               num_kv_heads, head_size, block_size, block_table_stride, causal);
+    pr.kv_heads_per_unit = 2;
     int v = validate_problem(pr);
     if (v) return static_cast<ua_status>(v);
     if (head_size != 128) return UA_ERR_UNSUPPORTED;
@@ -428,6 +443,8 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
     // ---- host-side checks, before any CUDA call
     Problem pr = make_problem(cu_seqlens_q_host, seqused_k_host, num_seqs, num_q_heads,
                               num_kv_heads, head_size, block_size, block_table_stride, causal);
+    // e4m3 pages: decode units take two adjacent kv heads (256-byte rows per slot)
+    if (kv_fp8) pr.kv_heads_per_unit = 2;
     int v = validate_problem(pr);
     if (v) return static_cast<ua_status>(v);
     if (!std::isfinite(softmax_scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
@@ -466,8 +483,11 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
     const int g = num_q_heads / num_kv_heads;
     CUtensorMap tm_kp, tm_vp, tm_q, tm_o, tm_k3;
     const int eb = kv_fp8 ? 1 : 2;
-    if (!encode_page_map(&tm_kp, k_cache, head_size, num_kv_heads, (uint64_t)num_blocks, eb) ||
-        !encode_page_map(&tm_vp, v_cache, head_size, num_kv_heads, (uint64_t)num_blocks, eb))
+    const int box_heads = plan.dec_heads_per_unit;   // 2 only for e4m3 pages (no prefill tiles)
+    if (!encode_page_map(&tm_kp, k_cache, head_size, num_kv_heads, (uint64_t)num_blocks, eb,
+                         box_heads) ||
+        !encode_page_map(&tm_vp, v_cache, head_size, num_kv_heads, (uint64_t)num_blocks, eb,
+                         box_heads))
         return UA_ERR_CUDA;
     // prefill: Q tiles (loads) and out tiles (stores) as [total_q, Hq, D], and K as
     // [num_blocks * 16, Hkv, D] with one box per 64 columns
@@ -543,6 +563,7 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
         dp.comb_count = reinterpret_cast<int32_t *>(pl + L.off_comb_count);
         dp.lse = lse;
         dp.v_scale = v_scale;
+        dp.heads_per_unit = plan.dec_heads_per_unit;
         dp.status = ds->status;
         e = launch_decode(head_size, kv_fp8 != 0, dp, tm_kp, tm_vp, plan.dec_ctas, stream);
         if (e != cudaSuccess) return UA_ERR_CUDA;

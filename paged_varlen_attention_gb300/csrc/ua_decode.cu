@@ -34,18 +34,26 @@
 
 namespace ua {
 
-// KV8: the cache holds e4m3 bytes (per-tensor scales); each consumer warp
-// converts its page to f16 in a scratch laid out like a bf16 page (so the
-// fragment loads are the same) and the MMAs run on f16 operands.
+// KV8: the cache holds e4m3 bytes (per-tensor scales).  Each consumer
+// thread reads its MMA fragments' bytes straight from the stage (16-byte
+// loads), widens them to f16 in registers, and the MMAs run on f16 operands.
+// The contraction index d of Q K^T is permuted so that a thread's K bytes
+// are contiguous (Q is read with the same permutation), and the output
+// column of P V is permuted so that its V bytes are (undone when the four
+// warps' results are merged).  A unit may hold two adjacent kv heads
+// (heads_per_unit = 2): one TMA box then brings both heads' 128-byte rows of
+// a slot, a 256-byte run of the cache, and the 16-row tile holds head kvh in
+// rows 0-7 and head kvh + 1 in rows 8-15; S and P V run once per head, each
+// keeping the rows of its own head.  D = 128 only.
 template <int D, bool KV8>
 struct DecCfg {
+    static_assert(!KV8 || D == 128, "the e4m3 path is laid out for D = 128");
     static constexpr int kChunks = D / 64;                        // 64-column TMA boxes per row
-    static constexpr int kPageBytes = kBlockSize * D * (KV8 ? 1 : 2);   // one page, one kv head, K or V
+    static constexpr int kHeadPageBytes = kBlockSize * D * (KV8 ? 1 : 2);   // one page of one kv head
+    static constexpr int kPageBytes = (KV8 ? 2 : 1) * kHeadPageBytes;      // K (or V) part of a stage
     static constexpr int kStageBytes = 2 * kPageBytes;           // K + V
-    static constexpr int kStages = (D == 128) ? 8 : 16;
+    static constexpr int kStages = (D == 128) ? 8 : 16;          // 64 KB of stages
     static constexpr int kConsumerWarps = 4;
-    static constexpr int kF16PageBytes = kBlockSize * D * 2;     // a converted page
-    static constexpr int kScratchBytes = KV8 ? kConsumerWarps * 2 * kF16PageBytes : 0;
     static constexpr int kThreads = (kConsumerWarps + 1) * 32;
     static constexpr int kMergeFloats = kDecRows * D + 2 * kDecRows;   // per warp
     // ring of piece descriptors + Q tiles, filled by the producer ahead of use
@@ -53,7 +61,7 @@ struct DecCfg {
     static constexpr int kQTileBytes = kDecRows * D * 2;
     static constexpr int kDescInts = 16;
     static constexpr size_t kMergeBytes = (size_t)kConsumerWarps * kMergeFloats * 4;
-    static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kScratchBytes +
+    static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes +
                                          kMergeBytes + (size_t)kRing * (kQTileBytes + kDescInts * 4) +
                                          (2 * kStages + 2 * kRing) * 8;
 };
@@ -63,6 +71,76 @@ enum : int {
     kDq0 = 0, kDlq, kDlk, kDkvh, kDrow0, kDnrows, kDpb, kDpe, kDslot, kDcomb, kDslot0, kDnslots
 };
 
+// e4m3 pages (D = 128): S += Q K^T for one 16-key page of one kv head at
+// shared address kb ([slot][128 B], 128-byte swizzle: 16-byte chunk j of
+// slot r sits at j ^ (r % 8)).  Thread (n = lane / 4, t = lane % 4) reads
+// key rows n and 8 + n, chunks 2t and 2t + 1; word w of chunk 2t + h holds
+// the bytes of k-step 4h + w (Q's fragments follow the same permutation).
+__device__ __forceinline__ void kv8_qk(float (&s)[2][4], const uint32_t (&qa)[8][4], uint32_t kb,
+                                       int lane) {
+    const int qr = lane >> 2;
+    uint32_t kr[2][2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = nt * 8 + qr;
+            const uint4 v = lds128(kb + r * 128 + (((2 * (lane & 3) + h) ^ qr) << 4));
+            kr[nt][h][0] = v.x;
+            kr[nt][h][1] = v.y;
+            kr[nt][h][2] = v.z;
+            kr[nt][h][3] = v.w;
+        }
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const uint32_t wd = kr[nt][ks >> 2][ks & 3];
+            mma_f16_16816(s[nt], qa[ks], e4m3x2_to_f16x2((uint16_t)(wd & 0xffffu)),
+                          e4m3x2_to_f16x2((uint16_t)(wd >> 16)));
+        }
+}
+
+// e4m3 pages (D = 128): O += P V for one page of one kv head at vb.  Thread
+// (n, t) reads chunk n of value rows 2t, 2t+1, 2t+8, 2t+9: byte b of word w
+// is d = 16n + 4w + b, i.e. output column n of n-tile 4w + b; the byte pairs
+// of rows (2t, 2t+1) and (2t+8, 2t+9) interleave into the two B registers.
+// vm0 / vm1 zero the keys past the context.
+__device__ __forceinline__ void kv8_pv(float (&o)[16][4], const uint32_t (&pa)[4], uint32_t vb,
+                                       int lane, uint32_t vm0, uint32_t vm1) {
+    const int qr = lane >> 2;
+    uint32_t vr[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = 2 * (lane & 3) + (i & 1) + (i >> 1) * 8;
+        const uint4 v = lds128(vb + r * 128 + ((qr ^ (r & 7)) << 4));
+        vr[i][0] = v.x;
+        vr[i][1] = v.y;
+        vr[i][2] = v.z;
+        vr[i][3] = v.w;
+    }
+#pragma unroll
+    for (int wd = 0; wd < 4; ++wd) {
+        const uint32_t lo0 = __byte_perm(vr[0][wd], vr[1][wd], 0x5140);
+        const uint32_t hi0 = __byte_perm(vr[0][wd], vr[1][wd], 0x7362);
+        const uint32_t lo1 = __byte_perm(vr[2][wd], vr[3][wd], 0x5140);
+        const uint32_t hi1 = __byte_perm(vr[2][wd], vr[3][wd], 0x7362);
+        mma_f16_16816(o[4 * wd], pa, e4m3x2_to_f16x2((uint16_t)(lo0 & 0xffffu)) & vm0,
+                      e4m3x2_to_f16x2((uint16_t)(lo1 & 0xffffu)) & vm1);
+        mma_f16_16816(o[4 * wd + 1], pa, e4m3x2_to_f16x2((uint16_t)(lo0 >> 16)) & vm0,
+                      e4m3x2_to_f16x2((uint16_t)(lo1 >> 16)) & vm1);
+        mma_f16_16816(o[4 * wd + 2], pa, e4m3x2_to_f16x2((uint16_t)(hi0 & 0xffffu)) & vm0,
+                      e4m3x2_to_f16x2((uint16_t)(hi1 & 0xffffu)) & vm1);
+        mma_f16_16816(o[4 * wd + 3], pa, e4m3x2_to_f16x2((uint16_t)(hi0 >> 16)) & vm0,
+                      e4m3x2_to_f16x2((uint16_t)(hi1 >> 16)) & vm1);
+    }
+}
+
+// Tile row r of a unit with hp kv heads: its head offset and its packed row
+// index within that head.
+__device__ __forceinline__ int tile_row_head(int r, int hp) { return hp == 2 ? r >> 3 : 0; }
+__device__ __forceinline__ int tile_row_idx(int r, int hp) { return hp == 2 ? r & 7 : r; }
+
 // Merge of the partials of split unit u (log2 domain) by the 128 consumer
 // threads of the CTA that wrote the unit's last partial.  Partial s holds
 // O_s = sum_j 2^(x_j - m_s) v_j, its max m_s and l_s = sum_j 2^(x_j - m_s):
@@ -70,10 +148,12 @@ enum : int {
 // The partials of other CTAs are read through L2 (ld.global.cg).
 template <int D>
 __device__ __forceinline__ void merge_unit(const DecodeParams &p, int q0, int kvh, int row0, int nrows,
-                                           int slot0, int nslots, int tid, int nthreads) {
-    for (int gi = tid; gi < nrows * (D / 4); gi += nthreads) {
+                                           int hp, int slot0, int nslots, int tid, int nthreads) {
+    const int tile_rows = hp == 2 ? kDecRows : nrows;
+    for (int gi = tid; gi < tile_rows * (D / 4); gi += nthreads) {
         const int row = gi / (D / 4);
         const int col = (gi % (D / 4)) * 4;
+        if (tile_row_idx(row, hp) >= nrows) continue;
         float M = -INFINITY;
         for (int s = 0; s < nslots; ++s)
             M = fmaxf(M, __ldcg(p.part_ml + 2 * ((int64_t)(slot0 + s) * kDecRows + row)));
@@ -93,9 +173,9 @@ __device__ __forceinline__ void merge_unit(const DecodeParams &p, int q0, int kv
             }
         }
         const float inv = W > 0.f ? p.v_scale / W : 0.f;
-        const int pr = row0 + row;
+        const int pr = row0 + tile_row_idx(row, hp);
         const int64_t t = (int64_t)q0 + pr / p.g;
-        const int h = kvh * p.g + pr % p.g;
+        const int h = (kvh + tile_row_head(row, hp)) * p.g + pr % p.g;
         if (p.lse != nullptr && col == 0) p.lse[t * p.hq + h] = row_lse(M, W);
         uint2 packed;
         packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
@@ -113,8 +193,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, 2)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *stages = smem;
-    uint8_t *scratch = smem + (size_t)C::kStages * C::kStageBytes;   // KV8: [warp][K, V] f16 pages
-    float *merge = reinterpret_cast<float *>(scratch + C::kScratchBytes);
+    float *merge = reinterpret_cast<float *>(smem + (size_t)C::kStages * C::kStageBytes);
     uint8_t *qring = reinterpret_cast<uint8_t *>(merge) + C::kMergeBytes;       // [kRing][16][D] bf16
     int *dring = reinterpret_cast<int *>(qring + C::kRing * C::kQTileBytes);   // [kRing][kDescInts]
     uint64_t *bars = reinterpret_cast<uint64_t *>(dring + C::kRing * C::kDescInts);
@@ -152,6 +231,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, 2)
             prefetch_tensormap(&tm_v);
         }
         const uint64_t policy = l2_policy_evict_first();
+        const int hp = KV8 ? p.heads_per_unit : 1;   // kv heads per unit (and per box)
         bool ok = true;
         uint32_t filled = 0;   // ring entries filled
         DecPiece nxt{};
@@ -188,17 +268,19 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, 2)
                         d[kDnslots] = cu.nslots;
                     }
                     const uint32_t pb = pfull0 + 8 * slot;
-                    mbar_arrive_expect_tx(pb, (uint32_t)pc.nrows * D * 2);
-                    for (int r = 0; r < pc.nrows;) {
-                        const int pr = pc.row0 + r;
-                        const int h0 = pr % p.g;
-                        const int cnt = min(p.g - h0, pc.nrows - r);
-                        const __nv_bfloat16 *src =
-                            p.q + ((int64_t)(q0 + pr / p.g) * p.hq + pc.kvh * p.g + h0) * D;
-                        bulk_load(qring0 + slot * C::kQTileBytes + r * D * 2, src,
-                                  (uint32_t)cnt * D * 2, pb);
-                        r += cnt;
-                    }
+                    mbar_arrive_expect_tx(pb, (uint32_t)(pc.nrows * hp) * D * 2);
+                    // head kvh + j's rows go to tile rows 8j + r (hp = 2) or r
+                    for (int j = 0; j < hp; ++j)
+                        for (int r = 0; r < pc.nrows;) {
+                            const int pr = pc.row0 + r;
+                            const int h0 = pr % p.g;
+                            const int cnt = min(p.g - h0, pc.nrows - r);
+                            const __nv_bfloat16 *src =
+                                p.q + ((int64_t)(q0 + pr / p.g) * p.hq + (pc.kvh + j) * p.g + h0) * D;
+                            bulk_load(qring0 + slot * C::kQTileBytes + (8 * j + r) * D * 2, src,
+                                      (uint32_t)cnt * D * 2, pb);
+                            r += cnt;
+                        }
                     ++filled;
                 }
             }
@@ -227,7 +309,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, 2)
                             const uint32_t fb = full0 + 8 * st;
                             const uint32_t kdst = stage0 + st * C::kStageBytes;
                             const uint32_t vdst = kdst + C::kPageBytes;
-                            mbar_arrive_expect_tx(fb, C::kStageBytes);
+                            mbar_arrive_expect_tx(fb, 2u * hp * C::kHeadPageBytes);
                             // one box per page and tensor: all D columns of 16 tokens,
                             // laid out [chunk][slot][64] with the 128-byte swizzle
                             tma_load_5d_hint(kdst, &tm_k, 0, 0, 0, pc.kvh, b, fb, policy);
@@ -254,6 +336,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, 2)
         float *mrg_l = mrg_m + kDecRows;
         uint32_t gbase = 0;
         bool ok = true;
+        const int hp = KV8 ? p.heads_per_unit : 1;   // kv heads per unit
         // Every consumer warp walks every piece (the merges use a named barrier),
         // even after a failed wait: a piece it could not get counts as empty.
         for (int pi = pbeg; pi < pend; ++pi) {
@@ -288,7 +371,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, 2)
             int kend[2];
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
-                const int r = qr + 8 * rr;
+                const int r = tile_row_idx(qr + 8 * rr, hp);
                 const int i = (pc.row0 + r) / p.g;
                 kend[rr] = (p.causal && r < pc.nrows) ? min(lk, lk - lq + i + 1) : lk;
             }
@@ -299,8 +382,11 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, 2)
 #pragma unroll
                 for (int ri = 0; ri < 4; ++ri) {
                     const int r = qr + (ri & 1) * 8;
-                    const int col = ks * 16 + qc + (ri >> 1) * 8;
-                    qa[ks][ri] = r < pc.nrows
+                    // KV8: logical k (2t, 2t+1 | 2t+8, 2t+9) of k-step ks is
+                    // d = 32t + 16(ks / 4) + 4(ks % 4) + (0, 1 | 2, 3)
+                    const int col = KV8 ? 32 * (lane & 3) + 16 * (ks >> 2) + 4 * (ks & 3) + (ri >> 1) * 2
+                                        : ks * 16 + qc + (ri >> 1) * 8;
+                    qa[ks][ri] = tile_row_idx(r, hp) < pc.nrows
                                      ? *reinterpret_cast<const uint32_t *>(qtile + (r * D + col) * 2)
                                      : 0u;
                     if (KV8) qa[ks][ri] = bf16x2_to_f16x2(qa[ks][ri]);
@@ -322,42 +408,8 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, 2)
                     ok = false;
                     break;
                 }
-                uint32_t kb = stage0 + st * C::kStageBytes;
-                uint32_t vb = kb + C::kPageBytes;
-                if (KV8) {
-                    // e4m3 page (16 rows x D bytes, 128-byte swizzle) -> f16 page in this
-                    // warp's scratch ([chunk][row][64], 128-byte swizzle), K then V; the
-                    // stage is free once both are converted
-                    uint8_t *wk = scratch + w * 2 * C::kF16PageBytes;
-                    __syncwarp();   // the previous page's fragment loads are done
-#pragma unroll 1
-                    for (int kv = 0; kv < 2; ++kv) {
-                        const uint8_t *src = stages + (size_t)st * C::kStageBytes + kv * C::kPageBytes;
-                        uint8_t *dst = wk + kv * C::kF16PageBytes;
-#pragma unroll 1
-                        for (int u = 0; u < (kBlockSize * D / 16) / 32; ++u) {
-                            const int idx = lane + 32 * u;
-                            const int r = idx / (D / 16), j = idx % (D / 16);
-                            const uint4 raw = *reinterpret_cast<const uint4 *>(src + r * D + ((j ^ (r & 7)) << 4));
-                            const int c = j >> 2, p0 = (j & 3) * 2;
-                            uint8_t *row = dst + c * 2048 + r * 128;
-                            *reinterpret_cast<uint4 *>(row + ((p0 ^ (r & 7)) << 4)) =
-                                make_uint4(e4m3x2_to_f16x2((uint16_t)(raw.x & 0xffffu)),
-                                           e4m3x2_to_f16x2((uint16_t)(raw.x >> 16)),
-                                           e4m3x2_to_f16x2((uint16_t)(raw.y & 0xffffu)),
-                                           e4m3x2_to_f16x2((uint16_t)(raw.y >> 16)));
-                            *reinterpret_cast<uint4 *>(row + (((p0 + 1) ^ (r & 7)) << 4)) =
-                                make_uint4(e4m3x2_to_f16x2((uint16_t)(raw.z & 0xffffu)),
-                                           e4m3x2_to_f16x2((uint16_t)(raw.z >> 16)),
-                                           e4m3x2_to_f16x2((uint16_t)(raw.w & 0xffffu)),
-                                           e4m3x2_to_f16x2((uint16_t)(raw.w >> 16)));
-                        }
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(empty0 + 8 * st);
-                    kb = smem_u32(wk);
-                    vb = kb + C::kF16PageBytes;
-                }
+                const uint32_t kb = stage0 + st * C::kStageBytes;
+                const uint32_t vb = kb + C::kPageBytes;
                 const int key0 = (pc.page_begin + k) * kBlockSize;
 
                 // S = Q K^T for 16 rows x 16 keys
@@ -366,17 +418,30 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, 2)
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
+                if constexpr (KV8) {
+                    kv8_qk(s, qa, kb, lane);
+                    if (hp == 2) {
+                        // head kvh + 1 (tile rows 8-15: accumulator entries 2, 3)
+                        float s1[2][4];
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const int c = ks >> 2;
-                    const int ch = (ks & 3) * 2 + ((lane >> 3) & 1);
-                    const int r = ((lane >> 4) << 3) + (lane & 7);
-                    uint32_t b0, b1, b2, b3;
-                    ldmatrix_x4(kb + c * 2048 + r * 128 + ((ch ^ (r & 7)) << 4), b0, b1, b2, b3);
-                    if (KV8) {
-                        mma_f16_16816(s[0], qa[ks], b0, b1);
-                        mma_f16_16816(s[1], qa[ks], b2, b3);
-                    } else {
+                        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) s1[nt][e] = 0.f;
+                        kv8_qk(s1, qa, kb + C::kHeadPageBytes, lane);
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            s[nt][2] = s1[nt][2];
+                            s[nt][3] = s1[nt][3];
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const int c = ks >> 2;
+                        const int ch = (ks & 3) * 2 + ((lane >> 3) & 1);
+                        const int r = ((lane >> 4) << 3) + (lane & 7);
+                        uint32_t b0, b1, b2, b3;
+                        ldmatrix_x4(kb + c * 2048 + r * 128 + ((ch ^ (r & 7)) << 4), b0, b1, b2, b3);
                         mma_bf16_16816(s[0], qa[ks], b0, b1);
                         mma_bf16_16816(s[1], qa[ks], b2, b3);
                     }
@@ -418,7 +483,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, 2)
                         l[e >> 1] += pv;
                     }
                 uint32_t pa[4];
-                if (KV8) {
+                if constexpr (KV8) {
                     pa[0] = pack_f16x2(s[0][0], s[0][1]);
                     pa[1] = pack_f16x2(s[0][2], s[0][3]);
                     pa[2] = pack_f16x2(s[1][0], s[1][1]);
@@ -437,23 +502,30 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, 2)
                     vm1 = (key0 + 8 + qc < lk ? 0x0000ffffu : 0u) |
                           (key0 + 9 + qc < lk ? 0xffff0000u : 0u);
                 }
-#pragma unroll
-                for (int np = 0; np < D / 16; ++np) {
-                    const int c = np >> 2;
-                    const int ch = (np & 3) * 2 + (lane >> 4);
-                    const int r = ((lane >> 3) & 1) * 8 + (lane & 7);
-                    uint32_t v0, v1, v2, v3;
-                    ldmatrix_x4_trans(vb + c * 2048 + r * 128 + ((ch ^ (r & 7)) << 4), v0, v1, v2, v3);
-                    if (KV8) {
-                        mma_f16_16816(o[2 * np], pa, v0 & vm0, v1 & vm1);
-                        mma_f16_16816(o[2 * np + 1], pa, v2 & vm0, v3 & vm1);
+                if constexpr (KV8) {
+                    if (hp == 2) {
+                        // each head's P rows against its own V page
+                        const uint32_t pa0[4] = {pa[0], 0u, pa[2], 0u};
+                        const uint32_t pa1[4] = {0u, pa[1], 0u, pa[3]};
+                        kv8_pv(o, pa0, vb, lane, vm0, vm1);
+                        kv8_pv(o, pa1, vb + C::kHeadPageBytes, lane, vm0, vm1);
                     } else {
+                        kv8_pv(o, pa, vb, lane, vm0, vm1);
+                    }
+                } else {
+#pragma unroll
+                    for (int np = 0; np < D / 16; ++np) {
+                        const int c = np >> 2;
+                        const int ch = (np & 3) * 2 + (lane >> 4);
+                        const int r = ((lane >> 3) & 1) * 8 + (lane & 7);
+                        uint32_t v0, v1, v2, v3;
+                        ldmatrix_x4_trans(vb + c * 2048 + r * 128 + ((ch ^ (r & 7)) << 4), v0, v1, v2, v3);
                         mma_bf16_16816(o[2 * np], pa, v0 & vm0, v1 & vm1);
                         mma_bf16_16816(o[2 * np + 1], pa, v2 & vm0, v3 & vm1);
                     }
                 }
                 __syncwarp();
-                if (!KV8 && lane == 0) mbar_arrive(empty0 + 8 * st);
+                if (lane == 0) mbar_arrive(empty0 + 8 * st);
             }
             gbase += npages;
 
@@ -463,11 +535,24 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, 2)
                 l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 1);
                 l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 2);
             }
+            if constexpr (KV8) {
+                // o[nt][e] is column d = 16 (2t + e % 2) + nt; stored at d ^ 4 (row % 8)
+                // (groups of 4 columns stay together for the readers below)
 #pragma unroll
-            for (int nt = 0; nt < D / 8; ++nt) {
-                const int col = nt * 8 + qc;
-                *reinterpret_cast<float2 *>(mrg_o + qr * D + col) = make_float2(o[nt][0], o[nt][1]);
-                *reinterpret_cast<float2 *>(mrg_o + (qr + 8) * D + col) = make_float2(o[nt][2], o[nt][3]);
+                for (int nt = 0; nt < D / 8; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int row = qr + (e >> 1) * 8;
+                        const int d = 16 * (qc + (e & 1)) + nt;
+                        mrg_o[row * D + (d ^ ((row & 7) << 2))] = o[nt][e];
+                    }
+            } else {
+#pragma unroll
+                for (int nt = 0; nt < D / 8; ++nt) {
+                    const int col = nt * 8 + qc;
+                    *reinterpret_cast<float2 *>(mrg_o + qr * D + col) = make_float2(o[nt][0], o[nt][1]);
+                    *reinterpret_cast<float2 *>(mrg_o + (qr + 8) * D + col) = make_float2(o[nt][2], o[nt][3]);
+                }
             }
             if ((lane & 3) == 0) {
                 mrg_m[qr] = m[0];
@@ -482,7 +567,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, 2)
             for (int gi = tid; gi < kDecRows * (D / 4); gi += C::kConsumerWarps * 32) {
                 const int row = gi / (D / 4);
                 const int col = (gi % (D / 4)) * 4;
-                if (row >= pc.nrows) continue;
+                if (tile_row_idx(row, hp) >= pc.nrows) continue;
                 float mw[C::kConsumerWarps];
                 float M = -INFINITY;
 #pragma unroll
@@ -497,8 +582,9 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, 2)
                     for (int ww = 0; ww < C::kConsumerWarps; ++ww) {
                         const float f = fast_exp2(mw[ww] - M);
                         L += f * merge[ww * C::kMergeFloats + kDecRows * D + kDecRows + row];
+                        const int scol = KV8 ? col ^ ((row & 7) << 2) : col;
                         const float4 ov =
-                            *reinterpret_cast<const float4 *>(merge + ww * C::kMergeFloats + row * D + col);
+                            *reinterpret_cast<const float4 *>(merge + ww * C::kMergeFloats + row * D + scol);
                         acc.x += f * ov.x;
                         acc.y += f * ov.y;
                         acc.z += f * ov.z;
@@ -507,9 +593,9 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, 2)
                 }
                 if (pc.slot < 0) {
                     const float inv = L > 0.f ? p.v_scale / L : 0.f;
-                    const int pr = pc.row0 + row;
+                    const int pr = pc.row0 + tile_row_idx(row, hp);
                     const int64_t t = (int64_t)q0 + pr / p.g;
-                    const int h = pc.kvh * p.g + pr % p.g;
+                    const int h = (pc.kvh + tile_row_head(row, hp)) * p.g + pr % p.g;
                     if (p.lse != nullptr && col == 0) p.lse[t * p.hq + h] = row_lse(M, L);
                     uint2 packed;
                     packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
@@ -530,7 +616,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, 2)
                 named_barrier_sync(1, C::kConsumerWarps * 32);
                 if (s_merge) {
                     __threadfence();
-                    merge_unit<D>(p, q0, pc.kvh, pc.row0, pc.nrows, pc.slot0, pc.nslots, tid,
+                    merge_unit<D>(p, q0, pc.kvh, pc.row0, pc.nrows, hp, pc.slot0, pc.nslots, tid,
                                   C::kConsumerWarps * 32);
                 }
             }

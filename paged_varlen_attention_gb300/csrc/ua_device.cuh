@@ -243,6 +243,15 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return r;
 }
 
+// 16 bytes from shared memory (16-byte aligned address).
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
 // Two e4m3 values (the low and the high byte of the 16 bits) to an f16 pair
 // (low byte -> low half); exact, e4m3 being a subset of f16.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {

@@ -31,6 +31,7 @@ struct DecodeParams {
     int32_t *comb_count;         // plan: partials written per split unit (zero at launch)
     float *lse;                  // optional [total_q, Hq]: natural-log normaliser per row
     float v_scale;               // scale of the V values (fp8 cache; 1 otherwise)
+    int32_t heads_per_unit;      // e4m3 pages: kv heads per unit (tile rows 8j.. are head kvh + j)
     int *status;                 // device status word
 };
 

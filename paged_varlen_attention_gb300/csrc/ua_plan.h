@@ -14,8 +14,10 @@
 //     packed rows (Lq * G) fit one 16-row warp-MMA tile.  Their KV pages are
 //     concatenated and cut into equal page ranges, one per persistent CTA, so
 //     every SM streams the same number of pages (split-KV).  A unit cut into
-//     several pieces writes fp32 partials that the combine kernel merges with
-//     a log-sum-exp rule.
+//     several pieces writes fp32 partials; the CTA that writes a unit's last
+//     partial merges them with a log-sum-exp rule.  With two kv heads per
+//     unit (the e4m3 cache), a unit is (sequence, kv heads h and h + 1,
+//     8-row tile): tile rows 0-7 belong to head h, rows 8-15 to head h + 1.
 //   * prefill tiles -- (sequence, kv head, 256-row tile) for the rest: two
 //     128-row tensor-core tiles that share every K/V tile they load, longest
 //     first.
@@ -44,9 +46,9 @@ constexpr size_t kAlign = 256;
 
 struct alignas(16) DecPiece {   // one contiguous page range of one decode unit
     int32_t seq;
-    int32_t kvh;
+    int32_t kvh;         // (first) kv head of the unit
     int32_t row0;        // first packed row of the unit
-    int32_t nrows;       // packed rows in the unit (<= kDecRows)
+    int32_t nrows;       // packed rows in the unit, per kv head (<= kDecRows / heads per unit)
     int32_t page_begin;  // first logical page of the range
     int32_t page_end;    // one past the last logical page
     int32_t slot;        // -1: the piece is the whole unit, write bf16 output; else partial slot
@@ -86,6 +88,7 @@ struct Problem {
     int32_t bs;
     int32_t bt_stride;
     bool causal;
+    int32_t kv_heads_per_unit = 1;   // decode units: 1, or 2 (adjacent heads, <= 8 rows each)
 };
 
 // Offsets of the plan sections inside the device workspace.

@@ -59,6 +59,10 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
     plan.layout = Layout{};
     const int g = p.hq / p.hkv;
     const bool pre_ok = prefill_enabled && prefill_supports(p);
+    // decode units cover 1 kv head, or 2 adjacent heads (p.hkv even) with at
+    // most kDecRows / 2 rows each
+    const int hpu = (p.kv_heads_per_unit == 2 && p.hkv % 2 == 0) ? 2 : 1;
+    plan.dec_heads_per_unit = hpu;
 
     struct Unit {
         int32_t seq, kvh, row0, nrows, pages;
@@ -97,14 +101,14 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
         if (lq == 0) continue;
         const int32_t rows = lq * g;
         const bool decode = rows <= kDecRows || !pre_ok || prefill_rows_to_decode;
-        const int32_t step = decode ? kDecRows : kPreTileRows;
+        const int32_t step = decode ? kDecRows / hpu : kPreTileRows;
         // visible keys of the last row of each row tile; the same for every kv head
         for (int32_t r0 = 0; r0 < rows; r0 += step) {
             const int32_t nr = std::min<int32_t>(step, rows - r0);
             const int32_t kend = p.causal ? std::min<int32_t>(lk, lk - lq + (r0 + nr - 1) / g + 1) : lk;
             if (decode) {
                 const int32_t pages = (kend + kBlockSize - 1) / kBlockSize;
-                for (int h = 0; h < p.hkv; ++h) units.push_back({s, h, r0, nr, pages});
+                for (int h = 0; h < p.hkv; h += hpu) units.push_back({s, h, r0, nr, pages});
             } else {
                 PreTile t{};
                 t.seq = s;

@@ -9,6 +9,7 @@ namespace ua {
 
 struct Plan {
     int32_t dec_ctas = 0;
+    int32_t dec_heads_per_unit = 1;     // kv heads per decode unit (1 or 2)
     int64_t dec_pages = 0;
     std::vector<int32_t> cta_begin;     // dec_ctas + 1
     std::vector<DecPiece> pieces;

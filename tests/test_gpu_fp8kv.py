@@ -4,9 +4,11 @@
 The FP8 cache is the "KV cache compression" discussed in the review thread of
 "[Kernel] [V1] Improved performance for V1 Triton (ROCm) backend" (vLLM PR
 #14152), which names the fp8_e4m3fn type; the reading here: E4M3 bytes,
-k = k_scale * e4m3(byte), v = v_scale * e4m3(byte).  The kernel turns each
-page into f16 (exact) and multiplies with f16 Q and P; the tolerance is the
-one of the bf16 path (max 2e-2, mean 1e-3), the normaliser within 2e-3."""
+k = k_scale * e4m3(byte), v = v_scale * e4m3(byte).  The kernel widens the
+bytes to f16 (exact) and multiplies with f16 Q and P; the tolerance is the
+one of the bf16 path (max 2e-2, mean 1e-3), the normaliser within 2e-3.
+With Hkv even a decode unit holds two adjacent kv heads (tile rows 0-7 and
+8-15); the odd-Hkv cases run one head per unit."""
 import zlib
 
 import numpy as np
@@ -60,6 +62,11 @@ CASES = [
     ([1, 5, 40, 1], [100, 40, 300, 4096], 8, 2, True),                 # prefill rows -> decode kernel
     ([3, 2, 17], [5, 30, 17], 16, 4, False),                            # non-causal
     ([1, 1, 1], [2, 3, 1], 4, 4, True),                                 # G = 1
+    # units of two adjacent kv heads need Hkv even; odd Hkv keeps one head per unit
+    ([1, 2, 1], [300, 50, 17], 8, 1, True),                             # Hkv = 1, G = 8
+    ([1, 4, 1], [100, 64, 33], 12, 3, True),                            # Hkv = 3
+    ([2, 1, 3], [500, 60, 30], 16, 2, True),                            # G = 8, 8-row tiles
+    ([1, 1], [200, 3000], 32, 2, True),                                 # G = 16: a token spans two tiles
 ]
 
 
