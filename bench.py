@@ -759,7 +759,8 @@ def run_fp8kv(args):
                    "parallelism": "1 GPU, no collective"},
         "roofline": {"kernel": "ua_decode_kernel<128, fp8 kv>", "bound": "hbm", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": None, "per_launch": f"{dec_bytes} algorithmic bytes (1-byte K/V)",
+                     "traffic": ncu_traffic("decode", FP8_WORKLOAD),
+                     "per_launch": f"{dec_bytes} algorithmic bytes (1-byte K/V)",
                      "launch_ms": dec_ms, "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"},
         "gpu_launches": steps,
         "clocks": clocks.summary(),
