@@ -75,6 +75,8 @@ typedef enum ua_status {
 /* Device status word bits (ua_device_status). */
 #define UA_DEVICE_BAD_BLOCK_ID 0x1   /* a block_table entry outside [0, num_blocks) was skipped */
 #define UA_DEVICE_WAIT_TIMEOUT 0x2   /* a pipeline wait gave up; the output is incomplete */
+#define UA_DEVICE_BAD_METADATA 0x4   /* the device planner rejected cu_seqlens_q / seqused_k
+                                        (or a capacity): nothing was computed */
 
 /*
  * unified_attention -- attention over a paged varlen batch (definition above,
@@ -165,8 +167,10 @@ ua_status ua_plan_inspect(const int32_t *cu_seqlens_q_host, const int32_t *sequs
  *   ms[0..3]       decode, prefill, combine kernel time and the plan copy
  *                  (-1 when that step did not run; the combine is always -1
  *                  now: split units are merged inside the decode kernel by
- *                  the CTA that writes a unit's last partial);
- *   launches[0..3] kernel launches of each kind (the copy counts as 0).
+ *                  the CTA that writes a unit's last partial); for
+ *                  unified_attention_device_plan, ms[3] is the planner kernel;
+ *   launches[0..3] kernel launches of each kind (the copy counts as 0, the
+ *                  planner kernel as 1).
  * calls_back must be below min(profiled calls, UA_PROFILE_RING).
  */
 #define UA_PROFILE_RING 64
@@ -264,10 +268,12 @@ ua_status unified_attention_append(const void *q, const void *k_new, const void 
  * NaN).  k_cache, v_cache: device uint8 [num_blocks, block_size, Hkv, D], 16-
  * byte aligned; q and out bf16 as for unified_attention; lse: optional fp32
  * [total_q, Hq] (as unified_attention_lse) or NULL.  Every row runs in the
- * decode kernel, whose warps turn each page into f16 (exact: e4m3 values are
- * f16 values) and multiply with f16 Q (q is rounded to f16, so |q| must stay
- * below 65504) and f16 P; k_scale is folded into the softmax scale and
- * v_scale into the output.  head_size 128 only (else UA_ERR_UNSUPPORTED).
+ * decode kernel, whose threads widen the cache bytes to f16 in registers
+ * (exact: e4m3 values are f16 values) and multiply with f16 Q (q is rounded
+ * to f16, so |q| must stay below 65504) and f16 P; k_scale is folded into the
+ * softmax scale and v_scale into the output.  With num_kv_heads even, each
+ * work unit covers two adjacent kv heads (one 256-byte run of a page slot per
+ * load).  head_size 128 only (else UA_ERR_UNSUPPORTED).
  * Workspace size from ua_workspace_size_fp8kv.  The FP8 cache is the "KV cache
  * compression" discussed on "[Kernel] [V1] Improved performance for V1 Triton
  * (ROCm) backend" (vLLM PR #14152, review thread); the pages fix neither the
@@ -324,6 +330,81 @@ ua_status unified_attention_no_alloc(const void *q, const void *k_cache, const v
                                      int32_t num_q_heads, int32_t num_kv_heads,
                                      int32_t head_size, int32_t block_size, int32_t num_blocks,
                                      int32_t block_table_stride, void *stream);
+
+/*
+ * unified_attention_device_plan -- unified_attention planned on the GPU: no
+ * host copies of cu_seqlens_q / seqused_k, no host-side work that depends on
+ * them, fixed launch shapes.  So one call can be captured in a CUDA graph and
+ * the graph replayed after the device metadata (cu_seqlens_q, seqused_k,
+ * block_table) and q have been rewritten for a new batch of the same
+ * num_seqs.  The pages' unified kernel consumes the engine's existing varlen
+ * metadata with no extra host step ("[Kernel] [V1] Improved performance for
+ * V1 Triton (ROCm) backend", vLLM PR #14152, section "How is this performance
+ * improvement achieved?").
+ *
+ * A planner kernel (one CTA) reads the device arrays and writes into the
+ * workspace the same plan the host planner makes for that batch: the same
+ * routing of rows to the decode and prefill kernels, decode page ranges, split
+ * pieces and prefill item order.  Then the decode kernel (kDecCtasPerSm x SMs
+ * CTAs) and, when the prefill kernel can take this head grouping and cache
+ * type, the prefill kernel (SMs CTAs) run; CTAs beyond the plan's count exit.
+ *
+ *   q, out       bf16 [max_total_q, Hq, D]: buffers sized for max_total_q
+ *                tokens; rows past cu_seqlens_q[num_seqs] are not written.
+ *   lse          optional fp32 [max_total_q, Hq] or NULL.
+ *   num_seqs     sequences in the batch (cu_seqlens_q has num_seqs + 1
+ *                entries); sequences with no query tokens are allowed.
+ *   max_total_q  the token capacity; the planner rejects a batch with
+ *                cu_seqlens_q[num_seqs] > max_total_q.
+ *   kv_fp8       0: bf16 caches; 1: e4m3 caches with k_scale / v_scale as
+ *                for unified_attention_fp8kv (head_size 128 only).
+ *   workspace    ua_workspace_size_device_plan bytes, 256-byte aligned; laid
+ *                out for (num_seqs, max_total_q, heads, head size,
+ *                block_table_stride, kv_fp8) and the device's SM count.
+ * Other arguments as for unified_attention.  The host checks shapes,
+ * pointers and the workspace; the metadata itself is checked on the device
+ * (the same rules as unified_attention): a bad batch leaves an empty plan (no
+ * output written) and sets UA_DEVICE_BAD_METADATA for ua_device_status.
+ * Asynchronous on `stream`; no allocation, no synchronisation.
+ */
+ua_status unified_attention_device_plan(const void *q, const void *k_cache, const void *v_cache,
+                                        const int32_t *cu_seqlens_q, const int32_t *seqused_k,
+                                        const int32_t *block_table, float softmax_scale,
+                                        int32_t causal, void *out, float *lse, int32_t num_seqs,
+                                        int32_t max_total_q, int32_t num_q_heads,
+                                        int32_t num_kv_heads, int32_t head_size,
+                                        int32_t block_size, int32_t num_blocks,
+                                        int32_t block_table_stride, int32_t kv_fp8,
+                                        float k_scale, float v_scale, void *workspace,
+                                        size_t workspace_bytes, void *stream);
+ua_status ua_workspace_size_device_plan(int32_t num_seqs, int32_t max_total_q,
+                                        int32_t num_q_heads, int32_t num_kv_heads,
+                                        int32_t head_size, int32_t block_size,
+                                        int32_t block_table_stride, int32_t kv_fp8,
+                                        size_t *bytes);
+
+/*
+ * ua_device_plan_build -- only the planner kernel of
+ * unified_attention_device_plan (same arguments), for inspecting the plan.
+ * ua_device_plan_layout -- host-only: where that plan lies in the workspace
+ * for a GPU with num_sms SMs.  offsets[8]: byte offsets of the header (int64
+ * {dec_ctas, n_pieces, n_comb, n_slots, pre_ctas, n_tiles, dec_pages,
+ * error}), cta_begin (int32), the decode pieces (8 x int32 each: seq, kvh,
+ * row0, nrows, page_begin, page_end, slot, unit), the split units (8 x
+ * int32), their arrival counters, the prefill items (8 x int32: seq, kvh,
+ * row0, nrows, kv_tiles, q0, lq, lk), pre_begin (int32), and the workspace
+ * size.  caps[8]: decode grid, unit, item, piece, split-unit and partial-slot
+ * capacities, histogram buckets, num_sms.
+ */
+ua_status ua_device_plan_build(const int32_t *cu_seqlens_q, const int32_t *seqused_k,
+                               int32_t causal, int32_t num_seqs, int32_t max_total_q,
+                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                               int32_t block_size, int32_t block_table_stride, int32_t kv_fp8,
+                               void *workspace, size_t workspace_bytes, void *stream);
+ua_status ua_device_plan_layout(int32_t num_seqs, int32_t max_total_q, int32_t num_q_heads,
+                                int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                int32_t block_table_stride, int32_t kv_fp8, int32_t num_sms,
+                                int64_t *offsets, int32_t *caps);
 
 #ifdef __cplusplus
 }

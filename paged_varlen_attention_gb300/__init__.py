@@ -14,7 +14,8 @@ _EXPORTS = ("UAError", "device_status", "library_path", "load_library", "plan_in
             "unified_attention", "unified_attention_fp8kv", "merge_attn_states", "kv_append",
             "workspace_size",
             "profile_enable",
-            "profile_read")
+            "profile_read", "unified_attention_device_plan", "workspace_size_device_plan",
+            "device_plan")
 
 
 def __getattr__(name):

@@ -22,11 +22,13 @@ STATUS = {0: "UA_OK", 1: "UA_ERR_INVALID_ARG", 2: "UA_ERR_UNSUPPORTED", 3: "UA_E
           4: "UA_ERR_CUDA", 5: "UA_ERR_DEVICE_CHECK"}
 DEVICE_BAD_BLOCK_ID = 0x1
 DEVICE_WAIT_TIMEOUT = 0x2
+DEVICE_BAD_METADATA = 0x4
 
 SYMBOLS = ("unified_attention", "unified_attention_lse", "ua_merge_attn_states", "ua_kv_append",
            "unified_attention_append", "unified_attention_fp8kv", "ua_workspace_size_fp8kv",
            "ua_workspace_size", "ua_status_string", "ua_device_status", "ua_plan_inspect",
-           "ua_profile_enable", "ua_profile_read")
+           "ua_profile_enable", "ua_profile_read", "unified_attention_device_plan",
+           "ua_workspace_size_device_plan", "ua_device_plan_build", "ua_device_plan_layout")
 
 
 class UAError(RuntimeError):
@@ -90,6 +92,19 @@ def load_library():
         lib.ua_profile_enable.restype = ctypes.c_int
         lib.ua_profile_read.argtypes = [I32, P, P]
         lib.ua_profile_read.restype = ctypes.c_int
+        lib.unified_attention_device_plan.argtypes = [P, P, P, P, P, P, ctypes.c_float, I32, P, P,
+                                                      I32, I32, I32, I32, I32, I32, I32, I32, I32,
+                                                      ctypes.c_float, ctypes.c_float, P,
+                                                      ctypes.c_size_t, P]
+        lib.unified_attention_device_plan.restype = ctypes.c_int
+        lib.ua_workspace_size_device_plan.argtypes = [I32, I32, I32, I32, I32, I32, I32, I32,
+                                                      ctypes.POINTER(ctypes.c_size_t)]
+        lib.ua_workspace_size_device_plan.restype = ctypes.c_int
+        lib.ua_device_plan_build.argtypes = [P, P, I32, I32, I32, I32, I32, I32, I32, I32, I32, P,
+                                             ctypes.c_size_t, P]
+        lib.ua_device_plan_build.restype = ctypes.c_int
+        lib.ua_device_plan_layout.argtypes = [I32, I32, I32, I32, I32, I32, I32, I32, I32, P, P]
+        lib.ua_device_plan_layout.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -381,3 +396,122 @@ def unified_attention_fp8kv(q, k_cache, v_cache, k_scale, v_scale, cu_seqlens_q,
                                      workspace.numel(), stream)
     _check(rc, "unified_attention_fp8kv")
     return out
+
+
+def _stream_handle(torch, device, stream):
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def workspace_size_device_plan(num_seqs, max_total_q, num_q_heads, num_kv_heads, head_size,
+                               block_table_stride, kv_fp8=False, block_size=16):
+    """Bytes of workspace ``unified_attention_device_plan`` needs for these capacities."""
+    lib = load_library()
+    need = ctypes.c_size_t(0)
+    _check(lib.ua_workspace_size_device_plan(int(num_seqs), int(max_total_q), int(num_q_heads),
+                                             int(num_kv_heads), int(head_size), int(block_size),
+                                             int(block_table_stride), int(bool(kv_fp8)),
+                                             ctypes.byref(need)),
+           "ua_workspace_size_device_plan")
+    return int(need.value)
+
+
+def unified_attention_device_plan(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table,
+                                  softmax_scale, causal=True, out=None, *, workspace, lse=None,
+                                  num_seqs=None, kv_fp8=False, k_scale=1.0, v_scale=1.0,
+                                  stream=None):
+    """Attention planned on the GPU (``unified_attention_device_plan``): no host copies of
+    the metadata, so the call can be captured in a CUDA graph and replayed after
+    ``cu_seqlens_q`` / ``seqused_k`` / ``block_table`` / ``q`` are rewritten in place.
+
+    q / out: bf16 [max_total_q, Hq, D] buffers (their first dimension is the token
+    capacity); k_cache / v_cache: bf16, or uint8 E4M3 codes with ``kv_fp8``; lse:
+    optional float32 [max_total_q, Hq].  ``workspace``: a uint8 CUDA tensor of at least
+    ``workspace_size_device_plan`` bytes, owned by the caller (a captured graph keeps
+    using it).  ``num_seqs`` defaults to ``seqused_k.shape[0]``.  Returns ``out``.
+    """
+    import torch
+
+    lib = load_library()
+    cache_dt = torch.uint8 if kv_fp8 else torch.bfloat16
+    for name, t, dt in (("q", q, torch.bfloat16), ("k_cache", k_cache, cache_dt),
+                        ("v_cache", v_cache, cache_dt),
+                        ("cu_seqlens_q", cu_seqlens_q, torch.int32),
+                        ("seqused_k", seqused_k, torch.int32),
+                        ("block_table", block_table, torch.int32),
+                        ("workspace", workspace, torch.uint8)):
+        if not t.is_cuda or t.dtype != dt or not t.is_contiguous():
+            raise UAError(1, f"{name} must be a contiguous CUDA {dt} tensor")
+    max_total_q, hq, d = q.shape
+    nb, bs, hk, d2 = k_cache.shape
+    if v_cache.shape != k_cache.shape or d2 != d:
+        raise UAError(1, "q / k_cache / v_cache shapes disagree")
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise UAError(1, "out must be a contiguous bf16 tensor shaped like q")
+    if lse is not None and (not lse.is_cuda or lse.dtype != torch.float32
+                            or tuple(lse.shape) != (max_total_q, hq) or not lse.is_contiguous()):
+        raise UAError(1, "lse must be a contiguous CUDA float32 tensor [max_total_q, Hq]")
+    ns = int(seqused_k.shape[0]) if num_seqs is None else int(num_seqs)
+    stride = int(block_table.shape[1]) if block_table.dim() == 2 else 0
+    rc = lib.unified_attention_device_plan(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), cu_seqlens_q.data_ptr(),
+        seqused_k.data_ptr(), block_table.data_ptr(), float(softmax_scale), int(bool(causal)),
+        out.data_ptr(), None if lse is None else lse.data_ptr(), ns, max_total_q, hq, hk, d, bs,
+        nb, stride, int(bool(kv_fp8)), float(k_scale), float(v_scale), workspace.data_ptr(),
+        workspace.numel(), _stream_handle(torch, q.device, stream))
+    _check(rc, "unified_attention_device_plan")
+    return out
+
+
+def device_plan(cu_seqlens_q, seqused_k, causal, num_q_heads, num_kv_heads, head_size,
+                block_table_stride, max_total_q, kv_fp8=False):
+    """Run only the device planner on CUDA int32 metadata and read the plan back (synchronises).
+
+    Returns a dict of numpy arrays: ``header`` (int64 dec_ctas, n_pieces, n_comb,
+    n_slots, pre_ctas, n_tiles, dec_pages, error), ``cta_begin`` [dec_ctas + 1],
+    ``pieces`` [n_pieces, 8] (seq, kvh, row0, nrows, page_begin, page_end, slot, unit),
+    ``comb`` [n_comb, 8], ``tiles`` [n_tiles, 8] (seq, kvh, row0, nrows, kv_tiles, q0,
+    lq, lk) and ``pre_begin`` [pre_ctas + 1].
+    """
+    import torch
+
+    lib = load_library()
+    dev = cu_seqlens_q.device
+    ns = int(seqused_k.shape[0])
+    nbytes = workspace_size_device_plan(ns, max_total_q, num_q_heads, num_kv_heads, head_size,
+                                        block_table_stride, kv_fp8)
+    ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    props = torch.cuda.get_device_properties(dev)
+    offs = np.zeros(8, np.int64)
+    caps = np.zeros(8, np.int32)
+    _check(lib.ua_device_plan_layout(ns, int(max_total_q), int(num_q_heads), int(num_kv_heads),
+                                     int(head_size), 16, int(block_table_stride),
+                                     int(bool(kv_fp8)), props.multi_processor_count,
+                                     _np_ptr(offs), _np_ptr(caps)), "ua_device_plan_layout")
+    _check(lib.ua_device_plan_build(cu_seqlens_q.data_ptr(), seqused_k.data_ptr(),
+                                    int(bool(causal)), ns, int(max_total_q), int(num_q_heads),
+                                    int(num_kv_heads), int(head_size), 16,
+                                    int(block_table_stride), int(bool(kv_fp8)), ws.data_ptr(),
+                                    ws.numel(), torch.cuda.current_stream(dev).cuda_stream),
+           "ua_device_plan_build")
+    torch.cuda.synchronize(dev)
+    raw = ws.cpu().numpy()
+
+    def i32(off, n, cols=1):
+        a = raw[off:off + 4 * n * cols].view(np.int32)
+        return a.reshape(n, cols) if cols > 1 else a
+
+    hdr = raw[offs[0]:offs[0] + 64].view(np.int64).copy()
+    dec_ctas, n_pieces, n_comb, _, pre_ctas, n_tiles = (int(x) for x in hdr[:6])
+    return {
+        "header": hdr,
+        "cta_begin": i32(offs[1], dec_ctas + 1).copy(),
+        "pieces": i32(offs[2], n_pieces, 8).copy(),
+        "comb": i32(offs[3], n_comb, 8).copy(),
+        "tiles": i32(offs[5], n_tiles, 8).copy(),
+        "pre_begin": i32(offs[6], pre_ctas + 1).copy(),
+        "caps": caps,
+    }

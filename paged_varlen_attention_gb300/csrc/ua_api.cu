@@ -726,3 +726,239 @@ extern "C" ua_status unified_attention_fp8kv(
                              num_blocks, block_table_stride, workspace, workspace_bytes, stream,
                              /*pinned_plan=*/true, lse, /*kv_fp8=*/1, k_scale, v_scale);
 }
+
+// ---------------------------------------------------------------------------
+// Calls planned on the device (no host copies of the lengths; graph-capturable)
+
+namespace ua {
+
+// Host-side checks of a device-plan call's shapes; fills the workspace shape.
+static ua_status device_plan_shape(int32_t num_seqs, int32_t max_total_q, int32_t hq, int32_t hkv,
+                                   int32_t d, int32_t bs, int32_t bt_stride, int32_t kv_fp8,
+                                   int sms, DevPlanShape *s) {
+    if (num_seqs < 0 || max_total_q < 0 || hq <= 0 || hkv <= 0 || bt_stride < 0)
+        return UA_ERR_INVALID_ARG;
+    if (hq % hkv != 0 || (d != 64 && d != 128) || bs != kBlockSize) return UA_ERR_UNSUPPORTED;
+    if (kv_fp8 && d != 128) return UA_ERR_UNSUPPORTED;
+    if ((int64_t)max_total_q * (hq / hkv) > INT32_MAX / 2) return UA_ERR_INVALID_ARG;
+    Problem pr = make_problem(nullptr, nullptr, 0, hq, hkv, d, bs, bt_stride, 1);
+    s->num_seqs = num_seqs;
+    s->max_total_q = max_total_q;
+    s->hq = hq;
+    s->hkv = hkv;
+    s->d = d;
+    s->bt_stride = bt_stride;
+    s->hpu = (kv_fp8 && hkv % 2 == 0) ? 2 : 1;
+    s->prefill_ok = (kPrefillEnabled && !kv_fp8 && prefill_supports(pr)) ? 1 : 0;
+    s->num_sms = sms;
+    return UA_OK;
+}
+
+static ua_status run_attention_device_plan(
+    const void *q, const void *k_cache, const void *v_cache, const int32_t *cu_seqlens_q,
+    const int32_t *seqused_k, const int32_t *block_table, float softmax_scale, int32_t causal,
+    void *out, float *lse, int32_t num_seqs, int32_t max_total_q, int32_t num_q_heads,
+    int32_t num_kv_heads, int32_t head_size, int32_t block_size, int32_t num_blocks,
+    int32_t block_table_stride, int32_t kv_fp8, float k_scale, float v_scale, void *workspace,
+    size_t workspace_bytes, void *stream_ptr, bool plan_only) {
+    DeviceState *ds = nullptr;
+    ua_status st = device_state(&ds);
+    if (st != UA_OK) return st;
+    DevPlanShape shape{};
+    st = device_plan_shape(num_seqs, max_total_q, num_q_heads, num_kv_heads, head_size, block_size,
+                           block_table_stride, kv_fp8, ds->sms, &shape);
+    if (st != UA_OK) return st;
+    if (!std::isfinite(softmax_scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+        return UA_ERR_INVALID_ARG;
+    if (num_seqs == 0 || max_total_q == 0) return UA_OK;
+    if (!cu_seqlens_q || !seqused_k) return UA_ERR_INVALID_ARG;
+    if (!plan_only) {
+        if (!q || !k_cache || !v_cache || !out || !block_table) return UA_ERR_INVALID_ARG;
+        if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+            !aligned(lse, 4))
+            return UA_ERR_INVALID_ARG;
+        if (num_blocks <= 0 || (int64_t)num_blocks * block_size >= ((int64_t)1 << 31))
+            return UA_ERR_INVALID_ARG;
+    }
+    const DevPlanLayout L = device_plan_layout(shape);
+    if (!L.valid) return UA_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < L.total_bytes || !aligned(workspace, kAlign))
+        return UA_ERR_WORKSPACE;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    if (plan_only) {
+        if (launch_device_plan(shape, L, cu_seqlens_q, seqused_k, causal, ws, ds->status, stream) !=
+            cudaSuccess)
+            return UA_ERR_CUDA;
+        return UA_OK;
+    }
+
+    // tensor maps over the caller's buffers (q / out sized for max_total_q tokens)
+    const int g = num_q_heads / num_kv_heads;
+    CUtensorMap tm_kp, tm_vp, tm_q, tm_o, tm_k3;
+    const int eb = kv_fp8 ? 1 : 2;
+    if (!encode_page_map(&tm_kp, k_cache, head_size, num_kv_heads, (uint64_t)num_blocks, eb, shape.hpu) ||
+        !encode_page_map(&tm_vp, v_cache, head_size, num_kv_heads, (uint64_t)num_blocks, eb, shape.hpu))
+        return UA_ERR_CUDA;
+    if (shape.prefill_ok &&
+        (!encode_map(&tm_q, q, head_size, num_q_heads, (uint64_t)max_total_q, g, kPreRows / g) ||
+         !encode_map(&tm_o, out, head_size, num_q_heads, (uint64_t)max_total_q, g, kPreRows / g) ||
+         !encode_map(&tm_k3, k_cache, head_size, num_kv_heads, (uint64_t)num_blocks * block_size, 1,
+                     kBlockSize)))
+        return UA_ERR_CUDA;
+
+    const bool prof = g_profile;
+    if (prof && !ds->events) {
+        for (int c = 0; c < UA_PROFILE_RING; ++c)
+            for (int i = 0; i < 5; ++i)
+                if (cudaEventCreate(&ds->ev[c][i]) != cudaSuccess) {
+                    cudaGetLastError();
+                    return UA_ERR_CUDA;
+                }
+        ds->events = true;
+    }
+    const int pslot = (int)(ds->calls % UA_PROFILE_RING);
+    auto mark = [&](int i) {
+        if (prof) cudaEventRecord(ds->ev[pslot][i], stream);
+    };
+    const float scale_log2 = softmax_scale * k_scale * 1.4426950408889634f;
+
+    mark(0);
+    if (launch_device_plan(shape, L, cu_seqlens_q, seqused_k, causal, ws, ds->status, stream) !=
+        cudaSuccess)
+        return UA_ERR_CUDA;
+    mark(1);
+    DecodeParams dp{};
+    dp.q = static_cast<const __nv_bfloat16 *>(q);
+    dp.out = static_cast<__nv_bfloat16 *>(out);
+    dp.cu = cu_seqlens_q;
+    dp.seqused_k = seqused_k;
+    dp.block_table = block_table;
+    dp.bt_stride = block_table_stride;
+    dp.num_blocks = num_blocks;
+    dp.hq = num_q_heads;
+    dp.hkv = num_kv_heads;
+    dp.g = g;
+    dp.causal = causal != 0;
+    dp.scale_log2 = scale_log2;
+    dp.cta_begin = reinterpret_cast<const int32_t *>(ws + L.off_cta);
+    dp.pieces = reinterpret_cast<const DecPiece *>(ws + L.off_pieces);
+    dp.part_o = reinterpret_cast<float *>(ws + L.off_part_o);
+    dp.part_ml = reinterpret_cast<float *>(ws + L.off_part_ml);
+    dp.comb = reinterpret_cast<const CombUnit *>(ws + L.off_comb);
+    dp.comb_count = reinterpret_cast<int32_t *>(ws + L.off_comb_count);
+    dp.lse = lse;
+    dp.v_scale = v_scale;
+    dp.heads_per_unit = shape.hpu;
+    dp.status = ds->status;
+    if (launch_decode(head_size, kv_fp8 != 0, dp, tm_kp, tm_vp, L.dec_grid, stream) != cudaSuccess)
+        return UA_ERR_CUDA;
+    mark(2);
+    if (shape.prefill_ok) {
+        PrefillParams pp{};
+        pp.k_cache = static_cast<const __nv_bfloat16 *>(k_cache);
+        pp.out = static_cast<__nv_bfloat16 *>(out);
+        pp.lse = lse;
+        pp.cu = cu_seqlens_q;
+        pp.seqused_k = seqused_k;
+        pp.block_table = block_table;
+        pp.bt_stride = block_table_stride;
+        pp.num_blocks = num_blocks;
+        pp.hq = num_q_heads;
+        pp.hkv = num_kv_heads;
+        pp.g = g;
+        pp.causal = causal != 0;
+        pp.scale_log2 = scale_log2;
+        pp.tiles = reinterpret_cast<const PreTile *>(ws + L.off_tiles);
+        pp.tile_begin = reinterpret_cast<const int32_t *>(ws + L.off_pre_begin);
+        pp.n_tiles = L.cap_items;
+        pp.status = ds->status;
+        if (launch_prefill(head_size, pp, tm_q, tm_o, tm_k3, tm_vp, shape.num_sms, stream) !=
+            cudaSuccess)
+            return UA_ERR_CUDA;
+    }
+    mark(3);
+    mark(4);
+    if (prof) {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        ds->ran[pslot][0] = true;
+        ds->ran[pslot][1] = shape.prefill_ok != 0;
+        ds->ran[pslot][2] = false;
+        ds->ran[pslot][3] = true;
+        ds->launches[pslot][0] = 1;
+        ds->launches[pslot][1] = shape.prefill_ok ? 1 : 0;
+        ds->launches[pslot][2] = 0;
+        ds->launches[pslot][3] = 1;   // the planner kernel
+        ++ds->calls;
+    }
+    return UA_OK;
+}
+
+}  // namespace ua
+
+extern "C" ua_status ua_workspace_size_device_plan(int32_t num_seqs, int32_t max_total_q,
+                                                   int32_t num_q_heads, int32_t num_kv_heads,
+                                                   int32_t head_size, int32_t block_size,
+                                                   int32_t block_table_stride, int32_t kv_fp8,
+                                                   size_t *bytes) {
+    if (!bytes) return UA_ERR_INVALID_ARG;
+    DeviceState *ds = nullptr;
+    ua_status st = device_state(&ds);
+    if (st != UA_OK) return st;
+    DevPlanShape shape{};
+    st = device_plan_shape(num_seqs, max_total_q, num_q_heads, num_kv_heads, head_size, block_size,
+                           block_table_stride, kv_fp8, ds->sms, &shape);
+    if (st != UA_OK) return st;
+    const DevPlanLayout L = device_plan_layout(shape);
+    if (!L.valid) return UA_ERR_UNSUPPORTED;
+    *bytes = L.total_bytes;
+    return UA_OK;
+}
+
+extern "C" ua_status ua_device_plan_layout(int32_t num_seqs, int32_t max_total_q,
+                                           int32_t num_q_heads, int32_t num_kv_heads,
+                                           int32_t head_size, int32_t block_size,
+                                           int32_t block_table_stride, int32_t kv_fp8,
+                                           int32_t num_sms, int64_t *offsets, int32_t *caps) {
+    if (!offsets || !caps || num_sms <= 0) return UA_ERR_INVALID_ARG;
+    DevPlanShape shape{};
+    ua_status st = device_plan_shape(num_seqs, max_total_q, num_q_heads, num_kv_heads, head_size,
+                                     block_size, block_table_stride, kv_fp8, num_sms, &shape);
+    if (st != UA_OK) return st;
+    const DevPlanLayout L = device_plan_layout(shape);
+    if (!L.valid) return UA_ERR_UNSUPPORTED;
+    const size_t off[8] = {L.off_header, L.off_cta,       L.off_pieces,    L.off_comb,
+                           L.off_comb_count, L.off_tiles, L.off_pre_begin, L.total_bytes};
+    for (int i = 0; i < 8; ++i) offsets[i] = (int64_t)off[i];
+    const int32_t cap[8] = {L.dec_grid, L.cap_units, L.cap_items, L.cap_pieces,
+                            L.cap_comb, L.cap_slots, L.n_buckets, shape.num_sms};
+    for (int i = 0; i < 8; ++i) caps[i] = cap[i];
+    return UA_OK;
+}
+
+extern "C" ua_status ua_device_plan_build(const int32_t *cu_seqlens_q, const int32_t *seqused_k,
+                                          int32_t causal, int32_t num_seqs, int32_t max_total_q,
+                                          int32_t num_q_heads, int32_t num_kv_heads,
+                                          int32_t head_size, int32_t block_size,
+                                          int32_t block_table_stride, int32_t kv_fp8,
+                                          void *workspace, size_t workspace_bytes, void *stream) {
+    return ua::run_attention_device_plan(nullptr, nullptr, nullptr, cu_seqlens_q, seqused_k, nullptr,
+                                         1.f, causal, nullptr, nullptr, num_seqs, max_total_q,
+                                         num_q_heads, num_kv_heads, head_size, block_size, 0,
+                                         block_table_stride, kv_fp8, 1.f, 1.f, workspace,
+                                         workspace_bytes, stream, /*plan_only=*/true);
+}
+
+extern "C" ua_status unified_attention_device_plan(
+    const void *q, const void *k_cache, const void *v_cache, const int32_t *cu_seqlens_q,
+    const int32_t *seqused_k, const int32_t *block_table, float softmax_scale, int32_t causal,
+    void *out, float *lse, int32_t num_seqs, int32_t max_total_q, int32_t num_q_heads,
+    int32_t num_kv_heads, int32_t head_size, int32_t block_size, int32_t num_blocks,
+    int32_t block_table_stride, int32_t kv_fp8, float k_scale, float v_scale, void *workspace,
+    size_t workspace_bytes, void *stream) {
+    return ua::run_attention_device_plan(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table,
+                                         softmax_scale, causal, out, lse, num_seqs, max_total_q,
+                                         num_q_heads, num_kv_heads, head_size, block_size,
+                                         num_blocks, block_table_stride, kv_fp8, k_scale, v_scale,
+                                         workspace, workspace_bytes, stream, /*plan_only=*/false);
+}

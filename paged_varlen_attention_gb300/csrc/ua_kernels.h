@@ -79,6 +79,42 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
                         void *stream, bool pinned_plan, float *lse, int kv_fp8 = 0,
                         float k_scale = 1.f, float v_scale = 1.f);
 
+// ---- plan built on the device (ua_device_plan.cu)
+// What a device-plan workspace is laid out for: the batch's sequence count,
+// the query-token capacity of q / out, the heads, head size, block-table
+// width, kv heads per decode unit, whether the prefill kernel may take rows,
+// and the SM count (decode grid kDecCtasPerSm * num_sms, prefill grid num_sms).
+struct DevPlanShape {
+    int32_t num_seqs;
+    int32_t max_total_q;
+    int32_t hq;
+    int32_t hkv;
+    int32_t d;
+    int32_t bt_stride;
+    int32_t hpu;
+    int32_t prefill_ok;
+    int32_t num_sms;
+};
+
+// Workspace sections (byte offsets) and capacities for one DevPlanShape.
+// The header holds int64 {dec_ctas, n_pieces, n_comb, n_slots, pre_ctas,
+// n_tiles, dec_pages, error} of the last plan built.
+struct DevPlanLayout {
+    size_t off_header, off_cta, off_pieces, off_comb, off_comb_count, off_tiles, off_pre_begin;
+    size_t off_part_o, off_part_ml, off_scratch, total_bytes;
+    int32_t dec_grid, cap_units, cap_items, cap_pieces, cap_comb, cap_slots, n_buckets;
+    bool valid;   // false: the capacities do not fit the planner's 32-bit counts
+};
+
+DevPlanLayout device_plan_layout(const DevPlanShape &s);
+
+// Builds the plan of (cu, seqused_k) into the workspace (one CTA).  Bad
+// metadata or an exceeded capacity leaves an empty plan and sets
+// UA_DEVICE_BAD_METADATA_BIT in *status.
+cudaError_t launch_device_plan(const DevPlanShape &s, const DevPlanLayout &L, const int32_t *cu,
+                               const int32_t *seqused_k, int32_t causal, void *workspace,
+                               int *status, cudaStream_t stream);
+
 // Writes the new tokens' K / V rows ([total_q, Hkv, D] bf16) into their
 // pages: token i of sequence s to position seqused_k[s] - Lq + i.
 cudaError_t launch_kv_append(const void *k_new, const void *v_new, const int32_t *cu,

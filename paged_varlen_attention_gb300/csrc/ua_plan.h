@@ -33,6 +33,7 @@
 
 #define UA_DEVICE_BAD_BLOCK_ID_BIT 0x1
 #define UA_DEVICE_WAIT_TIMEOUT_BIT 0x2
+#define UA_DEVICE_BAD_METADATA_BIT 0x4
 
 namespace ua {
 
