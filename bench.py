@@ -69,6 +69,9 @@ CASCADE_WORKLOAD = "llama3_8b_cascade_64dec_shared4k"
 APPEND_WORKLOAD = "kv_append_mistral_24b_16x1000"
 # The headline decode batch over an FP8 E4M3 KV cache (per-tensor scales).
 FP8_WORKLOAD = "llama3_8b_decode_64x2k-4k_fp8kv"
+# the headline decode batch through unified_attention_device_plan, captured once
+# as a CUDA graph and replayed (no host planning, no plan copy)
+GRAPH_WORKLOAD = "llama3_8b_decode_64x2k-4k_graph"
 
 
 def parse_args():
@@ -77,7 +80,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=sorted(WORKLOADS) + [CASCADE_WORKLOAD, APPEND_WORKLOAD, FP8_WORKLOAD])
+                    choices=sorted(WORKLOADS) + [CASCADE_WORKLOAD, APPEND_WORKLOAD, FP8_WORKLOAD,
+                                                 GRAPH_WORKLOAD])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -767,6 +771,95 @@ def run_fp8kv(args):
     }
 
 
+def run_graph(args):
+    """The headline decode batch planned on the GPU (unified_attention_device_plan):
+    one call captured as a CUDA graph, each step one replay (planner kernel, then the
+    decode kernel; the graph is decode-only -- max_seq_q = 1 -- so no prefill grid)."""
+    import torch
+    import paged_varlen_attention_gb300 as ua
+
+    ua.load_library()
+    dev = torch.device("cuda:0")
+    b = W.config_batch(WORKLOADS[DEFAULT_WORKLOAD], poison=False)
+    s_ = b.spec
+    d = device_batch(b, torch, dev)
+    out = torch.empty_like(d["q"])
+    nbytes = ua.workspace_size_device_plan(s_.num_seqs, s_.total_q, s_.num_q_heads,
+                                           s_.num_kv_heads, s_.head_size, b.block_table_stride,
+                                           max_seq_q=1)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
+
+    def call(stream):
+        ua.unified_attention_device_plan(d["q"], d["k_cache"], d["v_cache"], d["cu_seqlens_q"],
+                                         d["seqused_k"], d["block_table"], s_.softmax_scale, True,
+                                         out=out, workspace=ws, max_seq_q=1, stream=stream)
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for _ in range(max(args.warmup, 3)):
+            call(side)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call(torch.cuda.current_stream(dev))
+    for _ in range(max(args.warmup, 3)):
+        graph.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    steps = args.steps
+
+    def timed(fn):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        torch.cuda.synchronize()
+        for a, e in evs:
+            flush()
+            a.record(stream)
+            fn()
+            e.record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(e) for a, e in evs]
+
+    with ClockSampler(gpu_id_for_smi(torch, 0)) as clocks:
+        times = timed(graph.replay)
+        # per-kernel times: the same call made eagerly with the library's events
+        ua.profile_enable(True)
+        timed(lambda: call(stream))
+    prof = [ua.profile_read(k) for k in range(steps)]
+    ua.profile_enable(False)
+    if ua.device_status():
+        raise RuntimeError("device status set after the graph steps")
+    dec_ms = statistics.mean(p[0][0] for p in prof)
+    plan_ms = statistics.mean(p[0][3] for p in prof)
+    work = algorithmic_work(s_)
+    achieved = work["decode_bytes"] / (dec_ms / 1e3) / 1e9
+    peaks = measured_peaks()
+    total_s = sum(times) / 1e3
+    return {
+        "metric": METRIC, "value": s_.total_q * steps / total_s, "unit": "tokens/s", "n_gpus": 1,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": sum(times) / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, shuffled pages)",
+        "config": {"workload": GRAPH_WORKLOAD, "num_seqs": s_.num_seqs, "q_tokens": s_.total_q,
+                   "kv_tokens": work["kv_tokens"], "num_q_heads": s_.num_q_heads,
+                   "num_kv_heads": s_.num_kv_heads, "head_size": s_.head_size, "block_size": 16,
+                   "plan": "on the device (CUDA graph replay; no host planning or plan copy)",
+                   "l2": "L2 flushed between steps (256 MB write, then 256 MB read so the write-back is outside the timed interval)",
+                   "parallelism": "1 GPU, no collective"},
+        "roofline": {"kernel": "ua_decode_kernel", "bound": "hbm", "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": ncu_traffic("decode", DEFAULT_WORKLOAD),
+                     "per_launch": f"{work['decode_bytes']} algorithmic bytes",
+                     "launch_ms": dec_ms, "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"},
+        "call": {"kernel_ms": {"planner": plan_ms, "decode": dec_ms}},
+        "gpu_launches": 2 * steps,
+        "clocks": clocks.summary(),
+    }
+
+
 def main():
     args = parse_args()
     rank, world, local, dist = dist_setup(args.gpus)
@@ -779,11 +872,11 @@ def main():
         return
     import torch
 
-    if args.workload in (CASCADE_WORKLOAD, APPEND_WORKLOAD, FP8_WORKLOAD):
+    if args.workload in (CASCADE_WORKLOAD, APPEND_WORKLOAD, FP8_WORKLOAD, GRAPH_WORKLOAD):
         if world != 1:
             raise SystemExit("this workload runs on one GPU")
         fn = {CASCADE_WORKLOAD: run_cascade, APPEND_WORKLOAD: run_kv_append,
-              FP8_WORKLOAD: run_fp8kv}[args.workload]
+              FP8_WORKLOAD: run_fp8kv, GRAPH_WORKLOAD: run_graph}[args.workload]
         print(json.dumps(fn(args)), flush=True)
         return
     res = run_ours(args, rank, world, local, dist)

@@ -356,6 +356,10 @@ ua_status unified_attention_no_alloc(const void *q, const void *k_cache, const v
  *                entries); sequences with no query tokens are allowed.
  *   max_total_q  the token capacity; the planner rejects a batch with
  *                cu_seqlens_q[num_seqs] > max_total_q.
+ *   max_seq_q    the most query tokens one sequence may have (0: max_total_q);
+ *                the planner rejects a longer sequence.  When max_seq_q x
+ *                (Hq / Hkv) <= 16 no row can need the prefill kernel and it
+ *                is not launched (a decode-only graph).
  *   kv_fp8       0: bf16 caches; 1: e4m3 caches with k_scale / v_scale as
  *                for unified_attention_fp8kv (head_size 128 only).
  *   workspace    ua_workspace_size_device_plan bytes, 256-byte aligned; laid
@@ -371,14 +375,34 @@ ua_status unified_attention_device_plan(const void *q, const void *k_cache, cons
                                         const int32_t *cu_seqlens_q, const int32_t *seqused_k,
                                         const int32_t *block_table, float softmax_scale,
                                         int32_t causal, void *out, float *lse, int32_t num_seqs,
-                                        int32_t max_total_q, int32_t num_q_heads,
+                                        int32_t max_total_q, int32_t max_seq_q, int32_t num_q_heads,
                                         int32_t num_kv_heads, int32_t head_size,
                                         int32_t block_size, int32_t num_blocks,
                                         int32_t block_table_stride, int32_t kv_fp8,
                                         float k_scale, float v_scale, void *workspace,
                                         size_t workspace_bytes, void *stream);
+/*
+ * unified_attention_device_planned -- unified_attention_device_plan without the
+ * planner: the decode and prefill kernels read the plan that an earlier
+ * unified_attention_device_plan or ua_device_plan_build call left in the same
+ * workspace for the same cu_seqlens_q / seqused_k (and the same capacities).
+ * The layers of one model step share their lengths, so one plan per step
+ * serves every layer's attention.  Same arguments; the metadata must be
+ * unchanged since the plan was built (nothing checks that).
+ */
+ua_status unified_attention_device_planned(const void *q, const void *k_cache,
+                                           const void *v_cache, const int32_t *cu_seqlens_q,
+                                           const int32_t *seqused_k, const int32_t *block_table,
+                                           float softmax_scale, int32_t causal, void *out,
+                                           float *lse, int32_t num_seqs, int32_t max_total_q,
+                                           int32_t max_seq_q, int32_t num_q_heads,
+                                           int32_t num_kv_heads, int32_t head_size,
+                                           int32_t block_size, int32_t num_blocks,
+                                           int32_t block_table_stride, int32_t kv_fp8,
+                                           float k_scale, float v_scale, void *workspace,
+                                           size_t workspace_bytes, void *stream);
 ua_status ua_workspace_size_device_plan(int32_t num_seqs, int32_t max_total_q,
-                                        int32_t num_q_heads, int32_t num_kv_heads,
+                                        int32_t max_seq_q, int32_t num_q_heads, int32_t num_kv_heads,
                                         int32_t head_size, int32_t block_size,
                                         int32_t block_table_stride, int32_t kv_fp8,
                                         size_t *bytes);
@@ -398,10 +422,11 @@ ua_status ua_workspace_size_device_plan(int32_t num_seqs, int32_t max_total_q,
  */
 ua_status ua_device_plan_build(const int32_t *cu_seqlens_q, const int32_t *seqused_k,
                                int32_t causal, int32_t num_seqs, int32_t max_total_q,
-                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                               int32_t max_seq_q, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
                                int32_t block_size, int32_t block_table_stride, int32_t kv_fp8,
                                void *workspace, size_t workspace_bytes, void *stream);
-ua_status ua_device_plan_layout(int32_t num_seqs, int32_t max_total_q, int32_t num_q_heads,
+ua_status ua_device_plan_layout(int32_t num_seqs, int32_t max_total_q, int32_t max_seq_q,
+                                int32_t num_q_heads,
                                 int32_t num_kv_heads, int32_t head_size, int32_t block_size,
                                 int32_t block_table_stride, int32_t kv_fp8, int32_t num_sms,
                                 int64_t *offsets, int32_t *caps);

@@ -28,7 +28,8 @@ SYMBOLS = ("unified_attention", "unified_attention_lse", "ua_merge_attn_states",
            "unified_attention_append", "unified_attention_fp8kv", "ua_workspace_size_fp8kv",
            "ua_workspace_size", "ua_status_string", "ua_device_status", "ua_plan_inspect",
            "ua_profile_enable", "ua_profile_read", "unified_attention_device_plan",
-           "ua_workspace_size_device_plan", "ua_device_plan_build", "ua_device_plan_layout")
+           "ua_workspace_size_device_plan", "ua_device_plan_build", "ua_device_plan_layout",
+           "unified_attention_device_planned")
 
 
 class UAError(RuntimeError):
@@ -94,16 +95,18 @@ def load_library():
         lib.ua_profile_read.restype = ctypes.c_int
         lib.unified_attention_device_plan.argtypes = [P, P, P, P, P, P, ctypes.c_float, I32, P, P,
                                                       I32, I32, I32, I32, I32, I32, I32, I32, I32,
-                                                      ctypes.c_float, ctypes.c_float, P,
+                                                      I32, ctypes.c_float, ctypes.c_float, P,
                                                       ctypes.c_size_t, P]
         lib.unified_attention_device_plan.restype = ctypes.c_int
-        lib.ua_workspace_size_device_plan.argtypes = [I32, I32, I32, I32, I32, I32, I32, I32,
+        lib.unified_attention_device_planned.argtypes = lib.unified_attention_device_plan.argtypes
+        lib.unified_attention_device_planned.restype = ctypes.c_int
+        lib.ua_workspace_size_device_plan.argtypes = [I32, I32, I32, I32, I32, I32, I32, I32, I32,
                                                       ctypes.POINTER(ctypes.c_size_t)]
         lib.ua_workspace_size_device_plan.restype = ctypes.c_int
-        lib.ua_device_plan_build.argtypes = [P, P, I32, I32, I32, I32, I32, I32, I32, I32, I32, P,
-                                             ctypes.c_size_t, P]
+        lib.ua_device_plan_build.argtypes = [P, P, I32, I32, I32, I32, I32, I32, I32, I32, I32, I32,
+                                             P, ctypes.c_size_t, P]
         lib.ua_device_plan_build.restype = ctypes.c_int
-        lib.ua_device_plan_layout.argtypes = [I32, I32, I32, I32, I32, I32, I32, I32, I32, P, P]
+        lib.ua_device_plan_layout.argtypes = [I32, I32, I32, I32, I32, I32, I32, I32, I32, I32, P, P]
         lib.ua_device_plan_layout.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -405,11 +408,12 @@ def _stream_handle(torch, device, stream):
 
 
 def workspace_size_device_plan(num_seqs, max_total_q, num_q_heads, num_kv_heads, head_size,
-                               block_table_stride, kv_fp8=False, block_size=16):
+                               block_table_stride, kv_fp8=False, block_size=16, max_seq_q=0):
     """Bytes of workspace ``unified_attention_device_plan`` needs for these capacities."""
     lib = load_library()
     need = ctypes.c_size_t(0)
-    _check(lib.ua_workspace_size_device_plan(int(num_seqs), int(max_total_q), int(num_q_heads),
+    _check(lib.ua_workspace_size_device_plan(int(num_seqs), int(max_total_q), int(max_seq_q),
+                                             int(num_q_heads),
                                              int(num_kv_heads), int(head_size), int(block_size),
                                              int(block_table_stride), int(bool(kv_fp8)),
                                              ctypes.byref(need)),
@@ -419,8 +423,8 @@ def workspace_size_device_plan(num_seqs, max_total_q, num_q_heads, num_kv_heads,
 
 def unified_attention_device_plan(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table,
                                   softmax_scale, causal=True, out=None, *, workspace, lse=None,
-                                  num_seqs=None, kv_fp8=False, k_scale=1.0, v_scale=1.0,
-                                  stream=None):
+                                  num_seqs=None, max_seq_q=0, kv_fp8=False, k_scale=1.0,
+                                  v_scale=1.0, stream=None, reuse_plan=False):
     """Attention planned on the GPU (``unified_attention_device_plan``): no host copies of
     the metadata, so the call can be captured in a CUDA graph and replayed after
     ``cu_seqlens_q`` / ``seqused_k`` / ``block_table`` / ``q`` are rewritten in place.
@@ -429,7 +433,12 @@ def unified_attention_device_plan(q, k_cache, v_cache, cu_seqlens_q, seqused_k, 
     capacity); k_cache / v_cache: bf16, or uint8 E4M3 codes with ``kv_fp8``; lse:
     optional float32 [max_total_q, Hq].  ``workspace``: a uint8 CUDA tensor of at least
     ``workspace_size_device_plan`` bytes, owned by the caller (a captured graph keeps
-    using it).  ``num_seqs`` defaults to ``seqused_k.shape[0]``.  Returns ``out``.
+    using it; size it with the same ``max_seq_q``).  ``num_seqs`` defaults to
+    ``seqused_k.shape[0]``; ``max_seq_q`` bounds one sequence's query tokens (0: the
+    capacity) -- with ``max_seq_q * Hq / Hkv <= 16`` the prefill kernel is not launched.
+    ``reuse_plan``: skip the planner and use the plan an earlier call left in
+    ``workspace`` for the same metadata (``unified_attention_device_planned``; e.g.
+    every layer after the first in one model step).  Returns ``out``.
     """
     import torch
 
@@ -456,10 +465,12 @@ def unified_attention_device_plan(q, k_cache, v_cache, cu_seqlens_q, seqused_k, 
         raise UAError(1, "lse must be a contiguous CUDA float32 tensor [max_total_q, Hq]")
     ns = int(seqused_k.shape[0]) if num_seqs is None else int(num_seqs)
     stride = int(block_table.shape[1]) if block_table.dim() == 2 else 0
-    rc = lib.unified_attention_device_plan(
+    fn = lib.unified_attention_device_planned if reuse_plan else lib.unified_attention_device_plan
+    rc = fn(
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), cu_seqlens_q.data_ptr(),
         seqused_k.data_ptr(), block_table.data_ptr(), float(softmax_scale), int(bool(causal)),
-        out.data_ptr(), None if lse is None else lse.data_ptr(), ns, max_total_q, hq, hk, d, bs,
+        out.data_ptr(), None if lse is None else lse.data_ptr(), ns, max_total_q, int(max_seq_q),
+        hq, hk, d, bs,
         nb, stride, int(bool(kv_fp8)), float(k_scale), float(v_scale), workspace.data_ptr(),
         workspace.numel(), _stream_handle(torch, q.device, stream))
     _check(rc, "unified_attention_device_plan")
@@ -467,7 +478,7 @@ def unified_attention_device_plan(q, k_cache, v_cache, cu_seqlens_q, seqused_k, 
 
 
 def device_plan(cu_seqlens_q, seqused_k, causal, num_q_heads, num_kv_heads, head_size,
-                block_table_stride, max_total_q, kv_fp8=False):
+                block_table_stride, max_total_q, kv_fp8=False, max_seq_q=0):
     """Run only the device planner on CUDA int32 metadata and read the plan back (synchronises).
 
     Returns a dict of numpy arrays: ``header`` (int64 dec_ctas, n_pieces, n_comb,
@@ -482,17 +493,19 @@ def device_plan(cu_seqlens_q, seqused_k, causal, num_q_heads, num_kv_heads, head
     dev = cu_seqlens_q.device
     ns = int(seqused_k.shape[0])
     nbytes = workspace_size_device_plan(ns, max_total_q, num_q_heads, num_kv_heads, head_size,
-                                        block_table_stride, kv_fp8)
+                                        block_table_stride, kv_fp8, max_seq_q=max_seq_q)
     ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=dev)
     props = torch.cuda.get_device_properties(dev)
     offs = np.zeros(8, np.int64)
     caps = np.zeros(8, np.int32)
-    _check(lib.ua_device_plan_layout(ns, int(max_total_q), int(num_q_heads), int(num_kv_heads),
+    _check(lib.ua_device_plan_layout(ns, int(max_total_q), int(max_seq_q), int(num_q_heads),
+                                     int(num_kv_heads),
                                      int(head_size), 16, int(block_table_stride),
                                      int(bool(kv_fp8)), props.multi_processor_count,
                                      _np_ptr(offs), _np_ptr(caps)), "ua_device_plan_layout")
     _check(lib.ua_device_plan_build(cu_seqlens_q.data_ptr(), seqused_k.data_ptr(),
-                                    int(bool(causal)), ns, int(max_total_q), int(num_q_heads),
+                                    int(bool(causal)), ns, int(max_total_q), int(max_seq_q),
+                                    int(num_q_heads),
                                     int(num_kv_heads), int(head_size), 16,
                                     int(block_table_stride), int(bool(kv_fp8)), ws.data_ptr(),
                                     ws.numel(), torch.cuda.current_stream(dev).cuda_stream),

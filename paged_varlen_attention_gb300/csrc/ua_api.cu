@@ -733,10 +733,10 @@ extern "C" ua_status unified_attention_fp8kv(
 namespace ua {
 
 // Host-side checks of a device-plan call's shapes; fills the workspace shape.
-static ua_status device_plan_shape(int32_t num_seqs, int32_t max_total_q, int32_t hq, int32_t hkv,
-                                   int32_t d, int32_t bs, int32_t bt_stride, int32_t kv_fp8,
-                                   int sms, DevPlanShape *s) {
-    if (num_seqs < 0 || max_total_q < 0 || hq <= 0 || hkv <= 0 || bt_stride < 0)
+static ua_status device_plan_shape(int32_t num_seqs, int32_t max_total_q, int32_t max_seq_q,
+                                   int32_t hq, int32_t hkv, int32_t d, int32_t bs,
+                                   int32_t bt_stride, int32_t kv_fp8, int sms, DevPlanShape *s) {
+    if (num_seqs < 0 || max_total_q < 0 || max_seq_q < 0 || hq <= 0 || hkv <= 0 || bt_stride < 0)
         return UA_ERR_INVALID_ARG;
     if (hq % hkv != 0 || (d != 64 && d != 128) || bs != kBlockSize) return UA_ERR_UNSUPPORTED;
     if (kv_fp8 && d != 128) return UA_ERR_UNSUPPORTED;
@@ -744,12 +744,15 @@ static ua_status device_plan_shape(int32_t num_seqs, int32_t max_total_q, int32_
     Problem pr = make_problem(nullptr, nullptr, 0, hq, hkv, d, bs, bt_stride, 1);
     s->num_seqs = num_seqs;
     s->max_total_q = max_total_q;
+    s->max_seq_q = (max_seq_q == 0 || max_seq_q > max_total_q) ? max_total_q : max_seq_q;
     s->hq = hq;
     s->hkv = hkv;
     s->d = d;
     s->bt_stride = bt_stride;
     s->hpu = (kv_fp8 && hkv % 2 == 0) ? 2 : 1;
-    s->prefill_ok = (kPrefillEnabled && !kv_fp8 && prefill_supports(pr)) ? 1 : 0;
+    // no sequence can fill more than one decode tile: the prefill kernel never has work
+    const bool can_prefill = (int64_t)s->max_seq_q * (hq / hkv) > kDecRows;
+    s->prefill_ok = (kPrefillEnabled && !kv_fp8 && can_prefill && prefill_supports(pr)) ? 1 : 0;
     s->num_sms = sms;
     return UA_OK;
 }
@@ -757,16 +760,19 @@ static ua_status device_plan_shape(int32_t num_seqs, int32_t max_total_q, int32_
 static ua_status run_attention_device_plan(
     const void *q, const void *k_cache, const void *v_cache, const int32_t *cu_seqlens_q,
     const int32_t *seqused_k, const int32_t *block_table, float softmax_scale, int32_t causal,
-    void *out, float *lse, int32_t num_seqs, int32_t max_total_q, int32_t num_q_heads,
-    int32_t num_kv_heads, int32_t head_size, int32_t block_size, int32_t num_blocks,
-    int32_t block_table_stride, int32_t kv_fp8, float k_scale, float v_scale, void *workspace,
-    size_t workspace_bytes, void *stream_ptr, bool plan_only) {
+    void *out, float *lse, int32_t num_seqs, int32_t max_total_q, int32_t max_seq_q,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+    int32_t num_blocks, int32_t block_table_stride, int32_t kv_fp8, float k_scale, float v_scale,
+    void *workspace, size_t workspace_bytes, void *stream_ptr, int mode) {
+    // mode 0: plan, then attend; 1: plan only; 2: attend with the plan already
+    // in the workspace (built by an earlier call on the same metadata)
+    const bool plan_only = mode == 1;
     DeviceState *ds = nullptr;
     ua_status st = device_state(&ds);
     if (st != UA_OK) return st;
     DevPlanShape shape{};
-    st = device_plan_shape(num_seqs, max_total_q, num_q_heads, num_kv_heads, head_size, block_size,
-                           block_table_stride, kv_fp8, ds->sms, &shape);
+    st = device_plan_shape(num_seqs, max_total_q, max_seq_q, num_q_heads, num_kv_heads, head_size,
+                           block_size, block_table_stride, kv_fp8, ds->sms, &shape);
     if (st != UA_OK) return st;
     if (!std::isfinite(softmax_scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
         return UA_ERR_INVALID_ARG;
@@ -824,8 +830,9 @@ static ua_status run_attention_device_plan(
     const float scale_log2 = softmax_scale * k_scale * 1.4426950408889634f;
 
     mark(0);
-    if (launch_device_plan(shape, L, cu_seqlens_q, seqused_k, causal, ws, ds->status, stream) !=
-        cudaSuccess)
+    if (mode == 0 &&
+        launch_device_plan(shape, L, cu_seqlens_q, seqused_k, causal, ws, ds->status, stream) !=
+            cudaSuccess)
         return UA_ERR_CUDA;
     mark(1);
     DecodeParams dp{};
@@ -884,11 +891,11 @@ static ua_status run_attention_device_plan(
         ds->ran[pslot][0] = true;
         ds->ran[pslot][1] = shape.prefill_ok != 0;
         ds->ran[pslot][2] = false;
-        ds->ran[pslot][3] = true;
+        ds->ran[pslot][3] = mode == 0;
         ds->launches[pslot][0] = 1;
         ds->launches[pslot][1] = shape.prefill_ok ? 1 : 0;
         ds->launches[pslot][2] = 0;
-        ds->launches[pslot][3] = 1;   // the planner kernel
+        ds->launches[pslot][3] = mode == 0 ? 1 : 0;   // the planner kernel
         ++ds->calls;
     }
     return UA_OK;
@@ -897,17 +904,17 @@ static ua_status run_attention_device_plan(
 }  // namespace ua
 
 extern "C" ua_status ua_workspace_size_device_plan(int32_t num_seqs, int32_t max_total_q,
-                                                   int32_t num_q_heads, int32_t num_kv_heads,
-                                                   int32_t head_size, int32_t block_size,
-                                                   int32_t block_table_stride, int32_t kv_fp8,
-                                                   size_t *bytes) {
+                                                   int32_t max_seq_q, int32_t num_q_heads,
+                                                   int32_t num_kv_heads, int32_t head_size,
+                                                   int32_t block_size, int32_t block_table_stride,
+                                                   int32_t kv_fp8, size_t *bytes) {
     if (!bytes) return UA_ERR_INVALID_ARG;
     DeviceState *ds = nullptr;
     ua_status st = device_state(&ds);
     if (st != UA_OK) return st;
     DevPlanShape shape{};
-    st = device_plan_shape(num_seqs, max_total_q, num_q_heads, num_kv_heads, head_size, block_size,
-                           block_table_stride, kv_fp8, ds->sms, &shape);
+    st = device_plan_shape(num_seqs, max_total_q, max_seq_q, num_q_heads, num_kv_heads, head_size,
+                           block_size, block_table_stride, kv_fp8, ds->sms, &shape);
     if (st != UA_OK) return st;
     const DevPlanLayout L = device_plan_layout(shape);
     if (!L.valid) return UA_ERR_UNSUPPORTED;
@@ -916,14 +923,16 @@ extern "C" ua_status ua_workspace_size_device_plan(int32_t num_seqs, int32_t max
 }
 
 extern "C" ua_status ua_device_plan_layout(int32_t num_seqs, int32_t max_total_q,
-                                           int32_t num_q_heads, int32_t num_kv_heads,
-                                           int32_t head_size, int32_t block_size,
-                                           int32_t block_table_stride, int32_t kv_fp8,
-                                           int32_t num_sms, int64_t *offsets, int32_t *caps) {
+                                           int32_t max_seq_q, int32_t num_q_heads,
+                                           int32_t num_kv_heads, int32_t head_size,
+                                           int32_t block_size, int32_t block_table_stride,
+                                           int32_t kv_fp8, int32_t num_sms, int64_t *offsets,
+                                           int32_t *caps) {
     if (!offsets || !caps || num_sms <= 0) return UA_ERR_INVALID_ARG;
     DevPlanShape shape{};
-    ua_status st = device_plan_shape(num_seqs, max_total_q, num_q_heads, num_kv_heads, head_size,
-                                     block_size, block_table_stride, kv_fp8, num_sms, &shape);
+    ua_status st = device_plan_shape(num_seqs, max_total_q, max_seq_q, num_q_heads, num_kv_heads,
+                                     head_size, block_size, block_table_stride, kv_fp8, num_sms,
+                                     &shape);
     if (st != UA_OK) return st;
     const DevPlanLayout L = device_plan_layout(shape);
     if (!L.valid) return UA_ERR_UNSUPPORTED;
@@ -938,27 +947,42 @@ extern "C" ua_status ua_device_plan_layout(int32_t num_seqs, int32_t max_total_q
 
 extern "C" ua_status ua_device_plan_build(const int32_t *cu_seqlens_q, const int32_t *seqused_k,
                                           int32_t causal, int32_t num_seqs, int32_t max_total_q,
-                                          int32_t num_q_heads, int32_t num_kv_heads,
-                                          int32_t head_size, int32_t block_size,
-                                          int32_t block_table_stride, int32_t kv_fp8,
-                                          void *workspace, size_t workspace_bytes, void *stream) {
+                                          int32_t max_seq_q, int32_t num_q_heads,
+                                          int32_t num_kv_heads, int32_t head_size,
+                                          int32_t block_size, int32_t block_table_stride,
+                                          int32_t kv_fp8, void *workspace, size_t workspace_bytes,
+                                          void *stream) {
     return ua::run_attention_device_plan(nullptr, nullptr, nullptr, cu_seqlens_q, seqused_k, nullptr,
                                          1.f, causal, nullptr, nullptr, num_seqs, max_total_q,
-                                         num_q_heads, num_kv_heads, head_size, block_size, 0,
+                                         max_seq_q, num_q_heads, num_kv_heads, head_size, block_size, 0,
                                          block_table_stride, kv_fp8, 1.f, 1.f, workspace,
-                                         workspace_bytes, stream, /*plan_only=*/true);
+                                         workspace_bytes, stream, /*mode=*/1);
 }
 
 extern "C" ua_status unified_attention_device_plan(
     const void *q, const void *k_cache, const void *v_cache, const int32_t *cu_seqlens_q,
     const int32_t *seqused_k, const int32_t *block_table, float softmax_scale, int32_t causal,
-    void *out, float *lse, int32_t num_seqs, int32_t max_total_q, int32_t num_q_heads,
-    int32_t num_kv_heads, int32_t head_size, int32_t block_size, int32_t num_blocks,
-    int32_t block_table_stride, int32_t kv_fp8, float k_scale, float v_scale, void *workspace,
-    size_t workspace_bytes, void *stream) {
+    void *out, float *lse, int32_t num_seqs, int32_t max_total_q, int32_t max_seq_q,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+    int32_t num_blocks, int32_t block_table_stride, int32_t kv_fp8, float k_scale, float v_scale,
+    void *workspace, size_t workspace_bytes, void *stream) {
     return ua::run_attention_device_plan(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table,
                                          softmax_scale, causal, out, lse, num_seqs, max_total_q,
-                                         num_q_heads, num_kv_heads, head_size, block_size,
+                                         max_seq_q, num_q_heads, num_kv_heads, head_size, block_size,
                                          num_blocks, block_table_stride, kv_fp8, k_scale, v_scale,
-                                         workspace, workspace_bytes, stream, /*plan_only=*/false);
+                                         workspace, workspace_bytes, stream, /*mode=*/0);
+}
+
+extern "C" ua_status unified_attention_device_planned(
+    const void *q, const void *k_cache, const void *v_cache, const int32_t *cu_seqlens_q,
+    const int32_t *seqused_k, const int32_t *block_table, float softmax_scale, int32_t causal,
+    void *out, float *lse, int32_t num_seqs, int32_t max_total_q, int32_t max_seq_q,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+    int32_t num_blocks, int32_t block_table_stride, int32_t kv_fp8, float k_scale, float v_scale,
+    void *workspace, size_t workspace_bytes, void *stream) {
+    return ua::run_attention_device_plan(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table,
+                                         softmax_scale, causal, out, lse, num_seqs, max_total_q,
+                                         max_seq_q, num_q_heads, num_kv_heads, head_size, block_size,
+                                         num_blocks, block_table_stride, kv_fp8, k_scale, v_scale,
+                                         workspace, workspace_bytes, stream, /*mode=*/2);
 }

@@ -618,6 +618,9 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, 2)
                     __threadfence();
                     merge_unit<D>(p, q0, pc.kvh, pc.row0, pc.nrows, hp, pc.slot0, pc.nslots, tid,
                                   C::kConsumerWarps * 32);
+                    // every piece has arrived: nothing else touches the counter in this
+                    // launch; zero it for the next launch that reuses the plan
+                    if (tid == 0) p.comb_count[pc.comb] = 0;
                 }
             }
             named_barrier_sync(1, C::kConsumerWarps * 32);

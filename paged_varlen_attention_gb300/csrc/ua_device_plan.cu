@@ -30,6 +30,11 @@ namespace ua {
 namespace {
 
 constexpr int kPlanThreads = 1024;
+// The scratch arrays move into shared memory when they fit (most batches):
+// the planner is a chain of dependent lookups, which then cost shared-memory
+// rather than L2 latency.
+constexpr size_t kPlanSmemMax = 192 * 1024;
+constexpr int kPlanMaxGrid = 1024;    // decode CTAs the planner can partition over
 
 struct UnitRec {          // one decode unit (a run of one or two kv heads' pages)
     int32_t seq, kvh, row0, nrows, pages, npieces, comb, slot0;
@@ -113,7 +118,7 @@ __device__ int last_le(const T *a, int n, T x) {
 struct PlanArgs {
     const int32_t *cu;
     const int32_t *lk;
-    int32_t num_seqs, max_total_q, hq, hkv, g, bt_stride, hpu, prefill_ok, num_sms, causal;
+    int32_t num_seqs, max_total_q, max_seq_q, hq, hkv, g, bt_stride, hpu, prefill_ok, num_sms, causal;
     int32_t dec_grid, cap_units, cap_items, cap_pieces, cap_comb, cap_slots, n_buckets;
     long long *header;
     int32_t *cta_begin;       // [dec_grid + 1]
@@ -131,6 +136,7 @@ struct PlanArgs {
     int32_t *ikey;            // [cap_items]
     int32_t *hist;            // [n_buckets]
     int32_t *tmp;             // [max(cap_units, dec_grid) + 1]
+    uint32_t smem_bytes;      // dynamic shared memory for scratch arrays that fit
     int *status;
 };
 
@@ -141,10 +147,30 @@ __device__ void empty_plan(const PlanArgs &a, long long err) {
     if (threadIdx.x == 0 && err) record_status(a.status, UA_DEVICE_BAD_METADATA_BIT);
 }
 
-__global__ void __launch_bounds__(kPlanThreads, 1) ua_plan_kernel(const PlanArgs a) {
+__global__ void __launch_bounds__(kPlanThreads, 1) ua_plan_kernel(const PlanArgs args) {
+    extern __shared__ __align__(16) uint8_t plan_smem[];
+    // Scratch arrays that fit go to shared memory (generic pointers reach both;
+    // the decisions depend only on counts every thread knows).
+    PlanArgs a = args;
+    size_t sm_used = 0;
+    auto carve = [&](size_t bytes) -> uint8_t * {
+        uint8_t *p = plan_smem + sm_used;
+        sm_used = (sm_used + bytes + 15) & ~size_t(15);
+        return p;
+    };
+    if (8 * ((size_t)a.num_seqs + 1) <= a.smem_bytes) {
+        a.seq_u = reinterpret_cast<int32_t *>(carve(4 * ((size_t)a.num_seqs + 1)));
+        a.seq_i = reinterpret_cast<int32_t *>(carve(4 * ((size_t)a.num_seqs + 1)));
+    }
     __shared__ long long s_red[32];
     __shared__ int32_t s_part32[32];
     __shared__ long long s_part64[32];
+    // decode CTA c: pages [s_clo[c], s_clo[c + 1]), units s_uf[c] .. s_ul[c],
+    // pieces from s_cb[c]
+    __shared__ long long s_clo[kPlanMaxGrid + 1];
+    __shared__ int32_t s_uf[kPlanMaxGrid];
+    __shared__ int32_t s_ul[kPlanMaxGrid];
+    __shared__ int32_t s_cb[kPlanMaxGrid + 1];
     const int tid = threadIdx.x, nt = blockDim.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int ns = a.num_seqs;
@@ -155,7 +181,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) ua_plan_kernel(const PlanArgs
     for (int s = tid; s < ns; s += nt) {
         const long long lq = (long long)a.cu[s + 1] - a.cu[s];
         const long long lk = a.lk[s];
-        if (lq < 0 || lk < 0 || (lq > 0 && lk == 0) || (a.causal && lk < lq) ||
+        if (lq < 0 || lq > a.max_seq_q || lk < 0 || (lq > 0 && lk == 0) || (a.causal && lk < lq) ||
             (lk + kBlockSize - 1) / kBlockSize > a.bt_stride || lq * a.g > INT32_MAX / 2) {
             err = 1;
             continue;
@@ -196,6 +222,20 @@ __global__ void __launch_bounds__(kPlanThreads, 1) ua_plan_kernel(const PlanArgs
     if (n_units > a.cap_units || n_items > a.cap_items) {
         empty_plan(a, 2);
         return;
+    }
+    {
+        const size_t nb = (size_t)a.n_buckets, nu = (size_t)n_units, ni = (size_t)n_items;
+        const size_t need = 16 * 8 + sizeof(UnitRec) * nu + 8 * (nu + 1) + sizeof(PreTile) * ni + 4 * ni +
+                            4 * nb + 4 * (max(nu, (size_t)a.dec_grid) + 1);
+        if (sm_used + need <= a.smem_bytes) {
+            a.urec = reinterpret_cast<UnitRec *>(carve(sizeof(UnitRec) * nu));
+            sm_used = (sm_used + 7) & ~size_t(7);
+            a.ustart = reinterpret_cast<long long *>(carve(8 * (nu + 1)));
+            a.irec = reinterpret_cast<PreTile *>(carve(sizeof(PreTile) * ni));
+            a.ikey = reinterpret_cast<int32_t *>(carve(4 * ni));
+            a.hist = reinterpret_cast<int32_t *>(carve(4 * nb));
+            a.tmp = reinterpret_cast<int32_t *>(carve(4 * (max(nu, (size_t)a.dec_grid) + 1)));
+        }
     }
 
     // ---- units (order: sequence, row tile, kv head) and their page counts
@@ -248,15 +288,21 @@ __global__ void __launch_bounds__(kPlanThreads, 1) ua_plan_kernel(const PlanArgs
         const long long P = total_pages;
         dec_ctas = (int)min((long long)a.dec_grid, P);
         const int C = dec_ctas;
-        // pieces per CTA: the units its range touches
-        for (int c = tid; c < C; c += nt) {
-            const long long lo = P * c / C, hi = P * (c + 1) / C;
-            a.cta_begin[c] = last_le(a.ustart, n_units, hi - 1) - last_le(a.ustart, n_units, lo) + 1;
-        }
-        if (tid == 0) a.cta_begin[C] = 0;
+        // the CTAs' page ranges (the only 64-bit divisions), first and last units,
+        // and pieces per CTA: the units its range touches
+        for (int c = tid; c <= C; c += nt) s_clo[c] = P * c / C;
         __syncthreads();
-        n_pieces = block_scan(a.cta_begin, C + 1, s_part32);
-        for (int c = C + 1 + tid; c <= a.dec_grid; c += nt) a.cta_begin[c] = n_pieces;
+        for (int c = tid; c < C; c += nt) {
+            const int uf = last_le(a.ustart, n_units, s_clo[c]);
+            const int ul = last_le(a.ustart, n_units, s_clo[c + 1] - 1);
+            s_uf[c] = uf;
+            s_ul[c] = ul;
+            s_cb[c] = ul - uf + 1;
+        }
+        if (tid == 0) s_cb[C] = 0;
+        __syncthreads();
+        n_pieces = block_scan(s_cb, C + 1, s_part32);
+        for (int c = tid; c <= a.dec_grid; c += nt) a.cta_begin[c] = c <= C ? s_cb[c] : n_pieces;
         if (n_pieces > a.cap_pieces) {
             empty_plan(a, 2);
             return;
@@ -264,10 +310,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) ua_plan_kernel(const PlanArgs
         // pieces per unit: the CTAs its pages fall in; split units get a combine
         // entry and consecutive partial slots, in unit order
         for (int u = tid; u < n_units; u += nt) {
-            const long long st = a.ustart[u], en = a.ustart[u + 1];
-            const long long cf = ((st + 1) * C + P - 1) / P - 1;   // CTA holding page st
-            const long long cl = (en * C + P - 1) / P - 1;         // CTA holding page en - 1
-            const int np = (int)(cl - cf + 1);
+            const int cf = last_le(s_clo, C, a.ustart[u]);            // CTA holding its first page
+            const int cl = last_le(s_clo, C, a.ustart[u + 1] - 1);    // and its last
+            const int np = cl - cf + 1;
             a.urec[u].npieces = np;
             a.urec[u].comb = np > 1 ? 1 : 0;
             a.urec[u].slot0 = np > 1 ? np : 0;
@@ -296,15 +341,13 @@ __global__ void __launch_bounds__(kPlanThreads, 1) ua_plan_kernel(const PlanArgs
         for (int u = tid; u < n_units; u += nt) {
             const UnitRec r = a.urec[u];
             const long long st = a.ustart[u], en = a.ustart[u + 1];
-            const long long cf = ((st + 1) * C + P - 1) / P - 1;
+            const int cf = last_le(s_clo, C, st);
             for (int k = 0; k < r.npieces; ++k) {
-                const int c = (int)cf + k;
-                const long long lo = P * c / C, hi = P * (c + 1) / C;
-                const int uf = k == 0 ? last_le(a.ustart, n_units, lo) : u;
-                const int ul = last_le(a.ustart, n_units, hi - 1);
-                const int n = a.cta_begin[c + 1] - a.cta_begin[c];
-                int pos = u - uf;
-                if (n > 1 && a.urec[ul].npieces > 1) pos = (pos + 1) % n;
+                const int c = cf + k;
+                const long long lo = s_clo[c], hi = s_clo[c + 1];
+                const int n = s_cb[c + 1] - s_cb[c];
+                int pos = u - s_uf[c];
+                if (n > 1 && a.urec[s_ul[c]].npieces > 1) pos = pos + 1 == n ? 0 : pos + 1;
                 DecPiece pc;
                 pc.seq = r.seq;
                 pc.kvh = r.kvh;
@@ -314,7 +357,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) ua_plan_kernel(const PlanArgs
                 pc.page_end = (int32_t)(min(hi, en) - st);
                 pc.slot = r.npieces > 1 ? r.slot0 + k : -1;
                 pc.unit = r.comb;
-                a.pieces[a.cta_begin[c] + pos] = pc;
+                a.pieces[s_cb[c] + pos] = pc;
             }
             if (r.npieces > 1) {
                 CombUnit cu;
@@ -420,7 +463,8 @@ DevPlanLayout device_plan_layout(const DevPlanShape &s) {
     // keys of a sequence <= bt_stride * kBlockSize, so kv_tiles <= that / kKvTile rounded up
     const int64_t buckets = ((int64_t)s.bt_stride * kBlockSize + kKvTile - 1) / kKvTile + 2;
     // the planner counts in 32-bit integers
-    L.valid = units + L.dec_grid < INT32_MAX / 4 && items < INT32_MAX / 4 && buckets < INT32_MAX / 4;
+    L.valid = units + L.dec_grid < INT32_MAX / 4 && items < INT32_MAX / 4 &&
+              buckets < INT32_MAX / 4 && L.dec_grid <= kPlanMaxGrid;
     if (!L.valid) return L;
     L.cap_units = (int32_t)units;
     L.cap_items = (int32_t)items;
@@ -467,6 +511,7 @@ cudaError_t launch_device_plan(const DevPlanShape &s, const DevPlanLayout &L, co
     a.lk = seqused_k;
     a.num_seqs = s.num_seqs;
     a.max_total_q = s.max_total_q;
+    a.max_seq_q = s.max_seq_q;
     a.hq = s.hq;
     a.hkv = s.hkv;
     a.g = s.hq / s.hkv;
@@ -504,7 +549,17 @@ cudaError_t launch_device_plan(const DevPlanShape &s, const DevPlanLayout &L, co
     a.hist = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * (size_t)L.n_buckets));
     a.tmp = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * ((size_t)std::max(L.cap_units, L.dec_grid) + 1)));
     a.status = status;
-    ua_plan_kernel<<<1, kPlanThreads, 0, stream>>>(a);
+    a.smem_bytes = (uint32_t)kPlanSmemMax;
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        const cudaError_t e = cudaFuncSetAttribute(ua_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)kPlanSmemMax);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    ua_plan_kernel<<<1, kPlanThreads, kPlanSmemMax, stream>>>(a);
     return cudaGetLastError();
 }
 

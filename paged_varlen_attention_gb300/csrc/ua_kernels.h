@@ -28,7 +28,8 @@ struct DecodeParams {
     float *part_o;               // [slots][kDecRows][d]
     float *part_ml;              // [slots][kDecRows][2]: running max (log2 domain), sum
     const CombUnit *comb;        // plan: split units
-    int32_t *comb_count;         // plan: partials written per split unit (zero at launch)
+    int32_t *comb_count;         // plan: partials written per split unit (zero at launch; the
+                                 // merging CTA zeroes it again, so a reused plan stays valid)
     float *lse;                  // optional [total_q, Hq]: natural-log normaliser per row
     float v_scale;               // scale of the V values (fp8 cache; 1 otherwise)
     int32_t heads_per_unit;      // e4m3 pages: kv heads per unit (tile rows 8j.. are head kvh + j)
@@ -81,12 +82,14 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
 
 // ---- plan built on the device (ua_device_plan.cu)
 // What a device-plan workspace is laid out for: the batch's sequence count,
-// the query-token capacity of q / out, the heads, head size, block-table
-// width, kv heads per decode unit, whether the prefill kernel may take rows,
-// and the SM count (decode grid kDecCtasPerSm * num_sms, prefill grid num_sms).
+// the query-token capacity of q / out, the longest query of one sequence, the
+// heads, head size, block-table width, kv heads per decode unit, whether the
+// prefill kernel may take rows, and the SM count (decode grid
+// kDecCtasPerSm * num_sms, prefill grid num_sms).
 struct DevPlanShape {
     int32_t num_seqs;
     int32_t max_total_q;
+    int32_t max_seq_q;     // query tokens of one sequence at most
     int32_t hq;
     int32_t hkv;
     int32_t d;

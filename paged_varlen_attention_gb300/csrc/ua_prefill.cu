@@ -250,6 +250,9 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // a CTA of a fixed grid (plan built on the device) may have no item: it
+    // leaves before touching barriers or TMEM (the same answer for every thread)
+    if (p.tile_begin[blockIdx.x] == p.tile_begin[blockIdx.x + 1]) return;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {

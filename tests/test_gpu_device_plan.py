@@ -262,3 +262,61 @@ def test_bad_metadata_is_reported_and_nothing_runs():
                                      dev["seqused_k"], dev["block_table"], 0.125, True,
                                      out=torch.empty_like(q_big), workspace=ws)
     assert ua.device_status() == ua._binding.DEVICE_BAD_METADATA
+
+
+def test_decode_only_graph_skips_the_prefill_kernel():
+    """max_seq_q * G <= 16: only the planner and the decode kernel run; a longer
+    sequence is rejected as bad metadata."""
+    import torch
+    import paged_varlen_attention_gb300 as ua
+
+    spec = W.custom_spec([1] * 6, [40, 900, 3, 1500, 17, 64], 32, 8, 128, seed=21)
+    b = W.materialize(spec, poison=True)
+    dev = to_device(b)
+    ws = torch.empty(ua.workspace_size_device_plan(6, 6, 32, 8, 128, b.block_table_stride,
+                                                   max_seq_q=1), dtype=torch.uint8, device="cuda")
+    ua.profile_enable(True)
+    try:
+        out = ua.unified_attention_device_plan(dev["q"], dev["k_cache"], dev["v_cache"],
+                                               dev["cu_seqlens_q"], dev["seqused_k"],
+                                               dev["block_table"], spec.softmax_scale, True,
+                                               workspace=ws, max_seq_q=1)
+        ms, launches = ua.profile_read(0)
+    finally:
+        ua.profile_enable(False)
+    assert launches[1] == 0 and launches[0] == 1 and launches[3] == 1   # no prefill launch
+    ref, _ = oracle.attention_batch(b)
+    assert_close(out.float().cpu().numpy().astype(np.float64), ref, "decode-only device plan")
+    # a two-token sequence exceeds max_seq_q = 1
+    cu2 = _i32([0, 1, 2, 3, 4, 6, 6])
+    ua.device_status()
+    ua.unified_attention_device_plan(dev["q"], dev["k_cache"], dev["v_cache"], cu2,
+                                     dev["seqused_k"], dev["block_table"], spec.softmax_scale,
+                                     True, workspace=ws, max_seq_q=1)
+    assert ua.device_status() == ua._binding.DEVICE_BAD_METADATA
+
+
+def test_plan_built_once_serves_several_calls():
+    """Layers of one step share their lengths: one planner run, then calls with
+    reuse_plan (no planner launch) on other queries / caches give their own results."""
+    import torch
+    import paged_varlen_attention_gb300 as ua
+
+    spec = W.custom_spec([1, 1, 70, 1], [300, 1200, 70, 33], 16, 4, 128, seed=31)
+    layers = [W.materialize(W.custom_spec(spec.q_lens, spec.k_lens, 16, 4, 128, seed=31 + i),
+                            poison=True) for i in range(3)]
+    dev0 = to_device(layers[0])
+    ws = torch.empty(ua.workspace_size_device_plan(4, dev0["q"].shape[0], 16, 4, 128,
+                                                   layers[0].block_table_stride),
+                     dtype=torch.uint8, device="cuda")
+    for i, b in enumerate(layers):
+        dev = to_device(b)
+        # every layer has its own cache and page placement but the same lengths;
+        # the plan depends only on the lengths
+        out = ua.unified_attention_device_plan(dev["q"], dev["k_cache"], dev["v_cache"],
+                                               dev0["cu_seqlens_q"], dev0["seqused_k"],
+                                               dev["block_table"], spec.softmax_scale, True,
+                                               workspace=ws, reuse_plan=i > 0)
+        torch.cuda.synchronize()
+        ref, _ = oracle.attention_batch(b)
+        assert_close(out.float().cpu().numpy().astype(np.float64), ref, f"layer {i}")
