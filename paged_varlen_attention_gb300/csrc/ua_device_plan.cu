@@ -21,6 +21,7 @@
 // plan is a deterministic function of the metadata (no atomics decide an
 // order).
 #include <algorithm>
+#include <climits>
 
 #include "ua_device.cuh"
 #include "ua_kernels.h"
@@ -80,27 +81,100 @@ __device__ T block_scan(T *v, int n, T *s_part) {
     return total;
 }
 
-// Block-wide reductions (every thread gets the result).
-__device__ long long block_sum(long long v, long long *s_red) {
+// Two exclusive prefix sums (int32) in one pass; returns both totals.
+__device__ int2 block_scan2(int32_t *v, int32_t *w2, int n, int32_t *s_part /* [64] */) {
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, nw = blockDim.x >> 5;
+    const int per = (n + blockDim.x - 1) / blockDim.x;
+    const int b = min(n, tid * per), e = min(n, b + per);
+    int s1 = 0, s2 = 0;
+    for (int i = b; i < e; ++i) {
+        s1 += v[i];
+        s2 += w2[i];
+    }
+    int x1 = s1, x2 = s2;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = v;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y1 = __shfl_up_sync(0xffffffffu, x1, o), y2 = __shfl_up_sync(0xffffffffu, x2, o);
+        if (lane >= o) {
+            x1 += y1;
+            x2 += y2;
+        }
+    }
+    if (lane == 31) {
+        s_part[w] = x1;
+        s_part[32 + w] = x2;
+    }
     __syncthreads();
-    long long t = 0;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += s_red[i];
+    if (w == 0) {
+        int t1 = lane < nw ? s_part[lane] : 0, t2 = lane < nw ? s_part[32 + lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y1 = __shfl_up_sync(0xffffffffu, t1, o), y2 = __shfl_up_sync(0xffffffffu, t2, o);
+            if (lane >= o) {
+                t1 += y1;
+                t2 += y2;
+            }
+        }
+        s_part[lane] = t1;
+        s_part[32 + lane] = t2;
+    }
     __syncthreads();
-    return t;
+    const int2 total = make_int2(s_part[nw - 1], s_part[32 + nw - 1]);
+    int b1 = (w > 0 ? s_part[w - 1] : 0) + x1 - s1, b2 = (w > 0 ? s_part[32 + w - 1] : 0) + x2 - s2;
+    for (int i = b; i < e; ++i) {
+        const int t1 = v[i], t2 = w2[i];
+        v[i] = b1;
+        w2[i] = b2;
+        b1 += t1;
+        b2 += t2;
+    }
+    __syncthreads();
+    return total;
+}
+
+// Block-wide reductions (every thread gets the result): warps reduce with
+// shuffles, warp 0 reduces the warps' values, one shared slot broadcasts.
+// block_sum_max2 returns (sum of a, max of b, max of c) in one pass.
+__device__ void block_sum_max2(long long &a, long long &b, long long &c, long long *s_red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, o);
+        b = max(b, (long long)__shfl_xor_sync(0xffffffffu, b, o));
+        c = max(c, (long long)__shfl_xor_sync(0xffffffffu, c, o));
+    }
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    if (lane == 0) {
+        s_red[w] = a;
+        s_red[32 + w] = b;
+        s_red[64 + w] = c;
+    }
+    __syncthreads();
+    if (w == 0) {
+        long long x = lane < nw ? s_red[lane] : 0, y = lane < nw ? s_red[32 + lane] : LLONG_MIN,
+                  z = lane < nw ? s_red[64 + lane] : LLONG_MIN;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            x += __shfl_xor_sync(0xffffffffu, x, o);
+            y = max(y, (long long)__shfl_xor_sync(0xffffffffu, y, o));
+            z = max(z, (long long)__shfl_xor_sync(0xffffffffu, z, o));
+        }
+        if (lane == 0) {
+            s_red[96] = x;
+            s_red[97] = y;
+            s_red[98] = z;
+        }
+    }
+    __syncthreads();
+    a = s_red[96];
+    b = s_red[97];
+    c = s_red[98];
+    __syncthreads();   // s_red free for the next reduction
 }
 
 __device__ long long block_max(long long v, long long *s_red) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = max(v, (long long)__shfl_xor_sync(0xffffffffu, v, o));
-    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    long long t = s_red[0];
-    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) t = max(t, s_red[i]);
-    __syncthreads();
-    return t;
+    long long zero = 0, dummy = LLONG_MIN;
+    block_sum_max2(zero, v, dummy, s_red);
+    return v;
 }
 
 // Last index i in [0, n) with a[i] <= x (a non-decreasing, a[0] <= x).
@@ -136,6 +210,7 @@ struct PlanArgs {
     int32_t *ikey;            // [cap_items]
     int32_t *hist;            // [n_buckets]
     int32_t *tmp;             // [max(cap_units, dec_grid) + 1]
+    int32_t *tmp2;            // [max(cap_units, dec_grid) + 1]
     uint32_t smem_bytes;      // dynamic shared memory for scratch arrays that fit
     int *status;
 };
@@ -162,8 +237,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) ua_plan_kernel(const PlanArgs
         a.seq_u = reinterpret_cast<int32_t *>(carve(4 * ((size_t)a.num_seqs + 1)));
         a.seq_i = reinterpret_cast<int32_t *>(carve(4 * ((size_t)a.num_seqs + 1)));
     }
-    __shared__ long long s_red[32];
-    __shared__ int32_t s_part32[32];
+    __shared__ long long s_red[100];
+    __shared__ int32_t s_part32[64];
     __shared__ long long s_part64[32];
     // decode CTA c: pages [s_clo[c], s_clo[c + 1]), units s_uf[c] .. s_ul[c],
     // pieces from s_cb[c]
@@ -192,13 +267,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) ua_plan_kernel(const PlanArgs
             max_steps = max(max_steps, (lk + 63) / 64);
         }
     }
-    err = block_max(err, s_red);
+    block_sum_max2(items, err, max_steps, s_red);
     if (err) {
         empty_plan(a, 1);
         return;
     }
-    items = block_sum(items, s_red);
-    max_steps = block_max(max_steps, s_red);
     const bool pre_on =
         a.prefill_ok && !(items > 0 && items * 4 < max(a.num_sms, 1) && max_steps >= 32);
     const int step = kDecRows / a.hpu;        // rows per decode unit and kv head
@@ -217,8 +290,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) ua_plan_kernel(const PlanArgs
         a.seq_i[ns] = 0;
     }
     __syncthreads();
-    const int n_units = block_scan(a.seq_u, ns + 1, s_part32);
-    const int n_items = block_scan(a.seq_i, ns + 1, s_part32);
+    const int2 tot = block_scan2(a.seq_u, a.seq_i, ns + 1, s_part32);
+    const int n_units = tot.x, n_items = tot.y;
     if (n_units > a.cap_units || n_items > a.cap_items) {
         empty_plan(a, 2);
         return;
@@ -226,7 +299,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) ua_plan_kernel(const PlanArgs
     {
         const size_t nb = (size_t)a.n_buckets, nu = (size_t)n_units, ni = (size_t)n_items;
         const size_t need = 16 * 8 + sizeof(UnitRec) * nu + 8 * (nu + 1) + sizeof(PreTile) * ni + 4 * ni +
-                            4 * nb + 4 * (max(nu, (size_t)a.dec_grid) + 1);
+                            4 * nb + 8 * (max(nu, (size_t)a.dec_grid) + 1);
         if (sm_used + need <= a.smem_bytes) {
             a.urec = reinterpret_cast<UnitRec *>(carve(sizeof(UnitRec) * nu));
             sm_used = (sm_used + 7) & ~size_t(7);
@@ -235,6 +308,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) ua_plan_kernel(const PlanArgs
             a.ikey = reinterpret_cast<int32_t *>(carve(4 * ni));
             a.hist = reinterpret_cast<int32_t *>(carve(4 * nb));
             a.tmp = reinterpret_cast<int32_t *>(carve(4 * (max(nu, (size_t)a.dec_grid) + 1)));
+            a.tmp2 = reinterpret_cast<int32_t *>(carve(4 * (max(nu, (size_t)a.dec_grid) + 1)));
         }
     }
 
@@ -318,19 +392,25 @@ __global__ void __launch_bounds__(kPlanThreads, 1) ua_plan_kernel(const PlanArgs
             a.urec[u].slot0 = np > 1 ? np : 0;
         }
         __syncthreads();
-        // scans over the comb flags and the split units' piece counts (strided
-        // fields of urec: go through the scratch array)
-        for (int u = tid; u < n_units; u += nt) a.tmp[u] = a.urec[u].comb;
-        if (tid == 0) a.tmp[n_units] = 0;
+        // one pass of scans over the split flags and the split units' piece
+        // counts (urec's fields are strided: copy them to two arrays)
+        for (int u = tid; u < n_units; u += nt) {
+            a.tmp[u] = a.urec[u].comb;
+            a.tmp2[u] = a.urec[u].slot0;
+        }
+        if (tid == 0) {
+            a.tmp[n_units] = 0;
+            a.tmp2[n_units] = 0;
+        }
         __syncthreads();
-        n_comb = block_scan(a.tmp, n_units + 1, s_part32);
-        for (int u = tid; u < n_units; u += nt) a.urec[u].comb = a.urec[u].npieces > 1 ? a.tmp[u] : -1;
-        __syncthreads();
-        for (int u = tid; u < n_units; u += nt) a.tmp[u] = a.urec[u].slot0;
-        if (tid == 0) a.tmp[n_units] = 0;
-        __syncthreads();
-        n_slots = block_scan(a.tmp, n_units + 1, s_part32);
-        for (int u = tid; u < n_units; u += nt) a.urec[u].slot0 = a.urec[u].npieces > 1 ? a.tmp[u] : -1;
+        const int2 cs = block_scan2(a.tmp, a.tmp2, n_units + 1, s_part32);
+        n_comb = cs.x;
+        n_slots = cs.y;
+        for (int u = tid; u < n_units; u += nt) {
+            const bool split = a.urec[u].npieces > 1;
+            a.urec[u].comb = split ? a.tmp[u] : -1;
+            a.urec[u].slot0 = split ? a.tmp2[u] : -1;
+        }
         __syncthreads();
         if (n_comb > a.cap_comb || n_slots > a.cap_slots) {
             empty_plan(a, 2);
@@ -498,6 +578,7 @@ DevPlanLayout device_plan_layout(const DevPlanShape &s) {
     take(sizeof(int32_t) * (size_t)L.cap_items);                        // ikey
     take(sizeof(int32_t) * (size_t)L.n_buckets);                        // hist
     take(sizeof(int32_t) * ((size_t)std::max(L.cap_units, L.dec_grid) + 1));   // tmp
+    take(sizeof(int32_t) * ((size_t)std::max(L.cap_units, L.dec_grid) + 1));   // tmp2
     L.total_bytes = off;
     return L;
 }
@@ -548,6 +629,7 @@ cudaError_t launch_device_plan(const DevPlanShape &s, const DevPlanLayout &L, co
     a.ikey = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * (size_t)L.cap_items));
     a.hist = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * (size_t)L.n_buckets));
     a.tmp = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * ((size_t)std::max(L.cap_units, L.dec_grid) + 1)));
+    a.tmp2 = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * ((size_t)std::max(L.cap_units, L.dec_grid) + 1)));
     a.status = status;
     a.smem_bytes = (uint32_t)kPlanSmemMax;
     static thread_local int configured_device = -1;
