@@ -415,9 +415,21 @@ def run_reference(args, rank, world):
 
     if rank != 0:
         return None
-    idx = WORKLOADS[args.workload]
+    if args.workload in (CASCADE_WORKLOAD, APPEND_WORKLOAD):
+        raise SystemExit(f"--impl reference times the attention workloads; {args.workload} "
+                         "is not one (its parts are timed by the attention workloads)")
+    fp8 = args.workload == FP8_WORKLOAD
+    # the graph and fp8 workloads compute attention over the headline batch
+    idx = WORKLOADS.get(args.workload, WORKLOADS[DEFAULT_WORKLOAD])
     b = W.config_batch(idx, poison=False)
     s = b.spec
+    if fp8:
+        k8, v8 = W.fp8_caches(b, 0.05, 0.05)
+
+    def ref_attention(q, cu, sk, bt):
+        if fp8:
+            return oracle.attention_fp8kv(q, k8, v8, 0.05, 0.05, cu, sk, bt, s.softmax_scale, s.causal)
+        return oracle.attention(q, b.k_cache, b.v_cache, cu, sk, bt, s.softmax_scale, s.causal)
     # per step: a rotating window of sequences sized to a few tenths of a second
     per_step = max(1, min(s.num_seqs, 8 if idx in (1, 2) else 2))
     if idx == 1:
@@ -432,12 +444,12 @@ def run_reference(args, rank, world):
 
     for w in range(args.warmup):
         q, cu, sk, bt, _ = sub_batch(w * per_step)
-        oracle.attention(q, b.k_cache, b.v_cache, cu, sk, bt, s.softmax_scale, s.causal)
+        ref_attention(q, cu, sk, bt)
     tokens = 0
     t0 = time.perf_counter()
     for k in range(args.steps):
         q, cu, sk, bt, nt = sub_batch(k * per_step)
-        oracle.attention(q, b.k_cache, b.v_cache, cu, sk, bt, s.softmax_scale, s.causal)
+        ref_attention(q, cu, sk, bt)
         tokens += nt
     dt = time.perf_counter() - t0
     value = tokens / dt
@@ -445,7 +457,8 @@ def run_reference(args, rank, world):
               f"{tokens} query tokens over {args.steps} steps, fp64 C oracle with OpenMP")
     return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64 (e4m3 kv)" if fp8 else "f64",
             "data": "synthetic", "impl": "reference",
             "config": {"workload": args.workload, "num_seqs": s.num_seqs,
                        "q_tokens": s.total_q, "parallelism": "host cores"},

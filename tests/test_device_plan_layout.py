@@ -1,0 +1,87 @@
+"""Host logic of the device-planned call (no GPU): ua_device_plan_layout checks
+the shapes and lays the workspace out for the capacities.
+
+The capacities bound every batch that fits them: a sequence of Lq tokens makes
+ceil(Lq * G / step) row tiles (step = 16 rows, or 8 per head when a unit holds
+two kv heads), so at most Lq * G / step + 1, and the sum over sequences is at
+most max_total_q * G / step + num_seqs.  Every CTA boundary cuts at most one
+unit, so pieces <= units + CTAs, and split units' pieces <= 2 (CTAs - 1).
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+from paged_varlen_attention_gb300 import _binding as B
+from paged_varlen_attention_gb300 import build_lib
+
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return B.load_library()
+
+
+def layout(lib, num_seqs, max_total_q, max_seq_q, hq, hkv, d, stride, fp8=0, sms=152, bs=16):
+    offs = np.zeros(8, np.int64)
+    caps = np.zeros(8, np.int32)
+    rc = lib.ua_device_plan_layout(num_seqs, max_total_q, max_seq_q, hq, hkv, d, bs, stride, fp8, sms,
+                                   offs.ctypes.data_as(ctypes.c_void_p),
+                                   caps.ctypes.data_as(ctypes.c_void_p))
+    return rc, offs, caps
+
+
+def test_shapes_are_checked_on_the_host(lib):
+    assert layout(lib, 4, 64, 0, 32, 8, 96, 64)[0] == UNSUPPORTED      # head size
+    assert layout(lib, 4, 64, 0, 30, 8, 128, 64)[0] == UNSUPPORTED     # Hq not a multiple of Hkv
+    assert layout(lib, 4, 64, 0, 32, 8, 128, 64, bs=32)[0] == UNSUPPORTED   # page size
+    assert layout(lib, 4, 64, 0, 32, 8, 64, 64, fp8=1)[0] == UNSUPPORTED    # e4m3 needs D = 128
+    assert layout(lib, -1, 64, 0, 32, 8, 128, 64)[0] == INVALID
+    assert layout(lib, 4, -5, 0, 32, 8, 128, 64)[0] == INVALID
+    assert layout(lib, 4, 64, -1, 32, 8, 128, 64)[0] == INVALID
+    assert layout(lib, 4, 64, 0, 32, 8, 128, 64, sms=0)[0] == INVALID
+    # packed rows beyond 32-bit counts
+    assert layout(lib, 4, 2**30, 0, 32, 8, 128, 64)[0] == INVALID
+
+
+@pytest.mark.parametrize("ns,tq,msq,hq,hkv,d,stride,fp8", [
+    (64, 64, 0, 32, 8, 128, 256, 0),       # decode batch, prefill possible (capacity)
+    (64, 64, 1, 32, 8, 128, 256, 0),       # decode-only
+    (16, 16000, 0, 32, 8, 128, 63, 0),     # prefill batch
+    (300, 2304, 512, 32, 8, 128, 96, 0),   # mixed
+    (64, 64, 1, 32, 8, 128, 256, 1),       # e4m3, paired heads
+    (10, 40, 0, 12, 3, 128, 40, 1),        # e4m3, odd Hkv: one head per unit
+    (5, 900, 0, 4, 4, 64, 300, 0),         # G = 1, D = 64
+])
+def test_capacities_and_sections(lib, ns, tq, msq, hq, hkv, d, stride, fp8):
+    rc, offs, caps = layout(lib, ns, tq, msq, hq, hkv, d, stride, fp8)
+    assert rc == OK
+    g = hq // hkv
+    msq_eff = tq if msq == 0 or msq > tq else msq
+    hpu = 2 if fp8 and hkv % 2 == 0 else 1
+    step = 16 // hpu
+    dec_grid, cap_units, cap_items, cap_pieces, cap_comb, cap_slots, buckets, sms = caps.tolist()
+    assert sms == 152 and dec_grid == 2 * 152
+    assert cap_units == (hkv // hpu) * (ns + -(-tq * g // step))
+    prefill_possible = not fp8 and msq_eff * g > 16 and 128 % g == 0
+    assert cap_items == (hkv * (ns + -(-tq * g // 256)) if prefill_possible else 0)
+    assert cap_pieces == cap_units + dec_grid
+    assert cap_comb == min(cap_units, dec_grid)
+    assert cap_slots == 2 * dec_grid
+    assert buckets == -(-stride * 16 // 128) + 2
+    # sections in order, 256-byte aligned, inside the workspace
+    assert all(o % 256 == 0 for o in offs[:7])
+    assert list(offs[:7]) == sorted(offs[:7]) and offs[7] > offs[6]
+    assert offs[1] - offs[0] >= 64                                   # header
+    assert offs[2] - offs[1] >= 4 * (dec_grid + 1)                   # cta_begin
+    assert offs[3] - offs[2] >= 32 * cap_pieces                      # pieces
+    assert offs[6] - offs[5] >= 32 * cap_items                       # prefill items
+
+
+def test_workspace_grows_with_the_capacities(lib):
+    small = layout(lib, 64, 64, 1, 32, 8, 128, 256)[1][7]
+    more_tokens = layout(lib, 64, 4096, 0, 32, 8, 128, 256)[1][7]
+    more_seqs = layout(lib, 512, 512, 1, 32, 8, 128, 256)[1][7]
+    assert small < more_tokens and small < more_seqs
