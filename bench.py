@@ -20,12 +20,17 @@ bandwidth), the fp64 oracle timed on the host cores (cpu_baseline), an
 end-to-end number through the public API with host buffers, clocks sampled
 during the timed region, and the number of kernels launched.
 
---impl reference times the fp64 CPU oracle (the reference arm of this build)
-on the same workload, a bounded sample of sequences per step.
+--impl reference times the fp64 CPU oracle (the reference arm) on the same
+workload, a bounded sample of sequences per step.
 
---workload llama3_8b_cascade_64dec_shared4k times a cascade step instead
-(shared-prefix pass + own-keys pass + LSE merge) next to the same attention
-as one direct call.
+Other workloads: the standard batches by name (tiny_mixed_d64,
+mistral_24b_prefill_16x1000, llama3_8b_mixed_256dec_4x512chunk,
+llama3_70b_long_mixed_32x8k-32k_2x2048chunk); llama3_8b_cascade_64dec_shared4k
+(a cascade step: shared-prefix pass + own-keys pass + LSE merge, next to the
+same attention as one direct call); kv_append_mistral_24b_16x1000 (writing
+16 000 new tokens' K/V into their pages); llama3_8b_decode_64x2k-4k_fp8kv (the
+headline batch over an E4M3 cache); llama3_8b_decode_64x2k-4k_graph (the
+headline batch planned on the GPU, one CUDA-graph replay per step).
 
 Multi-GPU: one process per GPU under torchrun; each rank runs its own replica
 of the workload (no data-path collective, weak scaling); the time is the max
