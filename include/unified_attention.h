@@ -144,7 +144,9 @@ ua_status ua_device_status(int32_t *code);
  * If items != NULL, up to items_cap rows of 8 int32 are written:
  *   decode pieces   {0, cta, seq, kv_head, row0, nrows, page_begin, page_end}
  *                   followed by one row {1, slot or -1, unit, 0, 0, 0, 0, 0}
- *   prefill tiles   {2, order, seq, kv_head, row0, nrows, kv_tiles, 0}
+ *   prefill tiles   {2, cta, seq, kv_head, row0, nrows, kv_tiles, order}
+ *                   (cta -1: long items, claimed by the CTAs in order as they
+ *                   go; a call with head_size 128 and a positive scale)
  *   split units     {3, seq, kv_head, row0, nrows, slot_begin, nslots, 0}
  * Rows are packed (token, head-in-group) pairs: row r is token r / G, query
  * head kv_head * G + r % G, with G = num_q_heads / num_kv_heads.

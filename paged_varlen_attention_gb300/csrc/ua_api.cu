@@ -329,6 +329,7 @@ extern "C" ua_status ua_plan_inspect(const int32_t *cu_seqlens_q_host,
     if (!counts || num_sms <= 0) return UA_ERR_INVALID_ARG;
     Problem pr = make_problem(cu_seqlens_q_host, seqused_k_host, num_seqs, num_q_heads,
                               num_kv_heads, head_size, block_size, block_table_stride, causal);
+    pr.prefill_claim = head_size == 128;   // as a call with a positive softmax scale
     int v = validate_problem(pr);
     if (v) return static_cast<ua_status>(v);
     thread_local Plan plan;
@@ -361,8 +362,10 @@ extern "C" ua_status ua_plan_inspect(const int32_t *cu_seqlens_q_host,
         }
     for (size_t i = 0; i < plan.tiles.size(); ++i) {
         const PreTile &t = plan.tiles[i];
-        const int32_t cta = (int32_t)(std::upper_bound(plan.pre_begin.begin(), plan.pre_begin.end(),
-                                                       (int32_t)i) - plan.pre_begin.begin()) - 1;
+        const int32_t cta = plan.pre_claimed
+                                ? -1
+                                : (int32_t)(std::upper_bound(plan.pre_begin.begin(), plan.pre_begin.end(),
+                                                             (int32_t)i) - plan.pre_begin.begin()) - 1;
         put(2, cta, t.seq, t.kvh, t.row0, t.nrows, t.kv_tiles, (int32_t)i);
     }
     for (const CombUnit &u : plan.comb)
@@ -445,6 +448,8 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
                               num_kv_heads, head_size, block_size, block_table_stride, causal);
     // e4m3 pages: decode units take two adjacent kv heads (256-byte rows per slot)
     if (kv_fp8) pr.kv_heads_per_unit = 2;
+    // long prefill items may be claimed as the CTAs go (that kernel: D = 128, scale > 0)
+    pr.prefill_claim = head_size == 128 && softmax_scale * k_scale > 0.f;
     int v = validate_problem(pr);
     if (v) return static_cast<ua_status>(v);
     if (!std::isfinite(softmax_scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
@@ -586,9 +591,11 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
         pp.scale_log2 = scale_log2;
         pp.tiles = reinterpret_cast<const PreTile *>(pl + L.off_tiles);
         pp.tile_begin = reinterpret_cast<const int32_t *>(pl + L.off_pre_begin);
+        pp.sched = reinterpret_cast<int32_t *>(pl + L.off_sched);
         pp.n_tiles = (int32_t)plan.tiles.size();
         pp.status = ds->status;
-        e = launch_prefill(head_size, pp, tm_q, tm_o, tm_k3, tm_vp, plan.pre_ctas, stream);
+        e = launch_prefill(head_size, plan.pre_claimed, pp, tm_q, tm_o, tm_k3, tm_vp, plan.pre_ctas,
+                           stream);
         if (e != cudaSuccess) return UA_ERR_CUDA;
     }
     mark(3);
@@ -880,8 +887,8 @@ static ua_status run_attention_device_plan(
         pp.tile_begin = reinterpret_cast<const int32_t *>(ws + L.off_pre_begin);
         pp.n_tiles = L.cap_items;
         pp.status = ds->status;
-        if (launch_prefill(head_size, pp, tm_q, tm_o, tm_k3, tm_vp, shape.num_sms, stream) !=
-            cudaSuccess)
+        if (launch_prefill(head_size, /*claimed=*/false, pp, tm_q, tm_o, tm_k3, tm_vp, shape.num_sms,
+                           stream) != cudaSuccess)
             return UA_ERR_CUDA;
     }
     mark(3);

@@ -50,8 +50,9 @@ struct PrefillParams {
     int32_t g;
     int32_t causal;
     float scale_log2;
-    const PreTile *tiles;        // grouped by CTA
-    const int32_t *tile_begin;   // [ctas + 1]: CTA c runs tiles [tile_begin[c], tile_begin[c+1])
+    const PreTile *tiles;        // grouped by CTA (dealt), or longest first (claimed)
+    const int32_t *tile_begin;   // dealt: [ctas + 1], CTA c runs tiles [tile_begin[c], tile_begin[c+1])
+    int32_t *sched;              // claimed: [kSchedInts] next unclaimed item, CTAs done, item count
     int32_t n_tiles;
     int *status;
 };
@@ -59,9 +60,11 @@ struct PrefillParams {
 // Each returns the launch error (cudaSuccess when the launch was queued).
 cudaError_t launch_decode(int d, bool kv8, const DecodeParams &p, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, int ctas, cudaStream_t stream);
-cudaError_t launch_prefill(int d, const PrefillParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_o,
-                           const CUtensorMap &tm_k, const CUtensorMap &tm_v, int ctas,
-                           cudaStream_t stream);
+// claimed: the CTAs claim items from p.sched (D = 128 with a positive scale
+// only); otherwise each runs its range of p.tile_begin.
+cudaError_t launch_prefill(int d, bool claimed, const PrefillParams &p, const CUtensorMap &tm_q,
+                           const CUtensorMap &tm_o, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                           int ctas, cudaStream_t stream);
 
 // The whole call behind unified_attention (arguments as declared in
 // unified_attention.h).  pinned_plan: stage the plan through the library's

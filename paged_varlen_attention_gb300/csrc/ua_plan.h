@@ -20,7 +20,10 @@
 //     8-row tile): tile rows 0-7 belong to head h, rows 8-15 to head h + 1.
 //   * prefill tiles -- (sequence, kv head, 256-row tile) for the rest: two
 //     128-row tensor-core tiles that share every K/V tile they load, longest
-//     first.
+//     first.  Short items are dealt to the CTAs in advance (rounds of
+//     alternating direction); long ones (2048 visible keys or more on
+//     average) are claimed by the CTAs one at a time from the longest-first
+//     list (an atomic counter), so that CTAs that run faster take more.
 //
 // Rows are packed (token, head-in-group) pairs: packed row r of a (sequence,
 // kv head) is token r / G and query head kv_head * G + r % G.
@@ -44,6 +47,15 @@ constexpr int kPreTileRows = 256;   // packed rows per prefill work item (two MM
 constexpr int kKvTile = 128;        // keys per prefill KV tile (8 pages)
 constexpr int kDecCtasPerSm = 2;    // resident decode CTAs per SM
 constexpr size_t kAlign = 256;
+// The scheduling block of claimed prefill items: the index of the next
+// unclaimed item, the prefill CTAs that have finished (the last one zeroes
+// both again, so a plan can be reused), the number of items.
+enum : int { kSchedNext = 0, kSchedDone = 1, kSchedItems = 2, kSchedInts = 4 };
+// Prefill items are claimed as the CTAs go when they see this many 128-key
+// tiles on average (2048 keys): per-SM speed differences then add up to more
+// than claiming costs (measured: -14% on 2048-token chunks over 4096-token
+// contexts, +3% on 1000-token prompts, which are dealt in advance instead).
+constexpr int kClaimMinMeanKvTiles = 16;
 
 struct alignas(16) DecPiece {   // one contiguous page range of one decode unit
     int32_t seq;
@@ -90,6 +102,7 @@ struct Problem {
     int32_t bt_stride;
     bool causal;
     int32_t kv_heads_per_unit = 1;   // decode units: 1, or 2 (adjacent heads, <= 8 rows each)
+    bool prefill_claim = false;      // long prefill items may be claimed as the CTAs go
 };
 
 // Offsets of the plan sections inside the device workspace.
@@ -99,7 +112,8 @@ struct Layout {
     size_t off_comb;       // CombUnit [n_comb]
     size_t off_comb_count; // int32 [n_comb]: partials written so far (zero in the blob)
     size_t off_tiles;      // PreTile [n_tiles]
-    size_t off_pre_begin;  // int32 [pre_ctas + 1]
+    size_t off_pre_begin;  // int32 [pre_ctas + 1] (items dealt in advance)
+    size_t off_sched;      // int32 [kSchedInts] (items claimed as the CTAs go)
     size_t blob_bytes;     // bytes copied host -> device per call (offsets above are
                            // from the start of the workspace)
     size_t off_part_o;     // float [n_slots][kDecRows][d]

@@ -56,6 +56,7 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
     plan.tiles.clear();
     plan.pre_begin.clear();
     plan.pre_ctas = 0;
+    plan.pre_claimed = false;
     plan.layout = Layout{};
     const int g = p.hq / p.hkv;
     const bool pre_ok = prefill_enabled && prefill_supports(p);
@@ -126,37 +127,49 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
             }
         }
     }
-    // ---- prefill: longest first (counting sort, equal lengths keep batch order),
-    // then dealt to the CTAs in rounds whose direction alternates (CTA 0..n-1,
+    // ---- prefill: longest first (counting sort, equal lengths keep batch order).
+    // Long items on average (kClaimMinMeanKvTiles, when the caller allows it)
+    // are claimed by the CTAs from this list as they go.  Otherwise they are
+    // dealt to the CTAs in rounds whose direction alternates (CTA 0..n-1,
     // then n-1..0, ...): the CTA that got the longest item of a round gets the
     // shortest of the next, which keeps the CTAs' totals within about one
-    // item of each other at O(items) host cost
+    // item of each other.  O(items) host cost.
     if (!unsorted.empty()) {
         thread_local std::vector<PreTile> tl_sorted;
         thread_local std::vector<int32_t> tl_owner;
         std::vector<PreTile> &sorted = tl_sorted;
         std::vector<int32_t> &owner = tl_owner;
         counts.assign((size_t)max_kv + 2, 0);
-        for (const PreTile &t : unsorted) ++counts[(size_t)(max_kv - t.kv_tiles) + 1];
+        int64_t kv_sum = 0;
+        for (const PreTile &t : unsorted) {
+            ++counts[(size_t)(max_kv - t.kv_tiles) + 1];
+            kv_sum += t.kv_tiles;
+        }
         for (size_t b = 1; b < counts.size(); ++b) counts[b] += counts[b - 1];
         sorted.resize(unsorted.size());
         for (const PreTile &t : unsorted) sorted[(size_t)counts[(size_t)(max_kv - t.kv_tiles)]++] = t;
 
         const int32_t ctas = (int32_t)std::min<size_t>(sorted.size(), (size_t)std::max(num_sms, 1));
         plan.pre_ctas = ctas;
-        owner.resize(sorted.size());
-        plan.pre_begin.assign((size_t)ctas + 1, 0);
-        for (size_t i = 0; i < sorted.size(); ++i) {
-            const size_t round = i / (size_t)ctas, k = i % (size_t)ctas;
-            owner[i] = (int32_t)((round & 1) ? (size_t)ctas - 1 - k : k);
-            ++plan.pre_begin[(size_t)owner[i] + 1];
+        plan.pre_claimed =
+            p.prefill_claim && kv_sum >= (int64_t)kClaimMinMeanKvTiles * (int64_t)sorted.size();
+        if (plan.pre_claimed) {
+            plan.tiles = sorted;
+        } else {
+            owner.resize(sorted.size());
+            plan.pre_begin.assign((size_t)ctas + 1, 0);
+            for (size_t i = 0; i < sorted.size(); ++i) {
+                const size_t round = i / (size_t)ctas, k = i % (size_t)ctas;
+                owner[i] = (int32_t)((round & 1) ? (size_t)ctas - 1 - k : k);
+                ++plan.pre_begin[(size_t)owner[i] + 1];
+            }
+            for (int32_t c = 0; c < ctas; ++c) plan.pre_begin[(size_t)c + 1] += plan.pre_begin[(size_t)c];
+            // group by CTA, keeping each CTA's items in assignment (longest-first) order
+            counts.assign((size_t)ctas, 0);
+            for (int32_t c = 0; c < ctas; ++c) counts[(size_t)c] = plan.pre_begin[(size_t)c];
+            plan.tiles.resize(sorted.size());
+            for (size_t i = 0; i < sorted.size(); ++i) plan.tiles[(size_t)counts[(size_t)owner[i]]++] = sorted[i];
         }
-        for (int32_t c = 0; c < ctas; ++c) plan.pre_begin[(size_t)c + 1] += plan.pre_begin[(size_t)c];
-        // group by CTA, keeping each CTA's items in assignment (longest-first) order
-        counts.assign((size_t)ctas, 0);
-        for (int32_t c = 0; c < ctas; ++c) counts[(size_t)c] = plan.pre_begin[(size_t)c];
-        plan.tiles.resize(sorted.size());
-        for (size_t i = 0; i < sorted.size(); ++i) plan.tiles[(size_t)counts[(size_t)owner[i]]++] = sorted[i];
     }
 
     // ---- decode: equal page ranges over the concatenated units
@@ -253,6 +266,8 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
     off = align_up(off + sizeof(PreTile) * plan.tiles.size(), kAlign);
     L.off_pre_begin = off;
     off = align_up(off + sizeof(int32_t) * plan.pre_begin.size(), kAlign);
+    L.off_sched = off;
+    off = align_up(off + sizeof(int32_t) * kSchedInts, kAlign);
     L.blob_bytes = off;
     L.off_part_o = off;
     off = align_up(off + sizeof(float) * (size_t)plan.n_slots * kDecRows * p.d, kAlign);
@@ -274,6 +289,8 @@ void serialize_plan_to(const Plan &plan, uint8_t *dst) {
         std::memcpy(dst + L.off_tiles, plan.tiles.data(), sizeof(PreTile) * plan.tiles.size());
     if (!plan.pre_begin.empty())
         std::memcpy(dst + L.off_pre_begin, plan.pre_begin.data(), sizeof(int32_t) * plan.pre_begin.size());
+    const int32_t sched[kSchedInts] = {0, 0, (int32_t)plan.tiles.size(), 0};
+    std::memcpy(dst + L.off_sched, sched, sizeof(sched));
 }
 
 void serialize_plan(const Plan &plan, std::vector<uint8_t> &blob) {

@@ -15,9 +15,10 @@ struct Plan {
     std::vector<DecPiece> pieces;
     std::vector<CombUnit> comb;
     int32_t n_slots = 0;
-    std::vector<PreTile> tiles;         // grouped by prefill CTA
-    std::vector<int32_t> pre_begin;     // pre_ctas + 1: CTA c runs tiles [pre_begin[c], pre_begin[c+1])
+    std::vector<PreTile> tiles;         // grouped by prefill CTA (dealt), or longest first (claimed)
+    std::vector<int32_t> pre_begin;     // dealt: pre_ctas + 1, CTA c runs tiles [pre_begin[c], pre_begin[c+1])
     int32_t pre_ctas = 0;
+    bool pre_claimed = false;           // the prefill CTAs claim items from the list as they go
     Layout layout{};
 };
 

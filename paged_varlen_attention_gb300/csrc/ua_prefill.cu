@@ -7,9 +7,12 @@
 // distinguish between prefill + decode", vLLM PR #16828, PR description,
 // there done "to ensure the Tensor cores are well used").
 //
-// One persistent CTA per SM walks its work items (longest first).  A work item
-// is a pair of 128-row MMA tiles, A and B, of the same (sequence, KV head);
-// both use every K/V step the CTA loads.  A step is 64 keys (4 pages).
+// One persistent CTA per SM walks its work items, longest first: the items
+// dealt to it in advance, or (kClaimed: long items) items it claims from the
+// plan's longest-first list one at a time (an atomic counter), so that an SM
+// that runs faster takes more of them.  A work item is a pair of 128-row MMA
+// tiles, A and B, of the same (sequence, KV head); both use every K/V step
+// the CTA loads.  A step is 64 keys (4 pages).
 //
 // TMEM (512 columns) holds, per tile X: two S buffers of 64 fp32 columns
 // (steps alternate between them; P is written as bf16 pairs over the first 32
@@ -33,7 +36,10 @@
 //               in the order S(0), S(1), then P V(j) and S(j+2) as each buffer
 //               frees up.
 //   warp 11     the same for tile B
-//   warp 9      TMA producer of the Q tiles (box {64, G, 128/G} of [T, Hq, D])
+//   warp 9      (kClaimed) claims the CTA's items: lane 0 takes the next
+//               index with an atomic add and puts the item's record into a
+//               4-slot ring in shared memory that every role reads in order;
+//               and TMA producer of the Q tiles (box {64, G, 128/G} of [T, Hq, D])
 //               and of V (one box per 16-token page: a 5-D view of the cache,
 //               so one box holds all D columns of the page).  The step that
 //               holds a sequence's last, partial page lands on a barrier of its
@@ -91,7 +97,9 @@ enum : int {
     kBarPFull = 25,     // [4] 128 arrivals
     kBarPvDone = 29,    // [4]
     kBarDrain = 33,     // [2]
-    kNumBars = 35
+    kBarItemFull = 35,  // [kItemRing] (kClaimed) an item record is in the ring slot
+    kBarItemEmpty = 39, // [kItemRing] (kClaimed) kItemReaders arrivals: every reader has taken it
+    kNumBars = 43
 };
 
 struct SubInfo {
@@ -155,6 +163,51 @@ struct ItemCursor {
     __device__ __forceinline__ void advance(const PreTile &next) {
         cur = next;
         ++t;
+    }
+};
+
+// Claimed items pass through a ring of kItemRing records in shared memory:
+// slot k % kItemRing holds the CTA's k-th item (or an end marker, seq = -1)
+// once ItemFull completes its phase k / kItemRing; the kItemReaders reader
+// warps (10; 8 and 11; 0-7) arrive on ItemEmpty after reading it, which lets
+// warp 9 refill the slot.
+constexpr int kItemRing = 4;
+constexpr int kItemReaders = 11;
+
+// A role's walk over this CTA's items: dealt ones through ItemCursor, claimed
+// ones from the ring (reader warps release each slot).  take() returns 1 with
+// an item, 0 at the end, -1 when a wait gave up.
+template <bool kClaimed>
+struct ItemIter;
+
+template <>
+struct ItemIter<false> {
+    ItemCursor it;
+    PreTile nxt;
+    __device__ __forceinline__ ItemIter(const PrefillParams &p, const PreTile *, uint32_t, uint32_t)
+        : it(p) {}
+    __device__ __forceinline__ int take(const PrefillParams &p, uint32_t, bool, int, PreTile &out) {
+        if (!it.valid(p)) return 0;
+        out = it.take(p, nxt);
+        it.advance(nxt);
+        return 1;
+    }
+};
+
+template <>
+struct ItemIter<true> {
+    const PreTile *ring;
+    uint32_t full0, empty0;
+    __device__ __forceinline__ ItemIter(const PrefillParams &, const PreTile *r, uint32_t f, uint32_t e)
+        : ring(r), full0(f), empty0(e) {}
+    __device__ __forceinline__ int take(const PrefillParams &p, uint32_t k, bool release, int lane,
+                                        PreTile &out) {
+        const uint32_t slot = k % kItemRing;
+        if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * slot, (k / kItemRing) & 1, p.status))) return -1;
+        out = ring[slot];
+        __syncwarp();
+        if (release && lane == 0) mbar_arrive(empty0 + 8 * slot);
+        return out.seq < 0 ? 0 : 1;
     }
 };
 
@@ -228,7 +281,7 @@ __device__ __noinline__ void copy_partial_rows(__nv_bfloat16 *out, const uint8_t
     }
 }
 
-template <int D, bool kPos>
+template <int D, bool kPos, bool kClaimed>
 __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
     ua_prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_k,
@@ -244,15 +297,23 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
     uint8_t *stage_ptr = sv_ptr + C::kVStages * C::kKvBytes;     // [tile][128 rows][64] bf16, 128B swizzle
     const uint32_t sstage = smem_u32(stage_ptr);
     uint64_t *bars = reinterpret_cast<uint64_t *>(stage_ptr + 2 * C::kStageBytes);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
+    PreTile *ring = reinterpret_cast<PreTile *>(bars + ((kNumBars + 1) & ~1));   // 16-byte aligned
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ring + kItemRing);
     const uint32_t bar0 = smem_u32(bars);
     auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // a CTA of a fixed grid (plan built on the device) may have no item: it
-    // leaves before touching barriers or TMEM (the same answer for every thread)
-    if (p.tile_begin[blockIdx.x] == p.tile_begin[blockIdx.x + 1]) return;
+    // a CTA with no item (a fixed grid whose plan, built on the device, has
+    // fewer items than CTAs) leaves before touching barriers or TMEM (the same
+    // answer for every thread)
+    int n_items = 0;
+    if constexpr (kClaimed) {
+        n_items = p.sched[kSchedItems];
+        if (n_items == 0) return;
+    } else {
+        if (p.tile_begin[blockIdx.x] == p.tile_begin[blockIdx.x + 1]) return;
+    }
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
@@ -270,6 +331,11 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
             mbar_init(bar(kBarPvDone + i), 1);
         }
         mbar_init(bar(kBarVTail), 1);
+        if constexpr (kClaimed)
+            for (int i = 0; i < kItemRing; ++i) {
+                mbar_init(bar(kBarItemFull + i), 1);
+                mbar_init(bar(kBarItemEmpty + i), kItemReaders);
+            }
         fence_barrier_init();
     }
     if (warp == 8) {
@@ -290,9 +356,58 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
         bool ok = true;
         uint32_t e = 0, v_issued = 0, tails = 0;
         uint32_t q_issued[2] = {0, 0};
-        PreTile nxt_tile;
-        for (ItemCursor it(p); it.valid(p) && ok; it.advance(nxt_tile)) {
-            const PairInfo pi = make_pair(p, it.take(p, nxt_tile));
+        // (kClaimed) lane 0 claims items and publishes them in the ring.
+        // claim: the next index of the longest-first list (atomic add) and a
+        // load of its record, not waited for here; publish: once every reader
+        // has taken the slot's previous item, the record (or the end marker)
+        // goes into slot f % kItemRing; it returns 1 for an item, 0 for the end
+        // marker, -1 when the wait gave up.  Item k + 1 is claimed when item k
+        // starts and published once item k's loads are all issued (the claim's
+        // latency hides behind item k, and a CTA holds at most one unstarted
+        // item); with at most two items per CTA it is claimed only then, as
+        // claiming ahead would let the CTAs that start first take the items of
+        // those that start later.
+        uint32_t fetched = 0;
+        int more = 1;
+        int next_idx = 0;
+        PreTile next_rec{};
+        auto claim = [&]() {
+            next_idx = atomicAdd(p.sched + kSchedNext, 1);
+            next_rec = p.tiles[min(next_idx, n_items - 1)];
+        };
+        auto publish = [&]() -> int {
+            const uint32_t f = fetched, slot = f % kItemRing;
+            if (f >= (uint32_t)kItemRing &&
+                !mbar_wait(bar(kBarItemEmpty + slot), ((f / kItemRing) - 1) & 1, p.status))
+                return -1;
+            PreTile t = next_rec;
+            if (next_idx >= n_items) t.seq = -1;
+            ring[slot] = t;
+            mbar_arrive(bar(kBarItemFull + slot));   // release: the record is visible
+            ++fetched;
+            return next_idx < n_items ? 1 : 0;
+        };
+        const bool ahead = n_items > 2 * (int)gridDim.x;
+        if constexpr (kClaimed) {
+            if (lane == 0) {
+                claim();
+                more = publish();
+            }
+        }
+        ItemIter<kClaimed> items(p, ring, bar(kBarItemFull), bar(kBarItemEmpty));
+        for (uint32_t k = 0; ok; ++k) {
+            if constexpr (kClaimed) {
+                if (lane == 0 && more == 1 && ahead) claim();
+                if (__shfl_sync(0xffffffffu, more, 0) < 0) {
+                    ok = false;
+                    break;
+                }
+            }
+            PreTile cur;
+            const int got = items.take(p, k, false, lane, cur);
+            if (got < 0) ok = false;
+            if (got <= 0) break;
+            const PairInfo pi = make_pair(p, cur);
             int good = 1;
             if (lane == 0) {
 #pragma unroll
@@ -367,6 +482,13 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
                     }
                 }
             }
+            if constexpr (kClaimed) {
+                // this item's loads are all issued: publish the next item
+                if (lane == 0 && more == 1) {
+                    if (!ahead) claim();
+                    more = publish();
+                }
+            }
         }
         // drain: the last loads issued must land before the CTA can exit
         if (lane == 0) {
@@ -374,6 +496,15 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
                 mbar_wait(bar(kBarVFull + x % C::kVStages), (x / C::kVStages) & 1, p.status);
             for (int x = 0; x < 2; ++x)
                 if (q_issued[x] > 0) mbar_wait(bar(kBarQFull + x), (q_issued[x] - 1) & 1, p.status);
+            if constexpr (kClaimed) {
+                // this CTA claims no more; the last CTA to get here zeroes the
+                // counters for the next launch that reuses the plan
+                __threadfence();
+                if (atomicAdd(p.sched + kSchedDone, 1) == (int)gridDim.x - 1) {
+                    atomicExch(p.sched + kSchedNext, 0);
+                    atomicExch(p.sched + kSchedDone, 0);
+                }
+            }
         }
     } else if (warp == 10) {
         // ================================================================ K producer
@@ -381,9 +512,13 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
         const uint64_t pol_kv = l2_policy_evict_last();
         bool ok = true;
         uint32_t e = 0, k_issued = 0;
-        PreTile nxt_tile;
-        for (ItemCursor it(p); it.valid(p) && ok; it.advance(nxt_tile)) {
-            const PairInfo pi = make_pair(p, it.take(p, nxt_tile));
+        ItemIter<kClaimed> items(p, ring, bar(kBarItemFull), bar(kBarItemEmpty));
+        for (uint32_t k = 0; ok; ++k) {
+            PreTile cur;
+            const int got = items.take(p, k, true, lane, cur);
+            if (got < 0) ok = false;
+            if (got <= 0) break;
+            const PairInfo pi = make_pair(p, cur);
             const int kend = max(pi.sub[0].kend_max, pi.sub[1].kend_max);
             const int32_t *bt_row = p.block_table + (int64_t)pi.seq * p.bt_stride;
             for (int j = 0; j < pi.n && ok; ++j, ++e) {
@@ -471,9 +606,13 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
             ++pcnt;
             return true;
         };
-        PreTile nxt_tile;
-        for (ItemCursor it(p); it.valid(p) && ok; it.advance(nxt_tile)) {
-            const PairInfo pi = make_pair(p, it.take(p, nxt_tile));
+        ItemIter<kClaimed> items(p, ring, bar(kBarItemFull), bar(kBarItemEmpty));
+        for (uint32_t k = 0; ok; ++k) {
+            PreTile cur;
+            const int got = items.take(p, k, true, lane, cur);
+            if (got < 0) ok = false;
+            if (got <= 0) break;
+            const PairInfo pi = make_pair(p, cur);
             const int nx = x ? pi.sub[1].n : pi.sub[0].n;
             if (nx > 0) {
                 if (!mbar_wait(bar(kBarQFull + x), qcnt & 1, p.status)) {
@@ -521,9 +660,13 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
         const uint32_t o_addr = s_addr + C::kColO;
         bool ok = true;
         uint32_t ex = 0;    // steps of this tile slot over all items (S k lives in buffer k % 2)
-        PreTile nxt_tile;
-        for (ItemCursor it(p); it.valid(p) && ok; it.advance(nxt_tile)) {
-            const PairInfo pi = make_pair(p, it.take(p, nxt_tile));
+        ItemIter<kClaimed> items(p, ring, bar(kBarItemFull), bar(kBarItemEmpty));
+        for (uint32_t k = 0; ok; ++k) {
+            PreTile cur;
+            const int got = items.take(p, k, true, lane, cur);
+            if (got < 0) ok = false;
+            if (got <= 0) break;
+            const PairInfo pi = make_pair(p, cur);
             const SubInfo si = x ? pi.sub[1] : pi.sub[0];
             if (si.nrows == 0) continue;
             const int pr = si.row0 + r;
@@ -684,7 +827,7 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
     }
 }
 
-template <int D, bool kPos>
+template <int D, bool kPos, bool kClaimed>
 static cudaError_t launch_prefill_t(const PrefillParams &p, const CUtensorMap &tm_q,
                                     const CUtensorMap &tm_o, const CUtensorMap &tm_k, const CUtensorMap &tm_vp, int ctas,
                                     cudaStream_t stream) {
@@ -693,25 +836,31 @@ static cudaError_t launch_prefill_t(const PrefillParams &p, const CUtensorMap &t
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(ua_prefill_kernel<D, kPos>,
+        cudaError_t e = cudaFuncSetAttribute(ua_prefill_kernel<D, kPos, kClaimed>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    ua_prefill_kernel<D, kPos><<<ctas, C::kThreads, C::kSmemBytes, stream>>>(p, tm_q, tm_o, tm_k, tm_vp);
+    ua_prefill_kernel<D, kPos, kClaimed><<<ctas, C::kThreads, C::kSmemBytes, stream>>>(p, tm_q, tm_o, tm_k, tm_vp);
     return cudaGetLastError();
 }
 
-cudaError_t launch_prefill(int d, const PrefillParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_o,
-                           const CUtensorMap &tm_k, const CUtensorMap &tm_vp, int ctas,
-                           cudaStream_t stream) {
+cudaError_t launch_prefill(int d, bool claimed, const PrefillParams &p, const CUtensorMap &tm_q,
+                           const CUtensorMap &tm_o, const CUtensorMap &tm_k, const CUtensorMap &tm_vp,
+                           int ctas, cudaStream_t stream) {
     const bool pos = p.scale_log2 > 0.f;
+    if (claimed) {
+        // the claiming kernel exists for D = 128 with a positive scale (the
+        // planner claims only then)
+        if (d != 128 || !pos) return cudaErrorInvalidValue;
+        return launch_prefill_t<128, true, true>(p, tm_q, tm_o, tm_k, tm_vp, ctas, stream);
+    }
     if (d == 64)
-        return pos ? launch_prefill_t<64, true>(p, tm_q, tm_o, tm_k, tm_vp, ctas, stream)
-                   : launch_prefill_t<64, false>(p, tm_q, tm_o, tm_k, tm_vp, ctas, stream);
-    return pos ? launch_prefill_t<128, true>(p, tm_q, tm_o, tm_k, tm_vp, ctas, stream)
-               : launch_prefill_t<128, false>(p, tm_q, tm_o, tm_k, tm_vp, ctas, stream);
+        return pos ? launch_prefill_t<64, true, false>(p, tm_q, tm_o, tm_k, tm_vp, ctas, stream)
+                   : launch_prefill_t<64, false, false>(p, tm_q, tm_o, tm_k, tm_vp, ctas, stream);
+    return pos ? launch_prefill_t<128, true, false>(p, tm_q, tm_o, tm_k, tm_vp, ctas, stream)
+               : launch_prefill_t<128, false, false>(p, tm_q, tm_o, tm_k, tm_vp, ctas, stream);
 }
 
 }  // namespace ua

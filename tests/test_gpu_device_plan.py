@@ -90,7 +90,17 @@ def compare_plans(q_lens, k_lens, hq, hk, d, causal=True):
     if len(tiles):
         dev = dp["tiles"]
         cta = _cta_of(dp["pre_begin"], len(dev))
-        np.testing.assert_array_equal(np.column_stack([cta, dev[:, :5]]), tiles)
+        if np.all(tiles[:, 0] == -1):
+            # the host lets the CTAs claim long items as they go; the device deals
+            # them (its graph-captured launch is fixed): the same items, and the
+            # device's deal is the host's longest-first list dealt in rounds
+            host = tiles[:, 1:]
+            as_rows = lambda a: np.sort(np.ascontiguousarray(a, dtype=np.int32).view("i4,i4,i4,i4,i4"),  # noqa: E731
+                                        axis=0)
+            np.testing.assert_array_equal(as_rows(dev[:, :5]), as_rows(host))
+            assert np.all(np.diff(dp["pre_begin"]) >= 0)
+        else:
+            np.testing.assert_array_equal(np.column_stack([cta, dev[:, :5]]), tiles)
         # the records carry the sequence's token offset and lengths
         np.testing.assert_array_equal(dev[:, 5], cu[dev[:, 0]])
         np.testing.assert_array_equal(dev[:, 6], cu[dev[:, 0] + 1] - cu[dev[:, 0]])

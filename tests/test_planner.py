@@ -99,13 +99,22 @@ def check_plan(q_lens, k_lens, hq, hk, d=128, causal=True, num_sms=152):
             per_cta[pc[1]] += pc[7] - pc[6]
         assert per_cta.max() - per_cta.min() <= 1
         assert counts["dec_ctas"] <= 2 * num_sms
-    # prefill items: the CTAs' ranges cover the tile list in order, each CTA's
-    # items come longest first, and dealing the longest-first list in rounds of
-    # alternating direction keeps the CTAs' work within one item of each other
+    # prefill items.  Long ones on average (16 tiles of 128 keys or more, head
+    # size 128) form one longest-first list, equal lengths in batch order, that
+    # the CTAs claim from as they go (cta -1).  Otherwise the CTAs' ranges cover
+    # the tile list in order, each CTA's items come longest first, and dealing
+    # the longest-first list in rounds of alternating direction keeps the CTAs'
+    # work within one item of each other
     ctas = [t[1] for t in tiles]
-    assert ctas == sorted(ctas)
     assert [t[7] for t in tiles] == list(range(len(tiles)))
-    if tiles:
+    claimed = bool(tiles) and d == 128 and sum(t[6] for t in tiles) >= 16 * len(tiles)
+    if claimed:
+        assert all(c == -1 for c in ctas)
+        assert counts["prefill_ctas"] == min(len(tiles), num_sms)
+        keys = [(-t[6], t[2], t[4], t[3]) for t in tiles]
+        assert keys == sorted(keys)
+    elif tiles:
+        assert ctas == sorted(ctas) and min(ctas) >= 0
         assert counts["prefill_ctas"] == len(set(ctas)) <= num_sms
         load, biggest = {}, 0
         for t in tiles:
@@ -133,6 +142,22 @@ def test_long_mixed_batch():
     s = W.config_spec(5)
     c = check_plan(s.q_lens, s.k_lens, s.num_q_heads, s.num_kv_heads, s.head_size, s.causal)
     assert c["dec_ctas"] == 2 * 152
+
+
+def test_long_items_are_claimed_short_ones_dealt():
+    """2048-token chunks over 4096-token contexts (long items) are claimed by the
+    CTAs as they go; 1000-token prompts (short items) are dealt in advance; so
+    are long items at head size 64 (the claiming kernel is built for 128)."""
+    def prefill_ctas(q, k, hq, hk, d):
+        cu = np.concatenate([[0], np.cumsum(q)]).astype(np.int32)
+        _, items = B.plan_inspect(cu, np.asarray(k, np.int32), hq, hk, d,
+                                  int(-(-max(k) // 16)), True)
+        return [r[1] for r in items if r[0] == 2]
+    s = W.config_spec(5)
+    assert set(prefill_ctas(s.q_lens, s.k_lens, 64, 8, 128)) == {-1}
+    s = W.config_spec(3)
+    assert min(prefill_ctas(s.q_lens, s.k_lens, 32, 8, 128)) >= 0
+    assert min(prefill_ctas([2048], [6144], 16, 8, 64)) >= 0
 
 
 @pytest.mark.parametrize("case", [
