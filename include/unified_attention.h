@@ -37,9 +37,20 @@
  *                launch without a device-to-host read; they must hold the
  *                same values as the device arrays.
  *
- * Supported set: head_size 64 or 128, block_size 16, num_q_heads a multiple
- * of num_kv_heads.  Anything else returns UA_ERR_UNSUPPORTED before any
- * launch.
+ * Supported set: head_size 64 or 128, block_size a multiple of 16 up to 256,
+ * num_q_heads a multiple of num_kv_heads.  Anything else returns
+ * UA_ERR_UNSUPPORTED before any launch.
+ *
+ * Pages of block_size = 16 r tokens (r > 1): the same memory is a cache of
+ * num_blocks * r pages of 16 tokens (slot j of page b is slot j % 16 of
+ * 16-token page b r + j / 16), which is what the kernels read.  Every call on
+ * such a cache first expands the block table on the device (entry p becomes
+ * p r .. p r + r - 1; an entry outside [0, num_blocks) becomes one the
+ * kernels skip and report).  The expanded table lives in the workspace:
+ * num_seqs x block_table_stride x r int32, rounded up to 256 bytes, counted
+ * by every ua_workspace_size* function.  block_table_stride x r must stay
+ * below 2^29.  The result is the same, bit for bit, as the call on the
+ * 16-token view with the expanded table.
  *
  * Ownership: the caller owns every buffer.  The library never allocates
  * device memory on a call; split-KV partials and the launch plan live in the
@@ -225,7 +236,8 @@ ua_status ua_merge_attn_states(const void *out_a, const float *lse_a, const void
  * and V rows into their pages.  Token i of sequence s (0 <= i < Lq) goes to
  * context position p = seqused_k[s] - Lq + i (the new tokens are the last Lq
  * positions of the context that seqused_k counts, as in the bottom-right
- * causal mask), i.e. k_cache[block_table[s][p / 16]][p % 16][:][:] = k_new[t]
+ * causal mask), i.e. k_cache[block_table[s][p / block_size]][p % block_size]
+ * [:][:] = k_new[t]
  * with t = cu_seqlens_q[s] + i, and the same for V.  Nothing else in the
  * caches is written.  The metadata and cache arguments are those of
  * unified_attention; k_new, v_new: device bf16 [total_q, Hkv, D], 16-byte
@@ -366,7 +378,9 @@ ua_status unified_attention_no_alloc(const void *q, const void *k_cache, const v
  *                for unified_attention_fp8kv (head_size 128 only).
  *   workspace    ua_workspace_size_device_plan bytes, 256-byte aligned; laid
  *                out for (num_seqs, max_total_q, heads, head size,
- *                block_table_stride, kv_fp8) and the device's SM count.
+ *                block_table_stride, kv_fp8) and the device's SM count.  With
+ *                pages of more than 16 tokens the expanded block table follows
+ *                the plan (it is rebuilt on every call, planned or not).
  * Other arguments as for unified_attention.  The host checks shapes,
  * pointers and the workspace; the metadata itself is checked on the device
  * (the same rules as unified_attention): a bad batch leaves an empty plan (no

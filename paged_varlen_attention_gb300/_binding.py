@@ -158,8 +158,8 @@ def unified_attention(q, k_cache, v_cache, cu_seqlens_q, seqused_k, block_table,
                       workspace=None, stream=None, lse=None, k_new=None, v_new=None):
     """Attention over a paged varlen batch (see ``include/unified_attention.h``).
 
-    q: bf16 [total_q, Hq, D]; k_cache / v_cache: bf16 [num_blocks, 16, Hkv, D];
-    cu_seqlens_q int32 [N+1], seqused_k int32 [N], block_table int32 [N, stride],
+    q: bf16 [total_q, Hq, D]; k_cache / v_cache: bf16 [num_blocks, block_size, Hkv, D]
+    (block_size a multiple of 16, at most 256); cu_seqlens_q int32 [N+1], seqused_k int32 [N], block_table int32 [N, stride],
     all CUDA tensors.  Host copies of cu_seqlens_q / seqused_k may be passed to
     avoid a device-to-host read.  Returns ``out`` (bf16 [total_q, Hq, D]).
     lse: an fp32 CUDA tensor [total_q, Hq] to also receive each row's natural-log
@@ -352,7 +352,7 @@ def unified_attention_fp8kv(q, k_cache, v_cache, k_scale, v_scale, cu_seqlens_q,
                             stream=None, lse=None):
     """Attention over a paged cache of FP8 E4M3 bytes (``unified_attention_fp8kv``).
 
-    k_cache / v_cache: uint8 CUDA tensors [num_blocks, 16, Hkv, 128] of E4M3 codes
+    k_cache / v_cache: uint8 CUDA tensors [num_blocks, block_size, Hkv, 128] of E4M3 codes
     with k = k_scale * e4m3(byte), v = v_scale * e4m3(byte); the rest as
     ``unified_attention``.  Returns ``out``.
     """

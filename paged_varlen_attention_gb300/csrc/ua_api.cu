@@ -246,6 +246,14 @@ static bool aligned(const void *p, size_t a) {
     return (reinterpret_cast<uintptr_t>(p) % a) == 0;
 }
 
+// Workspace bytes of the block table expanded to 16-token pages (pages of
+// block_size = 16 r tokens); 0 for 16-token pages.
+static size_t expanded_table_bytes(int32_t num_seqs, int32_t stride, int32_t block_size) {
+    if (block_size == kBlockSize || num_seqs <= 0 || stride <= 0) return 0;
+    const size_t n = (size_t)num_seqs * (size_t)stride * (size_t)(block_size / kBlockSize);
+    return (n * sizeof(int32_t) + kAlign - 1) / kAlign * kAlign;
+}
+
 }  // namespace ua
 
 using namespace ua;
@@ -278,6 +286,14 @@ static Problem make_problem(const int32_t *cu, const int32_t *lk, int32_t num_se
     return p;
 }
 
+// The problem as the kernels see it: 16-token pages, a block table r times as
+// wide (the plan of a call with larger pages is built on that view).
+static void to_16_token_pages(Problem &p) {
+    if (p.bs == kBlockSize) return;
+    p.bt_stride *= p.bs / kBlockSize;
+    p.bs = kBlockSize;
+}
+
 extern "C" ua_status ua_workspace_size(const int32_t *cu_seqlens_q_host,
                                        const int32_t *seqused_k_host, int32_t num_seqs,
                                        int32_t num_q_heads, int32_t num_kv_heads,
@@ -289,12 +305,13 @@ extern "C" ua_status ua_workspace_size(const int32_t *cu_seqlens_q_host,
                               num_kv_heads, head_size, block_size, block_table_stride, causal);
     int v = validate_problem(pr);
     if (v) return static_cast<ua_status>(v);
+    to_16_token_pages(pr);
     DeviceState *ds = nullptr;
     ua_status st = device_state(&ds);
     if (st != UA_OK) return st;
     thread_local Plan plan;
     build_plan(pr, ds->sms, kPrefillEnabled, plan);
-    *bytes = plan.layout.total_bytes;
+    *bytes = plan.layout.total_bytes + expanded_table_bytes(num_seqs, block_table_stride, block_size);
     return UA_OK;
 }
 
@@ -311,12 +328,13 @@ extern "C" ua_status ua_workspace_size_fp8kv(const int32_t *cu_seqlens_q_host,
     int v = validate_problem(pr);
     if (v) return static_cast<ua_status>(v);
     if (head_size != 128) return UA_ERR_UNSUPPORTED;
+    to_16_token_pages(pr);
     DeviceState *ds = nullptr;
     ua_status st = device_state(&ds);
     if (st != UA_OK) return st;
     thread_local Plan plan;
     build_plan(pr, ds->sms, false, plan);     // every row in the decode kernel
-    *bytes = plan.layout.total_bytes;
+    *bytes = plan.layout.total_bytes + expanded_table_bytes(num_seqs, block_table_stride, block_size);
     return UA_OK;
 }
 
@@ -443,6 +461,34 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
                         int32_t block_table_stride, void *workspace, size_t workspace_bytes,
                         void *stream_ptr, bool pinned_plan, float *lse, int kv_fp8, float k_scale,
                         float v_scale) {
+    // Pages of block_size = 16 r tokens: the same memory is a cache of 16-token
+    // pages; expand the block table into the front of the workspace and run
+    // the call on that view.
+    if (block_size != kBlockSize) {
+        Problem chk = make_problem(cu_seqlens_q_host, seqused_k_host, num_seqs, num_q_heads,
+                                   num_kv_heads, head_size, block_size, block_table_stride, causal);
+        const int v = validate_problem(chk);
+        if (v) return static_cast<ua_status>(v);
+        if (num_seqs == 0 || cu_seqlens_q_host[num_seqs] == 0) return UA_OK;
+        const int32_t r = block_size / kBlockSize;
+        if (!block_table || num_blocks <= 0 ||
+            (int64_t)num_blocks * block_size >= ((int64_t)1 << 31))
+            return UA_ERR_INVALID_ARG;
+        const size_t xb = expanded_table_bytes(num_seqs, block_table_stride, block_size);
+        if (!workspace || workspace_bytes < xb || !aligned(workspace, kAlign)) return UA_ERR_WORKSPACE;
+        int32_t *xbt = static_cast<int32_t *>(workspace);
+        if (launch_expand_block_table(block_table, xbt, (int64_t)num_seqs * block_table_stride, r,
+                                      num_blocks, static_cast<cudaStream_t>(stream_ptr)) != cudaSuccess) {
+            cudaGetLastError();
+            return UA_ERR_CUDA;
+        }
+        return run_attention(q, k_cache, v_cache, cu_seqlens_q, seqused_k, xbt, softmax_scale, causal,
+                             out, cu_seqlens_q_host, seqused_k_host, num_seqs, num_q_heads,
+                             num_kv_heads, head_size, kBlockSize, num_blocks * r,
+                             block_table_stride * r, static_cast<uint8_t *>(workspace) + xb,
+                             workspace_bytes - xb, stream_ptr, pinned_plan, lse, kv_fp8, k_scale,
+                             v_scale);
+    }
     // ---- host-side checks, before any CUDA call
     Problem pr = make_problem(cu_seqlens_q_host, seqused_k_host, num_seqs, num_q_heads,
                               num_kv_heads, head_size, block_size, block_table_stride, causal);
@@ -681,8 +727,9 @@ extern "C" ua_status ua_kv_append(const void *k_new, const void *v_new, const in
     ua_status st = device_state(&ds);
     if (st != UA_OK) return st;
     if (launch_kv_append(k_new, v_new, cu_seqlens_q, seqused_k, block_table, k_cache, v_cache,
-                         num_seqs, cu_seqlens_q_host[num_seqs], num_kv_heads, head_size, num_blocks,
-                         block_table_stride, ds->status, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+                         num_seqs, cu_seqlens_q_host[num_seqs], num_kv_heads, head_size, block_size,
+                         num_blocks, block_table_stride, ds->status,
+                         static_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return UA_ERR_CUDA;
     }
@@ -745,17 +792,20 @@ static ua_status device_plan_shape(int32_t num_seqs, int32_t max_total_q, int32_
                                    int32_t bt_stride, int32_t kv_fp8, int sms, DevPlanShape *s) {
     if (num_seqs < 0 || max_total_q < 0 || max_seq_q < 0 || hq <= 0 || hkv <= 0 || bt_stride < 0)
         return UA_ERR_INVALID_ARG;
-    if (hq % hkv != 0 || (d != 64 && d != 128) || bs != kBlockSize) return UA_ERR_UNSUPPORTED;
+    if (hq % hkv != 0 || (d != 64 && d != 128)) return UA_ERR_UNSUPPORTED;
+    if (bs <= 0 || bs % kBlockSize != 0 || bs > kMaxBlockSize) return UA_ERR_UNSUPPORTED;
     if (kv_fp8 && d != 128) return UA_ERR_UNSUPPORTED;
+    if ((int64_t)bt_stride * (bs / kBlockSize) > INT32_MAX / 4) return UA_ERR_INVALID_ARG;
     if ((int64_t)max_total_q * (hq / hkv) > INT32_MAX / 2) return UA_ERR_INVALID_ARG;
-    Problem pr = make_problem(nullptr, nullptr, 0, hq, hkv, d, bs, bt_stride, 1);
+    Problem pr = make_problem(nullptr, nullptr, 0, hq, hkv, d, kBlockSize, bt_stride, 1);
+    s->page_ratio = bs / kBlockSize;
     s->num_seqs = num_seqs;
     s->max_total_q = max_total_q;
     s->max_seq_q = (max_seq_q == 0 || max_seq_q > max_total_q) ? max_total_q : max_seq_q;
     s->hq = hq;
     s->hkv = hkv;
     s->d = d;
-    s->bt_stride = bt_stride;
+    s->bt_stride = bt_stride * s->page_ratio;   // in 16-token pages
     s->hpu = (kv_fp8 && hkv % 2 == 0) ? 2 : 1;
     // no sequence can fill more than one decode tile: the prefill kernel never has work
     const bool can_prefill = (int64_t)s->max_seq_q * (hq / hkv) > kDecRows;
@@ -795,7 +845,10 @@ static ua_status run_attention_device_plan(
     }
     const DevPlanLayout L = device_plan_layout(shape);
     if (!L.valid) return UA_ERR_UNSUPPORTED;
-    if (!workspace || workspace_bytes < L.total_bytes || !aligned(workspace, kAlign))
+    // pages of 16 r tokens: the block table expanded to 16-token pages, after
+    // the plan's sections
+    const size_t xb = expanded_table_bytes(num_seqs, block_table_stride, block_size);
+    if (!workspace || workspace_bytes < L.total_bytes + xb || !aligned(workspace, kAlign))
         return UA_ERR_WORKSPACE;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -806,6 +859,16 @@ static ua_status run_attention_device_plan(
         return UA_OK;
     }
 
+    if (shape.page_ratio > 1) {
+        int32_t *xbt = reinterpret_cast<int32_t *>(ws + L.total_bytes);
+        if (launch_expand_block_table(block_table, xbt, (int64_t)num_seqs * block_table_stride,
+                                      shape.page_ratio, num_blocks, stream) != cudaSuccess)
+            return UA_ERR_CUDA;
+        block_table = xbt;
+        num_blocks *= shape.page_ratio;
+        block_table_stride = shape.bt_stride;
+        block_size = kBlockSize;
+    }
     // tensor maps over the caller's buffers (q / out sized for max_total_q tokens)
     const int g = num_q_heads / num_kv_heads;
     CUtensorMap tm_kp, tm_vp, tm_q, tm_o, tm_k3;
@@ -925,7 +988,7 @@ extern "C" ua_status ua_workspace_size_device_plan(int32_t num_seqs, int32_t max
     if (st != UA_OK) return st;
     const DevPlanLayout L = device_plan_layout(shape);
     if (!L.valid) return UA_ERR_UNSUPPORTED;
-    *bytes = L.total_bytes;
+    *bytes = L.total_bytes + expanded_table_bytes(num_seqs, block_table_stride, block_size);
     return UA_OK;
 }
 
@@ -943,8 +1006,9 @@ extern "C" ua_status ua_device_plan_layout(int32_t num_seqs, int32_t max_total_q
     if (st != UA_OK) return st;
     const DevPlanLayout L = device_plan_layout(shape);
     if (!L.valid) return UA_ERR_UNSUPPORTED;
+    const size_t total = L.total_bytes + expanded_table_bytes(num_seqs, block_table_stride, block_size);
     const size_t off[8] = {L.off_header, L.off_cta,       L.off_pieces,    L.off_comb,
-                           L.off_comb_count, L.off_tiles, L.off_pre_begin, L.total_bytes};
+                           L.off_comb_count, L.off_tiles, L.off_pre_begin, total};
     for (int i = 0; i < 8; ++i) offsets[i] = (int64_t)off[i];
     const int32_t cap[8] = {L.dec_grid, L.cap_units, L.cap_items, L.cap_pieces,
                             L.cap_comb, L.cap_slots, L.n_buckets, shape.num_sms};

@@ -90,6 +90,7 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
 // prefill kernel may take rows, and the SM count (decode grid
 // kDecCtasPerSm * num_sms, prefill grid num_sms).
 struct DevPlanShape {
+    int32_t page_ratio;    // caller's page size / 16 (bt_stride below counts 16-token pages)
     int32_t num_seqs;
     int32_t max_total_q;
     int32_t max_seq_q;     // query tokens of one sequence at most
@@ -122,11 +123,19 @@ cudaError_t launch_device_plan(const DevPlanShape &s, const DevPlanLayout &L, co
                                int *status, cudaStream_t stream);
 
 // Writes the new tokens' K / V rows ([total_q, Hkv, D] bf16) into their
-// pages: token i of sequence s to position seqused_k[s] - Lq + i.
+// pages of block_size tokens: token i of sequence s to position
+// seqused_k[s] - Lq + i.
 cudaError_t launch_kv_append(const void *k_new, const void *v_new, const int32_t *cu,
                              const int32_t *seqused_k, const int32_t *block_table, void *k_cache,
                              void *v_cache, int32_t num_seqs, int32_t total_q, int32_t num_kv_heads,
-                             int32_t head_size, int32_t num_blocks, int32_t bt_stride, int *status,
-                             cudaStream_t stream);
+                             int32_t head_size, int32_t block_size, int32_t num_blocks,
+                             int32_t bt_stride, int *status, cudaStream_t stream);
+
+// Pages of block_size = 16 r tokens as runs of r 16-token pages: entry j of
+// each block-table row (num_seqs * stride entries), page b, becomes entries
+// j r .. j r + r - 1 = b r .. b r + r - 1 of `out` (-1 for an entry outside
+// [0, num_blocks)).  ua_pages.cu.
+cudaError_t launch_expand_block_table(const int32_t *block_table, int32_t *out, int64_t entries,
+                                      int32_t r, int32_t num_blocks, cudaStream_t stream);
 
 }  // namespace ua

@@ -7,7 +7,8 @@
 // PR description: the FlashAttention-layout cache and the engine's varlen
 // metadata); the new tokens are the last Lq positions of that context
 // (bottom-right, as in the causal mask), so token i of sequence s goes to
-// position p = Lk - Lq + i: page block_table[s][p / 16], slot p % 16.
+// position p = Lk - Lq + i: page block_table[s][p / block_size], slot
+// p % block_size.
 //
 // A warp per token (grid-stride): it finds its sequence by binary search in
 // cu_seqlens_q and copies Hkv * D bf16 of K and of V with 16-byte loads and
@@ -37,7 +38,8 @@ __global__ void __launch_bounds__(256)
                         const int32_t *__restrict__ cu, const int32_t *__restrict__ seqused_k,
                         const int32_t *__restrict__ block_table, uint4 *__restrict__ k_cache,
                         uint4 *__restrict__ v_cache, int32_t num_seqs, int32_t total_q,
-                        int32_t row_vec, int32_t num_blocks, int32_t bt_stride, int *status) {
+                        int32_t row_vec, int32_t block_size, int32_t num_blocks, int32_t bt_stride,
+                        int *status) {
     const int lane = threadIdx.x & 31;
     const int32_t warps = (int32_t)(gridDim.x * (blockDim.x >> 5));
     for (int32_t t = (int32_t)(blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)); t < total_q;
@@ -51,13 +53,13 @@ __global__ void __launch_bounds__(256)
         const int32_t q0 = __ldg(cu + lo), lq = __ldg(cu + lo + 1) - q0;
         const int32_t pos = __ldg(seqused_k + lo) - lq + (t - q0);
         int32_t page = -1;
-        if (pos >= 0 && pos / kBlockSize < bt_stride)
-            page = __ldg(block_table + (int64_t)lo * bt_stride + pos / kBlockSize);
+        if (pos >= 0 && pos / block_size < bt_stride)
+            page = __ldg(block_table + (int64_t)lo * bt_stride + pos / block_size);
         if (page < 0 || page >= num_blocks) {
             if (lane == 0) atomicOr(status, UA_DEVICE_BAD_BLOCK_ID_BIT);
             continue;
         }
-        const int64_t dst = ((int64_t)page * kBlockSize + pos % kBlockSize) * row_vec;
+        const int64_t dst = ((int64_t)page * block_size + pos % block_size) * row_vec;
         const int64_t src = (int64_t)t * row_vec;
         uint4 kv[kAppendMaxVec], vv[kAppendMaxVec];
 #pragma unroll
@@ -82,8 +84,8 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_kv_append(const void *k_new, const void *v_new, const int32_t *cu,
                              const int32_t *seqused_k, const int32_t *block_table, void *k_cache,
                              void *v_cache, int32_t num_seqs, int32_t total_q, int32_t num_kv_heads,
-                             int32_t head_size, int32_t num_blocks, int32_t bt_stride, int *status,
-                             cudaStream_t stream) {
+                             int32_t head_size, int32_t block_size, int32_t num_blocks,
+                             int32_t bt_stride, int *status, cudaStream_t stream) {
     const int32_t row_vec = num_kv_heads * head_size * 2 / 16;
     if (row_vec > 32 * kAppendMaxVec) return cudaErrorInvalidValue;
     int dev = 0, sms = 0;
@@ -95,7 +97,7 @@ cudaError_t launch_kv_append(const void *k_new, const void *v_new, const int32_t
     ua_kv_append_kernel<<<blocks, 256, 0, stream>>>(
         static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), cu, seqused_k,
         block_table, static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), num_seqs, total_q,
-        row_vec, num_blocks, bt_stride, status);
+        row_vec, block_size, num_blocks, bt_stride, status);
     return cudaGetLastError();
 }
 

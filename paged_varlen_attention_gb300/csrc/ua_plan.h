@@ -40,7 +40,9 @@
 
 namespace ua {
 
-constexpr int kBlockSize = 16;      // tokens per KV page (the supported page size)
+constexpr int kBlockSize = 16;      // tokens per KV page as the kernels see it
+constexpr int kMaxBlockSize = 256;  // caller pages: multiples of kBlockSize up to this (viewed as
+                                    // runs of 16-token pages)
 constexpr int kDecRows = 16;        // packed rows per decode tile (warp MMA M)
 constexpr int kPreRows = 128;       // packed rows per tcgen05 tile (MMA M)
 constexpr int kPreTileRows = 256;   // packed rows per prefill work item (two MMA tiles)

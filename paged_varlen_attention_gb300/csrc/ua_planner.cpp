@@ -26,7 +26,9 @@ int validate_problem(const Problem &p) {
     if (p.num_seqs > 0 && (p.cu == nullptr || p.lk == nullptr)) return 1;
     if (p.hq % p.hkv != 0) return 2;
     if (p.d != 64 && p.d != 128) return 2;
-    if (p.bs != kBlockSize) return 2;
+    if (p.bs <= 0 || p.bs % kBlockSize != 0 || p.bs > kMaxBlockSize) return 2;
+    // the block table seen in 16-token pages stays indexable in int32
+    if ((int64_t)p.bt_stride * (p.bs / kBlockSize) > INT32_MAX / 4) return 1;
     if (p.num_seqs == 0) return 0;
     if (p.cu[0] != 0) return 1;
     for (int s = 0; s < p.num_seqs; ++s) {

@@ -36,7 +36,8 @@ def layout(lib, num_seqs, max_total_q, max_seq_q, hq, hkv, d, stride, fp8=0, sms
 def test_shapes_are_checked_on_the_host(lib):
     assert layout(lib, 4, 64, 0, 32, 8, 96, 64)[0] == UNSUPPORTED      # head size
     assert layout(lib, 4, 64, 0, 30, 8, 128, 64)[0] == UNSUPPORTED     # Hq not a multiple of Hkv
-    assert layout(lib, 4, 64, 0, 32, 8, 128, 64, bs=32)[0] == UNSUPPORTED   # page size
+    assert layout(lib, 4, 64, 0, 32, 8, 128, 64, bs=24)[0] == UNSUPPORTED   # page size
+    assert layout(lib, 4, 64, 0, 32, 8, 128, 64, bs=512)[0] == UNSUPPORTED
     assert layout(lib, 4, 64, 0, 32, 8, 64, 64, fp8=1)[0] == UNSUPPORTED    # e4m3 needs D = 128
     assert layout(lib, -1, 64, 0, 32, 8, 128, 64)[0] == INVALID
     assert layout(lib, 4, -5, 0, 32, 8, 128, 64)[0] == INVALID
@@ -78,6 +79,17 @@ def test_capacities_and_sections(lib, ns, tq, msq, hq, hkv, d, stride, fp8):
     assert offs[2] - offs[1] >= 4 * (dec_grid + 1)                   # cta_begin
     assert offs[3] - offs[2] >= 32 * cap_pieces                      # pieces
     assert offs[6] - offs[5] >= 32 * cap_items                       # prefill items
+
+
+def test_larger_pages_add_the_expanded_block_table(lib):
+    """Pages of 16 r tokens: the plan is the 16-token view's (block table r times
+    wider), and the workspace holds the expanded table too."""
+    rc16, o16, c16 = layout(lib, 8, 64, 0, 32, 8, 128, 128)
+    rc32, o32, c32 = layout(lib, 8, 64, 0, 32, 8, 128, 64, bs=32)
+    assert rc16 == rc32 == OK
+    assert list(o16[:7]) == list(o32[:7]) and list(c16) == list(c32)
+    table = -(-(8 * 64 * 2 * 4) // 256) * 256
+    assert o32[7] == o16[7] + table
 
 
 def test_workspace_grows_with_the_capacities(lib):

@@ -58,6 +58,8 @@ SDPA_CASES = [
     ([6, 1], [2, 1], 2, 2, 8, 16, False),          # non-causal allows Lq > Lk
     ([9, 2, 1], [23, 2, 50], 4, 4, 16, 4, True),   # small pages: many page crossings
     ([33], [70], 8, 2, 128, 16, True),
+    ([1, 40, 2], [130, 40, 64], 8, 2, 64, 64, True),   # larger pages: 64 tokens
+    ([3, 1], [100, 257], 4, 1, 16, 48, False),         # 48-token pages, ragged last page
 ]
 
 
@@ -334,7 +336,8 @@ def test_shared_prefix_cascade_equals_full_attention(causal_suffix):
         np.testing.assert_allclose(merged, ref, rtol=0, atol=1e-12)
 
 
-def test_kv_append_then_attention_equals_dense_attention():
+@pytest.mark.parametrize("bs", [16, 32])
+def test_kv_append_then_attention_equals_dense_attention(bs):
     """New tokens appended into the pages at positions Lk - Lq .. Lk - 1 (the
     reading that seqused_k counts them, bottom-right): attention over the cache
     afterwards equals attention over the dense concatenation old ++ new; the
@@ -343,16 +346,16 @@ def test_kv_append_then_attention_equals_dense_attention():
     hq, hk, d = 4, 2, 32
     k_lens = [o + n for o, n in zip(old, q_lens)]
     q, ks, vs, rng = random_dense(q_lens, k_lens, hq, hk, d, seed=47)
-    full = batch_from_dense(q, ks, vs, q_lens, hq, poison=False)
+    full = batch_from_dense(q, ks, vs, q_lens, hq, block_size=bs, poison=False)
     # the same pages, with the new tokens' rows holding garbage before the append
     before_k, before_v = full.k_cache.copy(), full.v_cache.copy()
     k_new = np.concatenate([k[o:] for k, o in zip(ks, old)])
     v_new = np.concatenate([v[o:] for v, o in zip(vs, old)])
     for s, (o, n) in enumerate(zip(old, q_lens)):
         for pos in range(o, o + n):
-            page = full.block_table[s, pos // 16]
-            before_k[page, pos % 16] = W.BF16_NAN
-            before_v[page, pos % 16] = W.BF16_NAN
+            page = full.block_table[s, pos // bs]
+            before_k[page, pos % bs] = W.BF16_NAN
+            before_v[page, pos % bs] = W.BF16_NAN
     after_k, after_v = oracle.kv_append(before_k, before_v, k_new, v_new, full.cu_seqlens_q,
                                         full.seqused_k, full.block_table)
     assert np.array_equal(after_k, full.k_cache) and np.array_equal(after_v, full.v_cache)
