@@ -1,6 +1,7 @@
 """Benchmark of unified paged varlen attention on one GB300 (or N replicas).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                    [--block-size 16|32|...|256]
 
 A step is one unified_attention call over one synthetic batch (the whole hot
 path: the partition pass, the plan copy, the decode / split-KV kernel with its
@@ -31,6 +32,8 @@ same attention as one direct call); kv_append_mistral_24b_16x1000 (writing
 16 000 new tokens' K/V into their pages); llama3_8b_decode_64x2k-4k_fp8kv (the
 headline batch over an E4M3 cache); llama3_8b_decode_64x2k-4k_graph (the
 headline batch planned on the GPU, one CUDA-graph replay per step).
+--block-size runs a standard batch over pages of 32 ... 256 tokens (same
+lengths and data recipe; the call then also expands the block table).
 
 Multi-GPU: one process per GPU under torchrun; each rank runs its own replica
 of the workload (no data-path collective, weak scaling); the time is the max
@@ -39,6 +42,7 @@ over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -90,7 +94,21 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--block-size", type=int, default=16,
+                    help="KV page size in tokens (a multiple of 16, at most 256) for the "
+                         "standard attention batches; the lengths and data recipe are unchanged")
+    args = ap.parse_args()
+    if args.block_size != 16 and args.workload not in WORKLOADS:
+        ap.error("--block-size applies to the standard attention batches only")
+    return args
+
+
+def workload_batch(idx, block_size=16):
+    """Standard batch ``idx`` (timed runs: no NaN poison) with pages of block_size tokens."""
+    spec = W.config_spec(idx)
+    if block_size != spec.block_size:
+        spec = dataclasses.replace(spec, block_size=block_size)
+    return W.materialize(spec, poison=False)
 
 
 def algorithmic_work(spec) -> dict:
@@ -297,13 +315,14 @@ def run_ours(args, rank, world, local, dist):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     idx = WORKLOADS[args.workload]
-    batch = W.config_batch(idx, poison=False)
+    batch = workload_batch(idx, args.block_size)
     spec = batch.spec
     dev = device_batch(batch, torch, device)
     out = torch.empty_like(dev["q"])
     cu_h, sk_h = batch.cu_seqlens_q.copy(), batch.seqused_k.copy()
     ws_bytes = ua.workspace_size(cu_h, sk_h, spec.num_q_heads, spec.num_kv_heads,
-                                 spec.head_size, batch.block_table_stride, spec.causal)
+                                 spec.head_size, batch.block_table_stride, spec.causal,
+                                 spec.block_size)
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
     flush = L2Flush(torch, device)
     stream = torch.cuda.current_stream(device)
@@ -352,6 +371,8 @@ def run_ours(args, rank, world, local, dist):
             if v >= 0:
                 kern[key].append(v)
         launches += sum(ln[:3])
+        # pages of more than 16 tokens: one block-table expansion launch per call
+        launches += int(spec.block_size != 16 and spec.total_q > 0)
     barrier(dist)
     ua.profile_enable(False)
     status = ua.device_status()
@@ -426,7 +447,7 @@ def run_reference(args, rank, world):
     fp8 = args.workload == FP8_WORKLOAD
     # the graph and fp8 workloads compute attention over the headline batch
     idx = WORKLOADS.get(args.workload, WORKLOADS[DEFAULT_WORKLOAD])
-    b = W.config_batch(idx, poison=False)
+    b = workload_batch(idx, args.block_size)
     s = b.spec
     if fp8:
         k8, v8 = W.fp8_caches(b, 0.05, 0.05)
@@ -466,7 +487,8 @@ def run_reference(args, rank, world):
             "dtype": "f64 (e4m3 kv)" if fp8 else "f64",
             "data": "synthetic", "impl": "reference",
             "config": {"workload": args.workload, "num_seqs": s.num_seqs,
-                       "q_tokens": s.total_q, "parallelism": "host cores"},
+                       "q_tokens": s.total_q, "block_size": s.block_size,
+                       "parallelism": "host cores"},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.max_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -487,14 +509,14 @@ def assemble(args, res, world, cpu):
         roof = {"kernel": "ua_prefill_kernel", "bound": "tensor", "achieved": achieved,
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"],
-                "traffic": ncu_traffic("prefill", args.workload),
+                "traffic": ncu_traffic("prefill", args.workload) if spec.block_size == 16 else None,
                 "per_launch": f"{work['flops']} algorithmic flops (4 Hq D per visible pair)",
                 "launch_ms": pre}
     else:
         achieved = work["decode_bytes"] / (dec / 1e3) / 1e9
         roof = {"kernel": "ua_decode_kernel", "bound": "hbm", "achieved": achieved,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                "traffic": ncu_traffic("decode", args.workload),
+                "traffic": ncu_traffic("decode", args.workload) if spec.block_size == 16 else None,
                 "per_launch": f"{work['decode_bytes']} algorithmic bytes (K+V rows once per kv "
                               "head, Q, O, block-table entries)",
                 "launch_ms": dec}
