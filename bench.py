@@ -31,7 +31,9 @@ llama3_70b_long_mixed_32x8k-32k_2x2048chunk); llama3_8b_cascade_64dec_shared4k
 same attention as one direct call); kv_append_mistral_24b_16x1000 (writing
 16 000 new tokens' K/V into their pages); llama3_8b_decode_64x2k-4k_fp8kv (the
 headline batch over an E4M3 cache); llama3_8b_decode_64x2k-4k_graph (the
-headline batch planned on the GPU, one CUDA-graph replay per step).
+headline batch planned on the GPU, one CUDA-graph replay per step);
+gemma2_9b_decode_64x2k-4k (the headline lengths with head size 256: Hq 16,
+Hkv 8).
 --block-size runs a standard batch over pages of 32 ... 256 tokens (same
 lengths and data recipe; the call then also expands the block table).
 
@@ -68,6 +70,7 @@ WORKLOADS = {
     "mistral_24b_prefill_16x1000": 3,
     "llama3_8b_mixed_256dec_4x512chunk": 4,
     "llama3_70b_long_mixed_32x8k-32k_2x2048chunk": 5,
+    "gemma2_9b_decode_64x2k-4k": 6,
 }
 DEFAULT_WORKLOAD = "llama3_8b_decode_64x2k-4k"
 # Cascade (shared-prefix) step: 64 decode sequences (Llama-3.1-8B heads) that
@@ -457,7 +460,7 @@ def run_reference(args, rank, world):
             return oracle.attention_fp8kv(q, k8, v8, 0.05, 0.05, cu, sk, bt, s.softmax_scale, s.causal)
         return oracle.attention(q, b.k_cache, b.v_cache, cu, sk, bt, s.softmax_scale, s.causal)
     # per step: a rotating window of sequences sized to a few tenths of a second
-    per_step = max(1, min(s.num_seqs, 8 if idx in (1, 2) else 2))
+    per_step = max(1, min(s.num_seqs, 8 if idx in (1, 2, 6) else 2))
     if idx == 1:
         per_step = s.num_seqs
 

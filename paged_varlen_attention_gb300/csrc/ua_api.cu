@@ -792,7 +792,7 @@ static ua_status device_plan_shape(int32_t num_seqs, int32_t max_total_q, int32_
                                    int32_t bt_stride, int32_t kv_fp8, int sms, DevPlanShape *s) {
     if (num_seqs < 0 || max_total_q < 0 || max_seq_q < 0 || hq <= 0 || hkv <= 0 || bt_stride < 0)
         return UA_ERR_INVALID_ARG;
-    if (hq % hkv != 0 || (d != 64 && d != 128)) return UA_ERR_UNSUPPORTED;
+    if (hq % hkv != 0 || (d != 64 && d != 128 && d != 256)) return UA_ERR_UNSUPPORTED;
     if (bs <= 0 || bs % kBlockSize != 0 || bs > kMaxBlockSize) return UA_ERR_UNSUPPORTED;
     if (kv_fp8 && d != 128) return UA_ERR_UNSUPPORTED;
     if ((int64_t)bt_stride * (bs / kBlockSize) > INT32_MAX / 4) return UA_ERR_INVALID_ARG;

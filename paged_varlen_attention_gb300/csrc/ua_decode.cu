@@ -45,14 +45,22 @@ namespace ua {
 // a slot, a 256-byte run of the cache, and the 16-row tile holds head kvh in
 // rows 0-7 and head kvh + 1 in rows 8-15; S and P V run once per head, each
 // keeping the rows of its own head.  D = 128 only.
+//
+// D = 256: a thread holds 64 registers of Q fragments and 128 of the O
+// accumulator, so the kernel runs one CTA per SM (up to 255 registers a
+// thread) with a deeper ring of 16 KB stages; every row of such a batch
+// comes here (the tensor-core prefill kernel is laid out for D <= 128).
 template <int D, bool KV8>
 struct DecCfg {
     static_assert(!KV8 || D == 128, "the e4m3 path is laid out for D = 128");
+    static_assert(D == 64 || D == 128 || D == 256, "head sizes 64, 128 and 256");
     static constexpr int kChunks = D / 64;                        // 64-column TMA boxes per row
     static constexpr int kHeadPageBytes = kBlockSize * D * (KV8 ? 1 : 2);   // one page of one kv head
     static constexpr int kPageBytes = (KV8 ? 2 : 1) * kHeadPageBytes;      // K (or V) part of a stage
     static constexpr int kStageBytes = 2 * kPageBytes;           // K + V
-    static constexpr int kStages = (D == 128) ? 8 : 16;          // 64 KB of stages
+    // 64 KB of stages at two CTAs per SM; 128 KB at one (D = 256)
+    static constexpr int kStages = (D == 64) ? 16 : 8;
+    static constexpr int kMinCtasPerSm = (D == 256) ? 1 : 2;
     static constexpr int kConsumerWarps = 4;
     static constexpr int kThreads = (kConsumerWarps + 1) * 32;
     static constexpr int kMergeFloats = kDecRows * D + 2 * kDecRows;   // per warp
@@ -64,6 +72,7 @@ struct DecCfg {
     static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes +
                                          kMergeBytes + (size_t)kRing * (kQTileBytes + kDescInts * 4) +
                                          (2 * kStages + 2 * kRing) * 8;
+    static_assert(kSmemBytes + 64 <= 232448, "dynamic shared memory above 227 KB");
 };
 
 // Fields of a piece descriptor in the shared-memory ring.
@@ -185,7 +194,7 @@ __device__ __forceinline__ void merge_unit(const DecodeParams &p, int q0, int kv
 }
 
 template <int D, bool KV8>
-__global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, 2)
+__global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, DecCfg<D, KV8>::kMinCtasPerSm)
     ua_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v) {
     using C = DecCfg<D, KV8>;
@@ -661,8 +670,12 @@ cudaError_t launch_decode(int d, bool kv8, const DecodeParams &p, const CUtensor
         if (d != 128) return cudaErrorInvalidValue;
         return launch_decode_t<128, true>(p, tm_k, tm_v, ctas, stream);
     }
-    return d == 64 ? launch_decode_t<64, false>(p, tm_k, tm_v, ctas, stream)
-                   : launch_decode_t<128, false>(p, tm_k, tm_v, ctas, stream);
+    switch (d) {
+        case 64: return launch_decode_t<64, false>(p, tm_k, tm_v, ctas, stream);
+        case 128: return launch_decode_t<128, false>(p, tm_k, tm_v, ctas, stream);
+        case 256: return launch_decode_t<256, false>(p, tm_k, tm_v, ctas, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace ua

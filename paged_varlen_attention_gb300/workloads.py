@@ -108,7 +108,7 @@ class Batch:
 
 
 # --------------------------------------------------------------------------
-# The five standard batches.  Index 1..5.
+# The five standard batches (index 1..5), and a head-size-256 decode batch (6).
 # --------------------------------------------------------------------------
 
 CONFIG_NAMES = {
@@ -117,6 +117,7 @@ CONFIG_NAMES = {
     3: "mistral_24b_prefill_16x1000",
     4: "llama3_8b_mixed_256dec_4x512chunk",
     5: "llama3_70b_long_mixed_32x8k-32k_2x2048chunk",
+    6: "gemma2_9b_decode_64x2k-4k",
 }
 
 
@@ -148,6 +149,12 @@ def config_spec(idx: int) -> Spec:
         q = np.concatenate([np.ones(32, np.int64), np.full(2, 2048)])
         k = np.concatenate([dec, np.full(2, 4096 + 2048)])
         return Spec(name, q, k, 64, 8, 128, data_seed=data_seed, layout_seed=layout_seed)
+    if idx == 6:
+        # the Llama-3.1-8B decode batch's lengths with Gemma-2-9B's attention
+        # heads (Hq 16, Hkv 8, head size 256, scale 1/sqrt(256))
+        k = rng.integers(2048, 4096, size=64, endpoint=True)
+        return Spec(name, np.ones(64, np.int32), k, 16, 8, 256,
+                    data_seed=data_seed, layout_seed=layout_seed)
     raise ValueError(f"unknown config {idx}")
 
 

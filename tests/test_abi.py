@@ -68,7 +68,8 @@ def _call(lib, cu, sk, hq=4, hk=2, d=64, bs=16, nb=8, stride=4, causal=1, scale=
     (dict(cu=[0, 3, 2], sk=[17, 40]), 1),         # decreasing cu
     (dict(cu=[0, 1, 6], sk=[17, 90]), 1),         # needs more pages than the table holds
     (dict(cu=[0, 1, 6], sk=[17, 40], hq=6, hk=4), 2),   # Hq not a multiple of Hkv
-    (dict(cu=[0, 1, 6], sk=[17, 40], d=96), 2),   # unsupported head size
+    (dict(cu=[0, 1, 6], sk=[17, 40], d=96), 2),   # unsupported head sizes
+    (dict(cu=[0, 1, 6], sk=[17, 40], d=512), 2),
     (dict(cu=[0, 1, 6], sk=[17, 40], bs=24), 2),  # pages not a multiple of 16 tokens
     (dict(cu=[0, 1, 6], sk=[17, 40], bs=512), 2), # pages above 256 tokens
     (dict(cu=[0, 1, 6], sk=[17, 40], bs=32, stride=2), 3),   # 32-token pages: no workspace for the table

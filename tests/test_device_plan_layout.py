@@ -39,6 +39,7 @@ def test_shapes_are_checked_on_the_host(lib):
     assert layout(lib, 4, 64, 0, 32, 8, 128, 64, bs=24)[0] == UNSUPPORTED   # page size
     assert layout(lib, 4, 64, 0, 32, 8, 128, 64, bs=512)[0] == UNSUPPORTED
     assert layout(lib, 4, 64, 0, 32, 8, 64, 64, fp8=1)[0] == UNSUPPORTED    # e4m3 needs D = 128
+    assert layout(lib, 4, 64, 0, 32, 8, 256, 64, fp8=1)[0] == UNSUPPORTED
     assert layout(lib, -1, 64, 0, 32, 8, 128, 64)[0] == INVALID
     assert layout(lib, 4, -5, 0, 32, 8, 128, 64)[0] == INVALID
     assert layout(lib, 4, 64, -1, 32, 8, 128, 64)[0] == INVALID
@@ -55,6 +56,7 @@ def test_shapes_are_checked_on_the_host(lib):
     (64, 64, 1, 32, 8, 128, 256, 1),       # e4m3, paired heads
     (10, 40, 0, 12, 3, 128, 40, 1),        # e4m3, odd Hkv: one head per unit
     (5, 900, 0, 4, 4, 64, 300, 0),         # G = 1, D = 64
+    (8, 3000, 0, 16, 8, 256, 250, 0),      # D = 256: every row in the decode kernel
 ])
 def test_capacities_and_sections(lib, ns, tq, msq, hq, hkv, d, stride, fp8):
     rc, offs, caps = layout(lib, ns, tq, msq, hq, hkv, d, stride, fp8)
@@ -66,7 +68,7 @@ def test_capacities_and_sections(lib, ns, tq, msq, hq, hkv, d, stride, fp8):
     dec_grid, cap_units, cap_items, cap_pieces, cap_comb, cap_slots, buckets, sms = caps.tolist()
     assert sms == 152 and dec_grid == 2 * 152
     assert cap_units == (hkv // hpu) * (ns + -(-tq * g // step))
-    prefill_possible = not fp8 and msq_eff * g > 16 and 128 % g == 0
+    prefill_possible = not fp8 and d <= 128 and msq_eff * g > 16 and 128 % g == 0
     assert cap_items == (hkv * (ns + -(-tq * g // 256)) if prefill_possible else 0)
     assert cap_pieces == cap_units + dec_grid
     assert cap_comb == min(cap_units, dec_grid)

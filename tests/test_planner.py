@@ -197,3 +197,13 @@ def test_few_long_prefill_items_go_to_the_decode_kernel():
     # short contexts stay on the prefill kernel even with few items
     c = check_plan([200], [200], 8, 2, 128)
     assert c["prefill_tiles"] > 0
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_head_size_256_puts_every_row_in_decode_units(causal):
+    """Head size 256: the tensor-core prefill kernel is laid out for D <= 128,
+    so prefill and chunked-prefill rows become 16-row decode units too."""
+    c = check_plan([1, 300, 64, 1, 1000], [4000, 300, 2000, 17, 1000], 16, 8, 256, causal=causal)
+    assert c["prefill_tiles"] == 0 and c["prefill_ctas"] == 0
+    units = 8 * sum(-(-lq * 2 // 16) for lq in [1, 300, 64, 1, 1000])    # G = 2, Hkv = 8
+    assert c["dec_ctas"] > 0 and c["pieces"] >= units
