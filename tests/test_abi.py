@@ -105,3 +105,17 @@ def test_kv_append_rejects_more_new_tokens_than_context(lib):
     rc = lib.ua_kv_append(p, p, p, p, p, p, p, cu.ctypes.data_as(ctypes.c_void_p),
                           sk.ctypes.data_as(ctypes.c_void_p), 1, 2, 64, 16, 8, 1, None)
     assert rc == 1                        # UA_ERR_INVALID_ARG, nothing launched
+
+
+def test_missing_library_raises_no_fallback(monkeypatch, tmp_path):
+    """Without the built CUDA library every entry point raises: nothing falls
+    back to another implementation."""
+    monkeypatch.setattr(B, "_lib", None)
+    monkeypatch.setattr(B, "_LIB_PATH", str(tmp_path / "libua_gb300.so"))
+    with pytest.raises(B.UAError) as e:
+        B.load_library()
+    assert e.value.status == 4
+    with pytest.raises(B.UAError):
+        B.workspace_size(np.array([0, 1], np.int32), np.array([5], np.int32), 4, 2, 64, 1)
+    with pytest.raises(B.UAError):
+        B.plan_inspect(np.array([0, 1], np.int32), np.array([5], np.int32), 4, 2, 64, 1)
