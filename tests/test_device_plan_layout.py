@@ -99,3 +99,36 @@ def test_workspace_grows_with_the_capacities(lib):
     more_tokens = layout(lib, 64, 4096, 0, 32, 8, 128, 256)[1][7]
     more_seqs = layout(lib, 512, 512, 1, 32, 8, 128, 256)[1][7]
     assert small < more_tokens and small < more_seqs
+
+
+@pytest.mark.parametrize("seed", range(200))
+def test_capacities_bound_the_plan_of_random_batches(lib, seed):
+    """The device planner writes the same plan as the host planner (a GPU test
+    checks that field for field), into sections sized by these capacities: for
+    any batch that fits the shape, every count of the host plan must fit."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    hq, hkv = [(32, 8), (8, 2), (4, 4), (16, 2), (64, 8), (12, 3), (32, 2)][seed % 7]
+    d = [64, 128, 256][seed % 3]
+    causal = bool(seed % 4)
+    ns = int(rng.integers(1, 49))
+    kind = rng.random(ns)
+    lq = np.where(kind < 0.6, 1, rng.integers(2, 700, ns))
+    lq = np.where(kind > 0.95, 0, lq)
+    lk = lq + rng.integers(0, 3000, ns)
+    lk = np.maximum(lk, 1)
+    cu = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    stride = int(-(-lk.max() // 16)) + int(rng.integers(0, 5))
+    total = int(cu[-1])
+    max_total_q = total + int(rng.integers(0, 64))
+    max_seq_q = int(rng.choice([0, int(lq.max()) + int(rng.integers(0, 8))]))
+    sms = 152
+    counts, _ = B.plan_inspect(cu, lk.astype(np.int32), hq, hkv, d, stride, causal, num_sms=sms)
+    rc, offs, caps = layout(lib, ns, max_total_q, max_seq_q, hq, hkv, d, stride, sms=sms)
+    assert rc == OK
+    dec_grid, cap_units, cap_items, cap_pieces, cap_comb, cap_slots, buckets, _ = caps.tolist()
+    assert counts["dec_ctas"] <= dec_grid
+    assert counts["pieces"] <= cap_pieces
+    assert counts["split_units"] <= cap_comb
+    assert counts["slots"] <= cap_slots
+    assert counts["prefill_tiles"] <= cap_items
+    assert counts["prefill_ctas"] <= sms
