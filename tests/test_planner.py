@@ -173,8 +173,9 @@ def test_small_shapes(case, num_sms, causal):
     check_plan(q, k, hq, hk, 64, causal, num_sms)
 
 
-def test_random_batches():
-    rng = np.random.default_rng(7)
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_random_batches(d):
+    rng = np.random.default_rng(7 + d)
     for _ in range(30):
         n = int(rng.integers(1, 12))
         q = rng.integers(0, 40, n)
@@ -182,7 +183,10 @@ def test_random_batches():
         k[(q == 0) & (k == 0)] = 1
         hk = int(rng.choice([1, 2, 4, 8]))
         hq = hk * int(rng.choice([1, 2, 3, 4, 8, 16]))
-        check_plan(q, k, hq, hk, 128, True, int(rng.integers(1, 200)))
+        causal = bool(rng.integers(0, 2))     # k >= q: both modes are valid
+        c = check_plan(q, k, hq, hk, d, causal, int(rng.integers(1, 200)))
+        if d == 256:
+            assert c["prefill_tiles"] == 0
 
 
 def test_few_long_prefill_items_go_to_the_decode_kernel():
