@@ -116,16 +116,15 @@ def check_plan(q_lens, k_lens, hq, hk, d=128, causal=True, num_sms=152):
     elif tiles:
         assert ctas == sorted(ctas) and min(ctas) >= 0
         assert counts["prefill_ctas"] == len(set(ctas)) <= num_sms
-        load, biggest = {}, 0
+        # the deal's key is the item's 128-key tiles (its row count is not
+        # weighed): totals of that key stay within the largest item
+        load = {}
         for t in tiles:
             _, cta, seq, kvh, row0, nrows, kvt, _ = t
-            cost = 3
-            for r0 in range(row0, row0 + nrows, 128):
-                last = min(r0 + 128, row0 + nrows) - 1
-                cost += -(-prefill_kend(int(q_lens[seq]), int(k_lens[seq]), last // g, causal) // 64)
-            load[cta] = load.get(cta, 0) + cost
-            biggest = max(biggest, cost)
-        assert max(load.values()) - min(load.values()) <= biggest
+            last = row0 + nrows - 1
+            assert kvt == -(-prefill_kend(int(q_lens[seq]), int(k_lens[seq]), last // g, causal) // 128)
+            load[cta] = load.get(cta, 0) + kvt
+        assert max(load.values()) - min(load.values()) <= max(t[6] for t in tiles)
         for c in set(ctas):
             kv = [t[6] for t in tiles if t[1] == c]
             assert kv == sorted(kv, reverse=True)
