@@ -194,10 +194,37 @@ def test_invariant_under_physical_placement():
     q, ks, vs, _ = random_dense(q_lens, k_lens, 4, 1, 64, seed=21)
     a = batch_from_dense(q, ks, vs, q_lens, 4, seed=1)
     b = batch_from_dense(q, ks, vs, q_lens, 4, seed=2, extra_blocks=5)
-    assert not np.array_equal(a.block_table[:, :1], b.block_table[:, :1]) or True
+    assert not np.array_equal(a.block_table, b.block_table)     # the pages do move
     oa, la = oracle.attention_batch(a)
     ob, lb = oracle.attention_batch(b)
     assert np.array_equal(oa, ob) and np.array_equal(la, lb)
+
+
+@pytest.mark.parametrize("bs", [32, 64, 256])
+def test_larger_pages_equal_their_16_token_view(bs):
+    """A cache of bs-token pages is, byte for byte, a cache of 16-token pages
+    with every block-table entry p replaced by p r .. p r + r - 1 (r = bs / 16):
+    the oracle gives the same bits over both views."""
+    q_lens, k_lens = [1, 40, 3], [300, 40, 257]
+    q, ks, vs, _ = random_dense(q_lens, k_lens, 8, 2, 32, seed=bs)
+    a = batch_from_dense(q, ks, vs, q_lens, 8, block_size=bs, seed=3)
+    r = bs // 16
+    nb, _, hk, d = a.k_cache.shape
+    bt = (a.block_table[:, :, None] * r + np.arange(r)).reshape(len(q_lens), -1).astype(np.int32)
+    oa, la = oracle.attention_batch(a)
+    ob, lb = oracle.attention(a.q, a.k_cache.reshape(nb * r, 16, hk, d),
+                              a.v_cache.reshape(nb * r, 16, hk, d), a.cu_seqlens_q, a.seqused_k,
+                              bt, a.spec.softmax_scale, True)
+    assert np.array_equal(oa, ob) and np.array_equal(la, lb)
+    # a wrong expansion (entries not multiplied by r) reads other keys; no NaN
+    # poison here, so that the wrong keys give finite, different rows
+    c = batch_from_dense(q, ks, vs, q_lens, 8, block_size=bs, seed=3, poison=False)
+    bad = (c.block_table[:, :, None] + np.arange(r)).reshape(len(q_lens), -1).astype(np.int32)
+    bad = np.minimum(bad, nb * r - 1)
+    oc, _ = oracle.attention(c.q, c.k_cache.reshape(nb * r, 16, hk, d),
+                             c.v_cache.reshape(nb * r, 16, hk, d), c.cu_seqlens_q, c.seqused_k,
+                             bad, c.spec.softmax_scale, True)
+    assert np.allclose(oracle.attention_batch(c)[0], oa) and not np.allclose(oc, oa)
 
 
 def test_aliased_pages_match_private_copies():
