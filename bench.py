@@ -431,7 +431,7 @@ def gpu_id_for_smi(torch, local):
     try:
         u = str(torch.cuda.get_device_properties(local).uuid)
         return u if u.startswith("GPU-") else f"GPU-{u}"
-    except Exception:
+    except (AttributeError, RuntimeError):
         vis = os.environ.get("CUDA_VISIBLE_DEVICES")
         if vis:
             return vis.split(",")[local].strip()
