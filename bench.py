@@ -704,8 +704,15 @@ def run_kv_append(args):
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
+    # The call's host work (argument checks, validation, launch) is long next to
+    # the ~20 us kernel and the L2 flush between calls, so the GPU would wait
+    # for each launch inside the timed interval.  A GPU-side spin before the
+    # first step (outside every interval) lets the host queue all steps first.
+    spin = getattr(torch.cuda, "_sleep", None)
     with ClockSampler(gpu_id_for_smi(torch, 0)) as clocks:
         torch.cuda.synchronize()
+        if spin is not None:
+            spin(200_000 * args.steps)          # ~100 us of cycles per queued step
         for a, e in evs:
             flush()
             a.record(stream)
@@ -729,7 +736,8 @@ def run_kv_append(args):
                    "parallelism": "1 GPU, no collective"},
         "roofline": {"kernel": "ua_kv_append_kernel", "bound": "hbm", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": None, "per_launch": f"{nbytes} bytes (K and V rows read + written)",
+                     "traffic": ncu_traffic("append", APPEND_WORKLOAD),
+                     "per_launch": f"{nbytes} bytes (K and V rows read + written)",
                      "launch_ms": ms, "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"},
         "gpu_launches": args.steps,
         "clocks": clocks.summary(),
