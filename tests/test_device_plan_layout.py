@@ -117,13 +117,15 @@ def test_capacities_bound_the_plan_of_random_batches(lib, seed):
     lk = lq + rng.integers(0, 3000, ns)
     lk = np.maximum(lk, 1)
     cu = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
-    stride = int(-(-lk.max() // 16)) + int(rng.integers(0, 5))
+    bs = [16, 32, 64, 256][(seed // 7) % 4]                   # page size in tokens
+    stride = int(-(-lk.max() // bs)) + int(rng.integers(0, 5))
     total = int(cu[-1])
     max_total_q = total + int(rng.integers(0, 64))
     max_seq_q = int(rng.choice([0, int(lq.max()) + int(rng.integers(0, 8))]))
     sms = 152
-    counts, _ = B.plan_inspect(cu, lk.astype(np.int32), hq, hkv, d, stride, causal, num_sms=sms)
-    rc, offs, caps = layout(lib, ns, max_total_q, max_seq_q, hq, hkv, d, stride, sms=sms)
+    counts, _ = B.plan_inspect(cu, lk.astype(np.int32), hq, hkv, d, stride, causal, num_sms=sms,
+                               block_size=bs)
+    rc, offs, caps = layout(lib, ns, max_total_q, max_seq_q, hq, hkv, d, stride, sms=sms, bs=bs)
     assert rc == OK
     dec_grid, cap_units, cap_items, cap_pieces, cap_comb, cap_slots, buckets, _ = caps.tolist()
     assert counts["dec_ctas"] <= dec_grid
