@@ -3,10 +3,10 @@
  * attention library (libua_gb300.so).
  *
  * The operation.  One call computes attention for a flattened batch that
- * mixes prefill, chunked-prefill and decode sequences.  This is the unified
- * kernel's statement of the problem: it "works like flash_attn_varlen_func"
- * for an arbitrary number of new query tokens per sequence, packs the query
- * heads that share a KV head together along the query dimension, and reads
+ * mixes prefill, chunked-prefill and decode sequences.  As the unified
+ * kernel states the problem, the call has the semantics of FlashAttention's
+ * varlen function for any number of new query tokens per sequence; it packs
+ * the query heads that share a KV head along the query dimension and reads
  * the key cache in the FlashAttention layout ("[Kernel] Unified Triton kernel
  * that doesn't distinguish between prefill + decode", vLLM PR #16828, PR
  * description, first and third bullets).  The batch is described by the

@@ -7,10 +7,10 @@
  *
  * What it computes follows the problem statement of the unified kernel
  * ("[Kernel] Unified Triton kernel that doesn't distinguish between prefill +
- * decode", vLLM PR #16828, PR description, first bullet): the kernel "works
- * like flash_attn_varlen_func" over an arbitrary number of new query tokens
- * per sequence, with the key cache in the FlashAttention layout (third
- * bullet).  Written out, for every sequence s, query head h and new token i:
+ * decode", vLLM PR #16828, PR description, first bullet): the kernel has the
+ * semantics of FlashAttention's varlen function over an arbitrary number of
+ * new query tokens per sequence, with the key cache in the FlashAttention
+ * layout (third bullet).  Written out, for every sequence s, query head h and new token i:
  *
  *     Lq = cu_seqlens_q[s+1] - cu_seqlens_q[s],   Lk = seqused_k[s]
  *     g  = h / (Hq / Hkv)                          (GQA: contiguous groups)
@@ -22,8 +22,8 @@
  *                     x_j  = scale * <q[t][h][:], k_j>       (fp64)
  *     out[t][h][:] = sum_j exp(x_j - max x) v_j / sum_j exp(x_j - max x)
  *
- * Non-causal mode (all Lk keys visible) is the review request on the same
- * page ("can we add support for non-casual attention too?").  The optional
+ * Non-causal mode (all Lk keys visible) answers a request in the review
+ * thread of the same page, which asks for it in addition to causal mode.  The optional
  * key window [key_lo, key_hi) restricts j further; it exists so tests can
  * form split-KV partials, and ua_oracle_merge() is the log-sum-exp merge of
  * such partials.
