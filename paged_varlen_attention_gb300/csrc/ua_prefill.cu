@@ -5,7 +5,7 @@
 // G heads and every K/V tile loaded from the paged cache feeds all of them
 // (the GQA packing of "[Kernel] Unified Triton kernel that doesn't
 // distinguish between prefill + decode", vLLM PR #16828, PR description,
-// there done "to ensure the Tensor cores are well used").
+// where it serves to keep the tensor cores busy).
 //
 // One persistent CTA per SM walks its work items, longest first: the items
 // dealt to it in advance, or (kClaimed: long items) items it claims from the

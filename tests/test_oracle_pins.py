@@ -1,7 +1,7 @@
 """Pins for the fp64 oracle: checks against things other than the oracle itself.
 
-The operation is attention over a flattened varlen batch "like
-flash_attn_varlen_func", with keys/values read page by page through a block
+The operation is attention over a flattened varlen batch with the semantics
+of FlashAttention's varlen function, with keys/values read page by page through a block
 table ("[Kernel] Unified Triton kernel that doesn't distinguish between prefill
 + decode", vLLM PR #16828, PR description).  Each test below would fail on a
 plausible mistake in the oracle: a wrong page/slot index, a top-left instead of
