@@ -21,10 +21,14 @@
 
 namespace ua {
 
+// out may alias out_a or out_b (the API allows merging in place), so the three
+// row pointers are not __restrict__ and are read with plain loads: each thread
+// reads its 8 elements of a row before it writes them, and no other thread
+// touches them.
 __global__ void __launch_bounds__(256)
-    ua_merge_kernel(const __nv_bfloat16 *__restrict__ out_a, const float *__restrict__ lse_a,
-                    const __nv_bfloat16 *__restrict__ out_b, const float *__restrict__ lse_b,
-                    __nv_bfloat16 *__restrict__ out, float *__restrict__ lse_out, int64_t rows, int d) {
+    ua_merge_kernel(const __nv_bfloat16 *out_a, const float *__restrict__ lse_a,
+                    const __nv_bfloat16 *out_b, const float *__restrict__ lse_b,
+                    __nv_bfloat16 *out, float *__restrict__ lse_out, int64_t rows, int d) {
     const int per_row = d / 8;
     const int64_t total = rows * per_row;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -40,8 +44,8 @@ __global__ void __launch_bounds__(256)
             lse = m + logf(wa + wb);
         }
         const float inv = (wa + wb) > 0.f ? 1.f / (wa + wb) : 0.f;
-        const uint4 va = __ldg(reinterpret_cast<const uint4 *>(out_a + r * d + c));
-        const uint4 vb = __ldg(reinterpret_cast<const uint4 *>(out_b + r * d + c));
+        const uint4 va = *reinterpret_cast<const uint4 *>(out_a + r * d + c);
+        const uint4 vb = *reinterpret_cast<const uint4 *>(out_b + r * d + c);
         const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&va);
         const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&vb);
         uint4 vo;

@@ -114,6 +114,12 @@ def test_merge_kernel_matches_fp64_merge():
     # a side with no key leaves the other side's row exactly
     only_b = np.isneginf(la) & ~np.isneginf(lb)
     assert np.array_equal(got[only_b], widen(ob)[only_b])
+    # in place (out = out_a, as the API allows): the same bits
+    a_dev = t(oa.view(np.int16), torch.bfloat16)
+    inplace, _ = ua.merge_attn_states(a_dev, t(la, torch.float32), t(ob.view(np.int16), torch.bfloat16),
+                                      t(lb, torch.float32), out=a_dev)
+    torch.cuda.synchronize()
+    assert inplace.data_ptr() == a_dev.data_ptr() and torch.equal(inplace, out)
 
 
 @pytest.mark.parametrize("hq,hk,d", [(32, 8, 128), (8, 8, 64)])
