@@ -119,3 +119,33 @@ def test_missing_library_raises_no_fallback(monkeypatch, tmp_path):
         B.workspace_size(np.array([0, 1], np.int32), np.array([5], np.int32), 4, 2, 64, 1)
     with pytest.raises(B.UAError):
         B.plan_inspect(np.array([0, 1], np.int32), np.array([5], np.int32), 4, 2, 64, 1)
+
+
+def test_binding_rejects_host_tensors_before_any_cuda_call(lib):
+    """The Python binding only marshals: tensors that are not contiguous CUDA
+    tensors of the right dtype are refused with UA_ERR_INVALID_ARG (1)."""
+    import torch
+    import paged_varlen_attention_gb300 as ua
+
+    q = torch.zeros(5, 4, 64, dtype=torch.bfloat16)
+    kc = torch.zeros(3, 16, 2, 64, dtype=torch.bfloat16)
+    cu = torch.tensor([0, 1, 5], dtype=torch.int32)
+    sk = torch.tensor([17, 40], dtype=torch.int32)
+    bt = torch.zeros(2, 3, dtype=torch.int32)
+    lse = torch.zeros(5, 4, dtype=torch.float32)
+    calls = [
+        lambda: ua.unified_attention(q, kc, kc, cu, sk, bt, 0.125, True,
+                                     cu_seqlens_q_host=cu.numpy(), seqused_k_host=sk.numpy()),
+        lambda: ua.kv_append(q[:, :2], q[:, :2], kc, kc, cu, sk, bt,
+                             cu_seqlens_q_host=cu.numpy(), seqused_k_host=sk.numpy()),
+        lambda: ua.merge_attn_states(q, lse, q, lse),
+        lambda: ua.unified_attention_fp8kv(q, kc.view(torch.uint8), kc.view(torch.uint8), 1.0, 1.0,
+                                           cu, sk, bt, 0.125, True, cu_seqlens_q_host=cu.numpy(),
+                                           seqused_k_host=sk.numpy()),
+        lambda: ua.unified_attention_device_plan(q, kc, kc, cu, sk, bt, 0.125, True,
+                                                 workspace=torch.zeros(256, dtype=torch.uint8)),
+    ]
+    for call in calls:
+        with pytest.raises(B.UAError) as e:
+            call()
+        assert e.value.status == 1
