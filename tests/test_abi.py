@@ -149,3 +149,32 @@ def test_binding_rejects_host_tensors_before_any_cuda_call(lib):
         with pytest.raises(B.UAError) as e:
             call()
         assert e.value.status == 1
+
+
+def test_header_is_plain_c_and_the_library_links_from_c(lib, tmp_path):
+    """The boundary is a C ABI: a C99 program includes the header, links the
+    library and makes a host-only call (shape check, no CUDA call)."""
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = tmp_path / "abi.c"
+    src.write_text(
+        '#include <stdio.h>\n#include "unified_attention.h"\n'
+        "int main(void) {\n"
+        "    int32_t cu[3] = {0, 1, 6}, sk[2] = {17, 40};\n"
+        "    size_t bytes = 0;\n"
+        "    ua_status st = ua_workspace_size(cu, sk, 2, 4, 2, 96, 16, 3, 1, &bytes);\n"
+        '    printf("%s\\n", ua_status_string(st));\n'
+        "    return st == UA_ERR_UNSUPPORTED ? 0 : 1;\n}\n")
+    libdir = os.path.dirname(B._LIB_PATH)
+    exe = tmp_path / "abi"
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(root, "include"),
+                        str(src), "-L", libdir, "-lua_gb300", f"-Wl,-rpath,{libdir}", "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.strip() == "UA_ERR_UNSUPPORTED", r.stdout + r.stderr
