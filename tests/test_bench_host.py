@@ -38,7 +38,7 @@ def test_algorithmic_work_counts_by_hand(bench):
     assert w["decode_bytes"] == w["kv_bytes"] + 2 * 4 * 4 * 8 * 2 + 4 * pages
 
 
-def test_workload_batch_changes_only_the_page_size(bench):
+def test_workload_batch_keeps_lengths_and_queries(bench):
     b16 = bench.workload_batch(2)
     b64 = bench.workload_batch(2, 64)
     assert b64.spec.block_size == 64 and b64.k_cache.shape[1] == 64
