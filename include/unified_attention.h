@@ -152,8 +152,10 @@ ua_status ua_device_status(int32_t *code);
  * achieved?").
  *
  * counts[0..7] receives: decode CTAs, decode pieces, split units (combined),
- * partial slots, prefill tiles, prefill CTAs, decode pages in total,
- * workspace bytes (saturated to INT32_MAX).
+ * partial slots, prefill tiles, prefill CTAs, decode pages in total, and the
+ * bytes of the plan and partials (saturated to INT32_MAX; ua_workspace_size
+ * adds the expanded block table to these for pages of more than 16 tokens).
+ * The partition is the 16-token view's for any supported block_size.
  * If items != NULL, up to items_cap rows of 8 int32 are written:
  *   decode pieces   {0, cta, seq, kv_head, row0, nrows, page_begin, page_end}
  *                   followed by one row {1, slot or -1, unit, 0, 0, 0, 0, 0}
