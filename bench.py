@@ -6,23 +6,30 @@
 A step is one unified_attention call over one synthetic batch (the whole hot
 path: the partition pass, the plan copy, the decode / split-KV kernel with its
 in-kernel merge of split units, and the prefill kernel when the batch has
-prefill rows).  The
-default workload is the Llama-3.1-8B-shaped pure-decode batch (64 sequences,
-one new token each, contexts uniform in [2048, 4096], Hq 32, Hkv 8, head size
-128, bf16, 16-token pages).  Inputs are resident in HBM when timing starts;
-the KV working set (~0.8 GB) is far larger than L2, and L2 is also flushed
-between timed steps, outside the timed interval: a 256 MB write, then a 256 MB
-read, so that the write's dirty lines are not written back inside the next
-timed step.
+prefill rows).  The default workload is the largest of the standard batches,
+the Llama-3.1-70B-shaped long-context mixed step: 32 decode sequences over
+contexts uniform in [8192, 32768] plus two 2048-token chunks over 4096-token
+prior contexts, Hq 64, Hkv 8, head size 128, bf16, 16-token pages -- both
+HBM-bound (the decode rows' 2.7 GB of K/V) and tensor-bound (the chunks' 687
+GFLOP).  Inputs are resident in HBM when timing starts; the KV working set is
+far larger than L2, and L2 is also flushed between timed steps, outside the
+timed interval: a 256 MB write, then a 256 MB read, so that the write's dirty
+lines are not written back inside the next timed step.
 
 The JSON line carries the metric (query tokens/s), the roofline of the
-dominant kernel (CUDA-event time per launch against the measured HBM
-bandwidth), the fp64 oracle timed on the host cores (cpu_baseline), an
-end-to-end number through the public API with host buffers, clocks sampled
-during the timed region, and the number of kernels launched.
+dominant kernel (CUDA-event time per launch against the measured peak), the
+call's own fractions (all algorithmic bytes over the call's time against HBM,
+all flops against the bf16 peak, and max(B / BW, F / P) / t for a batch bound
+by both), the same figures for the other standard batches (per_config), the
+fp64 oracle timed on the host cores (cpu_baseline), an end-to-end number
+through the public API with host buffers, clocks sampled during the timed
+regions, and the number of kernels launched.  Decode and prefill work is split
+the way the planner routes the batch (its host plan, read back through
+ua_plan_inspect), so each kernel is measured against its own work.
 
 --impl reference times the fp64 CPU oracle (the reference arm) on the same
-workload, a bounded sample of sequences per step.
+workload: per step a proportional sample (every m-th decode sequence and an
+m-th of each long query run, rotating), so the mix of the workload is kept.
 
 Other workloads: the standard batches by name (tiny_mixed_d64,
 mistral_24b_prefill_16x1000, llama3_8b_mixed_256dec_4x512chunk,
@@ -72,7 +79,12 @@ WORKLOADS = {
     "llama3_70b_long_mixed_32x8k-32k_2x2048chunk": 5,
     "gemma2_9b_decode_64x2k-4k": 6,
 }
-DEFAULT_WORKLOAD = "llama3_8b_decode_64x2k-4k"
+DEFAULT_WORKLOAD = "llama3_70b_long_mixed_32x8k-32k_2x2048chunk"
+# the other standard batches the default run also measures (one line, per_config)
+PER_CONFIG = ("llama3_8b_decode_64x2k-4k", "mistral_24b_prefill_16x1000",
+              "llama3_8b_mixed_256dec_4x512chunk")
+# the headline decode batch (fp8 / graph workloads run on it)
+DECODE_WORKLOAD = "llama3_8b_decode_64x2k-4k"
 # Cascade (shared-prefix) step: 64 decode sequences (Llama-3.1-8B heads) that
 # share a 4096-token prefix, own contexts U[256, 1024] tokens; prefix pass over
 # the whole group as one non-causal sequence + own-keys pass + LSE merge.
@@ -97,6 +109,8 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="measure only the chosen workload (no per_config block)")
     ap.add_argument("--block-size", type=int, default=16,
                     help="KV page size in tokens (a multiple of 16, at most 256) for the "
                          "standard attention batches; the lengths and data recipe are unchanged")
@@ -114,28 +128,100 @@ def workload_batch(idx, block_size=16):
     return W.materialize(spec, poison=False)
 
 
-def algorithmic_work(spec) -> dict:
+def algorithmic_work(spec, prefill_seqs=None) -> dict:
     """Minimum bytes and flops of one call (roofline numerators).
 
     bytes: each visible context token's K and V rows read once per KV head
     (GQA packing shares them across the group), Q read and O written once,
     the used block-table entries and the metadata.  flops: 4 * Hq * D per
     visible (query, key) pair; causally hidden pairs are not counted.
+
+    The decode_* / prefill_* parts split the same figures by the kernel that
+    runs each sequence: prefill_seqs is the set of sequences the planner sends
+    to the tensor-core prefill kernel (from its plan, see routed_prefill_seqs);
+    None applies the planner's basic rule (a sequence whose packed rows,
+    Lq * Hq / Hkv, exceed one 16-row decode tile).
     """
     ql = spec.q_lens.astype(np.int64)
     kl = spec.k_lens.astype(np.int64)
     hq, hk, d = spec.num_q_heads, spec.num_kv_heads, spec.head_size
-    pairs = int((ql * (kl - ql) + ql * (ql + 1) // 2).sum()) if spec.causal else int((ql * kl).sum())
+    seq_pairs = (ql * (kl - ql) + ql * (ql + 1) // 2) if spec.causal else ql * kl
+    pairs = int(seq_pairs.sum())
+    pages = spec.pages_per_seq()
     kv_bytes = int(kl.sum()) * 2 * hk * d * 2
     qo_bytes = 2 * spec.total_q * hq * d * 2
-    meta = 4 * (2 * spec.num_seqs + 1) + 4 * int(spec.pages_per_seq().sum())
-    decode = ql * hq // hk <= 16
-    dec_kv = int(kl[decode].sum()) * 2 * hk * d * 2
-    dec_qo = 2 * int(ql[decode].sum()) * hq * d * 2
-    dec_meta = 4 * int(spec.pages_per_seq()[decode].sum())
+    meta = 4 * (2 * spec.num_seqs + 1) + 4 * int(pages.sum())
+    if prefill_seqs is None:
+        prefill = ql * hq // hk > 16
+    else:
+        prefill = np.zeros(spec.num_seqs, dtype=bool)
+        prefill[list(prefill_seqs)] = True
+    decode = (~prefill) & (ql > 0)
+
+    def part(mask):
+        return (int(kl[mask].sum()) * 2 * hk * d * 2 + 2 * int(ql[mask].sum()) * hq * d * 2
+                + 4 * int(pages[mask].sum()))
+
     return {"bytes": kv_bytes + qo_bytes + meta, "kv_bytes": kv_bytes, "flops": 4 * hq * d * pairs,
-            "decode_bytes": dec_kv + dec_qo + dec_meta, "q_tokens": spec.total_q,
-            "kv_tokens": int(kl.sum()), "pairs": pairs}
+            "decode_bytes": part(decode), "decode_flops": 4 * hq * d * int(seq_pairs[decode].sum()),
+            "prefill_bytes": part(prefill), "prefill_flops": 4 * hq * d * int(seq_pairs[prefill].sum()),
+            "q_tokens": spec.total_q, "kv_tokens": int(kl.sum()), "pairs": pairs}
+
+
+def routed_prefill_seqs(ua, batch, num_sms):
+    """Sequences whose rows the planner sends to the prefill kernel (host plan,
+    ua_plan_inspect: record kind 2 is a prefill work item, field 2 its sequence)."""
+    s = batch.spec
+    _, items = ua.plan_inspect(batch.cu_seqlens_q, batch.seqused_k, s.num_q_heads,
+                               s.num_kv_heads, s.head_size, batch.block_table_stride, s.causal,
+                               num_sms=num_sms, block_size=s.block_size)
+    return sorted({int(r[2]) for r in items if r[0] == 2})
+
+
+def proportional_sample(b, k, m, g=None):
+    """Sub-batch k of m: every m-th decode sequence (offset k % m) and, of each
+    longer query run, a slice of about Lq / m consecutive rows (the k % m-th),
+    so that the sample keeps the workload's mix and m consecutive samples cover
+    it.  A slice of rows [a, a + r) of a sequence with Lq new tokens over Lk
+    keys is the sequence of r new tokens over Lk - Lq + a + r keys (causal;
+    the bottom-right mask gives each row the same keys), with the same pages.
+    Returns (q, cu_seqlens_q, seqused_k, block_table, query tokens)."""
+    s = b.spec
+    g = g if g is not None else s.num_q_heads // s.num_kv_heads
+    k %= m
+    rows, ql, kl, bts = [], [], [], []
+    dec = [j for j in range(s.num_seqs) if 0 < s.q_lens[j] * g <= 16]
+    for j in dec[k::m]:
+        q0 = int(b.cu_seqlens_q[j])
+        rows.append(np.arange(q0, q0 + int(s.q_lens[j])))
+        ql.append(int(s.q_lens[j]))
+        kl.append(int(s.k_lens[j]))
+        bts.append(b.block_table[j])
+    for j in range(s.num_seqs):
+        lq, lk = int(s.q_lens[j]), int(s.k_lens[j])
+        if lq * g <= 16:
+            continue
+        r = -(-lq // m)
+        a = min(k * r, lq)
+        r = min(r, lq - a)
+        if r <= 0:
+            continue
+        q0 = int(b.cu_seqlens_q[j])
+        rows.append(np.arange(q0 + a, q0 + a + r))
+        ql.append(r)
+        kl.append(lk - lq + a + r if s.causal else lk)
+        bts.append(b.block_table[j])
+    idx = np.concatenate(rows) if rows else np.zeros(0, np.int64)
+    cu = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+    return (b.q[idx], cu, np.asarray(kl, np.int32), np.stack(bts) if bts else b.block_table[:0],
+            int(sum(ql)))
+
+
+def sample_count(spec, flops_per_sample=10e9):
+    """m of proportional_sample: about flops_per_sample of the oracle's work per
+    sample (a few tenths of a second on 16 host cores), the whole batch when it
+    is smaller than that."""
+    return max(1, int(round(algorithmic_work(spec)["flops"] / flops_per_sample)))
 
 
 def measured_peaks():
@@ -284,41 +370,40 @@ def device_batch(batch, torch, device):
                 block_table=i32(batch.block_table))
 
 
-def cpu_baseline(spec_idx, budget_s=12.0):
-    """The fp64 oracle on the host cores over a bounded sample of the workload."""
+def cpu_baseline(spec_idx, budget_s=12.0, block_size=16):
+    """The fp64 oracle on the host cores over a bounded sample of the workload:
+    proportional samples (see proportional_sample) in turn until the budget is
+    spent; tokens/s = the sampled query tokens over the time taken."""
     import oracle
 
-    b = W.config_batch(spec_idx, poison=False)
+    b = workload_batch(spec_idx, block_size)
     s = b.spec
-    n = s.num_seqs
-    # sample: whole sequences in batch order until the token budget of ~the first call
-    t0 = time.perf_counter()
-    oracle.attention_batch(b)
-    one = time.perf_counter() - t0
-    reps = max(1, min(10, int(budget_s / max(one, 1e-3))))
-    t0 = time.perf_counter()
-    for _ in range(reps):
-        oracle.attention_batch(b)
-    dt = (time.perf_counter() - t0) / reps
-    return {"value": s.total_q / dt, "unit": "tokens/s", "cores": oracle.max_threads(),
+    m = sample_count(s)
+    tokens, t_total, n = 0, 0.0, 0
+    q, cu, sk, bt, _ = proportional_sample(b, 0, m)
+    oracle.attention(q, b.k_cache, b.v_cache, cu, sk, bt, s.softmax_scale, s.causal)   # untimed
+    while n < max(m, 1) * 4 and (t_total < budget_s or n == 0):
+        q, cu, sk, bt, nt = proportional_sample(b, n, m)
+        t0 = time.perf_counter()
+        oracle.attention(q, b.k_cache, b.v_cache, cu, sk, bt, s.softmax_scale, s.causal)
+        t_total += time.perf_counter() - t0
+        tokens += nt
+        n += 1
+    what = "the whole workload" if m == 1 else \
+        f"{n} proportional samples of 1/{m} of the workload (every {m}-th decode sequence and " \
+        f"1/{m} of each longer query run's rows, rotating)"
+    return {"value": tokens / t_total, "unit": "tokens/s", "cores": oracle.max_threads(),
             "kind": "oracle",
-            "sample": f"the whole workload ({n} sequences, {s.total_q} query tokens), "
-                      f"{reps} repetitions after one untimed call, fp64 C oracle with OpenMP",
-            "seconds_per_call": dt}
+            "sample": f"{what}: {tokens} query tokens in {t_total:.1f} s after one untimed "
+                      "sample, fp64 C oracle with OpenMP",
+            "seconds": t_total}
 
 
-def run_ours(args, rank, world, local, dist):
-    import torch
-
-    import paged_varlen_attention_gb300 as ua
-    from paged_varlen_attention_gb300 import build_lib
-
-    build_lib.build()
-    ua.load_library()
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    idx = WORKLOADS[args.workload]
-    batch = workload_batch(idx, args.block_size)
+def time_attention(ua, torch, device, batch, steps, warmup, dist, flush):
+    """Warm up, then time `steps` unified_attention calls on `batch` twice: once
+    plain (the reported step times) and once with the library's CUDA events
+    around each kernel (the per-kernel times).  Returns the times, the kernel
+    times per step and the kernels launched in the plain pass."""
     spec = batch.spec
     dev = device_batch(batch, torch, device)
     out = torch.empty_like(dev["q"])
@@ -327,7 +412,6 @@ def run_ours(args, rank, world, local, dist):
                                  spec.head_size, batch.block_table_stride, spec.causal,
                                  spec.block_size)
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
-    flush = L2Flush(torch, device)
     stream = torch.cuda.current_stream(device)
 
     def step():
@@ -336,12 +420,10 @@ def run_ours(args, rank, world, local, dist):
                              out=out, cu_seqlens_q_host=cu_h, seqused_k_host=sk_h, workspace=ws,
                              stream=stream)
 
-    for _ in range(max(args.warmup, 3)):
+    for _ in range(max(warmup, 3)):
         step()
     torch.cuda.synchronize()
     ua.device_status()
-    kern = {"decode": [], "prefill": [], "combine": [], "plan_copy": []}
-    steps = args.steps
     if steps > 64:
         raise SystemExit("--steps above 64 is not supported (per-kernel event ring)")
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
@@ -350,7 +432,7 @@ def run_ours(args, rank, world, local, dist):
     def timed_pass():
         # steps back to back (no host sync in between, so the host-side planning of
         # one step overlaps the GPU work of the previous one); L2 is flushed (a
-        # 256 MB write before every step, outside the timed interval
+        # 256 MB write, then a 256 MB read) before every step, outside the timed interval
         barrier(dist)
         torch.cuda.synchronize()
         for k in range(steps):
@@ -361,12 +443,12 @@ def run_ours(args, rank, world, local, dist):
         torch.cuda.synchronize()
         return [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
 
-    with ClockSampler(gpu_id_for_smi(torch, local)) as clocks:
-        # pass 1 (the reported value): no per-kernel events inside the calls
-        times = timed_pass()
-        # pass 2 (roofline): the library records CUDA events around each kernel
-        ua.profile_enable(True)
-        timed_pass()
+    # pass 1 (the reported value): no per-kernel events inside the calls
+    times = timed_pass()
+    # pass 2 (roofline): the library records CUDA events around each kernel
+    ua.profile_enable(True)
+    timed_pass()
+    kern = {"decode": [], "prefill": [], "combine": [], "plan_copy": []}
     launches = 0
     for back in range(steps):
         ms, ln = ua.profile_read(back)
@@ -381,15 +463,65 @@ def run_ours(args, rank, world, local, dist):
     status = ua.device_status()
     if status:
         raise RuntimeError(f"device status {status:#x} after the timed steps")
-    total_ms = sum(times)
-    total_ms = max_over_ranks(dist, total_ms, device)
-    work = algorithmic_work(spec)
+    return {"times": times, "kern": kern, "launches": launches, "dev": dev, "out": out, "ws": ws,
+            "cu_h": cu_h, "sk_h": sk_h, "stream": stream}
+
+
+def fractions(spec, work, kern, ms_per_step, peaks):
+    """Call-level and per-kernel roofline fractions of one batch.
+
+    call: all algorithmic bytes over the call's time against the HBM peak, all
+    flops against the bf16 peak, and max(B / BW, F / P) / t (for a batch bound
+    by both).  Kernels: the decode kernel's bytes (the sequences the planner
+    routes to it) over its CUDA-event time, the prefill kernel's flops (its own
+    sequences only) over its time."""
+    t = ms_per_step / 1e3
+    bw, pk = peaks["hbm_gbs"] * 1e9, peaks["bf16_tflops"] * 1e12
+    out = {"ms_per_step": ms_per_step, "tokens_per_s": spec.total_q / t,
+           "call": {"algorithmic_bytes": work["bytes"], "algorithmic_flops": work["flops"],
+                    "hbm_frac": work["bytes"] / t / bw, "tensor_frac": work["flops"] / t / pk,
+                    "combined_frac": max(work["bytes"] / bw, work["flops"] / pk) / t},
+           "kernel_ms": {k: (statistics.mean(v) if v else None) for k, v in kern.items()}}
+    if kern["decode"]:
+        dm = statistics.mean(kern["decode"])
+        gbs = work["decode_bytes"] / (dm / 1e3) / 1e9
+        out["decode_kernel"] = {"ms": dm, "bytes": work["decode_bytes"], "gbs": gbs,
+                                "frac": gbs / peaks["hbm_gbs"]}
+    if kern["prefill"]:
+        pm = statistics.mean(kern["prefill"])
+        tf = work["prefill_flops"] / (pm / 1e3) / 1e12
+        out["prefill_kernel"] = {"ms": pm, "flops": work["prefill_flops"], "tflops": tf,
+                                 "frac": tf / peaks["bf16_tflops"]}
+    return out
+
+
+def run_ours(args, rank, world, local, dist):
+    import torch
+
+    import paged_varlen_attention_gb300 as ua
+    from paged_varlen_attention_gb300 import build_lib
+
+    build_lib.build()
+    ua.load_library()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
     peaks = measured_peaks()
-    res = {"spec": spec, "work": work, "total_ms": total_ms, "times": times, "kern": kern,
-           "launches": launches, "clocks": clocks.summary(), "peaks": peaks}
+    flush = L2Flush(torch, device)
+    batch = workload_batch(WORKLOADS[args.workload], args.block_size)
+    spec = batch.spec
+    with ClockSampler(gpu_id_for_smi(torch, local)) as clocks:
+        r = time_attention(ua, torch, device, batch, args.steps, args.warmup, dist, flush)
+    total_ms = max_over_ranks(dist, sum(r["times"]), device)
+    work = algorithmic_work(spec, routed_prefill_seqs(ua, batch, sms))
+    res = {"spec": spec, "work": work, "total_ms": total_ms, "times": r["times"], "kern": r["kern"],
+           "launches": r["launches"], "clocks": clocks.summary(), "peaks": peaks,
+           "fractions": fractions(spec, work, r["kern"], total_ms / args.steps, peaks)}
 
     # end to end through the public API: pinned host q + metadata in, output back out
     if not args.no_e2e:
+        dev, out, ws, stream = r["dev"], r["out"], r["ws"], r["stream"]
+        cu_h, sk_h = r["cu_h"], r["sk_h"]
         pin = lambda t: t.cpu().pin_memory()  # noqa: E731
         host = {k: pin(dev[k]) for k in ("q", "cu_seqlens_q", "seqused_k", "block_table")}
         out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -409,13 +541,15 @@ def run_ours(args, rank, world, local, dist):
         for _ in range(3):
             e2e_step()
         torch.cuda.synchronize()
-        for k in range(steps):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for a, b in ev:
             flush()
-            ev0[k].record(stream)
+            a.record(stream)
             e2e_step()
-            ev1[k].record(stream)
+            b.record(stream)
         torch.cuda.synchronize()
-        et = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+        et = [a.elapsed_time(b) for a, b in ev]
         e2e_ms = max_over_ranks(dist, sum(et), device)
         res["e2e"] = {"value": world * spec.total_q * args.steps / (e2e_ms / 1e3),
                       "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
@@ -423,7 +557,53 @@ def run_ours(args, rank, world, local, dist):
                       "ms_per_step": e2e_ms / args.steps,
                       "note": "pinned host q + varlen metadata copied in and the output copied "
                               "back every step; the paged KV cache stays resident in HBM"}
+    del r
+
+    # the other standard batches, one GPU only (replicas run the chosen workload)
+    if world == 1 and not args.no_per_config and args.workload == DEFAULT_WORKLOAD:
+        per = {}
+        steps = min(args.steps, 20)
+        for name in PER_CONFIG:
+            b = workload_batch(WORKLOADS[name], args.block_size)
+            with ClockSampler(gpu_id_for_smi(torch, local)) as ck:
+                rr = time_attention(ua, torch, device, b, steps, 3, dist, flush)
+            w = algorithmic_work(b.spec, routed_prefill_seqs(ua, b, sms))
+            f = fractions(b.spec, w, rr["kern"], sum(rr["times"]) / steps, peaks)
+            f.update(steps=steps, gpu_launches=rr["launches"], clocks=ck.summary(),
+                     roofline=dominant_roofline(name, b.spec, w, rr["kern"], peaks))
+            per[name] = f
+            del rr, b
+            torch.cuda.empty_cache()
+        res["per_config"] = per
     return res
+
+
+def dominant_roofline(workload, spec, work, kern, peaks):
+    """Roofline of the kernel with the larger share of the call: the prefill
+    kernel against the bf16 peak (its own flops), or the decode kernel against
+    HBM (its own bytes), per launch over its CUDA-event time."""
+    dec = statistics.mean(kern["decode"]) if kern["decode"] else None
+    pre = statistics.mean(kern["prefill"]) if kern["prefill"] else None
+    if pre is not None and (dec is None or pre > dec):
+        achieved = work["prefill_flops"] / (pre / 1e3) / 1e12
+        roof = {"kernel": "ua_prefill_kernel", "bound": "tensor", "achieved": achieved,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"],
+                "traffic": ncu_traffic("prefill", workload) if spec.block_size == 16 else None,
+                "per_launch": f"{work['prefill_flops']} algorithmic flops (4 Hq D per visible "
+                              "pair of the sequences the planner sends to this kernel)",
+                "launch_ms": pre}
+    else:
+        achieved = work["decode_bytes"] / (dec / 1e3) / 1e9
+        roof = {"kernel": "ua_decode_kernel", "bound": "hbm", "achieved": achieved,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "traffic": ncu_traffic("decode", workload) if spec.block_size == 16 else None,
+                "per_launch": f"{work['decode_bytes']} algorithmic bytes (K+V rows once per kv "
+                              "head, Q, O, block-table entries of the sequences this kernel runs)",
+                "launch_ms": dec}
+    roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json, burst)" \
+        if peaks["source"] == "measured" else "fallback"
+    return roof
 
 
 def gpu_id_for_smi(torch, local):
@@ -449,7 +629,7 @@ def run_reference(args, rank, world):
                          "is not one (its parts are timed by the attention workloads)")
     fp8 = args.workload == FP8_WORKLOAD
     # the graph and fp8 workloads compute attention over the headline batch
-    idx = WORKLOADS.get(args.workload, WORKLOADS[DEFAULT_WORKLOAD])
+    idx = WORKLOADS.get(args.workload, WORKLOADS[DECODE_WORKLOAD])
     b = workload_batch(idx, args.block_size)
     s = b.spec
     if fp8:
@@ -459,31 +639,25 @@ def run_reference(args, rank, world):
         if fp8:
             return oracle.attention_fp8kv(q, k8, v8, 0.05, 0.05, cu, sk, bt, s.softmax_scale, s.causal)
         return oracle.attention(q, b.k_cache, b.v_cache, cu, sk, bt, s.softmax_scale, s.causal)
-    # per step: a rotating window of sequences sized to a few tenths of a second
-    per_step = max(1, min(s.num_seqs, 8 if idx in (1, 2, 6) else 2))
-    if idx == 1:
-        per_step = s.num_seqs
-
-    def sub_batch(start):
-        sel = [(start + j) % s.num_seqs for j in range(per_step)]
-        ql = s.q_lens[sel]
-        cu = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
-        rows = np.concatenate([np.arange(b.cu_seqlens_q[j], b.cu_seqlens_q[j + 1]) for j in sel])
-        return (b.q[rows], cu, b.seqused_k[sel], b.block_table[sel], int(ql.sum()))
+    # per step: one proportional sample (every m-th decode sequence and an m-th of
+    # each longer query run, rotating), a few tenths of a second of oracle work
+    m = sample_count(s)
 
     for w in range(args.warmup):
-        q, cu, sk, bt, _ = sub_batch(w * per_step)
+        q, cu, sk, bt, _ = proportional_sample(b, w, m)
         ref_attention(q, cu, sk, bt)
     tokens = 0
     t0 = time.perf_counter()
     for k in range(args.steps):
-        q, cu, sk, bt, nt = sub_batch(k * per_step)
+        q, cu, sk, bt, nt = proportional_sample(b, args.warmup + k, m)
         ref_attention(q, cu, sk, bt)
         tokens += nt
     dt = time.perf_counter() - t0
     value = tokens / dt
-    sample = (f"{per_step} of {s.num_seqs} sequences per step (a rotating window), "
-              f"{tokens} query tokens over {args.steps} steps, fp64 C oracle with OpenMP")
+    sample = ("the whole workload per step" if m == 1 else
+              f"per step a 1/{m} proportional sample (every {m}-th decode sequence and 1/{m} "
+              "of each longer query run's rows, rotating)") + \
+        f", {tokens} query tokens over {args.steps} steps, fp64 C oracle with OpenMP"
     return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -503,29 +677,7 @@ def assemble(args, res, world, cpu):
     k = args.steps
     total_s = res["total_ms"] / 1e3
     value = world * spec.total_q * k / total_s
-    kern = res["kern"]
-    dec = statistics.mean(kern["decode"]) if kern["decode"] else None
-    pre = statistics.mean(kern["prefill"]) if kern["prefill"] else None
-    # dominant kernel: the one with the larger share of the step
-    if pre is not None and (dec is None or pre > dec):
-        achieved = work["flops"] / (pre / 1e3) / 1e12
-        roof = {"kernel": "ua_prefill_kernel", "bound": "tensor", "achieved": achieved,
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"],
-                "traffic": ncu_traffic("prefill", args.workload) if spec.block_size == 16 else None,
-                "per_launch": f"{work['flops']} algorithmic flops (4 Hq D per visible pair)",
-                "launch_ms": pre}
-    else:
-        achieved = work["decode_bytes"] / (dec / 1e3) / 1e9
-        roof = {"kernel": "ua_decode_kernel", "bound": "hbm", "achieved": achieved,
-                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                "traffic": ncu_traffic("decode", args.workload) if spec.block_size == 16 else None,
-                "per_launch": f"{work['decode_bytes']} algorithmic bytes (K+V rows once per kv "
-                              "head, Q, O, block-table entries)",
-                "launch_ms": dec}
-    roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json)" if peaks["source"] == "measured" \
-        else "fallback"
-    call_gbs = work["bytes"] / (total_s / k) / 1e9
+    f = res["fractions"]
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": k,
         "warmup": args.warmup, "ms_per_step": res["total_ms"] / k, "higher_is_better": True,
@@ -538,10 +690,10 @@ def assemble(args, res, world, cpu):
                    "causal": bool(spec.causal),
                    "l2": "inputs larger than L2, and L2 flushed between steps (256 MB write, then 256 MB read so the write-back is outside the timed interval)",
                    "parallelism": f"{world} independent replica(s), no collective"},
-        "roofline": roof,
-        "call": {"kv_tokens_per_s": world * work["kv_tokens"] * k / total_s,
-                 "algorithmic_gbs": call_gbs, "algorithmic_tflops": work["flops"] / (total_s / k) / 1e12,
-                 "kernel_ms": {kk: (statistics.mean(v) if v else None) for kk, v in kern.items()}},
+        "roofline": dominant_roofline(args.workload, spec, work, res["kern"], peaks),
+        "call": dict(f["call"], kv_tokens_per_s=world * work["kv_tokens"] * k / total_s,
+                     kernel_ms=f["kernel_ms"],
+                     **{kk: f[kk] for kk in ("decode_kernel", "prefill_kernel") if kk in f}),
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
     }
@@ -549,6 +701,8 @@ def assemble(args, res, world, cpu):
         line["cpu_baseline"] = {kk: cpu[kk] for kk in ("value", "unit", "cores", "kind", "sample")}
     if "e2e" in res:
         line["e2e"] = res["e2e"]
+    if "per_config" in res:
+        line["per_config"] = res["per_config"]
     return line
 
 
@@ -752,7 +906,7 @@ def run_fp8kv(args):
 
     ua.load_library()
     dev = torch.device("cuda:0")
-    b = W.config_batch(WORKLOADS[DEFAULT_WORKLOAD], poison=False)
+    b = W.config_batch(WORKLOADS[DECODE_WORKLOAD], poison=False)
     s_ = b.spec
     ks, vs = 0.05, 0.05
     k8, v8 = W.fp8_caches(b, ks, vs)
@@ -831,7 +985,7 @@ def run_graph(args):
 
     ua.load_library()
     dev = torch.device("cuda:0")
-    b = W.config_batch(WORKLOADS[DEFAULT_WORKLOAD], poison=False)
+    b = W.config_batch(WORKLOADS[DECODE_WORKLOAD], poison=False)
     s_ = b.spec
     d = device_batch(b, torch, dev)
     out = torch.empty_like(d["q"])
@@ -902,7 +1056,7 @@ def run_graph(args):
                    "parallelism": "1 GPU, no collective"},
         "roofline": {"kernel": "ua_decode_kernel", "bound": "hbm", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": ncu_traffic("decode", DEFAULT_WORKLOAD),
+                     "traffic": ncu_traffic("decode", DECODE_WORKLOAD),
                      "per_launch": f"{work['decode_bytes']} algorithmic bytes",
                      "launch_ms": dec_ms, "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"},
         "call": {"kernel_ms": {"planner": plan_ms, "decode": dec_ms}},
@@ -933,7 +1087,7 @@ def main():
     res = run_ours(args, rank, world, local, dist)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(WORKLOADS[args.workload])
+        cpu = cpu_baseline(WORKLOADS[args.workload], block_size=args.block_size)
     if rank == 0:
         line = assemble(args, res, world, cpu)
         print(json.dumps(line), flush=True)

@@ -54,11 +54,26 @@
  * below 2^29.  The result is the same, bit for bit, as the call on the
  * 16-token view with the expanded table.
  *
- * Ownership: the caller owns every buffer.  The library never allocates
- * device memory on a call; split-KV partials and the launch plan live in the
- * caller's workspace (size from ua_workspace_size).  Calls are asynchronous on
- * the given stream.  Two calls that share a workspace must be ordered (same
- * stream, or synchronised by the caller).
+ * Ownership: the caller owns every buffer it passes.  Split-KV partials live
+ * in the caller's workspace (size from ua_workspace_size), which only the
+ * call's own kernels touch, in the order of the given stream.  The launch
+ * plan of a host-planned call goes to the GPU through the library's own
+ * memory: per device, a ring of 8 page-locked host buffers and 8 device
+ * buffers, each grown on demand (an allocation only when a plan is larger
+ * than any that buffer held before; none once the sizes have settled).  The
+ * plan copy runs on a library stream and is ordered only after the kernels
+ * of the earlier call that used the same ring buffer, so it overlaps what
+ * the caller's stream runs before the call; the caller's stream waits for it
+ * before the call's kernels.  Calls are asynchronous on the given stream.
+ * Two calls that share a workspace must be ordered (same stream, or
+ * synchronised by the caller).
+ *
+ * CUDA graphs: a host-planned call (unified_attention, _lse, _append, _fp8kv)
+ * fixes its plan, its grid sizes and its plan copy from this batch's host
+ * lengths, so a captured replay would run them against whatever batch the
+ * buffers hold by then.  Such a call made on a stream that is being captured
+ * returns UA_ERR_UNSUPPORTED and enqueues nothing.  Graph users call
+ * unified_attention_device_plan, which plans on the device.
  *
  * Errors are returned, never aborted on.  Invalid metadata is rejected on
  * the host before any launch.  Device-side problems (a block id outside
@@ -225,11 +240,13 @@ ua_status unified_attention_lse(const void *q, const void *k_cache, const void *
  *     out = (w_a out_a + w_b out_b) / (w_a + w_b),  lse_out = m + ln(w_a + w_b).
  * A side with lse = -inf (no key) gets weight 0; both -inf gives out = 0 and
  * lse_out = -inf.  out_a, out_b, out: device bf16 [rows][head_size], 16-byte
- * aligned (out may alias out_a or out_b); lse_a, lse_b: device fp32 [rows];
- * lse_out: device fp32 [rows] or NULL.  rows = total_q * Hq for the outputs
- * of two unified_attention_lse calls.  head_size: a multiple of 8.  Async on
- * stream; returns UA_ERR_INVALID_ARG for bad arguments (nothing launched),
- * UA_ERR_CUDA if the launch fails.
+ * aligned; lse_a, lse_b: device fp32 [rows]; lse_out: device fp32 [rows] or
+ * NULL.  In-place merges are allowed: out may be out_a or out_b, and lse_out
+ * may be lse_a or lse_b (the same pointer; a partial overlap is not
+ * supported).  rows = total_q * Hq for the outputs of two
+ * unified_attention_lse calls.  head_size: a multiple of 8, at most 2048
+ * (else UA_ERR_UNSUPPORTED).  Async on stream; returns UA_ERR_INVALID_ARG for
+ * bad arguments (nothing launched), UA_ERR_CUDA if the launch fails.
  */
 ua_status ua_merge_attn_states(const void *out_a, const float *lse_a, const void *out_b,
                                const float *lse_b, void *out, float *lse_out, int64_t rows,

@@ -15,6 +15,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <thread>
 #include <vector>
 
 #include "unified_attention.h"
@@ -51,31 +52,35 @@ static std::mutex g_mutex;
 static DeviceState g_devices[kMaxDevices];
 static bool g_profile = false;
 
-// Page-locked staging for the plan, per device: a ring of buffers that grow
-// on demand, each reused only after the copy that last read it has finished
-// (an event recorded behind that copy).  From page-locked memory the copy is
-// one DMA that does not hold up the host thread; from pageable memory the
-// driver stages it through its own buffers first.
-//
-// The copy runs on a library-owned stream.  It waits for the kernels of the
-// previous call (whatever its stream or workspace: a call's workspace layout
-// depends on its batch, so the previous call may still be reading the bytes
-// this plan goes to), and the caller's stream waits for the copy before this
-// call's kernels.  So the copy overlaps whatever the caller's stream runs
-// between two calls (other layers' kernels), though not the previous call's
-// own kernels.  One workspace must not serve calls that may run at the same
-// time (their plans and partials would collide anyway).
+// The plan of a host-planned call goes to the GPU through two rings per
+// device, both owned by the library and grown on demand (an allocation only
+// when a plan is larger than any that slot held before):
+//   * page-locked host buffers the plan is serialised into (from page-locked
+//     memory the copy is one DMA that does not hold up the host thread); a
+//     buffer is rewritten only after the copy that last read it has finished;
+//   * device buffers the kernels read the plan from; a buffer is overwritten
+//     only after the kernels of the call that last used it have finished (an
+//     event recorded on that call's stream behind its kernels).
+// The copy runs on a library-owned stream and touches library memory only,
+// so it needs no ordering with the caller's stream beyond that event: it
+// overlaps whatever the caller's stream runs before the call (other layers'
+// kernels, the previous call's own kernels), and the caller's stream waits
+// for the copy before this call's kernels.  The caller's workspace holds the
+// split-KV partials, which only this call's kernels touch, in stream order.
 struct PlanStaging {
     static constexpr int kSlots = 8;
-    uint8_t *buf[kSlots] = {};
+    uint8_t *buf[kSlots] = {};             // page-locked host
     size_t cap[kSlots] = {};
-    cudaEvent_t done[kSlots] = {};
+    cudaEvent_t done[kSlots] = {};         // behind the copy that read buf[i]
     bool busy[kSlots] = {};
+    uint8_t *dbuf[kSlots] = {};            // device
+    size_t dcap[kSlots] = {};
+    cudaEvent_t used[kSlots] = {};         // behind the kernels of the call that read dbuf[i]
+    bool used_pending[kSlots] = {};        // used[i] has been recorded and may not have completed
+    bool held[kSlots] = {};                // a call between its copy and its kernels owns slot i
     int next = 0;
     cudaStream_t side = nullptr;           // copy stream
     cudaEvent_t copied = nullptr;          // behind the latest copy
-    cudaEvent_t call_done = nullptr;       // behind the kernels of the latest call
-    bool called = false;
 };
 static std::mutex g_stage_mutex;
 static PlanStaging g_staging[kMaxDevices];
@@ -85,33 +90,49 @@ static ua_status cuda_failed() {
     return UA_ERR_CUDA;
 }
 
-// Copies the plan to the start of ws (see above); the caller's stream is made
-// to wait for it.
-static ua_status stage_plan(int dev, const Plan &plan, uint8_t *ws, cudaStream_t stream) {
+// Copies the plan into a device buffer of the ring (see above) and makes the
+// caller's stream wait for it; *dplan is where the kernels read it, *slot the
+// ring slot, which release_plan_slot must give back once the call's kernels
+// are enqueued (or the call gave up).
+static ua_status stage_plan(int dev, const Plan &plan, cudaStream_t stream, uint8_t **dplan,
+                            int *slot) {
     const size_t bytes = plan.layout.blob_bytes;
-    std::lock_guard<std::mutex> lock(g_stage_mutex);
+    std::unique_lock<std::mutex> lock(g_stage_mutex);
     PlanStaging &st = g_staging[dev];
     if (!st.side) {
         cudaStream_t sd = nullptr;
         if (cudaStreamCreateWithFlags(&sd, cudaStreamNonBlocking) != cudaSuccess) return cuda_failed();
-        if (cudaEventCreateWithFlags(&st.copied, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&st.call_done, cudaEventDisableTiming) != cudaSuccess) {
+        if (cudaEventCreateWithFlags(&st.copied, cudaEventDisableTiming) != cudaSuccess) {
             cudaStreamDestroy(sd);
             return cuda_failed();
         }
         st.side = sd;
     }
-    if (st.called && cudaStreamWaitEvent(st.side, st.call_done, 0) != cudaSuccess)
-        return cuda_failed();
-    // a staging buffer that no copy in flight still reads
-    const int i = st.next;
-    st.next = (st.next + 1) % PlanStaging::kSlots;
+    // a slot that no other call holds (more than kSlots calls between their
+    // copy and their launches at once, from several host threads: wait)
+    int i = -1;
+    while (i < 0) {
+        for (int k = 0; k < PlanStaging::kSlots && i < 0; ++k) {
+            const int c = (st.next + k) % PlanStaging::kSlots;
+            if (!st.held[c]) i = c;
+        }
+        if (i < 0) {
+            lock.unlock();
+            std::this_thread::yield();
+            lock.lock();
+        }
+    }
+    st.next = (i + 1) % PlanStaging::kSlots;
     if (st.busy[i]) {
         if (cudaEventSynchronize(st.done[i]) != cudaSuccess) return cuda_failed();
         st.busy[i] = false;
     }
     if (!st.done[i] && cudaEventCreateWithFlags(&st.done[i], cudaEventDisableTiming) != cudaSuccess) {
         st.done[i] = nullptr;
+        return cuda_failed();
+    }
+    if (!st.used[i] && cudaEventCreateWithFlags(&st.used[i], cudaEventDisableTiming) != cudaSuccess) {
+        st.used[i] = nullptr;
         return cuda_failed();
     }
     if (st.cap[i] < bytes) {
@@ -124,21 +145,49 @@ static ua_status stage_plan(int dev, const Plan &plan, uint8_t *ws, cudaStream_t
         st.buf[i] = static_cast<uint8_t *>(h);
         st.cap[i] = want;
     }
+    if (st.dcap[i] < bytes) {
+        // the kernels that last read the old buffer finish before it is freed
+        if (st.used_pending[i]) {
+            if (cudaEventSynchronize(st.used[i]) != cudaSuccess) return cuda_failed();
+            st.used_pending[i] = false;
+        }
+        if (st.dbuf[i]) cudaFree(st.dbuf[i]);
+        st.dbuf[i] = nullptr;
+        st.dcap[i] = 0;
+        const size_t want = (bytes + bytes / 2 + 4096 + kAlign - 1) / kAlign * kAlign;
+        void *d = nullptr;
+        if (cudaMalloc(&d, want) != cudaSuccess) return cuda_failed();
+        st.dbuf[i] = static_cast<uint8_t *>(d);
+        st.dcap[i] = want;
+    }
     serialize_plan_to(plan, st.buf[i]);
-    if (cudaMemcpyAsync(ws, st.buf[i], bytes, cudaMemcpyHostToDevice, st.side) != cudaSuccess ||
-        cudaEventRecord(st.done[i], st.side) != cudaSuccess || cudaEventRecord(st.copied, st.side) != cudaSuccess ||
+    if ((st.used_pending[i] && cudaStreamWaitEvent(st.side, st.used[i], 0) != cudaSuccess) ||
+        cudaMemcpyAsync(st.dbuf[i], st.buf[i], bytes, cudaMemcpyHostToDevice, st.side) != cudaSuccess ||
+        cudaEventRecord(st.done[i], st.side) != cudaSuccess ||
+        cudaEventRecord(st.copied, st.side) != cudaSuccess ||
         cudaStreamWaitEvent(stream, st.copied, 0) != cudaSuccess)
         return cuda_failed();
     st.busy[i] = true;
+    st.held[i] = true;
+    *dplan = st.dbuf[i];
+    *slot = i;
     return UA_OK;
 }
 
-// After this call's kernels are enqueued: the next call's plan copy waits for them.
-static ua_status mark_call_done(int dev, cudaStream_t stream) {
+// After this call's kernels are enqueued on stream (or the call gave up after
+// its copy): the slot's device buffer may be rewritten once they finish.
+static ua_status release_plan_slot(int dev, int slot, cudaStream_t stream) {
     std::lock_guard<std::mutex> lock(g_stage_mutex);
     PlanStaging &st = g_staging[dev];
-    if (cudaEventRecord(st.call_done, stream) != cudaSuccess) return cuda_failed();
-    st.called = true;
+    st.held[slot] = false;
+    if (cudaEventRecord(st.used[slot], stream) != cudaSuccess) {
+        // nothing tells when the buffer is free again: wait for the whole device
+        cudaGetLastError();
+        cudaDeviceSynchronize();
+        st.used_pending[slot] = false;
+        return UA_ERR_CUDA;
+    }
+    st.used_pending[slot] = true;
     return UA_OK;
 }
 
@@ -244,6 +293,19 @@ static bool encode_page_map(CUtensorMap *map, const void *base, int d, int hkv,
 
 static bool aligned(const void *p, size_t a) {
     return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+// A host-planned call is not captured into a CUDA graph: its plan, grid
+// sizes and plan copy are fixed by this batch's host lengths, and a replay
+// would run them against whatever batch the buffers hold by then.  Called
+// after the host-side checks and before anything is enqueued.
+static ua_status refuse_capture(cudaStream_t stream) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return UA_ERR_UNSUPPORTED;
+    }
+    return cs == cudaStreamCaptureStatusNone ? UA_OK : UA_ERR_UNSUPPORTED;
 }
 
 // Workspace bytes of the block table expanded to 16-token pages (pages of
@@ -477,6 +539,8 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
         const size_t xb = expanded_table_bytes(num_seqs, block_table_stride, block_size);
         if (!workspace || workspace_bytes < xb || !aligned(workspace, kAlign)) return UA_ERR_WORKSPACE;
         int32_t *xbt = static_cast<int32_t *>(workspace);
+        const ua_status cap = refuse_capture(static_cast<cudaStream_t>(stream_ptr));
+        if (cap != UA_OK) return cap;
         if (launch_expand_block_table(block_table, xbt, (int64_t)num_seqs * block_table_stride, r,
                                       num_blocks, static_cast<cudaStream_t>(stream_ptr)) != cudaSuccess) {
             cudaGetLastError();
@@ -513,10 +577,12 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
         return UA_ERR_INVALID_ARG;
     if (total_q >= ((int64_t)1 << 31)) return UA_ERR_INVALID_ARG;
 
-    DeviceState *ds = nullptr;
-    ua_status st = device_state(&ds);
-    if (st != UA_OK) return st;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    ua_status st = refuse_capture(stream);
+    if (st != UA_OK) return st;
+    DeviceState *ds = nullptr;
+    st = device_state(&ds);
+    if (st != UA_OK) return st;
 
     // ---- partition pass
     thread_local Plan plan;
@@ -567,29 +633,32 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
     const float scale_log2 = softmax_scale * k_scale * 1.4426950408889634f;
 
     mark(0);
-    // Once the plan copy is issued, every way out of this call records the
-    // call-done event behind whatever kernels it launched, so that the next
-    // call's copy cannot overwrite a plan that is still being read.
-    struct CallDone {
-        int dev = -1;
+    // The plan: in a device buffer of the library's ring (pinned_plan), or at
+    // the start of the workspace, copied in stream order from pageable memory
+    // (which allocates nothing).  Once a ring slot is taken, every way out of
+    // this call gives it back behind whatever kernels the call launched.
+    struct SlotGuard {
+        int dev = -1, slot = -1;
         cudaStream_t stream = nullptr;
-        ~CallDone() {
-            if (dev >= 0) mark_call_done(dev, stream);
+        ~SlotGuard() {
+            if (slot >= 0) release_plan_slot(dev, slot, stream);
         }
-    } call_done;
+    } guard;
+    uint8_t *pl = ws;
     if (L.blob_bytes > 0) {
         if (pinned_plan) {
-            st = stage_plan(ds->dev, plan, ws, stream);
+            int slot = -1;
+            st = stage_plan(ds->dev, plan, stream, &pl, &slot);
             if (st != UA_OK) return st;
-            call_done.dev = ds->dev;
-            call_done.stream = stream;
+            guard.dev = ds->dev;
+            guard.slot = slot;
+            guard.stream = stream;
         } else if (cudaMemcpyAsync(ws, blob.data(), L.blob_bytes, cudaMemcpyHostToDevice,
                                    stream) != cudaSuccess) {
             cudaGetLastError();
             return UA_ERR_CUDA;
         }
     }
-    uint8_t *pl = ws;   // this call's plan
     mark(1);
     cudaError_t e = cudaSuccess;
     if (plan.dec_ctas > 0) {
@@ -647,9 +716,10 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
     mark(3);
     // (split units are merged inside the decode kernel: no separate combine step)
     mark(4);
-    if (call_done.dev >= 0) {
-        call_done.dev = -1;
-        st = mark_call_done(ds->dev, stream);
+    if (guard.slot >= 0) {
+        const int slot = guard.slot;
+        guard.slot = -1;
+        st = release_plan_slot(ds->dev, slot, stream);
         if (st != UA_OK) return st;
     }
     if (prof) {
@@ -757,6 +827,8 @@ extern "C" ua_status unified_attention_append(
         return UA_ERR_WORKSPACE;
     if (!std::isfinite(softmax_scale) || !q || !out || !aligned(q, 16) || !aligned(out, 16))
         return UA_ERR_INVALID_ARG;
+    st = refuse_capture(static_cast<cudaStream_t>(stream));
+    if (st != UA_OK) return st;
     st = ua_kv_append(k_new, v_new, cu_seqlens_q, seqused_k, block_table, k_cache, v_cache,
                       cu_seqlens_q_host, seqused_k_host, num_seqs, num_kv_heads, head_size,
                       block_size, num_blocks, block_table_stride, stream);

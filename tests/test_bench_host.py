@@ -57,9 +57,12 @@ def test_traffic_record_is_dropped_once_its_sources_change(bench, tmp_path, monk
         dst = tmp_path / rel
         dst.parent.mkdir(parents=True, exist_ok=True)
         shutil.copy(os.path.join(ROOT, rel), dst)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    # the record as taken on these sources (the repository's own record may be
+    # stale: that is what this test is about)
+    entry = dict(entry, source_sha256_16=bench.source_hash(entry["sources"]))
     (tmp_path / "profiles").mkdir()
     (tmp_path / "profiles" / "ncu_traffic.json").write_text(json.dumps({key: entry}))
-    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.ncu_traffic("decode", "llama3_8b_decode_64x2k-4k") == float(entry["dram_bytes_per_launch"])
     assert bench.ncu_traffic("decode", "no_such_workload") is None
     with open(tmp_path / entry["sources"][0], "a") as fh:
@@ -82,3 +85,39 @@ def test_reference_arm_with_64_token_pages():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["config"]["block_size"] == 64 and d["value"] > 0
+
+
+def test_work_split_by_routing_adds_up(bench):
+    spec = W.custom_spec([1, 40, 1, 3], [900, 400, 50, 30], 8, 2, 64)
+    w = bench.algorithmic_work(spec, prefill_seqs=[1])
+    meta = 4 * (2 * spec.num_seqs + 1)
+    assert w["decode_bytes"] + w["prefill_bytes"] + meta == w["bytes"]
+    assert w["decode_flops"] + w["prefill_flops"] == w["flops"]
+    # sequence 1 alone (40 new tokens over 400 keys, causal)
+    assert w["prefill_flops"] == 4 * 8 * 64 * (40 * 360 + 40 * 41 // 2)
+    # the default rule: 40 * 4 = 160 packed rows > 16 -> prefill; 3 * 4 = 12 -> decode
+    assert bench.algorithmic_work(spec)["prefill_flops"] == w["prefill_flops"]
+
+
+def test_proportional_samples_cover_the_batch_and_keep_each_row(bench):
+    """m consecutive samples hold every query row once, and the oracle gives each
+    sampled row bit for bit the value it has in the whole batch (a slice of a
+    query run is a shorter run over fewer keys, by the bottom-right mask)."""
+    import oracle
+
+    spec = W.custom_spec([1, 1, 37, 1, 20], [300, 17, 100, 90, 20], 8, 2, 64, seed=4)
+    b = W.materialize(spec, poison=True)
+    whole, _ = oracle.attention_batch(b)
+    m = 4
+    seen = []
+    for k in range(m):
+        q, cu, sk, bt, nt = bench.proportional_sample(b, k, m)
+        assert nt == q.shape[0] == cu[-1]
+        got, _ = oracle.attention(q, b.k_cache, b.v_cache, cu, sk, bt, spec.softmax_scale, True)
+        # find each sampled row in the whole batch by its query vector
+        for r in range(q.shape[0]):
+            t = np.nonzero((b.q == q[r]).all(axis=(1, 2)))[0]
+            assert len(t) == 1
+            assert np.array_equal(got[r], whole[t[0]])
+            seen.append(int(t[0]))
+    assert sorted(seen) == list(range(spec.total_q))

@@ -37,44 +37,13 @@ def check_batch(batch, what):
     return assert_close(got, ref, what)
 
 
-@pytest.mark.parametrize("idx", [1, 2, 3, 4])
+@pytest.mark.parametrize("idx", [1, 2, 3, 4, 5])
 def test_standard_batch_matches_oracle(idx):
+    """Every output element of the five standard batches at full size against the
+    oracle, the long mixed step's two 2048-token chunks (the claimed-items prefill
+    kernel) included: ~700 GFLOP of fp64 work on the host cores for that batch."""
     b = W.config_batch(idx, poison=True)
     check_batch(b, W.CONFIG_NAMES[idx])
-
-
-def test_long_mixed_batch_sampled_rows():
-    """Llama-70B-shaped long mixed step at full size.
-
-    The 32 decode rows are checked whole; for the two 2048-token chunks,
-    sampled rows are checked through the decode-equals-prefill-row identity
-    (pinned on the oracle): row i of a chunk equals a one-token query over the
-    first Lk - Lq + i + 1 keys of the same block-table row.
-    """
-    b = W.config_batch(5, poison=True)
-    s = b.spec
-    got = run_gpu(b)
-    ndec = 32
-    dec = W.Batch(W.Spec("dec", s.q_lens[:ndec], s.k_lens[:ndec], s.num_q_heads,
-                         s.num_kv_heads, s.head_size, softmax_scale=s.softmax_scale),
-                  b.q[:ndec], b.k_cache, b.v_cache, b.cu_seqlens_q[:ndec + 1],
-                  b.seqused_k[:ndec], b.block_table[:ndec], b.poison_blocks)
-    ref, _ = oracle.attention_batch(dec)
-    assert_close(got[:ndec], ref, "long mixed: decode rows")
-    rows, lks, bts = [], [], []
-    for seq in (ndec, ndec + 1):
-        q0, lq, lk = int(b.cu_seqlens_q[seq]), int(s.q_lens[seq]), int(s.k_lens[seq])
-        for i in sorted({0, 1, 15, 16, 17, 127, 128, 129, 1000, lq - 2, lq - 1}):
-            rows.append(q0 + i)
-            lks.append(lk - lq + i + 1)
-            bts.append(b.block_table[seq])
-    n = len(rows)
-    samp = W.Batch(W.Spec("rows", np.ones(n), lks, s.num_q_heads, s.num_kv_heads, s.head_size,
-                          softmax_scale=s.softmax_scale),
-                   b.q[rows], b.k_cache, b.v_cache, np.arange(n + 1, dtype=np.int32),
-                   np.asarray(lks, np.int32), np.stack(bts), b.poison_blocks)
-    ref2, _ = oracle.attention_batch(samp)
-    assert_close(got[rows], ref2, "long mixed: sampled chunk rows")
 
 
 SWEEP = [
