@@ -61,7 +61,7 @@ def _compile(cmd, log_path):
 # Register ceilings of the kernels: the prefill kernel runs 384 threads on one
 # SM, so a thread may hold at most 65536 / 384 -> 168 registers; a build where
 # ptxas goes past that is refused.
-LAUNCH_REGS = {"ua_prefill_kernel": 168}
+LAUNCH_REGS = {"ua_prefill_kernel": 168, "ua_prefill_pair_kernel": 255}
 
 
 def _registers_by_kernel(log_text: str) -> dict:
@@ -86,21 +86,26 @@ def _check_launch_registers(log_path: str):
                                    f"the {want} its launch allows; refusing to build")
 
 
-def build(force: bool = False, verbose: bool = False, prefill=None) -> str:
+def build(force: bool = False, verbose: bool = False, prefill=None, pair=None) -> str:
     """Compile every CUDA / C++ source of the library; return the .so path.
 
     prefill=False builds a library whose planner sends every row tile to the
     decode kernel (used to cross-check the two kernels against each other);
-    prefill=None keeps the setting of the existing build (on by default).
+    pair=False runs head-size-128 prefill rows on one SM per work item instead
+    of on SM pairs.  None keeps the setting of the existing build (both on by
+    default).
     """
     stamp = os.path.join(BUILD, "prefill_flag")
     os.makedirs(BUILD, exist_ok=True)
     old_flag = open(stamp).read() if os.path.exists(stamp) else ""
+    old_defs = old_flag.split()
     if prefill is None:
-        prefill = old_flag != "-DUA_PREFILL_ENABLED=0"
-    defines = [f"-DUA_PREFILL_ENABLED={int(bool(prefill))}"]
+        prefill = "-DUA_PREFILL_ENABLED=0" not in old_defs
+    if pair is None:
+        pair = "-DUA_PREFILL_PAIR=0" not in old_defs
+    defines = [f"-DUA_PREFILL_ENABLED={int(bool(prefill))}", f"-DUA_PREFILL_PAIR={int(bool(pair))}"]
     if (not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime()
-            and old_flag == defines[0]):
+            and old_flag == " ".join(defines)):
         return LIB
     nvcc = _nvcc()
     cu, cpp = _sources()
@@ -130,10 +135,11 @@ def build(force: bool = False, verbose: bool = False, prefill=None) -> str:
     _compile(link, os.path.join(BUILD, "link.log"))
     os.replace(tmp, LIB)
     with open(stamp, "w") as fh:
-        fh.write(defines[0])
+        fh.write(" ".join(defines))
     return LIB
 
 
 if __name__ == "__main__":
     pf = False if "--no-prefill" in sys.argv else (True if "--prefill" in sys.argv else None)
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, prefill=pf))
+    pr = False if "--no-pair" in sys.argv else (True if "--pair" in sys.argv else None)
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, prefill=pf, pair=pr))

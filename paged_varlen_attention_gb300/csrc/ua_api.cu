@@ -31,6 +31,9 @@ __device__ int g_ua_device_status = 0;
 // row tile runs in the decode kernel (correct for any shape, slower for long
 // query runs).
 constexpr bool kPrefillEnabled = UA_PREFILL_ENABLED;
+// Head-size-128 prefill rows run on pairs of SMs (ua_prefill_pair.cu) when
+// this is set; otherwise on one SM per work item (ua_prefill.cu).
+constexpr bool kPairPrefill = UA_PREFILL_PAIR;
 
 constexpr int kMaxDevices = 64;
 
@@ -269,21 +272,25 @@ static bool encode_map(CUtensorMap *map, const void *base, uint64_t inner, uint6
 // eb: bytes per element, 2 (bf16) or 1 (e4m3): a 128-byte chunk is 64 or 128
 // elements, and a page row D * eb bytes.  box_heads: KV heads per box (1, or
 // 2 adjacent heads laid out [head][chunk][slot][128 B]).
+// box_chunks: 128-byte chunks per box (all D * eb / 128 of them, or 1: one
+// 64-column slice of the page, chosen by the chunk coordinate).
 static bool encode_page_map(CUtensorMap *map, const void *base, int d, int hkv,
-                            uint64_t num_blocks, int eb = 2, int box_heads = 1) {
+                            uint64_t num_blocks, int eb = 2, int box_heads = 1, int box_chunks = 0) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
     const uint64_t row = (uint64_t)hkv * d * eb;   // bytes between slots
     const cuuint32_t inner = 128 / eb, chunks = (cuuint32_t)(d * eb / 128);
     cuuint64_t dims[5] = {inner, (cuuint64_t)kBlockSize, chunks, (cuuint64_t)hkv, num_blocks};
     cuuint64_t strides[4] = {row, 128, (cuuint64_t)d * eb, row * kBlockSize};
-    cuuint32_t box[5] = {inner, (cuuint32_t)kBlockSize, chunks, (cuuint32_t)box_heads, 1};
+    const cuuint32_t bch = box_chunks > 0 ? (cuuint32_t)box_chunks : chunks;
+    cuuint32_t box[5] = {inner, (cuuint32_t)kBlockSize, bch, (cuuint32_t)box_heads, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     // the box's heads of one slot are the useful run (the whole slot when
     // they are all Hkv heads); with 128-byte runs (one e4m3 head at D = 128)
     // a 256-byte fill read 1.38x the algorithmic DRAM bytes
     const CUtensorMapL2promotion promo =
-        l2_fill(hkv == box_heads ? row * kBlockSize : (uint64_t)d * eb * box_heads);
+        l2_fill(bch != chunks ? (uint64_t)128 * bch
+                              : (hkv == box_heads ? row * kBlockSize : (uint64_t)d * eb * box_heads));
     CUresult r = enc(map, eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 5,
                      const_cast<void *>(base), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -306,6 +313,24 @@ static ua_status refuse_capture(cudaStream_t stream) {
         return UA_ERR_UNSUPPORTED;
     }
     return cs == cudaStreamCaptureStatusNone ? UA_OK : UA_ERR_UNSUPPORTED;
+}
+
+// Whether the head-size-128 prefill rows of this call run on SM pairs.
+static bool use_pair_prefill(int32_t head_size, int kv_fp8) {
+    return kPairPrefill && head_size == 128 && !kv_fp8;
+}
+
+// The prefill scheduling of a call: items dealt to SM pairs (two-SM kernel),
+// or to SMs with the long ones claimed as the CTAs go (one-SM kernel at head
+// size 128 with a positive scale).
+static void configure_prefill(Problem &pr, int sms, bool scale_positive, int kv_fp8) {
+    if (use_pair_prefill(pr.d, kv_fp8)) {
+        pr.prefill_claim = false;
+        pr.pre_workers = std::max(1, sms / 2);
+    } else {
+        pr.prefill_claim = pr.d == 128 && scale_positive;
+        pr.pre_workers = 0;
+    }
 }
 
 // Workspace bytes of the block table expanded to 16-token pages (pages of
@@ -371,6 +396,7 @@ extern "C" ua_status ua_workspace_size(const int32_t *cu_seqlens_q_host,
     DeviceState *ds = nullptr;
     ua_status st = device_state(&ds);
     if (st != UA_OK) return st;
+    configure_prefill(pr, ds->sms, true, 0);
     thread_local Plan plan;
     build_plan(pr, ds->sms, kPrefillEnabled, plan);
     *bytes = plan.layout.total_bytes + expanded_table_bytes(num_seqs, block_table_stride, block_size);
@@ -409,7 +435,7 @@ extern "C" ua_status ua_plan_inspect(const int32_t *cu_seqlens_q_host,
     if (!counts || num_sms <= 0) return UA_ERR_INVALID_ARG;
     Problem pr = make_problem(cu_seqlens_q_host, seqused_k_host, num_seqs, num_q_heads,
                               num_kv_heads, head_size, block_size, block_table_stride, causal);
-    pr.prefill_claim = head_size == 128;   // as a call with a positive softmax scale
+    configure_prefill(pr, num_sms, true, 0);   // as a call with a positive softmax scale
     int v = validate_problem(pr);
     if (v) return static_cast<ua_status>(v);
     thread_local Plan plan;
@@ -558,8 +584,6 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
                               num_kv_heads, head_size, block_size, block_table_stride, causal);
     // e4m3 pages: decode units take two adjacent kv heads (256-byte rows per slot)
     if (kv_fp8) pr.kv_heads_per_unit = 2;
-    // long prefill items may be claimed as the CTAs go (that kernel: D = 128, scale > 0)
-    pr.prefill_claim = head_size == 128 && softmax_scale * k_scale > 0.f;
     int v = validate_problem(pr);
     if (v) return static_cast<ua_status>(v);
     if (!std::isfinite(softmax_scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
@@ -587,6 +611,8 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
     // ---- partition pass
     thread_local Plan plan;
     thread_local std::vector<uint8_t> blob;
+    configure_prefill(pr, ds->sms, softmax_scale * k_scale > 0.f, kv_fp8);
+    const bool pair_prefill = use_pair_prefill(head_size, kv_fp8);
     // an fp8 cache is read by the decode kernel only
     build_plan(pr, ds->sms, kPrefillEnabled && !kv_fp8, plan);
     const Layout &L = plan.layout;
@@ -598,7 +624,7 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
 
     // ---- tensor maps: K/V page views (5-D), Q as [total_q, Hq, D]
     const int g = num_q_heads / num_kv_heads;
-    CUtensorMap tm_kp, tm_vp, tm_q, tm_o, tm_k3;
+    CUtensorMap tm_kp, tm_vp, tm_q, tm_o, tm_k3, tm_vh;
     const int eb = kv_fp8 ? 1 : 2;
     const int box_heads = plan.dec_heads_per_unit;   // 2 only for e4m3 pages (no prefill tiles)
     if (!encode_page_map(&tm_kp, k_cache, head_size, num_kv_heads, (uint64_t)num_blocks, eb,
@@ -613,6 +639,9 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
          !encode_map(&tm_o, out, head_size, num_q_heads, (uint64_t)total_q, g, kPreRows / g) ||
          !encode_map(&tm_k3, k_cache, head_size, num_kv_heads,
                      (uint64_t)num_blocks * block_size, 1, kBlockSize)))
+        return UA_ERR_CUDA;
+    if (!plan.tiles.empty() && pair_prefill &&
+        !encode_page_map(&tm_vh, v_cache, head_size, num_kv_heads, (uint64_t)num_blocks, 2, 1, 1))
         return UA_ERR_CUDA;
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -709,8 +738,9 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
         pp.sched = reinterpret_cast<int32_t *>(pl + L.off_sched);
         pp.n_tiles = (int32_t)plan.tiles.size();
         pp.status = ds->status;
-        e = launch_prefill(head_size, plan.pre_claimed, pp, tm_q, tm_o, tm_k3, tm_vp, plan.pre_ctas,
-                           stream);
+        e = pair_prefill ? launch_prefill_pair(pp, tm_q, tm_o, tm_k3, tm_vh, plan.pre_ctas, stream)
+                         : launch_prefill(head_size, plan.pre_claimed, pp, tm_q, tm_o, tm_k3, tm_vp,
+                                          plan.pre_ctas, stream);
         if (e != cudaSuccess) return UA_ERR_CUDA;
     }
     mark(3);
@@ -883,6 +913,8 @@ static ua_status device_plan_shape(int32_t num_seqs, int32_t max_total_q, int32_
     const bool can_prefill = (int64_t)s->max_seq_q * (hq / hkv) > kDecRows;
     s->prefill_ok = (kPrefillEnabled && !kv_fp8 && can_prefill && prefill_supports(pr)) ? 1 : 0;
     s->num_sms = sms;
+    s->pre_pair = use_pair_prefill(d, kv_fp8) ? 1 : 0;
+    s->pre_workers = s->pre_pair ? std::max(1, sms / 2) : sms;
     return UA_OK;
 }
 
@@ -943,10 +975,13 @@ static ua_status run_attention_device_plan(
     }
     // tensor maps over the caller's buffers (q / out sized for max_total_q tokens)
     const int g = num_q_heads / num_kv_heads;
-    CUtensorMap tm_kp, tm_vp, tm_q, tm_o, tm_k3;
+    CUtensorMap tm_kp, tm_vp, tm_q, tm_o, tm_k3, tm_vh;
     const int eb = kv_fp8 ? 1 : 2;
     if (!encode_page_map(&tm_kp, k_cache, head_size, num_kv_heads, (uint64_t)num_blocks, eb, shape.hpu) ||
         !encode_page_map(&tm_vp, v_cache, head_size, num_kv_heads, (uint64_t)num_blocks, eb, shape.hpu))
+        return UA_ERR_CUDA;
+    if (shape.prefill_ok && shape.pre_pair &&
+        !encode_page_map(&tm_vh, v_cache, head_size, num_kv_heads, (uint64_t)num_blocks, 2, 1, 1))
         return UA_ERR_CUDA;
     if (shape.prefill_ok &&
         (!encode_map(&tm_q, q, head_size, num_q_heads, (uint64_t)max_total_q, g, kPreRows / g) ||
@@ -1022,9 +1057,11 @@ static ua_status run_attention_device_plan(
         pp.tile_begin = reinterpret_cast<const int32_t *>(ws + L.off_pre_begin);
         pp.n_tiles = L.cap_items;
         pp.status = ds->status;
-        if (launch_prefill(head_size, /*claimed=*/false, pp, tm_q, tm_o, tm_k3, tm_vp, shape.num_sms,
-                           stream) != cudaSuccess)
-            return UA_ERR_CUDA;
+        const cudaError_t pe =
+            shape.pre_pair ? launch_prefill_pair(pp, tm_q, tm_o, tm_k3, tm_vh, shape.pre_workers, stream)
+                           : launch_prefill(head_size, /*claimed=*/false, pp, tm_q, tm_o, tm_k3, tm_vp,
+                                            shape.num_sms, stream);
+        if (pe != cudaSuccess) return UA_ERR_CUDA;
     }
     mark(3);
     mark(4);

@@ -193,6 +193,7 @@ struct PlanArgs {
     const int32_t *cu;
     const int32_t *lk;
     int32_t num_seqs, max_total_q, max_seq_q, hq, hkv, g, bt_stride, hpu, prefill_ok, num_sms, causal;
+    int32_t pre_workers;      // prefill items are dealt to this many workers
     int32_t dec_grid, cap_units, cap_items, cap_pieces, cap_comb, cap_slots, n_buckets;
     long long *header;
     int32_t *cta_begin;       // [dec_grid + 1]
@@ -476,7 +477,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) ua_plan_kernel(const PlanArgs
         // ranks, in batch order within a bucket: chunks of nt items; in a chunk,
         // the warps take their turn, each group of equal keys in a warp reading
         // and advancing its bucket's cursor once
-        const int C = min(n_items, a.num_sms);
+        const int C = min(n_items, a.pre_workers);
         pre_ctas = C;
         const int R = n_items / C, rem = n_items % C;
         for (int c = tid; c <= a.num_sms; c += nt) {
@@ -600,6 +601,7 @@ cudaError_t launch_device_plan(const DevPlanShape &s, const DevPlanLayout &L, co
     a.hpu = s.hpu;
     a.prefill_ok = s.prefill_ok;
     a.num_sms = s.num_sms;
+    a.pre_workers = s.pre_workers;
     a.causal = causal != 0;
     a.dec_grid = L.dec_grid;
     a.cap_units = L.cap_units;

@@ -65,6 +65,12 @@ cudaError_t launch_decode(int d, bool kv8, const DecodeParams &p, const CUtensor
 cudaError_t launch_prefill(int d, bool claimed, const PrefillParams &p, const CUtensorMap &tm_q,
                            const CUtensorMap &tm_o, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                            int ctas, cudaStream_t stream);
+// The two-SM prefill kernel (ua_prefill_pair.cu), head size 128: `pairs`
+// clusters of two CTAs, pair c running tiles [tile_begin[c], tile_begin[c+1]).
+// tm_vh: the page view of the V cache with one 64-column chunk per box.
+cudaError_t launch_prefill_pair(const PrefillParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_o,
+                                const CUtensorMap &tm_k, const CUtensorMap &tm_vh, int pairs,
+                                cudaStream_t stream);
 
 // The whole call behind unified_attention (arguments as declared in
 // unified_attention.h).  pinned_plan: stage the plan through the library's
@@ -101,6 +107,8 @@ struct DevPlanShape {
     int32_t hpu;
     int32_t prefill_ok;
     int32_t num_sms;
+    int32_t pre_workers;   // prefill items are dealt to this many workers (<= num_sms)
+    int32_t pre_pair;      // the workers are CTA pairs of the two-SM prefill kernel
 };
 
 // Workspace sections (byte offsets) and capacities for one DevPlanShape.

@@ -105,6 +105,8 @@ struct Problem {
     bool causal;
     int32_t kv_heads_per_unit = 1;   // decode units: 1, or 2 (adjacent heads, <= 8 rows each)
     bool prefill_claim = false;      // long prefill items may be claimed as the CTAs go
+    int32_t pre_workers = 0;         // prefill items are dealt to this many workers (CTAs, or
+                                     // CTA pairs for the two-SM kernel); 0: one per SM
 };
 
 // Offsets of the plan sections inside the device workspace.

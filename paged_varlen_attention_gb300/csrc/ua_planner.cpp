@@ -152,7 +152,8 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
         sorted.resize(unsorted.size());
         for (const PreTile &t : unsorted) sorted[(size_t)counts[(size_t)(max_kv - t.kv_tiles)]++] = t;
 
-        const int32_t ctas = (int32_t)std::min<size_t>(sorted.size(), (size_t)std::max(num_sms, 1));
+        const int32_t workers = p.pre_workers > 0 ? p.pre_workers : std::max(num_sms, 1);
+        const int32_t ctas = (int32_t)std::min<size_t>(sorted.size(), (size_t)workers);
         plan.pre_ctas = ctas;
         plan.pre_claimed =
             p.prefill_claim && kv_sum >= (int64_t)kClaimMinMeanKvTiles * (int64_t)sorted.size();

@@ -1,0 +1,687 @@
+// ua_prefill_pair.cu -- tensor-core prefill on pairs of SMs (tcgen05 cta_group::2),
+// head size 128.
+//
+// The same operation as the one-SM prefill kernel (ua_prefill.cu): query runs
+// longer than one 16-row decode tile, the query heads of one KV head stacked
+// along M so that every K/V tile feeds all of them (the GQA packing of
+// "[Kernel] Unified Triton kernel that doesn't distinguish between prefill +
+// decode", vLLM PR #16828, PR description, where it keeps the tensor cores
+// busy).  Here a work item -- 256 packed rows of one (sequence, KV head) --
+// runs on a cluster of two CTAs on two SMs: CTA r holds rows 128 r .. 128 r +
+// 127 of the item, and one MMA instruction computes all 256 rows (M = 256).
+// What the pair buys:
+//   * 128-key score tiles (N = 128).  Each SM reads its own 128 Q rows and
+//     half of the K tile per instruction from shared memory (96 bytes per
+//     cycle at full rate, against 128 available); with one SM per 128-row
+//     tile and N = 64 (the one-SM kernel) it reads 192, so score MMAs ran
+//     at about two thirds of the rate.
+//   * K and V are loaded once per pair: CTA r loads keys 64 r .. 64 r + 63 of
+//     each 128-key step (the B operand of S = Q K^T is split by N) and the
+//     columns 64 r .. 64 r + 63 of V for all 128 keys (the B operand of
+//     O += P V is split by N = D).
+//   * TMEM per SM: three 128-column score buffers and O (128 columns), so
+//     the scores of step j + 1 and j + 2 can be computed while the softmax of
+//     step j runs, and S(j + 2) reuses the buffer of P V(j - 1), which had a
+//     whole step to complete.
+//
+// Roles (7 warps per CTA):
+//   warps 0-3  softmax of the CTA's 128 rows (one row per thread = TMEM
+//              lane): scale into the log2 domain, bottom-right causal mask,
+//              row max, exp2, row sum, P as bf16 over the first 64 columns of
+//              the step's score buffer; every warp then arrives on the
+//              leader's P barrier (the peer's warps remotely).  O is rescaled
+//              only when a row max grows by more than 2^8.  After an item's
+//              last P V: O / l as bf16 rows of out (TMA store of the 128-row
+//              tile, or by hand for a tile that ends early).
+//   warp 4     leader CTA: allocates TMEM (both CTAs' warp 4 do, collectively)
+//              and issues the pair's MMAs (one elected lane): S(x) = Q K^T
+//              for the flattened sequence of KV steps of the pair's items,
+//              two ahead: S(0), S(1), then for each step y: P V(y), S(y + 2).
+//              Commits arrive on the barrier at the same offset in both CTAs.
+//              Peer CTA: relays "this CTA's half of Q / K / V has landed" to
+//              the leader's barriers (the leader's MMAs read both halves).
+//   warp 5     TMA producer of the CTA's Q tiles (double-buffered, so the next
+//              item's scores can start before this item ends) and K halves
+//              (four {64, 1, 16} boxes per 64 columns of [pages*16, Hkv, D]).
+//   warp 6     TMA producer of the CTA's V halves (one {64, 16, 1, 1, 1} box
+//              per page: its 64 columns of the page); zeroes the rows past
+//              the context of a sequence's last, partial page (they may hold
+//              anything, NaN included, and 0 x NaN is NaN) before it releases
+//              that step.
+// Pages past a step's last visible key are read out of bounds (zero fill).
+// Every wait is bounded (see ua_device.cuh); TMEM is always freed.
+#include "ua_device.cuh"
+#include "ua_kernels.h"
+
+namespace ua {
+namespace {
+
+constexpr int kD = 128;                          // head size of this kernel
+constexpr int kPStep = 128;                      // keys per KV step
+constexpr int kPStepPages = kPStep / kBlockSize; // 8
+constexpr int kPHalfPages = kPStepPages / 2;     // K pages per CTA per step
+constexpr int kPStages = 3;                      // K / V stages = score buffers
+constexpr int kPThreads = 224;                   // 7 warps
+constexpr int kPQBytes = kPreRows * kD * 2;      // one 128-row Q tile
+constexpr int kPKBytes = (kPStep / 2) * kD * 2;  // 64 keys x 128 columns
+constexpr int kPVBytes = kPStep * 64 * 2;        // 128 keys x 64 columns
+constexpr int kPStgBytes = kPreRows * kD * 2;    // epilogue staging (two 64-column passes)
+constexpr uint32_t kColO = 3 * kPStep;           // O after the three score buffers
+constexpr int kPTmemCols = 512;
+constexpr float kPRescaleThreshold = 8.0f;       // log2 units
+constexpr size_t kPSmemUsed = 1024 + 2 * (size_t)kPQBytes + kPStages * (size_t)(kPKBytes + kPVBytes) +
+                              kPStgBytes + 512;
+
+enum : int {
+    bQFull = 0,     // [2] this CTA's Q tile landed (TMA tx)
+    bQEmpty = 2,    // [2] the item's last S is done (commit, both CTAs)
+    bQPeer = 4,     // [2] leader: the peer's Q tile landed (relayed)
+    bKFull = 6,     // [3]
+    bKEmpty = 9,    // [3]
+    bKPeer = 12,    // [3] leader
+    bVFull = 15,    // [3]
+    bVEmpty = 18,   // [3]
+    bVPeer = 21,    // [3] leader
+    bVTail = 24,    // a step that holds a sequence's partial last page lands here first
+    bSFull = 25,    // [3] scores of the step are in the buffer (commit, both CTAs)
+    bPFull = 28,    // [3] leader: P of the step written by the 8 softmax warps of the pair
+    bPvDone = 31,   // [3] P V of the step completed (commit, both CTAs)
+    bDrain = 34,
+    kPNumBars = 35
+};
+
+// A work item as one CTA of the pair sees it.
+struct PairItem {
+    int seq, q0, lq, lk, kvh;
+    int n;                 // 128-key steps of the pair (its last valid row's keys)
+    int kend;              // keys visible to the pair's last valid row
+    int my_row0;           // first packed row of this CTA's tile
+    int my_nrows;          // valid rows of this CTA's tile (0 .. 128)
+    int my_kend_lo;        // keys visible to this tile's first row
+};
+
+__device__ __forceinline__ int pair_visible(const PrefillParams &p, int lq, int lk, int row) {
+    if (!p.causal) return lk;
+    return min(lk, lk - lq + row / p.g + 1);
+}
+
+__device__ __forceinline__ PairItem make_item(const PrefillParams &p, const PreTile &t, uint32_t rank) {
+    PairItem it;
+    it.seq = t.seq;
+    it.q0 = t.q0;
+    it.lq = t.lq;
+    it.lk = t.lk;
+    it.kvh = t.kvh;
+    it.kend = pair_visible(p, t.lq, t.lk, t.row0 + t.nrows - 1);
+    it.n = (it.kend + kPStep - 1) / kPStep;
+    it.my_row0 = t.row0 + (int)rank * kPreRows;
+    it.my_nrows = max(0, min(kPreRows, t.nrows - (int)rank * kPreRows));
+    it.my_kend_lo = it.my_nrows > 0 ? pair_visible(p, t.lq, t.lk, it.my_row0) : it.kend;
+    return it;
+}
+
+// The pair's items: its range of the plan's list (dealt in advance).
+struct PairCursor {
+    int t, end;
+    __device__ __forceinline__ PairCursor(const PrefillParams &p, int pair)
+        : t(p.tile_begin[pair]), end(p.tile_begin[pair + 1]) {}
+    __device__ __forceinline__ bool next(const PrefillParams &p, PreTile &out) {
+        if (t >= end) return false;
+        out = p.tiles[t++];
+        return true;
+    }
+};
+
+// Block id of page `page` of the sequence for a step whose pair sees `kend`
+// keys (out-of-range or not-needed pages give num_blocks: TMA reads zeros).
+__device__ __forceinline__ int page_block_id(const PrefillParams &p, const int32_t *bt_row, int page,
+                                             int kend) {
+    int bid = p.num_blocks;
+    if (page * kBlockSize < kend) {
+        bid = __ldg(bt_row + page);
+        if (bid < 0 || bid >= p.num_blocks) {
+            record_status(p.status, UA_DEVICE_BAD_BLOCK_ID_BIT);
+            bid = p.num_blocks;
+        }
+    }
+    return bid;
+}
+
+// Waits whose outcome is the same in every lane of the warp (a lane that
+// gave up makes them all give up), so that the warp stays converged for the
+// elect.sync of the MMA issue.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, int *status) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
+}
+
+__device__ __forceinline__ bool wait_warp_cluster(uint32_t bar, uint32_t parity, int *status) {
+    return __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity, status));
+}
+
+__device__ __forceinline__ void local_commit_warp(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+
+// Rows [r_lo, r_hi) of a staged 64-column slice of O (row r at r * 128 bytes,
+// 16-byte pieces XOR-ed with r % 8) to out, by the tile's 128 threads.
+__device__ __noinline__ void pair_copy_rows(__nv_bfloat16 *out, const uint8_t *stg, int tid, int nrows,
+                                            int row0, int q0, int kvh, int g, int hq, int col0) {
+    for (int u = tid; u < nrows * 8; u += 128) {
+        const int row = u >> 3, piece = u & 7;
+        const uint4 val = *reinterpret_cast<const uint4 *>(stg + row * 128 + ((piece ^ (row & 7)) << 4));
+        const int prr = row0 + row;
+        *reinterpret_cast<uint4 *>(out + ((int64_t)(q0 + prr / g) * hq + kvh * g + prr % g) * kD + col0 +
+                                   8 * piece) = val;
+    }
+}
+
+}  // namespace
+
+template <bool kPos>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
+    ua_prefill_pair_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tm_q,
+                           const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_vh) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sq = smem_u32(smem);                              // Q[2]: [chunk][128 rows][64]
+    const uint32_t sk = sq + 2 * kPQBytes;                           // K[3]: [chunk][64 keys][64]
+    const uint32_t sv = sk + kPStages * kPKBytes;                    // V[3]: [page][16 keys][64]
+    uint8_t *sv_ptr = smem + 2 * kPQBytes + kPStages * kPKBytes;
+    uint8_t *stage_ptr = sv_ptr + kPStages * kPVBytes;               // [chunk][128 rows][64] bf16
+    const uint32_t sstage = smem_u32(stage_ptr);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(stage_ptr + kPStgBytes);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kPNumBars + 1);
+    const uint32_t bar0 = smem_u32(bars);
+    auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int pair = (int)(blockIdx.x >> 1);
+    // a pair with no item leaves before touching barriers or TMEM (both CTAs
+    // of the pair read the same range)
+    if (p.tile_begin[pair] == p.tile_begin[pair + 1]) return;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(bQFull + i), 1);
+            mbar_init(bar(bQEmpty + i), 1);
+            mbar_init(bar(bQPeer + i), 1);
+        }
+        for (int i = 0; i < kPStages; ++i) {
+            mbar_init(bar(bKFull + i), 1);
+            mbar_init(bar(bKEmpty + i), 1);
+            mbar_init(bar(bKPeer + i), 1);
+            mbar_init(bar(bVFull + i), 1);
+            mbar_init(bar(bVEmpty + i), 1);
+            mbar_init(bar(bVPeer + i), 1);
+            mbar_init(bar(bSFull + i), 1);
+            mbar_init(bar(bPFull + i), 8);
+            mbar_init(bar(bPvDone + i), 1);
+        }
+        mbar_init(bar(bVTail), 1);
+        mbar_init(bar(bDrain), 1);
+        fence_barrier_init();
+    }
+    if (warp == 4) {
+        tmem_alloc_pair(smem_u32(tmem_slot), kPTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync_all();       // barriers of both CTAs initialised, TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint64_t pol_kv = l2_policy_evict_last();   // K/V steps are re-read by sibling items
+
+    if (warp == 5) {
+        // ================================================================ Q + K producer
+        if (lane == 0) {
+            prefetch_tensormap(&tm_q);
+            prefetch_tensormap(&tm_k);
+        }
+        bool ok = true;
+        uint32_t e = 0, k_issued = 0, q_issued = 0;
+        PairCursor cur(p, pair);
+        PreTile t;
+        for (uint32_t k = 0; ok && cur.next(p, t); ++k) {
+            const PairItem it = make_item(p, t, rank);
+            int good = 1;
+            if (lane == 0) {
+                const uint32_t qb = k & 1;
+                // buffer qb is free once the last S of item k - 2 is done
+                if (k >= 2 && !mbar_wait(bar(bQEmpty + qb), ((k >> 1) - 1) & 1, p.status)) {
+                    good = 0;
+                } else {
+                    mbar_arrive_expect_tx(bar(bQFull + qb), kPQBytes);
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+                        tma_load_3d(sq + qb * kPQBytes + c * (kPreRows * 128), &tm_q, c * 64, it.kvh * p.g,
+                                    it.q0 + it.my_row0 / p.g, bar(bQFull + qb));
+                    ++q_issued;
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+            const int32_t *bt_row = p.block_table + (int64_t)it.seq * p.bt_stride;
+            for (int j = 0; j < it.n && ok; ++j, ++e) {
+                // lanes 0-3: this CTA's four pages of the step
+                int bid = p.num_blocks;
+                if (lane < kPHalfPages)
+                    bid = page_block_id(p, bt_row, j * kPStepPages + (int)rank * kPHalfPages + lane, it.kend);
+                int b[kPHalfPages];
+#pragma unroll
+                for (int i = 0; i < kPHalfPages; ++i) b[i] = __shfl_sync(0xffffffffu, bid, i);
+                const uint32_t s = e % kPStages, ph = (e / kPStages) & 1;
+                good = 1;
+                if (lane == 0) {
+                    if (!mbar_wait(bar(bKEmpty + s), ph ^ 1, p.status)) {
+                        good = 0;
+                    } else {
+                        mbar_arrive_expect_tx(bar(bKFull + s), kPKBytes);
+#pragma unroll
+                        for (int i = 0; i < kPHalfPages; ++i)
+#pragma unroll
+                            for (int c = 0; c < 2; ++c)
+                                tma_load_3d_hint(sk + s * kPKBytes + c * (kPKBytes / 2) + i * 2048, &tm_k, c * 64,
+                                                 it.kvh, b[i] * kBlockSize, bar(bKFull + s), pol_kv);
+                        ++k_issued;
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+            }
+        }
+        // drain: the last loads issued land before the CTA can exit
+        if (lane == 0) {
+            for (uint32_t x = (k_issued > (uint32_t)kPStages ? k_issued - kPStages : 0); x < k_issued; ++x)
+                mbar_wait(bar(bKFull + x % kPStages), (x / kPStages) & 1, p.status);
+            for (uint32_t x = (q_issued > 2u ? q_issued - 2 : 0); x < q_issued; ++x)
+                mbar_wait(bar(bQFull + (x & 1)), (x >> 1) & 1, p.status);
+        }
+    } else if (warp == 6) {
+        // ================================================================ V producer
+        if (lane == 0) prefetch_tensormap(&tm_vh);
+        bool ok = true;
+        uint32_t e = 0, v_issued = 0, tails = 0;
+        PairCursor cur(p, pair);
+        PreTile t;
+        while (ok && cur.next(p, t)) {
+            const PairItem it = make_item(p, t, rank);
+            const int32_t *bt_row = p.block_table + (int64_t)it.seq * p.bt_stride;
+            // the step holding the sequence's partial last page, if a row of the pair sees it
+            const int last_page_start = (it.lk - 1) & ~(kBlockSize - 1);
+            const int tail_step = ((it.lk & (kBlockSize - 1)) != 0 && last_page_start < it.kend)
+                                      ? last_page_start / kPStep : -1;
+            for (int j = 0; j < it.n && ok; ++j, ++e) {
+                int bid = p.num_blocks;
+                if (lane < kPStepPages) bid = page_block_id(p, bt_row, j * kPStepPages + lane, it.kend);
+                int b[kPStepPages];
+#pragma unroll
+                for (int i = 0; i < kPStepPages; ++i) b[i] = __shfl_sync(0xffffffffu, bid, i);
+                const uint32_t s = e % kPStages, ph = (e / kPStages) & 1;
+                const bool tail = (j == tail_step);
+                const uint32_t land = tail ? bar(bVTail) : bar(bVFull + s);
+                int good = 1;
+                if (lane == 0) {
+                    if (!mbar_wait(bar(bVEmpty + s), ph ^ 1, p.status)) {
+                        good = 0;
+                    } else {
+                        mbar_arrive_expect_tx(land, kPVBytes);
+#pragma unroll
+                        for (int i = 0; i < kPStepPages; ++i)
+                            tma_load_5d_hint(sv + s * kPVBytes + i * 2048, &tm_vh, 0, 0, (int)rank, it.kvh, b[i],
+                                             land, pol_kv);
+                        ++v_issued;
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+                if (ok && tail) {
+                    // wait for the step, zero the key rows past the context in the last
+                    // page (this CTA's 64 columns), then release the step to the MMAs
+                    const bool landed = mbar_wait(bar(bVTail), tails & 1, p.status);
+                    ++tails;
+                    if (!__all_sync(0xffffffffu, landed)) {
+                        ok = false;
+                    } else {
+                        const int k0 = it.lk - j * kPStep;                       // first key to clear
+                        const int k1 = last_page_start + kBlockSize - j * kPStep;  // end of the page
+                        for (int u = lane; u < (k1 - k0) * 8; u += 32) {
+                            const int key = k0 + (u >> 3);
+                            const int piece = u & 7;
+                            *reinterpret_cast<uint4 *>(sv_ptr + s * kPVBytes + (key / kBlockSize) * 2048 +
+                                                       (key % kBlockSize) * 128 + piece * 16) = make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(bVFull + s));
+                    }
+                }
+            }
+        }
+        if (lane == 0) {
+            for (uint32_t x = (v_issued > (uint32_t)kPStages ? v_issued - kPStages : 0); x < v_issued; ++x)
+                mbar_wait(bar(bVFull + x % kPStages), (x / kPStages) & 1, p.status);
+        }
+    } else if (warp == 4 && rank == 1) {
+        // ================================================================ relay (peer CTA)
+        // The leader's MMAs read this CTA's halves of Q, K and V; tell it when
+        // each has landed, in the order the leader consumes them.
+        const uint32_t lead_q = mapa_shared(bar(bQPeer), 0);
+        const uint32_t lead_k = mapa_shared(bar(bKPeer), 0);
+        const uint32_t lead_v = mapa_shared(bar(bVPeer), 0);
+        bool ok = true;
+        uint32_t e = 0;
+        PairCursor cur(p, pair);
+        PreTile t;
+        for (uint32_t k = 0; ok && cur.next(p, t); ++k) {
+            const PairItem it = make_item(p, t, rank);
+            const uint32_t qb = k & 1;
+            if (!wait_warp(bar(bQFull + qb), (k >> 1) & 1, p.status)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) mbar_arrive_cluster(lead_q + 8 * qb);
+            for (int j = 0; j < it.n && ok; ++j, ++e) {
+                const uint32_t s = e % kPStages, ph = (e / kPStages) & 1;
+                if (!wait_warp(bar(bKFull + s), ph, p.status)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) mbar_arrive_cluster(lead_k + 8 * s);
+                if (!wait_warp(bar(bVFull + s), ph, p.status)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) mbar_arrive_cluster(lead_v + 8 * s);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 4) {
+        // ================================================================ MMA issuer (leader CTA)
+        constexpr uint32_t idesc_s = umma_idesc_bf16(2 * kPreRows, kPStep, 0, 0);
+        constexpr uint32_t idesc_pv = umma_idesc_bf16(2 * kPreRows, kD, 0, 1);
+        bool ok = true;
+        bool issued_any = false;
+        // two cursors over the same item list: S runs two KV steps ahead of P V
+        PairCursor scur(p, pair), pcur(p, pair);
+        PreTile st{}, pt{};
+        PairItem sit{}, pit{};
+        int sj = 0, pj = 0;                // step within the S / P V cursor's item
+        uint32_t sk_item = 0;              // index of the S cursor's item (its Q buffer)
+        bool s_more = scur.next(p, st), p_more = pcur.next(p, pt);
+        if (s_more) sit = make_item(p, st, rank);
+        if (p_more) pit = make_item(p, pt, rank);
+        uint32_t x = 0, y = 0;             // S and P V issued so far (global KV step indices)
+        // S(x) into buffer x % 3; false when a wait gave up
+        auto issue_s = [&]() -> bool {
+            const uint32_t b = x % kPStages, ph = (x / kPStages) & 1;
+            const uint32_t qb = sk_item & 1;
+            if (sj == 0) {
+                // this item's Q tiles of both CTAs
+                if (!wait_warp(bar(bQFull + qb), (sk_item >> 1) & 1, p.status) ||
+                    !wait_warp_cluster(bar(bQPeer + qb), (sk_item >> 1) & 1, p.status))
+                    return false;
+            }
+            // the buffer's previous P has been read by P V(x - 3)
+            if (x >= (uint32_t)kPStages &&
+                !wait_warp(bar(bPvDone + b), ((x - kPStages) / kPStages) & 1, p.status))
+                return false;
+            if (!wait_warp(bar(bKFull + b), ph, p.status) || !wait_warp_cluster(bar(bKPeer + b), ph, p.status))
+                return false;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+                const uint32_t qoff = qb * kPQBytes + (kk >> 2) * (kPreRows * 128) + (kk & 3) * 32;
+                const uint32_t koff = b * kPKBytes + (kk >> 2) * (kPKBytes / 2) + (kk & 3) * 32;
+                umma_pair_ss_warp(tmem + b * kPStep, umma_desc_sw128(sq + qoff, 16, 1024),
+                                  umma_desc_sw128(sk + koff, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+            }
+            umma_pair_commit_warp(bar(bSFull + b));
+            umma_pair_commit_warp(bar(bKEmpty + b));
+            issued_any = true;
+            ++x;
+            if (++sj == sit.n) {
+                umma_pair_commit_warp(bar(bQEmpty + qb));   // the item's last S: its Q buffer is free
+                sj = 0;
+                ++sk_item;
+                s_more = scur.next(p, st);
+                if (s_more) sit = make_item(p, st, rank);
+            }
+            return true;
+        };
+        // O += P(y) V(y); the item's first step starts O from zero
+        auto issue_pv = [&]() -> bool {
+            const uint32_t b = y % kPStages, ph = (y / kPStages) & 1;
+            if (!wait_warp_cluster(bar(bPFull + b), ph, p.status)) return false;
+            if (!wait_warp(bar(bVFull + b), ph, p.status) || !wait_warp_cluster(bar(bVPeer + b), ph, p.status))
+                return false;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kPStepPages; ++kk) {
+                // 16 keys per MMA = one page of V: P columns b*128 + kk*8 .. +8 (bf16
+                // pairs); V page kk is [16 keys][64 columns], MN-major, 8-key groups 1 KB apart
+                const uint64_t bdesc = umma_desc_sw128(sv + b * kPVBytes + kk * 2048, 2048, 1024);
+                umma_pair_ts_warp(tmem + kColO, tmem + b * kPStep + kk * 8, bdesc, idesc_pv,
+                                  (pj == 0 && kk == 0) ? 0u : 1u);
+            }
+            umma_pair_commit_warp(bar(bPvDone + b));
+            umma_pair_commit_warp(bar(bVEmpty + b));
+            ++y;
+            if (++pj == pit.n) {
+                pj = 0;
+                p_more = pcur.next(p, pt);
+                if (p_more) pit = make_item(p, pt, rank);
+            }
+            return true;
+        };
+        for (int i = 0; i < 2 && ok && s_more; ++i) ok = issue_s();
+        while (ok && p_more) {
+            ok = issue_pv();
+            if (ok && s_more) ok = issue_s();
+        }
+        // every MMA issued has completed before TMEM is released
+        if (issued_any) {
+            local_commit_warp(bar(bDrain));
+            wait_warp(bar(bDrain), 0, p.status);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ================================================================ softmax + epilogue
+        const int r = warp * 32 + lane;                 // row of the tile = TMEM lane
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t s_base = tmem + lane_off;
+        const uint32_t o_addr = s_base + kColO;
+        const uint32_t lead_p = mapa_shared(bar(bPFull), 0);
+        bool ok = true;
+        uint32_t y = 0;     // KV steps over all items (step y lives in buffer y % 3)
+        PairCursor cur(p, pair);
+        PreTile t;
+        while (ok && cur.next(p, t)) {
+            const PairItem it = make_item(p, t, rank);
+            const int pr = it.my_row0 + r;
+            const bool valid = r < it.my_nrows;
+            const int i = pr / p.g;
+            const int kend = (p.causal && valid) ? min(it.lk, it.lk - it.lq + i + 1) : it.lk;
+            float m_run = -INFINITY;
+            float l = 0.f;
+            for (int j = 0; j < it.n; ++j, ++y) {
+                const uint32_t b = y % kPStages, ph = (y / kPStages) & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(bar(bSFull + b), ph, p.status))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t s_addr = s_base + b * kPStep;
+                uint32_t xs[kPStep];
+                {
+                    uint32_t (&lo)[64] = *reinterpret_cast<uint32_t (*)[64]>(&xs[0]);
+                    uint32_t (&hi)[64] = *reinterpret_cast<uint32_t (*)[64]>(&xs[64]);
+                    tmem_ld64(s_addr, lo);
+                    tmem_ld64(s_addr + 64, hi);
+                }
+                if (!kPos) {
+#pragma unroll
+                    for (int k = 0; k < kPStep; ++k)
+                        xs[k] = __float_as_uint(__uint_as_float(xs[k]) * p.scale_log2);
+                }
+                constexpr uint32_t kNegInf = 0xff800000u;
+                if ((j + 1) * kPStep > it.my_kend_lo) {
+                    const int lim = kend - j * kPStep;               // visible keys of this step
+#pragma unroll
+                    for (int k = 0; k < kPStep; ++k) xs[k] = k < lim ? xs[k] : kNegInf;
+                }
+                float m8[8];
+#pragma unroll
+                for (int a = 0; a < 8; ++a) m8[a] = __uint_as_float(xs[a]);
+#pragma unroll
+                for (int k = 8; k < kPStep; k += 2)
+                    m8[(k >> 1) & 7] = fmax3(m8[(k >> 1) & 7], __uint_as_float(xs[k]), __uint_as_float(xs[k + 1]));
+                float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+                if (kPos) mx *= p.scale_log2;
+                if (j == 0) {
+                    m_run = mx;
+                } else if (__any_sync(0xffffffffu, mx > m_run + kPRescaleThreshold)) {
+                    // a row max of this warp grew a lot: move the warp's rows to their new
+                    // max and rescale O (after the P V of the previous step) and l
+                    const float m_new = fmaxf(m_run, mx);
+                    const float alpha = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run - m_new);
+                    const uint32_t pb = (y - 1) % kPStages, pph = ((y - 1) / kPStages) & 1;
+                    if (!__all_sync(0xffffffffu, mbar_wait(bar(bPvDone + pb), pph, p.status))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < kD / 32; ++c) {
+                        uint32_t v[32];
+                        tmem_ld32(o_addr + 32 * c, v);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+                        tmem_st32(o_addr + 32 * c, v);
+                    }
+                    l *= alpha;
+                    m_run = m_new;
+                }
+                const float mu = (m_run == -INFINITY) ? 0.f : m_run;
+                // p = 2^(s * c - mu), two lanes of work per FMA, summed in 4 chains,
+                // packed to bf16 pairs over the first 64 columns of this score buffer
+                const float2 c2 = kPos ? make_float2(p.scale_log2, p.scale_log2) : make_float2(1.f, 1.f);
+                const float2 nmu2 = make_float2(-mu, -mu);
+                float2 l4[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) l4[a] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        const float2 yv = ffma2(make_float2(__uint_as_float(xs[64 * h + 2 * k]),
+                                                            __uint_as_float(xs[64 * h + 2 * k + 1])),
+                                                c2, nmu2);
+                        const float2 pv = make_float2(fast_exp2(yv.x), fast_exp2(yv.y));
+                        l4[k & 3] = fadd2(l4[k & 3], pv);
+                        pk[k] = pack_bf16x2(pv.x, pv.y);
+                    }
+                    tmem_st32(s_addr + 32 * h, pk);
+                }
+                l += ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) + ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y));
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(lead_p + 8 * b);
+            }
+            if (!ok) break;
+            // ---- epilogue: O / l -> bf16 rows of out (after the item's last P V)
+            const uint32_t lb = (y - 1) % kPStages, lph = ((y - 1) / kPStages) & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(bPvDone + lb), lph, p.status))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            if (p.lse != nullptr && valid)
+                p.lse[(int64_t)(it.q0 + i) * p.hq + it.kvh * p.g + pr % p.g] = row_lse(m_run, l);
+            const bool leader = r == 0;
+            // the previous item's stores have read the staging buffer
+            if (leader) bulk_wait_read_all();
+            named_barrier_sync(1, 128);
+#pragma unroll 1
+            for (int h = 0; h < kD / 64; ++h) {
+                uint8_t *stg = stage_ptr + h * (kPreRows * 128);
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(o_addr + 64 * h + 32 * c, v);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        *reinterpret_cast<uint4 *>(stg + r * 128 + (((4 * c + k) ^ (r & 7)) << 4)) = make_uint4(
+                            pack_bf16x2(__uint_as_float(v[8 * k]) * inv, __uint_as_float(v[8 * k + 1]) * inv),
+                            pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv),
+                            pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv),
+                            pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv));
+                }
+            }
+            fence_proxy_async_smem();
+            named_barrier_sync(1, 128);
+            if (it.my_nrows == kPreRows) {
+                if (leader) {
+#pragma unroll
+                    for (int h = 0; h < kD / 64; ++h)
+                        tma_store_3d(&tm_o, sstage + h * (kPreRows * 128), 64 * h, it.kvh * p.g,
+                                     it.q0 + it.my_row0 / p.g);
+                    bulk_commit_group();
+                }
+            } else if (it.my_nrows > 0) {
+                // a tile that ends before 128 rows: the box would run into the next
+                // sequence's rows, so its rows are copied out by hand
+#pragma unroll 1
+                for (int h = 0; h < kD / 64; ++h)
+                    pair_copy_rows(p.out, stage_ptr + h * (kPreRows * 128), r, it.my_nrows, it.my_row0, it.q0,
+                                   it.kvh, p.g, p.hq, 64 * h);
+                named_barrier_sync(1, 128);     // the buffer is free for the next item
+            }
+            // O is read: the next item's first P V (which overwrites O) waits for this
+            // CTA's P of that item, which comes after these loads
+        }
+        // the output stores have completed before the CTA's shared memory goes away
+        if (r == 0) bulk_wait_all();
+    }
+
+    // ---- teardown: both CTAs are done with TMEM and with each other's barriers
+    tc_fence_before();
+    cluster_sync_all();
+    if (warp == 4) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, kPTmemCols);
+    }
+    cluster_sync_all();
+}
+
+template <bool kPos>
+static cudaError_t launch_pair_t(const PrefillParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_o,
+                                 const CUtensorMap &tm_k, const CUtensorMap &tm_vh, int pairs,
+                                 cudaStream_t stream) {
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(ua_prefill_pair_kernel<kPos>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmemUsed);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    ua_prefill_pair_kernel<kPos><<<2 * pairs, kPThreads, kPSmemUsed, stream>>>(p, tm_q, tm_o, tm_k, tm_vh);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_pair(const PrefillParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_o,
+                                const CUtensorMap &tm_k, const CUtensorMap &tm_vh, int pairs,
+                                cudaStream_t stream) {
+    return p.scale_log2 > 0.f ? launch_pair_t<true>(p, tm_q, tm_o, tm_k, tm_vh, pairs, stream)
+                              : launch_pair_t<false>(p, tm_q, tm_o, tm_k, tm_vh, pairs, stream);
+}
+
+}  // namespace ua
