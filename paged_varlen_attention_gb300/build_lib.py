@@ -58,10 +58,10 @@ def _compile(cmd, log_path):
     return log_path
 
 
-# Register ceilings of the kernels: the prefill kernel runs 384 threads on one
+# Register ceilings of the kernels: both prefill kernels run 384 threads on one
 # SM, so a thread may hold at most 65536 / 384 -> 168 registers; a build where
 # ptxas goes past that is refused.
-LAUNCH_REGS = {"ua_prefill_kernel": 168, "ua_prefill_pair_kernel": 255}
+LAUNCH_REGS = {"ua_prefill_kernel": 168, "ua_prefill_pair_kernel": 168}
 
 
 def _registers_by_kernel(log_text: str) -> dict:

@@ -24,26 +24,34 @@
 //     step j runs, and S(j + 2) reuses the buffer of P V(j - 1), which had a
 //     whole step to complete.
 //
-// Roles (7 warps per CTA):
-//   warps 0-3  softmax of the CTA's 128 rows (one row per thread = TMEM
-//              lane): scale into the log2 domain, bottom-right causal mask,
-//              row max, exp2, row sum, P as bf16 over the first 64 columns of
-//              the step's score buffer; every warp then arrives on the
-//              leader's P barrier (the peer's warps remotely).  O is rescaled
-//              only when a row max grows by more than 2^8.  After an item's
-//              last P V: O / l as bf16 rows of out (TMA store of the 128-row
-//              tile, or by hand for a tile that ends early).
-//   warp 4     leader CTA: allocates TMEM (both CTAs' warp 4 do, collectively)
-//              and issues the pair's MMAs (one elected lane): S(x) = Q K^T
-//              for the flattened sequence of KV steps of the pair's items,
-//              two ahead: S(0), S(1), then for each step y: P V(y), S(y + 2).
+// Roles (12 warps per CTA):
+//   warps 0-7  softmax of the CTA's 128 rows: warp w takes the rows of TMEM lane
+//              quarter w % 4 (one row per thread) and half w / 4 of each step's
+//              keys; the two warps of a quarter combine each row's max through
+//              shared memory.  Scale into the log2 domain, bottom-right causal
+//              mask, row max, exp2, row sum, P as bf16 over the first 64
+//              columns of the step's score buffer; every warp then arrives on
+//              the leader's P barrier (the peer's warps remotely).  O is
+//              rescaled only when a row max grows by more than 2^8.  After an
+//              item's last P V: O / l as bf16 rows of out (each warp its half
+//              of the columns; TMA store of the 128-row tile, or by hand for a
+//              tile that ends early).
+//   warp 8     allocates TMEM (warp 8 of both CTAs, collectively).  Leader
+//              CTA: one lane issues the pair's score MMAs S(x) = Q K^T over the
+//              KV steps of the pair's items in order, each once its buffer's
+//              previous P has been read (P V(x - 3) done).  Peer CTA: one lane
+//              relays "this CTA's Q tile / K half has landed" to the leader's
+//              barriers (the leader's MMAs read both halves).
+//   warp 11    leader CTA: one lane issues O += P(y) V(y) once the pair's P(y)
+//              and both V halves are there.  Peer CTA: relays its V halves.
+//              Two issuing lanes, because one lane that waits for its barriers
+//              and issues 16 MMAs and their commits per step was measured to
+//              take longer than the tensor core needs for them.
 //              Commits arrive on the barrier at the same offset in both CTAs.
-//              Peer CTA: relays "this CTA's half of Q / K / V has landed" to
-//              the leader's barriers (the leader's MMAs read both halves).
-//   warp 5     TMA producer of the CTA's Q tiles (double-buffered, so the next
+//   warp 9     TMA producer of the CTA's Q tiles (double-buffered, so the next
 //              item's scores can start before this item ends) and K halves
 //              (four {64, 1, 16} boxes per 64 columns of [pages*16, Hkv, D]).
-//   warp 6     TMA producer of the CTA's V halves (one {64, 16, 1, 1, 1} box
+//   warp 10    TMA producer of the CTA's V halves (one {64, 16, 1, 1, 1} box
 //              per page: its 64 columns of the page); zeroes the rows past
 //              the context of a sequence's last, partial page (they may hold
 //              anything, NaN included, and 0 x NaN is NaN) before it releases
@@ -61,7 +69,7 @@ constexpr int kPStep = 128;                      // keys per KV step
 constexpr int kPStepPages = kPStep / kBlockSize; // 8
 constexpr int kPHalfPages = kPStepPages / 2;     // K pages per CTA per step
 constexpr int kPStages = 3;                      // K / V stages = score buffers
-constexpr int kPThreads = 224;                   // 7 warps
+constexpr int kPThreads = 384;                   // 12 warps
 constexpr int kPQBytes = kPreRows * kD * 2;      // one 128-row Q tile
 constexpr int kPKBytes = (kPStep / 2) * kD * 2;  // 64 keys x 128 columns
 constexpr int kPVBytes = kPStep * 64 * 2;        // 128 keys x 64 columns
@@ -69,8 +77,9 @@ constexpr int kPStgBytes = kPreRows * kD * 2;    // epilogue staging (two 64-col
 constexpr uint32_t kColO = 3 * kPStep;           // O after the three score buffers
 constexpr int kPTmemCols = 512;
 constexpr float kPRescaleThreshold = 8.0f;       // log2 units
+constexpr int kPRedBytes = 3 * 2 * kPreRows * 4;  // row max (two step parities) and sum exchange
 constexpr size_t kPSmemUsed = 1024 + 2 * (size_t)kPQBytes + kPStages * (size_t)(kPKBytes + kPVBytes) +
-                              kPStgBytes + 512;
+                              kPStgBytes + 512 + kPRedBytes;
 
 enum : int {
     bQFull = 0,     // [2] this CTA's Q tile landed (TMA tx)
@@ -84,10 +93,11 @@ enum : int {
     bVPeer = 21,    // [3] leader
     bVTail = 24,    // a step that holds a sequence's partial last page lands here first
     bSFull = 25,    // [3] scores of the step are in the buffer (commit, both CTAs)
-    bPFull = 28,    // [3] leader: P of the step written by the 8 softmax warps of the pair
+    bPFull = 28,    // [3] leader: P of the step written by the 16 softmax warps of the pair
     bPvDone = 31,   // [3] P V of the step completed (commit, both CTAs)
-    bDrain = 34,
-    kPNumBars = 35
+    bDrain = 34,    // the S issuer's MMAs have completed
+    bDrain2 = 35,   // the P V issuer's MMAs have completed
+    kPNumBars = 36
 };
 
 // A work item as one CTA of the pair sees it.
@@ -147,23 +157,40 @@ __device__ __forceinline__ int page_block_id(const PrefillParams &p, const int32
     return bid;
 }
 
-// Waits whose outcome is the same in every lane of the warp (a lane that
-// gave up makes them all give up), so that the warp stays converged for the
-// elect.sync of the MMA issue.
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, int *status) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
-}
-
-__device__ __forceinline__ bool wait_warp_cluster(uint32_t bar, uint32_t parity, int *status) {
-    return __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity, status));
-}
-
-__device__ __forceinline__ void local_commit_warp(uint32_t bar) {
+// tcgen05 issue by one thread (the issuing warps run their loops on lane 0).
+__device__ __forceinline__ void umma_pair_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+__device__ __forceinline__ void umma_pair_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on the barrier at offset `bar` in both CTAs once this thread's MMAs so far have completed.
+__device__ __forceinline__ void umma_pair_commit(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .b16 m;\n\t"
+        "mov.b16 m, 3;\n\t"
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], m;\n\t}" ::"r"(bar)
+        : "memory");
+}
+
+// The same on this CTA's barrier only.
+__device__ __forceinline__ void umma_local_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
 }
 
 // Rows [r_lo, r_hi) of a staged 64-column slice of O (row r at r * 128 bytes,
@@ -196,6 +223,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     const uint32_t sstage = smem_u32(stage_ptr);
     uint64_t *bars = reinterpret_cast<uint64_t *>(stage_ptr + kPStgBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kPNumBars + 1);
+    float *red = reinterpret_cast<float *>(stage_ptr + kPStgBytes + 512);   // [3][2][128]
     const uint32_t bar0 = smem_u32(bars);
     auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
 
@@ -221,14 +249,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             mbar_init(bar(bVEmpty + i), 1);
             mbar_init(bar(bVPeer + i), 1);
             mbar_init(bar(bSFull + i), 1);
-            mbar_init(bar(bPFull + i), 8);
+            mbar_init(bar(bPFull + i), 16);
             mbar_init(bar(bPvDone + i), 1);
         }
         mbar_init(bar(bVTail), 1);
         mbar_init(bar(bDrain), 1);
+        mbar_init(bar(bDrain2), 1);
         fence_barrier_init();
     }
-    if (warp == 4) {
+    if (warp == 8) {
         tmem_alloc_pair(smem_u32(tmem_slot), kPTmemCols);
         tmem_relinquish_pair();
     }
@@ -238,7 +267,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const uint64_t pol_kv = l2_policy_evict_last();   // K/V steps are re-read by sibling items
 
-    if (warp == 5) {
+    if (warp == 9) {
         // ================================================================ Q + K producer
         if (lane == 0) {
             prefetch_tensormap(&tm_q);
@@ -301,7 +330,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             for (uint32_t x = (q_issued > 2u ? q_issued - 2 : 0); x < q_issued; ++x)
                 mbar_wait(bar(bQFull + (x & 1)), (x >> 1) & 1, p.status);
         }
-    } else if (warp == 6) {
+    } else if (warp == 10) {
         // ================================================================ V producer
         if (lane == 0) prefetch_tensormap(&tm_vh);
         bool ok = true;
@@ -365,136 +394,140 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             for (uint32_t x = (v_issued > (uint32_t)kPStages ? v_issued - kPStages : 0); x < v_issued; ++x)
                 mbar_wait(bar(bVFull + x % kPStages), (x / kPStages) & 1, p.status);
         }
-    } else if (warp == 4 && rank == 1) {
-        // ================================================================ relay (peer CTA)
-        // The leader's MMAs read this CTA's halves of Q, K and V; tell it when
-        // each has landed, in the order the leader consumes them.
-        const uint32_t lead_q = mapa_shared(bar(bQPeer), 0);
-        const uint32_t lead_k = mapa_shared(bar(bKPeer), 0);
-        const uint32_t lead_v = mapa_shared(bar(bVPeer), 0);
-        bool ok = true;
-        uint32_t e = 0;
-        PairCursor cur(p, pair);
-        PreTile t;
-        for (uint32_t k = 0; ok && cur.next(p, t); ++k) {
-            const PairItem it = make_item(p, t, rank);
-            const uint32_t qb = k & 1;
-            if (!wait_warp(bar(bQFull + qb), (k >> 1) & 1, p.status)) {
-                ok = false;
-                break;
-            }
-            if (lane == 0) mbar_arrive_cluster(lead_q + 8 * qb);
-            for (int j = 0; j < it.n && ok; ++j, ++e) {
-                const uint32_t s = e % kPStages, ph = (e / kPStages) & 1;
-                if (!wait_warp(bar(bKFull + s), ph, p.status)) {
-                    ok = false;
-                    break;
+    } else if ((warp == 8 || warp == 11) && rank == 1) {
+        // ================================================================ relays (peer CTA)
+        // The leader's MMAs read this CTA's halves of Q, K (warp 8) and V (warp 11);
+        // tell it when each has landed, in the order the leader consumes them.
+        // The loads are complete once this lane has seen their barrier, so the
+        // arrivals need no ordering of their own (relaxed: a release at cluster
+        // scope cost 500-1,400 ns per arrival here).
+        if (lane == 0) {
+            const bool qk = warp == 8;
+            const uint32_t lead_q = mapa_shared(bar(bQPeer), 0);
+            const uint32_t lead_kv = mapa_shared(bar(qk ? bKPeer : bVPeer), 0);
+            const int full = qk ? bKFull : bVFull;
+            bool ok = true;
+            uint32_t e = 0;
+            PairCursor cur(p, pair);
+            PreTile t;
+            for (uint32_t k = 0; ok && cur.next(p, t); ++k) {
+                const PairItem it = make_item(p, t, rank);
+                const uint32_t qb = k & 1;
+                if (qk) {
+                    if (!mbar_wait(bar(bQFull + qb), (k >> 1) & 1, p.status)) break;
+                    mbar_arrive_cluster_relaxed(lead_q + 8 * qb);
                 }
-                if (lane == 0) mbar_arrive_cluster(lead_k + 8 * s);
-                if (!wait_warp(bar(bVFull + s), ph, p.status)) {
-                    ok = false;
-                    break;
+                for (int j = 0; j < it.n; ++j, ++e) {
+                    const uint32_t s = e % kPStages, ph = (e / kPStages) & 1;
+                    if (!mbar_wait(bar(full + s), ph, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_cluster_relaxed(lead_kv + 8 * s);
                 }
-                if (lane == 0) mbar_arrive_cluster(lead_v + 8 * s);
             }
         }
         __syncwarp();
-    } else if (warp == 4) {
-        // ================================================================ MMA issuer (leader CTA)
-        constexpr uint32_t idesc_s = umma_idesc_bf16(2 * kPreRows, kPStep, 0, 0);
-        constexpr uint32_t idesc_pv = umma_idesc_bf16(2 * kPreRows, kD, 0, 1);
-        bool ok = true;
-        bool issued_any = false;
-        // two cursors over the same item list: S runs two KV steps ahead of P V
-        PairCursor scur(p, pair), pcur(p, pair);
-        PreTile st{}, pt{};
-        PairItem sit{}, pit{};
-        int sj = 0, pj = 0;                // step within the S / P V cursor's item
-        uint32_t sk_item = 0;              // index of the S cursor's item (its Q buffer)
-        bool s_more = scur.next(p, st), p_more = pcur.next(p, pt);
-        if (s_more) sit = make_item(p, st, rank);
-        if (p_more) pit = make_item(p, pt, rank);
-        uint32_t x = 0, y = 0;             // S and P V issued so far (global KV step indices)
-        // S(x) into buffer x % 3; false when a wait gave up
-        auto issue_s = [&]() -> bool {
-            const uint32_t b = x % kPStages, ph = (x / kPStages) & 1;
-            const uint32_t qb = sk_item & 1;
-            if (sj == 0) {
-                // this item's Q tiles of both CTAs
-                if (!wait_warp(bar(bQFull + qb), (sk_item >> 1) & 1, p.status) ||
-                    !wait_warp_cluster(bar(bQPeer + qb), (sk_item >> 1) & 1, p.status))
-                    return false;
-            }
-            // the buffer's previous P has been read by P V(x - 3)
-            if (x >= (uint32_t)kPStages &&
-                !wait_warp(bar(bPvDone + b), ((x - kPStages) / kPStages) & 1, p.status))
-                return false;
-            if (!wait_warp(bar(bKFull + b), ph, p.status) || !wait_warp_cluster(bar(bKPeer + b), ph, p.status))
-                return false;
-            tc_fence_after();
+    } else if (warp == 8) {
+        // ================================================================ S issuer (leader CTA)
+        // One lane issues S(x) = Q K^T into score buffer x % 3 for the pair's
+        // KV steps in order, as soon as that buffer's previous P has been read
+        // (P V(x - 3) done) and both CTAs' K halves of the step have landed.
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = umma_idesc_bf16(2 * kPreRows, kPStep, 0, 0);
+            bool ok = true, issued_any = false;
+            uint32_t x = 0;
+            PairCursor cur(p, pair);
+            PreTile t;
+            for (uint32_t k = 0; ok && cur.next(p, t); ++k) {
+                const PairItem it = make_item(p, t, rank);
+                const uint32_t qb = k & 1, qph = (k >> 1) & 1;
+                if (!mbar_wait(bar(bQFull + qb), qph, p.status) ||
+                    !mbar_wait_cluster(bar(bQPeer + qb), qph, p.status))
+                    break;
+                const uint64_t qd = umma_desc_sw128(sq + qb * kPQBytes, 16, 1024);
+                for (int j = 0; j < it.n; ++j, ++x) {
+                    const uint32_t b = x % kPStages, ph = (x / kPStages) & 1;
+                    if ((x >= (uint32_t)kPStages &&
+                         !mbar_wait(bar(bPvDone + b), ((x - kPStages) / kPStages) & 1, p.status)) ||
+                        !mbar_wait(bar(bKFull + b), ph, p.status) ||
+                        !mbar_wait_cluster(bar(bKPeer + b), ph, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t kd = umma_desc_sw128(sk + b * kPKBytes, 16, 1024);
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
-                const uint32_t qoff = qb * kPQBytes + (kk >> 2) * (kPreRows * 128) + (kk & 3) * 32;
-                const uint32_t koff = b * kPKBytes + (kk >> 2) * (kPKBytes / 2) + (kk & 3) * 32;
-                umma_pair_ss_warp(tmem + b * kPStep, umma_desc_sw128(sq + qoff, 16, 1024),
-                                  umma_desc_sw128(sk + koff, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < kD / 16; ++kk)
+                        umma_pair_ss(tmem + b * kPStep, qd + (uint64_t)(((kk >> 2) * (kPreRows * 128) + (kk & 3) * 32) >> 4),
+                                     kd + (uint64_t)(((kk >> 2) * (kPKBytes / 2) + (kk & 3) * 32) >> 4), idesc_s,
+                                     kk > 0 ? 1u : 0u);
+                    umma_pair_commit(bar(bSFull + b));
+                    umma_pair_commit(bar(bKEmpty + b));
+                    issued_any = true;
+                }
+                if (ok) umma_pair_commit(bar(bQEmpty + qb));   // the item's last S: its Q buffer is free
             }
-            umma_pair_commit_warp(bar(bSFull + b));
-            umma_pair_commit_warp(bar(bKEmpty + b));
-            issued_any = true;
-            ++x;
-            if (++sj == sit.n) {
-                umma_pair_commit_warp(bar(bQEmpty + qb));   // the item's last S: its Q buffer is free
-                sj = 0;
-                ++sk_item;
-                s_more = scur.next(p, st);
-                if (s_more) sit = make_item(p, st, rank);
+            // every MMA issued has completed before TMEM is released
+            if (issued_any) {
+                umma_local_commit(bar(bDrain));
+                mbar_wait(bar(bDrain), 0, p.status);
             }
-            return true;
-        };
-        // O += P(y) V(y); the item's first step starts O from zero
-        auto issue_pv = [&]() -> bool {
-            const uint32_t b = y % kPStages, ph = (y / kPStages) & 1;
-            if (!wait_warp_cluster(bar(bPFull + b), ph, p.status)) return false;
-            if (!wait_warp(bar(bVFull + b), ph, p.status) || !wait_warp_cluster(bar(bVPeer + b), ph, p.status))
-                return false;
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < kPStepPages; ++kk) {
-                // 16 keys per MMA = one page of V: P columns b*128 + kk*8 .. +8 (bf16
-                // pairs); V page kk is [16 keys][64 columns], MN-major, 8-key groups 1 KB apart
-                const uint64_t bdesc = umma_desc_sw128(sv + b * kPVBytes + kk * 2048, 2048, 1024);
-                umma_pair_ts_warp(tmem + kColO, tmem + b * kPStep + kk * 8, bdesc, idesc_pv,
-                                  (pj == 0 && kk == 0) ? 0u : 1u);
-            }
-            umma_pair_commit_warp(bar(bPvDone + b));
-            umma_pair_commit_warp(bar(bVEmpty + b));
-            ++y;
-            if (++pj == pit.n) {
-                pj = 0;
-                p_more = pcur.next(p, pt);
-                if (p_more) pit = make_item(p, pt, rank);
-            }
-            return true;
-        };
-        for (int i = 0; i < 2 && ok && s_more; ++i) ok = issue_s();
-        while (ok && p_more) {
-            ok = issue_pv();
-            if (ok && s_more) ok = issue_s();
-        }
-        // every MMA issued has completed before TMEM is released
-        if (issued_any) {
-            local_commit_warp(bar(bDrain));
-            wait_warp(bar(bDrain), 0, p.status);
         }
         __syncwarp();
-    } else if (warp < 4) {
+    } else if (warp == 11) {
+        // ================================================================ P V issuer (leader CTA)
+        // One lane issues O += P(y) V(y) once the pair's 8 softmax warps have
+        // written P(y) and both CTAs' V halves of the step have landed; an
+        // item's first step starts O from zero.
+        if (lane == 0) {
+            constexpr uint32_t idesc_pv = umma_idesc_bf16(2 * kPreRows, kD, 0, 1);
+            bool ok = true, issued_any = false;
+            uint32_t y = 0;
+            PairCursor cur(p, pair);
+            PreTile t;
+            while (ok && cur.next(p, t)) {
+                const PairItem it = make_item(p, t, rank);
+                for (int j = 0; j < it.n; ++j, ++y) {
+                    const uint32_t b = y % kPStages, ph = (y / kPStages) & 1;
+                    if (!mbar_wait_cluster(bar(bPFull + b), ph, p.status) ||
+                        !mbar_wait(bar(bVFull + b), ph, p.status) ||
+                        !mbar_wait_cluster(bar(bVPeer + b), ph, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // 16 keys per MMA = one page of V: P columns b*128 + kk*8 .. +8 (bf16
+                    // pairs); V page kk is [16 keys][64 columns], MN-major, 8-key groups 1 KB apart
+                    const uint64_t vd = umma_desc_sw128(sv + b * kPVBytes, 2048, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < kPStepPages; ++kk)
+                        umma_pair_ts(tmem + kColO, tmem + b * kPStep + kk * 8, vd + (uint64_t)((kk * 2048) >> 4),
+                                     idesc_pv, (j == 0 && kk == 0) ? 0u : 1u);
+                    umma_pair_commit(bar(bPvDone + b));
+                    umma_pair_commit(bar(bVEmpty + b));
+                    issued_any = true;
+                }
+            }
+            if (issued_any) {
+                umma_local_commit(bar(bDrain2));
+                mbar_wait(bar(bDrain2), 0, p.status);
+            }
+        }
+        __syncwarp();
+    } else if (warp < 8) {
         // ================================================================ softmax + epilogue
-        const int r = warp * 32 + lane;                 // row of the tile = TMEM lane
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        // Warp w takes the rows of TMEM lane quarter q = w % 4 (one row per
+        // thread) and half h = w / 4 of each step's 128 keys and of O's 128
+        // columns; the two warps of a quarter (one SMSP) combine each row's max
+        // every step, and its sum at the item's end, through shared memory.
+        const int q = warp & 3, h = warp >> 2;
+        const int r = q * 32 + lane;                    // row of the tile = TMEM lane
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         const uint32_t s_base = tmem + lane_off;
-        const uint32_t o_addr = s_base + kColO;
+        const uint32_t o_addr = s_base + kColO + 64 * h;
         const uint32_t lead_p = mapa_shared(bar(bPFull), 0);
+        const int qbar = 2 + q;                         // named barrier of the quarter's two warps
         bool ok = true;
         uint32_t y = 0;     // KV steps over all items (step y lives in buffer y % 3)
         PairCursor cur(p, pair);
@@ -506,7 +539,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             const int i = pr / p.g;
             const int kend = (p.causal && valid) ? min(it.lk, it.lk - it.lq + i + 1) : it.lk;
             float m_run = -INFINITY;
-            float l = 0.f;
+            float l = 0.f;          // this half's share of the row sum
             for (int j = 0; j < it.n; ++j, ++y) {
                 const uint32_t b = y % kPStages, ph = (y / kPStages) & 1;
                 if (!__all_sync(0xffffffffu, mbar_wait(bar(bSFull + b), ph, p.status))) {
@@ -514,38 +547,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t s_addr = s_base + b * kPStep;
-                uint32_t xs[kPStep];
-                {
-                    uint32_t (&lo)[64] = *reinterpret_cast<uint32_t (*)[64]>(&xs[0]);
-                    uint32_t (&hi)[64] = *reinterpret_cast<uint32_t (*)[64]>(&xs[64]);
-                    tmem_ld64(s_addr, lo);
-                    tmem_ld64(s_addr + 64, hi);
-                }
+                uint32_t xs[64];
+                tmem_ld64(s_base + b * kPStep + 64 * h, xs);
                 if (!kPos) {
 #pragma unroll
-                    for (int k = 0; k < kPStep; ++k)
-                        xs[k] = __float_as_uint(__uint_as_float(xs[k]) * p.scale_log2);
+                    for (int k = 0; k < 64; ++k) xs[k] = __float_as_uint(__uint_as_float(xs[k]) * p.scale_log2);
                 }
                 constexpr uint32_t kNegInf = 0xff800000u;
                 if ((j + 1) * kPStep > it.my_kend_lo) {
-                    const int lim = kend - j * kPStep;               // visible keys of this step
+                    const int lim = kend - j * kPStep - 64 * h;     // visible keys of this half step
 #pragma unroll
-                    for (int k = 0; k < kPStep; ++k) xs[k] = k < lim ? xs[k] : kNegInf;
+                    for (int k = 0; k < 64; ++k) xs[k] = k < lim ? xs[k] : kNegInf;
                 }
                 float m8[8];
 #pragma unroll
                 for (int a = 0; a < 8; ++a) m8[a] = __uint_as_float(xs[a]);
 #pragma unroll
-                for (int k = 8; k < kPStep; k += 2)
+                for (int k = 8; k < 64; k += 2)
                     m8[(k >> 1) & 7] = fmax3(m8[(k >> 1) & 7], __uint_as_float(xs[k]), __uint_as_float(xs[k + 1]));
-                float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+                const float mh = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+                // the row's max over both halves (slots alternate by step, so a warp
+                // never overwrites a value its partner has not read yet)
+                float *xm = red + (y & 1) * (2 * kPreRows);
+                xm[h * kPreRows + r] = mh;
+                named_barrier_sync(qbar, 64);
+                float mx = fmaxf(mh, xm[(1 - h) * kPreRows + r]);
                 if (kPos) mx *= p.scale_log2;
                 if (j == 0) {
                     m_run = mx;
                 } else if (__any_sync(0xffffffffu, mx > m_run + kPRescaleThreshold)) {
-                    // a row max of this warp grew a lot: move the warp's rows to their new
-                    // max and rescale O (after the P V of the previous step) and l
+                    // a row max of this quarter grew a lot (both warps of the quarter see
+                    // the same maxes, so both take this path): move the rows to their new
+                    // max and rescale this half of O (after the P V of the previous step) and l
                     const float m_new = fmaxf(m_run, mx);
                     const float alpha = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run - m_new);
                     const uint32_t pb = (y - 1) % kPStages, pph = ((y - 1) / kPStages) & 1;
@@ -555,7 +588,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                     }
                     tc_fence_after();
 #pragma unroll
-                    for (int c = 0; c < kD / 32; ++c) {
+                    for (int c = 0; c < 2; ++c) {
                         uint32_t v[32];
                         tmem_ld32(o_addr + 32 * c, v);
 #pragma unroll
@@ -567,31 +600,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                 }
                 const float mu = (m_run == -INFINITY) ? 0.f : m_run;
                 // p = 2^(s * c - mu), two lanes of work per FMA, summed in 4 chains,
-                // packed to bf16 pairs over the first 64 columns of this score buffer
+                // packed to bf16 pairs: keys 64 h .. 64 h + 63 go over columns 32 h ..
+                // 32 h + 31 of this score buffer
                 const float2 c2 = kPos ? make_float2(p.scale_log2, p.scale_log2) : make_float2(1.f, 1.f);
                 const float2 nmu2 = make_float2(-mu, -mu);
                 float2 l4[4];
 #pragma unroll
                 for (int a = 0; a < 4; ++a) l4[a] = make_float2(0.f, 0.f);
+                uint32_t pk[32];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const float2 yv = ffma2(make_float2(__uint_as_float(xs[64 * h + 2 * k]),
-                                                            __uint_as_float(xs[64 * h + 2 * k + 1])),
-                                                c2, nmu2);
-                        const float2 pv = make_float2(fast_exp2(yv.x), fast_exp2(yv.y));
-                        l4[k & 3] = fadd2(l4[k & 3], pv);
-                        pk[k] = pack_bf16x2(pv.x, pv.y);
-                    }
-                    tmem_st32(s_addr + 32 * h, pk);
+                for (int k = 0; k < 32; ++k) {
+                    const float2 yv = ffma2(make_float2(__uint_as_float(xs[2 * k]), __uint_as_float(xs[2 * k + 1])),
+                                            c2, nmu2);
+                    const float2 pv = make_float2(fast_exp2(yv.x), fast_exp2(yv.y));
+                    l4[k & 3] = fadd2(l4[k & 3], pv);
+                    pk[k] = pack_bf16x2(pv.x, pv.y);
                 }
+                tmem_st32(s_base + b * kPStep + 32 * h, pk);
                 l += ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) + ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y));
+                // P is in TMEM once tcgen05.wait::st returns; the leader's MMA reads it
+                // after seeing this arrival.  The leader's own warps arrive locally; the
+                // peer's with relaxed ordering (a release at cluster scope would wait
+                // for the SM's tensor work in flight: 1,000-2,700 cycles a step)
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(lead_p + 8 * b);
+                if (lane == 0) {
+                    if (rank == 0)
+                        mbar_arrive(bar(bPFull + b));
+                    else
+                        mbar_arrive_cluster_relaxed(lead_p + 8 * b);
+                }
             }
             if (!ok) break;
             // ---- epilogue: O / l -> bf16 rows of out (after the item's last P V)
@@ -601,59 +640,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                 break;
             }
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            if (p.lse != nullptr && valid)
-                p.lse[(int64_t)(it.q0 + i) * p.hq + it.kvh * p.g + pr % p.g] = row_lse(m_run, l);
-            const bool leader = r == 0;
+            // the row sum over both halves (the next write to these slots comes after
+            // a step barrier that the partner passes only after this read)
+            float *xl = red + 4 * kPreRows;
+            xl[h * kPreRows + r] = l;
+            named_barrier_sync(qbar, 64);
+            const float lt = l + xl[(1 - h) * kPreRows + r];
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            if (p.lse != nullptr && valid && h == 0)
+                p.lse[(int64_t)(it.q0 + i) * p.hq + it.kvh * p.g + pr % p.g] = row_lse(m_run, lt);
+            const bool leader = warp == 0 && lane == 0;
             // the previous item's stores have read the staging buffer
             if (leader) bulk_wait_read_all();
-            named_barrier_sync(1, 128);
-#pragma unroll 1
-            for (int h = 0; h < kD / 64; ++h) {
-                uint8_t *stg = stage_ptr + h * (kPreRows * 128);
+            named_barrier_sync(1, 256);
+            uint8_t *stg = stage_ptr + h * (kPreRows * 128);   // this half = one 64-column chunk
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(o_addr + 64 * h + 32 * c, v);
+            for (int c = 0; c < 2; ++c) {
+                uint32_t v[32];
+                tmem_ld32(o_addr + 32 * c, v);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        *reinterpret_cast<uint4 *>(stg + r * 128 + (((4 * c + k) ^ (r & 7)) << 4)) = make_uint4(
-                            pack_bf16x2(__uint_as_float(v[8 * k]) * inv, __uint_as_float(v[8 * k + 1]) * inv),
-                            pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv),
-                            pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv),
-                            pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv));
-                }
+                for (int k = 0; k < 4; ++k)
+                    *reinterpret_cast<uint4 *>(stg + r * 128 + (((4 * c + k) ^ (r & 7)) << 4)) = make_uint4(
+                        pack_bf16x2(__uint_as_float(v[8 * k]) * inv, __uint_as_float(v[8 * k + 1]) * inv),
+                        pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv),
+                        pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv),
+                        pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv));
             }
             fence_proxy_async_smem();
-            named_barrier_sync(1, 128);
+            named_barrier_sync(1, 256);
             if (it.my_nrows == kPreRows) {
                 if (leader) {
 #pragma unroll
-                    for (int h = 0; h < kD / 64; ++h)
-                        tma_store_3d(&tm_o, sstage + h * (kPreRows * 128), 64 * h, it.kvh * p.g,
+                    for (int c = 0; c < kD / 64; ++c)
+                        tma_store_3d(&tm_o, sstage + c * (kPreRows * 128), 64 * c, it.kvh * p.g,
                                      it.q0 + it.my_row0 / p.g);
                     bulk_commit_group();
                 }
             } else if (it.my_nrows > 0) {
                 // a tile that ends before 128 rows: the box would run into the next
-                // sequence's rows, so its rows are copied out by hand
-#pragma unroll 1
-                for (int h = 0; h < kD / 64; ++h)
-                    pair_copy_rows(p.out, stage_ptr + h * (kPreRows * 128), r, it.my_nrows, it.my_row0, it.q0,
-                                   it.kvh, p.g, p.hq, 64 * h);
-                named_barrier_sync(1, 128);     // the buffer is free for the next item
+                // sequence's rows, so its rows are copied out by hand (each half its chunk)
+                pair_copy_rows(p.out, stg, r, it.my_nrows, it.my_row0, it.q0, it.kvh, p.g, p.hq, 64 * h);
+                named_barrier_sync(1, 256);     // the buffer is free for the next item
             }
             // O is read: the next item's first P V (which overwrites O) waits for this
             // CTA's P of that item, which comes after these loads
         }
         // the output stores have completed before the CTA's shared memory goes away
-        if (r == 0) bulk_wait_all();
+        if (warp == 0 && lane == 0) bulk_wait_all();
     }
 
     // ---- teardown: both CTAs are done with TMEM and with each other's barriers
     tc_fence_before();
     cluster_sync_all();
-    if (warp == 4) {
+    if (warp == 8) {
         tc_fence_after();
         tmem_dealloc_pair(tmem, kPTmemCols);
     }
