@@ -320,17 +320,12 @@ static bool use_pair_prefill(int32_t head_size, int kv_fp8) {
     return kPairPrefill && head_size == 128 && !kv_fp8;
 }
 
-// The prefill scheduling of a call: items dealt to SM pairs (two-SM kernel),
-// or to SMs with the long ones claimed as the CTAs go (one-SM kernel at head
-// size 128 with a positive scale).
-static void configure_prefill(Problem &pr, int sms, bool scale_positive, int kv_fp8) {
-    if (use_pair_prefill(pr.d, kv_fp8)) {
-        pr.prefill_claim = false;
-        pr.pre_workers = std::max(1, sms / 2);
-    } else {
-        pr.prefill_claim = pr.d == 128 && scale_positive;
-        pr.pre_workers = 0;
-    }
+// The prefill scheduling options of a call: long items on SM pairs
+// (two-SM kernel, head size 128), or else claimed by the one-SM CTAs as they
+// go (head size 128 with a positive scale); the planner decides per batch.
+static void configure_prefill(Problem &pr, bool scale_positive, int kv_fp8) {
+    pr.prefill_pair = use_pair_prefill(pr.d, kv_fp8);
+    pr.prefill_claim = !pr.prefill_pair && pr.d == 128 && scale_positive;
 }
 
 // Workspace bytes of the block table expanded to 16-token pages (pages of
@@ -396,7 +391,7 @@ extern "C" ua_status ua_workspace_size(const int32_t *cu_seqlens_q_host,
     DeviceState *ds = nullptr;
     ua_status st = device_state(&ds);
     if (st != UA_OK) return st;
-    configure_prefill(pr, ds->sms, true, 0);
+    configure_prefill(pr, true, 0);
     thread_local Plan plan;
     build_plan(pr, ds->sms, kPrefillEnabled, plan);
     *bytes = plan.layout.total_bytes + expanded_table_bytes(num_seqs, block_table_stride, block_size);
@@ -435,7 +430,7 @@ extern "C" ua_status ua_plan_inspect(const int32_t *cu_seqlens_q_host,
     if (!counts || num_sms <= 0) return UA_ERR_INVALID_ARG;
     Problem pr = make_problem(cu_seqlens_q_host, seqused_k_host, num_seqs, num_q_heads,
                               num_kv_heads, head_size, block_size, block_table_stride, causal);
-    configure_prefill(pr, num_sms, true, 0);   // as a call with a positive softmax scale
+    configure_prefill(pr, true, 0);   // as a call with a positive softmax scale
     int v = validate_problem(pr);
     if (v) return static_cast<ua_status>(v);
     thread_local Plan plan;
@@ -611,10 +606,10 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
     // ---- partition pass
     thread_local Plan plan;
     thread_local std::vector<uint8_t> blob;
-    configure_prefill(pr, ds->sms, softmax_scale * k_scale > 0.f, kv_fp8);
-    const bool pair_prefill = use_pair_prefill(head_size, kv_fp8);
+    configure_prefill(pr, softmax_scale * k_scale > 0.f, kv_fp8);
     // an fp8 cache is read by the decode kernel only
     build_plan(pr, ds->sms, kPrefillEnabled && !kv_fp8, plan);
+    const bool pair_prefill = plan.pre_pair;
     const Layout &L = plan.layout;
     if (L.total_bytes > 0) {
         if (!workspace || workspace_bytes < L.total_bytes || !aligned(workspace, kAlign))
@@ -913,8 +908,10 @@ static ua_status device_plan_shape(int32_t num_seqs, int32_t max_total_q, int32_
     const bool can_prefill = (int64_t)s->max_seq_q * (hq / hkv) > kDecRows;
     s->prefill_ok = (kPrefillEnabled && !kv_fp8 && can_prefill && prefill_supports(pr)) ? 1 : 0;
     s->num_sms = sms;
-    s->pre_pair = use_pair_prefill(d, kv_fp8) ? 1 : 0;
-    s->pre_workers = s->pre_pair ? std::max(1, sms / 2) : sms;
+    // dealt to one SM per item: the kernel is fixed at capture, before the
+    // batch (and so its item lengths) is known
+    s->pre_pair = 0;
+    s->pre_workers = sms;
     return UA_OK;
 }
 

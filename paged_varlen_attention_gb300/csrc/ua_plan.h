@@ -53,10 +53,14 @@ constexpr size_t kAlign = 256;
 // unclaimed item, the prefill CTAs that have finished (the last one zeroes
 // both again, so a plan can be reused), the number of items.
 enum : int { kSchedNext = 0, kSchedDone = 1, kSchedItems = 2, kSchedInts = 4 };
-// Prefill items are claimed as the CTAs go when they see this many 128-key
-// tiles on average (2048 keys): per-SM speed differences then add up to more
-// than claiming costs (measured: -14% on 2048-token chunks over 4096-token
-// contexts, +3% on 1000-token prompts, which are dealt in advance instead).
+// Long prefill items: this many 128-key tiles on average (2048 keys) or more.
+// They run on SM pairs when the two-SM kernel may take them (measured on the
+// 2048-token chunks over 4096-token contexts: 486-497 us against 521 us for
+// one SM per item, claimed), otherwise they are claimed by the one-SM CTAs
+// as they go (-14% against dealing them).  Shorter items are dealt to one SM
+// each: on 1000-token prompts the one-SM kernel takes 151 us against 177-183
+// us on pairs (a pair spends an item's fixed costs on 128 rows per SM, one
+// SM on 256), and claiming them gained nothing.
 constexpr int kClaimMinMeanKvTiles = 16;
 
 struct alignas(16) DecPiece {   // one contiguous page range of one decode unit
@@ -105,8 +109,7 @@ struct Problem {
     bool causal;
     int32_t kv_heads_per_unit = 1;   // decode units: 1, or 2 (adjacent heads, <= 8 rows each)
     bool prefill_claim = false;      // long prefill items may be claimed as the CTAs go
-    int32_t pre_workers = 0;         // prefill items are dealt to this many workers (CTAs, or
-                                     // CTA pairs for the two-SM kernel); 0: one per SM
+    bool prefill_pair = false;       // long prefill items may run on SM pairs (two-SM kernel)
 };
 
 // Offsets of the plan sections inside the device workspace.

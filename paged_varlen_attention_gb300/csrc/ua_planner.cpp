@@ -60,6 +60,7 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
     plan.pre_begin.clear();
     plan.pre_ctas = 0;
     plan.pre_claimed = false;
+    plan.pre_pair = false;
     plan.layout = Layout{};
     const int g = p.hq / p.hkv;
     const bool pre_ok = prefill_enabled && prefill_supports(p);
@@ -131,12 +132,13 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
         }
     }
     // ---- prefill: longest first (counting sort, equal lengths keep batch order).
-    // Long items on average (kClaimMinMeanKvTiles, when the caller allows it)
-    // are claimed by the CTAs from this list as they go.  Otherwise they are
-    // dealt to the CTAs in rounds whose direction alternates (CTA 0..n-1,
-    // then n-1..0, ...): the CTA that got the longest item of a round gets the
-    // shortest of the next, which keeps the CTAs' totals within about one
-    // item of each other.  O(items) host cost.
+    // Long items on average (kClaimMinMeanKvTiles) go to SM pairs when the
+    // caller allows it, or else are claimed by the CTAs from this list as they
+    // go.  Otherwise (and on pairs) they are dealt to the workers in rounds
+    // whose direction alternates (0..n-1, then n-1..0, ...): the worker that
+    // got the longest item of a round gets the shortest of the next, which
+    // keeps the workers' totals within about one item of each other.
+    // O(items) host cost.
     if (!unsorted.empty()) {
         thread_local std::vector<PreTile> tl_sorted;
         thread_local std::vector<int32_t> tl_owner;
@@ -152,11 +154,12 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
         sorted.resize(unsorted.size());
         for (const PreTile &t : unsorted) sorted[(size_t)counts[(size_t)(max_kv - t.kv_tiles)]++] = t;
 
-        const int32_t workers = p.pre_workers > 0 ? p.pre_workers : std::max(num_sms, 1);
+        const bool long_items = kv_sum >= (int64_t)kClaimMinMeanKvTiles * (int64_t)sorted.size();
+        plan.pre_pair = p.prefill_pair && long_items;
+        const int32_t workers = plan.pre_pair ? std::max(num_sms / 2, 1) : std::max(num_sms, 1);
         const int32_t ctas = (int32_t)std::min<size_t>(sorted.size(), (size_t)workers);
         plan.pre_ctas = ctas;
-        plan.pre_claimed =
-            p.prefill_claim && kv_sum >= (int64_t)kClaimMinMeanKvTiles * (int64_t)sorted.size();
+        plan.pre_claimed = !plan.pre_pair && p.prefill_claim && long_items;
         if (plan.pre_claimed) {
             plan.tiles = sorted;
         } else {

@@ -16,9 +16,10 @@ struct Plan {
     std::vector<CombUnit> comb;
     int32_t n_slots = 0;
     std::vector<PreTile> tiles;         // grouped by prefill CTA (dealt), or longest first (claimed)
-    std::vector<int32_t> pre_begin;     // dealt: pre_ctas + 1, CTA c runs tiles [pre_begin[c], pre_begin[c+1])
-    int32_t pre_ctas = 0;
+    std::vector<int32_t> pre_begin;     // dealt: pre_ctas + 1, worker c runs tiles [pre_begin[c], pre_begin[c+1])
+    int32_t pre_ctas = 0;               // prefill workers: CTAs, or CTA pairs (pre_pair)
     bool pre_claimed = false;           // the prefill CTAs claim items from the list as they go
+    bool pre_pair = false;              // the items are dealt to SM pairs (two-SM kernel)
     Layout layout{};
 };
 

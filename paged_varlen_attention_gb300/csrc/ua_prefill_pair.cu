@@ -27,8 +27,7 @@
 // Roles (12 warps per CTA):
 //   warps 0-7  softmax of the CTA's 128 rows: warp w takes the rows of TMEM lane
 //              quarter w % 4 (one row per thread) and half w / 4 of each step's
-//              keys; the two warps of a quarter combine each row's max through
-//              shared memory.  Scale into the log2 domain, bottom-right causal
+//              keys (each reads the other half's scores too, for the row max).  Scale into the log2 domain, bottom-right causal
 //              mask, row max, exp2, row sum, P as bf16 over the first 64
 //              columns of the step's score buffer; every warp then arrives on
 //              the leader's P barrier (the peer's warps remotely).  O is
@@ -77,7 +76,7 @@ constexpr int kPStgBytes = kPreRows * kD * 2;    // epilogue staging (two 64-col
 constexpr uint32_t kColO = 3 * kPStep;           // O after the three score buffers
 constexpr int kPTmemCols = 512;
 constexpr float kPRescaleThreshold = 8.0f;       // log2 units
-constexpr int kPRedBytes = 3 * 2 * kPreRows * 4;  // row max (two step parities) and sum exchange
+constexpr int kPRedBytes = 2 * kPreRows * 4;      // row sums of the two halves at an item's end
 constexpr size_t kPSmemUsed = 1024 + 2 * (size_t)kPQBytes + kPStages * (size_t)(kPKBytes + kPVBytes) +
                               kPStgBytes + 512 + kPRedBytes;
 
@@ -223,7 +222,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     const uint32_t sstage = smem_u32(stage_ptr);
     uint64_t *bars = reinterpret_cast<uint64_t *>(stage_ptr + kPStgBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kPNumBars + 1);
-    float *red = reinterpret_cast<float *>(stage_ptr + kPStgBytes + 512);   // [3][2][128]
+    float *red = reinterpret_cast<float *>(stage_ptr + kPStgBytes + 512);   // [2][128]
     const uint32_t bar0 = smem_u32(bars);
     auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
 
@@ -519,8 +518,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         // ================================================================ softmax + epilogue
         // Warp w takes the rows of TMEM lane quarter q = w % 4 (one row per
         // thread) and half h = w / 4 of each step's 128 keys and of O's 128
-        // columns; the two warps of a quarter (one SMSP) combine each row's max
-        // every step, and its sum at the item's end, through shared memory.
+        // columns; each warp reads the other half's scores too, for the row max,
+        // and the two warps of a quarter (one SMSP) combine each row's sum at
+        // the item's end through shared memory.
         const int q = warp & 3, h = warp >> 2;
         const int r = q * 32 + lane;                    // row of the tile = TMEM lane
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
@@ -554,10 +554,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                     for (int k = 0; k < 64; ++k) xs[k] = __float_as_uint(__uint_as_float(xs[k]) * p.scale_log2);
                 }
                 constexpr uint32_t kNegInf = 0xff800000u;
-                if ((j + 1) * kPStep > it.my_kend_lo) {
-                    const int lim = kend - j * kPStep - 64 * h;     // visible keys of this half step
+                const bool masked = (j + 1) * kPStep > it.my_kend_lo;
+                const int lim = kend - j * kPStep;              // visible keys of this step
+                if (masked) {
 #pragma unroll
-                    for (int k = 0; k < 64; ++k) xs[k] = k < lim ? xs[k] : kNegInf;
+                    for (int k = 0; k < 64; ++k) xs[k] = (64 * h + k) < lim ? xs[k] : kNegInf;
                 }
                 float m8[8];
 #pragma unroll
@@ -565,13 +566,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
 #pragma unroll
                 for (int k = 8; k < 64; k += 2)
                     m8[(k >> 1) & 7] = fmax3(m8[(k >> 1) & 7], __uint_as_float(xs[k]), __uint_as_float(xs[k + 1]));
-                const float mh = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-                // the row's max over both halves (slots alternate by step, so a warp
-                // never overwrites a value its partner has not read yet)
-                float *xm = red + (y & 1) * (2 * kPreRows);
-                xm[h * kPreRows + r] = mh;
-                named_barrier_sync(qbar, 64);
-                float mx = fmaxf(mh, xm[(1 - h) * kPreRows + r]);
+                // the other half's scores, for the row max only (each warp computes the
+                // full max itself: no exchange with its partner, which would hold the
+                // two warps of an SMSP in step)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t ys[32];
+                    tmem_ld32(s_base + b * kPStep + 64 * (1 - h) + 32 * c, ys);
+                    if (!kPos) {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) ys[k] = __float_as_uint(__uint_as_float(ys[k]) * p.scale_log2);
+                    }
+                    if (masked) {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) ys[k] = (64 * (1 - h) + 32 * c + k) < lim ? ys[k] : kNegInf;
+                    }
+#pragma unroll
+                    for (int k = 0; k < 32; k += 4)
+                        m8[(k >> 2) & 7] = fmax3(m8[(k >> 2) & 7], fmax3(__uint_as_float(ys[k]), __uint_as_float(ys[k + 1]),
+                                                                         __uint_as_float(ys[k + 2])),
+                                                 __uint_as_float(ys[k + 3]));
+                }
+                float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
                 if (kPos) mx *= p.scale_log2;
                 if (j == 0) {
                     m_run = mx;
@@ -607,16 +623,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                 float2 l4[4];
 #pragma unroll
                 for (int a = 0; a < 4; ++a) l4[a] = make_float2(0.f, 0.f);
-                uint32_t pk[32];
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const float2 yv = ffma2(make_float2(__uint_as_float(xs[2 * k]), __uint_as_float(xs[2 * k + 1])),
-                                            c2, nmu2);
-                    const float2 pv = make_float2(fast_exp2(yv.x), fast_exp2(yv.y));
-                    l4[k & 3] = fadd2(l4[k & 3], pv);
-                    pk[k] = pack_bf16x2(pv.x, pv.y);
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const int e2 = 32 * c + 2 * k;
+                        const float2 yv = ffma2(make_float2(__uint_as_float(xs[e2]), __uint_as_float(xs[e2 + 1])), c2, nmu2);
+                        const float2 pv = make_float2(fast_exp2(yv.x), fast_exp2(yv.y));
+                        l4[k & 3] = fadd2(l4[k & 3], pv);
+                        pk[k] = pack_bf16x2(pv.x, pv.y);
+                    }
+                    tmem_st16(s_base + b * kPStep + 32 * h + 16 * c, pk);
                 }
-                tmem_st32(s_base + b * kPStep + 32 * h, pk);
                 l += ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) + ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y));
                 // P is in TMEM once tcgen05.wait::st returns; the leader's MMA reads it
                 // after seeing this arrival.  The leader's own warps arrive locally; the
@@ -640,9 +659,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                 break;
             }
             tc_fence_after();
-            // the row sum over both halves (the next write to these slots comes after
-            // a step barrier that the partner passes only after this read)
-            float *xl = red + 4 * kPreRows;
+            // the row sum over both halves (the barrier before the next item's write to
+            // these slots is the epilogue's first 256-thread barrier, which the partner
+            // reaches only after this read)
+            float *xl = red;
             xl[h * kPreRows + r] = l;
             named_barrier_sync(qbar, 64);
             const float lt = l + xl[(1 - h) * kPreRows + r];

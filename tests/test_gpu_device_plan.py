@@ -8,7 +8,9 @@ captured call serves every batch of the same sequence count.
 
 * The device plan equals the host plan (ua_plan_inspect) field for field on
   the standard batches and on edge cases (routing of few long prefill items
-  to the decode kernel, empty sequences, non-causal, G = 1).
+  to the decode kernel, empty sequences, non-causal, G = 1); where the host
+  deals long prefill items to SM pairs, the device deals the same items to
+  single SMs.
 * Attention through the device plan matches the fp64 oracle.
 * One CUDA graph, captured once, replayed on several batches whose metadata
   and queries are rewritten in place, matches the oracle each time.
@@ -80,8 +82,17 @@ def compare_plans(q_lens, k_lens, hq, hk, d, causal=True):
     assert h[7] == 0, "device planner reported an error"
     assert (int(h[0]), int(h[1]), int(h[2]), int(h[3])) == (
         counts["dec_ctas"], counts["pieces"], counts["split_units"], counts["slots"])
-    assert (int(h[4]), int(h[5])) == (counts["prefill_ctas"], counts["prefill_tiles"])
     pieces, slots, tiles, comb = _host_plan_rows(items)
+    # long items at head size 128: the host deals them to SM pairs (the two-SM
+    # kernel), the device to single SMs (its graph-captured launch is fixed
+    # before the batch's item lengths are known)
+    host_pairs = len(tiles) > 0 and d == 128 and tiles[:, 5].sum() >= 16 * len(tiles)
+    if host_pairs:
+        assert int(h[5]) == counts["prefill_tiles"]
+        assert int(h[4]) == min(counts["prefill_tiles"], sms)
+        assert counts["prefill_ctas"] == min(counts["prefill_tiles"], sms // 2)
+    else:
+        assert (int(h[4]), int(h[5])) == (counts["prefill_ctas"], counts["prefill_tiles"])
     if len(pieces):
         dev = dp["pieces"]
         cta = _cta_of(dp["cta_begin"], len(dev))
@@ -90,10 +101,10 @@ def compare_plans(q_lens, k_lens, hq, hk, d, causal=True):
     if len(tiles):
         dev = dp["tiles"]
         cta = _cta_of(dp["pre_begin"], len(dev))
-        if np.all(tiles[:, 0] == -1):
-            # the host lets the CTAs claim long items as they go; the device deals
-            # them (its graph-captured launch is fixed): the same items, and the
-            # device's deal is the host's longest-first list dealt in rounds
+        if host_pairs or np.all(tiles[:, 0] == -1):
+            # the host deals long items to SM pairs (or, built without the two-SM
+            # kernel, lets the CTAs claim them as they go); the device deals them
+            # to single SMs: the same items, dealt by the device in rounds
             host = tiles[:, 1:]
             as_rows = lambda a: np.sort(np.ascontiguousarray(a, dtype=np.int32).view("i4,i4,i4,i4,i4"),  # noqa: E731
                                         axis=0)

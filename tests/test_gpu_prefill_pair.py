@@ -1,13 +1,15 @@
 """GPU: the two-SM prefill kernel (head size 128) against the fp64 oracle.
 
-A work item of 256 packed rows runs on a pair of SMs, 128 rows each, with
-128-key steps.  These cases reach its edges: items whose second tile holds no
-valid rows (the peer SM still computes, nothing is stored) or part of one
-(rows copied out by hand), query-head groups from 1 to 128, keys ending
-inside a step and inside a page (the V rows past the context zeroed), a
-negative scale (the scale is applied before the max), non-causal rows with
-more queries than keys, the per-row log-sum-exp, and more than two items per
-pair.  Tolerance as in the other parity tests.
+Long prefill items (16 tiles of 128 keys or more on average) run on pairs of
+SMs: a work item of 256 packed rows, 128 on each SM, with 128-key steps.
+These cases reach its edges: items whose second tile holds no valid rows (the
+peer SM still computes, nothing is stored) or part of one (rows copied out by
+hand), query-head groups from 1 to 128, keys ending inside a step and inside a
+page (the V rows past the context zeroed), a negative scale (the scale is
+applied before the max), non-causal rows with more queries than keys beside
+long ones, the per-row log-sum-exp, and more than two items per pair.  Each
+case first checks, on the host, that its plan deals the items to SM pairs.
+Tolerance as in the other parity tests.
 """
 import zlib
 
@@ -48,15 +50,17 @@ def prefill_items(spec):
     return counts, [r for r in items if r[0] == 2], sms
 
 
+# Every case has 40 items or more: with fewer, long items go to the split-KV
+# decode kernel instead (a few items would leave most SMs idle).
 CASES = [
     # q_lens, k_lens, Hq, Hkv, causal, scale
-    ([40], [40], 8, 2, True, None),              # 160 rows: second tile 32 rows
-    ([16], [300], 8, 1, True, None),             # G = 8, 128 rows: second tile empty
-    ([33, 200, 1], [500, 257, 90], 32, 8, True, None),   # G = 4, keys end inside steps / pages
-    ([1000], [1000], 4, 4, True, None),          # G = 1: four items, the last partial
-    ([300], [300], 128, 1, True, None),          # G = 128: one token per tile row group
-    ([64, 20], [30, 500], 8, 2, False, None),    # non-causal, Lq > Lk in the first
-    ([129, 255], [129, 700], 8, 2, True, -0.07), # negative scale
+    ([40] * 20, [2100] * 20, 8, 2, True, None),             # 160 rows: second tile 32 rows
+    ([16] * 40, [2300] * 40, 8, 1, True, None),             # G = 8, 128 rows: second tile empty
+    ([33, 200, 1] * 8, [2500, 2257, 90] * 8, 32, 8, True, None),   # G = 4, keys end inside steps / pages
+    ([1000] * 10, [3000] * 10, 4, 4, True, None),           # G = 1: four items each, the last partial
+    ([300], [2300], 128, 1, True, None),                    # G = 128: 150 items
+    ([64, 20] * 10, [30, 5000] * 10, 8, 2, False, None),    # non-causal, Lq > Lk beside long rows
+    ([129, 255] * 6, [2129, 2700] * 6, 8, 2, True, -0.07),  # negative scale
     ([256] * 40, [2048 + 256 + 16 * i for i in range(40)], 8, 8, True, None),   # 320 items
 ]
 
@@ -68,7 +72,8 @@ def test_pair_kernel_matches_oracle(case):
                          seed=zlib.crc32(str(case).encode()) % 1000)
     counts, items, sms = prefill_items(spec)
     assert items, "the case must have prefill work items"
-    assert counts["prefill_ctas"] <= sms // 2       # dealt to SM pairs
+    assert sum(r[6] for r in items) >= 16 * len(items)      # long items on average
+    assert counts["prefill_ctas"] <= sms // 2               # dealt to SM pairs
     b = W.materialize(spec, poison=True)
     got = run_gpu(b)
     ref, _ = oracle.attention_batch(b)
@@ -79,7 +84,7 @@ def test_pair_kernel_lse_and_repeatability():
     import torch
     import paged_varlen_attention_gb300 as ua
 
-    spec = W.custom_spec([200, 1, 77], [1200, 3000, 77], 32, 8, 128, seed=71)
+    spec = W.custom_spec([200, 1, 77], [2400, 3000, 2477], 32, 8, 128, seed=71)
     b = W.materialize(spec, poison=True)
     dev = to_device(b)
     lse = torch.full((dev["q"].shape[0], spec.num_q_heads), float("nan"), dtype=torch.float32,

@@ -99,14 +99,15 @@ def check_plan(q_lens, k_lens, hq, hk, d=128, causal=True, num_sms=152):
             per_cta[pc[1]] += pc[7] - pc[6]
         assert per_cta.max() - per_cta.min() <= 1
         assert counts["dec_ctas"] <= 2 * num_sms
-    # prefill items: the workers' ranges (one per SM, or one per pair of SMs
-    # for the two-SM kernel at head size 128) cover the tile list in order,
-    # each worker's items come longest first, and dealing the longest-first
-    # list in rounds of alternating direction keeps the workers' work within
-    # one item of each other
+    # prefill items: the workers' ranges cover the tile list in order, each
+    # worker's items come longest first, and dealing the longest-first list in
+    # rounds of alternating direction keeps the workers' work within one item
+    # of each other.  Workers are SMs, or pairs of SMs (the two-SM kernel) for
+    # long items (16 tiles of 128 keys or more on average) at head size 128
     ctas = [t[1] for t in tiles]
     assert [t[7] for t in tiles] == list(range(len(tiles)))
-    workers = max(1, num_sms // 2) if d == 128 else num_sms
+    long_items = bool(tiles) and sum(t[6] for t in tiles) >= 16 * len(tiles)
+    workers = max(1, num_sms // 2) if (d == 128 and long_items) else num_sms
     if tiles:
         assert ctas == sorted(ctas) and min(ctas) >= 0
         assert counts["prefill_ctas"] == len(set(ctas)) == min(len(tiles), workers)
@@ -137,18 +138,21 @@ def test_long_mixed_batch():
     assert c["dec_ctas"] == 2 * 152
 
 
-def test_prefill_items_go_to_sm_pairs_at_head_size_128():
-    """Head size 128: the prefill items are dealt to the 76 SM pairs of a
-    152-SM GPU (the two-SM kernel), long or short; head size 64: to the 152 SMs."""
+def test_long_prefill_items_go_to_sm_pairs_at_head_size_128():
+    """Head size 128: long items (2048-token chunks over 4096-token contexts) are
+    dealt to the 76 SM pairs of a 152-SM GPU (the two-SM kernel), short ones
+    (1000-token prompts) to the 152 SMs; head size 64: always to SMs."""
     def prefill_ctas(q, k, hq, hk, d):
         cu = np.concatenate([[0], np.cumsum(q)]).astype(np.int32)
         counts, items = B.plan_inspect(cu, np.asarray(k, np.int32), hq, hk, d,
                                        int(-(-max(k) // 16)), True)
         return counts, [r[1] for r in items if r[0] == 2]
-    for idx in (3, 5):
-        s = W.config_spec(idx)
-        counts, ctas = prefill_ctas(s.q_lens, s.k_lens, s.num_q_heads, s.num_kv_heads, 128)
-        assert min(ctas) == 0 and max(ctas) == 75 and counts["prefill_ctas"] == 76
+    s = W.config_spec(5)
+    counts, ctas = prefill_ctas(s.q_lens, s.k_lens, s.num_q_heads, s.num_kv_heads, 128)
+    assert min(ctas) == 0 and max(ctas) == 75 and counts["prefill_ctas"] == 76
+    s = W.config_spec(3)
+    counts, ctas = prefill_ctas(s.q_lens, s.k_lens, s.num_q_heads, s.num_kv_heads, 128)
+    assert min(ctas) == 0 and max(ctas) == 151 and counts["prefill_ctas"] == 152
     counts, ctas = prefill_ctas([2048], [6144], 16, 8, 64)
     assert min(ctas) == 0 and counts["prefill_ctas"] == len(set(ctas)) == 128   # 128 items
 
