@@ -210,6 +210,19 @@ ua_status ua_profile_enable(int32_t enable);
 ua_status ua_profile_read(int32_t calls_back, float *ms, int32_t *launches);
 
 /*
+ * ua_test_set_wait_limit -- test hook for the failure path of the device
+ * waits: the decode / split-KV kernel of the calls made after it (any
+ * thread) gives each wait of its main loop at most limit_ns nanoseconds
+ * instead of the library's 4 s (0 restores that).  A wait that runs out sets
+ * UA_DEVICE_WAIT_TIMEOUT in the device status word and the kernel winds
+ * down: the warps that share barriers stop together, the loads it has issued
+ * are waited for (with the 4 s limit) and it returns, leaving its output
+ * incomplete.  Nothing else faults or stops; the next call with the normal
+ * limit is correct.  Not for production use.
+ */
+ua_status ua_test_set_wait_limit(uint64_t limit_ns);
+
+/*
  * unified_attention_lse -- unified_attention that also writes, for every
  * query row, the natural-log normaliser of its softmax,
  *     lse[t][h] = ln( sum over visible keys j of e^(softmax_scale * <q_t,h, k_j>) ),

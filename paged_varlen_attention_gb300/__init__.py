@@ -13,7 +13,7 @@ generator) can be used on machines without the built library.
 _EXPORTS = ("UAError", "device_status", "library_path", "load_library", "plan_inspect",
             "unified_attention", "unified_attention_fp8kv", "merge_attn_states", "kv_append",
             "workspace_size",
-            "profile_enable",
+            "profile_enable", "set_test_wait_limit",
             "profile_read", "unified_attention_device_plan", "workspace_size_device_plan",
             "device_plan")
 

@@ -29,7 +29,7 @@ SYMBOLS = ("unified_attention", "unified_attention_lse", "ua_merge_attn_states",
            "ua_workspace_size", "ua_status_string", "ua_device_status", "ua_plan_inspect",
            "ua_profile_enable", "ua_profile_read", "unified_attention_device_plan",
            "ua_workspace_size_device_plan", "ua_device_plan_build", "ua_device_plan_layout",
-           "unified_attention_device_planned")
+           "unified_attention_device_planned", "ua_test_set_wait_limit")
 
 
 class UAError(RuntimeError):
@@ -89,6 +89,8 @@ def load_library():
         lib.ua_plan_inspect.argtypes = [P, P, I32, I32, I32, I32, I32, I32, I32, I32, P, P, I64,
                                         ctypes.POINTER(I64)]
         lib.ua_plan_inspect.restype = ctypes.c_int
+        lib.ua_test_set_wait_limit.argtypes = [ctypes.c_uint64]
+        lib.ua_test_set_wait_limit.restype = ctypes.c_int
         lib.ua_profile_enable.argtypes = [I32]
         lib.ua_profile_enable.restype = ctypes.c_int
         lib.ua_profile_read.argtypes = [I32, P, P]
@@ -296,6 +298,12 @@ def plan_inspect(cu_seqlens_q_host, seqused_k_host, num_q_heads, num_kv_heads, h
     keys = ("dec_ctas", "pieces", "split_units", "slots", "prefill_tiles", "prefill_ctas",
             "dec_pages", "workspace_bytes")
     return dict(zip(keys, (int(c) for c in counts))), items[:int(n.value)]
+
+
+def set_test_wait_limit(limit_ns: int = 0):
+    """Test hook (``ua_test_set_wait_limit``): the decode kernel's main-loop waits of
+    later calls give up after limit_ns nanoseconds (0: the library's 4 s)."""
+    _check(load_library().ua_test_set_wait_limit(int(limit_ns)), "ua_test_set_wait_limit")
 
 
 def profile_enable(on: bool = True):

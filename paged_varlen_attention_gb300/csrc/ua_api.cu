@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -54,6 +55,14 @@ struct DeviceState {
 static std::mutex g_mutex;
 static DeviceState g_devices[kMaxDevices];
 static bool g_profile = false;
+// Limit of the decode kernel's main-loop waits for calls made from now on
+// (ua_test_set_wait_limit; 0: the library's limit, kWaitLimitNs).
+static std::atomic<unsigned long long> g_wait_limit_ns{0};
+
+static unsigned long long wait_limit_ns() {
+    const unsigned long long v = g_wait_limit_ns.load(std::memory_order_relaxed);
+    return v ? v : kWaitLimitNs;
+}
 
 // The plan of a host-planned call goes to the GPU through two rings per
 // device, both owned by the library and grown on demand (an allocation only
@@ -497,6 +506,11 @@ extern "C" ua_status ua_device_status(int32_t *code) {
     return UA_OK;
 }
 
+extern "C" ua_status ua_test_set_wait_limit(uint64_t limit_ns) {
+    g_wait_limit_ns.store(limit_ns, std::memory_order_relaxed);
+    return UA_OK;
+}
+
 extern "C" ua_status ua_profile_enable(int32_t enable) {
     std::lock_guard<std::mutex> lock(g_mutex);
     g_profile = enable != 0;
@@ -709,6 +723,7 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
         dp.v_scale = v_scale;
         dp.heads_per_unit = plan.dec_heads_per_unit;
         dp.status = ds->status;
+        dp.wait_ns = wait_limit_ns();
         e = launch_decode(head_size, kv_fp8 != 0, dp, tm_kp, tm_vp, plan.dec_ctas, stream);
         if (e != cudaSuccess) return UA_ERR_CUDA;
     }
@@ -1032,6 +1047,7 @@ static ua_status run_attention_device_plan(
     dp.v_scale = v_scale;
     dp.heads_per_unit = shape.hpu;
     dp.status = ds->status;
+    dp.wait_ns = wait_limit_ns();
     if (launch_decode(head_size, kv_fp8 != 0, dp, tm_kp, tm_vp, L.dec_grid, stream) != cudaSuccess)
         return UA_ERR_CUDA;
     mark(2);

@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, DecCfg<D, KV8>::kMin
             int good = 1;
             if (lane == 0) {
                 const uint32_t slot = filled % C::kRing, ph = (filled / C::kRing) & 1;
-                if (!mbar_wait(pempty0 + 8 * slot, ph ^ 1, p.status)) {
+                if (!mbar_wait(pempty0 + 8 * slot, ph ^ 1, p.status, p.wait_ns)) {
                     good = 0;
                 } else {
                     int *d = dring + slot * C::kDescInts;
@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, DecCfg<D, KV8>::kMin
                     if (lane == 0) {
                         const uint32_t st = issued % C::kStages;
                         const uint32_t ph = (issued / C::kStages) & 1;
-                        if (!mbar_wait(empty0 + 8 * st, ph ^ 1, p.status)) {
+                        if (!mbar_wait(empty0 + 8 * st, ph ^ 1, p.status, p.wait_ns)) {
                             good = 0;
                         } else {
                             const uint32_t fb = full0 + 8 * st;
@@ -347,14 +347,17 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, DecCfg<D, KV8>::kMin
         bool ok = true;
         const int hp = KV8 ? p.heads_per_unit : 1;   // kv heads per unit
         // Every consumer warp walks every piece (the merges use a named barrier),
-        // even after a failed wait: a piece it could not get counts as empty.
+        // even after a failed wait: a piece it could not get counts as empty.  The
+        // four warps decide together whether they have the piece (a barrier that
+        // ANDs their results), so that they agree on the merge steps below.
         for (int pi = pbeg; pi < pend; ++pi) {
             // the piece's descriptor and Q rows, prepared by the producer
             const uint32_t ring = (uint32_t)(pi - pbeg);
             const uint32_t slot = ring % C::kRing;
             if (ok && !__all_sync(0xffffffffu,
-                                  mbar_wait(pfull0 + 8 * slot, (ring / C::kRing) & 1, p.status)))
+                                  mbar_wait(pfull0 + 8 * slot, (ring / C::kRing) & 1, p.status, p.wait_ns)))
                 ok = false;
+            ok = named_barrier_and(1, C::kConsumerWarps * 32, ok);
             const int *d = dring + slot * C::kDescInts;
             struct {
                 int kvh, row0, nrows, page_begin, page_end, slot, comb, slot0, nslots;
@@ -413,7 +416,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, DecCfg<D, KV8>::kMin
                 const uint32_t gidx = gbase + k;
                 const uint32_t st = gidx % C::kStages;
                 const uint32_t ph = (gidx / C::kStages) & 1;
-                if (!mbar_wait(full0 + 8 * st, ph, p.status)) {
+                if (!mbar_wait(full0 + 8 * st, ph, p.status, p.wait_ns)) {
                     ok = false;
                     break;
                 }

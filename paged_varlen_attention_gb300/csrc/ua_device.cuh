@@ -15,8 +15,6 @@
 
 namespace ua {
 
-constexpr unsigned long long kWaitLimitNs = 4000000000ull;   // 4 s; real waits are microseconds
-
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -76,7 +74,10 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait until the phase with the given parity has completed.  Bounded.
+// Wait until the phase with the given parity has completed.  Bounded: gives
+// up after kWaitLimitNs.  try_wait itself suspends the thread for a while
+// (until the phase completes or a hardware time runs out), so the timer is
+// read only every 32 attempts.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *status) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
@@ -89,6 +90,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *st
             return false;
         }
     }
+}
+
+// The same with a caller-given limit.  Below the library's limit (a test of
+// the failure path) it polls with the non-blocking test_wait, so that the
+// limit, not try_wait's suspension, decides when it gives up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *status,
+                                          unsigned long long limit_ns) {
+    if (limit_ns >= kWaitLimitNs) return mbar_wait(bar, parity, status);
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_test(bar, parity)) {
+        if (globaltimer_ns() - t0 > limit_ns) {
+            record_status(status, UA_DEVICE_WAIT_TIMEOUT_BIT);
+            return false;
+        }
+    }
+    return true;
 }
 
 // ---------------------------------------------------------------- TMA
@@ -322,6 +339,23 @@ __device__ __forceinline__ float row_lse(float m, float l) {
 
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// A named barrier that also returns the AND of `pred` over the nthreads
+// threads.  Warps that share named barriers decide to give up (after a wait
+// ran out) through it, together: a warp that left early would leave the others
+// waiting at a barrier it never reaches.
+__device__ __forceinline__ bool named_barrier_and(int id, int nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
 }
 
 // ---------------------------------------------------------------- tcgen05 (UMMA + TMEM)

@@ -34,6 +34,7 @@ struct DecodeParams {
     float v_scale;               // scale of the V values (fp8 cache; 1 otherwise)
     int32_t heads_per_unit;      // e4m3 pages: kv heads per unit (tile rows 8j.. are head kvh + j)
     int *status;                 // device status word
+    unsigned long long wait_ns;  // limit of the main loop's waits (the drains keep kWaitLimitNs)
 };
 
 struct PrefillParams {

@@ -40,6 +40,10 @@
 
 namespace ua {
 
+// Every wait of the kernels gives up after this long (real waits are
+// microseconds), records UA_DEVICE_WAIT_TIMEOUT and winds the kernel down.
+constexpr unsigned long long kWaitLimitNs = 4000000000ull;   // 4 s
+
 constexpr int kBlockSize = 16;      // tokens per KV page as the kernels see it
 constexpr int kMaxBlockSize = 256;  // caller pages: multiples of kBlockSize up to this (viewed as
                                     // runs of 16-token pages)

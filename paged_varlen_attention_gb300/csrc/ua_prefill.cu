@@ -664,7 +664,13 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
         for (uint32_t k = 0; ok; ++k) {
             PreTile cur;
             const int got = items.take(p, k, true, lane, cur);
-            if (got < 0) ok = false;
+            if constexpr (kClaimed) {
+                // the tile's four warps wait for the item each; they give up together
+                if (!named_barrier_and(1 + x, 128, got >= 0)) {
+                    ok = false;
+                    break;
+                }
+            }
             if (got <= 0) break;
             const PairInfo pi = make_pair(p, cur);
             const SubInfo si = x ? pi.sub[1] : pi.sub[0];
@@ -760,14 +766,17 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
                 tc_fence_before();
                 mbar_arrive(bar(kBarPFull + 2 * x + b));
             }
-            if (!ok) break;
-            // ---- epilogue: O / l -> bf16 rows of out (after the last P V of this tile)
-            const uint32_t lb = (ex - 1) & 1;
-            if (!__all_sync(0xffffffffu,
-                            mbar_wait(bar(kBarPvDone + 2 * x + lb), ((ex - 1) >> 1) & 1, p.status))) {
-                ok = false;
-                break;
+            // ---- epilogue: O / l -> bf16 rows of out (after the last P V of this tile).
+            // The tile's four warps decide together whether they go on: a warp
+            // whose wait ran out must not leave the others at the barriers below.
+            bool eok = ok;
+            if (eok) {
+                const uint32_t lb = (ex - 1) & 1;
+                eok = __all_sync(0xffffffffu,
+                                 mbar_wait(bar(kBarPvDone + 2 * x + lb), ((ex - 1) >> 1) & 1, p.status));
             }
+            ok = named_barrier_and(1 + x, 128, eok);
+            if (!ok) break;
             tc_fence_after();
             // O / l as bf16, 64 columns per pass, into the tile's staging buffer in
             // the layout of a Q tile (row r at r * 128 bytes, 16-byte pieces XOR-ed

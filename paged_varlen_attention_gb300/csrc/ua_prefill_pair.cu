@@ -651,13 +651,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                         mbar_arrive_cluster_relaxed(lead_p + 8 * b);
                 }
             }
-            if (!ok) break;
-            // ---- epilogue: O / l -> bf16 rows of out (after the item's last P V)
-            const uint32_t lb = (y - 1) % kPStages, lph = ((y - 1) / kPStages) & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(bPvDone + lb), lph, p.status))) {
-                ok = false;
-                break;
+            // ---- epilogue: O / l -> bf16 rows of out (after the item's last P V).
+            // The eight softmax warps decide together whether they go on: a warp
+            // whose wait ran out must not leave the others at the barriers below.
+            bool eok = ok;
+            if (eok) {
+                const uint32_t lb = (y - 1) % kPStages, lph = ((y - 1) / kPStages) & 1;
+                eok = __all_sync(0xffffffffu, mbar_wait(bar(bPvDone + lb), lph, p.status));
             }
+            ok = named_barrier_and(1, 256, eok);
+            if (!ok) break;
             tc_fence_after();
             // the row sum over both halves (the barrier before the next item's write to
             // these slots is the epilogue's first 256-thread barrier, which the partner
