@@ -40,7 +40,8 @@ same attention as one direct call); kv_append_mistral_24b_16x1000 (writing
 headline batch over an E4M3 cache); llama3_8b_decode_64x2k-4k_graph (the
 headline batch planned on the GPU, one CUDA-graph replay per step);
 gemma2_9b_decode_64x2k-4k (the headline lengths with head size 256: Hq 16,
-Hkv 8).
+Hkv 8); phi3_mini_decode_64x2k-4k (the same lengths with head size 96:
+Hq = Hkv = 32).
 --block-size runs a standard batch over pages of 32 ... 256 tokens (same
 lengths and data recipe; the call then also expands the block table).
 
@@ -78,6 +79,7 @@ WORKLOADS = {
     "llama3_8b_mixed_256dec_4x512chunk": 4,
     "llama3_70b_long_mixed_32x8k-32k_2x2048chunk": 5,
     "gemma2_9b_decode_64x2k-4k": 6,
+    "phi3_mini_decode_64x2k-4k": 7,
 }
 DEFAULT_WORKLOAD = "llama3_70b_long_mixed_32x8k-32k_2x2048chunk"
 # the other standard batches the default run also measures (one line, per_config)
@@ -866,7 +868,7 @@ def run_kv_append(args):
     with ClockSampler(gpu_id_for_smi(torch, 0)) as clocks:
         torch.cuda.synchronize()
         if spin is not None:
-            spin(200_000 * args.steps)          # ~100 us of cycles per queued step
+            spin(1_000_000 * args.steps)        # ~500 us of cycles per queued step
         for a, e in evs:
             flush()
             a.record(stream)

@@ -307,6 +307,37 @@ static bool encode_page_map(CUtensorMap *map, const void *base, int d, int hkv,
     return r == CUDA_SUCCESS;
 }
 
+// 4-D bf16 map over the paged cache of a head narrower than 128 columns (80,
+// 96, 112): (d, 16 slots, Hkv, blocks), boxes of {64, 16, 1, 1} with the
+// 128-byte swizzle.  The box at column 64 runs past d, and TMA fills those
+// columns with zeros without reading them: the page lands in the layout of
+// a 128-column page, [chunk][slot][64], with zeros past d.
+static bool encode_page_map_narrow(CUtensorMap *map, const void *base, int d, int hkv,
+                                   uint64_t num_blocks) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const uint64_t row = (uint64_t)hkv * d * 2;   // bytes between slots
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)kBlockSize, (cuuint64_t)hkv, num_blocks};
+    cuuint64_t strides[3] = {row, (cuuint64_t)d * 2, row * kBlockSize};
+    cuuint32_t box[4] = {64, (cuuint32_t)kBlockSize, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     l2_fill((uint64_t)d * 2), CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// The decode kernel's K / V maps of a call: the 5-D page view (whole pages of
+// D = 64, 128, 256 or of an e4m3 cache), or the narrow view above.
+static bool encode_decode_maps(CUtensorMap *tk, CUtensorMap *tv, const void *k, const void *v, int d,
+                               int hkv, uint64_t num_blocks, int eb, int box_heads) {
+    if (kernel_head_size(d) != d)
+        return encode_page_map_narrow(tk, k, d, hkv, num_blocks) &&
+               encode_page_map_narrow(tv, v, d, hkv, num_blocks);
+    return encode_page_map(tk, k, d, hkv, num_blocks, eb, box_heads) &&
+           encode_page_map(tv, v, d, hkv, num_blocks, eb, box_heads);
+}
+
 static bool aligned(const void *p, size_t a) {
     return (reinterpret_cast<uintptr_t>(p) % a) == 0;
 }
@@ -636,10 +667,8 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
     CUtensorMap tm_kp, tm_vp, tm_q, tm_o, tm_k3, tm_vh;
     const int eb = kv_fp8 ? 1 : 2;
     const int box_heads = plan.dec_heads_per_unit;   // 2 only for e4m3 pages (no prefill tiles)
-    if (!encode_page_map(&tm_kp, k_cache, head_size, num_kv_heads, (uint64_t)num_blocks, eb,
-                         box_heads) ||
-        !encode_page_map(&tm_vp, v_cache, head_size, num_kv_heads, (uint64_t)num_blocks, eb,
-                         box_heads))
+    if (!encode_decode_maps(&tm_kp, &tm_vp, k_cache, v_cache, head_size, num_kv_heads,
+                            (uint64_t)num_blocks, eb, box_heads))
         return UA_ERR_CUDA;
     // prefill: Q tiles (loads) and out tiles (stores) as [total_q, Hq, D], and K as
     // [num_blocks * 16, Hkv, D] with one box per 64 columns
@@ -724,6 +753,7 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
         dp.heads_per_unit = plan.dec_heads_per_unit;
         dp.status = ds->status;
         dp.wait_ns = wait_limit_ns();
+        dp.dq = head_size;
         e = launch_decode(head_size, kv_fp8 != 0, dp, tm_kp, tm_vp, plan.dec_ctas, stream);
         if (e != cudaSuccess) return UA_ERR_CUDA;
     }
@@ -904,7 +934,7 @@ static ua_status device_plan_shape(int32_t num_seqs, int32_t max_total_q, int32_
                                    int32_t bt_stride, int32_t kv_fp8, int sms, DevPlanShape *s) {
     if (num_seqs < 0 || max_total_q < 0 || max_seq_q < 0 || hq <= 0 || hkv <= 0 || bt_stride < 0)
         return UA_ERR_INVALID_ARG;
-    if (hq % hkv != 0 || (d != 64 && d != 128 && d != 256)) return UA_ERR_UNSUPPORTED;
+    if (hq % hkv != 0 || !head_size_supported(d)) return UA_ERR_UNSUPPORTED;
     if (bs <= 0 || bs % kBlockSize != 0 || bs > kMaxBlockSize) return UA_ERR_UNSUPPORTED;
     if (kv_fp8 && d != 128) return UA_ERR_UNSUPPORTED;
     if ((int64_t)bt_stride * (bs / kBlockSize) > INT32_MAX / 4) return UA_ERR_INVALID_ARG;
@@ -989,8 +1019,8 @@ static ua_status run_attention_device_plan(
     const int g = num_q_heads / num_kv_heads;
     CUtensorMap tm_kp, tm_vp, tm_q, tm_o, tm_k3, tm_vh;
     const int eb = kv_fp8 ? 1 : 2;
-    if (!encode_page_map(&tm_kp, k_cache, head_size, num_kv_heads, (uint64_t)num_blocks, eb, shape.hpu) ||
-        !encode_page_map(&tm_vp, v_cache, head_size, num_kv_heads, (uint64_t)num_blocks, eb, shape.hpu))
+    if (!encode_decode_maps(&tm_kp, &tm_vp, k_cache, v_cache, head_size, num_kv_heads,
+                            (uint64_t)num_blocks, eb, shape.hpu))
         return UA_ERR_CUDA;
     if (shape.prefill_ok && shape.pre_pair &&
         !encode_page_map(&tm_vh, v_cache, head_size, num_kv_heads, (uint64_t)num_blocks, 2, 1, 1))
@@ -1048,6 +1078,7 @@ static ua_status run_attention_device_plan(
     dp.heads_per_unit = shape.hpu;
     dp.status = ds->status;
     dp.wait_ns = wait_limit_ns();
+    dp.dq = head_size;
     if (launch_decode(head_size, kv_fp8 != 0, dp, tm_kp, tm_vp, L.dec_grid, stream) != cudaSuccess)
         return UA_ERR_CUDA;
     mark(2);

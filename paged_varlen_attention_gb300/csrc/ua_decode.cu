@@ -49,7 +49,13 @@ namespace ua {
 // D = 256: a thread holds 64 registers of Q fragments and 128 of the O
 // accumulator, so the kernel runs one CTA per SM (up to 255 registers a
 // thread) with a deeper ring of 16 KB stages; every row of such a batch
-// comes here (the tensor-core prefill kernel is laid out for D <= 128).
+// comes here (the tensor-core prefill kernels are built for D 64 and 128).
+//
+// Head sizes 80, 96 and 112 run in the D = 128 kernel (p.dq < D): the K / V
+// pages arrive through a 4-D view of the cache whose rows end at dq, two
+// 64-column boxes per page, and TMA fills the columns past dq with zeros
+// (they are not read from memory); Q's tile rows are zero past dq; the output
+// keeps the first dq columns.  Every row of such a batch comes here too.
 template <int D, bool KV8>
 struct DecCfg {
     static_assert(!KV8 || D == 128, "the e4m3 path is laid out for D = 128");
@@ -155,7 +161,7 @@ __device__ __forceinline__ int tile_row_idx(int r, int hp) { return hp == 2 ? r 
 // O_s = sum_j 2^(x_j - m_s) v_j, its max m_s and l_s = sum_j 2^(x_j - m_s):
 //   M = max_s m_s,  out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
 // The partials of other CTAs are read through L2 (ld.global.cg).
-template <int D>
+template <int D, bool kNarrow>
 __device__ __forceinline__ void merge_unit(const DecodeParams &p, int q0, int kvh, int row0, int nrows,
                                            int hp, int slot0, int nslots, int tid, int nthreads) {
     const int tile_rows = hp == 2 ? kDecRows : nrows;
@@ -186,14 +192,17 @@ __device__ __forceinline__ void merge_unit(const DecodeParams &p, int q0, int kv
         const int64_t t = (int64_t)q0 + pr / p.g;
         const int h = (kvh + tile_row_head(row, hp)) * p.g + pr % p.g;
         if (p.lse != nullptr && col == 0) p.lse[t * p.hq + h] = row_lse(M, W);
+        const int dq = kNarrow ? p.dq : D;
+        if (kNarrow && col >= dq) continue;          // zero padding of a narrower head
         uint2 packed;
         packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
         packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2 *>(p.out + (t * p.hq + h) * D + col) = packed;
+        *reinterpret_cast<uint2 *>(p.out + (t * p.hq + h) * dq + col) = packed;
     }
 }
 
-template <int D, bool KV8>
+// kNarrow: a head narrower than D (p.dq < D, see above).
+template <int D, bool KV8, bool kNarrow>
 __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, DecCfg<D, KV8>::kMinCtasPerSm)
     ua_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v) {
@@ -226,6 +235,17 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, DecCfg<D, KV8>::kMin
             mbar_init(pempty0 + 8 * i, 1);
         }
         fence_barrier_init();
+    }
+    // A head narrower than D (80, 96, 112 in the D = 128 kernel): the Q tiles'
+    // columns dq .. D - 1 are zero for good (the copies below fill only the
+    // first dq), and so are those of K and V (the tensor map ends at dq).
+    if constexpr (kNarrow) {
+        const int pad = D - p.dq;
+        for (int u = threadIdx.x; u < C::kRing * kDecRows * pad; u += C::kThreads) {
+            const int row = u / pad, c = p.dq + u % pad;
+            reinterpret_cast<__nv_bfloat16 *>(qring)[row * D + c] = __float2bfloat16_rn(0.f);
+        }
+        fence_proxy_async_smem();
     }
     __syncthreads();
 
@@ -277,17 +297,19 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, DecCfg<D, KV8>::kMin
                         d[kDnslots] = cu.nslots;
                     }
                     const uint32_t pb = pfull0 + 8 * slot;
-                    mbar_arrive_expect_tx(pb, (uint32_t)(pc.nrows * hp) * D * 2);
-                    // head kvh + j's rows go to tile rows 8j + r (hp = 2) or r
+                    const int dq = kNarrow ? p.dq : D;
+                    mbar_arrive_expect_tx(pb, (uint32_t)(pc.nrows * hp) * dq * 2);
+                    // head kvh + j's rows go to tile rows 8j + r (hp = 2) or r; a row of
+                    // dq < D columns is copied alone (the tile's rows are D wide)
                     for (int j = 0; j < hp; ++j)
                         for (int r = 0; r < pc.nrows;) {
                             const int pr = pc.row0 + r;
                             const int h0 = pr % p.g;
-                            const int cnt = min(p.g - h0, pc.nrows - r);
+                            const int cnt = dq == D ? min(p.g - h0, pc.nrows - r) : 1;
                             const __nv_bfloat16 *src =
-                                p.q + ((int64_t)(q0 + pr / p.g) * p.hq + (pc.kvh + j) * p.g + h0) * D;
+                                p.q + ((int64_t)(q0 + pr / p.g) * p.hq + (pc.kvh + j) * p.g + h0) * dq;
                             bulk_load(qring0 + slot * C::kQTileBytes + (8 * j + r) * D * 2, src,
-                                      (uint32_t)cnt * D * 2, pb);
+                                      (uint32_t)cnt * dq * 2, pb);
                             r += cnt;
                         }
                     ++filled;
@@ -319,10 +341,20 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, DecCfg<D, KV8>::kMin
                             const uint32_t kdst = stage0 + st * C::kStageBytes;
                             const uint32_t vdst = kdst + C::kPageBytes;
                             mbar_arrive_expect_tx(fb, 2u * hp * C::kHeadPageBytes);
-                            // one box per page and tensor: all D columns of 16 tokens,
-                            // laid out [chunk][slot][64] with the 128-byte swizzle
-                            tma_load_5d_hint(kdst, &tm_k, 0, 0, 0, pc.kvh, b, fb, policy);
-                            tma_load_5d_hint(vdst, &tm_v, 0, 0, 0, pc.kvh, b, fb, policy);
+                            if constexpr (!kNarrow) {
+                                // one box per page and tensor: all D columns of 16 tokens,
+                                // laid out [chunk][slot][64] with the 128-byte swizzle
+                                tma_load_5d_hint(kdst, &tm_k, 0, 0, 0, pc.kvh, b, fb, policy);
+                                tma_load_5d_hint(vdst, &tm_v, 0, 0, 0, pc.kvh, b, fb, policy);
+                            } else {
+                                // a narrower head: one box per 64 columns of (dq, slot, kv
+                                // head, block), the same layout, zeros past dq
+#pragma unroll
+                                for (int c = 0; c < C::kChunks; ++c) {
+                                    tma_load_4d_hint(kdst + c * 2048, &tm_k, 64 * c, 0, pc.kvh, b, fb, policy);
+                                    tma_load_4d_hint(vdst + c * 2048, &tm_v, 64 * c, 0, pc.kvh, b, fb, policy);
+                                }
+                            }
                         }
                     }
                     ok = __shfl_sync(0xffffffffu, good, 0) != 0;
@@ -609,10 +641,13 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, DecCfg<D, KV8>::kMin
                     const int64_t t = (int64_t)q0 + pr / p.g;
                     const int h = (pc.kvh + tile_row_head(row, hp)) * p.g + pr % p.g;
                     if (p.lse != nullptr && col == 0) p.lse[t * p.hq + h] = row_lse(M, L);
-                    uint2 packed;
-                    packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-                    packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-                    *reinterpret_cast<uint2 *>(p.out + (t * p.hq + h) * D + col) = packed;
+                    const int dq = kNarrow ? p.dq : D;
+                    if (!kNarrow || col < dq) {       // not the zero padding of a narrower head
+                        uint2 packed;
+                        packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+                        packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+                        *reinterpret_cast<uint2 *>(p.out + (t * p.hq + h) * dq + col) = packed;
+                    }
                 } else {
                     // partial: unnormalised sum relative to M, plus (M, L)
                     const int64_t base = ((int64_t)pc.slot * kDecRows + row);
@@ -628,8 +663,8 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, DecCfg<D, KV8>::kMin
                 named_barrier_sync(1, C::kConsumerWarps * 32);
                 if (s_merge) {
                     __threadfence();
-                    merge_unit<D>(p, q0, pc.kvh, pc.row0, pc.nrows, hp, pc.slot0, pc.nslots, tid,
-                                  C::kConsumerWarps * 32);
+                    merge_unit<D, kNarrow>(p, q0, pc.kvh, pc.row0, pc.nrows, hp, pc.slot0, pc.nslots, tid,
+                                           C::kConsumerWarps * 32);
                     // every piece has arrived: nothing else touches the counter in this
                     // launch; zero it for the next launch that reuses the plan
                     if (tid == 0) p.comb_count[pc.comb] = 0;
@@ -649,7 +684,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, DecCfg<D, KV8>::kMin
     }
 }
 
-template <int D, bool KV8>
+template <int D, bool KV8, bool kNarrow = false>
 static cudaError_t launch_decode_t(const DecodeParams &p, const CUtensorMap &tm_k,
                                    const CUtensorMap &tm_v, int ctas, cudaStream_t stream) {
     using C = DecCfg<D, KV8>;
@@ -657,13 +692,13 @@ static cudaError_t launch_decode_t(const DecodeParams &p, const CUtensorMap &tm_
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(ua_decode_kernel<D, KV8>,
+        cudaError_t e = cudaFuncSetAttribute(ua_decode_kernel<D, KV8, kNarrow>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    ua_decode_kernel<D, KV8><<<ctas, C::kThreads, C::kSmemBytes, stream>>>(p, tm_k, tm_v);
+    ua_decode_kernel<D, KV8, kNarrow><<<ctas, C::kThreads, C::kSmemBytes, stream>>>(p, tm_k, tm_v);
     return cudaGetLastError();
 }
 
@@ -673,8 +708,12 @@ cudaError_t launch_decode(int d, bool kv8, const DecodeParams &p, const CUtensor
         if (d != 128) return cudaErrorInvalidValue;
         return launch_decode_t<128, true>(p, tm_k, tm_v, ctas, stream);
     }
+    if (p.dq != d) return cudaErrorInvalidValue;
     switch (d) {
         case 64: return launch_decode_t<64, false>(p, tm_k, tm_v, ctas, stream);
+        case 80:
+        case 96:
+        case 112: return launch_decode_t<128, false, true>(p, tm_k, tm_v, ctas, stream);
         case 128: return launch_decode_t<128, false>(p, tm_k, tm_v, ctas, stream);
         case 256: return launch_decode_t<256, false>(p, tm_k, tm_v, ctas, stream);
         default: return cudaErrorInvalidValue;

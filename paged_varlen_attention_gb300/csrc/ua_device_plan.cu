@@ -568,7 +568,7 @@ DevPlanLayout device_plan_layout(const DevPlanShape &s) {
     L.off_comb_count = take(sizeof(int32_t) * (size_t)L.cap_comb);
     L.off_tiles = take(sizeof(PreTile) * (size_t)L.cap_items);
     L.off_pre_begin = take(sizeof(int32_t) * ((size_t)s.num_sms + 1));
-    L.off_part_o = take(sizeof(float) * (size_t)L.cap_slots * kDecRows * s.d);
+    L.off_part_o = take(sizeof(float) * (size_t)L.cap_slots * kDecRows * kernel_head_size(s.d));
     L.off_part_ml = take(2 * sizeof(float) * (size_t)L.cap_slots * kDecRows);
     L.off_scratch = off;
     take(sizeof(int32_t) * ((size_t)s.num_seqs + 1));                  // seq_u

@@ -35,6 +35,8 @@ struct DecodeParams {
     int32_t heads_per_unit;      // e4m3 pages: kv heads per unit (tile rows 8j.. are head kvh + j)
     int *status;                 // device status word
     unsigned long long wait_ns;  // limit of the main loop's waits (the drains keep kWaitLimitNs)
+    int32_t dq;                  // head size of q, out and the cache rows: the kernel's D, or
+                                 // 80 / 96 / 112 in the D = 128 kernel (rows zero-padded)
 };
 
 struct PrefillParams {
@@ -59,6 +61,9 @@ struct PrefillParams {
 };
 
 // Each returns the launch error (cudaSuccess when the launch was queued).
+// launch_decode: d is the head size (p.dq); for 80, 96 and 112 the D = 128
+// kernel runs with tm_k / tm_v mapping the cache as (d, 16 slots, Hkv,
+// blocks), two 64-column boxes per page, the second zero-filled past d.
 cudaError_t launch_decode(int d, bool kv8, const DecodeParams &p, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, int ctas, cudaStream_t stream);
 // claimed: the CTAs claim items from p.sched (D = 128 with a positive scale

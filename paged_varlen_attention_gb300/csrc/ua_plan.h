@@ -67,6 +67,15 @@ enum : int { kSchedNext = 0, kSchedDone = 1, kSchedItems = 2, kSchedInts = 4 };
 // SM on 256), and claiming them gained nothing.
 constexpr int kClaimMinMeanKvTiles = 16;
 
+// Head sizes: 64, 128 and 256 run in kernels of their own size; 80, 96 and
+// 112 run in the head-size-128 decode kernel, their rows zero-padded to 128
+// columns in shared memory (the padding is never read from memory).
+inline bool head_size_supported(int d) {
+    return d == 64 || d == 80 || d == 96 || d == 112 || d == 128 || d == 256;
+}
+// The head size of the kernel that runs head size d (its partials' row length).
+inline int kernel_head_size(int d) { return (d > 64 && d < 128) ? 128 : d; }
+
 struct alignas(16) DecPiece {   // one contiguous page range of one decode unit
     int32_t seq;
     int32_t kvh;         // (first) kv head of the unit

@@ -18,15 +18,15 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool prefill_supports(const Problem &p) {
     const int g = p.hq / p.hkv;
-    // the tensor-core kernel's TMEM budget is laid out for D <= 128
-    return p.d <= 128 && g >= 1 && g <= kPreRows && (kPreRows % g) == 0;
+    // the tensor-core kernels are built for head sizes 64 and 128
+    return (p.d == 64 || p.d == 128) && g >= 1 && g <= kPreRows && (kPreRows % g) == 0;
 }
 
 int validate_problem(const Problem &p) {
     if (p.num_seqs < 0 || p.hq <= 0 || p.hkv <= 0 || p.bt_stride < 0) return 1;
     if (p.num_seqs > 0 && (p.cu == nullptr || p.lk == nullptr)) return 1;
     if (p.hq % p.hkv != 0) return 2;
-    if (p.d != 64 && p.d != 128 && p.d != 256) return 2;
+    if (!head_size_supported(p.d)) return 2;
     if (p.bs <= 0 || p.bs % kBlockSize != 0 || p.bs > kMaxBlockSize) return 2;
     // the block table seen in 16-token pages stays indexable in int32
     if ((int64_t)p.bt_stride * (p.bs / kBlockSize) > INT32_MAX / 4) return 1;
@@ -277,7 +277,7 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
     off = align_up(off + sizeof(int32_t) * kSchedInts, kAlign);
     L.blob_bytes = off;
     L.off_part_o = off;
-    off = align_up(off + sizeof(float) * (size_t)plan.n_slots * kDecRows * p.d, kAlign);
+    off = align_up(off + sizeof(float) * (size_t)plan.n_slots * kDecRows * kernel_head_size(p.d), kAlign);
     L.off_part_ml = off;
     off = align_up(off + 2 * sizeof(float) * (size_t)plan.n_slots * kDecRows, kAlign);
     L.total_bytes = (plan.pieces.empty() && plan.tiles.empty()) ? 0 : off;

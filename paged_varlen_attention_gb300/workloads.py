@@ -108,7 +108,8 @@ class Batch:
 
 
 # --------------------------------------------------------------------------
-# The five standard batches (index 1..5), and a head-size-256 decode batch (6).
+# The five standard batches (index 1..5), a head-size-256 decode batch (6) and
+# a head-size-96 decode batch (7).
 # --------------------------------------------------------------------------
 
 CONFIG_NAMES = {
@@ -118,6 +119,7 @@ CONFIG_NAMES = {
     4: "llama3_8b_mixed_256dec_4x512chunk",
     5: "llama3_70b_long_mixed_32x8k-32k_2x2048chunk",
     6: "gemma2_9b_decode_64x2k-4k",
+    7: "phi3_mini_decode_64x2k-4k",
 }
 
 
@@ -154,6 +156,12 @@ def config_spec(idx: int) -> Spec:
         # heads (Hq 16, Hkv 8, head size 256, scale 1/sqrt(256))
         k = rng.integers(2048, 4096, size=64, endpoint=True)
         return Spec(name, np.ones(64, np.int32), k, 16, 8, 256,
+                    data_seed=data_seed, layout_seed=layout_seed)
+    if idx == 7:
+        # the same lengths with Phi-3-mini's attention heads (Hq = Hkv = 32,
+        # head size 96, scale 1/sqrt(96))
+        k = rng.integers(2048, 4096, size=64, endpoint=True)
+        return Spec(name, np.ones(64, np.int32), k, 32, 32, 96,
                     data_seed=data_seed, layout_seed=layout_seed)
     raise ValueError(f"unknown config {idx}")
 

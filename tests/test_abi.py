@@ -68,7 +68,7 @@ def _call(lib, cu, sk, hq=4, hk=2, d=64, bs=16, nb=8, stride=4, causal=1, scale=
     (dict(cu=[0, 3, 2], sk=[17, 40]), 1),         # decreasing cu
     (dict(cu=[0, 1, 6], sk=[17, 90]), 1),         # needs more pages than the table holds
     (dict(cu=[0, 1, 6], sk=[17, 40], hq=6, hk=4), 2),   # Hq not a multiple of Hkv
-    (dict(cu=[0, 1, 6], sk=[17, 40], d=96), 2),   # unsupported head sizes
+    (dict(cu=[0, 1, 6], sk=[17, 40], d=72), 2),   # unsupported head sizes
     (dict(cu=[0, 1, 6], sk=[17, 40], d=512), 2),
     (dict(cu=[0, 1, 6], sk=[17, 40], bs=24), 2),  # pages not a multiple of 16 tokens
     (dict(cu=[0, 1, 6], sk=[17, 40], bs=512), 2), # pages above 256 tokens
@@ -167,7 +167,7 @@ def test_header_is_plain_c_and_the_library_links_from_c(lib, tmp_path):
         "int main(void) {\n"
         "    int32_t cu[3] = {0, 1, 6}, sk[2] = {17, 40};\n"
         "    size_t bytes = 0;\n"
-        "    ua_status st = ua_workspace_size(cu, sk, 2, 4, 2, 96, 16, 3, 1, &bytes);\n"
+        "    ua_status st = ua_workspace_size(cu, sk, 2, 4, 2, 72, 16, 3, 1, &bytes);\n"
         '    printf("%s\\n", ua_status_string(st));\n'
         "    return st == UA_ERR_UNSUPPORTED ? 0 : 1;\n}\n")
     libdir = os.path.dirname(B._LIB_PATH)

@@ -34,7 +34,7 @@ def layout(lib, num_seqs, max_total_q, max_seq_q, hq, hkv, d, stride, fp8=0, sms
 
 
 def test_shapes_are_checked_on_the_host(lib):
-    assert layout(lib, 4, 64, 0, 32, 8, 96, 64)[0] == UNSUPPORTED      # head size
+    assert layout(lib, 4, 64, 0, 32, 8, 72, 64)[0] == UNSUPPORTED      # head size
     assert layout(lib, 4, 64, 0, 30, 8, 128, 64)[0] == UNSUPPORTED     # Hq not a multiple of Hkv
     assert layout(lib, 4, 64, 0, 32, 8, 128, 64, bs=24)[0] == UNSUPPORTED   # page size
     assert layout(lib, 4, 64, 0, 32, 8, 128, 64, bs=512)[0] == UNSUPPORTED

@@ -61,6 +61,7 @@ SDPA_CASES = [
     ([1, 40, 2], [130, 40, 64], 8, 2, 64, 64, True),   # larger pages: 64 tokens
     ([3, 1], [100, 257], 4, 1, 16, 48, False),         # 48-token pages, ragged last page
     ([2, 1], [40, 70], 4, 2, 256, 32, True),            # head size 256
+    ([5, 1], [37, 90], 8, 2, 96, 16, True),             # head size 96
 ]
 
 
