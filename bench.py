@@ -422,7 +422,9 @@ def time_attention(ua, torch, device, batch, steps, warmup, dist, flush):
                              out=out, cu_seqlens_q_host=cu_h, seqused_k_host=sk_h, workspace=ws,
                              stream=stream)
 
+    # warm-up steps as the timed ones (an L2 flush before each call)
     for _ in range(max(warmup, 3)):
+        flush()
         step()
     torch.cuda.synchronize()
     ua.device_status()
@@ -541,6 +543,7 @@ def run_ours(args, rank, world, local, dist):
             out_h.copy_(out, non_blocking=True)
 
         for _ in range(3):
+            flush()
             e2e_step()
         torch.cuda.synchronize()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -765,7 +768,9 @@ def run_cascade(args):
                              cu_seqlens_q_host=cu_o, seqused_k_host=sk_f)
 
     for _ in range(max(args.warmup, 3)):
+        flush()
         cascade()
+        flush()
         direct()
     torch.cuda.synchronize()
     diff = (out.float() - out_f.float()).abs()
@@ -855,7 +860,9 @@ def run_kv_append(args):
         ua.kv_append(k_new, v_new, kc, vc, cu, sk, bt, cu_seqlens_q_host=b.cu_seqlens_q,
                      seqused_k_host=b.seqused_k)
 
+    # warm-up steps are the timed steps without the events (L2 flush, then the call)
     for _ in range(max(args.warmup, 3)):
+        flush()
         step()
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -927,6 +934,7 @@ def run_fp8kv(args):
                                    cu_seqlens_q_host=b.cu_seqlens_q, seqused_k_host=b.seqused_k)
 
     for _ in range(max(args.warmup, 3)):
+        flush()
         step()
     torch.cuda.synchronize()
     steps = args.steps
@@ -1013,6 +1021,7 @@ def run_graph(args):
     with torch.cuda.graph(graph):
         call(torch.cuda.current_stream(dev))
     for _ in range(max(args.warmup, 3)):
+        flush()
         graph.replay()
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream(dev)

@@ -55,11 +55,14 @@ namespace ua {
 // pages arrive through a 4-D view of the cache whose rows end at dq, two
 // 64-column boxes per page, and TMA fills the columns past dq with zeros
 // (they are not read from memory); Q's tile rows are zero past dq; the output
-// keeps the first dq columns.  Every row of such a batch comes here too.
-template <int D, bool KV8>
+// keeps the first dq columns.  Every row of such a batch comes here too; the
+// k-steps of Q K^T past dq and the n-tiles of P V past dq (all zeros) are
+// skipped.
+template <int D, bool KV8, bool kNarrow = false>
 struct DecCfg {
     static_assert(!KV8 || D == 128, "the e4m3 path is laid out for D = 128");
     static_assert(D == 64 || D == 128 || D == 256, "head sizes 64, 128 and 256");
+    static_assert(!kNarrow || (D == 128 && !KV8), "narrower heads run in the bf16 D = 128 kernel");
     static constexpr int kChunks = D / 64;                        // 64-column TMA boxes per row
     static constexpr int kHeadPageBytes = kBlockSize * D * (KV8 ? 1 : 2);   // one page of one kv head
     static constexpr int kPageBytes = (KV8 ? 2 : 1) * kHeadPageBytes;      // K (or V) part of a stage
@@ -203,10 +206,11 @@ __device__ __forceinline__ void merge_unit(const DecodeParams &p, int q0, int kv
 
 // kNarrow: a head narrower than D (p.dq < D, see above).
 template <int D, bool KV8, bool kNarrow>
-__global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, DecCfg<D, KV8>::kMinCtasPerSm)
+__global__ void __launch_bounds__(DecCfg<D, KV8, kNarrow>::kThreads,
+                                  DecCfg<D, KV8, kNarrow>::kMinCtasPerSm)
     ua_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v) {
-    using C = DecCfg<D, KV8>;
+    using C = DecCfg<D, KV8, kNarrow>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -481,6 +485,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, DecCfg<D, KV8>::kMin
                 } else {
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
+                        if (kNarrow && ks * 16 >= p.dq) break;     // zero columns of both operands
                         const int c = ks >> 2;
                         const int ch = (ks & 3) * 2 + ((lane >> 3) & 1);
                         const int r = ((lane >> 4) << 3) + (lane & 7);
@@ -559,6 +564,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, DecCfg<D, KV8>::kMin
                 } else {
 #pragma unroll
                     for (int np = 0; np < D / 16; ++np) {
+                        if (kNarrow && np * 16 >= p.dq) break;     // output columns past the head
                         const int c = np >> 2;
                         const int ch = (np & 3) * 2 + (lane >> 4);
                         const int r = ((lane >> 3) & 1) * 8 + (lane & 7);
@@ -687,7 +693,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::kThreads, DecCfg<D, KV8>::kMin
 template <int D, bool KV8, bool kNarrow = false>
 static cudaError_t launch_decode_t(const DecodeParams &p, const CUtensorMap &tm_k,
                                    const CUtensorMap &tm_v, int ctas, cudaStream_t stream) {
-    using C = DecCfg<D, KV8>;
+    using C = DecCfg<D, KV8, kNarrow>;
     static thread_local int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);

@@ -52,7 +52,22 @@ CASES = [([1, 5, 0, 1], [17, 40, 3, 1], 4, 2, 64),
          ([1] * 16 + [300, 64], [100 * (i + 1) for i in range(16)] + [300, 2000], 32, 8, 128)]
 
 
-@pytest.mark.parametrize("case", CASES, ids=["small", "mixed"])
+_RNG = np.random.Generator(np.random.PCG64(4100))
+_MANY_K = [int(x) for x in _RNG.integers(1, 60, 5000)]
+# more cases for the copy alone: 5000 sequences (more than the kernel stages in
+# shared memory, so the lookup reads the lengths from global memory), the
+# widest row (Hkv * D = 2048), a row of 48 pieces (D = 96), a long prefill
+# spread over many CTAs with a ragged last one
+COPY_CASES = CASES + [
+    ([1] * 5000, _MANY_K, 2, 1, 64),
+    ([1, 700, 3, 1], [9, 1500, 3, 4000], 16, 16, 128),
+    ([5, 1, 257, 2], [5, 80, 300, 33], 8, 4, 96),
+    ([1999, 1], [2100, 1], 8, 8, 128),
+]
+
+
+@pytest.mark.parametrize("case", COPY_CASES,
+                         ids=["small", "mixed", "many_seqs", "widest_row", "d96", "long_ragged"])
 def test_append_matches_oracle_bit_for_bit(case):
     import torch
     import paged_varlen_attention_gb300 as ua
