@@ -77,9 +77,11 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 // Wait until the phase with the given parity has completed.  Bounded: gives
 // up after kWaitLimitNs.  try_wait itself suspends the thread for a while
 // (until the phase completes or a hardware time runs out), so the timer is
-// read only every 32 attempts.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *status) {
-    if (mbar_try_wait(bar, parity)) return true;
+// read only every 32 attempts.  Only the first try_wait is inline: the
+// bounded loop is one out-of-line copy, as inlined at every wait site it made
+// the warp-specialised kernels larger than the instruction cache (measured:
+// 7% of the one-SM prefill kernel's time on 1000-token prompts).
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, int *status) {
     const uint64_t t0 = globaltimer_ns();
     while (true) {
 #pragma unroll 1
@@ -90,6 +92,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *st
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, status);
 }
 
 // The same with a caller-given limit.  Below the library's limit (a test of

@@ -145,24 +145,25 @@ __device__ __forceinline__ PairInfo make_pair(const PrefillParams &p, const PreT
     return pi;
 }
 
-// Walks this CTA's work items (its range of the plan); the record of the next
-// item is loaded one item ahead so that its latency hides behind the current one.
+// Walks this CTA's work items (its range of the plan).  Records are loaded two
+// items ahead: take() hands out the record loaded one item earlier and starts
+// the load of the one after next, so no role waits on a record's load at an
+// item boundary (only the first two loads are waited for).
 struct ItemCursor {
     int t, end;
-    PreTile cur;
+    PreTile cur, nxt;
     __device__ __forceinline__ ItemCursor(const PrefillParams &p)
         : t(p.tile_begin[blockIdx.x]), end(p.tile_begin[blockIdx.x + 1]) {
         if (t < end) cur = p.tiles[t];
+        if (t + 1 < end) nxt = p.tiles[t + 1];
     }
     __device__ __forceinline__ bool valid(const PrefillParams &) const { return t < end; }
-    // returns the current record and starts the load of the next one
-    __device__ __forceinline__ PreTile take(const PrefillParams &p, PreTile &next) const {
-        next = (t + 1 < end) ? p.tiles[t + 1] : cur;
-        return cur;
-    }
-    __device__ __forceinline__ void advance(const PreTile &next) {
-        cur = next;
+    __device__ __forceinline__ PreTile take(const PrefillParams &p) {
+        const PreTile out = cur;
+        cur = nxt;
+        if (t + 2 < end) nxt = p.tiles[t + 2];
         ++t;
+        return out;
     }
 };
 
@@ -180,16 +181,29 @@ constexpr int kItemReaders = 11;
 template <bool kClaimed>
 struct ItemIter;
 
+// A record made warp-uniform: every field from lane 0 (the compiler then sees
+// values derived from it, such as MMA operands and loop bounds, as uniform).
+__device__ __forceinline__ PreTile uniform_tile(const PreTile &t) {
+    PreTile u;
+    u.seq = __shfl_sync(0xffffffffu, t.seq, 0);
+    u.kvh = __shfl_sync(0xffffffffu, t.kvh, 0);
+    u.row0 = __shfl_sync(0xffffffffu, t.row0, 0);
+    u.nrows = __shfl_sync(0xffffffffu, t.nrows, 0);
+    u.kv_tiles = __shfl_sync(0xffffffffu, t.kv_tiles, 0);
+    u.q0 = __shfl_sync(0xffffffffu, t.q0, 0);
+    u.lq = __shfl_sync(0xffffffffu, t.lq, 0);
+    u.lk = __shfl_sync(0xffffffffu, t.lk, 0);
+    return u;
+}
+
 template <>
 struct ItemIter<false> {
     ItemCursor it;
-    PreTile nxt;
     __device__ __forceinline__ ItemIter(const PrefillParams &p, const PreTile *, uint32_t, uint32_t)
         : it(p) {}
     __device__ __forceinline__ int take(const PrefillParams &p, uint32_t, bool, int, PreTile &out) {
         if (!it.valid(p)) return 0;
-        out = it.take(p, nxt);
-        it.advance(nxt);
+        out = uniform_tile(it.take(p));
         return 1;
     }
 };
@@ -204,7 +218,7 @@ struct ItemIter<true> {
                                         PreTile &out) {
         const uint32_t slot = k % kItemRing;
         if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * slot, (k / kItemRing) & 1, p.status))) return -1;
-        out = ring[slot];
+        out = uniform_tile(ring[slot]);
         __syncwarp();
         if (release && lane == 0) mbar_arrive(empty0 + 8 * slot);
         return out.seq < 0 ? 0 : 1;
@@ -302,7 +316,9 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
     const uint32_t bar0 = smem_u32(bars);
     auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
 
-    const int warp = threadIdx.x >> 5;
+    // the warp index and TMEM base broadcast from lane 0, so that the compiler
+    // sees them as warp-uniform (MMA operands built from them need no per-lane loop)
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
     const int lane = threadIdx.x & 31;
     // a CTA with no item (a fixed grid whose plan, built on the device, has
     // fewer items than CTAs) leaves before touching barriers or TMEM (the same
@@ -345,7 +361,7 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
     if (warp == 9) {
         // ================================================================ Q + V producer
         if (lane == 0) {
@@ -620,14 +636,14 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
                     break;
                 }
                 ++qcnt;
-                ok = issue_s(e);
-                if (ok && nx > 1) ok = issue_s(e + 1);
-                if (ok && nx <= 2) umma_commit_warp(bar(kBarQEmpty + x));   // after the last S
-                for (int j = 0; j < nx && ok; ++j) {
-                    ok = issue_pv(e + j, j == 0);
-                    if (ok && j + 2 < nx) {
-                        ok = issue_s(e + j + 2);
-                        if (ok && j + 2 == nx - 1) umma_commit_warp(bar(kBarQEmpty + x));
+                // S(0), S(1), then P V(t-2) and S(t) as each S buffer frees up; Q is
+                // released after the last S.  (One loop, so that each issue sequence
+                // exists once in the code: the kernel's speed depends on its size.)
+                for (int t = 0; t < nx + 2 && ok; ++t) {
+                    if (t >= 2) ok = issue_pv(e + t - 2, t == 2);
+                    if (ok && t < nx) {
+                        ok = issue_s(e + t);
+                        if (ok && t == nx - 1) umma_commit_warp(bar(kBarQEmpty + x));
                     }
                 }
             }
@@ -732,7 +748,8 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-#pragma unroll
+                    // a rare path: kept rolled, out of the instruction cache's way
+#pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t v[32];
                         tmem_ld32(o_addr + 32 * c, v);
