@@ -578,9 +578,8 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 }
 
 // mbar_wait for a barrier that threads of the peer CTA arrive on (acquire at
-// cluster scope).  Bounded like mbar_wait.
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int *status) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
+// cluster scope).  Bounded like mbar_wait, its slow path out of line too.
+static __device__ __noinline__ bool mbar_wait_cluster_slow(uint32_t bar, uint32_t parity, int *status) {
     const uint64_t t0 = globaltimer_ns();
     while (true) {
 #pragma unroll 1
@@ -591,6 +590,11 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int *status) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    return mbar_wait_cluster_slow(bar, parity, status);
 }
 
 // tcgen05 on a CTA pair (cta_group::2): TMEM is allocated by one warp of each

@@ -129,14 +129,22 @@ __device__ __forceinline__ PairItem make_item(const PrefillParams &p, const PreT
     return it;
 }
 
-// The pair's items: its range of the plan's list (dealt in advance).
+// The pair's items: its range of the plan's list (dealt in advance).  Records
+// are loaded two items ahead: next() hands out the one loaded an item earlier.
 struct PairCursor {
     int t, end;
+    PreTile cur, nxt;
     __device__ __forceinline__ PairCursor(const PrefillParams &p, int pair)
-        : t(p.tile_begin[pair]), end(p.tile_begin[pair + 1]) {}
+        : t(p.tile_begin[pair]), end(p.tile_begin[pair + 1]) {
+        if (t < end) cur = p.tiles[t];
+        if (t + 1 < end) nxt = p.tiles[t + 1];
+    }
     __device__ __forceinline__ bool next(const PrefillParams &p, PreTile &out) {
         if (t >= end) return false;
-        out = p.tiles[t++];
+        out = cur;
+        cur = nxt;
+        if (t + 2 < end) nxt = p.tiles[t + 2];
+        ++t;
         return true;
     }
 };
@@ -226,7 +234,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     const uint32_t bar0 = smem_u32(bars);
     auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
 
-    const int warp = threadIdx.x >> 5;
+    // the warp index and TMEM base broadcast from lane 0, so that the compiler
+    // sees them as warp-uniform
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
     const int pair = (int)(blockIdx.x >> 1);
@@ -263,7 +273,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     tc_fence_before();
     cluster_sync_all();       // barriers of both CTAs initialised, TMEM allocated
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
     const uint64_t pol_kv = l2_policy_evict_last();   // K/V steps are re-read by sibling items
 
     if (warp == 9) {
