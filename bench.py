@@ -38,7 +38,8 @@ llama3_70b_long_mixed_32x8k-32k_2x2048chunk); llama3_8b_cascade_64dec_shared4k
 same attention as one direct call); kv_append_mistral_24b_16x1000 (writing
 16 000 new tokens' K/V into their pages); llama3_8b_decode_64x2k-4k_fp8kv (the
 headline batch over an E4M3 cache); llama3_8b_decode_64x2k-4k_graph (the
-headline batch planned on the GPU, one CUDA-graph replay per step);
+headline batch planned on the GPU, one CUDA-graph replay per step; its line
+also times a model step of 32 layers' calls sharing one plan);
 gemma2_9b_decode_64x2k-4k (the headline lengths with head size 256: Hq 16,
 Hkv 8); phi3_mini_decode_64x2k-4k (the same lengths with head size 96:
 Hq = Hkv = 32).
@@ -93,11 +94,16 @@ DECODE_WORKLOAD = "llama3_8b_decode_64x2k-4k"
 CASCADE_WORKLOAD = "llama3_8b_cascade_64dec_shared4k"
 # KV-cache append of the 16 x 1000-token prefill batch's new tokens (Hkv 8, D 128).
 APPEND_WORKLOAD = "kv_append_mistral_24b_16x1000"
-# The headline decode batch over an FP8 E4M3 KV cache (per-tensor scales).
+# The headline decode batch over an FP8 E4M3 KV cache (per-tensor scales), and
+# the 16 x 1000-token prefill batch over one (its pages decoded for the
+# tensor-core prefill kernel inside the call).
 FP8_WORKLOAD = "llama3_8b_decode_64x2k-4k_fp8kv"
+FP8_WORKLOADS = {FP8_WORKLOAD: 2, "mistral_24b_prefill_16x1000_fp8kv": 3}
 # the headline decode batch through unified_attention_device_plan, captured once
 # as a CUDA graph and replayed (no host planning, no plan copy)
 GRAPH_WORKLOAD = "llama3_8b_decode_64x2k-4k_graph"
+# attention layers per model step in the plan-reuse graph (Llama-3.1-8B: 32)
+LAYERS = 32
 
 
 def parse_args():
@@ -106,8 +112,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=sorted(WORKLOADS) + [CASCADE_WORKLOAD, APPEND_WORKLOAD, FP8_WORKLOAD,
-                                                 GRAPH_WORKLOAD])
+                    choices=sorted(WORKLOADS) + [CASCADE_WORKLOAD, APPEND_WORKLOAD, GRAPH_WORKLOAD]
+                    + sorted(FP8_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -632,9 +638,9 @@ def run_reference(args, rank, world):
     if args.workload in (CASCADE_WORKLOAD, APPEND_WORKLOAD):
         raise SystemExit(f"--impl reference times the attention workloads; {args.workload} "
                          "is not one (its parts are timed by the attention workloads)")
-    fp8 = args.workload == FP8_WORKLOAD
-    # the graph and fp8 workloads compute attention over the headline batch
-    idx = WORKLOADS.get(args.workload, WORKLOADS[DECODE_WORKLOAD])
+    fp8 = args.workload in FP8_WORKLOADS
+    # the graph workload computes attention over the headline batch
+    idx = FP8_WORKLOADS[args.workload] if fp8 else WORKLOADS.get(args.workload, WORKLOADS[DECODE_WORKLOAD])
     b = workload_batch(idx, args.block_size)
     s = b.spec
     if fp8:
@@ -908,14 +914,16 @@ def run_kv_append(args):
 
 
 def run_fp8kv(args):
-    """The headline decode batch over an E4M3 cache: the same call as the default
-    workload, with K / V read as one byte per element (half the bytes)."""
+    """A standard batch over an E4M3 cache: the headline decode batch (K / V read
+    as one byte per element, half the bytes) or the 16 x 1000-token prefill batch
+    (its pages decoded to bf16 in the workspace, then the tensor-core prefill
+    kernel; the roofline is that pair of launches against the bf16 peak)."""
     import torch
     import paged_varlen_attention_gb300 as ua
 
     ua.load_library()
     dev = torch.device("cuda:0")
-    b = W.config_batch(WORKLOADS[DECODE_WORKLOAD], poison=False)
+    b = W.config_batch(FP8_WORKLOADS[args.workload], poison=False)
     s_ = b.spec
     ks, vs = 0.05, 0.05
     k8, v8 = W.fp8_caches(b, ks, vs)
@@ -955,33 +963,47 @@ def run_fp8kv(args):
         times = timed()
         ua.profile_enable(True)
         timed()
-    dec = [ua.profile_read(k)[0][0] for k in range(steps)]
+    prof = [ua.profile_read(k) for k in range(steps)]
     ua.profile_enable(False)
     if ua.device_status():
         raise RuntimeError("device status set after the fp8 steps")
-    work = algorithmic_work(s_)
+    dec = [p[0][0] for p in prof if p[0][0] >= 0]
+    pre = [p[0][1] for p in prof if p[0][1] >= 0]
+    launches = sum(sum(p[1][:3]) for p in prof) // steps
+    work = algorithmic_work(s_, routed_prefill_seqs(ua, b, torch.cuda.get_device_properties(0).multi_processor_count))
     # K and V one byte per element: the bf16 figure's K+V bytes halved
-    dec_bytes = work["decode_bytes"] - work["kv_bytes"] // 2
-    dec_ms = statistics.mean(dec)
-    achieved = dec_bytes / (dec_ms / 1e3) / 1e9
+    dec_bytes = work["decode_bytes"] - work["kv_bytes"] // 2 if not pre else work["decode_bytes"]
     peaks = measured_peaks()
     total_s = sum(times) / 1e3
+    if pre:
+        pre_ms = statistics.mean(pre)
+        achieved = work["prefill_flops"] / (pre_ms / 1e3) / 1e12
+        roof = {"kernel": "ua_dequant_pages_kernel + ua_prefill_kernel", "bound": "tensor",
+                "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "per_launch": f"{work['prefill_flops']} algorithmic flops (the page decode's "
+                              "time counted in)",
+                "launch_ms": pre_ms, "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json, burst)"}
+    else:
+        dec_ms = statistics.mean(dec)
+        achieved = dec_bytes / (dec_ms / 1e3) / 1e9
+        roof = {"kernel": "ua_decode_kernel<128, fp8 kv>", "bound": "hbm", "achieved": achieved,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "traffic": ncu_traffic("decode", FP8_WORKLOAD),
+                "per_launch": f"{dec_bytes} algorithmic bytes (1-byte K/V)",
+                "launch_ms": dec_ms, "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"}
     return {
         "metric": METRIC, "value": s_.total_q * steps / total_s, "unit": "tokens/s", "n_gpus": 1,
         "steps": steps, "warmup": args.warmup, "ms_per_step": sum(times) / steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 q/o, e4m3 kv",
         "data": "synthetic (seeded N(0,1) bf16 quantised to e4m3 with scale 0.05, shuffled pages)",
-        "config": {"workload": FP8_WORKLOAD, "num_seqs": s_.num_seqs, "q_tokens": s_.total_q,
+        "config": {"workload": args.workload, "num_seqs": s_.num_seqs, "q_tokens": s_.total_q,
                    "kv_tokens": work["kv_tokens"], "num_q_heads": s_.num_q_heads,
                    "num_kv_heads": s_.num_kv_heads, "head_size": s_.head_size, "block_size": 16,
                    "l2": "L2 flushed between steps (256 MB write, then 256 MB read so the write-back is outside the timed interval)",
                    "parallelism": "1 GPU, no collective"},
-        "roofline": {"kernel": "ua_decode_kernel<128, fp8 kv>", "bound": "hbm", "achieved": achieved,
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": ncu_traffic("decode", FP8_WORKLOAD),
-                     "per_launch": f"{dec_bytes} algorithmic bytes (1-byte K/V)",
-                     "launch_ms": dec_ms, "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"},
-        "gpu_launches": steps,
+        "roofline": roof,
+        "gpu_launches": launches * steps,
         "clocks": clocks.summary(),
     }
 
@@ -1039,8 +1061,29 @@ def run_graph(args):
         torch.cuda.synchronize()
         return [a.elapsed_time(e) for a, e in evs]
 
+    # A model step: one plan serves every layer's attention call (same lengths),
+    # so the graph runs the planner once, then the attention of LAYERS layers,
+    # the first planning and the rest reusing the plan in the workspace.  (One
+    # K/V cache for all layers: at 0.8 GB it is far larger than L2, so every
+    # call still reads its K/V from HBM.)
+    def layer_call(stream, reuse):
+        ua.unified_attention_device_plan(d["q"], d["k_cache"], d["v_cache"], d["cu_seqlens_q"],
+                                         d["seqused_k"], d["block_table"], s_.softmax_scale, True,
+                                         out=out, workspace=ws, max_seq_q=1, stream=stream,
+                                         reuse_plan=reuse)
+
+    model_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(model_graph):
+        for layer in range(LAYERS):
+            layer_call(torch.cuda.current_stream(dev), layer > 0)
+    for _ in range(max(args.warmup, 3)):
+        flush()
+        model_graph.replay()
+    torch.cuda.synchronize()
+
     with ClockSampler(gpu_id_for_smi(torch, 0)) as clocks:
         times = timed(graph.replay)
+        model_times = timed(model_graph.replay)
         # per-kernel times: the same call made eagerly with the library's events
         ua.profile_enable(True)
         timed(lambda: call(stream))
@@ -1048,6 +1091,7 @@ def run_graph(args):
     ua.profile_enable(False)
     if ua.device_status():
         raise RuntimeError("device status set after the graph steps")
+    model_ms = statistics.mean(model_times)
     dec_ms = statistics.mean(p[0][0] for p in prof)
     plan_ms = statistics.mean(p[0][3] for p in prof)
     work = algorithmic_work(s_)
@@ -1071,6 +1115,12 @@ def run_graph(args):
                      "per_launch": f"{work['decode_bytes']} algorithmic bytes",
                      "launch_ms": dec_ms, "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"},
         "call": {"kernel_ms": {"planner": plan_ms, "decode": dec_ms}},
+        "plan_reuse": {"layers": LAYERS, "ms_per_model_step": model_ms,
+                       "ms_per_call": model_ms / LAYERS,
+                       "tokens_per_s_per_call": s_.total_q / (model_ms / LAYERS / 1e3),
+                       "note": "one CUDA graph per model step: the planner once, then the "
+                               "attention call of every layer, the first planning and the "
+                               "rest reusing the plan; L2 flushed between model steps only"},
         "gpu_launches": 2 * steps,
         "clocks": clocks.summary(),
     }
@@ -1088,11 +1138,11 @@ def main():
         return
     import torch
 
-    if args.workload in (CASCADE_WORKLOAD, APPEND_WORKLOAD, FP8_WORKLOAD, GRAPH_WORKLOAD):
+    if args.workload in (CASCADE_WORKLOAD, APPEND_WORKLOAD, GRAPH_WORKLOAD) or args.workload in FP8_WORKLOADS:
         if world != 1:
             raise SystemExit("this workload runs on one GPU")
         fn = {CASCADE_WORKLOAD: run_cascade, APPEND_WORKLOAD: run_kv_append,
-              FP8_WORKLOAD: run_fp8kv, GRAPH_WORKLOAD: run_graph}[args.workload]
+              GRAPH_WORKLOAD: run_graph}.get(args.workload, run_fp8kv)
         print(json.dumps(fn(args)), flush=True)
         return
     res = run_ours(args, rank, world, local, dist)

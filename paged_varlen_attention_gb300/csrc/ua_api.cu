@@ -355,17 +355,18 @@ static ua_status refuse_capture(cudaStream_t stream) {
     return cs == cudaStreamCaptureStatusNone ? UA_OK : UA_ERR_UNSUPPORTED;
 }
 
-// Whether the head-size-128 prefill rows of this call run on SM pairs.
-static bool use_pair_prefill(int32_t head_size, int kv_fp8) {
-    return kPairPrefill && head_size == 128 && !kv_fp8;
-}
+// Whether the head-size-128 prefill rows of this call may run on SM pairs.
+static bool use_pair_prefill(int32_t head_size) { return kPairPrefill && head_size == 128; }
 
 // The prefill scheduling options of a call: long items on SM pairs
 // (two-SM kernel, head size 128), or else claimed by the one-SM CTAs as they
 // go (head size 128 with a positive scale); the planner decides per batch.
+// An e4m3 cache's prefill rows read a bf16 copy of their pages that the call
+// decodes first (ua_pages.cu), so they take the same kernels.
 static void configure_prefill(Problem &pr, bool scale_positive, int kv_fp8) {
-    pr.prefill_pair = use_pair_prefill(pr.d, kv_fp8);
+    pr.prefill_pair = use_pair_prefill(pr.d);
     pr.prefill_claim = !pr.prefill_pair && pr.d == 128 && scale_positive;
+    pr.dequant_prefill = kv_fp8 != 0;
 }
 
 // Workspace bytes of the block table expanded to 16-token pages (pages of
@@ -431,7 +432,8 @@ extern "C" ua_status ua_workspace_size(const int32_t *cu_seqlens_q_host,
     DeviceState *ds = nullptr;
     ua_status st = device_state(&ds);
     if (st != UA_OK) return st;
-    configure_prefill(pr, true, 0);
+    // items dealt in advance (the plan of either sign of the scale fits in this)
+    configure_prefill(pr, false, 0);
     thread_local Plan plan;
     build_plan(pr, ds->sms, kPrefillEnabled, plan);
     *bytes = plan.layout.total_bytes + expanded_table_bytes(num_seqs, block_table_stride, block_size);
@@ -455,8 +457,11 @@ extern "C" ua_status ua_workspace_size_fp8kv(const int32_t *cu_seqlens_q_host,
     DeviceState *ds = nullptr;
     ua_status st = device_state(&ds);
     if (st != UA_OK) return st;
+    // items dealt in advance (the plan of either sign of the scale fits in this),
+    // the decoded bf16 copy of the prefill sequences' pages included
+    configure_prefill(pr, false, 1);
     thread_local Plan plan;
-    build_plan(pr, ds->sms, false, plan);     // every row in the decode kernel
+    build_plan(pr, ds->sms, kPrefillEnabled, plan);
     *bytes = plan.layout.total_bytes + expanded_table_bytes(num_seqs, block_table_stride, block_size);
     return UA_OK;
 }
@@ -652,8 +657,7 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
     thread_local Plan plan;
     thread_local std::vector<uint8_t> blob;
     configure_prefill(pr, softmax_scale * k_scale > 0.f, kv_fp8);
-    // an fp8 cache is read by the decode kernel only
-    build_plan(pr, ds->sms, kPrefillEnabled && !kv_fp8, plan);
+    build_plan(pr, ds->sms, kPrefillEnabled, plan);
     const bool pair_prefill = plan.pre_pair;
     const Layout &L = plan.layout;
     if (L.total_bytes > 0) {
@@ -671,18 +675,30 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
                             (uint64_t)num_blocks, eb, box_heads))
         return UA_ERR_CUDA;
     // prefill: Q tiles (loads) and out tiles (stores) as [total_q, Hq, D], and K as
-    // [num_blocks * 16, Hkv, D] with one box per 64 columns
+    // [num_blocks * 16, Hkv, D] with one box per 64 columns.  With an e4m3 cache
+    // the prefill kernels read the bf16 copy of their sequences' pages that the
+    // call decodes into the workspace, through its own block table.
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const bool dq = plan.dq_pages > 0;
+    const void *k_pre = dq ? static_cast<const void *>(ws + L.off_dq_k) : k_cache;
+    const void *v_pre = dq ? static_cast<const void *>(ws + L.off_dq_v) : v_cache;
+    const int32_t *bt_pre = dq ? reinterpret_cast<const int32_t *>(ws + L.off_dq_bt) : block_table;
+    const int64_t blocks_pre = dq ? plan.dq_pages : num_blocks;
+    CUtensorMap tm_vpre = tm_vp, tm_kpre_unused;
     if (!plan.tiles.empty() &&
         (!encode_map(&tm_q, q, head_size, num_q_heads, (uint64_t)total_q, g, kPreRows / g) ||
          !encode_map(&tm_o, out, head_size, num_q_heads, (uint64_t)total_q, g, kPreRows / g) ||
-         !encode_map(&tm_k3, k_cache, head_size, num_kv_heads,
-                     (uint64_t)num_blocks * block_size, 1, kBlockSize)))
+         !encode_map(&tm_k3, k_pre, head_size, num_kv_heads, (uint64_t)blocks_pre * block_size, 1,
+                     kBlockSize)))
+        return UA_ERR_CUDA;
+    if (!plan.tiles.empty() && dq && !pair_prefill &&
+        !encode_decode_maps(&tm_kpre_unused, &tm_vpre, k_pre, v_pre, head_size, num_kv_heads,
+                            (uint64_t)blocks_pre, 2, 1))
         return UA_ERR_CUDA;
     if (!plan.tiles.empty() && pair_prefill &&
-        !encode_page_map(&tm_vh, v_cache, head_size, num_kv_heads, (uint64_t)num_blocks, 2, 1, 1))
+        !encode_page_map(&tm_vh, v_pre, head_size, num_kv_heads, (uint64_t)blocks_pre, 2, 1, 1))
         return UA_ERR_CUDA;
 
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
     const bool prof = g_profile;
     if (prof && !ds->events) {
         for (int c = 0; c < UA_PROFILE_RING; ++c)
@@ -759,15 +775,24 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
     }
     mark(2);
     if (!plan.tiles.empty()) {
+        if (dq) {
+            e = launch_dequant_pages(k_cache, v_cache, block_table, block_table_stride, num_blocks,
+                                     reinterpret_cast<const int32_t *>(pl + L.off_dq),
+                                     (int32_t)plan.dq_seq.size(), plan.dq_pages,
+                                     reinterpret_cast<int32_t *>(ws + L.off_dq_bt), ws + L.off_dq_k,
+                                     ws + L.off_dq_v, num_kv_heads, head_size, ds->status, stream);
+            if (e != cudaSuccess) return UA_ERR_CUDA;
+        }
         PrefillParams pp{};
-        pp.k_cache = static_cast<const __nv_bfloat16 *>(k_cache);
+        pp.k_cache = static_cast<const __nv_bfloat16 *>(k_pre);
         pp.out = static_cast<__nv_bfloat16 *>(out);
         pp.lse = lse;
         pp.cu = cu_seqlens_q;
         pp.seqused_k = seqused_k;
-        pp.block_table = block_table;
+        pp.block_table = bt_pre;
         pp.bt_stride = block_table_stride;
-        pp.num_blocks = num_blocks;
+        pp.num_blocks = (int32_t)blocks_pre;
+        pp.v_scale = v_scale;
         pp.hq = num_q_heads;
         pp.hkv = num_kv_heads;
         pp.g = g;
@@ -779,7 +804,7 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
         pp.n_tiles = (int32_t)plan.tiles.size();
         pp.status = ds->status;
         e = pair_prefill ? launch_prefill_pair(pp, tm_q, tm_o, tm_k3, tm_vh, plan.pre_ctas, stream)
-                         : launch_prefill(head_size, plan.pre_claimed, pp, tm_q, tm_o, tm_k3, tm_vp,
+                         : launch_prefill(head_size, plan.pre_claimed, pp, tm_q, tm_o, tm_k3, tm_vpre,
                                           plan.pre_ctas, stream);
         if (e != cudaSuccess) return UA_ERR_CUDA;
     }
@@ -799,7 +824,7 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
         ds->ran[pslot][2] = false;
         ds->ran[pslot][3] = L.blob_bytes > 0;
         ds->launches[pslot][0] = plan.dec_ctas > 0 ? 1 : 0;
-        ds->launches[pslot][1] = plan.tiles.empty() ? 0 : 1;
+        ds->launches[pslot][1] = plan.tiles.empty() ? 0 : (dq ? 2 : 1);   // page decode + prefill
         ds->launches[pslot][2] = 0;
         ds->launches[pslot][3] = 0;
         ++ds->calls;
@@ -1100,6 +1125,7 @@ static ua_status run_attention_device_plan(
         pp.tiles = reinterpret_cast<const PreTile *>(ws + L.off_tiles);
         pp.tile_begin = reinterpret_cast<const int32_t *>(ws + L.off_pre_begin);
         pp.n_tiles = L.cap_items;
+        pp.v_scale = v_scale;
         pp.status = ds->status;
         const cudaError_t pe =
             shape.pre_pair ? launch_prefill_pair(pp, tm_q, tm_o, tm_k3, tm_vh, shape.pre_workers, stream)

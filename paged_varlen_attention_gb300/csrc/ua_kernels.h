@@ -57,6 +57,7 @@ struct PrefillParams {
     const int32_t *tile_begin;   // dealt: [ctas + 1], CTA c runs tiles [tile_begin[c], tile_begin[c+1])
     int32_t *sched;              // claimed: [kSchedInts] next unclaimed item, CTAs done, item count
     int32_t n_tiles;
+    float v_scale;               // output scale (an e4m3 cache's V scale; 1 for bf16)
     int *status;
 };
 
@@ -151,5 +152,14 @@ cudaError_t launch_kv_append(const void *k_new, const void *v_new, const int32_t
 // [0, num_blocks)).  ua_pages.cu.
 cudaError_t launch_expand_block_table(const int32_t *block_table, int32_t *out, int64_t entries,
                                       int32_t r, int32_t num_blocks, cudaStream_t stream);
+
+// An e4m3 cache's pages for the prefill kernels: decoded page t belongs to
+// sequence dq[n_dq + 1 + j] for the last j with dq[j] <= t (page t - dq[j] of
+// it); its K and V (16 slots x Hkv x d e4m3 bytes each) are written as bf16
+// into k16 / v16 at page t, and dq_bt[seq][page] = t.  ua_pages.cu.
+cudaError_t launch_dequant_pages(const void *k8, const void *v8, const int32_t *block_table,
+                                 int32_t bt_stride, int32_t num_blocks, const int32_t *dq, int32_t n_dq,
+                                 int64_t dq_pages, int32_t *dq_bt, void *k16, void *v16, int32_t num_kv_heads,
+                                 int32_t head_size, int *status, cudaStream_t stream);
 
 }  // namespace ua

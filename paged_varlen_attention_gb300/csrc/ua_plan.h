@@ -123,6 +123,8 @@ struct Problem {
     int32_t kv_heads_per_unit = 1;   // decode units: 1, or 2 (adjacent heads, <= 8 rows each)
     bool prefill_claim = false;      // long prefill items may be claimed as the CTAs go
     bool prefill_pair = false;       // long prefill items may run on SM pairs (two-SM kernel)
+    bool dequant_prefill = false;    // e4m3 cache: the prefill rows' pages are decoded to bf16
+                                     // in the workspace first (the plan lays that region out)
 };
 
 // Offsets of the plan sections inside the device workspace.
@@ -134,10 +136,15 @@ struct Layout {
     size_t off_tiles;      // PreTile [n_tiles]
     size_t off_pre_begin;  // int32 [pre_ctas + 1] (items dealt in advance)
     size_t off_sched;      // int32 [kSchedInts] (items claimed as the CTAs go)
+    size_t off_dq;         // int32 [n_dq + 1] first decoded page of each prefill sequence,
+                           // then int32 [n_dq] the sequences (e4m3 cache only)
     size_t blob_bytes;     // bytes copied host -> device per call (offsets above are
                            // from the start of the workspace)
     size_t off_part_o;     // float [n_slots][kDecRows][d]
     size_t off_part_ml;    // float [n_slots][kDecRows][2]
+    size_t off_dq_bt;      // int32 [num_seqs][bt_stride]: block table of the decoded pages
+    size_t off_dq_k;       // bf16 [dq_pages][16][Hkv][d]: the prefill sequences' K pages
+    size_t off_dq_v;       // bf16 [dq_pages][16][Hkv][d]: and V pages
     size_t total_bytes;    // workspace bytes
 };
 

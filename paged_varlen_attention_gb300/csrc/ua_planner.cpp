@@ -258,6 +258,26 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
         }
     }
 
+    // ---- e4m3 cache: the pages the prefill items read, decoded to bf16 in the
+    // workspace (a sequence's items all see its context up to the end of it,
+    // so its whole context is decoded, once)
+    plan.dq_seq.clear();
+    plan.dq_base.clear();
+    plan.dq_pages = 0;
+    if (p.dequant_prefill && !plan.tiles.empty()) {
+        thread_local std::vector<uint8_t> tl_has;
+        std::vector<uint8_t> &has = tl_has;
+        has.assign((size_t)p.num_seqs, 0);
+        for (const PreTile &t : plan.tiles) has[(size_t)t.seq] = 1;
+        for (int32_t s = 0; s < p.num_seqs; ++s) {
+            if (!has[(size_t)s]) continue;
+            plan.dq_seq.push_back(s);
+            plan.dq_base.push_back((int32_t)plan.dq_pages);
+            plan.dq_pages += (p.lk[s] + kBlockSize - 1) / kBlockSize;
+        }
+        plan.dq_base.push_back((int32_t)plan.dq_pages);
+    }
+
     // ---- workspace layout
     Layout &L = plan.layout;
     size_t off = 0;
@@ -275,11 +295,21 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
     off = align_up(off + sizeof(int32_t) * plan.pre_begin.size(), kAlign);
     L.off_sched = off;
     off = align_up(off + sizeof(int32_t) * kSchedInts, kAlign);
+    L.off_dq = off;
+    off = align_up(off + sizeof(int32_t) * (plan.dq_base.size() + plan.dq_seq.size()), kAlign);
     L.blob_bytes = off;
     L.off_part_o = off;
     off = align_up(off + sizeof(float) * (size_t)plan.n_slots * kDecRows * kernel_head_size(p.d), kAlign);
     L.off_part_ml = off;
     off = align_up(off + 2 * sizeof(float) * (size_t)plan.n_slots * kDecRows, kAlign);
+    const bool dq = plan.dq_pages > 0;
+    const size_t dq_page_bytes = (size_t)kBlockSize * (size_t)p.hkv * (size_t)p.d * 2;
+    L.off_dq_bt = off;
+    off = align_up(off + (dq ? sizeof(int32_t) * (size_t)p.num_seqs * (size_t)p.bt_stride : 0), kAlign);
+    L.off_dq_k = off;
+    off = align_up(off + (size_t)plan.dq_pages * dq_page_bytes, kAlign);
+    L.off_dq_v = off;
+    off = align_up(off + (size_t)plan.dq_pages * dq_page_bytes, kAlign);
     L.total_bytes = (plan.pieces.empty() && plan.tiles.empty()) ? 0 : off;
 }
 
@@ -298,6 +328,11 @@ void serialize_plan_to(const Plan &plan, uint8_t *dst) {
         std::memcpy(dst + L.off_pre_begin, plan.pre_begin.data(), sizeof(int32_t) * plan.pre_begin.size());
     const int32_t sched[kSchedInts] = {0, 0, (int32_t)plan.tiles.size(), 0};
     std::memcpy(dst + L.off_sched, sched, sizeof(sched));
+    if (!plan.dq_base.empty()) {
+        std::memcpy(dst + L.off_dq, plan.dq_base.data(), sizeof(int32_t) * plan.dq_base.size());
+        std::memcpy(dst + L.off_dq + sizeof(int32_t) * plan.dq_base.size(), plan.dq_seq.data(),
+                    sizeof(int32_t) * plan.dq_seq.size());
+    }
 }
 
 void serialize_plan(const Plan &plan, std::vector<uint8_t> &blob) {

@@ -20,6 +20,12 @@ struct Plan {
     int32_t pre_ctas = 0;               // prefill workers: CTAs, or CTA pairs (pre_pair)
     bool pre_claimed = false;           // the prefill CTAs claim items from the list as they go
     bool pre_pair = false;              // the items are dealt to SM pairs (two-SM kernel)
+    // e4m3 cache (Problem::dequant_prefill): the sequences with prefill items, in
+    // order, and the first of their pages in the decoded bf16 copy (n_dq + 1
+    // entries); each sequence's whole context is decoded
+    std::vector<int32_t> dq_seq;
+    std::vector<int32_t> dq_base;
+    int64_t dq_pages = 0;
     Layout layout{};
 };
 

@@ -801,7 +801,7 @@ __global__ void __launch_bounds__(PreCfg<D>::kThreads, 1)
             // out.  A tile that ends before 128 rows (the last of its sequence)
             // copies its rows out by hand instead, as the box would run into the
             // next sequence's rows.
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = l > 0.f ? p.v_scale / l : 0.f;
             if (p.lse != nullptr && valid)
                 p.lse[(int64_t)(pi.q0 + i) * p.hq + pi.kvh * p.g + pr % p.g] = row_lse(m_run, l);
             const bool leader = quarter == 0 && lane == 0;

@@ -679,7 +679,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             xl[h * kPreRows + r] = l;
             named_barrier_sync(qbar, 64);
             const float lt = l + xl[(1 - h) * kPreRows + r];
-            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            const float inv = lt > 0.f ? p.v_scale / lt : 0.f;
             if (p.lse != nullptr && valid && h == 0)
                 p.lse[(int64_t)(it.q0 + i) * p.hq + it.kvh * p.g + pr % p.g] = row_lse(m_run, lt);
             const bool leader = warp == 0 && lane == 0;

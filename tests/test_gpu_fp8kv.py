@@ -8,7 +8,9 @@ k = k_scale * e4m3(byte), v = v_scale * e4m3(byte).  The kernel widens the
 bytes to f16 (exact) and multiplies with f16 Q and P; the tolerance is the
 one of the bf16 path (max 2e-2, mean 1e-3), the normaliser within 2e-3.
 With Hkv even a decode unit holds two adjacent kv heads (tile rows 0-7 and
-8-15); the odd-Hkv cases run one head per unit."""
+8-15); the odd-Hkv cases run one head per unit.  Rows of more than 16 packed
+rows run in the tensor-core prefill kernels over a decoded bf16 copy of their
+pages (tests/test_gpu_fp8kv_prefill.py covers that path in detail)."""
 import zlib
 
 import numpy as np
@@ -59,7 +61,7 @@ def run_fp8(b, k8, v8, lse=False):
 CASES = [
     # q_lens, k_lens, Hq, Hkv, causal
     ([1] * 8, [17, 40, 2048, 3000, 1, 16, 700, 5000], 32, 8, True),    # decode, split units
-    ([1, 5, 40, 1], [100, 40, 300, 4096], 8, 2, True),                 # prefill rows -> decode kernel
+    ([1, 5, 40, 1], [100, 40, 300, 4096], 8, 2, True),                 # prefill rows beside decode rows
     ([3, 2, 17], [5, 30, 17], 16, 4, False),                            # non-causal
     ([1, 1, 1], [2, 3, 1], 4, 4, True),                                 # G = 1
     # units of two adjacent kv heads need Hkv even; odd Hkv keeps one head per unit
