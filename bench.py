@@ -42,7 +42,8 @@ headline batch planned on the GPU, one CUDA-graph replay per step; its line
 also times a model step of 32 layers' calls sharing one plan);
 gemma2_9b_decode_64x2k-4k (the headline lengths with head size 256: Hq 16,
 Hkv 8); phi3_mini_decode_64x2k-4k (the same lengths with head size 96:
-Hq = Hkv = 32).
+Hq = Hkv = 32); gemma2_9b_prefill_16x1000 (the 16 x 1000-token prompts with
+head size 256: Hq 16, Hkv 8).
 --block-size runs a standard batch over pages of 32 ... 256 tokens (same
 lengths and data recipe; the call then also expands the block table).
 
@@ -81,6 +82,7 @@ WORKLOADS = {
     "llama3_70b_long_mixed_32x8k-32k_2x2048chunk": 5,
     "gemma2_9b_decode_64x2k-4k": 6,
     "phi3_mini_decode_64x2k-4k": 7,
+    "gemma2_9b_prefill_16x1000": 8,
 }
 DEFAULT_WORKLOAD = "llama3_70b_long_mixed_32x8k-32k_2x2048chunk"
 # the other standard batches the default run also measures (one line, per_config)
@@ -597,7 +599,8 @@ def dominant_roofline(workload, spec, work, kern, peaks):
     pre = statistics.mean(kern["prefill"]) if kern["prefill"] else None
     if pre is not None and (dec is None or pre > dec):
         achieved = work["prefill_flops"] / (pre / 1e3) / 1e12
-        roof = {"kernel": "ua_prefill_kernel", "bound": "tensor", "achieved": achieved,
+        roof = {"kernel": "ua_prefill_kernel / ua_prefill_pair_kernel (as the planner routes)",
+                "bound": "tensor", "achieved": achieved,
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"],
                 "traffic": ncu_traffic("prefill", workload) if spec.block_size == 16 else None,

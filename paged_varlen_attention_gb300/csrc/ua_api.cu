@@ -355,8 +355,11 @@ static ua_status refuse_capture(cudaStream_t stream) {
     return cs == cudaStreamCaptureStatusNone ? UA_OK : UA_ERR_UNSUPPORTED;
 }
 
-// Whether the head-size-128 prefill rows of this call may run on SM pairs.
-static bool use_pair_prefill(int32_t head_size) { return kPairPrefill && head_size == 128; }
+// Whether the prefill rows of this call may run on SM pairs: head size 128
+// (long items), 256 (every item: the one-SM kernel is built for 64 and 128).
+static bool use_pair_prefill(int32_t head_size) {
+    return kPairPrefill && (head_size == 128 || head_size == 256);
+}
 
 // The prefill scheduling options of a call: long items on SM pairs
 // (two-SM kernel, head size 128), or else claimed by the one-SM CTAs as they
@@ -696,7 +699,7 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
                             (uint64_t)blocks_pre, 2, 1))
         return UA_ERR_CUDA;
     if (!plan.tiles.empty() && pair_prefill &&
-        !encode_page_map(&tm_vh, v_pre, head_size, num_kv_heads, (uint64_t)blocks_pre, 2, 1, 1))
+        !encode_page_map(&tm_vh, v_pre, head_size, num_kv_heads, (uint64_t)blocks_pre, 2, 1, head_size / 128))
         return UA_ERR_CUDA;
 
     const bool prof = g_profile;
@@ -803,7 +806,7 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
         pp.sched = reinterpret_cast<int32_t *>(pl + L.off_sched);
         pp.n_tiles = (int32_t)plan.tiles.size();
         pp.status = ds->status;
-        e = pair_prefill ? launch_prefill_pair(pp, tm_q, tm_o, tm_k3, tm_vh, plan.pre_ctas, stream)
+        e = pair_prefill ? launch_prefill_pair(head_size, pp, tm_q, tm_o, tm_k3, tm_vh, plan.pre_ctas, stream)
                          : launch_prefill(head_size, plan.pre_claimed, pp, tm_q, tm_o, tm_k3, tm_vpre,
                                           plan.pre_ctas, stream);
         if (e != cudaSuccess) return UA_ERR_CUDA;
@@ -1048,7 +1051,8 @@ static ua_status run_attention_device_plan(
                             (uint64_t)num_blocks, eb, shape.hpu))
         return UA_ERR_CUDA;
     if (shape.prefill_ok && shape.pre_pair &&
-        !encode_page_map(&tm_vh, v_cache, head_size, num_kv_heads, (uint64_t)num_blocks, 2, 1, 1))
+        !encode_page_map(&tm_vh, v_cache, head_size, num_kv_heads, (uint64_t)num_blocks, 2, 1,
+                         std::max(head_size / 128, 1)))
         return UA_ERR_CUDA;
     if (shape.prefill_ok &&
         (!encode_map(&tm_q, q, head_size, num_q_heads, (uint64_t)max_total_q, g, kPreRows / g) ||
@@ -1128,7 +1132,7 @@ static ua_status run_attention_device_plan(
         pp.v_scale = v_scale;
         pp.status = ds->status;
         const cudaError_t pe =
-            shape.pre_pair ? launch_prefill_pair(pp, tm_q, tm_o, tm_k3, tm_vh, shape.pre_workers, stream)
+            shape.pre_pair ? launch_prefill_pair(head_size, pp, tm_q, tm_o, tm_k3, tm_vh, shape.pre_workers, stream)
                            : launch_prefill(head_size, /*claimed=*/false, pp, tm_q, tm_o, tm_k3, tm_vp,
                                             shape.num_sms, stream);
         if (pe != cudaSuccess) return UA_ERR_CUDA;

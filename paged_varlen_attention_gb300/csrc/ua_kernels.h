@@ -72,10 +72,11 @@ cudaError_t launch_decode(int d, bool kv8, const DecodeParams &p, const CUtensor
 cudaError_t launch_prefill(int d, bool claimed, const PrefillParams &p, const CUtensorMap &tm_q,
                            const CUtensorMap &tm_o, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                            int ctas, cudaStream_t stream);
-// The two-SM prefill kernel (ua_prefill_pair.cu), head size 128: `pairs`
-// clusters of two CTAs, pair c running tiles [tile_begin[c], tile_begin[c+1]).
-// tm_vh: the page view of the V cache with one 64-column chunk per box.
-cudaError_t launch_prefill_pair(const PrefillParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_o,
+// The two-SM prefill kernel (ua_prefill_pair.cu), head size d = 128 or 256:
+// `pairs` clusters of two CTAs, pair c running tiles [tile_begin[c],
+// tile_begin[c+1]).  tm_vh: the page view of the V cache with d / 128
+// 64-column chunks per box (the half of a page's columns one SM holds).
+cudaError_t launch_prefill_pair(int d, const PrefillParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_o,
                                 const CUtensorMap &tm_k, const CUtensorMap &tm_vh, int pairs,
                                 cudaStream_t stream);
 

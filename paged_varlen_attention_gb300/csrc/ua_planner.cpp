@@ -18,8 +18,10 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool prefill_supports(const Problem &p) {
     const int g = p.hq / p.hkv;
-    // the tensor-core kernels are built for head sizes 64 and 128
-    return (p.d == 64 || p.d == 128) && g >= 1 && g <= kPreRows && (kPreRows % g) == 0;
+    // the one-SM tensor-core kernel is built for head sizes 64 and 128, the
+    // two-SM kernel for 128 and 256
+    return (p.d == 64 || p.d == 128 || (p.d == 256 && p.prefill_pair)) && g >= 1 && g <= kPreRows &&
+           (kPreRows % g) == 0;
 }
 
 int validate_problem(const Problem &p) {
@@ -155,7 +157,8 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
         for (const PreTile &t : unsorted) sorted[(size_t)counts[(size_t)(max_kv - t.kv_tiles)]++] = t;
 
         const bool long_items = kv_sum >= (int64_t)kClaimMinMeanKvTiles * (int64_t)sorted.size();
-        plan.pre_pair = p.prefill_pair && long_items;
+        // head size 256 has only the two-SM kernel: every item goes to SM pairs
+        plan.pre_pair = p.prefill_pair && (long_items || p.d == 256);
         const int32_t workers = plan.pre_pair ? std::max(num_sms / 2, 1) : std::max(num_sms, 1);
         const int32_t ctas = (int32_t)std::min<size_t>(sorted.size(), (size_t)workers);
         plan.pre_ctas = ctas;

@@ -63,22 +63,37 @@
 namespace ua {
 namespace {
 
-constexpr int kD = 128;                          // head size of this kernel
 constexpr int kPStep = 128;                      // keys per KV step
 constexpr int kPStepPages = kPStep / kBlockSize; // 8
 constexpr int kPHalfPages = kPStepPages / 2;     // K pages per CTA per step
-constexpr int kPStages = 3;                      // K / V stages = score buffers
 constexpr int kPThreads = 384;                   // 12 warps
-constexpr int kPQBytes = kPreRows * kD * 2;      // one 128-row Q tile
-constexpr int kPKBytes = (kPStep / 2) * kD * 2;  // 64 keys x 128 columns
-constexpr int kPVBytes = kPStep * 64 * 2;        // 128 keys x 64 columns
-constexpr int kPStgBytes = kPreRows * kD * 2;    // epilogue staging (two 64-column passes)
-constexpr uint32_t kColO = 3 * kPStep;           // O after the three score buffers
+constexpr int kPStgBytes = kPreRows * 128 * 2;   // epilogue staging: a 64-column slice per half
 constexpr int kPTmemCols = 512;
 constexpr float kPRescaleThreshold = 8.0f;       // log2 units
 constexpr int kPRedBytes = 2 * kPreRows * 4;      // row sums of the two halves at an item's end
-constexpr size_t kPSmemUsed = 1024 + 2 * (size_t)kPQBytes + kPStages * (size_t)(kPKBytes + kPVBytes) +
-                              kPStgBytes + 512 + kPRedBytes;
+
+// Sizes by head size.  Per SM: Q is this CTA's 128 rows x D, a K stage its 64
+// of the step's 128 keys x D, a V stage all 128 keys x its D / 2 columns (the
+// B operand of P V is split by N = D), and TMEM holds the score buffers (128
+// columns each) and O (D columns).  D = 256 fits 512 TMEM columns and 227 KB
+// of shared memory with two stages and one Q tile.
+template <int D>
+struct PairCfg {
+    static_assert(D == 128 || D == 256, "head sizes 128 and 256");
+    static constexpr int kChunks = D / 64;                   // 64-column chunks of a Q / K row
+    static constexpr int kHalfChunks = D / 128;              // of the D / 2 columns of V and O a half holds
+    static constexpr int kStages = D == 128 ? 3 : 2;         // K / V stages = score buffers
+    static constexpr int kQBufs = D == 128 ? 2 : 1;          // Q tiles (two: the next item's S starts early)
+    static constexpr int kQBytes = kPreRows * D * 2;
+    static constexpr int kKBytes = (kPStep / 2) * D * 2;
+    static constexpr int kVPage = kBlockSize * (D / 2) * 2;  // one page of this SM's V columns
+    static constexpr int kVBytes = kPStepPages * kVPage;
+    static constexpr uint32_t kColO = kStages * kPStep;      // O after the score buffers
+    static_assert(kColO + D <= (uint32_t)kPTmemCols, "TMEM: score buffers + O");
+    static constexpr size_t kSmemUsed = 1024 + kQBufs * (size_t)kQBytes +
+                                        kStages * (size_t)(kKBytes + kVBytes) + kPStgBytes + 512 + kPRedBytes;
+    static_assert(kSmemUsed <= 232448, "dynamic shared memory above 227 KB");
+};
 
 enum : int {
     bQFull = 0,     // [2] this CTA's Q tile landed (TMA tx)
@@ -202,31 +217,33 @@ __device__ __forceinline__ void umma_local_commit(uint32_t bar) {
 
 // Rows [r_lo, r_hi) of a staged 64-column slice of O (row r at r * 128 bytes,
 // 16-byte pieces XOR-ed with r % 8) to out, by the tile's 128 threads.
+template <int D>
 __device__ __noinline__ void pair_copy_rows(__nv_bfloat16 *out, const uint8_t *stg, int tid, int nrows,
                                             int row0, int q0, int kvh, int g, int hq, int col0) {
     for (int u = tid; u < nrows * 8; u += 128) {
         const int row = u >> 3, piece = u & 7;
         const uint4 val = *reinterpret_cast<const uint4 *>(stg + row * 128 + ((piece ^ (row & 7)) << 4));
         const int prr = row0 + row;
-        *reinterpret_cast<uint4 *>(out + ((int64_t)(q0 + prr / g) * hq + kvh * g + prr % g) * kD + col0 +
+        *reinterpret_cast<uint4 *>(out + ((int64_t)(q0 + prr / g) * hq + kvh * g + prr % g) * D + col0 +
                                    8 * piece) = val;
     }
 }
 
 }  // namespace
 
-template <bool kPos>
+template <bool kPos, int D>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     ua_prefill_pair_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_vh) {
+    using C = PairCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t sq = smem_u32(smem);                              // Q[2]: [chunk][128 rows][64]
-    const uint32_t sk = sq + 2 * kPQBytes;                           // K[3]: [chunk][64 keys][64]
-    const uint32_t sv = sk + kPStages * kPKBytes;                    // V[3]: [page][16 keys][64]
-    uint8_t *sv_ptr = smem + 2 * kPQBytes + kPStages * kPKBytes;
-    uint8_t *stage_ptr = sv_ptr + kPStages * kPVBytes;               // [chunk][128 rows][64] bf16
+    const uint32_t sq = smem_u32(smem);                              // Q[kQBufs]: [chunk][128 rows][64]
+    const uint32_t sk = sq + C::kQBufs * C::kQBytes;                 // K[kStages]: [chunk][64 keys][64]
+    const uint32_t sv = sk + C::kStages * C::kKBytes;                // V[kStages]: [page][chunk][16 keys][64]
+    uint8_t *sv_ptr = smem + C::kQBufs * C::kQBytes + C::kStages * C::kKBytes;
+    uint8_t *stage_ptr = sv_ptr + C::kStages * C::kVBytes;           // [half][128 rows][64] bf16
     const uint32_t sstage = smem_u32(stage_ptr);
     uint64_t *bars = reinterpret_cast<uint64_t *>(stage_ptr + kPStgBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kPNumBars + 1);
@@ -250,7 +267,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             mbar_init(bar(bQEmpty + i), 1);
             mbar_init(bar(bQPeer + i), 1);
         }
-        for (int i = 0; i < kPStages; ++i) {
+        for (int i = 0; i < C::kStages; ++i) {
             mbar_init(bar(bKFull + i), 1);
             mbar_init(bar(bKEmpty + i), 1);
             mbar_init(bar(bKPeer + i), 1);
@@ -290,15 +307,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             const PairItem it = make_item(p, t, rank);
             int good = 1;
             if (lane == 0) {
-                const uint32_t qb = k & 1;
-                // buffer qb is free once the last S of item k - 2 is done
-                if (k >= 2 && !mbar_wait(bar(bQEmpty + qb), ((k >> 1) - 1) & 1, p.status)) {
+                const uint32_t qb = k % C::kQBufs;
+                // buffer qb is free once the last S of item k - kQBufs is done
+                if (k >= (uint32_t)C::kQBufs &&
+                    !mbar_wait(bar(bQEmpty + qb), ((k / C::kQBufs) - 1) & 1, p.status)) {
                     good = 0;
                 } else {
-                    mbar_arrive_expect_tx(bar(bQFull + qb), kPQBytes);
+                    mbar_arrive_expect_tx(bar(bQFull + qb), C::kQBytes);
 #pragma unroll
-                    for (int c = 0; c < 2; ++c)
-                        tma_load_3d(sq + qb * kPQBytes + c * (kPreRows * 128), &tm_q, c * 64, it.kvh * p.g,
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(sq + qb * C::kQBytes + c * (kPreRows * 128), &tm_q, c * 64, it.kvh * p.g,
                                     it.q0 + it.my_row0 / p.g, bar(bQFull + qb));
                     ++q_issued;
                 }
@@ -313,18 +331,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                 int b[kPHalfPages];
 #pragma unroll
                 for (int i = 0; i < kPHalfPages; ++i) b[i] = __shfl_sync(0xffffffffu, bid, i);
-                const uint32_t s = e % kPStages, ph = (e / kPStages) & 1;
+                const uint32_t s = e % C::kStages, ph = (e / C::kStages) & 1;
                 good = 1;
                 if (lane == 0) {
                     if (!mbar_wait(bar(bKEmpty + s), ph ^ 1, p.status)) {
                         good = 0;
                     } else {
-                        mbar_arrive_expect_tx(bar(bKFull + s), kPKBytes);
+                        mbar_arrive_expect_tx(bar(bKFull + s), C::kKBytes);
 #pragma unroll
                         for (int i = 0; i < kPHalfPages; ++i)
 #pragma unroll
-                            for (int c = 0; c < 2; ++c)
-                                tma_load_3d_hint(sk + s * kPKBytes + c * (kPKBytes / 2) + i * 2048, &tm_k, c * 64,
+                            for (int c = 0; c < C::kChunks; ++c)
+                                tma_load_3d_hint(sk + s * C::kKBytes + c * 8192 + i * 2048, &tm_k, c * 64,
                                                  it.kvh, b[i] * kBlockSize, bar(bKFull + s), pol_kv);
                         ++k_issued;
                     }
@@ -334,10 +352,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         }
         // drain: the last loads issued land before the CTA can exit
         if (lane == 0) {
-            for (uint32_t x = (k_issued > (uint32_t)kPStages ? k_issued - kPStages : 0); x < k_issued; ++x)
-                mbar_wait(bar(bKFull + x % kPStages), (x / kPStages) & 1, p.status);
-            for (uint32_t x = (q_issued > 2u ? q_issued - 2 : 0); x < q_issued; ++x)
-                mbar_wait(bar(bQFull + (x & 1)), (x >> 1) & 1, p.status);
+            for (uint32_t x = (k_issued > (uint32_t)C::kStages ? k_issued - C::kStages : 0); x < k_issued; ++x)
+                mbar_wait(bar(bKFull + x % C::kStages), (x / C::kStages) & 1, p.status);
+            for (uint32_t x = (q_issued > (uint32_t)C::kQBufs ? q_issued - C::kQBufs : 0); x < q_issued; ++x)
+                mbar_wait(bar(bQFull + x % C::kQBufs), (x / C::kQBufs) & 1, p.status);
         }
     } else if (warp == 10) {
         // ================================================================ V producer
@@ -359,7 +377,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                 int b[kPStepPages];
 #pragma unroll
                 for (int i = 0; i < kPStepPages; ++i) b[i] = __shfl_sync(0xffffffffu, bid, i);
-                const uint32_t s = e % kPStages, ph = (e / kPStages) & 1;
+                const uint32_t s = e % C::kStages, ph = (e / C::kStages) & 1;
                 const bool tail = (j == tail_step);
                 const uint32_t land = tail ? bar(bVTail) : bar(bVFull + s);
                 int good = 1;
@@ -367,11 +385,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                     if (!mbar_wait(bar(bVEmpty + s), ph ^ 1, p.status)) {
                         good = 0;
                     } else {
-                        mbar_arrive_expect_tx(land, kPVBytes);
+                        mbar_arrive_expect_tx(land, C::kVBytes);
 #pragma unroll
                         for (int i = 0; i < kPStepPages; ++i)
-                            tma_load_5d_hint(sv + s * kPVBytes + i * 2048, &tm_vh, 0, 0, (int)rank, it.kvh, b[i],
-                                             land, pol_kv);
+                            tma_load_5d_hint(sv + s * C::kVBytes + i * C::kVPage, &tm_vh, 0, 0,
+                                             (int)rank * C::kHalfChunks, it.kvh, b[i], land, pol_kv);
                         ++v_issued;
                     }
                 }
@@ -386,11 +404,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                     } else {
                         const int k0 = it.lk - j * kPStep;                       // first key to clear
                         const int k1 = last_page_start + kBlockSize - j * kPStep;  // end of the page
-                        for (int u = lane; u < (k1 - k0) * 8; u += 32) {
-                            const int key = k0 + (u >> 3);
+                        for (int u = lane; u < (k1 - k0) * 8 * C::kHalfChunks; u += 32) {
                             const int piece = u & 7;
-                            *reinterpret_cast<uint4 *>(sv_ptr + s * kPVBytes + (key / kBlockSize) * 2048 +
-                                                       (key % kBlockSize) * 128 + piece * 16) = make_uint4(0, 0, 0, 0);
+                            const int cc = (u >> 3) % C::kHalfChunks;            // this SM's 64-column chunk
+                            const int key = k0 + (u >> 3) / C::kHalfChunks;
+                            *reinterpret_cast<uint4 *>(sv_ptr + s * C::kVBytes + (key / kBlockSize) * C::kVPage +
+                                                       cc * 2048 + (key % kBlockSize) * 128 + piece * 16) =
+                                make_uint4(0, 0, 0, 0);
                         }
                         fence_proxy_async_smem();
                         __syncwarp();
@@ -400,8 +420,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             }
         }
         if (lane == 0) {
-            for (uint32_t x = (v_issued > (uint32_t)kPStages ? v_issued - kPStages : 0); x < v_issued; ++x)
-                mbar_wait(bar(bVFull + x % kPStages), (x / kPStages) & 1, p.status);
+            for (uint32_t x = (v_issued > (uint32_t)C::kStages ? v_issued - C::kStages : 0); x < v_issued; ++x)
+                mbar_wait(bar(bVFull + x % C::kStages), (x / C::kStages) & 1, p.status);
         }
     } else if ((warp == 8 || warp == 11) && rank == 1) {
         // ================================================================ relays (peer CTA)
@@ -421,13 +441,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             PreTile t;
             for (uint32_t k = 0; ok && cur.next(p, t); ++k) {
                 const PairItem it = make_item(p, t, rank);
-                const uint32_t qb = k & 1;
+                const uint32_t qb = k % C::kQBufs;
                 if (qk) {
-                    if (!mbar_wait(bar(bQFull + qb), (k >> 1) & 1, p.status)) break;
+                    if (!mbar_wait(bar(bQFull + qb), (k / C::kQBufs) & 1, p.status)) break;
                     mbar_arrive_cluster_relaxed(lead_q + 8 * qb);
                 }
                 for (int j = 0; j < it.n; ++j, ++e) {
-                    const uint32_t s = e % kPStages, ph = (e / kPStages) & 1;
+                    const uint32_t s = e % C::kStages, ph = (e / C::kStages) & 1;
                     if (!mbar_wait(bar(full + s), ph, p.status)) {
                         ok = false;
                         break;
@@ -450,26 +470,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             PreTile t;
             for (uint32_t k = 0; ok && cur.next(p, t); ++k) {
                 const PairItem it = make_item(p, t, rank);
-                const uint32_t qb = k & 1, qph = (k >> 1) & 1;
+                const uint32_t qb = k % C::kQBufs, qph = (k / C::kQBufs) & 1;
                 if (!mbar_wait(bar(bQFull + qb), qph, p.status) ||
                     !mbar_wait_cluster(bar(bQPeer + qb), qph, p.status))
                     break;
-                const uint64_t qd = umma_desc_sw128(sq + qb * kPQBytes, 16, 1024);
+                const uint64_t qd = umma_desc_sw128(sq + qb * C::kQBytes, 16, 1024);
                 for (int j = 0; j < it.n; ++j, ++x) {
-                    const uint32_t b = x % kPStages, ph = (x / kPStages) & 1;
-                    if ((x >= (uint32_t)kPStages &&
-                         !mbar_wait(bar(bPvDone + b), ((x - kPStages) / kPStages) & 1, p.status)) ||
+                    const uint32_t b = x % C::kStages, ph = (x / C::kStages) & 1;
+                    if ((x >= (uint32_t)C::kStages &&
+                         !mbar_wait(bar(bPvDone + b), ((x - C::kStages) / C::kStages) & 1, p.status)) ||
                         !mbar_wait(bar(bKFull + b), ph, p.status) ||
                         !mbar_wait_cluster(bar(bKPeer + b), ph, p.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t kd = umma_desc_sw128(sk + b * kPKBytes, 16, 1024);
+                    const uint64_t kd = umma_desc_sw128(sk + b * C::kKBytes, 16, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < kD / 16; ++kk)
+                    for (int kk = 0; kk < D / 16; ++kk)
                         umma_pair_ss(tmem + b * kPStep, qd + (uint64_t)(((kk >> 2) * (kPreRows * 128) + (kk & 3) * 32) >> 4),
-                                     kd + (uint64_t)(((kk >> 2) * (kPKBytes / 2) + (kk & 3) * 32) >> 4), idesc_s,
+                                     kd + (uint64_t)(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), idesc_s,
                                      kk > 0 ? 1u : 0u);
                     umma_pair_commit(bar(bSFull + b));
                     umma_pair_commit(bar(bKEmpty + b));
@@ -490,7 +510,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         // written P(y) and both CTAs' V halves of the step have landed; an
         // item's first step starts O from zero.
         if (lane == 0) {
-            constexpr uint32_t idesc_pv = umma_idesc_bf16(2 * kPreRows, kD, 0, 1);
+            constexpr uint32_t idesc_pv = umma_idesc_bf16(2 * kPreRows, D, 0, 1);
             bool ok = true, issued_any = false;
             uint32_t y = 0;
             PairCursor cur(p, pair);
@@ -498,7 +518,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             while (ok && cur.next(p, t)) {
                 const PairItem it = make_item(p, t, rank);
                 for (int j = 0; j < it.n; ++j, ++y) {
-                    const uint32_t b = y % kPStages, ph = (y / kPStages) & 1;
+                    const uint32_t b = y % C::kStages, ph = (y / C::kStages) & 1;
                     if (!mbar_wait_cluster(bar(bPFull + b), ph, p.status) ||
                         !mbar_wait(bar(bVFull + b), ph, p.status) ||
                         !mbar_wait_cluster(bar(bVPeer + b), ph, p.status)) {
@@ -507,12 +527,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                     }
                     tc_fence_after();
                     // 16 keys per MMA = one page of V: P columns b*128 + kk*8 .. +8 (bf16
-                    // pairs); V page kk is [16 keys][64 columns], MN-major, 8-key groups 1 KB apart
-                    const uint64_t vd = umma_desc_sw128(sv + b * kPVBytes, 2048, 1024);
+                    // pairs); V page kk is [chunk][16 keys][64 columns], MN-major: this SM's
+                    // 64-column chunks 2 KB apart, 8-key groups 1 KB apart
+                    const uint64_t vd = umma_desc_sw128(sv + b * C::kVBytes, 2048, 1024);
 #pragma unroll
                     for (int kk = 0; kk < kPStepPages; ++kk)
-                        umma_pair_ts(tmem + kColO, tmem + b * kPStep + kk * 8, vd + (uint64_t)((kk * 2048) >> 4),
-                                     idesc_pv, (j == 0 && kk == 0) ? 0u : 1u);
+                        umma_pair_ts(tmem + C::kColO, tmem + b * kPStep + kk * 8,
+                                     vd + (uint64_t)((kk * C::kVPage) >> 4), idesc_pv,
+                                     (j == 0 && kk == 0) ? 0u : 1u);
                     umma_pair_commit(bar(bPvDone + b));
                     umma_pair_commit(bar(bVEmpty + b));
                     issued_any = true;
@@ -535,7 +557,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         const int r = q * 32 + lane;                    // row of the tile = TMEM lane
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         const uint32_t s_base = tmem + lane_off;
-        const uint32_t o_addr = s_base + kColO + 64 * h;
+        const uint32_t o_addr = s_base + C::kColO + (D / 2) * h;   // this half's O columns
         const uint32_t lead_p = mapa_shared(bar(bPFull), 0);
         const int qbar = 2 + q;                         // named barrier of the quarter's two warps
         bool ok = true;
@@ -551,7 +573,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             float m_run = -INFINITY;
             float l = 0.f;          // this half's share of the row sum
             for (int j = 0; j < it.n; ++j, ++y) {
-                const uint32_t b = y % kPStages, ph = (y / kPStages) & 1;
+                const uint32_t b = y % C::kStages, ph = (y / C::kStages) & 1;
                 if (!__all_sync(0xffffffffu, mbar_wait(bar(bSFull + b), ph, p.status))) {
                     ok = false;
                     break;
@@ -607,14 +629,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                     // max and rescale this half of O (after the P V of the previous step) and l
                     const float m_new = fmaxf(m_run, mx);
                     const float alpha = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run - m_new);
-                    const uint32_t pb = (y - 1) % kPStages, pph = ((y - 1) / kPStages) & 1;
+                    const uint32_t pb = (y - 1) % C::kStages, pph = ((y - 1) / C::kStages) & 1;
                     if (!__all_sync(0xffffffffu, mbar_wait(bar(bPvDone + pb), pph, p.status))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
+                    for (int c = 0; c < D / 64; ++c) {
                         uint32_t v[32];
                         tmem_ld32(o_addr + 32 * c, v);
 #pragma unroll
@@ -666,7 +688,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             // whose wait ran out must not leave the others at the barriers below.
             bool eok = ok;
             if (eok) {
-                const uint32_t lb = (y - 1) % kPStages, lph = ((y - 1) / kPStages) & 1;
+                const uint32_t lb = (y - 1) % C::kStages, lph = ((y - 1) / C::kStages) & 1;
                 eok = __all_sync(0xffffffffu, mbar_wait(bar(bPvDone + lb), lph, p.status));
             }
             ok = named_barrier_and(1, 256, eok);
@@ -683,37 +705,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             if (p.lse != nullptr && valid && h == 0)
                 p.lse[(int64_t)(it.q0 + i) * p.hq + it.kvh * p.g + pr % p.g] = row_lse(m_run, lt);
             const bool leader = warp == 0 && lane == 0;
-            // the previous item's stores have read the staging buffer
-            if (leader) bulk_wait_read_all();
-            named_barrier_sync(1, 256);
-            uint8_t *stg = stage_ptr + h * (kPreRows * 128);   // this half = one 64-column chunk
+            // O / l in passes of one 64-column chunk per half: each warp writes its
+            // rows of the chunk into its half of the staging buffer, then the
+            // leader stores both chunks (TMA), or each half copies its rows by hand
+            // for a tile that ends before 128 rows (a box would run into the next
+            // sequence's rows)
+#pragma unroll 1
+            for (int pass = 0; pass < C::kHalfChunks; ++pass) {
+                // the previous pass's (or item's) stores have read the staging buffer
+                if (leader) bulk_wait_read_all();
+                named_barrier_sync(1, 256);
+                uint8_t *stg = stage_ptr + h * (kPreRows * 128);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t v[32];
-                tmem_ld32(o_addr + 32 * c, v);
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(o_addr + 64 * pass + 32 * c, v);
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    *reinterpret_cast<uint4 *>(stg + r * 128 + (((4 * c + k) ^ (r & 7)) << 4)) = make_uint4(
-                        pack_bf16x2(__uint_as_float(v[8 * k]) * inv, __uint_as_float(v[8 * k + 1]) * inv),
-                        pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv),
-                        pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv),
-                        pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv));
-            }
-            fence_proxy_async_smem();
-            named_barrier_sync(1, 256);
-            if (it.my_nrows == kPreRows) {
-                if (leader) {
-#pragma unroll
-                    for (int c = 0; c < kD / 64; ++c)
-                        tma_store_3d(&tm_o, sstage + c * (kPreRows * 128), 64 * c, it.kvh * p.g,
-                                     it.q0 + it.my_row0 / p.g);
-                    bulk_commit_group();
+                    for (int k = 0; k < 4; ++k)
+                        *reinterpret_cast<uint4 *>(stg + r * 128 + (((4 * c + k) ^ (r & 7)) << 4)) = make_uint4(
+                            pack_bf16x2(__uint_as_float(v[8 * k]) * inv, __uint_as_float(v[8 * k + 1]) * inv),
+                            pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv),
+                            pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv),
+                            pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv));
                 }
-            } else if (it.my_nrows > 0) {
-                // a tile that ends before 128 rows: the box would run into the next
-                // sequence's rows, so its rows are copied out by hand (each half its chunk)
-                pair_copy_rows(p.out, stg, r, it.my_nrows, it.my_row0, it.q0, it.kvh, p.g, p.hq, 64 * h);
-                named_barrier_sync(1, 256);     // the buffer is free for the next item
+                fence_proxy_async_smem();
+                named_barrier_sync(1, 256);
+                if (it.my_nrows == kPreRows) {
+                    if (leader) {
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh)
+                            tma_store_3d(&tm_o, sstage + hh * (kPreRows * 128), 64 * (hh * C::kHalfChunks + pass),
+                                         it.kvh * p.g, it.q0 + it.my_row0 / p.g);
+                        bulk_commit_group();
+                    }
+                } else if (it.my_nrows > 0) {
+                    pair_copy_rows<D>(p.out, stg, r, it.my_nrows, it.my_row0, it.q0, it.kvh, p.g, p.hq,
+                                      64 * (h * C::kHalfChunks + pass));
+                    named_barrier_sync(1, 256);     // the buffer is free for the next pass
+                }
             }
             // O is read: the next item's first P V (which overwrites O) waits for this
             // CTA's P of that item, which comes after these loads
@@ -732,28 +761,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     cluster_sync_all();
 }
 
-template <bool kPos>
+template <bool kPos, int D>
 static cudaError_t launch_pair_t(const PrefillParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_o,
                                  const CUtensorMap &tm_k, const CUtensorMap &tm_vh, int pairs,
                                  cudaStream_t stream) {
+    using C = PairCfg<D>;
     static thread_local int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(ua_prefill_pair_kernel<kPos>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmemUsed);
+        cudaError_t e = cudaFuncSetAttribute(ua_prefill_pair_kernel<kPos, D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemUsed);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    ua_prefill_pair_kernel<kPos><<<2 * pairs, kPThreads, kPSmemUsed, stream>>>(p, tm_q, tm_o, tm_k, tm_vh);
+    ua_prefill_pair_kernel<kPos, D><<<2 * pairs, kPThreads, C::kSmemUsed, stream>>>(p, tm_q, tm_o, tm_k, tm_vh);
     return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_pair(const PrefillParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_o,
+cudaError_t launch_prefill_pair(int d, const PrefillParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_o,
                                 const CUtensorMap &tm_k, const CUtensorMap &tm_vh, int pairs,
                                 cudaStream_t stream) {
-    return p.scale_log2 > 0.f ? launch_pair_t<true>(p, tm_q, tm_o, tm_k, tm_vh, pairs, stream)
-                              : launch_pair_t<false>(p, tm_q, tm_o, tm_k, tm_vh, pairs, stream);
+    const bool pos = p.scale_log2 > 0.f;
+    switch (d) {
+        case 128:
+            return pos ? launch_pair_t<true, 128>(p, tm_q, tm_o, tm_k, tm_vh, pairs, stream)
+                       : launch_pair_t<false, 128>(p, tm_q, tm_o, tm_k, tm_vh, pairs, stream);
+        case 256:
+            return pos ? launch_pair_t<true, 256>(p, tm_q, tm_o, tm_k, tm_vh, pairs, stream)
+                       : launch_pair_t<false, 256>(p, tm_q, tm_o, tm_k, tm_vh, pairs, stream);
+        default:
+            return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace ua

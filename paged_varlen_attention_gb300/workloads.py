@@ -108,8 +108,8 @@ class Batch:
 
 
 # --------------------------------------------------------------------------
-# The five standard batches (index 1..5), a head-size-256 decode batch (6) and
-# a head-size-96 decode batch (7).
+# The five standard batches (index 1..5), a head-size-256 decode batch (6), a
+# head-size-96 decode batch (7) and a head-size-256 prefill batch (8).
 # --------------------------------------------------------------------------
 
 CONFIG_NAMES = {
@@ -120,6 +120,7 @@ CONFIG_NAMES = {
     5: "llama3_70b_long_mixed_32x8k-32k_2x2048chunk",
     6: "gemma2_9b_decode_64x2k-4k",
     7: "phi3_mini_decode_64x2k-4k",
+    8: "gemma2_9b_prefill_16x1000",
 }
 
 
@@ -162,6 +163,10 @@ def config_spec(idx: int) -> Spec:
         # head size 96, scale 1/sqrt(96))
         k = rng.integers(2048, 4096, size=64, endpoint=True)
         return Spec(name, np.ones(64, np.int32), k, 32, 32, 96,
+                    data_seed=data_seed, layout_seed=layout_seed)
+    if idx == 8:
+        # the 16 x 1000-token prompts with Gemma-2-9B's attention heads
+        return Spec(name, np.full(16, 1000), np.full(16, 1000), 16, 8, 256,
                     data_seed=data_seed, layout_seed=layout_seed)
     raise ValueError(f"unknown config {idx}")
 

@@ -132,5 +132,9 @@ def test_capacities_bound_the_plan_of_random_batches(lib, seed):
     assert counts["pieces"] <= cap_pieces
     assert counts["split_units"] <= cap_comb
     assert counts["slots"] <= cap_slots
-    assert counts["prefill_tiles"] <= cap_items
+    if d != 256:
+        # (head size 256: the host plan sends prefill rows to the two-SM kernel, which
+        # the device planner does not deal for; a device-planned call runs them in the
+        # decode kernel, so only the decode sections above are shared)
+        assert counts["prefill_tiles"] <= cap_items
     assert counts["prefill_ctas"] <= sms

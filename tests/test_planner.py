@@ -103,11 +103,12 @@ def check_plan(q_lens, k_lens, hq, hk, d=128, causal=True, num_sms=152):
     # worker's items come longest first, and dealing the longest-first list in
     # rounds of alternating direction keeps the workers' work within one item
     # of each other.  Workers are SMs, or pairs of SMs (the two-SM kernel) for
-    # long items (16 tiles of 128 keys or more on average) at head size 128
+    # long items (16 tiles of 128 keys or more on average) at head size 128 and
+    # for every item at head size 256
     ctas = [t[1] for t in tiles]
     assert [t[7] for t in tiles] == list(range(len(tiles)))
     long_items = bool(tiles) and sum(t[6] for t in tiles) >= 16 * len(tiles)
-    workers = max(1, num_sms // 2) if (d == 128 and long_items) else num_sms
+    workers = max(1, num_sms // 2) if ((d == 128 and long_items) or d == 256) else num_sms
     if tiles:
         assert ctas == sorted(ctas) and min(ctas) >= 0
         assert counts["prefill_ctas"] == len(set(ctas)) == min(len(tiles), workers)
@@ -181,9 +182,12 @@ def test_random_batches(d):
         hk = int(rng.choice([1, 2, 4, 8]))
         hq = hk * int(rng.choice([1, 2, 3, 4, 8, 16]))
         causal = bool(rng.integers(0, 2))     # k >= q: both modes are valid
-        c = check_plan(q, k, hq, hk, d, causal, int(rng.integers(1, 200)))
-        if d in (96, 256):
+        sms = int(rng.integers(1, 200))
+        c = check_plan(q, k, hq, hk, d, causal, sms)
+        if d == 96:
             assert c["prefill_tiles"] == 0       # decode units only
+        if d == 256 and c["prefill_tiles"] > 0:
+            assert c["prefill_ctas"] <= max(sms // 2, 1)   # SM pairs only
 
 
 def test_few_long_prefill_items_go_to_the_decode_kernel():
@@ -201,10 +205,13 @@ def test_few_long_prefill_items_go_to_the_decode_kernel():
 
 
 @pytest.mark.parametrize("causal", [True, False])
-def test_head_size_256_puts_every_row_in_decode_units(causal):
-    """Head size 256: the tensor-core prefill kernel is laid out for D <= 128,
-    so prefill and chunked-prefill rows become 16-row decode units too."""
-    c = check_plan([1, 300, 64, 1, 1000], [4000, 300, 2000, 17, 1000], 16, 8, 256, causal=causal)
-    assert c["prefill_tiles"] == 0 and c["prefill_ctas"] == 0
-    units = 8 * sum(-(-lq * 2 // 16) for lq in [1, 300, 64, 1, 1000])    # G = 2, Hkv = 8
-    assert c["dec_ctas"] > 0 and c["pieces"] >= units
+def test_head_size_256_prefill_items_go_to_sm_pairs(causal):
+    """Head size 256: the one-SM prefill kernel is laid out for D <= 128, so
+    every prefill item, long or short, is dealt to an SM pair (the two-SM
+    kernel holds O's 256 columns in TMEM); decode rows stay decode units."""
+    q = [1, 300, 64, 1, 1000]
+    c = check_plan(q, [4000, 300, 2000, 17, 1000], 16, 8, 256, causal=causal)
+    items = 8 * sum(-(-lq * 2 // 256) for lq in q if lq * 2 > 16)    # G = 2, Hkv = 8
+    assert c["prefill_tiles"] == items
+    assert 0 < c["prefill_ctas"] <= 152 // 2
+    assert c["dec_ctas"] > 0 and c["pieces"] >= 8 * 2                 # the two decode rows
