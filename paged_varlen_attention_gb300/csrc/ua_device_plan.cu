@@ -357,17 +357,40 @@ __global__ void __launch_bounds__(kPlanThreads, 1) ua_plan_kernel(const PlanArgs
     __syncthreads();
     const long long total_pages = block_scan(a.ustart, n_units + 1, s_part64);
 
-    // ---- decode: equal page ranges, one per CTA
+    // ---- decode: equal shares of cost (kDecUnitCost + pages per unit), one per CTA
     int dec_ctas = 0, n_pieces = 0, n_comb = 0, n_slots = 0;
     if (total_pages > 0) {
         const long long P = total_pages;
         dec_ctas = (int)min((long long)a.dec_grid, P);
         const int C = dec_ctas;
-        // the CTAs' page ranges (the only 64-bit divisions), first and last units,
-        // and pieces per CTA: the units its range touches
-        for (int c = tid; c <= C; c += nt) s_clo[c] = P * c / C;
+        const long long T = P + kDecUnitCost * (long long)n_units;
+        // the CTAs' page ranges (the only 64-bit divisions): cost T c / C mapped to
+        // a page (the first page of the unit whose fixed part holds it, or the page
+        // it falls on), then first and last units and pieces per CTA
+        for (int c = tid; c <= C; c += nt) {
+            if (c == C) {
+                s_clo[c] = P;
+                continue;
+            }
+            const long long x = T * c / C;
+            int lo = 0, hi = n_units;    // the last unit u with ustart[u] + K u <= x
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (a.ustart[mid] + kDecUnitCost * (long long)mid <= x) lo = mid;
+                else hi = mid;
+            }
+            const long long off = x - a.ustart[lo] - kDecUnitCost * (long long)lo - kDecUnitCost;
+            const long long pages = a.ustart[lo + 1] - a.ustart[lo];
+            s_clo[c] = a.ustart[lo] + min(max(off, 0LL), pages);
+        }
         __syncthreads();
         for (int c = tid; c < C; c += nt) {
+            if (s_clo[c + 1] == s_clo[c]) {      // an empty share (at a unit boundary)
+                s_uf[c] = 0;
+                s_ul[c] = -1;
+                s_cb[c] = 0;
+                continue;
+            }
             const int uf = last_le(a.ustart, n_units, s_clo[c]);
             const int ul = last_le(a.ustart, n_units, s_clo[c + 1] - 1);
             s_uf[c] = uf;

@@ -52,6 +52,13 @@ constexpr int kPreRows = 128;       // packed rows per tcgen05 tile (MMA M)
 constexpr int kPreTileRows = 256;   // packed rows per prefill work item (two MMA tiles)
 constexpr int kKvTile = 128;        // keys per prefill KV tile (8 pages)
 constexpr int kDecCtasPerSm = 2;    // resident decode CTAs per SM
+// A decode unit's fixed cost in pages of one kv head (its Q tile and
+// descriptor, the merge of the four consumer warps' partial results, the
+// output): the decode CTAs get equal shares of pages + kDecUnitCost per unit,
+// not of pages alone.  Measured on 256 sequences of ~40 pages: a CTA spends
+// ~2 us per unit outside its pages (~5-7 pages' time), and with equal pages
+// the CTAs that drew many short units ended 33 us after the median.
+constexpr int64_t kDecUnitCost = 6;
 constexpr size_t kAlign = 256;
 // The scheduling block of claimed prefill items: the index of the next
 // unclaimed item, the prefill CTAs that have finished (the last one zeroes

@@ -182,7 +182,11 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
         }
     }
 
-    // ---- decode: equal page ranges over the concatenated units
+    // ---- decode: equal shares of cost over the concatenated units, a unit
+    // costing kDecUnitCost + its pages.  CTA c takes cost [T c / C, T (c+1) / C);
+    // a cost position inside unit u's fixed part maps to u's first page, one in
+    // its pages to that page, so the CTAs' page ranges tile the pages in order
+    // (a range may be empty, always at a unit boundary).
     int64_t total = 0;
     for (const Unit &u : units) total += u.pages;
     plan.dec_pages = total;
@@ -191,13 +195,32 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
         const int64_t ctas = std::min<int64_t>(want, total);
         plan.dec_ctas = (int32_t)ctas;
         plan.cta_begin.assign(ctas + 1, 0);
+        const int64_t cost = total + kDecUnitCost * (int64_t)units.size();
+        thread_local std::vector<int64_t> tl_bound;
+        std::vector<int64_t> &bound = tl_bound;      // CTA c's pages: [bound[c], bound[c + 1])
+        bound.assign((size_t)ctas + 1, total);
+        {
+            size_t u = 0;
+            int64_t ustart = 0;                      // first page of unit u
+            for (int64_t c = 0; c < ctas; ++c) {
+                const int64_t x = cost * c / ctas;
+                // the last unit whose cost starts at or before x
+                while (u + 1 < units.size() &&
+                       ustart + units[u].pages + kDecUnitCost * (int64_t)(u + 1) <= x) {
+                    ustart += units[u].pages;
+                    ++u;
+                }
+                const int64_t off = x - ustart - kDecUnitCost * (int64_t)u - kDecUnitCost;
+                bound[(size_t)c] = ustart + std::min<int64_t>(std::max<int64_t>(off, 0), units[u].pages);
+            }
+        }
         counts.assign(units.size(), 0);              // pieces per unit
         size_t ui = 0;
         int64_t unit_start = 0;                      // global page index of units[ui]'s first page
         for (int64_t c = 0; c < ctas; ++c) {
             plan.cta_begin[c] = (int32_t)plan.pieces.size();
-            const int64_t lo = total * c / ctas;
-            const int64_t hi = total * (c + 1) / ctas;
+            const int64_t lo = bound[(size_t)c];
+            const int64_t hi = bound[(size_t)c + 1];
             int64_t pos = lo;
             while (pos < hi) {
                 while (unit_start + units[ui].pages <= pos) {

@@ -134,6 +134,10 @@ PLAN_CASES = [
     ([5, 17, 300], [5, 30, 1000], 16, 4, 64, False),                   # non-causal
     ([1] * 40 + [129, 33], list(range(100, 4100, 100)) + [129, 40], 4, 4, 64, True),   # G = 1
     ([1] * 300, [17 + 13 * i for i in range(300)], 32, 8, 128, True),  # many short units
+    # one unit's pages spread over all CTAs: shares smaller than a unit's fixed
+    # cost, so the first CTAs' page ranges are empty
+    ([1], [5000], 4, 1, 128, True),
+    ([1, 1], [9000, 17], 8, 2, 128, True),
 ]
 
 

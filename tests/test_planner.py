@@ -29,6 +29,10 @@ def prefill_kend(lq, lk, last_token, causal):
     return min(lk, lk - lq + last_token + 1) if causal else lk
 
 
+# a decode unit's fixed cost in pages, as the planners count it
+UNIT_COST = 6
+
+
 def check_plan(q_lens, k_lens, hq, hk, d=128, causal=True, num_sms=152):
     q_lens = np.asarray(q_lens, np.int64)
     k_lens = np.asarray(k_lens, np.int64)
@@ -92,12 +96,15 @@ def check_plan(q_lens, k_lens, hq, hk, d=128, causal=True, num_sms=152):
     assert len(slots) == len(set(slots)) == counts["slots"]
     assert total_pages == counts["dec_pages"]
 
-    # balance across decode CTAs
+    # balance across decode CTAs: equal shares of cost, a unit costing its
+    # pages plus UNIT_COST (its fixed part, counted in the CTA that runs its
+    # first page); a share boundary inside a unit's fixed part moves that part
+    # to the next CTA, so shares differ by at most two fixed parts
     if counts["dec_ctas"]:
         per_cta = np.zeros(counts["dec_ctas"], np.int64)
         for pc, _ in pieces:
-            per_cta[pc[1]] += pc[7] - pc[6]
-        assert per_cta.max() - per_cta.min() <= 1
+            per_cta[pc[1]] += pc[7] - pc[6] + (UNIT_COST if pc[6] == 0 else 0)
+        assert per_cta.max() - per_cta.min() <= 2 * UNIT_COST + 2
         assert counts["dec_ctas"] <= 2 * num_sms
     # prefill items: the workers' ranges cover the tile list in order, each
     # worker's items come longest first, and dealing the longest-first list in
