@@ -17,7 +17,8 @@
 //     into a ring of shared-memory stages (128-byte swizzle);
 //   * consumer warp w takes pages w, w+4, ... of each piece: S = Q K^T with
 //     mma.sync m16n8k16 (bf16 in, fp32 accumulate), bottom-right causal mask,
-//     online softmax in the exp2 domain, O += P V;
+//     online softmax in the exp2 domain (O and l rescaled only when a row
+//     max grows by more than 2^8), O += P V;
 //   * at the end of each piece the four warps merge their (m, l, O) through
 //     shared memory and write the bf16 output, or an fp32 partial plus its
 //     running (max, sum) when the unit was split across CTAs (split-KV);
@@ -83,6 +84,8 @@ struct DecCfg {
                                          (2 * kStages + 2 * kRing) * 8;
     static_assert(kSmemBytes + 64 <= 232448, "dynamic shared memory above 227 KB");
 };
+
+constexpr float kDecRescale = 8.0f;   // log2 units
 
 // Fields of a piece descriptor in the shared-memory ring.
 enum : int {
@@ -507,22 +510,31 @@ __global__ void __launch_bounds__(DecCfg<D, KV8, kNarrow>::kThreads,
                         s[nt][e] = x;
                         mx[rr] = fmaxf(mx[rr], x);
                     }
+                // The running max moves only when a row max of this warp grows by
+                // more than kDecRescale (log2 units): until then p = 2^(s - m) <= 2^8,
+                // exact after O / l, and O and l need no rescaling (most pages).
                 float mu[2];
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr) {
                     mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
                     mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
-                    const float mn = fmaxf(m[rr], mx[rr]);
-                    mu[rr] = (mn == -INFINITY) ? 0.f : mn;
-                    const float alpha = fast_exp2(m[rr] - mu[rr]);
-                    m[rr] = mn;
-                    l[rr] *= alpha;
+                }
+                if (__any_sync(0xffffffffu, mx[0] > m[0] + kDecRescale || mx[1] > m[1] + kDecRescale)) {
 #pragma unroll
-                    for (int nt = 0; nt < D / 8; ++nt) {
-                        o[nt][2 * rr] *= alpha;
-                        o[nt][2 * rr + 1] *= alpha;
+                    for (int rr = 0; rr < 2; ++rr) {
+                        const float mn = fmaxf(m[rr], mx[rr]);
+                        const float alpha = fast_exp2(m[rr] - ((mn == -INFINITY) ? 0.f : mn));
+                        m[rr] = mn;
+                        l[rr] *= alpha;
+#pragma unroll
+                        for (int nt = 0; nt < D / 8; ++nt) {
+                            o[nt][2 * rr] *= alpha;
+                            o[nt][2 * rr + 1] *= alpha;
+                        }
                     }
                 }
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) mu[rr] = (m[rr] == -INFINITY) ? 0.f : m[rr];
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
