@@ -37,15 +37,15 @@ namespace ua {
 
 // KV8: the cache holds e4m3 bytes (per-tensor scales).  Each consumer
 // thread reads its MMA fragments' bytes straight from the stage (16-byte
-// loads), widens them to f16 in registers, and the MMAs run on f16 operands.
-// The contraction index d of Q K^T is permuted so that a thread's K bytes
-// are contiguous (Q is read with the same permutation), and the output
-// column of P V is permuted so that its V bytes are (undone when the four
-// warps' results are merged).  A unit may hold two adjacent kv heads
-// (heads_per_unit = 2): one TMA box then brings both heads' 128-byte rows of
-// a slot, a 256-byte run of the cache, and the 16-row tile holds head kvh in
-// rows 0-7 and head kvh + 1 in rows 8-15; S and P V run once per head, each
-// keeping the rows of its own head.  D = 128 only.
+// loads) and widens them to f16 in registers; the MMAs run on f16 operands
+// (Q converted once per piece, in shared memory).  A unit may hold two
+// adjacent kv heads (heads_per_unit = 2): one TMA box then brings both
+// heads' 128-byte rows of a slot, a 256-byte run of the cache, and the
+// 16-row tile holds head kvh in rows 0-7 and head kvh + 1 in rows 8-15.  Each
+// head's 8 rows run as the N side of transposed MMAs (S^T = K Q^T, then
+// O^T += V^T P^T, see kv8_page), so no MMA carries the other head's rows;
+// the contraction index d of K Q^T and the d rows of O^T are permuted so
+// that a thread's K and V bytes are contiguous.  D = 128 only.
 //
 // D = 256: a thread holds 64 registers of Q fragments and 128 of the O
 // accumulator, so the kernel runs one CTA per SM (up to 255 registers a
@@ -92,68 +92,193 @@ enum : int {
     kDq0 = 0, kDlq, kDlk, kDkvh, kDrow0, kDnrows, kDpb, kDpe, kDslot, kDcomb, kDslot0, kDnslots
 };
 
-// e4m3 pages (D = 128): S += Q K^T for one 16-key page of one kv head at
-// shared address kb ([slot][128 B], 128-byte swizzle: 16-byte chunk j of
-// slot r sits at j ^ (r % 8)).  Thread (n = lane / 4, t = lane % 4) reads
-// key rows n and 8 + n, chunks 2t and 2t + 1; word w of chunk 2t + h holds
-// the bytes of k-step 4h + w (Q's fragments follow the same permutation).
-__device__ __forceinline__ void kv8_qk(float (&s)[2][4], const uint32_t (&qa)[8][4], uint32_t kb,
-                                       int lane) {
-    const int qr = lane >> 2;
+// e4m3 pages (D = 128).  The tile's 16 rows are two groups of 8: group j
+// holds head kvh + j's rows (two heads per unit) or rows 8j .. 8j + 7 of
+// head kvh (one).  Each group runs transposed, with its rows as the N = 8
+// side of the m16n8k16 MMA, so no MMA carries another head's rows:
+//   S^T = K Q^T  (M = 16 keys, N = 8 rows, K = d: eight k-steps),
+//   O^T += V^T P^T  (M = 16 columns of d per m-tile, eight m-tiles, K = 16 keys).
+// A thread (n = lane / 4, t = lane % 4) then holds S^T at keys n, n + 8 and
+// rows 2t, 2t + 1, and O^T at columns 16n + i, 16n + 8 + i (m-tile i) and the
+// same two rows.  P^T reaches the B-operand layout of the second MMA by an
+// 8 x 8 transpose in registers (movmatrix).
+
+// The Q tile of an e4m3 piece ([16 rows][128] at 256 bytes a row) is
+// converted in place from bf16 to f16 before the pages, 16-byte chunk c of
+// row r moving to chunk c ^ kv8_qswz(r, c): the reads of kv8_qk_t are then
+// free of bank conflicts.  The map swaps chunks within {2q, 2q + 1} (q < 4)
+// and within {8, 9, 10, 11} and {12, 13, 14, 15}.
+__device__ __forceinline__ int kv8_qswz(int r, int c) { return (((c >> 3) & 1) << 1) | (r & 1); }
+
+// S^T += K Q^T for group J: the K page at shared address kb ([slot][128 B],
+// 128-byte swizzle: 16-byte chunk c of slot r sits at c ^ (r % 8)), the f16
+// Q tile at qt.  Thread (n, t) reads key rows n and 8 + n, chunks 2t and
+// 2t + 1; word w of chunk 2t + h holds the 4 bytes of k-step 4h + w, which
+// are logical k (2t, 2t + 1 | 2t + 8, 2t + 9): d = 32t + 16(ks / 4) +
+// 4(ks % 4) + (0, 1 | 2, 3).  The B operand (Q^T, row 8J + n) takes the same
+// columns of Q: chunk 4t + 2h + x of the row holds k-steps 4h + 2x and
+// 4h + 2x + 1.
+template <int J>
+__device__ __forceinline__ void kv8_qk_t(float (&s)[4], uint32_t qt, uint32_t kb, int lane) {
+    const int n = lane >> 2, t = lane & 3;
+    const int row = 8 * J + n;
     uint32_t kr[2][2][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int r = nt * 8 + qr;
-            const uint4 v = lds128(kb + r * 128 + (((2 * (lane & 3) + h) ^ qr) << 4));
-            kr[nt][h][0] = v.x;
-            kr[nt][h][1] = v.y;
-            kr[nt][h][2] = v.z;
-            kr[nt][h][3] = v.w;
+            const uint4 v = lds128(kb + (rr * 8 + n) * 128 + (((2 * t + h) ^ n) << 4));
+            kr[rr][h][0] = v.x;
+            kr[rr][h][1] = v.y;
+            kr[rr][h][2] = v.z;
+            kr[rr][h][3] = v.w;
         }
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
+    for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const uint32_t wd = kr[nt][ks >> 2][ks & 3];
-            mma_f16_16816(s[nt], qa[ks], e4m3x2_to_f16x2((uint16_t)(wd & 0xffffu)),
-                          e4m3x2_to_f16x2((uint16_t)(wd >> 16)));
+        for (int x = 0; x < 2; ++x) {
+            const int c = 4 * t + 2 * h + x;
+            const uint4 q = lds128(qt + row * 256 + ((c ^ kv8_qswz(row, c)) << 4));
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const uint32_t w0 = kr[0][h][2 * x + u], w1 = kr[1][h][2 * x + u];
+                const uint32_t a[4] = {e4m3x2_to_f16x2((uint16_t)(w0 & 0xffffu)),
+                                       e4m3x2_to_f16x2((uint16_t)(w1 & 0xffffu)),
+                                       e4m3x2_to_f16x2((uint16_t)(w0 >> 16)),
+                                       e4m3x2_to_f16x2((uint16_t)(w1 >> 16))};
+                mma_f16_16816(s, a, u ? q.z : q.x, u ? q.w : q.y);
+            }
         }
 }
 
-// e4m3 pages (D = 128): O += P V for one page of one kv head at vb.  Thread
-// (n, t) reads chunk n of value rows 2t, 2t+1, 2t+8, 2t+9: byte b of word w
-// is d = 16n + 4w + b, i.e. output column n of n-tile 4w + b; the byte pairs
-// of rows (2t, 2t+1) and (2t+8, 2t+9) interleave into the two B registers.
-// vm0 / vm1 zero the keys past the context.
-__device__ __forceinline__ void kv8_pv(float (&o)[16][4], const uint32_t (&pa)[4], uint32_t vb,
-                                       int lane, uint32_t vm0, uint32_t vm1) {
-    const int qr = lane >> 2;
+// O^T += V^T P^T for one group: the V page at vb.  Thread (n, t) reads chunk
+// n (d = 16n .. 16n + 15) of value rows 2t, 2t + 1, 2t + 8, 2t + 9; m-tile i
+// takes bytes i and 8 + i of the chunk, the byte pairs of rows (2t, 2t + 1)
+// and (2t + 8, 2t + 9) interleaved into f16 pairs.  vm0 / vm1 zero the keys
+// past the context; pb: P^T in the B-operand layout; o: this group's eight
+// m-tiles.
+template <bool kMask>
+__device__ __forceinline__ void kv8_pv_t(float (*o)[4], const uint32_t (&pb)[2], uint32_t vb, int lane,
+                                         uint32_t vm0, uint32_t vm1) {
+    const int n = lane >> 2;
     uint32_t vr[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int r = 2 * (lane & 3) + (i & 1) + (i >> 1) * 8;
-        const uint4 v = lds128(vb + r * 128 + ((qr ^ (r & 7)) << 4));
+        const uint4 v = lds128(vb + r * 128 + ((n ^ (r & 7)) << 4));
         vr[i][0] = v.x;
         vr[i][1] = v.y;
         vr[i][2] = v.z;
         vr[i][3] = v.w;
     }
 #pragma unroll
-    for (int wd = 0; wd < 4; ++wd) {
-        const uint32_t lo0 = __byte_perm(vr[0][wd], vr[1][wd], 0x5140);
-        const uint32_t hi0 = __byte_perm(vr[0][wd], vr[1][wd], 0x7362);
-        const uint32_t lo1 = __byte_perm(vr[2][wd], vr[3][wd], 0x5140);
-        const uint32_t hi1 = __byte_perm(vr[2][wd], vr[3][wd], 0x7362);
-        mma_f16_16816(o[4 * wd], pa, e4m3x2_to_f16x2((uint16_t)(lo0 & 0xffffu)) & vm0,
-                      e4m3x2_to_f16x2((uint16_t)(lo1 & 0xffffu)) & vm1);
-        mma_f16_16816(o[4 * wd + 1], pa, e4m3x2_to_f16x2((uint16_t)(lo0 >> 16)) & vm0,
-                      e4m3x2_to_f16x2((uint16_t)(lo1 >> 16)) & vm1);
-        mma_f16_16816(o[4 * wd + 2], pa, e4m3x2_to_f16x2((uint16_t)(hi0 & 0xffffu)) & vm0,
-                      e4m3x2_to_f16x2((uint16_t)(hi1 & 0xffffu)) & vm1);
-        mma_f16_16816(o[4 * wd + 3], pa, e4m3x2_to_f16x2((uint16_t)(hi0 >> 16)) & vm0,
-                      e4m3x2_to_f16x2((uint16_t)(hi1 >> 16)) & vm1);
+    for (int w = 0; w < 2; ++w)
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+            // bytes 2hb, 2hb + 1 of word w (d = 16n + 4w + 2hb + (0, 1)) and of word
+            // w + 2 (d + 8), rows (2t, 2t + 1) and (2t + 8, 2t + 9) interleaved
+            const uint32_t sel = hb ? 0x7362u : 0x5140u;
+            const uint32_t x0 = __byte_perm(vr[0][w], vr[1][w], sel);
+            const uint32_t x1 = __byte_perm(vr[2][w], vr[3][w], sel);
+            const uint32_t x0h = __byte_perm(vr[0][w + 2], vr[1][w + 2], sel);
+            const uint32_t x1h = __byte_perm(vr[2][w + 2], vr[3][w + 2], sel);
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                const int sh = 16 * b;
+                uint32_t a[4] = {e4m3x2_to_f16x2((uint16_t)(x0 >> sh)), e4m3x2_to_f16x2((uint16_t)(x0h >> sh)),
+                                 e4m3x2_to_f16x2((uint16_t)(x1 >> sh)), e4m3x2_to_f16x2((uint16_t)(x1h >> sh))};
+                if (kMask) {
+                    a[0] &= vm0;
+                    a[1] &= vm0;
+                    a[2] &= vm1;
+                    a[3] &= vm1;
+                }
+                mma_f16_16816(o[4 * w + 2 * hb + b], a, pb[0], pb[1]);
+            }
+        }
+}
+
+// One e4m3 page for the groups j < ng: S^T, the mask, the online softmax
+// (per thread: rows 2t + r of group j, m[j][r] the running max, l[j][r] this
+// thread's part of the running sum, summed over the warp at the end of the
+// piece) and O^T += V^T P^T.  kpage: bytes from one head's page to the
+// next (two heads per unit) or 0.  kend[j][r]: visible-key limit of the row.
+__device__ __forceinline__ void kv8_page(float (&o)[16][4], float (&m)[2][2], float (&l)[2][2],
+                                         uint32_t qt, uint32_t kb, uint32_t vb,
+                                         uint32_t kpage, int ng, int key0, const int (&kend)[2][2],
+                                         int lk, float scale_log2, float rescale, int lane) {
+    const int n = lane >> 2, t2 = (lane & 3) * 2;
+    float s[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[j][e] = 0.f;
+    // both groups without a branch between them (a group that does not run has
+    // zero Q rows and every key masked), so their MMA chains interleave
+    kv8_qk_t<0>(s[0], qt, kb, lane);
+    kv8_qk_t<1>(s[1], qt, kb + kpage, lane);
+    // scale into the log2 domain and mask (entry e: key n + 8(e / 2), row 2t + e % 2)
+    float lm[2][2];
+    bool grow = false;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int key = key0 + n + (e >> 1) * 8;
+            s[j][e] = key < kend[j][e & 1] ? s[j][e] * scale_log2 : -INFINITY;
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            lm[j][r] = fmaxf(s[j][r], s[j][r + 2]);
+            grow |= lm[j][r] > m[j][r] + rescale;
+        }
+    }
+    // The running max moves only when a row max grows by more than `rescale`
+    // (log2 units); the test needs no reduction: a row's max grows that much
+    // exactly when one of its eight threads sees it.
+    if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                float mx = lm[j][r];
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float mn = fmaxf(m[j][r], mx);
+                const float alpha = fast_exp2(m[j][r] - ((mn == -INFINITY) ? 0.f : mn));
+                m[j][r] = mn;
+                l[j][r] *= alpha;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    o[8 * j + i][r] *= alpha;
+                    o[8 * j + i][r + 2] *= alpha;
+                }
+            }
+    }
+    // V rows past the context (last page) may hold anything, NaN included:
+    // zero them so 0 * NaN never reaches O.
+    const bool tail = key0 + kBlockSize > lk;
+    const uint32_t vm0 = (key0 + t2 < lk ? 0x0000ffffu : 0u) | (key0 + t2 + 1 < lk ? 0xffff0000u : 0u);
+    const uint32_t vm1 = (key0 + 8 + t2 < lk ? 0x0000ffffu : 0u) | (key0 + 9 + t2 < lk ? 0xffff0000u : 0u);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        if (j == 1 && ng < 2) break;
+        float p[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float mu = m[j][e & 1] == -INFINITY ? 0.f : m[j][e & 1];
+            p[e] = fast_exp2(s[j][e] - mu);
+            l[j][e & 1] += p[e];
+        }
+        // P^T (keys n, n + 8 x rows 2t, 2t + 1) to the B layout (keys 2t, 2t + 1
+        // | 2t + 8, 2t + 9 x row n)
+        const uint32_t pb[2] = {movmatrix_trans(pack_f16x2(p[0], p[1])),
+                                movmatrix_trans(pack_f16x2(p[2], p[3]))};
+        if (tail)
+            kv8_pv_t<true>(o + 8 * j, pb, vb + (j ? kpage : 0u), lane, vm0, vm1);
+        else
+            kv8_pv_t<false>(o + 8 * j, pb, vb + (j ? kpage : 0u), lane, vm0, vm1);
     }
 }
 
@@ -396,6 +521,30 @@ __global__ void __launch_bounds__(DecCfg<D, KV8, kNarrow>::kThreads,
             if (ok && !__all_sync(0xffffffffu,
                                   mbar_wait(pfull0 + 8 * slot, (ring / C::kRing) & 1, p.status, p.wait_ns)))
                 ok = false;
+            if constexpr (KV8) {
+                // the Q tile to f16 in place (rows past the unit to zeros), swizzled for
+                // kv8_qk_t: thread (r, q) moves chunks c1, c2 of row r, a pair the
+                // swizzle maps onto itself
+                if (ok) {
+                    const int r = threadIdx.x >> 3, q = threadIdx.x & 7;
+                    const int c1 = q < 4 ? 2 * q : 8 + 4 * ((q - 4) >> 1) + ((q - 4) & 1);
+                    const int c2 = q < 4 ? c1 + 1 : c1 ^ kv8_qswz(r, c1);
+                    const bool live = tile_row_idx(r, hp) < dring[slot * C::kDescInts + kDnrows];
+                    uint8_t *rowp = qring + slot * C::kQTileBytes + r * (D * 2);
+                    uint4 v1 = *reinterpret_cast<const uint4 *>(rowp + c1 * 16);
+                    uint4 v2 = *reinterpret_cast<const uint4 *>(rowp + c2 * 16);
+                    v1 = live ? make_uint4(bf16x2_to_f16x2(v1.x), bf16x2_to_f16x2(v1.y), bf16x2_to_f16x2(v1.z),
+                                           bf16x2_to_f16x2(v1.w))
+                              : make_uint4(0u, 0u, 0u, 0u);
+                    v2 = live ? make_uint4(bf16x2_to_f16x2(v2.x), bf16x2_to_f16x2(v2.y), bf16x2_to_f16x2(v2.z),
+                                           bf16x2_to_f16x2(v2.w))
+                              : make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4 *>(rowp + (c1 ^ kv8_qswz(r, c1)) * 16) = v1;
+                    *reinterpret_cast<uint4 *>(rowp + (c2 ^ kv8_qswz(r, c2)) * 16) = v2;
+                    // the ring slot is refilled by bulk copies (async proxy) later
+                    fence_proxy_async_smem();
+                }
+            }
             ok = named_barrier_and(1, C::kConsumerWarps * 32, ok);
             const int *d = dring + slot * C::kDescInts;
             struct {
@@ -426,22 +575,34 @@ __global__ void __launch_bounds__(DecCfg<D, KV8, kNarrow>::kThreads,
                 const int i = (pc.row0 + r) / p.g;
                 kend[rr] = (p.causal && r < pc.nrows) ? min(lk, lk - lq + i + 1) : lk;
             }
-            // Q fragments (A operand), zero for rows past the unit
-            uint32_t qa[D / 16][4];
+            // KV8: groups of 8 tile rows (head kvh + j, or rows 8j.. of head kvh);
+            // the second one runs when it holds rows.  kend8[j][r]: row 8j + 2t + r
+            // (0 for a group that does not run: every key masked)
+            const int ng = (hp == 2 || pc.nrows > 8) ? 2 : 1;
+            int kend8[2][2];
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks)
+            for (int j = 0; j < 2; ++j)
 #pragma unroll
-                for (int ri = 0; ri < 4; ++ri) {
-                    const int r = qr + (ri & 1) * 8;
-                    // KV8: logical k (2t, 2t+1 | 2t+8, 2t+9) of k-step ks is
-                    // d = 32t + 16(ks / 4) + 4(ks % 4) + (0, 1 | 2, 3)
-                    const int col = KV8 ? 32 * (lane & 3) + 16 * (ks >> 2) + 4 * (ks & 3) + (ri >> 1) * 2
-                                        : ks * 16 + qc + (ri >> 1) * 8;
-                    qa[ks][ri] = tile_row_idx(r, hp) < pc.nrows
-                                     ? *reinterpret_cast<const uint32_t *>(qtile + (r * D + col) * 2)
-                                     : 0u;
-                    if (KV8) qa[ks][ri] = bf16x2_to_f16x2(qa[ks][ri]);
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int r = tile_row_idx(8 * j + qc + rr, hp);
+                    const int i = (pc.row0 + r) / p.g;
+                    kend8[j][rr] = j >= ng ? 0 : (p.causal && r < pc.nrows) ? min(lk, lk - lq + i + 1) : lk;
                 }
+            // Q fragments (A operand), zero for rows past the unit (bf16 pages; the
+            // e4m3 path reads its f16 tile from shared memory)
+            uint32_t qa[KV8 ? 1 : D / 16][4];
+            if constexpr (!KV8) {
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+#pragma unroll
+                    for (int ri = 0; ri < 4; ++ri) {
+                        const int r = qr + (ri & 1) * 8;
+                        const int col = ks * 16 + qc + (ri >> 1) * 8;
+                        qa[ks][ri] = tile_row_idx(r, hp) < pc.nrows
+                                         ? *reinterpret_cast<const uint32_t *>(qtile + (r * D + col) * 2)
+                                         : 0u;
+                    }
+            }
 
             float o[D / 8][4];
 #pragma unroll
@@ -450,6 +611,8 @@ __global__ void __launch_bounds__(DecCfg<D, KV8, kNarrow>::kThreads,
                 for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
             float m[2] = {-INFINITY, -INFINITY};
             float l[2] = {0.f, 0.f};
+            float m8[2][2] = {{-INFINITY, -INFINITY}, {-INFINITY, -INFINITY}};
+            float l8[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
 
             for (int k = w; k < npages && ok; k += C::kConsumerWarps) {
                 const uint32_t gidx = gbase + k;
@@ -463,29 +626,17 @@ __global__ void __launch_bounds__(DecCfg<D, KV8, kNarrow>::kThreads,
                 const uint32_t vb = kb + C::kPageBytes;
                 const int key0 = (pc.page_begin + k) * kBlockSize;
 
-                // S = Q K^T for 16 rows x 16 keys
-                float s[2][4];
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
                 if constexpr (KV8) {
-                    kv8_qk(s, qa, kb, lane);
-                    if (hp == 2) {
-                        // head kvh + 1 (tile rows 8-15: accumulator entries 2, 3)
-                        float s1[2][4];
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) s1[nt][e] = 0.f;
-                        kv8_qk(s1, qa, kb + C::kHeadPageBytes, lane);
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            s[nt][2] = s1[nt][2];
-                            s[nt][3] = s1[nt][3];
-                        }
-                    }
+                    kv8_page(o, m8, l8, qring0 + slot * C::kQTileBytes, kb, vb,
+                             hp == 2 ? (uint32_t)C::kHeadPageBytes : 0u, ng, key0,
+                             kend8, lk, p.scale_log2, kDecRescale, lane);
                 } else {
+                    // S = Q K^T for 16 rows x 16 keys
+                    float s[2][4];
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
                         if (kNarrow && ks * 16 >= p.dq) break;     // zero columns of both operands
@@ -497,83 +648,64 @@ __global__ void __launch_bounds__(DecCfg<D, KV8, kNarrow>::kThreads,
                         mma_bf16_16816(s[0], qa[ks], b0, b1);
                         mma_bf16_16816(s[1], qa[ks], b2, b3);
                     }
-                }
-                // scale into the log2 domain and mask
-                float mx[2] = {-INFINITY, -INFINITY};
+                    // scale into the log2 domain and mask
+                    float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
+                    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int rr = e >> 1;
-                        const int key = key0 + nt * 8 + qc + (e & 1);
-                        const float x = key < kend[rr] ? s[nt][e] * p.scale_log2 : -INFINITY;
-                        s[nt][e] = x;
-                        mx[rr] = fmaxf(mx[rr], x);
-                    }
-                // The running max moves only when a row max of this warp grows by
-                // more than kDecRescale (log2 units): until then p = 2^(s - m) <= 2^8,
-                // exact after O / l, and O and l need no rescaling (most pages).
-                float mu[2];
-#pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                    mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
-                    mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
-                }
-                if (__any_sync(0xffffffffu, mx[0] > m[0] + kDecRescale || mx[1] > m[1] + kDecRescale)) {
+                        for (int e = 0; e < 4; ++e) {
+                            const int rr = e >> 1;
+                            const int key = key0 + nt * 8 + qc + (e & 1);
+                            const float x = key < kend[rr] ? s[nt][e] * p.scale_log2 : -INFINITY;
+                            s[nt][e] = x;
+                            mx[rr] = fmaxf(mx[rr], x);
+                        }
+                    // The running max moves only when a row max of this warp grows by
+                    // more than kDecRescale (log2 units): until then p = 2^(s - m) <= 2^8,
+                    // exact after O / l, and O and l need no rescaling (most pages).
+                    float mu[2];
 #pragma unroll
                     for (int rr = 0; rr < 2; ++rr) {
-                        const float mn = fmaxf(m[rr], mx[rr]);
-                        const float alpha = fast_exp2(m[rr] - ((mn == -INFINITY) ? 0.f : mn));
-                        m[rr] = mn;
-                        l[rr] *= alpha;
+                        mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
+                        mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
+                    }
+                    if (__any_sync(0xffffffffu, mx[0] > m[0] + kDecRescale || mx[1] > m[1] + kDecRescale)) {
 #pragma unroll
-                        for (int nt = 0; nt < D / 8; ++nt) {
-                            o[nt][2 * rr] *= alpha;
-                            o[nt][2 * rr + 1] *= alpha;
+                        for (int rr = 0; rr < 2; ++rr) {
+                            const float mn = fmaxf(m[rr], mx[rr]);
+                            const float alpha = fast_exp2(m[rr] - ((mn == -INFINITY) ? 0.f : mn));
+                            m[rr] = mn;
+                            l[rr] *= alpha;
+#pragma unroll
+                            for (int nt = 0; nt < D / 8; ++nt) {
+                                o[nt][2 * rr] *= alpha;
+                                o[nt][2 * rr + 1] *= alpha;
+                            }
                         }
                     }
-                }
 #pragma unroll
-                for (int rr = 0; rr < 2; ++rr) mu[rr] = (m[rr] == -INFINITY) ? 0.f : m[rr];
+                    for (int rr = 0; rr < 2; ++rr) mu[rr] = (m[rr] == -INFINITY) ? 0.f : m[rr];
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
+                    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float pv = fast_exp2(s[nt][e] - mu[e >> 1]);
-                        s[nt][e] = pv;
-                        l[e >> 1] += pv;
-                    }
-                uint32_t pa[4];
-                if constexpr (KV8) {
-                    pa[0] = pack_f16x2(s[0][0], s[0][1]);
-                    pa[1] = pack_f16x2(s[0][2], s[0][3]);
-                    pa[2] = pack_f16x2(s[1][0], s[1][1]);
-                    pa[3] = pack_f16x2(s[1][2], s[1][3]);
-                } else {
+                        for (int e = 0; e < 4; ++e) {
+                            const float pv = fast_exp2(s[nt][e] - mu[e >> 1]);
+                            s[nt][e] = pv;
+                            l[e >> 1] += pv;
+                        }
+                    uint32_t pa[4];
                     pa[0] = pack_bf16x2(s[0][0], s[0][1]);
                     pa[1] = pack_bf16x2(s[0][2], s[0][3]);
                     pa[2] = pack_bf16x2(s[1][0], s[1][1]);
                     pa[3] = pack_bf16x2(s[1][2], s[1][3]);
-                }
-                // V rows past the context (last page) may hold anything, NaN
-                // included: zero them so 0 * NaN never reaches O.
-                uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
-                if (key0 + kBlockSize > lk) {
-                    vm0 = (key0 + qc < lk ? 0x0000ffffu : 0u) | (key0 + qc + 1 < lk ? 0xffff0000u : 0u);
-                    vm1 = (key0 + 8 + qc < lk ? 0x0000ffffu : 0u) |
-                          (key0 + 9 + qc < lk ? 0xffff0000u : 0u);
-                }
-                if constexpr (KV8) {
-                    if (hp == 2) {
-                        // each head's P rows against its own V page
-                        const uint32_t pa0[4] = {pa[0], 0u, pa[2], 0u};
-                        const uint32_t pa1[4] = {0u, pa[1], 0u, pa[3]};
-                        kv8_pv(o, pa0, vb, lane, vm0, vm1);
-                        kv8_pv(o, pa1, vb + C::kHeadPageBytes, lane, vm0, vm1);
-                    } else {
-                        kv8_pv(o, pa, vb, lane, vm0, vm1);
+                    // V rows past the context (last page) may hold anything, NaN
+                    // included: zero them so 0 * NaN never reaches O.
+                    uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+                    if (key0 + kBlockSize > lk) {
+                        vm0 = (key0 + qc < lk ? 0x0000ffffu : 0u) | (key0 + qc + 1 < lk ? 0xffff0000u : 0u);
+                        vm1 = (key0 + 8 + qc < lk ? 0x0000ffffu : 0u) |
+                              (key0 + 9 + qc < lk ? 0xffff0000u : 0u);
                     }
-                } else {
 #pragma unroll
                     for (int np = 0; np < D / 16; ++np) {
                         if (kNarrow && np * 16 >= p.dq) break;     // output columns past the head
@@ -592,35 +724,50 @@ __global__ void __launch_bounds__(DecCfg<D, KV8, kNarrow>::kThreads,
             gbase += npages;
 
             // ---- merge the four warps' states and write the result
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 1);
-                l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 2);
-            }
             if constexpr (KV8) {
-                // o[nt][e] is column d = 16 (2t + e % 2) + nt; stored at d ^ 4 (row % 8)
-                // (groups of 4 columns stay together for the readers below)
+                // row 8j + 2t + r: l8 summed over the row's eight threads; o[8j + i][r + 2h]
+                // is column 16n + 8h + i, so a thread holds 16 consecutive columns of
+                // each of its rows: four float4 stores at column d ^ 4 ((row / 2) % 8)
+                // (conflict-free; groups of 4 columns stay together for the readers)
 #pragma unroll
-                for (int nt = 0; nt < D / 8; ++nt)
+                for (int j = 0; j < 2; ++j)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int row = qr + (e >> 1) * 8;
-                        const int d = 16 * (qc + (e & 1)) + nt;
-                        mrg_o[row * D + (d ^ ((row & 7) << 2))] = o[nt][e];
+                    for (int rr = 0; rr < 2; ++rr) {
+                        float lt = l8[j][rr];
+                        lt += __shfl_xor_sync(0xffffffffu, lt, 4);
+                        lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+                        lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+                        const int row = 8 * j + qc + rr;
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const int i0 = 8 * j + 4 * (q4 & 1), e = rr + 2 * (q4 >> 1);
+                            const int d = 16 * qr + 4 * q4;
+                            *reinterpret_cast<float4 *>(mrg_o + row * D + (d ^ (((row >> 1) & 7) << 2))) =
+                                make_float4(o[i0][e], o[i0 + 1][e], o[i0 + 2][e], o[i0 + 3][e]);
+                        }
+                        if (qr == 0) {
+                            mrg_m[row] = m8[j][rr];
+                            mrg_l[row] = lt;
+                        }
                     }
             } else {
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 1);
+                    l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 2);
+                }
 #pragma unroll
                 for (int nt = 0; nt < D / 8; ++nt) {
                     const int col = nt * 8 + qc;
                     *reinterpret_cast<float2 *>(mrg_o + qr * D + col) = make_float2(o[nt][0], o[nt][1]);
                     *reinterpret_cast<float2 *>(mrg_o + (qr + 8) * D + col) = make_float2(o[nt][2], o[nt][3]);
                 }
-            }
-            if ((lane & 3) == 0) {
-                mrg_m[qr] = m[0];
-                mrg_m[qr + 8] = m[1];
-                mrg_l[qr] = l[0];
-                mrg_l[qr + 8] = l[1];
+                if ((lane & 3) == 0) {
+                    mrg_m[qr] = m[0];
+                    mrg_m[qr + 8] = m[1];
+                    mrg_l[qr] = l[0];
+                    mrg_l[qr + 8] = l[1];
+                }
             }
             named_barrier_sync(1, C::kConsumerWarps * 32);
             // every consumer has its copy of the descriptor and Q: free the ring slot
@@ -644,7 +791,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV8, kNarrow>::kThreads,
                     for (int ww = 0; ww < C::kConsumerWarps; ++ww) {
                         const float f = fast_exp2(mw[ww] - M);
                         L += f * merge[ww * C::kMergeFloats + kDecRows * D + kDecRows + row];
-                        const int scol = KV8 ? col ^ ((row & 7) << 2) : col;
+                        const int scol = KV8 ? col ^ (((row >> 1) & 7) << 2) : col;
                         const float4 ov =
                             *reinterpret_cast<const float4 *>(merge + ww * C::kMergeFloats + row * D + scol);
                         acc.x += f * ov.x;

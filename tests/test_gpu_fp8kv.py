@@ -69,6 +69,7 @@ CASES = [
     ([1, 4, 1], [100, 64, 33], 12, 3, True),                            # Hkv = 3
     ([2, 1, 3], [500, 60, 30], 16, 2, True),                            # G = 8, 8-row tiles
     ([1, 1], [200, 3000], 32, 2, True),                                 # G = 16: a token spans two tiles
+    ([3, 1, 2], [400, 90, 2], 5, 1, True),                               # one head per unit, 15 rows
 ]
 
 
