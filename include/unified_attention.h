@@ -39,11 +39,12 @@
  *
  * Supported set: head_size 64, 80, 96, 112, 128 or 256, block_size a
  * multiple of 16 up to 256, num_q_heads a multiple of num_kv_heads.  Anything
- * else returns UA_ERR_UNSUPPORTED before any launch.  With head_size 80, 96,
- * 112 or 256 every row, prefill rows included, runs in the decode / split-KV
- * kernel (16-row units; 80, 96 and 112 in its 128-wide instance, the columns
- * past head_size read as zeros and never written); the tensor-core prefill
- * kernels take head sizes 64 and 128.
+ * else returns UA_ERR_UNSUPPORTED before any launch.  With head_size 80, 96
+ * or 112 every row, prefill rows included, runs in the decode / split-KV
+ * kernel (its 128-wide instance, the columns past head_size read as zeros and
+ * never written; units of two adjacent kv heads when num_kv_heads is even);
+ * the tensor-core prefill kernels take head sizes 64 and 128 (one SM per
+ * work item, or SM pairs for long items) and 256 (SM pairs).
  *
  * Pages of block_size = 16 r tokens (r > 1): the same memory is a cache of
  * num_blocks * r pages of 16 tokens (slot j of page b is slot j % 16 of

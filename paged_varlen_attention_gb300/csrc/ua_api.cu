@@ -308,18 +308,18 @@ static bool encode_page_map(CUtensorMap *map, const void *base, int d, int hkv,
 }
 
 // 4-D bf16 map over the paged cache of a head narrower than 128 columns (80,
-// 96, 112): (d, 16 slots, Hkv, blocks), boxes of {64, 16, 1, 1} with the
-// 128-byte swizzle.  The box at column 64 runs past d, and TMA fills those
-// columns with zeros without reading them: the page lands in the layout of
-// a 128-column page, [chunk][slot][64], with zeros past d.
+// 96, 112): (d, 16 slots, Hkv, blocks), boxes of {64, 16, box_heads, 1} with
+// the 128-byte swizzle.  The box at column 64 runs past d, and TMA fills those
+// columns with zeros without reading them: each head's page lands in the
+// layout of a 128-column page, [chunk][head][slot][64], with zeros past d.
 static bool encode_page_map_narrow(CUtensorMap *map, const void *base, int d, int hkv,
-                                   uint64_t num_blocks) {
+                                   uint64_t num_blocks, int box_heads) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
     const uint64_t row = (uint64_t)hkv * d * 2;   // bytes between slots
     cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)kBlockSize, (cuuint64_t)hkv, num_blocks};
     cuuint64_t strides[3] = {row, (cuuint64_t)d * 2, row * kBlockSize};
-    cuuint32_t box[4] = {64, (cuuint32_t)kBlockSize, 1, 1};
+    cuuint32_t box[4] = {64, (cuuint32_t)kBlockSize, (cuuint32_t)box_heads, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -332,8 +332,8 @@ static bool encode_page_map_narrow(CUtensorMap *map, const void *base, int d, in
 static bool encode_decode_maps(CUtensorMap *tk, CUtensorMap *tv, const void *k, const void *v, int d,
                                int hkv, uint64_t num_blocks, int eb, int box_heads) {
     if (kernel_head_size(d) != d)
-        return encode_page_map_narrow(tk, k, d, hkv, num_blocks) &&
-               encode_page_map_narrow(tv, v, d, hkv, num_blocks);
+        return encode_page_map_narrow(tk, k, d, hkv, num_blocks, box_heads) &&
+               encode_page_map_narrow(tv, v, d, hkv, num_blocks, box_heads);
     return encode_page_map(tk, k, d, hkv, num_blocks, eb, box_heads) &&
            encode_page_map(tv, v, d, hkv, num_blocks, eb, box_heads);
 }
@@ -409,6 +409,9 @@ static Problem make_problem(const int32_t *cu, const int32_t *lk, int32_t num_se
     p.bs = bs;
     p.bt_stride = bt_stride;
     p.causal = causal != 0;
+    // heads narrower than 128 columns: decode units of two adjacent kv heads,
+    // whose rows of a slot are one run of the cache (see the decode kernel)
+    if (kernel_head_size(d) != d) p.kv_heads_per_unit = 2;
     return p;
 }
 
@@ -673,7 +676,8 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
     const int g = num_q_heads / num_kv_heads;
     CUtensorMap tm_kp, tm_vp, tm_q, tm_o, tm_k3, tm_vh;
     const int eb = kv_fp8 ? 1 : 2;
-    const int box_heads = plan.dec_heads_per_unit;   // 2 only for e4m3 pages (no prefill tiles)
+    const int box_heads = plan.dec_heads_per_unit;   // 2 only for e4m3 pages and narrower heads
+                                                     // (no prefill tiles for either)
     if (!encode_decode_maps(&tm_kp, &tm_vp, k_cache, v_cache, head_size, num_kv_heads,
                             (uint64_t)num_blocks, eb, box_heads))
         return UA_ERR_CUDA;
@@ -976,7 +980,7 @@ static ua_status device_plan_shape(int32_t num_seqs, int32_t max_total_q, int32_
     s->hkv = hkv;
     s->d = d;
     s->bt_stride = bt_stride * s->page_ratio;   // in 16-token pages
-    s->hpu = (kv_fp8 && hkv % 2 == 0) ? 2 : 1;
+    s->hpu = ((kv_fp8 || kernel_head_size(d) != d) && hkv % 2 == 0) ? 2 : 1;
     // no sequence can fill more than one decode tile: the prefill kernel never has work
     const bool can_prefill = (int64_t)s->max_seq_q * (hq / hkv) > kDecRows;
     s->prefill_ok = (kPrefillEnabled && !kv_fp8 && can_prefill && prefill_supports(pr)) ? 1 : 0;

@@ -58,7 +58,13 @@ namespace ua {
 // (they are not read from memory); Q's tile rows are zero past dq; the output
 // keeps the first dq columns.  Every row of such a batch comes here too; the
 // k-steps of Q K^T past dq and the n-tiles of P V past dq (all zeros) are
-// skipped.
+// skipped.  A unit takes two adjacent kv heads when Hkv is even (rows 0-7
+// head kvh, rows 8-15 head kvh + 1, as for e4m3 pages): their rows of a slot
+// are one run of 2 dq elements in the cache, which for dq = 96 is three whole
+// 128-byte lines, where one head's 192 bytes share a line with a neighbour
+// head's row (a head fetched alone read 4/3 of its bytes from memory).  The
+// MMAs then run once per head over the 16-row tile, each head keeping its
+// own rows.
 template <int D, bool KV8, bool kNarrow = false>
 struct DecCfg {
     static_assert(!KV8 || D == 128, "the e4m3 path is laid out for D = 128");
@@ -66,10 +72,11 @@ struct DecCfg {
     static_assert(!kNarrow || (D == 128 && !KV8), "narrower heads run in the bf16 D = 128 kernel");
     static constexpr int kChunks = D / 64;                        // 64-column TMA boxes per row
     static constexpr int kHeadPageBytes = kBlockSize * D * (KV8 ? 1 : 2);   // one page of one kv head
-    static constexpr int kPageBytes = (KV8 ? 2 : 1) * kHeadPageBytes;      // K (or V) part of a stage
+    // K (or V) part of a stage: room for two kv heads' pages (e4m3, narrower heads)
+    static constexpr int kPageBytes = (KV8 || kNarrow ? 2 : 1) * kHeadPageBytes;
     static constexpr int kStageBytes = 2 * kPageBytes;           // K + V
     // 64 KB of stages at two CTAs per SM; 128 KB at one (D = 256)
-    static constexpr int kStages = (D == 64) ? 16 : 8;
+    static constexpr int kStages = (D == 64) ? 16 : kNarrow ? 4 : 8;
     static constexpr int kMinCtasPerSm = (D == 256) ? 1 : 2;
     static constexpr int kConsumerWarps = 4;
     static constexpr int kThreads = (kConsumerWarps + 1) * 32;
@@ -392,7 +399,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV8, kNarrow>::kThreads,
             prefetch_tensormap(&tm_v);
         }
         const uint64_t policy = l2_policy_evict_first();
-        const int hp = KV8 ? p.heads_per_unit : 1;   // kv heads per unit (and per box)
+        const int hp = KV8 || kNarrow ? p.heads_per_unit : 1;   // kv heads per unit (and per box)
         bool ok = true;
         uint32_t filled = 0;   // ring entries filled
         DecPiece nxt{};
@@ -480,11 +487,12 @@ __global__ void __launch_bounds__(DecCfg<D, KV8, kNarrow>::kThreads,
                                 tma_load_5d_hint(vdst, &tm_v, 0, 0, 0, pc.kvh, b, fb, policy);
                             } else {
                                 // a narrower head: one box per 64 columns of (dq, slot, kv
-                                // head, block), the same layout, zeros past dq
+                                // head, block), zeros past dq, each box the unit's hp heads:
+                                // laid out [chunk][head][slot][64]
 #pragma unroll
                                 for (int c = 0; c < C::kChunks; ++c) {
-                                    tma_load_4d_hint(kdst + c * 2048, &tm_k, 64 * c, 0, pc.kvh, b, fb, policy);
-                                    tma_load_4d_hint(vdst + c * 2048, &tm_v, 64 * c, 0, pc.kvh, b, fb, policy);
+                                    tma_load_4d_hint(kdst + c * hp * 2048, &tm_k, 64 * c, 0, pc.kvh, b, fb, policy);
+                                    tma_load_4d_hint(vdst + c * hp * 2048, &tm_v, 64 * c, 0, pc.kvh, b, fb, policy);
                                 }
                             }
                         }
@@ -509,7 +517,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV8, kNarrow>::kThreads,
         float *mrg_l = mrg_m + kDecRows;
         uint32_t gbase = 0;
         bool ok = true;
-        const int hp = KV8 ? p.heads_per_unit : 1;   // kv heads per unit
+        const int hp = KV8 || kNarrow ? p.heads_per_unit : 1;   // kv heads per unit
         // Every consumer warp walks every piece (the merges use a named barrier),
         // even after a failed wait: a piece it could not get counts as empty.  The
         // four warps decide together whether they have the piece (a barrier that
@@ -637,16 +645,46 @@ __global__ void __launch_bounds__(DecCfg<D, KV8, kNarrow>::kThreads,
                     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
+                    if constexpr (kNarrow) {
+                        // head j's page at kb + 2048 j (chunks hp * 2048 apart); with two
+                        // heads, rows 8-15 (entries 2, 3) take the second head's scores
 #pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        if (kNarrow && ks * 16 >= p.dq) break;     // zero columns of both operands
-                        const int c = ks >> 2;
-                        const int ch = (ks & 3) * 2 + ((lane >> 3) & 1);
-                        const int r = ((lane >> 4) << 3) + (lane & 7);
-                        uint32_t b0, b1, b2, b3;
-                        ldmatrix_x4(kb + c * 2048 + r * 128 + ((ch ^ (r & 7)) << 4), b0, b1, b2, b3);
-                        mma_bf16_16816(s[0], qa[ks], b0, b1);
-                        mma_bf16_16816(s[1], qa[ks], b2, b3);
+                        for (int j = 0; j < 2; ++j) {
+                            if (j >= hp) break;
+                            float sj[2][4];
+#pragma unroll
+                            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) sj[nt][e] = 0.f;
+#pragma unroll
+                            for (int ks = 0; ks < D / 16; ++ks) {
+                                if (ks * 16 >= p.dq) break;     // zero columns of both operands
+                                const int c = ks >> 2;
+                                const int ch = (ks & 3) * 2 + ((lane >> 3) & 1);
+                                const int r = ((lane >> 4) << 3) + (lane & 7);
+                                uint32_t b0, b1, b2, b3;
+                                ldmatrix_x4(kb + (c * hp + j) * 2048 + r * 128 + ((ch ^ (r & 7)) << 4), b0,
+                                            b1, b2, b3);
+                                mma_bf16_16816(sj[0], qa[ks], b0, b1);
+                                mma_bf16_16816(sj[1], qa[ks], b2, b3);
+                            }
+#pragma unroll
+                            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    if (j == 0 || e >= 2) s[nt][e] = sj[nt][e];
+                        }
+                    } else {
+#pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks) {
+                            const int c = ks >> 2;
+                            const int ch = (ks & 3) * 2 + ((lane >> 3) & 1);
+                            const int r = ((lane >> 4) << 3) + (lane & 7);
+                            uint32_t b0, b1, b2, b3;
+                            ldmatrix_x4(kb + c * 2048 + r * 128 + ((ch ^ (r & 7)) << 4), b0, b1, b2, b3);
+                            mma_bf16_16816(s[0], qa[ks], b0, b1);
+                            mma_bf16_16816(s[1], qa[ks], b2, b3);
+                        }
                     }
                     // scale into the log2 domain and mask
                     float mx[2] = {-INFINITY, -INFINITY};
@@ -706,16 +744,38 @@ __global__ void __launch_bounds__(DecCfg<D, KV8, kNarrow>::kThreads,
                         vm1 = (key0 + 8 + qc < lk ? 0x0000ffffu : 0u) |
                               (key0 + 9 + qc < lk ? 0xffff0000u : 0u);
                     }
+                    if constexpr (kNarrow) {
+                        // each head's P rows against its own V page
 #pragma unroll
-                    for (int np = 0; np < D / 16; ++np) {
-                        if (kNarrow && np * 16 >= p.dq) break;     // output columns past the head
-                        const int c = np >> 2;
-                        const int ch = (np & 3) * 2 + (lane >> 4);
-                        const int r = ((lane >> 3) & 1) * 8 + (lane & 7);
-                        uint32_t v0, v1, v2, v3;
-                        ldmatrix_x4_trans(vb + c * 2048 + r * 128 + ((ch ^ (r & 7)) << 4), v0, v1, v2, v3);
-                        mma_bf16_16816(o[2 * np], pa, v0 & vm0, v1 & vm1);
-                        mma_bf16_16816(o[2 * np + 1], pa, v2 & vm0, v3 & vm1);
+                        for (int j = 0; j < 2; ++j) {
+                            if (j >= hp) break;
+                            uint32_t pj[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) pj[i] = (hp == 1 || (i & 1) == j) ? pa[i] : 0u;
+#pragma unroll
+                            for (int np = 0; np < D / 16; ++np) {
+                                if (np * 16 >= p.dq) break;     // output columns past the head
+                                const int c = np >> 2;
+                                const int ch = (np & 3) * 2 + (lane >> 4);
+                                const int r = ((lane >> 3) & 1) * 8 + (lane & 7);
+                                uint32_t v0, v1, v2, v3;
+                                ldmatrix_x4_trans(vb + (c * hp + j) * 2048 + r * 128 + ((ch ^ (r & 7)) << 4), v0,
+                                                  v1, v2, v3);
+                                mma_bf16_16816(o[2 * np], pj, v0 & vm0, v1 & vm1);
+                                mma_bf16_16816(o[2 * np + 1], pj, v2 & vm0, v3 & vm1);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int np = 0; np < D / 16; ++np) {
+                            const int c = np >> 2;
+                            const int ch = (np & 3) * 2 + (lane >> 4);
+                            const int r = ((lane >> 3) & 1) * 8 + (lane & 7);
+                            uint32_t v0, v1, v2, v3;
+                            ldmatrix_x4_trans(vb + c * 2048 + r * 128 + ((ch ^ (r & 7)) << 4), v0, v1, v2, v3);
+                            mma_bf16_16816(o[2 * np], pa, v0 & vm0, v1 & vm1);
+                            mma_bf16_16816(o[2 * np + 1], pa, v2 & vm0, v3 & vm1);
+                        }
                     }
                 }
                 __syncwarp();

@@ -16,8 +16,9 @@
 //     every SM streams the same number of pages (split-KV).  A unit cut into
 //     several pieces writes fp32 partials; the CTA that writes a unit's last
 //     partial merges them with a log-sum-exp rule.  With two kv heads per
-//     unit (the e4m3 cache), a unit is (sequence, kv heads h and h + 1,
-//     8-row tile): tile rows 0-7 belong to head h, rows 8-15 to head h + 1.
+//     unit (the e4m3 cache, and heads narrower than 128 columns; Hkv even),
+//     a unit is (sequence, kv heads h and h + 1, 8-row tile): tile rows 0-7
+//     belong to head h, rows 8-15 to head h + 1.
 //   * prefill tiles -- (sequence, kv head, 256-row tile) for the rest: two
 //     128-row tensor-core tiles that share every K/V tile they load, longest
 //     first.  Short items are dealt to the CTAs in advance (rounds of

@@ -8,8 +8,11 @@ brought in through a tensor map whose innermost extent is the real head size,
 so the copy engine fills columns d..127 of the shared-memory tile with zeros;
 Q rows are copied at their real width into a zeroed ring slot; only the first
 d columns of a result are written.  Prefill and chunked-prefill rows of such a
-batch become 16-row units of the same kernel.  Checked: mixed batches with
-split-KV contexts, causal and non-causal rows, G from 1 to 16, the per-row
+batch become units of the same kernel; a unit takes two adjacent kv heads (8
+rows of each) when Hkv is even, so that their rows of a slot are fetched as
+one run of the cache.  Checked: mixed batches with
+split-KV contexts, causal and non-causal rows, G from 1 to 16, odd Hkv (one
+head per unit), a head's rows over two units, the per-row
 log-sum-exp and the merge, 32- and 64-token pages, the device-planned call,
 append + attend, and the refusal of an E4M3 cache at these sizes.
 """
@@ -50,6 +53,9 @@ CASES = [
     ([1, 3, 1], [2, 3, 1], 4, 4, True),                               # G = 1, tiny contexts
     ([1, 1, 7], [200, 3000, 7], 32, 2, True),                         # G = 16: a token fills a tile
     ([0, 129, 1], [5, 129, 9000], 16, 4, True),                       # empty query, ragged tiles, long split
+    # two kv heads per decode unit need Hkv even; odd Hkv keeps one head per unit
+    ([1, 9, 1], [300, 60, 17], 12, 3, True),                          # Hkv = 3
+    ([9, 1, 2], [500, 33, 2000], 6, 6, True),                         # G = 1: 9 rows of a head span two units
 ]
 
 

@@ -41,6 +41,9 @@ def check_plan(q_lens, k_lens, hq, hk, d=128, causal=True, num_sms=152):
     counts, items = B.plan_inspect(cu, k_lens.astype(np.int32), hq, hk, d, stride, causal,
                                    num_sms=num_sms)
     g = hq // hk
+    # heads narrower than 128 columns: decode units of two adjacent kv heads
+    # (Hkv even), at most 8 rows of each
+    hpu = 2 if d in (80, 96, 112) and hk % 2 == 0 else 1
     pieces = [(items[i], items[i + 1]) for i in range(len(items) - 1)
               if items[i][0] == 0 and items[i + 1][0] == 1]
     tiles = [r for r in items if r[0] == 2]
@@ -57,9 +60,10 @@ def check_plan(q_lens, k_lens, hq, hk, d=128, causal=True, num_sms=152):
         units.setdefault((seq, kvh, row0, nrows), []).append((cta, pb, pe, ex[1]))
     for key in units:
         seq, kvh, row0, nrows = key
-        assert 1 <= nrows <= 16
-        for r in range(row0, row0 + nrows):
-            covered[(seq, kvh, r)] = covered.get((seq, kvh, r), 0) + 1
+        assert 1 <= nrows <= 16 // hpu and kvh % hpu == 0
+        for h in range(kvh, kvh + hpu):
+            for r in range(row0, row0 + nrows):
+                covered[(seq, h, r)] = covered.get((seq, h, r), 0) + 1
     for t in tiles:
         _, _, seq, kvh, row0, nrows, kvt, _ = t
         assert 1 <= nrows <= 256 and row0 % 256 == 0
