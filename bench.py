@@ -188,6 +188,20 @@ def routed_prefill_seqs(ua, batch, num_sms):
     return sorted({int(r[2]) for r in items if r[0] == 2})
 
 
+def planned_work(ua, batch, num_sms):
+    """algorithmic_work split by the planner's routing, plus the SMs each kernel
+    gets: a call that runs its two kernels side by side gives the prefill kernel
+    `side_sms` of the GPU's `num_sms` and the decode kernel the rest."""
+    s = batch.spec
+    counts, _ = ua.plan_inspect(batch.cu_seqlens_q, batch.seqused_k, s.num_q_heads,
+                                s.num_kv_heads, s.head_size, batch.block_table_stride, s.causal,
+                                num_sms=num_sms, block_size=s.block_size)
+    work = algorithmic_work(s, routed_prefill_seqs(ua, batch, num_sms))
+    work["num_sms"] = num_sms
+    work["side_sms"] = counts["prefill_sms_side_by_side"]
+    return work
+
+
 def proportional_sample(b, k, m, g=None):
     """Sub-batch k of m: every m-th decode sequence (offset k % m) and, of each
     longer query run, a slice of about Lq / m consecutive rows (the k % m-th),
@@ -494,6 +508,10 @@ def fractions(spec, work, kern, ms_per_step, peaks):
                     "hbm_frac": work["bytes"] / t / bw, "tensor_frac": work["flops"] / t / pk,
                     "combined_frac": max(work["bytes"] / bw, work["flops"] / pk) / t},
            "kernel_ms": {k: (statistics.mean(v) if v else None) for k, v in kern.items()}}
+    side, n = work.get("side_sms", 0), work.get("num_sms", 0)
+    if side:
+        # both kernels timed from the fork of the second stream to their own end
+        out["side_by_side"] = {"prefill_sms": side, "decode_sms": n - side}
     if kern["decode"]:
         dm = statistics.mean(kern["decode"])
         gbs = work["decode_bytes"] / (dm / 1e3) / 1e9
@@ -504,6 +522,8 @@ def fractions(spec, work, kern, ms_per_step, peaks):
         tf = work["prefill_flops"] / (pm / 1e3) / 1e12
         out["prefill_kernel"] = {"ms": pm, "flops": work["prefill_flops"], "tflops": tf,
                                  "frac": tf / peaks["bf16_tflops"]}
+        if side:
+            out["prefill_kernel"]["frac_of_its_sms"] = tf / (peaks["bf16_tflops"] * side / n)
     return out
 
 
@@ -525,7 +545,7 @@ def run_ours(args, rank, world, local, dist):
     with ClockSampler(gpu_id_for_smi(torch, local)) as clocks:
         r = time_attention(ua, torch, device, batch, args.steps, args.warmup, dist, flush)
     total_ms = max_over_ranks(dist, sum(r["times"]), device)
-    work = algorithmic_work(spec, routed_prefill_seqs(ua, batch, sms))
+    work = planned_work(ua, batch, sms)
     res = {"spec": spec, "work": work, "total_ms": total_ms, "times": r["times"], "kern": r["kern"],
            "launches": r["launches"], "clocks": clocks.summary(), "peaks": peaks,
            "fractions": fractions(spec, work, r["kern"], total_ms / args.steps, peaks)}
@@ -612,7 +632,7 @@ def run_ours(args, rank, world, local, dist):
             b = workload_batch(WORKLOADS[name], args.block_size)
             with ClockSampler(gpu_id_for_smi(torch, local)) as ck:
                 rr = time_attention(ua, torch, device, b, steps, 3, dist, flush)
-            w = algorithmic_work(b.spec, routed_prefill_seqs(ua, b, sms))
+            w = planned_work(ua, b, sms)
             f = fractions(b.spec, w, rr["kern"], sum(rr["times"]) / steps, peaks)
             f.update(steps=steps, gpu_launches=rr["launches"], clocks=ck.summary(),
                      roofline=dominant_roofline(name, b.spec, w, rr["kern"], peaks))
@@ -629,12 +649,15 @@ def dominant_roofline(workload, spec, work, kern, peaks):
     HBM (its own bytes), per launch over its CUDA-event time."""
     dec = statistics.mean(kern["decode"]) if kern["decode"] else None
     pre = statistics.mean(kern["prefill"]) if kern["prefill"] else None
-    if pre is not None and (dec is None or pre > dec):
+    side, n = work.get("side_sms", 0), work.get("num_sms", 0)
+    if pre is not None and (dec is None or pre > dec or side):
         achieved = work["prefill_flops"] / (pre / 1e3) / 1e12
+        # side by side, the kernel has `side` of the n SMs: its peak is that share
+        peak = peaks["bf16_tflops"] * (side / n if side else 1.0)
         roof = {"kernel": "ua_prefill_kernel / ua_prefill_pair_kernel (as the planner routes)",
                 "bound": "tensor", "achieved": achieved,
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"],
+                "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak,
                 "traffic": ncu_traffic("prefill", workload) if spec.block_size == 16 else None,
                 "per_launch": f"{work['prefill_flops']} algorithmic flops (4 Hq D per visible "
                               "pair of the sequences the planner sends to this kernel)",
@@ -649,6 +672,10 @@ def dominant_roofline(workload, spec, work, kern, peaks):
                 "launch_ms": dec}
     roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json, burst)" \
         if peaks["source"] == "measured" else "fallback"
+    if side and roof["bound"] == "tensor":
+        roof["peak_source"] += (f" x {side}/{n} SMs: the kernel ran on {side} SMs beside the decode "
+                                f"kernel on the other {n - side}; timed from the fork to its end")
+        roof["sms"] = side
     return roof
 
 

@@ -120,7 +120,13 @@ typedef enum ua_status {
  *   num_blocks     pages in k_cache / v_cache; num_blocks * block_size < 2^31.
  *   workspace      device scratch of at least ua_workspace_size() bytes,
  *                  256-byte aligned; may be NULL only when that size is 0.
- *   stream         a cudaStream_t (NULL = legacy default stream).
+ *   stream         a cudaStream_t (NULL = legacy default stream).  All work is
+ *                  ordered on it: a batch of decode rows and long prefill
+ *                  items may run its decode kernel on a second stream of the
+ *                  library at the same time as its prefill kernel (on other
+ *                  SMs), forked from `stream` after the plan upload and
+ *                  joined back into it before the call returns (see
+ *                  ua_plan_inspect).
  *
  * Host-side checks (UA_ERR_INVALID_ARG): cu_seqlens_q_host[0] == 0 and
  * non-decreasing; seqused_k_host[s] >= 0; Lk > 0 whenever Lq > 0; Lk >= Lq
@@ -169,10 +175,16 @@ ua_status ua_device_status(int32_t *code);
  * decode badly (vLLM PR #14152, section "How is this performance improvement
  * achieved?").
  *
- * counts[0..7] receives: decode CTAs, decode pieces, split units (combined),
- * partial slots, prefill tiles, prefill CTAs, decode pages in total, and the
+ * counts[0..8] receives: decode CTAs, decode pieces, split units (combined),
+ * partial slots, prefill tiles, prefill CTAs, decode pages in total, the
  * bytes of the plan and partials (saturated to INT32_MAX; ua_workspace_size
- * adds the expanded block table to these for pages of more than 16 tokens).
+ * adds the expanded block table to these for pages of more than 16 tokens),
+ * and the SMs the prefill kernel gets when the call runs its two kernels side
+ * by side (0: one after the other, each on every SM).  A batch of decode rows
+ * and long prefill items (head size 128, bf16 cache) runs them side by side
+ * when that is estimated to save time: the prefill kernel on that many SMs,
+ * launched first, and the decode kernel on the rest, on a second stream of
+ * the library's forked from and joined back to the caller's.
  * The partition is the 16-token view's for any supported block_size.
  * If items != NULL, up to items_cap rows of 8 int32 are written:
  *   decode pieces   {0, cta, seq, kv_head, row0, nrows, page_begin, page_end}

@@ -286,7 +286,7 @@ def plan_inspect(cu_seqlens_q_host, seqused_k_host, num_q_heads, num_kv_heads, h
     lib = load_library()
     cu = _host_i32(cu_seqlens_q_host)
     sk = _host_i32(seqused_k_host)
-    counts = np.zeros(8, dtype=np.int32)
+    counts = np.zeros(9, dtype=np.int32)
     n = ctypes.c_int64(0)
     args = (_np_ptr(cu), _np_ptr(sk), len(sk), num_q_heads, num_kv_heads, head_size, block_size,
             block_table_stride, int(bool(causal)), num_sms)
@@ -296,7 +296,7 @@ def plan_inspect(cu_seqlens_q_host, seqused_k_host, num_q_heads, num_kv_heads, h
     _check(lib.ua_plan_inspect(*args, _np_ptr(counts), _np_ptr(items), int(n.value),
                                ctypes.byref(n)), "ua_plan_inspect")
     keys = ("dec_ctas", "pieces", "split_units", "slots", "prefill_tiles", "prefill_ctas",
-            "dec_pages", "workspace_bytes")
+            "dec_pages", "workspace_bytes", "prefill_sms_side_by_side")
     return dict(zip(keys, (int(c) for c in counts))), items[:int(n.value)]
 
 

@@ -48,6 +48,12 @@ struct DeviceState {
     // decode, after prefill, after combine; what ran and how many launches
     cudaEvent_t ev[UA_PROFILE_RING][5] = {};
     bool ran[UA_PROFILE_RING][4] = {};
+    bool split[UA_PROFILE_RING] = {};  // the call ran its two kernels side by side
+    // a second stream for the decode kernel of a call whose two kernels run side by
+    // side, and the events that fork it from the caller's stream and join it back
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    std::mutex side_mutex;             // a record of fork / join and the wait on it go together
     int launches[UA_PROFILE_RING][4] = {};
     int64_t calls = 0;                 // profiled calls so far
 };
@@ -58,6 +64,22 @@ static bool g_profile = false;
 // Limit of the decode kernel's main-loop waits for calls made from now on
 // (ua_test_set_wait_limit; 0: the library's limit, kWaitLimitNs).
 static std::atomic<unsigned long long> g_wait_limit_ns{0};
+
+// The device's second stream and fork / join events (created on first use).
+static ua_status side_stream(DeviceState *ds) {
+    if (ds->side) return UA_OK;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (ds->side) return UA_OK;
+    cudaStream_t s = nullptr;
+    if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ds->fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ds->join, cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        return UA_ERR_CUDA;
+    }
+    ds->side = s;
+    return UA_OK;
+}
 
 static unsigned long long wait_limit_ns() {
     const unsigned long long v = g_wait_limit_ns.load(std::memory_order_relaxed);
@@ -412,6 +434,7 @@ static Problem make_problem(const int32_t *cu, const int32_t *lk, int32_t num_se
     // heads narrower than 128 columns: decode units of two adjacent kv heads,
     // whose rows of a slot are one run of the cache (see the decode kernel)
     if (kernel_head_size(d) != d) p.kv_heads_per_unit = 2;
+    p.split_sms = true;
     return p;
 }
 
@@ -494,6 +517,7 @@ extern "C" ua_status ua_plan_inspect(const int32_t *cu_seqlens_q_host,
     counts[5] = plan.pre_ctas;
     counts[6] = (int32_t)std::min<int64_t>(plan.dec_pages, INT32_MAX);
     counts[7] = (int32_t)std::min<size_t>(plan.layout.total_bytes, (size_t)INT32_MAX);
+    counts[8] = plan.split_pre_sms;
     const int64_t need = 2 * (int64_t)plan.pieces.size() + (int64_t)plan.tiles.size() +
                          (int64_t)plan.comb.size();
     if (n_items) *n_items = need;
@@ -572,7 +596,8 @@ extern "C" ua_status ua_profile_read(int32_t calls_back, float *ms, int32_t *lau
         return UA_ERR_CUDA;
     }
     // ev 0 before the plan copy, 1 after it, 2 after decode, 3 after prefill, 4 after combine
-    const int from[4] = {1, 2, 3, 0};
+    // a call whose kernels ran side by side: both timed from the fork (event 1)
+    const int from[4] = {1, ds->split[slot] ? 1 : 2, 3, 0};
     const int to[4] = {2, 3, 4, 1};
     for (int i = 0; i < 4; ++i) {
         ms[i] = -1.f;
@@ -751,71 +776,109 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
     }
     mark(1);
     cudaError_t e = cudaSuccess;
-    if (plan.dec_ctas > 0) {
-        DecodeParams dp{};
-        dp.q = static_cast<const __nv_bfloat16 *>(q);
-        dp.out = static_cast<__nv_bfloat16 *>(out);
-        dp.cu = cu_seqlens_q;
-        dp.seqused_k = seqused_k;
-        dp.block_table = block_table;
-        dp.bt_stride = block_table_stride;
-        dp.num_blocks = num_blocks;
-        dp.hq = num_q_heads;
-        dp.hkv = num_kv_heads;
-        dp.g = g;
-        dp.causal = causal != 0;
-        dp.scale_log2 = scale_log2;
-        dp.cta_begin = reinterpret_cast<const int32_t *>(pl + L.off_cta);
-        dp.pieces = reinterpret_cast<const DecPiece *>(pl + L.off_pieces);
-        dp.part_o = reinterpret_cast<float *>(ws + L.off_part_o);
-        dp.part_ml = reinterpret_cast<float *>(ws + L.off_part_ml);
-        dp.comb = reinterpret_cast<const CombUnit *>(pl + L.off_comb);
-        dp.comb_count = reinterpret_cast<int32_t *>(pl + L.off_comb_count);
-        dp.lse = lse;
-        dp.v_scale = v_scale;
-        dp.heads_per_unit = plan.dec_heads_per_unit;
-        dp.status = ds->status;
-        dp.wait_ns = wait_limit_ns();
-        dp.dq = head_size;
-        e = launch_decode(head_size, kv_fp8 != 0, dp, tm_kp, tm_vp, plan.dec_ctas, stream);
-        if (e != cudaSuccess) return UA_ERR_CUDA;
-    }
-    mark(2);
-    if (!plan.tiles.empty()) {
-        if (dq) {
-            e = launch_dequant_pages(k_cache, v_cache, block_table, block_table_stride, num_blocks,
-                                     reinterpret_cast<const int32_t *>(pl + L.off_dq),
-                                     (int32_t)plan.dq_seq.size(), plan.dq_pages,
-                                     reinterpret_cast<int32_t *>(ws + L.off_dq_bt), ws + L.off_dq_k,
-                                     ws + L.off_dq_v, num_kv_heads, head_size, ds->status, stream);
+    auto launch_dec = [&](cudaStream_t s) -> ua_status {
+        if (plan.dec_ctas > 0) {
+            DecodeParams dp{};
+            dp.q = static_cast<const __nv_bfloat16 *>(q);
+            dp.out = static_cast<__nv_bfloat16 *>(out);
+            dp.cu = cu_seqlens_q;
+            dp.seqused_k = seqused_k;
+            dp.block_table = block_table;
+            dp.bt_stride = block_table_stride;
+            dp.num_blocks = num_blocks;
+            dp.hq = num_q_heads;
+            dp.hkv = num_kv_heads;
+            dp.g = g;
+            dp.causal = causal != 0;
+            dp.scale_log2 = scale_log2;
+            dp.cta_begin = reinterpret_cast<const int32_t *>(pl + L.off_cta);
+            dp.pieces = reinterpret_cast<const DecPiece *>(pl + L.off_pieces);
+            dp.part_o = reinterpret_cast<float *>(ws + L.off_part_o);
+            dp.part_ml = reinterpret_cast<float *>(ws + L.off_part_ml);
+            dp.comb = reinterpret_cast<const CombUnit *>(pl + L.off_comb);
+            dp.comb_count = reinterpret_cast<int32_t *>(pl + L.off_comb_count);
+            dp.lse = lse;
+            dp.v_scale = v_scale;
+            dp.heads_per_unit = plan.dec_heads_per_unit;
+            dp.status = ds->status;
+            dp.wait_ns = wait_limit_ns();
+            dp.dq = head_size;
+            e = launch_decode(head_size, kv_fp8 != 0, dp, tm_kp, tm_vp, plan.dec_ctas, s);
             if (e != cudaSuccess) return UA_ERR_CUDA;
         }
-        PrefillParams pp{};
-        pp.k_cache = static_cast<const __nv_bfloat16 *>(k_pre);
-        pp.out = static_cast<__nv_bfloat16 *>(out);
-        pp.lse = lse;
-        pp.cu = cu_seqlens_q;
-        pp.seqused_k = seqused_k;
-        pp.block_table = bt_pre;
-        pp.bt_stride = block_table_stride;
-        pp.num_blocks = (int32_t)blocks_pre;
-        pp.v_scale = v_scale;
-        pp.hq = num_q_heads;
-        pp.hkv = num_kv_heads;
-        pp.g = g;
-        pp.causal = causal != 0;
-        pp.scale_log2 = scale_log2;
-        pp.tiles = reinterpret_cast<const PreTile *>(pl + L.off_tiles);
-        pp.tile_begin = reinterpret_cast<const int32_t *>(pl + L.off_pre_begin);
-        pp.sched = reinterpret_cast<int32_t *>(pl + L.off_sched);
-        pp.n_tiles = (int32_t)plan.tiles.size();
-        pp.status = ds->status;
-        e = pair_prefill ? launch_prefill_pair(head_size, pp, tm_q, tm_o, tm_k3, tm_vh, plan.pre_ctas, stream)
-                         : launch_prefill(head_size, plan.pre_claimed, pp, tm_q, tm_o, tm_k3, tm_vpre,
-                                          plan.pre_ctas, stream);
-        if (e != cudaSuccess) return UA_ERR_CUDA;
+        return UA_OK;
+    };
+    auto launch_pre = [&](cudaStream_t s) -> ua_status {
+        if (!plan.tiles.empty()) {
+            if (dq) {
+                e = launch_dequant_pages(k_cache, v_cache, block_table, block_table_stride, num_blocks,
+                                         reinterpret_cast<const int32_t *>(pl + L.off_dq),
+                                         (int32_t)plan.dq_seq.size(), plan.dq_pages,
+                                         reinterpret_cast<int32_t *>(ws + L.off_dq_bt), ws + L.off_dq_k,
+                                         ws + L.off_dq_v, num_kv_heads, head_size, ds->status, s);
+                if (e != cudaSuccess) return UA_ERR_CUDA;
+            }
+            PrefillParams pp{};
+            pp.k_cache = static_cast<const __nv_bfloat16 *>(k_pre);
+            pp.out = static_cast<__nv_bfloat16 *>(out);
+            pp.lse = lse;
+            pp.cu = cu_seqlens_q;
+            pp.seqused_k = seqused_k;
+            pp.block_table = bt_pre;
+            pp.bt_stride = block_table_stride;
+            pp.num_blocks = (int32_t)blocks_pre;
+            pp.v_scale = v_scale;
+            pp.hq = num_q_heads;
+            pp.hkv = num_kv_heads;
+            pp.g = g;
+            pp.causal = causal != 0;
+            pp.scale_log2 = scale_log2;
+            pp.tiles = reinterpret_cast<const PreTile *>(pl + L.off_tiles);
+            pp.tile_begin = reinterpret_cast<const int32_t *>(pl + L.off_pre_begin);
+            pp.sched = reinterpret_cast<int32_t *>(pl + L.off_sched);
+            pp.n_tiles = (int32_t)plan.tiles.size();
+            pp.status = ds->status;
+            e = pair_prefill ? launch_prefill_pair(head_size, pp, tm_q, tm_o, tm_k3, tm_vh, plan.pre_ctas, s)
+                             : launch_prefill(head_size, plan.pre_claimed, pp, tm_q, tm_o, tm_k3, tm_vpre,
+                                              plan.pre_ctas, s);
+            if (e != cudaSuccess) return UA_ERR_CUDA;
+        }
+        return UA_OK;
+    };
+    const bool split = plan.split_pre_sms > 0;
+    if (split) {
+        // side by side: the prefill kernel first (its CTAs take their SMs), the
+        // decode kernel on the library's second stream (the rest of the SMs)
+        st = side_stream(ds);
+        if (st != UA_OK) return st;
+        {
+            std::lock_guard<std::mutex> lock(ds->side_mutex);
+            if (cudaEventRecord(ds->fork, stream) != cudaSuccess ||
+                cudaStreamWaitEvent(ds->side, ds->fork, 0) != cudaSuccess) {
+                cudaGetLastError();
+                return UA_ERR_CUDA;
+            }
+        }
+        st = launch_pre(stream);
+        if (st != UA_OK) return st;
+        mark(3);
+        st = launch_dec(ds->side);
+        if (st != UA_OK) return st;
+        if (prof) cudaEventRecord(ds->ev[pslot][2], ds->side);
+        std::lock_guard<std::mutex> lock(ds->side_mutex);
+        if (cudaEventRecord(ds->join, ds->side) != cudaSuccess ||
+            cudaStreamWaitEvent(stream, ds->join, 0) != cudaSuccess) {
+            cudaGetLastError();
+            return UA_ERR_CUDA;
+        }
+    } else {
+        st = launch_dec(stream);
+        if (st != UA_OK) return st;
+        mark(2);
+        st = launch_pre(stream);
+        if (st != UA_OK) return st;
+        mark(3);
     }
-    mark(3);
     // (split units are merged inside the decode kernel: no separate combine step)
     mark(4);
     if (guard.slot >= 0) {
@@ -830,6 +893,7 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
         ds->ran[pslot][1] = !plan.tiles.empty();
         ds->ran[pslot][2] = false;
         ds->ran[pslot][3] = L.blob_bytes > 0;
+        ds->split[pslot] = split;
         ds->launches[pslot][0] = plan.dec_ctas > 0 ? 1 : 0;
         ds->launches[pslot][1] = plan.tiles.empty() ? 0 : (dq ? 2 : 1);   // page decode + prefill
         ds->launches[pslot][2] = 0;

@@ -53,6 +53,7 @@ int validate_problem(const Problem &p) {
 void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan) {
     // reuse the vectors' capacity across calls (the plan is thread-local in the API)
     plan.dec_ctas = 0;
+    plan.split_pre_sms = 0;
     plan.dec_pages = 0;
     plan.cta_begin.clear();
     plan.pieces.clear();
@@ -141,6 +142,43 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
     // got the longest item of a round gets the shortest of the next, which
     // keeps the workers' totals within about one item of each other.
     // O(items) host cost.
+    // ---- both kinds of work: the two kernels side by side on disjoint SMs
+    // (long items on SM pairs only; see kSplitDecodeGBsPerSm)
+    int32_t pre_sms = num_sms, dec_sms = num_sms;
+    if (p.split_sms && p.prefill_pair && !p.dequant_prefill && p.d == 128 && !units.empty() &&
+        !unsorted.empty() && num_sms >= 2 * kSplitMinDecodeSms) {
+        double bytes = 0.0, flops = 0.0, kv_sum = 0.0;
+        for (const Unit &u : units)
+            bytes += (double)(u.pages + kDecUnitCost) * (2.0 * kBlockSize * p.d * 2 * hpu);
+        for (const PreTile &t : unsorted) {
+            flops += 4.0 * t.nrows * (double)t.kv_tiles * kKvTile * p.d;
+            kv_sum += t.kv_tiles;
+        }
+        // the two-SM kernel takes long items only (as the deal below decides)
+        if (kv_sum >= (double)kClaimMinMeanKvTiles * (double)unsorted.size()) {
+            const double N = num_sms, r = kSplitDecodeGBsPerSm * 1e9, f = kSplitPairGflopsPerSm * 1e9;
+            const double bw = kSplitHbmGBs * 1e9;
+            auto t_dec = [&](double n) { return std::max(bytes / bw, bytes / (n * r)); };
+            auto t_pre = [&](double n) { return flops / (n * f); };
+            // F / (n f) = B / ((N - n) r)
+            const double n_bal = flops * r * N / (flops * r + bytes * f);
+            int32_t best = 0;
+            double best_t = t_dec(N) + t_pre(N);
+            for (int32_t n = std::max<int32_t>(2, ((int32_t)n_bal - 4) & ~1);
+                 n <= std::min<int32_t>(num_sms - kSplitMinDecodeSms, (int32_t)n_bal + 4); n += 2) {
+                const double t = std::max(t_pre(n), t_dec(N - n));
+                if (t < best_t) {
+                    best_t = t;
+                    best = n;
+                }
+            }
+            if (best > 0 && best_t * 100.0 <= (t_dec(N) + t_pre(N)) * (100 - kSplitMinGainPct)) {
+                pre_sms = best;
+                dec_sms = num_sms - best;
+                plan.split_pre_sms = best;
+            }
+        }
+    }
     if (!unsorted.empty()) {
         thread_local std::vector<PreTile> tl_sorted;
         thread_local std::vector<int32_t> tl_owner;
@@ -159,7 +197,7 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
         const bool long_items = kv_sum >= (int64_t)kClaimMinMeanKvTiles * (int64_t)sorted.size();
         // head size 256 has only the two-SM kernel: every item goes to SM pairs
         plan.pre_pair = p.prefill_pair && (long_items || p.d == 256);
-        const int32_t workers = plan.pre_pair ? std::max(num_sms / 2, 1) : std::max(num_sms, 1);
+        const int32_t workers = plan.pre_pair ? std::max(pre_sms / 2, 1) : std::max(pre_sms, 1);
         const int32_t ctas = (int32_t)std::min<size_t>(sorted.size(), (size_t)workers);
         plan.pre_ctas = ctas;
         plan.pre_claimed = !plan.pre_pair && p.prefill_claim && long_items;
@@ -191,7 +229,7 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
     for (const Unit &u : units) total += u.pages;
     plan.dec_pages = total;
     if (total > 0) {
-        const int64_t want = (int64_t)kDecCtasPerSm * std::max(num_sms, 1);
+        const int64_t want = (int64_t)kDecCtasPerSm * std::max(dec_sms, 1);
         const int64_t ctas = std::min<int64_t>(want, total);
         plan.dec_ctas = (int32_t)ctas;
         plan.cta_begin.assign(ctas + 1, 0);

@@ -9,6 +9,8 @@ namespace ua {
 
 struct Plan {
     int32_t dec_ctas = 0;
+    int32_t split_pre_sms = 0;          // > 0: the prefill kernel runs on this many SMs and the decode
+                                        // kernel on the rest, at the same time
     int32_t dec_heads_per_unit = 1;     // kv heads per decode unit (1 or 2)
     int64_t dec_pages = 0;
     std::vector<int32_t> cta_begin;     // dec_ctas + 1

@@ -80,9 +80,20 @@ def compare_plans(q_lens, k_lens, hq, hk, d, causal=True):
     dp = ua.device_plan(_i32(cu), _i32(sk), causal, hq, hk, d, stride, max_total_q=int(cu[-1]) + 7)
     h = dp["header"]
     assert h[7] == 0, "device planner reported an error"
+    pieces, slots, tiles, comb = _host_plan_rows(items)
+    # a host plan that runs its two kernels side by side gives the decode kernel
+    # part of the SMs; the device plan (fixed grids) gives it all of them: only
+    # the prefill items are compared then
+    side = counts["prefill_sms_side_by_side"]
+    if side:
+        assert int(h[0]) == 2 * sms and counts["dec_ctas"] == 2 * (sms - side)
+        assert int(h[5]) == counts["prefill_tiles"] and counts["prefill_ctas"] == side // 2
+        as_rows = lambda a: np.sort(np.ascontiguousarray(a, dtype=np.int32).view("i4,i4,i4,i4,i4"),  # noqa: E731
+                                    axis=0)
+        np.testing.assert_array_equal(as_rows(dp["tiles"][:, :5]), as_rows(tiles[:, 1:]))
+        return counts
     assert (int(h[0]), int(h[1]), int(h[2]), int(h[3])) == (
         counts["dec_ctas"], counts["pieces"], counts["split_units"], counts["slots"])
-    pieces, slots, tiles, comb = _host_plan_rows(items)
     # long items at head size 128: the host deals them to SM pairs (the two-SM
     # kernel), the device to single SMs (its graph-captured launch is fixed
     # before the batch's item lengths are known)

@@ -119,7 +119,14 @@ def check_plan(q_lens, k_lens, hq, hk, d=128, causal=True, num_sms=152):
     ctas = [t[1] for t in tiles]
     assert [t[7] for t in tiles] == list(range(len(tiles)))
     long_items = bool(tiles) and sum(t[6] for t in tiles) >= 16 * len(tiles)
-    workers = max(1, num_sms // 2) if ((d == 128 and long_items) or d == 256) else num_sms
+    # side by side (decode rows beside long items on SM pairs): the prefill
+    # kernel gets that many SMs, the decode kernel the rest
+    side = counts["prefill_sms_side_by_side"]
+    if side:
+        assert d == 128 and long_items and pieces and side % 2 == 0
+        assert counts["dec_ctas"] <= 2 * (num_sms - side)
+    pre_sms = side or num_sms
+    workers = max(1, pre_sms // 2) if ((d == 128 and long_items) or d == 256) else pre_sms
     if tiles:
         assert ctas == sorted(ctas) and min(ctas) >= 0
         assert counts["prefill_ctas"] == len(set(ctas)) == min(len(tiles), workers)
@@ -145,9 +152,34 @@ def test_standard_batches(idx):
 
 
 def test_long_mixed_batch():
+    """Llama-3-70B-shaped long mixed step: 2.7 GB of decode pages beside 0.7
+    PFLOP of long prefill items.  Side by side, the balance of the decode
+    kernel's ~60 GB/s per SM and the two-SM kernel's ~9.8 TFLOP/s per SM puts
+    the prefill kernel on ~94 SMs and the decode kernel's two CTAs per SM on
+    the rest."""
     s = W.config_spec(5)
     c = check_plan(s.q_lens, s.k_lens, s.num_q_heads, s.num_kv_heads, s.head_size, s.causal)
-    assert c["dec_ctas"] == 2 * 152
+    side = c["prefill_sms_side_by_side"]
+    assert 84 <= side <= 104
+    assert c["dec_ctas"] == 2 * (152 - side)
+    assert c["prefill_ctas"] == side // 2
+
+
+def test_side_by_side_only_for_long_items_on_sm_pairs():
+    """Batches that keep their two kernels one after the other: short prefill
+    items (one SM each), head size 64, no decode rows, and few SMs."""
+    s = W.config_spec(4)       # 256 decode rows beside 512-token chunks: short items
+    c = check_plan(s.q_lens, s.k_lens, s.num_q_heads, s.num_kv_heads, s.head_size, s.causal)
+    assert c["prefill_sms_side_by_side"] == 0 and c["dec_ctas"] == 2 * 152
+    s = W.config_spec(5)
+    c = check_plan(s.q_lens, s.k_lens, s.num_q_heads, s.num_kv_heads, 64, s.causal)
+    assert c["prefill_sms_side_by_side"] == 0
+    c = check_plan(s.q_lens[s.q_lens > 1], s.k_lens[s.q_lens > 1], s.num_q_heads,
+                   s.num_kv_heads, s.head_size, s.causal)
+    assert c["prefill_sms_side_by_side"] == 0 and c["pieces"] == 0
+    c = check_plan(s.q_lens, s.k_lens, s.num_q_heads, s.num_kv_heads, s.head_size, s.causal,
+                   num_sms=12)
+    assert c["prefill_sms_side_by_side"] == 0
 
 
 def test_long_prefill_items_go_to_sm_pairs_at_head_size_128():
@@ -161,6 +193,10 @@ def test_long_prefill_items_go_to_sm_pairs_at_head_size_128():
         return counts, [r[1] for r in items if r[0] == 2]
     s = W.config_spec(5)
     counts, ctas = prefill_ctas(s.q_lens, s.k_lens, s.num_q_heads, s.num_kv_heads, 128)
+    pairs = (counts["prefill_sms_side_by_side"] or 152) // 2     # beside the decode kernel
+    assert min(ctas) == 0 and max(ctas) == pairs - 1 and counts["prefill_ctas"] == pairs
+    counts, ctas = prefill_ctas(s.q_lens[s.q_lens > 1], s.k_lens[s.q_lens > 1], s.num_q_heads,
+                                s.num_kv_heads, 128)
     assert min(ctas) == 0 and max(ctas) == 75 and counts["prefill_ctas"] == 76
     s = W.config_spec(3)
     counts, ctas = prefill_ctas(s.q_lens, s.k_lens, s.num_q_heads, s.num_kv_heads, 128)
