@@ -137,21 +137,25 @@ struct Problem {
                                      // side by side on disjoint sets of SMs
 };
 
-// Side by side.  A batch of decode rows and long prefill items (the two-SM
-// kernel, head size 128, bf16 cache) can run its decode kernel (HBM-bound)
-// and its prefill kernel (tensor-bound) at the same time on disjoint SMs:
-// the prefill kernel is launched first and its CTA pairs take n SMs, the
-// decode kernel's 2 (N - n) CTAs take the rest.  n balances the two
-// estimated times, each kernel on its own SMs: the decode kernel moves up to
-// kSplitDecodeGBsPerSm GB/s per SM (the pages in flight of its two CTAs; at
-// most kSplitHbmGBs in all), the two-SM prefill kernel runs
-// kSplitPairGflopsPerSm GFLOP/s per SM (both measured on a GB300).  The split
-// is taken when it is estimated to save kSplitMinGainPct percent or more of
-// the two kernels' time one after the other.
-constexpr double kSplitDecodeGBsPerSm = 60.0;
+// Side by side.  A batch of decode rows and prefill items (head size 128,
+// bf16 cache) can run its decode kernel (HBM-bound) and its prefill kernel
+// (tensor-bound) at the same time on disjoint SMs: the prefill kernel is
+// launched first and its CTAs (or CTA pairs) take n SMs, the decode kernel's
+// 2 (N - n) CTAs take the rest.  n balances the two estimated times, each
+// kernel on its own SMs: the decode kernel moves up to kSplitDecodeGBsPerSm
+// GB/s per SM (the pages in flight of its two CTAs; at most kSplitHbmGBs in
+// all), a unit costing kSplitUnitPages pages more; the two-SM prefill kernel
+// runs kSplitPairGflopsPerSm GFLOP/s per SM, the one-SM kernel
+// kSplitOneGflopsPerSm (all measured on a GB300: the Llama-3-70B long mixed
+// step and the Llama-3.1-8B step of 256 decode rows beside four 512-token
+// chunks).  The split is taken when it is estimated to save kSplitMinGainPct
+// percent or more of the two kernels' time one after the other.
+constexpr double kSplitDecodeGBsPerSm = 61.0;
 constexpr double kSplitHbmGBs = 6200.0;
+constexpr double kSplitUnitPages = 18.0;
 constexpr double kSplitPairGflopsPerSm = 9800.0;
-constexpr int kSplitMinGainPct = 10;
+constexpr double kSplitOneGflopsPerSm = 5700.0;
+constexpr int kSplitMinGainPct = 8;
 constexpr int kSplitMinDecodeSms = 8;
 
 // Offsets of the plan sections inside the device workspace.

@@ -143,40 +143,40 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
     // keeps the workers' totals within about one item of each other.
     // O(items) host cost.
     // ---- both kinds of work: the two kernels side by side on disjoint SMs
-    // (long items on SM pairs only; see kSplitDecodeGBsPerSm)
+    // (head size 128, bf16 cache; see kSplitDecodeGBsPerSm)
     int32_t pre_sms = num_sms, dec_sms = num_sms;
-    if (p.split_sms && p.prefill_pair && !p.dequant_prefill && p.d == 128 && !units.empty() &&
-        !unsorted.empty() && num_sms >= 2 * kSplitMinDecodeSms) {
+    if (p.split_sms && !p.dequant_prefill && p.d == 128 && !units.empty() && !unsorted.empty() &&
+        num_sms >= 2 * kSplitMinDecodeSms) {
+        const double page_bytes = 2.0 * kBlockSize * p.d * 2 * hpu;
         double bytes = 0.0, flops = 0.0, kv_sum = 0.0;
-        for (const Unit &u : units)
-            bytes += (double)(u.pages + kDecUnitCost) * (2.0 * kBlockSize * p.d * 2 * hpu);
+        for (const Unit &u : units) bytes += ((double)u.pages + kSplitUnitPages) * page_bytes;
         for (const PreTile &t : unsorted) {
             flops += 4.0 * t.nrows * (double)t.kv_tiles * kKvTile * p.d;
             kv_sum += t.kv_tiles;
         }
-        // the two-SM kernel takes long items only (as the deal below decides)
-        if (kv_sum >= (double)kClaimMinMeanKvTiles * (double)unsorted.size()) {
-            const double N = num_sms, r = kSplitDecodeGBsPerSm * 1e9, f = kSplitPairGflopsPerSm * 1e9;
-            const double bw = kSplitHbmGBs * 1e9;
-            auto t_dec = [&](double n) { return std::max(bytes / bw, bytes / (n * r)); };
-            auto t_pre = [&](double n) { return flops / (n * f); };
-            // F / (n f) = B / ((N - n) r)
-            const double n_bal = flops * r * N / (flops * r + bytes * f);
-            int32_t best = 0;
-            double best_t = t_dec(N) + t_pre(N);
-            for (int32_t n = std::max<int32_t>(2, ((int32_t)n_bal - 4) & ~1);
-                 n <= std::min<int32_t>(num_sms - kSplitMinDecodeSms, (int32_t)n_bal + 4); n += 2) {
-                const double t = std::max(t_pre(n), t_dec(N - n));
-                if (t < best_t) {
-                    best_t = t;
-                    best = n;
-                }
+        // long items run on SM pairs (as the deal below decides), short ones on one SM each
+        const bool pairs = p.prefill_pair && kv_sum >= (double)kClaimMinMeanKvTiles * (double)unsorted.size();
+        const double N = num_sms, r = kSplitDecodeGBsPerSm * 1e9, bw = kSplitHbmGBs * 1e9;
+        const double f = (pairs ? kSplitPairGflopsPerSm : kSplitOneGflopsPerSm) * 1e9;
+        auto t_dec = [&](double n) { return std::max(bytes / bw, bytes / (n * r)); };
+        auto t_pre = [&](double n) { return flops / (n * f); };
+        // F / (n f) = B / ((N - n) r)
+        const double n_bal = flops * r * N / (flops * r + bytes * f);
+        const int32_t step = pairs ? 2 : 1;
+        int32_t best = 0;
+        double best_t = t_dec(N) + t_pre(N);
+        for (int32_t n = std::max<int32_t>(step, ((int32_t)n_bal - 4) / step * step);
+             n <= std::min<int32_t>(num_sms - kSplitMinDecodeSms, (int32_t)n_bal + 4); n += step) {
+            const double t = std::max(t_pre(n), t_dec(N - n));
+            if (t < best_t) {
+                best_t = t;
+                best = n;
             }
-            if (best > 0 && best_t * 100.0 <= (t_dec(N) + t_pre(N)) * (100 - kSplitMinGainPct)) {
-                pre_sms = best;
-                dec_sms = num_sms - best;
-                plan.split_pre_sms = best;
-            }
+        }
+        if (best > 0 && best_t * 100.0 <= (t_dec(N) + t_pre(N)) * (100 - kSplitMinGainPct)) {
+            pre_sms = best;
+            dec_sms = num_sms - best;
+            plan.split_pre_sms = best;
         }
     }
     if (!unsorted.empty()) {

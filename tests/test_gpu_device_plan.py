@@ -87,7 +87,8 @@ def compare_plans(q_lens, k_lens, hq, hk, d, causal=True):
     side = counts["prefill_sms_side_by_side"]
     if side:
         assert int(h[0]) == 2 * sms and counts["dec_ctas"] == 2 * (sms - side)
-        assert int(h[5]) == counts["prefill_tiles"] and counts["prefill_ctas"] == side // 2
+        assert int(h[5]) == counts["prefill_tiles"]
+        assert counts["prefill_ctas"] in (min(side, counts["prefill_tiles"]), side // 2)
         as_rows = lambda a: np.sort(np.ascontiguousarray(a, dtype=np.int32).view("i4,i4,i4,i4,i4"),  # noqa: E731
                                     axis=0)
         np.testing.assert_array_equal(as_rows(dp["tiles"][:, :5]), as_rows(tiles[:, 1:]))
