@@ -660,6 +660,9 @@ ua_status run_attention(const void *q, const void *k_cache, const void *v_cache,
                               num_kv_heads, head_size, block_size, block_table_stride, causal);
     // e4m3 pages: decode units take two adjacent kv heads (256-byte rows per slot)
     if (kv_fp8) pr.kv_heads_per_unit = 2;
+    // the entry point that must allocate nothing creates no second stream either:
+    // its two kernels run one after the other (its plan is sized that way)
+    if (!pinned_plan) pr.split_sms = false;
     int v = validate_problem(pr);
     if (v) return static_cast<ua_status>(v);
     if (!std::isfinite(softmax_scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
