@@ -11,6 +11,11 @@ capture by the host-planned entry points, and in-place log-sum-exp merges.
 * A host-planned call fixes its plan and grid sizes from the host lengths of
   one batch; on a stream that is being captured it returns UA_ERR_UNSUPPORTED
   and enqueues nothing (graph users plan on the device instead).
+* A call that runs its decode and prefill kernels side by side (the decode
+  kernel on a library stream forked from the caller's) is still ordered on
+  the caller's stream: work the caller enqueues after it sees the whole
+  output, and the next call may reuse the workspace at once; calls from two
+  streams that share the library's second stream give the same results.
 * ua_merge_attn_states may write lse_out over lse_a (chained cascade merges);
   at head size 96 a row's 12 threads cross warp boundaries, which is where a
   write of the merged lse could reach a thread that has not read it yet.
@@ -113,6 +118,53 @@ def test_interleaved_calls_on_two_streams():
     for si in range(len(streams)):
         for k in range(len(batches)):
             assert torch.equal(outs[si][k], want[k]), (si, k)
+
+
+SIDE_BY_SIDE = [
+    # decode rows beside short prefill items (the one-SM kernel) and beside a
+    # long chunk (SM pairs); both run side by side on a 152-SM GB300
+    ([1] * 32 + [512] * 2, [1000] * 32 + [512] * 2, 32, 8),
+    ([1] * 16 + [1024], [8000] * 16 + [4096], 32, 8),
+]
+
+
+@pytest.mark.parametrize("case", SIDE_BY_SIDE, ids=["one_sm", "pairs"])
+def test_side_by_side_call_is_ordered_on_the_callers_stream(case):
+    import torch
+    import paged_varlen_attention_gb300 as ua
+
+    q_lens, k_lens, hq, hk = case
+    b = W.materialize(W.custom_spec(q_lens, k_lens, hq, hk, 128, seed=31))
+    s = b.spec
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    counts, _ = ua.plan_inspect(b.cu_seqlens_q, b.seqused_k, hq, hk, 128, b.block_table_stride,
+                                s.causal, num_sms=sms)
+    if counts["prefill_sms_side_by_side"] == 0:
+        pytest.skip(f"this batch runs its kernels one after the other on {sms} SMs")
+    dev = to_device(b)
+    want = _call(b, dev, None).clone()
+    torch.cuda.synchronize()
+    need = ua.workspace_size(b.cu_seqlens_q, b.seqused_k, hq, hk, 128, b.block_table_stride,
+                             s.causal)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    wss = [torch.empty(need, dtype=torch.uint8, device="cuda") for _ in streams]
+    outs = [torch.empty_like(want) for _ in streams]
+    copies = [[] for _ in streams]
+    for st in streams:
+        st.wait_stream(torch.cuda.current_stream())
+    # back to back on each stream, no host synchronisation: the output is
+    # cleared, computed and copied on the stream; the next call reuses the
+    # workspace and the output straight away
+    for _ in range(4):
+        for si, st in enumerate(streams):
+            with torch.cuda.stream(st):
+                outs[si].fill_(float("nan"))
+                _call(b, dev, outs[si], ws=wss[si], stream=st)
+                copies[si].append(outs[si].clone())
+    torch.cuda.synchronize()
+    for si in range(len(streams)):
+        for c in copies[si]:
+            assert torch.equal(c, want), si
 
 
 def test_host_planned_call_refuses_stream_capture():
