@@ -676,6 +676,7 @@ def dominant_roofline(workload, spec, work, kern, peaks):
         roof["peak_source"] += (f" x {side}/{n} SMs: the kernel ran on {side} SMs beside the decode "
                                 f"kernel on the other {n - side}; timed from the fork to its end")
         roof["sms"] = side
+        roof["frac_of_whole_gpu_peak"] = roof["achieved"] / peaks["bf16_tflops"]
     return roof
 
 
