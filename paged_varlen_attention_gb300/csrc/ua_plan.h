@@ -143,7 +143,7 @@ struct Problem {
 // launched first and its CTAs (or CTA pairs) take n SMs, the decode kernel's
 // 2 (N - n) CTAs take the rest.  n balances the two estimated times, each
 // kernel on its own SMs: the decode kernel moves up to kSplitDecodeGBsPerSm
-// GB/s per SM (~30 GB/s for each of its two CTAs; at most kSplitHbmGBs in
+// GB/s per SM (the pages in flight of its two CTAs; at most kSplitHbmGBs in
 // all), a unit costing kSplitUnitPages pages more; the two-SM prefill kernel
 // runs kSplitPairGflopsPerSm GFLOP/s per SM, the one-SM kernel
 // kSplitOneGflopsPerSm (all measured on a GB300: the Llama-3-70B long mixed
