@@ -9,12 +9,13 @@
 // distinguish between prefill + decode", vLLM PR #16828, PR description):
 // each page is fetched once and feeds all heads of its group.
 //
-// Structure (one persistent CTA = 4 consumer warps + 1 producer warp):
-//   * the producer walks the CTA's pieces (contiguous page ranges of
+// Structure (one persistent CTA = 4 consumer warps + 2 producer warps):
+//   * the K producer walks the CTA's pieces (contiguous page ranges of
 //     (sequence, kv head, row tile) units), reads 32 block-table entries at a
-//     time, and issues one TMA box per K page and one per V page (a 5-D view
-//     of the cache, so one box holds all D columns of the page's 16 tokens)
-//     into a ring of shared-memory stages (128-byte swizzle);
+//     time, and issues one TMA box per K page (a 5-D view of the cache, so
+//     one box holds all D columns of the page's 16 tokens) into a ring of
+//     shared-memory stages (128-byte swizzle); the V producer walks the same
+//     pages and issues their V boxes into the same stages;
 //   * consumer warp w takes pages w, w+4, ... of each piece: S = Q K^T with
 //     mma.sync m16n8k16 (bf16 in, fp32 accumulate), bottom-right causal mask,
 //     online softmax in the exp2 domain (O and l rescaled only when a row
@@ -79,7 +80,11 @@ struct DecCfg {
     static constexpr int kStages = (D == 64) ? 16 : kNarrow ? 4 : 8;
     static constexpr int kMinCtasPerSm = (D == 256) ? 1 : 2;
     static constexpr int kConsumerWarps = 4;
-    static constexpr int kThreads = (kConsumerWarps + 1) * 32;
+    // consumer warps, then the K producer (descriptors, Q rows, K boxes), then
+    // the V producer (V boxes): one warp issuing both boxes of every page
+    // held a CTA to ~30 GB/s (a copy of the kernel without its page compute
+    // moved no more, nor with 16 stages instead of 8)
+    static constexpr int kThreads = (kConsumerWarps + 2) * 32;
     static constexpr int kMergeFloats = kDecRows * D + 2 * kDecRows;   // per warp
     // ring of piece descriptors + Q tiles, filled by the producer ahead of use
     static constexpr int kRing = 3;
@@ -339,6 +344,22 @@ __device__ __forceinline__ void merge_unit(const DecodeParams &p, int q0, int kv
     }
 }
 
+// One page's box(es) of one tensor into dst, completing on bar: the 5-D view
+// (all D columns of 16 slots, [chunk][slot][64], 128-byte swizzle; hp heads
+// of an e4m3 page in one box), or for a narrower head one box per 64
+// columns of (dq, slot, kv head, block), zeros past dq, each box the unit's
+// hp heads: [chunk][head][slot][64].
+template <bool kNarrow, int kChunks>
+__device__ __forceinline__ void issue_page(uint32_t dst, const CUtensorMap *tm, int kvh, int b, int hp,
+                                           uint32_t bar, uint64_t policy) {
+    if constexpr (!kNarrow) {
+        tma_load_5d_hint(dst, tm, 0, 0, 0, kvh, b, bar, policy);
+    } else {
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) tma_load_4d_hint(dst + c * hp * 2048, tm, 64 * c, 0, kvh, b, bar, policy);
+    }
+}
+
 // kNarrow: a head narrower than D (p.dq < D, see above).
 template <int D, bool KV8, bool kNarrow>
 __global__ void __launch_bounds__(DecCfg<D, KV8, kNarrow>::kThreads,
@@ -394,10 +415,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV8, kNarrow>::kThreads,
 
     if (warp == C::kConsumerWarps) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
-        }
+        if (lane == 0) prefetch_tensormap(&tm_k);
         const uint64_t policy = l2_policy_evict_first();
         const int hp = KV8 || kNarrow ? p.heads_per_unit : 1;   // kv heads per unit (and per box)
         bool ok = true;
@@ -477,24 +495,17 @@ __global__ void __launch_bounds__(DecCfg<D, KV8, kNarrow>::kThreads,
                             good = 0;
                         } else {
                             const uint32_t fb = full0 + 8 * st;
-                            const uint32_t kdst = stage0 + st * C::kStageBytes;
-                            const uint32_t vdst = kdst + C::kPageBytes;
+                            // the stage's K and V bytes (the V producer's boxes complete
+                            // on the same barrier, before or after this)
                             mbar_arrive_expect_tx(fb, 2u * hp * C::kHeadPageBytes);
-                            if constexpr (!kNarrow) {
-                                // one box per page and tensor: all D columns of 16 tokens,
-                                // laid out [chunk][slot][64] with the 128-byte swizzle
-                                tma_load_5d_hint(kdst, &tm_k, 0, 0, 0, pc.kvh, b, fb, policy);
-                                tma_load_5d_hint(vdst, &tm_v, 0, 0, 0, pc.kvh, b, fb, policy);
-                            } else {
-                                // a narrower head: one box per 64 columns of (dq, slot, kv
-                                // head, block), zeros past dq, each box the unit's hp heads:
-                                // laid out [chunk][head][slot][64]
-#pragma unroll
-                                for (int c = 0; c < C::kChunks; ++c) {
-                                    tma_load_4d_hint(kdst + c * hp * 2048, &tm_k, 64 * c, 0, pc.kvh, b, fb, policy);
-                                    tma_load_4d_hint(vdst + c * hp * 2048, &tm_v, 64 * c, 0, pc.kvh, b, fb, policy);
-                                }
-                            }
+                            issue_page<kNarrow, C::kChunks>(stage0 + st * C::kStageBytes, &tm_k, pc.kvh, b, hp,
+                                                            fb, policy);
+                            // a narrower head's pages (two boxes per tensor) were measured
+                            // faster from this one warp (Phi-3-mini-shaped decode: 405 against
+                            // 420 us with the V producer)
+                            if constexpr (kNarrow)
+                                issue_page<kNarrow, C::kChunks>(stage0 + st * C::kStageBytes + C::kPageBytes,
+                                                                &tm_v, pc.kvh, b, hp, fb, policy);
                         }
                     }
                     ok = __shfl_sync(0xffffffffu, good, 0) != 0;
@@ -507,6 +518,49 @@ __global__ void __launch_bounds__(DecCfg<D, KV8, kNarrow>::kThreads,
         if (lane == 0)
             for (uint32_t x = (filled > (uint32_t)C::kRing ? filled - C::kRing : 0); x < filled; ++x)
                 mbar_wait(pfull0 + 8 * (x % C::kRing), (x / C::kRing) & 1, p.status);
+    } else if (warp == C::kConsumerWarps + 1) {
+        // (a narrower head's V boxes come from the K producer)
+        if constexpr (!kNarrow) {
+            // ------------------------------------------------------------ V producer
+            // The same pages in the same order as the K producer, into the same
+            // stages: each V box once the stage is free (the K producer's
+            // expect-tx covers its bytes; a box that lands first leaves the
+            // barrier's transaction count below zero until then, and the phase
+            // cannot complete before the K producer's arrival).
+            if (lane == 0) prefetch_tensormap(&tm_v);
+            const uint64_t policy = l2_policy_evict_first();
+            const int hp = KV8 || kNarrow ? p.heads_per_unit : 1;
+            bool ok = true;
+            uint32_t vissued = 0;
+            for (int pi = pbeg; pi < pend && ok; ++pi) {
+                const DecPiece pc = p.pieces[pi];
+                const int32_t *bt_row = p.block_table + (int64_t)pc.seq * p.bt_stride;
+                for (int base = pc.page_begin; base < pc.page_end && ok; base += 32) {
+                    const int n = min(32, pc.page_end - base);
+                    int bid = 0;
+                    if (lane < n) {
+                        bid = __ldg(bt_row + base + lane);
+                        if (bid < 0 || bid >= p.num_blocks) bid = p.num_blocks;   // reported by the K producer
+                    }
+                    for (int k = 0; k < n; ++k) {
+                        const int b = __shfl_sync(0xffffffffu, bid, k);
+                        int good = 1;
+                        if (lane == 0) {
+                            const uint32_t st = vissued % C::kStages;
+                            const uint32_t ph = (vissued / C::kStages) & 1;
+                            if (!mbar_wait(empty0 + 8 * st, ph ^ 1, p.status, p.wait_ns))
+                                good = 0;
+                            else
+                                issue_page<kNarrow, C::kChunks>(stage0 + st * C::kStageBytes + C::kPageBytes, &tm_v,
+                                                                pc.kvh, b, hp, full0 + 8 * st, policy);
+                        }
+                        ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+                        if (!ok) break;
+                        ++vissued;
+                    }
+                }
+            }
+        }
     } else {
         // ------------------------------------------------------------ consumers
         const int w = warp;

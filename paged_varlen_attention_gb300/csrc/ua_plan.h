@@ -143,14 +143,16 @@ struct Problem {
 // launched first and its CTAs (or CTA pairs) take n SMs, the decode kernel's
 // 2 (N - n) CTAs take the rest.  n balances the two estimated times, each
 // kernel on its own SMs: the decode kernel moves up to kSplitDecodeGBsPerSm
-// GB/s per SM (the pages in flight of its two CTAs; at most kSplitHbmGBs in
-// all), a unit costing kSplitUnitPages pages more; the two-SM prefill kernel
-// runs kSplitPairGflopsPerSm GFLOP/s per SM, the one-SM kernel
+// GB/s per SM (~33 GB/s for each of its two CTAs, what their producer warps
+// issue; at most kSplitHbmGBs in all), a unit costing kSplitUnitPages pages
+// more; the two-SM prefill kernel
+// runs kSplitPairGflopsPerSm GFLOP/s per SM (the pair with the most long
+// items ends last), the one-SM kernel
 // kSplitOneGflopsPerSm (all measured on a GB300: the Llama-3-70B long mixed
 // step and the Llama-3.1-8B step of 256 decode rows beside four 512-token
 // chunks).  The split is taken when it is estimated to save kSplitMinGainPct
 // percent or more of the two kernels' time one after the other.
-constexpr double kSplitDecodeGBsPerSm = 61.0;
+constexpr double kSplitDecodeGBsPerSm = 68.0;
 constexpr double kSplitHbmGBs = 6200.0;
 constexpr double kSplitUnitPages = 18.0;
 constexpr double kSplitPairGflopsPerSm = 9800.0;

@@ -10,6 +10,7 @@
 #include "ua_planner.h"
 
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 
 namespace ua {
@@ -159,7 +160,14 @@ void build_plan(const Problem &p, int num_sms, bool prefill_enabled, Plan &plan)
         const double N = num_sms, r = kSplitDecodeGBsPerSm * 1e9, bw = kSplitHbmGBs * 1e9;
         const double f = (pairs ? kSplitPairGflopsPerSm : kSplitOneGflopsPerSm) * 1e9;
         auto t_dec = [&](double n) { return std::max(bytes / bw, bytes / (n * r)); };
-        auto t_pre = [&](double n) { return flops / (n * f); };
+        // long items on pairs: the pair with the most items (the deal gives each
+        // ceil(items / pairs) or one fewer, of about equal length) ends last
+        const double n_items = (double)unsorted.size();
+        auto t_pre = [&](double n) {
+            if (!pairs) return flops / (n * f);
+            const double per = std::ceil(n_items / std::max(1.0, std::floor(n / 2)));
+            return flops / n_items * per / (2.0 * f);
+        };
         // F / (n f) = B / ((N - n) r)
         const double n_bal = flops * r * N / (flops * r + bytes * f);
         const int32_t step = pairs ? 2 : 1;
