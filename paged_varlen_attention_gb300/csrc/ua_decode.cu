@@ -83,8 +83,12 @@ struct DecCfg {
     // consumer warps, then the K producer (descriptors, Q rows, K boxes), then
     // the V producer (V boxes): one warp issuing both boxes of every page
     // held a CTA to ~30 GB/s (a copy of the kernel without its page compute
-    // moved no more, nor with 16 stages instead of 8)
-    static constexpr int kThreads = (kConsumerWarps + 2) * 32;
+    // moved no more, nor with 16 stages instead of 8).  A narrower head's
+    // kernel keeps one producer warp for both (measured faster there: the
+    // Phi-3-mini-shaped decode 405 us against 420 with two, 424 with an idle
+    // sixth warp)
+    static constexpr int kProducerWarps = kNarrow ? 1 : 2;
+    static constexpr int kThreads = (kConsumerWarps + kProducerWarps) * 32;
     static constexpr int kMergeFloats = kDecRows * D + 2 * kDecRows;   // per warp
     // ring of piece descriptors + Q tiles, filled by the producer ahead of use
     static constexpr int kRing = 3;
@@ -415,7 +419,10 @@ __global__ void __launch_bounds__(DecCfg<D, KV8, kNarrow>::kThreads,
 
     if (warp == C::kConsumerWarps) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) prefetch_tensormap(&tm_k);
+        if (lane == 0) {
+            prefetch_tensormap(&tm_k);
+            if constexpr (kNarrow) prefetch_tensormap(&tm_v);
+        }
         const uint64_t policy = l2_policy_evict_first();
         const int hp = KV8 || kNarrow ? p.heads_per_unit : 1;   // kv heads per unit (and per box)
         bool ok = true;
@@ -498,14 +505,19 @@ __global__ void __launch_bounds__(DecCfg<D, KV8, kNarrow>::kThreads,
                             // the stage's K and V bytes (the V producer's boxes complete
                             // on the same barrier, before or after this)
                             mbar_arrive_expect_tx(fb, 2u * hp * C::kHeadPageBytes);
-                            issue_page<kNarrow, C::kChunks>(stage0 + st * C::kStageBytes, &tm_k, pc.kvh, b, hp,
-                                                            fb, policy);
-                            // a narrower head's pages (two boxes per tensor) were measured
-                            // faster from this one warp (Phi-3-mini-shaped decode: 405 against
-                            // 420 us with the V producer)
-                            if constexpr (kNarrow)
-                                issue_page<kNarrow, C::kChunks>(stage0 + st * C::kStageBytes + C::kPageBytes,
-                                                                &tm_v, pc.kvh, b, hp, fb, policy);
+                            const uint32_t kdst = stage0 + st * C::kStageBytes;
+                            if constexpr (!kNarrow) {
+                                issue_page<kNarrow, C::kChunks>(kdst, &tm_k, pc.kvh, b, hp, fb, policy);
+                            } else {
+                                // a narrower head's kernel has no V producer warp: both
+                                // tensors' boxes, one per 64 columns (see issue_page)
+                                const uint32_t vdst = kdst + C::kPageBytes;
+#pragma unroll
+                                for (int c = 0; c < C::kChunks; ++c) {
+                                    tma_load_4d_hint(kdst + c * hp * 2048, &tm_k, 64 * c, 0, pc.kvh, b, fb, policy);
+                                    tma_load_4d_hint(vdst + c * hp * 2048, &tm_v, 64 * c, 0, pc.kvh, b, fb, policy);
+                                }
+                            }
                         }
                     }
                     ok = __shfl_sync(0xffffffffu, good, 0) != 0;
@@ -519,7 +531,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV8, kNarrow>::kThreads,
             for (uint32_t x = (filled > (uint32_t)C::kRing ? filled - C::kRing : 0); x < filled; ++x)
                 mbar_wait(pfull0 + 8 * (x % C::kRing), (x / C::kRing) & 1, p.status);
     } else if (warp == C::kConsumerWarps + 1) {
-        // (a narrower head's V boxes come from the K producer)
+        // (no such warp in a narrower head's kernel: its V boxes come from the K producer)
         if constexpr (!kNarrow) {
             // ------------------------------------------------------------ V producer
             // The same pages in the same order as the K producer, into the same
