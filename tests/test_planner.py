@@ -163,6 +163,10 @@ def test_long_mixed_batch():
     assert 84 <= side <= 104
     assert c["dec_ctas"] == 2 * (152 - side)
     assert c["prefill_ctas"] == side // 2
+    # the balance counts the items of the busiest pair: 1024 items on 47 or 48
+    # pairs put 22 on one (no faster than 47), on 49 pairs 21
+    pairs = side // 2
+    assert -(-c["prefill_tiles"] // pairs) < -(-c["prefill_tiles"] // (pairs - 1))
 
 
 def test_side_by_side_with_short_prefill_items():
