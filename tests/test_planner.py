@@ -169,6 +169,21 @@ def test_long_mixed_batch():
     assert -(-c["prefill_tiles"] // pairs) < -(-c["prefill_tiles"] // (pairs - 1))
 
 
+def test_side_by_side_split_follows_the_decode_bytes():
+    """The long mixed step with its decode contexts scaled: more decode bytes
+    take SMs from the prefill kernel, fewer give it more."""
+    s = W.config_spec(5)
+    dec = s.q_lens == 1
+    sides = []
+    for scale in (0.5, 1.0, 1.5, 2.0):
+        k = s.k_lens.astype(np.int64).copy()
+        k[dec] = (k[dec] * scale).astype(np.int64)
+        c = check_plan(s.q_lens, k, s.num_q_heads, s.num_kv_heads, s.head_size, s.causal)
+        assert c["prefill_sms_side_by_side"] > 0
+        sides.append(c["prefill_sms_side_by_side"])
+    assert sides == sorted(sides, reverse=True) and sides[0] > sides[-1]
+
+
 def test_side_by_side_with_short_prefill_items():
     """Llama-3.1-8B-shaped step of 256 decode rows beside four 512-token chunks
     (short items, one SM each): at ~5.7 TFLOP/s per prefill SM the balance
