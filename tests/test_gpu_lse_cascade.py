@@ -8,7 +8,9 @@ between prefill + decode" (vLLM PR #16828): the prefix pages shared by a group
 of sequences are attended once per query token without the causal mask, each
 sequence's own pages with it, and the two results are merged by their
 normalisers.  Tolerances: lse within 2e-3 (fp32 sums of exp2 terms, against
-fp64); outputs as in the other parity tests (max 2e-2, mean 1e-3).
+fp64); outputs as in the other parity tests (max 2e-2, mean 1e-3).  The
+normaliser cases include batches whose decode and prefill kernels run side
+by side (both write rows of the one lse array).
 """
 import math
 import zlib
@@ -68,6 +70,10 @@ CASES = [
     ([200, 1, 64], [200, 1500, 1000], 8, 2, 128, True),     # prefill tiles + decode
     ([33, 17], [100, 17], 8, 2, 128, False),                # non-causal prefill
     ([129, 255], [129, 700], 4, 1, 64, True),               # D = 64 prefill
+    # decode rows beside short and beside long prefill items: the two kernels
+    # side by side on a 152-SM GB300 (one-SM kernel; SM pairs)
+    ([1] * 32 + [512] * 2, [1000] * 32 + [512] * 2, 32, 8, 128, True),
+    ([1] * 16 + [1024], [8000] * 16 + [4096], 32, 8, 128, True),
 ]
 
 
